@@ -1,0 +1,179 @@
+/*
+ * qerl.h -- C ABI of libqerl: the NVFP4 weight-only linear layer with a LoRA
+ * branch and Adaptive Quantization Noise, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (QeRL, "QeRL: Beyond Efficiency -- Quantization-enhanced
+ * Reinforcement Learning for LLMs", paper-graph-ui digest, section 3.4):
+ *
+ *   y = x~ . dequant(Wq)^T + (alpha / r) . (x~ . A) . B,   x~ = bf16(x (.) (1 + z))
+ *
+ *   dequant: "NVFP4 Quantization", Eq. 6: W_hat = S_FP32 * (S_E4M3 (.) W~),
+ *            E2M1 codes, one E4M3 scale per 16 contiguous elements along K,
+ *            one FP32 tensor scale.
+ *   LoRA:    "Low-Rank Adaptation (LoRA) Within Quantized Layers", Eq. 2
+ *            forward y = x W_hat + x B A; both branches see the same noisy
+ *            activations.  The library names the adapters in x.A.B order:
+ *            A is K x r, B is r x N.
+ *   noise:   "Adaptive Quantization Noise (AQN)", Eq. 7 (one Gaussian value
+ *            per input channel), Eq. 8 (exponential decay of sigma), and
+ *            "Noise Merging", Eq. 10-12 (the noise merged into the RMSNorm
+ *            scale acts as the per-input-channel factor (1 + z)).
+ *
+ * Conventions for every call:
+ *   - The caller owns every buffer; the library never allocates or frees
+ *     memory and keeps no global state.  Pointers marked "device" must be
+ *     CUDA device (or managed) memory of the current device.
+ *   - All device work is asynchronous and ordered on `stream` (a
+ *     cudaStream_t passed as void*; NULL = the legacy default stream).
+ *   - Argument errors are detected on the host and returned immediately; no
+ *     work is enqueued then.  Errors found by a kernel (a non-finite weight,
+ *     a wait that timed out) are recorded in a status word inside the
+ *     caller's workspace and read back with qerl_read_status().
+ *   - Matrices are row-major.  bf16 values are IEEE bfloat16 bit patterns.
+ */
+#ifndef QERL_H
+#define QERL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QERL_API __attribute__((visibility("default")))
+#else
+#define QERL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QERL_OK = 0,
+    QERL_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative size, bad dtype, ld too small */
+    QERL_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of the required block, r too large */
+    QERL_ERR_MISALIGNED = 3,        /* a pointer or leading dimension breaks the stated alignment */
+    QERL_ERR_CUDA = 4,              /* a CUDA runtime call failed (the CUDA error is not cleared) */
+    QERL_ERR_TIMEOUT = 5,           /* a kernel's bounded wait expired (recorded in the status word) */
+    QERL_ERR_NONFINITE = 6,         /* NaN or Inf in the weights (recorded in the status word) */
+    QERL_ERR_WORKSPACE = 7          /* workspace missing or smaller than the *_workspace_size() */
+} qerl_status;
+
+typedef enum { QERL_F32 = 0, QERL_BF16 = 1 } qerl_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+QERL_API const char* qerl_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+QERL_API int qerl_version(void);
+
+/* ========================================================================
+ * NVFP4 quantization ("NVFP4 Quantization", Eq. 6; the encoder is the
+ * library's reading, since the digest gives only the decoder):
+ *   S     = amax(|W|) / (6 * 448)           (E2M1 q_max 6 times E4M3 max 448;
+ *                                            S = 1 if that is 0)
+ *   r_b   = (amax_b / 6) / S                 per 16-element block b along K
+ *   s_b   = E4M3(r_b)  round-to-nearest-even, saturating at 448
+ *   c     = E2M1(w / (S * dec(s_b)))  nearest level, ties to the even code,
+ *           saturating at 6; a value rounding to zero is code 0x0 (never -0)
+ * All arithmetic is IEEE fp32 in exactly that order, so results are
+ * bit-reproducible.
+ *
+ * W       device, n x k, dtype w_dtype (QERL_F32 or QERL_BF16), row stride
+ *         ld_w elements; 16-byte aligned, ld_w * sizeof(elem) % 16 == 0.
+ * codes   device, n x k/2 bytes, row-major; element 2j in the low nibble of
+ *         byte j, element 2j+1 in the high nibble.  E2M1 nibble: sign bit 3,
+ *         exponent bits 2..1, mantissa bit 0.  16-byte aligned.
+ * scales  device, n x k/16 bytes (E4M3 bit patterns), row-major.
+ * tensor_scale  device, one float (S).  Written by qerl_nvfp4_quantize;
+ *         read by qerl_nvfp4_quantize_with_scale.
+ * workspace device, >= qerl_nvfp4_quantize_workspace_size() bytes,
+ *         256-byte aligned, zero-filled before its first use.
+ * Requires k % 32 == 0, n >= 0, ld_w >= k.  A non-finite weight sets
+ * QERL_ERR_NONFINITE in the workspace status word; tensor_scale is then NaN
+ * and codes/scales are unspecified.
+ * ======================================================================== */
+QERL_API size_t qerl_nvfp4_quantize_workspace_size(void);
+
+QERL_API qerl_status qerl_nvfp4_quantize(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w,
+                                uint8_t* codes, uint8_t* scales, float* tensor_scale,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/* Same encoding with a caller-provided tensor scale (e.g. the S of a larger
+ * tensor this W is a shard of).  *tensor_scale must be finite and > 0. */
+QERL_API qerl_status qerl_nvfp4_quantize_with_scale(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w,
+                                           const float* tensor_scale, uint8_t* codes, uint8_t* scales,
+                                           void* workspace, size_t ws_bytes, void* stream);
+
+/* amax(|W|) into *amax (device float), e.g. to combine shards before
+ * computing S = amax / 2688.  NaN/Inf give a non-finite *amax. */
+QERL_API qerl_status qerl_nvfp4_amax(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w, float* amax,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* ========================================================================
+ * AQN schedule ("Adaptive Quantization Noise", Eq. 8 and Algorithm 1).
+ * Host functions, pure, no CUDA.
+ *
+ * qerl_aqn_sigma: Eq. 8, sigma(k) = sigma_start * (sigma_end/sigma_start)^((k-1)/(K-1))
+ * for k = 1..K, indexed by stage = k - 1 in [0, K).  stage < 0 returns 0
+ * (Algorithm 1's warm-up stage: quantization noise only); stage >= K clamps
+ * to K-1; num_stages <= 1 returns sigma_start.
+ *
+ * qerl_aqn_stage: Algorithm 1's stage of a training step: total_steps split
+ * into num_stages stages of floor(total_steps / num_stages) steps (at least
+ * 1); stage = min(step / that, num_stages - 1); step < 0 gives -1.
+ * ======================================================================== */
+QERL_API double qerl_aqn_sigma(int stage, int num_stages, double sigma_start, double sigma_end);
+QERL_API int qerl_aqn_stage(int64_t step, int64_t total_steps, int num_stages);
+
+/* AQN noise vector ("Adaptive Quantization Noise", Eq. 7: Z ~ N(0, sigma^2 I),
+ * one value per input channel, resampled per forward pass).  Generator (the
+ * digest only says Gaussian): channels 4i..4i+3 come from Philox4x32-10
+ * (Salmon et al., SC'11) with counter (i, stream_id, counter_lo, counter_hi)
+ * and key (seed_lo, seed_hi); u = (bits + 0.5) * 2^-32; Box-Muller in fp64,
+ * (u0,u1) -> channels 4i, 4i+1 and (u2,u3) -> 4i+2, 4i+3; z = (float)(sigma * n).
+ * z: device float[k].  Requires k >= 0 (k == 0 is a no-op). */
+QERL_API qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, uint32_t stream_id,
+                            uint64_t counter, void* stream);
+
+/* ========================================================================
+ * The linear layer.
+ *
+ *   x~[m][k] = bf16_RN( float(x[m][k]) * (1.0f + z[k]) )       (z == NULL: x~ = x)
+ *   y[m][n]  = out_RN( S * sum_k x~[m][k] * dec(scales[n][k/16]) * e2m1(codes[n][k])
+ *                     + (alpha / r) * sum_j (sum_k x~[m][k] * A[k][j]) * B[j][n] )
+ *
+ * x       device bf16, m x k, row stride ldx elements (ldx >= k, ldx % 8 == 0,
+ *         16-byte aligned).
+ * codes, scales, tensor_scale: as written by qerl_nvfp4_quantize for an
+ *         n x k weight (n = output features, k = input features).  codes
+ *         16-byte aligned, scales 4-byte aligned.
+ * z       device float[k] or NULL (no noise).
+ * A       device bf16 k x r, B device bf16 r x n, or both NULL / r == 0 (no
+ *         LoRA branch).  0 <= r <= 128.
+ * y       device, m x n (row stride n), y_dtype QERL_BF16 (round to nearest
+ *         even) or QERL_F32.
+ * workspace device, >= qerl_lora_linear_workspace_size(m, n, k, r) bytes,
+ *         256-byte aligned, zero-filled before its first use; holds the
+ *         staged noisy activations, the LoRA down-projection x~.A and the
+ *         status word.  Calls sharing a workspace must be stream-ordered.
+ * Requires k % 64 == 0, k > 0, m >= 0, n >= 0 (m == 0 or n == 0: no-op).
+ * Accumulation is fp32; x~ and the dequantized weights enter the tensor
+ * cores exactly (see the design notes for the power-of-two row staging).
+ * ======================================================================== */
+QERL_API size_t qerl_lora_linear_workspace_size(int64_t m, int64_t n, int64_t k, int r);
+
+QERL_API qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx,
+                             const uint8_t* codes, const uint8_t* scales, const float* tensor_scale, int64_t n,
+                             const float* z, const void* A, const void* B, int r, float alpha,
+                             void* y, int y_dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, returns the status word recorded in `workspace` by
+ * the kernels of earlier calls (QERL_OK if none failed) and resets it to
+ * QERL_OK.  A failing CUDA call returns QERL_ERR_CUDA. */
+QERL_API qerl_status qerl_read_status(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QERL_H */

@@ -1,0 +1,223 @@
+"""Python binding of libqerl (C ABI in include/qerl.h): NVFP4 weight-only
+linear with a LoRA branch and Adaptive Quantization Noise on GB300.
+
+Argument marshalling only: every function hands raw device pointers, sizes
+and the current CUDA stream to the C library, whose CUDA kernels do all the
+work.  There is no CPU path; if libqerl.so is missing every call raises.
+
+The functions named like the C entry points take torch tensors:
+
+    qerl_nvfp4_quantize(W, codes, scales, tensor_scale, workspace)
+    qerl_nvfp4_quantize_with_scale(W, tensor_scale, codes, scales, workspace)
+    qerl_nvfp4_amax(W, amax, workspace)
+    qerl_aqn_sigma(stage, num_stages, sigma_start, sigma_end)       (host)
+    qerl_aqn_stage(step, total_steps, num_stages)                   (host)
+    qerl_aqn_sample(z, sigma, seed, stream_id, counter)
+    qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, workspace)
+    qerl_read_status(workspace)
+
+and return the qerl_status integer (QERL_OK == 0).  `check()` turns a
+non-zero status into an exception.  `quantize()` and `lora_linear()` are
+conveniences that allocate the outputs with torch (the library itself never
+allocates).
+"""
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "QERL_OK", "QERL_F32", "QERL_BF16", "QerlError", "check", "lib", "lib_path", "status_string",
+    "qerl_nvfp4_quantize", "qerl_nvfp4_quantize_with_scale", "qerl_nvfp4_amax",
+    "qerl_nvfp4_quantize_workspace_size", "qerl_aqn_sigma", "qerl_aqn_stage", "qerl_aqn_sample",
+    "qerl_lora_linear_workspace_size", "qerl_lora_linear", "qerl_read_status",
+    "quantize", "lora_linear", "workspace",
+]
+
+QERL_OK = 0
+QERL_F32, QERL_BF16 = 0, 1
+STATUS_NAMES = {0: "QERL_OK", 1: "QERL_ERR_INVALID_ARGUMENT", 2: "QERL_ERR_UNSUPPORTED_SHAPE",
+                3: "QERL_ERR_MISALIGNED", 4: "QERL_ERR_CUDA", 5: "QERL_ERR_TIMEOUT", 6: "QERL_ERR_NONFINITE",
+                7: "QERL_ERR_WORKSPACE"}
+
+_lib = None
+_lock = threading.Lock()
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+class QerlError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libqerl.so.  Raises if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"libqerl.so not built at {_build.LIB}; run "
+                                   "nvfp4_weight_quantized_03_gb300.build.build() (nvcc, sm_103a)")
+            L = ctypes.CDLL(_build.LIB)
+            L.qerl_status_string.restype = ctypes.c_char_p
+            L.qerl_status_string.argtypes = [ctypes.c_int]
+            L.qerl_version.restype = ctypes.c_int
+            L.qerl_version.argtypes = []
+            L.qerl_nvfp4_quantize_workspace_size.restype = ctypes.c_size_t
+            L.qerl_nvfp4_quantize_workspace_size.argtypes = []
+            L.qerl_nvfp4_quantize.restype = ctypes.c_int
+            L.qerl_nvfp4_quantize.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                              ctypes.c_size_t, _vp]
+            L.qerl_nvfp4_quantize_with_scale.restype = ctypes.c_int
+            L.qerl_nvfp4_quantize_with_scale.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                                         ctypes.c_size_t, _vp]
+            L.qerl_nvfp4_amax.restype = ctypes.c_int
+            L.qerl_nvfp4_amax.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, ctypes.c_size_t, _vp]
+            L.qerl_aqn_sigma.restype = ctypes.c_double
+            L.qerl_aqn_sigma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double]
+            L.qerl_aqn_stage.restype = ctypes.c_int
+            L.qerl_aqn_stage.argtypes = [_i64, _i64, ctypes.c_int]
+            L.qerl_aqn_sample.restype = ctypes.c_int
+            L.qerl_aqn_sample.argtypes = [_vp, _i64, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
+                                          ctypes.c_uint64, _vp]
+            L.qerl_lora_linear_workspace_size.restype = ctypes.c_size_t
+            L.qerl_lora_linear_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.c_int]
+            L.qerl_lora_linear.restype = ctypes.c_int
+            L.qerl_lora_linear.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_int,
+                                           ctypes.c_float, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+            L.qerl_read_status.restype = ctypes.c_int
+            L.qerl_read_status.argtypes = [_vp, _vp]
+            _lib = L
+    return _lib
+
+
+def status_string(st: int) -> str:
+    return lib().qerl_status_string(int(st)).decode()
+
+
+def check(st: int, where: str = "qerl") -> None:
+    if st != QERL_OK:
+        raise QerlError(st, where)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _wdtype(W):
+    if W.dtype == torch.float32:
+        return QERL_F32
+    if W.dtype == torch.bfloat16:
+        return QERL_BF16
+    raise TypeError("W must be float32 or bfloat16")
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+# ---- C entry points ---------------------------------------------------------
+
+def qerl_nvfp4_quantize_workspace_size() -> int:
+    return lib().qerl_nvfp4_quantize_workspace_size()
+
+
+def qerl_nvfp4_quantize(W, codes, scales, tensor_scale, workspace, stream=None) -> int:
+    n, k = W.shape
+    return lib().qerl_nvfp4_quantize(_p(W), _wdtype(W), n, k, W.stride(0), _p(codes), _p(scales),
+                                     _p(tensor_scale), _p(workspace), _nbytes(workspace), _stream(stream))
+
+
+def qerl_nvfp4_quantize_with_scale(W, tensor_scale, codes, scales, workspace, stream=None) -> int:
+    n, k = W.shape
+    return lib().qerl_nvfp4_quantize_with_scale(_p(W), _wdtype(W), n, k, W.stride(0), _p(tensor_scale),
+                                                _p(codes), _p(scales), _p(workspace), _nbytes(workspace),
+                                                _stream(stream))
+
+
+def qerl_nvfp4_amax(W, amax, workspace, stream=None) -> int:
+    n, k = W.shape
+    return lib().qerl_nvfp4_amax(_p(W), _wdtype(W), n, k, W.stride(0), _p(amax), _p(workspace),
+                                 _nbytes(workspace), _stream(stream))
+
+
+def qerl_aqn_sigma(stage: int, num_stages: int, sigma_start: float = 1e-2, sigma_end: float = 5e-4) -> float:
+    return lib().qerl_aqn_sigma(int(stage), int(num_stages), float(sigma_start), float(sigma_end))
+
+
+def qerl_aqn_stage(step: int, total_steps: int, num_stages: int) -> int:
+    return lib().qerl_aqn_stage(int(step), int(total_steps), int(num_stages))
+
+
+def qerl_aqn_sample(z, sigma: float, seed: int, stream_id: int = 0, counter: int = 0, stream=None) -> int:
+    return lib().qerl_aqn_sample(_p(z), z.numel(), float(sigma), int(seed) & (2**64 - 1),
+                                 int(stream_id) & 0xFFFFFFFF, int(counter) & (2**64 - 1), _stream(stream))
+
+
+def qerl_lora_linear_workspace_size(m: int, n: int, k: int, r: int) -> int:
+    return lib().qerl_lora_linear_workspace_size(int(m), int(n), int(k), int(r))
+
+
+def qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, workspace, stream=None) -> int:
+    m, k = x.shape
+    n = codes.shape[0]
+    r = 0 if A is None else A.shape[1]
+    ydt = QERL_F32 if y.dtype == torch.float32 else QERL_BF16
+    return lib().qerl_lora_linear(_p(x), m, k, x.stride(0), _p(codes), _p(scales), _p(tensor_scale), n, _p(z),
+                                  _p(A), _p(B), r, float(alpha), _p(y), ydt, _p(workspace), _nbytes(workspace),
+                                  _stream(stream))
+
+
+def qerl_read_status(workspace, stream=None) -> int:
+    return lib().qerl_read_status(_p(workspace), _stream(stream))
+
+
+# ---- conveniences (allocation by torch; compute by the library) -------------
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled, 256-byte aligned device workspace of at least nbytes."""
+    return torch.zeros(max(256, (nbytes + 255) // 256 * 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def quantize(W: torch.Tensor, ws: torch.Tensor = None):
+    """NVFP4-quantize an n x k float32/bfloat16 CUDA tensor -> (codes, scales, tensor_scale)."""
+    n, k = W.shape
+    codes = torch.empty((n, k // 2), dtype=torch.uint8, device=W.device)
+    scales = torch.empty((n, k // 16), dtype=torch.uint8, device=W.device)
+    ts = torch.empty(1, dtype=torch.float32, device=W.device)
+    ws = workspace(qerl_nvfp4_quantize_workspace_size(), W.device) if ws is None else ws
+    check(qerl_nvfp4_quantize(W, codes, scales, ts, ws), "qerl_nvfp4_quantize")
+    return codes, scales, ts
+
+
+def lora_linear(x, codes, scales, tensor_scale, z=None, A=None, B=None, alpha=0.0, out_dtype=torch.bfloat16,
+                ws=None):
+    """y = bf16(x(1+z)) . dequant(W)^T + (alpha/r) (x~ A) B for bf16 x [m, k]."""
+    m, k = x.shape
+    n = codes.shape[0]
+    r = 0 if A is None else A.shape[1]
+    y = torch.empty((m, n), dtype=out_dtype, device=x.device)
+    ws = workspace(qerl_lora_linear_workspace_size(m, n, k, r), x.device) if ws is None else ws
+    check(qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, ws), "qerl_lora_linear")
+    return y

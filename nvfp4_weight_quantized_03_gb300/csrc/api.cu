@@ -1,0 +1,169 @@
+// api.cu -- the extern "C" entry points declared in include/qerl.h: argument
+// validation on the host, workspace layout, and the kernel launches.
+#include <cstdint>
+
+#include "qerl_internal.h"
+#include "qerl_ptx.cuh"
+
+namespace {
+
+using qerl::kWsHeaderBytes;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+qerl_status check_weight_args(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w) {
+  if (w_dtype != QERL_F32 && w_dtype != QERL_BF16) return QERL_ERR_INVALID_ARGUMENT;
+  if (n < 0 || k < 0 || ld_w < k) return QERL_ERR_INVALID_ARGUMENT;
+  if (k % 32 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (n > 0 && k > 0 && W == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  const int64_t esz = w_dtype == QERL_BF16 ? 2 : 4;
+  if (!aligned(W, 16) || (ld_w * esz) % 16 != 0) return QERL_ERR_MISALIGNED;
+  if (n > INT32_MAX || k > INT32_MAX) return QERL_ERR_UNSUPPORTED_SHAPE;
+  return QERL_OK;
+}
+
+qerl_status check_ws(void* workspace, size_t ws_bytes, size_t need) {
+  if (workspace == nullptr || ws_bytes < need) return QERL_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return QERL_ERR_MISALIGNED;
+  return QERL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qerl_status_string(int status) {
+  switch (status) {
+    case QERL_OK: return "QERL_OK";
+    case QERL_ERR_INVALID_ARGUMENT: return "QERL_ERR_INVALID_ARGUMENT";
+    case QERL_ERR_UNSUPPORTED_SHAPE: return "QERL_ERR_UNSUPPORTED_SHAPE";
+    case QERL_ERR_MISALIGNED: return "QERL_ERR_MISALIGNED";
+    case QERL_ERR_CUDA: return "QERL_ERR_CUDA";
+    case QERL_ERR_TIMEOUT: return "QERL_ERR_TIMEOUT";
+    case QERL_ERR_NONFINITE: return "QERL_ERR_NONFINITE";
+    case QERL_ERR_WORKSPACE: return "QERL_ERR_WORKSPACE";
+    default: return "QERL_ERR_UNKNOWN";
+  }
+}
+
+int qerl_version(void) { return 100; }
+
+size_t qerl_nvfp4_quantize_workspace_size(void) { return kWsHeaderBytes; }
+
+qerl_status qerl_nvfp4_amax(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w, float* amax,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  qerl_status st = check_weight_args(W, w_dtype, n, k, ld_w);
+  if (st != QERL_OK) return st;
+  if (amax == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if ((st = check_ws(workspace, ws_bytes, kWsHeaderBytes)) != QERL_OK) return st;
+  auto* hdr = static_cast<qerl::WsHeader*>(workspace);
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemsetAsync(&hdr->amax_bits, 0, sizeof(unsigned), s) != cudaSuccess) return QERL_ERR_CUDA;
+  if ((st = qerl::launch_amax(W, w_dtype == QERL_BF16, n, k, ld_w, &hdr->amax_bits, s)) != QERL_OK) return st;
+  return qerl::launch_amax_to_float(&hdr->amax_bits, amax, s);
+}
+
+qerl_status qerl_nvfp4_quantize(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w, uint8_t* codes,
+                                uint8_t* scales, float* tensor_scale, void* workspace, size_t ws_bytes,
+                                void* stream) {
+  qerl_status st = check_weight_args(W, w_dtype, n, k, ld_w);
+  if (st != QERL_OK) return st;
+  if (tensor_scale == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (n > 0 && k > 0 && (codes == nullptr || scales == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(codes, 16)) return QERL_ERR_MISALIGNED;
+  if ((st = check_ws(workspace, ws_bytes, kWsHeaderBytes)) != QERL_OK) return st;
+  auto* hdr = static_cast<qerl::WsHeader*>(workspace);
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemsetAsync(&hdr->amax_bits, 0, sizeof(unsigned), s) != cudaSuccess) return QERL_ERR_CUDA;
+  const bool bf16 = w_dtype == QERL_BF16;
+  if ((st = qerl::launch_amax(W, bf16, n, k, ld_w, &hdr->amax_bits, s)) != QERL_OK) return st;
+  return qerl::launch_encode(W, bf16, n, k, ld_w, &hdr->amax_bits, nullptr, tensor_scale, codes, scales,
+                             &hdr->status, s);
+}
+
+qerl_status qerl_nvfp4_quantize_with_scale(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w,
+                                           const float* tensor_scale, uint8_t* codes, uint8_t* scales,
+                                           void* workspace, size_t ws_bytes, void* stream) {
+  qerl_status st = check_weight_args(W, w_dtype, n, k, ld_w);
+  if (st != QERL_OK) return st;
+  if (tensor_scale == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (n > 0 && k > 0 && (codes == nullptr || scales == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(codes, 16)) return QERL_ERR_MISALIGNED;
+  if ((st = check_ws(workspace, ws_bytes, kWsHeaderBytes)) != QERL_OK) return st;
+  auto* hdr = static_cast<qerl::WsHeader*>(workspace);
+  if (n == 0 || k == 0) return QERL_OK;
+  return qerl::launch_encode(W, w_dtype == QERL_BF16, n, k, ld_w, nullptr, tensor_scale, nullptr, codes, scales,
+                             &hdr->status, as_stream(stream));
+}
+
+qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, uint32_t stream_id, uint64_t counter,
+                            void* stream) {
+  if (k < 0) return QERL_ERR_INVALID_ARGUMENT;
+  if (k == 0) return QERL_OK;
+  if (z == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (k > (int64_t{1} << 34)) return QERL_ERR_UNSUPPORTED_SHAPE;
+  return qerl::launch_aqn_sample(z, k, sigma, seed, stream_id, counter, as_stream(stream));
+}
+
+size_t qerl_lora_linear_workspace_size(int64_t m, int64_t n, int64_t k, int r) {
+  (void)n;
+  if (m < 0 || k < 0 || r < 0) return 0;
+  return qerl::linear_workspace_bytes(m, k, r);
+}
+
+qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, const uint8_t* codes,
+                             const uint8_t* scales, const float* tensor_scale, int64_t n, const float* z,
+                             const void* A, const void* B, int r, float alpha, void* y, int y_dtype,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  if (m < 0 || n < 0 || k <= 0 || ldx < k || r < 0) return QERL_ERR_INVALID_ARGUMENT;
+  if (y_dtype != QERL_BF16 && y_dtype != QERL_F32) return QERL_ERR_INVALID_ARGUMENT;
+  if ((A == nullptr) != (B == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
+  if (r > 0 && A == nullptr) r = 0;
+  if (A != nullptr && r == 0) return QERL_ERR_INVALID_ARGUMENT;
+  if (k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (r > 128) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX || m * k > (int64_t{1} << 40))
+    return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (m == 0 || n == 0) return QERL_OK;
+  if (x == nullptr || codes == nullptr || scales == nullptr || tensor_scale == nullptr || y == nullptr)
+    return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(codes, 16) || !aligned(scales, 4)) return QERL_ERR_MISALIGNED;
+  if (z != nullptr && !aligned(z, 16)) return QERL_ERR_MISALIGNED;
+  if (y_dtype == QERL_F32 ? !aligned(y, 4) : !aligned(y, 2)) return QERL_ERR_MISALIGNED;
+  if (A != nullptr && (!aligned(A, 2) || !aligned(B, 2))) return QERL_ERR_MISALIGNED;
+  qerl_status st = check_ws(workspace, ws_bytes, qerl::linear_workspace_bytes(m, k, r));
+  if (st != QERL_OK) return st;
+  qerl::LinearArgs a{};
+  a.x = x;
+  a.m = m;
+  a.k = k;
+  a.ldx = ldx;
+  a.n = n;
+  a.codes = codes;
+  a.scales = scales;
+  a.tensor_scale = tensor_scale;
+  a.z = z;
+  a.A = A;
+  a.B = B;
+  a.r = r;
+  a.alpha = alpha;
+  a.y = y;
+  a.y_f32 = y_dtype == QERL_F32;
+  a.workspace = workspace;
+  a.ws_bytes = ws_bytes;
+  return qerl::launch_lora_linear(a, as_stream(stream));
+}
+
+qerl_status qerl_read_status(void* workspace, void* stream) {
+  if (workspace == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = as_stream(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return QERL_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return QERL_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return QERL_ERR_CUDA;
+  return static_cast<qerl_status>(host);
+}
+
+}  // extern "C"

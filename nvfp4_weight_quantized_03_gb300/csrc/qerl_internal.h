@@ -1,0 +1,50 @@
+// qerl_internal.h -- host-side declarations shared by the library's .cu files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qerl.h"
+
+namespace qerl {
+
+constexpr size_t kWsHeaderBytes = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline qerl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QERL_OK : QERL_ERR_CUDA; }
+
+// quantize.cu
+qerl_status launch_amax(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w, unsigned* amax_bits,
+                        cudaStream_t s);
+qerl_status launch_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w,
+                          const unsigned* amax_bits, const float* s_in, float* s_out, uint8_t* codes,
+                          uint8_t* scales, int* status, cudaStream_t s);
+qerl_status launch_amax_to_float(const unsigned* amax_bits, float* amax, cudaStream_t s);
+
+// aqn.cu
+qerl_status launch_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, uint32_t stream_id,
+                              uint64_t counter, cudaStream_t s);
+
+// linear.cu
+struct LinearArgs {
+  const void* x;
+  int64_t m, k, ldx, n;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* tensor_scale;
+  const float* z;
+  const void* A;
+  const void* B;
+  int r;
+  float alpha;
+  void* y;
+  bool y_f32;
+  void* workspace;
+  size_t ws_bytes;
+};
+size_t linear_workspace_bytes(int64_t m, int64_t k, int r);
+qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s);
+
+}  // namespace qerl

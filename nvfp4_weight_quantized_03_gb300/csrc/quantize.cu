@@ -1,0 +1,181 @@
+// quantize.cu -- NVFP4 quantizer kernels (QeRL digest, section 3.4 "NVFP4
+// Quantization": E2M1 elements, one E4M3 scale per 16 contiguous elements,
+// one FP32 tensor scale; Eq. 6 is the decoder this encoder inverts).
+//
+// Two streaming passes over W (HBM-bound):
+//   1. amax_kernel  : max |w| over the tensor as fp32 bit patterns.  For
+//      non-negative floats the unsigned order equals the float order and
+//      NaN/Inf sort above every finite value, so one atomicMax per CTA both
+//      reduces and flags non-finite input.
+//   2. encode_kernel: per 16-element block: amax_b, E4M3 block scale, the
+//      decoded scale times S, 16 E2M1 codes packed two per byte.  Every fp32
+//      operation is a single IEEE RN operation (__fdiv_rn / __fmul_rn) in the
+//      documented order, so codes and scales are bit-reproducible.
+#include <cuda_bf16.h>
+
+#include "qerl_internal.h"
+#include "qerl_ptx.cuh"
+
+namespace qerl {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ unsigned abs_bits_f32(uint32_t w) { return w & 0x7FFFFFFFu; }
+__device__ __forceinline__ unsigned abs_bits_bf16(uint32_t h) { return (h & 0x7FFFu) << 16; }
+
+__device__ __forceinline__ unsigned max_bits_of_vec(uint4 v, bool bf16) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  unsigned m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (bf16) {
+      m = max(m, abs_bits_bf16(w[i] & 0xFFFFu));
+      m = max(m, abs_bits_bf16(w[i] >> 16));
+    } else {
+      m = max(m, abs_bits_f32(w[i]));
+    }
+  }
+  return m;
+}
+
+// Rows are strided over CTAs, 16-byte vectors over threads.
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint8_t* __restrict__ W, int64_t n,
+                                                        int64_t row_vecs, int64_t ld_bytes, bool bf16,
+                                                        unsigned* __restrict__ amax_bits) {
+  unsigned m = 0;
+  for (int64_t row = blockIdx.x; row < n; row += gridDim.x) {
+    const uint4* p = reinterpret_cast<const uint4*>(W + row * ld_bytes);
+    for (int64_t v = threadIdx.x; v < row_vecs; v += kThreads) m = max(m, max_bits_of_vec(__ldg(p + v), bf16));
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ unsigned red[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    unsigned v = threadIdx.x < kThreads / 32 ? red[threadIdx.x] : 0u;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if (threadIdx.x == 0 && v != 0u) atomicMax(amax_bits, v);
+  }
+}
+
+// One thread per 16-element block; threads of a warp cover consecutive blocks
+// of a row, so loads (64 B or 32 B per thread) and the 8-byte code stores are
+// contiguous across the warp.
+__global__ void __launch_bounds__(kThreads) encode_kernel(const uint8_t* __restrict__ W, int64_t n, int64_t k,
+                                                          int64_t ld_bytes, bool bf16,
+                                                          const unsigned* __restrict__ amax_bits,
+                                                          const float* __restrict__ s_in, float* __restrict__ s_out,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                          int* __restrict__ status) {
+  float S;
+  if (s_in != nullptr) {
+    S = *s_in;
+    if (!(S > 0.0f) || !isfinite(S)) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) record_error(status, isfinite(S) ? 1 : 6);
+      return;
+    }
+  } else {
+    const unsigned ab = *amax_bits;
+    if (ab >= 0x7F800000u) {  // NaN or Inf somewhere in W
+      if (blockIdx.x == 0 && threadIdx.x == 0) {
+        record_error(status, 6);
+        *s_out = __uint_as_float(0x7FC00000u);
+      }
+      return;
+    }
+    S = __fdiv_rn(__uint_as_float(ab), 2688.0f);  // amax / (6 * 448)
+    if (S == 0.0f) S = 1.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && s_out != nullptr) *s_out = S;
+  }
+
+  const int64_t nb = k / 16;
+  for (int64_t row = blockIdx.x; row < n; row += gridDim.x) {
+    const uint8_t* rowp = W + row * ld_bytes;
+    for (int64_t b = threadIdx.x; b < nb; b += kThreads) {
+      float w[16];
+      if (bf16) {
+        const uint4* p = reinterpret_cast<const uint4*>(rowp) + 2 * b;
+        uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
+        uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          w[2 * i] = __uint_as_float(u[i] << 16);
+          w[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+        }
+      } else {
+        const float4* p = reinterpret_cast<const float4*>(rowp) + 4 * b;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float4 v = __ldg(p + i);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+      }
+      unsigned mb = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mb = max(mb, __float_as_uint(w[i]) & 0x7FFFFFFFu);
+      if (mb >= 0x7F800000u) {  // only reachable with a caller-given scale
+        record_error(status, 6);
+        continue;
+      }
+      const float rb = __fdiv_rn(__fdiv_rn(__uint_as_float(mb), 6.0f), S);
+      const uint32_t sb = f32_to_e4m3_satfinite(rb);
+      const float dec = __half2float(__low2half(e4m3x2_to_half2(sb)));
+      const float sc = __fmul_rn(S, dec);
+      uint32_t packed[2] = {0u, 0u};
+      if (sc != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t byte = f32x2_to_e2m1x2_satfinite(__fdiv_rn(w[2 * i], sc), __fdiv_rn(w[2 * i + 1], sc));
+          if ((byte & 0x07u) == 0u) byte &= 0xF0u;  // a zero magnitude is +0 (code 0x0)
+          if ((byte & 0x70u) == 0u) byte &= 0x0Fu;
+          packed[i >> 2] |= byte << (8 * (i & 3));
+        }
+      }
+      *reinterpret_cast<uint2*>(codes + row * (k / 2) + b * 8) = make_uint2(packed[0], packed[1]);
+      scales[row * nb + b] = static_cast<uint8_t>(sb);
+    }
+  }
+}
+
+__global__ void amax_to_float_kernel(const unsigned* amax_bits, float* amax) { *amax = __uint_as_float(*amax_bits); }
+
+int grid_for_rows(int64_t n) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t g = sms * 8;
+  if (g > n) g = n;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
+}  // namespace
+
+qerl_status launch_amax(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w, unsigned* amax_bits,
+                        cudaStream_t s) {
+  if (n == 0 || k == 0) return QERL_OK;
+  const int64_t esz = bf16 ? 2 : 4;
+  amax_kernel<<<grid_for_rows(n), kThreads, 0, s>>>(static_cast<const uint8_t*>(W), n, k * esz / 16, ld_w * esz,
+                                                     bf16, amax_bits);
+  return cuda_status(cudaGetLastError());
+}
+
+qerl_status launch_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w,
+                          const unsigned* amax_bits, const float* s_in, float* s_out, uint8_t* codes,
+                          uint8_t* scales, int* status, cudaStream_t s) {
+  const int64_t esz = bf16 ? 2 : 4;
+  encode_kernel<<<grid_for_rows(n > 0 ? n : 1), kThreads, 0, s>>>(static_cast<const uint8_t*>(W), n, k,
+                                                                   ld_w * esz, bf16, amax_bits, s_in, s_out,
+                                                                   codes, scales, status);
+  return cuda_status(cudaGetLastError());
+}
+
+qerl_status launch_amax_to_float(const unsigned* amax_bits, float* amax, cudaStream_t s) {
+  amax_to_float_kernel<<<1, 1, 0, s>>>(amax_bits, amax);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace qerl

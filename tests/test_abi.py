@@ -1,0 +1,141 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+entry point declared in include/qerl.h, its host-only functions agree with the
+oracle, and argument validation rejects bad calls before touching the device.
+Also checks that the product package and the oracle never import each other."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+import nvfp4_weight_quantized_03_gb300 as q
+
+
+@pytest.fixture(scope="module")
+def L():
+    from nvfp4_weight_quantized_03_gb300 import build
+    build.build()
+    return q.lib()
+
+
+def declared_symbols():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"QERL_API\s+[\w\s\*]+?\b(qerl_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert len(names) >= 12
+    out = subprocess.run(["nm", "-D", "--defined-only", q.lib_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r" T (\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        getattr(L, n)  # resolvable through ctypes too
+
+
+def test_status_strings(L):
+    for code, name in q.STATUS_NAMES.items():
+        assert q.status_string(code) == name
+    assert q.status_string(99) == "QERL_ERR_UNKNOWN"
+
+
+def test_host_schedule_matches_oracle(L, orc):
+    for K in (1, 2, 5, 10):
+        for stage in range(-2, K + 3):
+            for s0, s1 in ((1e-2, 5e-4), (0.1, 1e-3)):
+                assert q.qerl_aqn_sigma(stage, K, s0, s1) == orc.aqn_sigma(stage, K, s0, s1)
+    for total in (1, 7, 600, 8192):
+        for K in (1, 3, 10):
+            for step in list(range(-2, 30)) + [total - 1, total, 5 * total]:
+                assert q.qerl_aqn_stage(step, total, K) == orc.aqn_stage(step, total, K)
+
+
+# The validation tests pass fake (non-dereferenceable) pointers; a call that
+# unexpectedly passed validation would launch on them.  They only run where no
+# GPU is visible, so such a mistake cannot reach a device.
+no_gpu_only = pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                                 reason="fake-pointer validation tests run only without a GPU")
+
+
+def _lin(L, **kw):
+    a = dict(x=0x1000, m=4, k=128, ldx=128, codes=0x2000, scales=0x3000, ts=0x4000, n=256, z=None, A=None,
+             B=None, r=0, alpha=0.0, y=0x5000, ydt=q.QERL_BF16, ws=0x10000, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return L.qerl_lora_linear(a["x"], a["m"], a["k"], a["ldx"], a["codes"], a["scales"], a["ts"], a["n"], a["z"],
+                              a["A"], a["B"], a["r"], a["alpha"], a["y"], a["ydt"], a["ws"], a["wsb"], a["stream"])
+
+
+@no_gpu_only
+def test_linear_validation(L):
+    E = q.STATUS_NAMES
+    name = lambda st: E[st]
+    assert name(_lin(L, k=96, ldx=96)) == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert name(_lin(L, k=0)) == "QERL_ERR_INVALID_ARGUMENT"
+    assert name(_lin(L, m=-1)) == "QERL_ERR_INVALID_ARGUMENT"
+    assert name(_lin(L, ldx=64)) == "QERL_ERR_INVALID_ARGUMENT"
+    assert name(_lin(L, A=0x6000)) == "QERL_ERR_INVALID_ARGUMENT"  # A without B
+    assert name(_lin(L, A=0x6000, B=0x7000, r=0)) == "QERL_ERR_INVALID_ARGUMENT"
+    assert name(_lin(L, A=0x6000, B=0x7000, r=129)) == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert name(_lin(L, ydt=7)) == "QERL_ERR_INVALID_ARGUMENT"
+    assert name(_lin(L, x=None)) == "QERL_ERR_INVALID_ARGUMENT"
+    assert name(_lin(L, x=0x1008)) == "QERL_ERR_MISALIGNED"
+    assert name(_lin(L, ldx=132)) == "QERL_ERR_MISALIGNED"
+    assert name(_lin(L, codes=0x2004)) == "QERL_ERR_MISALIGNED"
+    assert name(_lin(L, scales=0x3002)) == "QERL_ERR_MISALIGNED"
+    assert name(_lin(L, z=0x8004)) == "QERL_ERR_MISALIGNED"
+    assert name(_lin(L, ws=None)) == "QERL_ERR_WORKSPACE"
+    need = L.qerl_lora_linear_workspace_size(4, 256, 128, 0)
+    assert name(_lin(L, wsb=need - 1)) == "QERL_ERR_WORKSPACE"
+    assert name(_lin(L, ws=0x10080)) == "QERL_ERR_MISALIGNED"
+    assert _lin(L, m=0) == 0 and _lin(L, n=0) == 0  # empty problems are no-ops
+
+
+def test_workspace_size_grows(L):
+    a = L.qerl_lora_linear_workspace_size(1, 128, 64, 0)
+    b = L.qerl_lora_linear_workspace_size(128, 128, 3584, 32)
+    assert a >= 256 and a % 256 == 0 and b > a
+    assert b >= 128 * 3584 * 2 + 128 * 32 * 4
+    assert L.qerl_nvfp4_quantize_workspace_size() == 256
+
+
+@no_gpu_only
+def test_quantize_validation(L):
+    E = q.STATUS_NAMES
+    qz = lambda **kw: L.qerl_nvfp4_quantize(
+        kw.get("W", 0x1000), kw.get("dt", q.QERL_F32), kw.get("n", 4), kw.get("k", 64), kw.get("ld", 64),
+        kw.get("codes", 0x2000), kw.get("scales", 0x3000), kw.get("ts", 0x4000), kw.get("ws", 0x10000),
+        kw.get("wsb", 256), None)
+    assert E[qz(k=48, ld=48)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[qz(dt=5)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[qz(ld=32)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[qz(W=0x1004)] == "QERL_ERR_MISALIGNED"
+    assert E[qz(ld=66)] == "QERL_ERR_MISALIGNED"
+    assert E[qz(codes=0x2008)] == "QERL_ERR_MISALIGNED"
+    assert E[qz(ts=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[qz(wsb=255)] == "QERL_ERR_WORKSPACE"
+    assert E[L.qerl_aqn_sample(None, -1, 1.0, 0, 0, 0, None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert L.qerl_aqn_sample(None, 0, 1.0, 0, 0, 0, None) == 0
+
+
+def test_product_and_oracle_are_independent():
+    pkg = os.path.join(ROOT, "nvfp4_weight_quantized_03_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in re.findall(r"(?:import|from)\s+(\w+)", text), fn
+                assert "qerl_oracle" not in text, fn
+    for fn in os.listdir(os.path.join(ROOT, "oracle")):
+        if fn.endswith((".py", ".c", ".h")):
+            text = open(os.path.join(ROOT, "oracle", fn)).read()
+            assert "nvfp4_weight_quantized_03_gb300" not in re.findall(r"(?:import|from)\s+([\w.]+)", text), fn
+            assert "#include" not in text or ("qerl_ptx" not in text and "qerl.h" not in text), fn
