@@ -1,0 +1,576 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 weight-only linear with LoRA and AQN on GB300.
+
+One step = one rollout decode pass of a Qwen2.5-7B-shaped decoder layer's
+seven LoRA linears (q, k, v, o, gate, up, down; r = 32, alpha = 64) at each
+decode batch M in {1, 8, 32, 128}: per M, four AQN noise vectors (groups qkv,
+o, gate_up, down; sigma from the exponential-decay schedule, stage = step mod
+10) and seven qerl_lora_linear calls.  Inputs are synthetic and seeded; the
+weights are NVFP4-quantized by the library from fp32 N(0, 0.02^2) with 0.5% of
+input channels scaled x10.  Weights rotate over 8 distinct layer copies
+(1.05 GB, far above the 129 MB L2), so every linear streams its weights from
+HBM.  Each (stage, M) sub-step is one CUDA graph replay.
+
+`value` is decode throughput in GB/s of NVFP4 weight bytes (0.5625 B per
+weight: E2M1 code + E4M3 scale share) over the timed steps.  Also reported:
+prefill TFLOP/s (Qwen2.5-14B-shaped layer, M = 4096), quantizer GB/s, an
+end-to-end figure through the public API with host buffers, the roofline of
+the decode path, the oracle timed on host cores, and SM clocks sampled during
+the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun with N > 1 every rank runs the same workload on its own GPU
+(independent replicas, weak scaling); the timed region is bracketed by a
+barrier, and the max over ranks is reported.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "NVFP4+LoRA linear: decode HBM GB/s (% of peak); prefill TFLOP/s (% of peak)"
+UNIT = "GB/s"
+DECODE_MS = (1, 8, 32, 128)
+RANK_R = 32
+ALPHA = 64.0
+NUM_STAGES = 10
+SIGMA_START, SIGMA_END = 1e-2, 5e-4
+N_COPIES = 8
+BYTES_PER_WEIGHT = 0.5625
+WORKLOAD = ("Qwen2.5-7B decoder-layer linears q,k,v,o,gate,up,down (N x K: 3584x3584, 512x3584 x2, "
+            "3584x3584, 18944x3584 x2, 3584x18944), decode M in {1,8,32,128}, LoRA r=32 alpha=64, "
+            "AQN sigma by exponential decay 1e-2 -> 5e-4 over 10 stages (stage = step mod 10)")
+
+
+# ---------------------------------------------------------------- environment
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None, "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- workload
+
+class QLinear:
+    """One NVFP4-quantized linear with its LoRA adapters (device)."""
+
+    def __init__(self, q, lin, seed, *path, r=RANK_R, w_dtype=torch.float32):
+        W = wl.weight_f32_device(lin.n, lin.k, seed, *path)
+        if w_dtype == torch.bfloat16:
+            W = W.to(torch.bfloat16)
+        self.lin = lin
+        self.codes, self.scales, self.S = q.quantize(W)
+        del W
+        self.A = wl.normal_bf16_device((lin.k, r), 1.0 / math.sqrt(lin.k), seed, *path, 2)
+        self.B = wl.normal_bf16_device((r, lin.n), 0.01, seed, *path, 3)
+
+    @property
+    def weight_bytes(self):
+        return self.lin.n * self.lin.k * BYTES_PER_WEIGHT
+
+
+def layer_weights(q, shapes, seed, copy):
+    return [QLinear(q, lin, seed, copy, li) for li, lin in enumerate(shapes)]
+
+
+class Activations:
+    """Per-M inputs (one x and one z per AQN group), outputs and a workspace."""
+
+    def __init__(self, q, shapes, m, seed):
+        self.m = m
+        ks = {}
+        for lin in shapes:
+            ks[lin.group] = lin.k
+        self.x = {g: wl.normal_bf16_device((m, k), 1.0, seed, m, gi, 11) for gi, (g, k) in enumerate(ks.items())}
+        self.z = {g: torch.zeros(k, dtype=torch.float32, device="cuda") for g, k in ks.items()}
+        self.y = [torch.empty((m, lin.n), dtype=torch.bfloat16, device="cuda") for lin in shapes]
+        need = max(q.qerl_lora_linear_workspace_size(m, lin.n, lin.k, RANK_R) for lin in shapes)
+        self.ws = q.workspace(need)
+
+    def io_bytes(self):
+        h2d = sum(t.numel() * t.element_size() for t in self.x.values())
+        d2h = sum(t.numel() * t.element_size() for t in self.y)
+        return h2d, d2h
+
+
+def run_substep(q, layer, act, sigma, counter):
+    """One decode batch through the layer: 4 AQN samples + 7 linears (all on the current stream)."""
+    for gi, g in enumerate(wl.NOISE_GROUPS):
+        if g in act.z:
+            q.check(q.qerl_aqn_sample(act.z[g], sigma, 0, gi, counter), "qerl_aqn_sample")
+    for ql, y in zip(layer, act.y):
+        g = ql.lin.group
+        q.check(q.qerl_lora_linear(act.x[g], ql.codes, ql.scales, ql.S, act.z[g], ql.A, ql.B, ALPHA, y, act.ws),
+                "qerl_lora_linear")
+
+
+def linear_algorithmic_bytes(lin, m, r=RANK_R):
+    """Minimum HBM/L2 bytes of one linear call: weights + x + z + y + LoRA adapters."""
+    return (lin.n * lin.k * BYTES_PER_WEIGHT + m * lin.k * 2 + lin.k * 4 + m * lin.n * 2
+            + lin.k * r * 2 + r * lin.n * 2)
+
+
+def linear_flops(lin, m, r=RANK_R):
+    return 2.0 * m * lin.n * lin.k + 2.0 * m * lin.k * r + 2.0 * m * r * lin.n
+
+
+# ---------------------------------------------------------------- our arm
+
+def bench_ours(args):
+    import nvfp4_weight_quantized_03_gb300 as q
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev_index = torch.cuda.current_device()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    q.lib()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+    shapes = wl.QWEN_7B
+    seed = 0
+
+    # ---- setup: quantize N_COPIES layer copies on the device
+    layers = [layer_weights(q, shapes, seed, c) for c in range(N_COPIES)]
+    acts = [Activations(q, shapes, m, seed) for m in DECODE_MS]
+    layer_wbytes = sum(ql.weight_bytes for ql in layers[0])
+    step_wbytes = layer_wbytes * len(DECODE_MS)
+
+    def copy_for(step, j):
+        return (len(DECODE_MS) * step + j) % N_COPIES
+
+    def sigma_for(step):
+        return q.qerl_aqn_sigma(step % NUM_STAGES, NUM_STAGES, SIGMA_START, SIGMA_END)
+
+    # eager warm-up (kernel attributes, driver entry points), then capture graphs
+    for j, act in enumerate(acts):
+        run_substep(q, layers[copy_for(0, j)], act, sigma_for(0), 0)
+    torch.cuda.synchronize()
+    for act in acts:
+        q.check(q.qerl_read_status(act.ws), "status after warm-up")
+
+    cap_stream = torch.cuda.Stream()
+    graphs = {}
+    for st in range(NUM_STAGES):
+        for j, act in enumerate(acts):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap_stream):
+                run_substep(q, layers[copy_for(st, j)], act, sigma_for(st), st)
+            graphs[(st, j)] = g
+    torch.cuda.synchronize()
+
+    def step(i):
+        for j in range(len(DECODE_MS)):
+            graphs[(i % NUM_STAGES, j)].replay()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    # ---- timed region
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(DECODE_MS) + 1)] for _ in range(K)]
+    clocks = ClockSampler(dev_index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(K):
+        for j in range(len(DECODE_MS)):
+            ev[i][j].record()
+            graphs[(i % NUM_STAGES, j)].replay()
+        ev[i][-1].record()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = tt.item()
+    for act in acts:
+        q.check(q.qerl_read_status(act.ws), "status after timed region")
+
+    per_m = {}
+    sub_bytes_total, sub_time_total = 0.0, 0.0
+    for j, m in enumerate(DECODE_MS):
+        t_ms = sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K
+        alg = sum(linear_algorithmic_bytes(lin, m) for lin in shapes)
+        sub_bytes_total += alg
+        sub_time_total += t_ms
+        flops = sum(linear_flops(lin, m) for lin in shapes)
+        t_bw = layer_wbytes / (hbm_peak * 1e9) * 1e3
+        t_tc = flops / (bf16_peak * 1e12) * 1e3
+        per_m[str(m)] = {
+            "ms_per_layer": round(t_ms, 5),
+            "weight_GBps": round(layer_wbytes / (t_ms * 1e-3) / 1e9, 1),
+            "all_bytes_GBps": round(alg / (t_ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm_peak": round(layer_wbytes / (t_ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "roofline_frac_max_bw_tc": round(max(t_bw, t_tc) / t_ms, 4),
+            "TFLOPs": round(flops / (t_ms * 1e-3) / 1e12, 2),
+            "tokens_per_s_per_layer": round(m / (t_ms * 1e-3), 1),
+        }
+    value = world * step_wbytes * K / (elapsed_ms * 1e-3) / 1e9
+
+    # ---- prefill (14B-shaped layer, M = 4096) and quantizer throughput
+    extra_prefill = bench_prefill(q, args, bf16_peak) if not args.skip_extra else None
+    extra_quant = bench_quantize(q, hbm_peak) if not args.skip_extra else None
+
+    # ---- end to end through the public API with host buffers (no graph)
+    e2e = bench_e2e(q, layers, acts, args, copy_for, sigma_for, step_wbytes, world, barrier)
+
+    launches_per_step = len(DECODE_MS) * (len(wl.NOISE_GROUPS) + 2 * len(shapes))
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1*e4m3 (exact fp16) x bf16-as-exact-fp16 -> f32 accumulate, bf16 out",
+        "data": "synthetic (seeded; random-init weights, no checkpoint)",
+        "config": {
+            "workload": WORKLOAD,
+            "weights": "NVFP4 (E2M1 + E4M3 per 16 along K + FP32 tensor scale) quantized by the library from fp32 "
+                       "N(0,0.02^2), 0.5% input channels x10",
+            "weight_bytes_per_step": int(step_wbytes),
+            "l2": f"weights rotate over {N_COPIES} distinct layer copies "
+                  f"({N_COPIES * layer_wbytes / 1e9:.2f} GB) > 129 MB L2; activations stay hot",
+            "launch": "one CUDA graph per (stage, M): 4 AQN samples + 7 linears",
+            "parallelism": f"replicas x{world}",
+        },
+        "per_m": per_m,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "decode linear path per (M, layer) sub-step: 7 x (prep + tcgen05 dequant-MMA) + 4 AQN samples",
+            "achieved": round(sub_bytes_total / (sub_time_total * 1e-3) / 1e9, 1),
+            "peak": hbm_peak,
+            "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)",
+            "unit": "GB/s",
+            "frac": round(sub_bytes_total / (sub_time_total * 1e-3) / 1e9 / hbm_peak, 4),
+            "traffic": None,
+        },
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if extra_prefill:
+        out["prefill"] = extra_prefill
+    if extra_quant:
+        out["quantize"] = extra_quant
+    if rank == 0 and not args.skip_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_oracle(seconds_budget=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def bench_prefill(q, args, bf16_peak):
+    shapes = wl.QWEN_14B
+    m = 4096
+    sigma = 5e-3
+    layer = [QLinear(q, lin, 1, 0, li) for li, lin in enumerate(shapes)]
+    act = Activations(q, shapes, m, 1)
+    run_substep(q, layer, act, sigma, 0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        run_substep(q, layer, act, sigma, 0)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = 10
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t_ms = e0.elapsed_time(e1) / reps
+    q.check(q.qerl_read_status(act.ws), "prefill status")
+    flops = sum(linear_flops(lin, m) for lin in shapes)
+    tf = flops / (t_ms * 1e-3) / 1e12
+    res = {"workload": "Qwen2.5-14B decoder-layer linears, M=4096 (8 x 512 prompt tokens), r=32 alpha=64, "
+                       "AQN sigma=5e-3", "ms_per_layer": round(t_ms, 4), "TFLOPs": round(tf, 1),
+           "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_TFLOPs": bf16_peak,
+           "note": "fp16 operands run at the bf16 dense rate; peak = measured cuBLAS bf16 burst"}
+    del layer, act
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_quantize(q, hbm_peak):
+    shapes = wl.QWEN_7B
+    Ws = [wl.weight_f32_device(lin.n, lin.k, 2, 0, li).to(torch.bfloat16) for li, lin in enumerate(shapes)]
+    outs = [(torch.empty((lin.n, lin.k // 2), dtype=torch.uint8, device="cuda"),
+             torch.empty((lin.n, lin.k // 16), dtype=torch.uint8, device="cuda"),
+             torch.empty(1, dtype=torch.float32, device="cuda")) for lin in shapes]
+    ws = q.workspace(256)
+
+    def run():
+        for W, (c, s, S) in zip(Ws, outs):
+            q.check(q.qerl_nvfp4_quantize(W, c, s, S, ws), "qerl_nvfp4_quantize")
+
+    run()
+    torch.cuda.synchronize()
+    reps = 5
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    t_ms = e0.elapsed_time(e1) / reps
+    q.check(q.qerl_read_status(ws), "quantize status")
+    nw = sum(lin.n * lin.k for lin in shapes)
+    two_pass = nw * (2 + 2 + BYTES_PER_WEIGHT)
+    res = {"workload": "NVFP4 quantization of one Qwen2.5-7B layer's 7 matrices from bf16 (233 M weights)",
+           "ms": round(t_ms, 4), "GBps_two_pass_bytes": round(two_pass / (t_ms * 1e-3) / 1e9, 1),
+           "frac_of_hbm_peak": round(two_pass / (t_ms * 1e-3) / 1e9 / hbm_peak, 4),
+           "bytes_note": "4.5625 B/weight: bf16 read twice (amax pass + encode pass) + 0.5625 B written"}
+    del Ws, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_e2e(q, layers, acts, args, copy_for, sigma_for, step_wbytes, world, barrier):
+    """Same decode step through the public API, eager calls, inputs copied from pinned host
+    memory and outputs copied back to pinned host memory inside the timed region."""
+    host_x = [{g: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for g, t in a.x.items()}
+              for a in acts]
+    host_y = [[torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in a.y] for a in acts]
+    h2d = sum(a.io_bytes()[0] for a in acts)
+    d2h = sum(a.io_bytes()[1] for a in acts)
+
+    def e2e_step(i):
+        for j, a in enumerate(acts):
+            for g, t in a.x.items():
+                t.copy_(host_x[j][g], non_blocking=True)
+            run_substep(q, layers[copy_for(i, j)], a, sigma_for(i), i % NUM_STAGES)
+            for y, hy in zip(a.y, host_y[j]):
+                hy.copy_(y, non_blocking=True)
+
+    for i in range(max(2, args.warmup)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 20))
+    barrier()
+    t = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        e2e_step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t
+    barrier()
+    dev_ms = e0.elapsed_time(e1)
+    t_s = max(wall, dev_ms * 1e-3)
+    return {"value": round(world * step_wbytes * steps / t_s / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": round(t_s * 1e3 / steps, 4),
+            "path": "python binding -> C ABI, eager calls (no graph), pinned host x/y copies in the timed region"}
+
+
+# ---------------------------------------------------------------- oracle (CPU baseline / reference arm)
+
+def _oracle_layer_sample(cols_per_linear=None, shapes=None, seed=0):
+    """Oracle-quantized weights of a 7B-shaped layer (host, from the seeded workload draws)."""
+    import oracle
+    shapes = shapes or wl.QWEN_7B
+    out = []
+    for li, lin in enumerate(shapes):
+        n = lin.n if cols_per_linear is None else min(lin.n, cols_per_linear)
+        W = wl.weight_f32(n, lin.k, seed, 100, li)
+        codes, scales, S = oracle.quantize(W)
+        A = wl.lora_A_bits(lin.k, RANK_R, seed, 100, li)
+        B = wl.lora_B_bits(RANK_R, n, seed, 100, li)
+        out.append((lin, n, codes, scales, S, A, B))
+    return out
+
+
+def _oracle_inputs(layer, ms, seed):
+    """Seeded activations per (M, input group), drawn before any timing."""
+    ks = {lin.group: lin.k for (lin, *_r) in layer}
+    return {m: {g: wl.activations_bits(m, k, seed, 200, m, gi) for gi, (g, k) in enumerate(ks.items())} for m in ms}
+
+
+def _oracle_step(layer, xs, ms, step):
+    """One pass of the oracle over the sample: per M, the AQN sigma and noise of
+    each group present, then every linear of the sample."""
+    import oracle
+    wbytes = 0.0
+    groups = {lin.group: lin.k for (lin, *_r) in layer}
+    for m in ms:
+        sig = oracle.aqn_sigma(step % NUM_STAGES, NUM_STAGES, SIGMA_START, SIGMA_END)
+        zs = {g: oracle.aqn_sample(k, sig, 0, gi, step % NUM_STAGES) for gi, (g, k) in enumerate(groups.items())}
+        for (lin, n, codes, scales, S, A, B) in layer:
+            oracle.lora_linear(xs[m][lin.group], codes, scales, S, z=zs[lin.group], A_bits=A, B_bits=B, alpha=ALPHA)
+            wbytes += n * lin.k * BYTES_PER_WEIGHT
+    return wbytes
+
+
+def cpu_baseline_oracle(seconds_budget=15.0):
+    """The oracle as it stands (single-threaded C, fp64), on a bounded sample of the workload."""
+    layer = _oracle_layer_sample()
+    xs = _oracle_inputs(layer, DECODE_MS, 0)
+    t = time.perf_counter()
+    wbytes = 0.0
+    ms_done = []
+    for m in DECODE_MS:
+        if time.perf_counter() - t > seconds_budget and ms_done:
+            break
+        wbytes += _oracle_step(layer, xs, (m,), 0)
+        ms_done.append(m)
+    dt = time.perf_counter() - t
+    return {"value": round(wbytes / dt / 1e9, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"full 7B-shaped layer (7 linears + 4 AQN samples) at decode M in {ms_done}, one pass each; "
+                      f"{dt:.1f} s; plain C fp64, single thread", "host_cpus": os.cpu_count()}
+
+
+def bench_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cols = 256
+    layer = [e for e in _oracle_layer_sample(cols_per_linear=cols) if e[0].name in ("q", "down")]
+    xs = _oracle_inputs(layer, DECODE_MS, 0)
+    for i in range(args.warmup):
+        _oracle_step(layer, xs, DECODE_MS, i)
+    t = time.perf_counter()
+    wbytes = 0.0
+    for i in range(args.steps):
+        wbytes += _oracle_step(layer, xs, DECODE_MS, i)
+    dt = time.perf_counter() - t
+    value = wbytes / dt / 1e9
+    sample = (f"oracle (plain C fp64, 1 thread) on the q and down linears of the 7B-shaped layer restricted to "
+              f"{cols} output columns, M in {list(DECODE_MS)}, 4 AQN samples per M, per step")
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "sample": sample},
+           "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-extra", action="store_true", help="skip the prefill and quantizer measurements")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -156,7 +156,7 @@ QERL_API qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t 
  *         256-byte aligned, zero-filled before its first use; holds the
  *         staged noisy activations, the LoRA down-projection x~.A and the
  *         status word.  Calls sharing a workspace must be stream-ordered.
- * Requires k % 64 == 0, k > 0, m >= 0, n >= 0 (m == 0 or n == 0: no-op).
+ * Requires k % 64 == 0, 0 < k <= 65536, m >= 0, n >= 0 (m == 0 or n == 0: no-op).
  * Accumulation is fp32; x~ and the dequantized weights enter the tensor
  * cores exactly (see the design notes for the power-of-two row staging).
  * ======================================================================== */

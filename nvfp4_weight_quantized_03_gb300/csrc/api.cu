@@ -123,7 +123,7 @@ qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, c
   if (r > 0 && A == nullptr) r = 0;
   if (A != nullptr && r == 0) return QERL_ERR_INVALID_ARGUMENT;
   if (k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
-  if (r > 128) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (r > 128 || k > 65536) return QERL_ERR_UNSUPPORTED_SHAPE;
   if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX || m * k > (int64_t{1} << 40))
     return QERL_ERR_UNSUPPORTED_SHAPE;
   if (m == 0 || n == 0) return QERL_OK;

@@ -31,28 +31,29 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 key) {
   return c;
 }
 
+// One thread per Box-Muller pair: pair p covers channels 2p, 2p+1 and uses
+// words (x, y) or (z, w) of the Philox block of counter index p / 2.  fp64
+// transcendental throughput per SM is low, so blocks are small and spread the
+// pairs over many SMs.
 __global__ void aqn_sample_kernel(float* __restrict__ z, int64_t k, float sigma, uint64_t seed, uint32_t stream_id,
                                   uint64_t counter) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (4 * i >= k) return;
+  const int64_t pair = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (2 * pair >= k) return;
+  const int64_t i = pair >> 1;
   const uint4 bits = philox4x32_10(
       make_uint4(static_cast<uint32_t>(i), stream_id, static_cast<uint32_t>(counter),
                  static_cast<uint32_t>(counter >> 32)),
       make_uint2(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)));
   constexpr double kInv32 = 1.0 / 4294967296.0;
   constexpr double kTwoPi = 6.283185307179586476925286766559;
-  const double u0 = (static_cast<double>(bits.x) + 0.5) * kInv32;
-  const double u1 = (static_cast<double>(bits.y) + 0.5) * kInv32;
-  const double u2 = (static_cast<double>(bits.z) + 0.5) * kInv32;
-  const double u3 = (static_cast<double>(bits.w) + 0.5) * kInv32;
-  const double rho0 = sqrt(-2.0 * log(u0));
-  const double rho1 = sqrt(-2.0 * log(u2));
-  const double nrm[4] = {rho0 * cos(kTwoPi * u1), rho0 * sin(kTwoPi * u1), rho1 * cos(kTwoPi * u3),
-                         rho1 * sin(kTwoPi * u3)};
+  const uint32_t w0 = (pair & 1) ? bits.z : bits.x;
+  const uint32_t w1 = (pair & 1) ? bits.w : bits.y;
+  const double ua = (static_cast<double>(w0) + 0.5) * kInv32;
+  const double ub = (static_cast<double>(w1) + 0.5) * kInv32;
+  const double rho = sqrt(-2.0 * log(ua));
   const double sd = static_cast<double>(sigma);
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (4 * i + j < k) z[4 * i + j] = static_cast<float>(sd * nrm[j]);
+  z[2 * pair] = static_cast<float>(sd * (rho * cos(kTwoPi * ub)));
+  if (2 * pair + 1 < k) z[2 * pair + 1] = static_cast<float>(sd * (rho * sin(kTwoPi * ub)));
 }
 
 }  // namespace
@@ -60,9 +61,9 @@ __global__ void aqn_sample_kernel(float* __restrict__ z, int64_t k, float sigma,
 qerl_status launch_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, uint32_t stream_id,
                               uint64_t counter, cudaStream_t s) {
   if (k == 0) return QERL_OK;
-  const int64_t groups = (k + 3) / 4;
-  const int threads = 128;
-  const int64_t blocks = (groups + threads - 1) / threads;
+  const int64_t pairs = (k + 1) / 2;
+  const int threads = 32;
+  const int64_t blocks = (pairs + threads - 1) / threads;
   aqn_sample_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(z, k, sigma, seed, stream_id, counter);
   return cuda_status(cudaGetLastError());
 }

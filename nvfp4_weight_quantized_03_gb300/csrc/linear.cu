@@ -16,21 +16,24 @@
 //   - LoRA tasks: t = x~ . A over a K-slice, fp32, reduced with atomics.
 //
 // mma_kernel  (tcgen05 + TMA, the hot loop): a 128-output-feature tile of W
-//   is the MMA's M side, tokens are the MMA's N side (16..256), K streams in
-//   64-element stages.
-//     warp 8      producer: TMA of the packed codes (128 rows x 32 B, 32-byte
-//                 swizzle), cp.async of the E4M3 scales (128 x 4 B), TMA of the
-//                 staged x~ tile (n_tok x 64 fp16, 128-byte swizzle).
+//   is the MMA's M side, tokens are the MMA's N side (16..256).
+//     warp 8      weight producer: per 256-wide K stage, TMA of the packed
+//                 codes (128 rows x 128 contiguous bytes, 128-byte swizzle)
+//                 and cp.async of the E4M3 scales (128 rows x 16 bytes).
 //     warps 0..7  dequant: E2M1 pairs -> fp16 pairs (cvt.f16x2.e2m1x2), times
-//                 the block scale (cvt.f16x2.e4m3x2) -- exact products -- written
-//                 in the 128-byte-swizzled K-major layout the MMA reads.
-//     warp 9      MMA issuer: 4 x tcgen05.mma kind::f16 (M=128, N=n_tok, K=16)
-//                 per stage into an fp32 TMEM accumulator; tcgen05.commit frees
-//                 the stage.
-//   Epilogue (warps 0..7): TMEM -> registers, y = acc * S * 2^-e_m
-//   + (alpha/r) t.B, rounded to bf16.  Small-N decode shapes split K across a
-//   thread-block cluster; partner CTAs reduce their fp32 partial tiles
-//   through distributed shared memory, with no global scratch and no atomics.
+//                 the block scale (cvt.f16x2.e4m3x2) -- exact products --
+//                 written per 64-wide K stage in the 128-byte-swizzled K-major
+//                 layout the MMA reads; they also build the LoRA operands.
+//     warp 10     activation producer: TMA of the staged x~ tile per 64-wide
+//                 K stage (n_tok x 64 fp16).
+//     warp 9      MMA issuer: 4 x tcgen05.mma kind::f16 (M=128, N=n_tok,
+//                 K=16) per stage into an fp32 TMEM accumulator D; the LoRA
+//                 up-projection runs on the tensor cores too, into a second
+//                 accumulator D2 = B^T . (t_hi + t_lo), bf16 x bf16 -> fp32.
+//   Epilogue (warps 0..7): y = S * 2^-e_m * D + (alpha/r) * D2, rounded to
+//   bf16.  Small-N decode shapes split K across a thread-block cluster; each
+//   CTA writes its scaled partial tile to shared memory and partner CTAs sum
+//   them through distributed shared memory (no global scratch, no atomics).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -76,6 +79,9 @@ __device__ __forceinline__ float noisy(float xv, float zv) {
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int tid = threadIdx.x;
+  // The MMA kernel may start its prologue (barriers, TMEM, weight loads) now;
+  // it waits for this grid's results before it reads them.
+  griddep_launch_dependents();
   if (blockIdx.x < p.row_tasks) {
     // ---- row task: x~ row -> smem (bf16), amax, then fp16 * 2^e
     const int m = blockIdx.x;
@@ -173,14 +179,19 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
 
 // ------------------------------------------------------------------ MMA kernel
 
-constexpr int kMmaThreads = 320;  // warps 0-7 dequant+epilogue, 8 producer, 9 MMA
+constexpr int kMmaThreads = 352;  // warps 0-7 dequant + epilogue, 8 weight producer, 9 MMA, 10 activation producer
 constexpr int kTileN = 128;       // output features per CTA (MMA M)
-constexpr int kStageK = 64;       // K per pipeline stage
-constexpr int kCodesStageBytes = kTileN * kStageK / 2;   // 4096
-constexpr int kScalesStageBytes = kTileN * kStageK / 16; // 512
-constexpr int kAStageBytes = kTileN * kStageK * 2;       // 16384 (fp16)
-constexpr int kMaxStages = 8;
+constexpr int kStageK = 64;       // K per MMA stage (4 x K=16 instructions)
+constexpr int kRawK = 256;        // K per weight-load stage: 128 contiguous bytes of codes per row
+constexpr int kSub = kRawK / kStageK;                  // MMA stages per weight stage
+constexpr int kCodesRawBytes = kTileN * kRawK / 2;     // 16384
+constexpr int kScalesRawBytes = kTileN * kRawK / 16;   // 2048
+constexpr int kAStageBytes = kTileN * kStageK * 2;     // 16384 (fp16)
+constexpr int kLoraChunkK = 64;                        // r is processed in 64-wide chunks (one 128-B swizzle atom)
+constexpr int kBtChunkBytes = kTileN * 128;            // B^T chunk: 128 rows x 64 bf16
+constexpr int kMaxRaw = 8, kMaxAB = 8;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
+constexpr int kBarBytes = 512;
 
 struct MmaParams {
   const uint8_t* scales;
@@ -191,38 +202,20 @@ struct MmaParams {
   void* y;
   int* status;
   int M, N, K, r;
-  int n_tok;   // tokens per tile (MMA N), multiple of 16, <= 256
-  int split;   // K split across the cluster (gridDim.x)
-  int stages;  // pipeline depth
+  int n_tok;       // tokens per tile (MMA N), multiple of 16, <= 256
+  int split;       // K split across the cluster (gridDim.x), in weight stages
+  int raw_stages;  // weight-stage ring depth
+  int ab_stages;   // dequantized-A / activation-B ring depth
   int tmem_cols;
-  uint32_t bars_off;  // barrier block offset: after both the ring and the epilogue staging
+  uint32_t off_codes, off_a, off_b, off_scales, off_lora, off_sm, off_bars;
+  int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
   float lora_scale;
   int y_f32;
 };
 
-struct SmemLayout {
-  uint32_t a, b, codes, scales, ring_bytes;
-};
-
-__host__ __device__ inline SmemLayout smem_layout(int n_tok, int stages) {
-  SmemLayout L;
-  const uint32_t b_stage = static_cast<uint32_t>(n_tok) * 128u;
-  L.a = 0;
-  L.b = L.a + stages * kAStageBytes;
-  L.codes = L.b + stages * b_stage;
-  L.scales = L.codes + stages * kCodesStageBytes;
-  L.ring_bytes = L.scales + stages * kScalesStageBytes;
-  return L;
-}
-
-__host__ __device__ inline uint32_t epilogue_bytes(int n_tok, int r, int split) {
-  uint32_t part = split > 1 ? static_cast<uint32_t>(n_tok) * kTileN * 4u : 0u;
-  return part + static_cast<uint32_t>(n_tok) * r * 4u + static_cast<uint32_t>(r) * kTileN * 4u +
-         static_cast<uint32_t>(n_tok) * 4u;
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+__host__ __device__ inline int lora_chunks(int r) { return (r + kLoraChunkK - 1) / kLoraChunkK; }
+__host__ __device__ inline uint32_t lora_bytes(int r, int n_tok) {
+  return r > 0 ? static_cast<uint32_t>(lora_chunks(r)) * (kBtChunkBytes + 2u * n_tok * 128u) : 0u;
 }
 
 __device__ __forceinline__ void store_out(const MmaParams& p, int m, int n, float v) {
@@ -233,36 +226,122 @@ __device__ __forceinline__ void store_out(const MmaParams& p, int m, int n, floa
     reinterpret_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(v);
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// LoRA up-projection operands in the 128-byte-swizzled K-major layout (the
+// rank index j is the MMA's K), built by warps 0-7 (tid 0..255) at `base`:
+//   B^T chunk c:  128 rows n  x 64 j   bf16  = B[c*64 + j][n0 + n]           (exact copy)
+//   t_hi chunk c: n_tok rows m x 64 j  bf16  = bf16(t[m0 + m][c*64 + j])
+//   t_lo chunk c: n_tok rows m x 64 j  bf16  = bf16(t - t_hi)
+// so that B^T . t_hi + B^T . t_lo carries t to ~16 significant bits.  Zero
+// past M, N and r.
+__device__ void build_lora_tiles(const MmaParams& p, uint32_t base, int m0, int n0, int tid) {
+  const int rc = lora_chunks(p.r);
+  for (int idx = tid; idx < rc * kTileN * 8; idx += 256) {
+    const int c = idx / (kTileN * 8), rem = idx - c * (kTileN * 8);
+    const int g = rem / kTileN, n = rem - g * kTileN;
+    const bool nin = n0 + n < p.N;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j0 = c * kLoraChunkK + g * 8 + 2 * e;
+      const uint32_t lo = (nin && j0 < p.r) ? __bfloat16_as_ushort(p.B[static_cast<int64_t>(j0) * p.N + n0 + n]) : 0u;
+      const uint32_t hi =
+          (nin && j0 + 1 < p.r) ? __bfloat16_as_ushort(p.B[static_cast<int64_t>(j0 + 1) * p.N + n0 + n]) : 0u;
+      w[e] = lo | (hi << 16);
+    }
+    sts128(base + c * kBtChunkBytes + n * 128 + ((g ^ (n & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+  }
+  const uint32_t thi = base + rc * kBtChunkBytes;
+  const uint32_t tlo = thi + rc * p.n_tok * 128;
+  for (int idx = tid; idx < rc * p.n_tok * 8; idx += 256) {
+    const int c = idx / (p.n_tok * 8), rem = idx - c * (p.n_tok * 8);
+    const int ml = rem >> 3, g = rem & 7;
+    const int m = m0 + ml;
+    float tv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int j = c * kLoraChunkK + g * 8 + e;
+      tv[e] = (m < p.M && j < p.r) ? __ldg(p.t + static_cast<int64_t>(m) * p.r + j) : 0.0f;
+    }
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float h0 = __bfloat162float(__float2bfloat16_rn(tv[2 * e]));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(tv[2 * e + 1]));
+      hw[e] = pack_bf16x2(h0, h1);
+      lw[e] = pack_bf16x2(tv[2 * e] - h0, tv[2 * e + 1] - h1);
+    }
+    const uint32_t off = c * p.n_tok * 128 + ml * 128 + ((g ^ (ml & 7)) << 4);
+    sts128(thi + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    sts128(tlo + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+  }
+}
+
+// D2 (+)= B^T . t_hi^T + B^T . t_lo^T over the rank dimension (bf16 x bf16 -> fp32).
+__device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, uint32_t base, uint32_t d2) {
+  const int rc = lora_chunks(p.r);
+  const uint32_t idesc = idesc_bf16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
+  const uint32_t thi = base + rc * kBtChunkBytes;
+  const uint32_t tlo = thi + rc * p.n_tok * 128;
+  uint32_t acc = 0;
+  for (int c = 0; c < rc; ++c)
+    for (int kk = 0; kk < kLoraChunkK / 16 && c * kLoraChunkK + kk * 16 < p.r; ++kk) {
+      const uint64_t ad = sw128_kmajor_desc(base + c * kBtChunkBytes + kk * 32);
+      tc_mma_f16(d2, ad, sw128_kmajor_desc(thi + c * p.n_tok * 128 + kk * 32), idesc, acc);
+      tc_mma_f16(d2, ad, sw128_kmajor_desc(tlo + c * p.n_tok * 128 + kk * 32), idesc, 1u);
+      acc = 1;
+    }
+}
+
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_xs,
                const MmaParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemLayout L = smem_layout(p.n_tok, p.stages);
-  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + p.bars_off);
-  uint64_t* op_full = raw_full + kMaxStages;
-  uint64_t* empty = op_full + kMaxStages;
-  uint64_t* acc_full = empty + kMaxStages;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem_gen = smem_raw + (sbase - raw_addr);  // generic view (abort flag, TMEM holder)
+  const uint32_t bars = sbase + p.off_bars;
+  auto raw_full = [&](int s) { return bars + 8u * s; };
+  auto raw_empty = [&](int s) { return bars + 8u * (kMaxRaw + s); };
+  auto ab_full = [&](int s) { return bars + 8u * (2 * kMaxRaw + s); };
+  auto ab_empty = [&](int s) { return bars + 8u * (2 * kMaxRaw + kMaxAB + s); };
+  constexpr int kB2 = 2 * kMaxRaw + 2 * kMaxAB;
+  const uint32_t ring_free = bars + 8u * kB2;
+  const uint32_t lora_full = bars + 8u * (kB2 + 1);
+  const uint32_t acc_full = bars + 8u * (kB2 + 2);
+  const uint32_t tmem_holder = bars + 8u * (kB2 + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_gen + p.off_bars + 8 * (kB2 + 3) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split_idx = blockIdx.x;
   const int n0 = blockIdx.y * kTileN;
   const int m0 = blockIdx.z * p.n_tok;
-  const int ks_total = p.K / kStageK;
-  const int ks_begin = static_cast<int>(static_cast<int64_t>(split_idx) * ks_total / p.split);
-  const int ks_end = static_cast<int>(static_cast<int64_t>(split_idx + 1) * ks_total / p.split);
-  const int nks = ks_end - ks_begin;
-  const int stages = p.stages;
+  const int raw_total = (p.K + kRawK - 1) / kRawK;
+  const int rb = static_cast<int>(static_cast<int64_t>(split_idx) * raw_total / p.split);
+  const int re = static_cast<int>(static_cast<int64_t>(split_idx + 1) * raw_total / p.split);
+  const int nraw = re - rb;
+  const int kb_total = p.K / kStageK;
+  const int mma_begin = kSub * rb;
+  const int nmma = min(kSub * re, kb_total) - mma_begin;
+  const int RS = p.raw_stages, AS = p.ab_stages;
+  const bool do_lora = p.r > 0 && split_idx == 0;  // one CTA of a K-split cluster adds the LoRA term
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(&raw_full[s], 33);  // producer expect_tx + 32 cp.async arrivals
-      mbar_init(&op_full[s], 9);    // 8 dequant warps + producer expect_tx (x~ tile)
-      mbar_init(&empty[s], 1);      // tcgen05.commit
+    for (int s = 0; s < RS; ++s) {
+      mbar_init_a(raw_full(s), 33);  // producer expect_tx + 32 cp.async arrivals
+      mbar_init_a(raw_empty(s), 8);  // 8 dequant warps
     }
-    mbar_init(acc_full, 1);
+    for (int s = 0; s < AS; ++s) {
+      mbar_init_a(ab_full(s), 9);   // 8 dequant warps + activation producer expect_tx
+      mbar_init_a(ab_empty(s), 1);  // tcgen05.commit
+    }
+    mbar_init_a(ring_free, 1);
+    mbar_init_a(lora_full, 8);
+    mbar_init_a(acc_full, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -277,162 +356,215 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_holder;
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem_gen + p.off_bars + 8 * (kB2 + 3));
+  const uint32_t d_acc = tmem_base;
+  const uint32_t d_lora = tmem_base + static_cast<uint32_t>(p.n_tok);
+  const uint32_t lora_base = p.lora_early ? sbase + p.off_lora : sbase;  // late: inside the idle ring
+  const uint32_t smv = sbase + p.off_sm;
 
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ weight producer
     const int kq = p.K / 16;  // scale bytes per row
-    for (int i = 0; i < nks; ++i) {
-      const int s = i % stages;
-      const uint32_t ph = (i / stages) & 1;
+    const bool vec_scales = (p.K % kRawK) == 0;
+    for (int i = 0; i < nraw; ++i) {
+      const int s = i % RS;
+      const uint32_t ph = (i / RS) & 1;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status);
+      if (lane == 0) ok = mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
-      const int kidx = ks_begin + i;
+      const int rst = rb + i;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&raw_full[s], kCodesStageBytes);
-        tma_load_2d(smem + L.codes + s * kCodesStageBytes, &tm_codes, kidx * (kStageK / 2), n0, &raw_full[s]);
+        mbar_arrive_expect_tx_a(raw_full(s), kCodesRawBytes);
+        tma_load_2d(sbase + p.off_codes + s * kCodesRawBytes, &tm_codes, rst * (kRawK / 2), n0, raw_full(s));
       }
-      uint8_t* sdst = smem + L.scales + s * kScalesStageBytes;
+      const uint32_t sdst = sbase + p.off_scales + s * kScalesRawBytes;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int row = lane * 4 + j;
         const int n = n0 + row;
         const bool in = n < p.N;
-        const uint8_t* src = p.scales + static_cast<int64_t>(in ? n : 0) * kq + kidx * 4;
-        cp_async_4(sdst + row * 4, src, in ? 4u : 0u);
+        const uint8_t* src = p.scales + static_cast<int64_t>(in ? n : 0) * kq + rst * 16;
+        if (vec_scales) {
+          cp_async_16(sdst + row * 16, src, in ? 16u : 0u);
+        } else {
+#pragma unroll
+          for (int qq = 0; qq < kSub; ++qq) {
+            const bool v = in && (rst * kSub + qq) < kb_total;
+            cp_async_4(sdst + row * 16 + 4 * qq, v ? src + 4 * qq : p.scales, v ? 4u : 0u);
+          }
+        }
       }
-      cp_async_mbar_arrive_noinc(&raw_full[s]);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&op_full[s], static_cast<uint32_t>(p.n_tok) * 128u);
-        tma_load_2d(smem + L.b + s * (p.n_tok * 128), &tm_xs, kidx * kStageK, m0, &op_full[s]);
+      cp_async_mbar_arrive_noinc(raw_full(s));
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ activation producer
+    griddep_wait();  // the staged activations are written by the preceding kernel
+    if (lane == 0) {
+      for (int j = 0; j < nmma; ++j) {
+        const int s = j % AS;
+        const uint32_t ph = (j / AS) & 1;
+        if (!mbar_wait_a(ab_empty(s), ph ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx_a(ab_full(s), static_cast<uint32_t>(p.n_tok) * 128u);
+        tma_load_2d(sbase + p.off_b + s * (p.n_tok * 128), &tm_xs, (mma_begin + j) * kStageK, m0, ab_full(s));
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      if (do_lora && p.lora_early) {
+        if (mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
+          tc_fence_after();
+          issue_lora_mmas(p, lora_base, d_lora);
+        }
+      }
       const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
-      for (int i = 0; i < nks; ++i) {
-        const int s = i % stages;
-        const uint32_t ph = (i / stages) & 1;
-        if (!mbar_wait(&op_full[s], ph, abort_flag, p.status)) break;
+      for (int j = 0; j < nmma; ++j) {
+        const int s = j % AS;
+        const uint32_t ph = (j / AS) & 1;
+        if (!mbar_wait_a(ab_full(s), ph, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(smem + L.a + s * kAStageBytes);
-        const uint32_t b_addr = smem_u32(smem + L.b + s * (p.n_tok * 128));
+        const uint32_t a_addr = sbase + p.off_a + s * kAStageBytes;
+        const uint32_t b_addr = sbase + p.off_b + s * (p.n_tok * 128);
 #pragma unroll
         for (int kk = 0; kk < kStageK / 16; ++kk)
-          tc_mma_f16(tmem_base, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&empty[s]);
+          tc_mma_f16(d_acc, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(ab_empty(s));
+      }
+      if (do_lora && !p.lora_early) {
+        tc_commit(ring_free);  // the ring is idle once the mainloop MMAs are done
+        if (mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
+          tc_fence_after();
+          issue_lora_mmas(p, lora_base, d_lora);
+        }
       }
       tc_commit(acc_full);  // always, so the epilogue's wait completes even after an abort
     }
   } else {
-    // ------------------------------------------------------------ dequant (warps 0-7)
-    const int row = 16 * warp + (lane & 15);
-    const int half = lane >> 4;
-    for (int i = 0; i < nks; ++i) {
-      const int s = i % stages;
-      const uint32_t ph = (i / stages) & 1;
-      if (!mbar_wait(&raw_full[s], ph, abort_flag, p.status)) break;
-      uint32_t coff = static_cast<uint32_t>(row * 32 + half * 16);
-      coff ^= ((coff >> 7) & 1u) << 4;  // 32-byte TMA swizzle: bit 4 ^= bit 7
-      const uint4 cw = *reinterpret_cast<const uint4*>(smem + L.codes + s * kCodesStageBytes + coff);
-      const uint32_t sc2 =
-          *reinterpret_cast<const uint16_t*>(smem + L.scales + s * kScalesStageBytes + row * 4 + half * 2);
-      const __half2 s01 = e4m3x2_to_half2(sc2);
-      const __half2 sa = __low2half2(s01), sb = __high2half2(s01);
-      const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-      uint8_t* arow = smem + L.a + s * kAStageBytes + row * 128;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const __half2 sq = q < 2 ? sa : sb;
-        uint4 o;
-        __half2* oh = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) oh[b] = __hmul2(e2m1x2_to_half2((words[q] >> (8 * b)) & 0xFFu), sq);
-        const int chunk = half * 4 + q;
-        *reinterpret_cast<uint4*>(arow + ((chunk ^ (row & 7)) << 4)) = o;
-      }
+    // ------------------------------------------------------------ warps 0-7: dequant
+    griddep_wait();  // row scales (and t) come from the preceding kernel
+    {
+      const float S = *p.tensor_scale;
+      for (int i = threadIdx.x; i < p.n_tok; i += 256)
+        stsf(smv + 4u * i, (m0 + i < p.M) ? S * __ldg(p.rinv + m0 + i) : 0.0f);
+    }
+    if (do_lora && p.lora_early) {
+      build_lora_tiles(p, lora_base, m0, n0, threadIdx.x);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&op_full[s]);
+      if (lane == 0) mbar_arrive_a(lora_full);
+    }
+    const int row = 16 * warp + (lane & 15);
+    const int half = lane >> 4;
+    const uint32_t arow = static_cast<uint32_t>(row * 128);
+    int j = 0;
+    for (int i = 0; i < nraw; ++i) {
+      const int s = i % RS;
+      const uint32_t ph = (i / RS) & 1;
+      if (!mbar_wait_a(raw_full(s), ph, abort_flag, p.status)) break;
+      const uint32_t crow = sbase + p.off_codes + s * kCodesRawBytes + row * 128;
+      const uint32_t srow = sbase + p.off_scales + s * kScalesRawBytes + row * 16 + half * 2;
+      bool ok = true;
+      for (int q = 0; q < kSub && j < nmma; ++q, ++j) {
+        const int as = j % AS;
+        const uint32_t aph = (j / AS) & 1;
+        if (!mbar_wait_a(ab_empty(as), aph ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        // 32 codes (16 B) of this thread: 16-byte chunk (2q + half) of the row, 128-byte TMA swizzle
+        const uint4 cw = lds128(crow + (((2 * q + half) ^ (row & 7)) << 4));
+        const uint32_t sc2 = lds16(srow + 4 * q);
+        const __half2 s01 = e4m3x2_to_half2(sc2);
+        const __half2 sa = __low2half2(s01), sb = __high2half2(s01);
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        const uint32_t a_s = sbase + p.off_a + as * kAStageBytes + arow;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const __half2 sq = qq < 2 ? sa : sb;
+          uint4 o;
+          __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+          for (int b = 0; b < 4; ++b) oh[b] = __hmul2(e2m1x2_to_half2((words[qq] >> (8 * b)) & 0xFFu), sq);
+          const int chunk = half * 4 + qq;
+          sts128(a_s + ((chunk ^ (row & 7)) << 4), o);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_a(ab_full(as));
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_a(raw_empty(s));
+    }
+    if (do_lora && !p.lora_early) {
+      if (mbar_wait_a(ring_free, 0, abort_flag, p.status)) build_lora_tiles(p, lora_base, m0, n0, threadIdx.x);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_a(lora_full);
     }
   }
 
   // ---------------------------------------------------------------- epilogue
-  float* part = reinterpret_cast<float*>(smem);  // [n_tok][128] fp32 partial (split > 1)
-  float* ts = part + (p.split > 1 ? p.n_tok * kTileN : 0);  // [n_tok][r]
-  float* bs = ts + p.n_tok * p.r;                            // [r][128]
-  float* sm = bs + p.r * kTileN;                             // [n_tok] S * 2^-e_m
+  const uint32_t part = sbase;  // [n_tok][128] fp32 scaled partial tile (split > 1), ring reused
   if (warp < 8) {
-    const bool ok = mbar_wait(acc_full, 0, abort_flag, p.status);
+    const bool ok = mbar_wait_a(acc_full, 0, abort_flag, p.status);
     tc_fence_after();
-    // The ring is idle once the accumulator is complete: stage the epilogue operands there.
-    const float S = *p.tensor_scale;
-    for (int i = threadIdx.x; i < p.n_tok * p.r; i += 256) {
-      const int m = m0 + i / p.r;
-      ts[i] = (m < p.M) ? p.t[static_cast<int64_t>(m) * p.r + (i % p.r)] : 0.0f;
-    }
-    for (int i = threadIdx.x; i < p.r * kTileN; i += 256) {
-      const int n = n0 + (i % kTileN);
-      bs[i] = (n < p.N) ? __bfloat162float(p.B[static_cast<int64_t>(i / kTileN) * p.N + n]) : 0.0f;
-    }
-    for (int i = threadIdx.x; i < p.n_tok; i += 256) sm[i] = (m0 + i < p.M) ? S * p.rinv[m0 + i] : 0.0f;
-    named_bar_sync(1, 256);
-
     const int q = warp & 3;
     const int nl = q * 32 + lane;
     const int n = n0 + nl;
     const int cols = p.n_tok / 2;
     const int c0 = (warp >> 2) * cols;
-    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     for (int c = c0; c < c0 + cols; c += 8) {
-      float v[8];
-      tmem_ld_x8(taddr + c, v);
+      float v[8], l[8];
+      tmem_ld_x8(d_acc + lane_off + c, v);
+      if (do_lora) tmem_ld_x8(d_lora + lane_off + c, l);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int ml = c + j;
-        const float acc = ok ? v[j] : 0.0f;
-        if (p.split > 1) {
-          part[ml * kTileN + nl] = acc;
-        } else if (m0 + ml < p.M && n < p.N) {
-          float l = 0.0f;
-          for (int jj = 0; jj < p.r; ++jj) l = fmaf(ts[ml * p.r + jj], bs[jj * kTileN + nl], l);
-          store_out(p, m0 + ml, n, fmaf(p.lora_scale, l, acc * sm[ml]));
-        }
+      for (int e = 0; e < 8; ++e) {
+        float out = ok ? v[e] * ldsf(smv + 4u * (c + e)) : 0.0f;
+        if (do_lora && ok) out = fmaf(p.lora_scale, l[e], out);
+        if (p.split > 1)
+          stsf(part + 4u * ((c + e) * kTileN + nl), out);
+        else if (m0 + c + e < p.M && n < p.N)
+          store_out(p, m0 + c + e, n, out);
       }
     }
   }
   if (*abort_flag) {
     // Let copies that were already issued land before shared memory is released.
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 50000ull) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < 200000ll) {
     }
   }
   tc_fence_before();
   __syncthreads();
 
   if (p.split > 1) {
-    cluster_sync_all();  // every partner's partial tile is in its shared memory
+    cluster_sync_all();  // every partner's scaled partial tile is in its shared memory
     if (warp < 8) {
       const int rank = static_cast<int>(cluster_ctarank());
       const int per = (p.n_tok + p.split - 1) / p.split;
       const int mb = rank * per;
-      const int me = min(p.n_tok, mb + per);
-      const uint32_t part_addr = smem_u32(part);
-      for (int i = threadIdx.x; i < (me - mb) * kTileN; i += 256) {
-        const int ml = mb + i / kTileN, nl = i % kTileN;
-        const int n = n0 + nl;
-        if (m0 + ml >= p.M || n >= p.N) continue;
-        const uint32_t off = static_cast<uint32_t>(ml * kTileN + nl) * 4u;
-        float acc = 0.0f;
-        for (int qq = 0; qq < p.split; ++qq) acc += ld_shared_cluster_f32(mapa_shared(part_addr + off, qq));
-        float l = 0.0f;
-        for (int jj = 0; jj < p.r; ++jj) l = fmaf(ts[ml * p.r + jj], bs[jj * kTileN + nl], l);
-        store_out(p, m0 + ml, n, fmaf(p.lora_scale, l, acc * sm[ml]));
+      const int me = min(min(p.n_tok, mb + per), p.M - m0);
+      for (int it = threadIdx.x; it < (me - mb) * (kTileN / 4); it += 256) {
+        const int ml = mb + it / (kTileN / 4);
+        const int nl4 = 4 * (it % (kTileN / 4));
+        const uint32_t off = 4u * static_cast<uint32_t>(ml * kTileN + nl4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int qq = 0; qq < p.split; ++qq) {
+          const float4 v = ld_shared_cluster_f32x4(mapa_shared(part + off, qq));
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        const float out[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (n0 + nl4 + e < p.N) store_out(p, m0 + ml, n0 + nl4 + e, out[e]);
       }
     }
     cluster_sync_all();  // partners are done reading this CTA's partial tile
@@ -470,16 +602,11 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uin
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct DeviceInfo {
-  int sms = 148;
-};
-
-DeviceInfo device_info() {
-  DeviceInfo d;
-  int dev = 0;
+int sm_count() {
+  int dev = 0, sms = 148;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-  return d;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
 }
 
 struct LinearLayout {
@@ -509,7 +636,88 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   __half* xs = reinterpret_cast<__half*>(ws + WL.xs);
   float* rinv = reinterpret_cast<float*>(ws + WL.rinv);
   float* t = reinterpret_cast<float*>(ws + WL.t);
-  const DeviceInfo dev = device_info();
+  const int sms = sm_count();
+
+  // Kernel attributes are set once per process (not per call), so calls can be
+  // captured into CUDA graphs.
+  constexpr int kPrepSmemLimit = kSmemLimit - 1024;  // leaves room for the kernel's static shared memory
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemLimit);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  });
+  if (attr_err != cudaSuccess) return QERL_ERR_CUDA;
+
+  // ---- tile shape and pipeline depth (host-side checks before any launch)
+  int n_tok, m_tiles;
+  if (M <= 256) {
+    n_tok = (M + 15) / 16 * 16;
+    m_tiles = 1;
+  } else {
+    n_tok = 256;
+    m_tiles = (M + 255) / 256;
+  }
+  const int n_tiles = (N + kTileN - 1) / kTileN;
+  const int raw_total = (K + kRawK - 1) / kRawK;
+  int split = 1;
+  if (n_tok <= 128) {
+    // K split across a cluster when the tiles alone leave SMs idle: minimise
+    // waves x weight stages per CTA, with a small per-CTA fixed cost.
+    double best = 1e30;
+    for (int sp = 1; sp <= 8 && sp <= raw_total; ++sp) {
+      const int ctas = n_tiles * m_tiles * sp;
+      const int waves = (ctas + sms - 1) / sms;
+      const double cost = waves * (static_cast<double>((raw_total + sp - 1) / sp) + 1.5);
+      if (cost < best - 1e-9) {
+        best = cost;
+        split = sp;
+      }
+    }
+  }
+  const uint32_t lb = lora_bytes(r, n_tok);
+  const int lora_early = (r > 0 && n_tok <= 128) ? 1 : 0;
+  const uint32_t part_bytes = split > 1 ? static_cast<uint32_t>(n_tok) * kTileN * 4u : 0u;
+  const uint32_t b_stage = static_cast<uint32_t>(n_tok) * 128u;
+  struct Plan {
+    uint32_t codes, a, b, scales, lora, sm, bars, total;
+  };
+  auto plan_for = [&](int rs, int as) {
+    Plan P;
+    P.codes = 0;
+    P.a = P.codes + rs * kCodesRawBytes;
+    P.b = P.a + as * kAStageBytes;
+    P.scales = P.b + as * b_stage;
+    uint32_t ring = P.scales + rs * kScalesRawBytes;
+    if (!lora_early) ring = std::max(ring, lb);  // late LoRA tiles are built inside the ring
+    ring = std::max(ring, part_bytes);
+    P.lora = static_cast<uint32_t>(align_up(ring, 1024));
+    P.sm = P.lora + (lora_early ? lb : 0u);
+    P.bars = static_cast<uint32_t>(align_up(P.sm + static_cast<uint32_t>(n_tok) * 4u, 16));
+    P.total = P.bars + kBarBytes + 1024u;  // + 1024-byte alignment slack
+    return P;
+  };
+  int ab_stages = n_tok <= 64 ? 6 : (n_tok <= 128 ? 4 : 3);
+  int raw_stages = 0;
+  for (; ab_stages >= 2 && raw_stages < 2; --ab_stages) {
+    for (raw_stages = kMaxRaw; raw_stages >= 2; --raw_stages)
+      if (plan_for(raw_stages, ab_stages).total <= static_cast<uint32_t>(kSmemLimit)) break;
+    if (raw_stages >= 2) break;
+  }
+  if (raw_stages < 2 || ab_stages < 2) return QERL_ERR_UNSUPPORTED_SHAPE;
+  const Plan P = plan_for(raw_stages, ab_stages);
+  int tmem_cols = 32;
+  while (tmem_cols < (r > 0 ? 2 * n_tok : n_tok)) tmem_cols *= 2;
+
+  CUtensorMap tm_codes, tm_xs;
+  if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, static_cast<uint64_t>(K) / 2,
+                   static_cast<uint64_t>(N), static_cast<uint64_t>(K) / 2, kRawK / 2, kTileN,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return QERL_ERR_CUDA;
+  if (!make_map_2d(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xs, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(K) * 2, kStageK, static_cast<uint32_t>(n_tok), CU_TENSOR_MAP_SWIZZLE_128B))
+    return QERL_ERR_CUDA;
 
   // ---- prep: noise + fp16 staging (+ LoRA down-projection)
   PrepParams pp{};
@@ -530,7 +738,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     pp.lora_rows = std::min(kLoraMaxRows, kPrepThreads * kLoraOutPerThread / r);
     pp.lora_row_tiles = (M + pp.lora_rows - 1) / pp.lora_rows;
     const int k64 = K / 64;
-    const int target = 2 * dev.sms;
+    const int target = 2 * sms;
     int per = (k64 * pp.lora_row_tiles + target - 1) / target;
     per = std::max(per, 1);
     pp.k64_per_chunk = per;
@@ -539,58 +747,9 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   }
   size_t prep_smem = static_cast<size_t>(K) * 2;
   if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>(pp.lora_rows * 64 + 64 * r) * 4);
-  if (prep_smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(prep_smem)) != cudaSuccess)
-      return QERL_ERR_CUDA;
-  }
+  if (prep_smem > static_cast<size_t>(kPrepSmemLimit)) return QERL_ERR_UNSUPPORTED_SHAPE;
   prep_kernel<<<M + lora_blocks, kPrepThreads, prep_smem, s>>>(pp);
   if (cudaGetLastError() != cudaSuccess) return QERL_ERR_CUDA;
-
-  // ---- tile shape
-  int n_tok, m_tiles;
-  if (M <= 256) {
-    n_tok = (M + 15) / 16 * 16;
-    m_tiles = 1;
-  } else {
-    n_tok = 256;
-    m_tiles = (M + 255) / 256;
-  }
-  const int n_tiles = (N + kTileN - 1) / kTileN;
-  const int ks_total = K / kStageK;
-  int split = 1;
-  if (n_tok <= 128) {
-    // K split across a cluster when the tiles alone leave SMs idle: minimise
-    // waves x stages per CTA, with a small per-CTA fixed cost.
-    double best = 1e30;
-    for (int sp = 1; sp <= 8 && sp <= ks_total; ++sp) {
-      const int ctas = n_tiles * m_tiles * sp;
-      const int waves = (ctas + dev.sms - 1) / dev.sms;
-      const double cost = waves * (static_cast<double>((ks_total + sp - 1) / sp) + 3.0);
-      if (cost < best - 1e-9) {
-        best = cost;
-        split = sp;
-      }
-    }
-  }
-  const uint32_t epi = epilogue_bytes(n_tok, r, split);
-  int stages = kMaxStages;
-  while (stages > 2 && std::max(smem_layout(n_tok, stages).ring_bytes, epi) + 256 + 1024 > kSmemLimit) --stages;
-  const SmemLayout SL = smem_layout(n_tok, stages);
-  const uint32_t bars_off = static_cast<uint32_t>(align_up(std::max(SL.ring_bytes, epi), 16));
-  const uint32_t smem_bytes = bars_off + 256 + 1024;  // + barrier block + 1024-byte alignment slack
-  if (smem_bytes > kSmemLimit) return QERL_ERR_UNSUPPORTED_SHAPE;
-  int tmem_cols = 32;
-  while (tmem_cols < n_tok) tmem_cols *= 2;
-
-  CUtensorMap tm_codes, tm_xs;
-  if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, static_cast<uint64_t>(K) / 2,
-                   static_cast<uint64_t>(N), static_cast<uint64_t>(K) / 2, kStageK / 2, kTileN,
-                   CU_TENSOR_MAP_SWIZZLE_32B))
-    return QERL_ERR_CUDA;
-  if (!make_map_2d(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xs, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
-                   static_cast<uint64_t>(K) * 2, kStageK, static_cast<uint32_t>(n_tok), CU_TENSOR_MAP_SWIZZLE_128B))
-    return QERL_ERR_CUDA;
 
   MmaParams mp{};
   mp.scales = a.scales;
@@ -606,31 +765,35 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.r = r;
   mp.n_tok = n_tok;
   mp.split = split;
-  mp.stages = stages;
+  mp.raw_stages = raw_stages;
+  mp.ab_stages = ab_stages;
   mp.tmem_cols = tmem_cols;
-  mp.bars_off = bars_off;
+  mp.off_codes = P.codes;
+  mp.off_a = P.a;
+  mp.off_b = P.b;
+  mp.off_scales = P.scales;
+  mp.off_lora = P.lora;
+  mp.off_sm = P.sm;
+  mp.off_bars = P.bars;
+  mp.lora_early = lora_early;
   mp.lora_scale = lora ? a.alpha / static_cast<float>(r) : 0.0f;
   mp.y_f32 = a.y_f32 ? 1 : 0;
-
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-  });
-  if (attr_err != cudaSuccess) return QERL_ERR_CUDA;
+  const uint32_t smem_bytes = P.total;
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(split), static_cast<unsigned>(n_tiles), static_cast<unsigned>(m_tiles));
   cfg.blockDim = dim3(kMmaThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = static_cast<unsigned>(split);
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, mma_kernel, tm_codes, tm_xs, mp) != cudaSuccess) return QERL_ERR_CUDA;
   return QERL_OK;
 }

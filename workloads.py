@@ -118,3 +118,29 @@ def noise_vector(k: int, sigma: float, seed: int, *path: int) -> np.ndarray:
     """A channel-wise noise vector z [k] fp32 = sigma * N(0, 1), drawn on the host.
     (Used as a plain input of the linear; the library's own sampler is separate.)"""
     return (rng(seed, *path, 6).standard_normal(k) * sigma).astype(np.float32)
+
+
+# ---- device-side draws for the large benchmark workloads ---------------------
+
+
+def torch_generator(seed: int, *path: int, device="cuda") -> torch.Generator:
+    """A torch generator on `device` seeded from (seed, *path) via SeedSequence."""
+    s = int(np.random.SeedSequence([int(seed), *[int(p) for p in path]]).generate_state(1, dtype=np.uint64)[0])
+    g = torch.Generator(device=device)
+    g.manual_seed(s & ((1 << 63) - 1))
+    return g
+
+
+def weight_f32_device(n: int, k: int, seed: int, *path: int, std: float = 0.02, outlier_frac: float = 0.005,
+                      outlier_scale: float = 10.0, device="cuda") -> torch.Tensor:
+    """Device fp32 W [n, k] ~ N(0, std^2) with round(outlier_frac * k) input channels x outlier_scale."""
+    g = torch_generator(seed, *path, 1, device=device)
+    W = torch.randn((n, k), generator=g, device=device, dtype=torch.float32) * std
+    cols = torch.from_numpy(outlier_channels(k, seed, *path, frac=outlier_frac)).to(device)
+    W[:, cols] *= outlier_scale
+    return W
+
+
+def normal_bf16_device(shape, std: float, seed: int, *path: int, device="cuda") -> torch.Tensor:
+    g = torch_generator(seed, *path, 3, device=device)
+    return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
