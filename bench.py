@@ -142,8 +142,8 @@ class QLinear:
         self.lin = lin
         self.codes, self.scales, self.S = q.quantize(W)
         del W
-        self.A = wl.normal_bf16_device((lin.k, r), 1.0 / math.sqrt(lin.k), seed, *path, 2)
-        self.B = wl.normal_bf16_device((r, lin.n), 0.01, seed, *path, 3)
+        self.A = wl.normal_bf16_device((r, lin.k), 1.0 / math.sqrt(lin.k), seed, *path, 2)
+        self.B = wl.normal_bf16_device((lin.n, r), 0.01, seed, *path, 3)
 
     @property
     def weight_bytes(self):
@@ -482,8 +482,8 @@ def _oracle_layer_sample(cols_per_linear=None, shapes=None, seed=0):
         n = lin.n if cols_per_linear is None else min(lin.n, cols_per_linear)
         W = wl.weight_f32(n, lin.k, seed, 100, li)
         codes, scales, S = oracle.quantize(W)
-        A = wl.lora_A_bits(lin.k, RANK_R, seed, 100, li)
-        B = wl.lora_B_bits(RANK_R, n, seed, 100, li)
+        A = wl.lora_A_bits(RANK_R, lin.k, seed, 100, li)
+        B = wl.lora_B_bits(n, RANK_R, seed, 100, li)
         out.append((lin, n, codes, scales, S, A, B))
     return out
 

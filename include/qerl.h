@@ -5,15 +5,17 @@
  * The operation (QeRL, "QeRL: Beyond Efficiency -- Quantization-enhanced
  * Reinforcement Learning for LLMs", paper-graph-ui digest, section 3.4):
  *
- *   y = x~ . dequant(Wq)^T + (alpha / r) . (x~ . A) . B,   x~ = bf16(x (.) (1 + z))
+ *   y = x~ . dequant(Wq)^T + (alpha / r) . (x~ . A^T) . B^T,   x~ = bf16(x (.) (1 + z))
  *
  *   dequant: "NVFP4 Quantization", Eq. 6: W_hat = S_FP32 * (S_E4M3 (.) W~),
  *            E2M1 codes, one E4M3 scale per 16 contiguous elements along K,
  *            one FP32 tensor scale.
- *   LoRA:    "Low-Rank Adaptation (LoRA) Within Quantized Layers", Eq. 2
- *            forward y = x W_hat + x B A; both branches see the same noisy
- *            activations.  The library names the adapters in x.A.B order:
- *            A is K x r, B is r x N.
+ *   LoRA:    "Low-Rank Adaptation (LoRA) Within Quantized Layers", Eq. 2:
+ *            W + BA with B in R^{d x r} and A in R^{r x k} (d = N output,
+ *            k = K input features), so the forward of an input row x is
+ *            x W^T + x A^T B^T; both branches see the same noisy activations.
+ *            A is r x K and B is N x r, row-major (the layout of a PEFT
+ *            lora_A / lora_B weight).
  *   noise:   "Adaptive Quantization Noise (AQN)", Eq. 7 (one Gaussian value
  *            per input channel), Eq. 8 (exponential decay of sigma), and
  *            "Noise Merging", Eq. 10-12 (the noise merged into the RMSNorm
@@ -140,7 +142,7 @@ QERL_API qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t 
  *
  *   x~[m][k] = bf16_RN( float(x[m][k]) * (1.0f + z[k]) )       (z == NULL: x~ = x)
  *   y[m][n]  = out_RN( S * sum_k x~[m][k] * dec(scales[n][k/16]) * e2m1(codes[n][k])
- *                     + (alpha / r) * sum_j (sum_k x~[m][k] * A[k][j]) * B[j][n] )
+ *                     + (alpha / r) * sum_j (sum_k x~[m][k] * A[j][k]) * B[n][j] )
  *
  * x       device bf16, m x k, row stride ldx elements (ldx >= k, ldx % 8 == 0,
  *         16-byte aligned).
@@ -148,8 +150,9 @@ QERL_API qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t 
  *         n x k weight (n = output features, k = input features).  codes
  *         16-byte aligned, scales 4-byte aligned.
  * z       device float[k] or NULL (no noise).
- * A       device bf16 k x r, B device bf16 r x n, or both NULL / r == 0 (no
- *         LoRA branch).  0 <= r <= 128.
+ * A       device bf16 r x k, B device bf16 n x r (row-major), or both NULL /
+ *         r == 0 (no LoRA branch).  r % 8 == 0 and r <= 128; A and B
+ *         16-byte aligned.
  * y       device, m x n (row stride n), y_dtype QERL_BF16 (round to nearest
  *         even) or QERL_F32.
  * workspace device, >= qerl_lora_linear_workspace_size(m, n, k, r) bytes,

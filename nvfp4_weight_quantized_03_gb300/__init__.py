@@ -180,9 +180,10 @@ def qerl_lora_linear_workspace_size(m: int, n: int, k: int, r: int) -> int:
 
 
 def qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, workspace, stream=None) -> int:
+    """A: [r, k] bf16 (LoRA down-projection), B: [n, r] bf16 (LoRA up-projection)."""
     m, k = x.shape
     n = codes.shape[0]
-    r = 0 if A is None else A.shape[1]
+    r = 0 if A is None else A.shape[0]
     ydt = QERL_F32 if y.dtype == torch.float32 else QERL_BF16
     return lib().qerl_lora_linear(_p(x), m, k, x.stride(0), _p(codes), _p(scales), _p(tensor_scale), n, _p(z),
                                   _p(A), _p(B), r, float(alpha), _p(y), ydt, _p(workspace), _nbytes(workspace),
@@ -213,10 +214,11 @@ def quantize(W: torch.Tensor, ws: torch.Tensor = None):
 
 def lora_linear(x, codes, scales, tensor_scale, z=None, A=None, B=None, alpha=0.0, out_dtype=torch.bfloat16,
                 ws=None):
-    """y = bf16(x(1+z)) . dequant(W)^T + (alpha/r) (x~ A) B for bf16 x [m, k]."""
+    """y = x~ . dequant(W)^T + (alpha/r) (x~ A^T) B^T, x~ = bf16(x(1+z)), for bf16 x [m, k],
+    A [r, k], B [n, r]."""
     m, k = x.shape
     n = codes.shape[0]
-    r = 0 if A is None else A.shape[1]
+    r = 0 if A is None else A.shape[0]
     y = torch.empty((m, n), dtype=out_dtype, device=x.device)
     ws = workspace(qerl_lora_linear_workspace_size(m, n, k, r), x.device) if ws is None else ws
     check(qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, ws), "qerl_lora_linear")

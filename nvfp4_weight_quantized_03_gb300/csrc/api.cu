@@ -123,7 +123,7 @@ qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, c
   if (r > 0 && A == nullptr) r = 0;
   if (A != nullptr && r == 0) return QERL_ERR_INVALID_ARGUMENT;
   if (k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
-  if (r > 128 || k > 65536) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (r > 128 || r % 8 != 0 || k > 65536) return QERL_ERR_UNSUPPORTED_SHAPE;
   if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX || m * k > (int64_t{1} << 40))
     return QERL_ERR_UNSUPPORTED_SHAPE;
   if (m == 0 || n == 0) return QERL_OK;
@@ -132,7 +132,7 @@ qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, c
   if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(codes, 16) || !aligned(scales, 4)) return QERL_ERR_MISALIGNED;
   if (z != nullptr && !aligned(z, 16)) return QERL_ERR_MISALIGNED;
   if (y_dtype == QERL_F32 ? !aligned(y, 4) : !aligned(y, 2)) return QERL_ERR_MISALIGNED;
-  if (A != nullptr && (!aligned(A, 2) || !aligned(B, 2))) return QERL_ERR_MISALIGNED;
+  if (A != nullptr && (!aligned(A, 16) || !aligned(B, 16))) return QERL_ERR_MISALIGNED;
   qerl_status st = check_ws(workspace, ws_bytes, qerl::linear_workspace_bytes(m, k, r));
   if (st != QERL_OK) return st;
   qerl::LinearArgs a{};

@@ -52,23 +52,25 @@ namespace {
 // ------------------------------------------------------------------ prep
 
 constexpr int kPrepThreads = 256;
-constexpr int kLoraMaxRows = 64;  // token rows per LoRA task (fewer for large r)
-constexpr int kLoraOutPerThread = 8;
+constexpr int kLoraTileM = 64;   // token rows per LoRA task
+constexpr int kLoraTileR = 32;   // ranks per LoRA task
+constexpr int kLoraKc = 64;      // K per shared-memory chunk
+constexpr int kLoraPad = 68;     // padded row length (floats): conflict-free float4 reads
 
 struct PrepParams {
   const __nv_bfloat16* x;
   const float* z;
-  const __nv_bfloat16* A;
+  const __nv_bfloat16* A;  // [r][K]
   __half* xs;   // [M][K] staged x~ * 2^e_m
   float* rinv;  // [M] 2^-e_m
-  float* t;     // [M][r]
+  float* t;     // [M][r] (zero-initialised; tasks add their K-slice)
   int64_t ldx;
   int M, K, r;
-  int row_tasks;       // = M
-  int lora_rows;       // token rows per LoRA task: rows * r <= 256 * kLoraOutPerThread
-  int lora_row_tiles;  // ceil(M / lora_rows)
-  int lora_k_chunks;   // number of K slices
-  int k64_per_chunk;   // 64-wide K blocks per slice
+  int row_tasks;        // = M
+  int lora_m_tiles;     // ceil(M / kLoraTileM)
+  int lora_r_tiles;     // ceil(r / kLoraTileR)
+  int lora_k_slices;    // number of K slices
+  int kc_per_slice;     // 64-wide K chunks per slice
 };
 
 __device__ __forceinline__ float noisy(float xv, float zv) {
@@ -132,54 +134,100 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     }
     return;
   }
-  // ---- LoRA task: t[rows][:] += x~[rows][kslice] . A[kslice][:]
+  // ---- LoRA task: t[rows][ranks] += sum over a K slice of x~[row][k] * A[rank][k].
+  // 64 rows x 32 ranks per task; thread (tx, ty) owns rows {2ty, 2ty+1} and
+  // ranks {tx, tx+8, tx+16, tx+24}: 8 fp32 accumulators, float4 smem reads.
   const int task = blockIdx.x - p.row_tasks;
-  const int rt = task % p.lora_row_tiles;
-  const int kc = task / p.lora_row_tiles;
-  const int row0 = rt * p.lora_rows;
-  const int rows = min(p.lora_rows, p.M - row0);
-  const int r = p.r;
-  float* xsm = reinterpret_cast<float*>(sm);  // [lora_rows][64]
-  float* asm_ = xsm + p.lora_rows * 64;       // [64][r]
-  const int nout = rows * r;
-  float acc[kLoraOutPerThread];
+  const int mt = task % p.lora_m_tiles;
+  const int rt = (task / p.lora_m_tiles) % p.lora_r_tiles;
+  const int ks = task / (p.lora_m_tiles * p.lora_r_tiles);
+  const int row0 = mt * kLoraTileM, rank0 = rt * kLoraTileR;
+  float* xsm = reinterpret_cast<float*>(sm);     // [kLoraTileM][kLoraPad]
+  float* asm_ = xsm + kLoraTileM * kLoraPad;     // [kLoraTileR][kLoraPad]
+  const int tx = tid & 7, ty = tid >> 3;
+  float acc[2][4];
 #pragma unroll
-  for (int i = 0; i < kLoraOutPerThread; ++i) acc[i] = 0.0f;
-  const int kb_begin = kc * p.k64_per_chunk;
-  const int kb_end = min(p.K / 64, kb_begin + p.k64_per_chunk);
-  for (int kb = kb_begin; kb < kb_end; ++kb) {
-    __syncthreads();
-    const int k0 = kb * 64;
-    for (int i = tid; i < rows * 64; i += kPrepThreads) {
-      const int rr = i / 64, kk = i % 64;
-      const float xv = __bfloat162float(p.x[static_cast<int64_t>(row0 + rr) * p.ldx + k0 + kk]);
-      xsm[rr * 64 + kk] = p.z != nullptr ? noisy(xv, __ldg(p.z + k0 + kk)) : xv;
-    }
-    for (int i = tid; i < 64 * r; i += kPrepThreads)
-      asm_[i] = __bfloat162float(p.A[static_cast<int64_t>(k0) * r + i]);
-    __syncthreads();
+  for (int i = 0; i < 2; ++i)
 #pragma unroll
-    for (int q = 0; q < kLoraOutPerThread; ++q) {
-      const int o = tid + q * kPrepThreads;
-      if (o < nout) {
-        const int rr = o / r, j = o % r;
-        float s = acc[q];
-#pragma unroll 8
-        for (int kk = 0; kk < 64; ++kk) s = fmaf(xsm[rr * 64 + kk], asm_[kk * r + j], s);
-        acc[q] = s;
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  const int kc_begin = ks * p.kc_per_slice;
+  const int kc_end = min(p.K / kLoraKc, kc_begin + p.kc_per_slice);
+  for (int kc = kc_begin; kc < kc_end; ++kc) {
+    const int k0 = kc * kLoraKc;
+    __syncthreads();
+    // x~ tile: 64 rows x 64 k, 8 bf16 per vector -> 512 vectors
+    for (int v = tid; v < kLoraTileM * kLoraKc / 8; v += kPrepThreads) {
+      const int rr = v >> 3, kk = (v & 7) * 8;
+      float f[8];
+      if (row0 + rr < p.M) {
+        uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(row0 + rr) * p.ldx + k0 + kk));
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
+        if (p.z != nullptr) {
+          const float4 z0 = __ldg(reinterpret_cast<const float4*>(p.z + k0 + kk));
+          const float4 z1 = __ldg(reinterpret_cast<const float4*>(p.z + k0 + kk) + 1);
+          const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = noisy(f[j], zz[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = 0.0f;
       }
+      float4* d = reinterpret_cast<float4*>(xsm + rr * kLoraPad + kk);
+      d[0] = make_float4(f[0], f[1], f[2], f[3]);
+      d[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    // A tile: 32 ranks x 64 k -> 256 vectors
+    for (int v = tid; v < kLoraTileR * kLoraKc / 8; v += kPrepThreads) {
+      const int jj = v >> 3, kk = (v & 7) * 8;
+      float f[8];
+      if (rank0 + jj < p.r) {
+        uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(rank0 + jj) * p.K + k0 + kk));
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = 0.0f;
+      }
+      float4* d = reinterpret_cast<float4*>(asm_ + jj * kLoraPad + kk);
+      d[0] = make_float4(f[0], f[1], f[2], f[3]);
+      d[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < kLoraKc; kk += 4) {
+      float4 xv[2], av[4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) xv[i] = *reinterpret_cast<const float4*>(xsm + (2 * ty + i) * kLoraPad + kk);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) av[j] = *reinterpret_cast<const float4*>(asm_ + (tx + 8 * j) * kLoraPad + kk);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = fmaf(xv[i].x, av[j].x, acc[i][j]);
+          acc[i][j] = fmaf(xv[i].y, av[j].y, acc[i][j]);
+          acc[i][j] = fmaf(xv[i].z, av[j].z, acc[i][j]);
+          acc[i][j] = fmaf(xv[i].w, av[j].w, acc[i][j]);
+        }
     }
   }
 #pragma unroll
-  for (int q = 0; q < kLoraOutPerThread; ++q) {
-    const int o = tid + q * kPrepThreads;
-    if (o < nout) atomicAdd(p.t + static_cast<int64_t>(row0 + o / r) * r + (o % r), acc[q]);
-  }
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int row = row0 + 2 * ty + i, rank = rank0 + tx + 8 * j;
+      if (row < p.M && rank < p.r) atomicAdd(p.t + static_cast<int64_t>(row) * p.r + rank, acc[i][j]);
+    }
 }
 
 // ------------------------------------------------------------------ MMA kernel
 
-constexpr int kMmaThreads = 352;  // warps 0-7 dequant + epilogue, 8 weight producer, 9 MMA, 10 activation producer
+constexpr int kMmaThreads = 384;  // warps 0-7 dequant + epilogue, 8 weight producer, 9 MMA, 10 activation producer,
+                                  // 11 LoRA operands
 constexpr int kTileN = 128;       // output features per CTA (MMA M)
 constexpr int kStageK = 64;       // K per MMA stage (4 x K=16 instructions)
 constexpr int kRawK = 256;        // K per weight-load stage: 128 contiguous bytes of codes per row
@@ -231,33 +279,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
-// LoRA up-projection operands in the 128-byte-swizzled K-major layout (the
-// rank index j is the MMA's K), built by warps 0-7 (tid 0..255) at `base`:
-//   B^T chunk c:  128 rows n  x 64 j   bf16  = B[c*64 + j][n0 + n]           (exact copy)
+// LoRA up-projection operands, in the 128-byte-swizzled K-major layout (the
+// rank index j is the MMA's K):
+//   B^T chunk c:  128 rows n  x 64 j   bf16  = B[n0 + n][c*64 + j]   (TMA from B [N][r])
 //   t_hi chunk c: n_tok rows m x 64 j  bf16  = bf16(t[m0 + m][c*64 + j])
 //   t_lo chunk c: n_tok rows m x 64 j  bf16  = bf16(t - t_hi)
-// so that B^T . t_hi + B^T . t_lo carries t to ~16 significant bits.  Zero
-// past M, N and r.
-__device__ void build_lora_tiles(const MmaParams& p, uint32_t base, int m0, int n0, int tid) {
+// so B^T . t_hi + B^T . t_lo carries t to ~16 significant bits.  The t tiles
+// are built by `nthr` threads (tid < nthr); zero past M and r.
+__device__ void build_t_tiles(const MmaParams& p, uint32_t base, int m0, int tid, int nthr) {
   const int rc = lora_chunks(p.r);
-  for (int idx = tid; idx < rc * kTileN * 8; idx += 256) {
-    const int c = idx / (kTileN * 8), rem = idx - c * (kTileN * 8);
-    const int g = rem / kTileN, n = rem - g * kTileN;
-    const bool nin = n0 + n < p.N;
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j0 = c * kLoraChunkK + g * 8 + 2 * e;
-      const uint32_t lo = (nin && j0 < p.r) ? __bfloat16_as_ushort(p.B[static_cast<int64_t>(j0) * p.N + n0 + n]) : 0u;
-      const uint32_t hi =
-          (nin && j0 + 1 < p.r) ? __bfloat16_as_ushort(p.B[static_cast<int64_t>(j0 + 1) * p.N + n0 + n]) : 0u;
-      w[e] = lo | (hi << 16);
-    }
-    sts128(base + c * kBtChunkBytes + n * 128 + ((g ^ (n & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
-  }
   const uint32_t thi = base + rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
-  for (int idx = tid; idx < rc * p.n_tok * 8; idx += 256) {
+  for (int idx = tid; idx < rc * p.n_tok * 8; idx += nthr) {
     const int c = idx / (p.n_tok * 8), rem = idx - c * (p.n_tok * 8);
     const int ml = rem >> 3, g = rem & 7;
     const int m = m0 + ml;
@@ -281,6 +314,26 @@ __device__ void build_lora_tiles(const MmaParams& p, uint32_t base, int m0, int 
   }
 }
 
+// TMA of the B^T chunks (rows n0..n0+127 of B [N][r], 64 ranks per chunk,
+// zero-filled past N and r) into `base`, completing on `bar`.
+__device__ __forceinline__ void load_bt_tiles(const MmaParams& p, const CUtensorMap* tm_bl, uint32_t base, int n0,
+                                              uint32_t bar) {
+  const int rc = lora_chunks(p.r);
+  mbar_arrive_expect_tx_a(bar, static_cast<uint32_t>(rc) * kBtChunkBytes);
+  for (int c = 0; c < rc; ++c) tma_load_2d(base + c * kBtChunkBytes, tm_bl, c * kLoraChunkK, n0, bar);
+}
+
+// Warp-cooperative bounded wait: lane 0 polls, the warp converges, then every
+// lane confirms the (already completed) phase for its own acquire.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait_a(bar, parity, abort_flag, status);
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (ok) (void)mbar_try_wait_a(bar, parity);
+  return ok != 0;
+}
+
 // D2 (+)= B^T . t_hi^T + B^T . t_lo^T over the rank dimension (bf16 x bf16 -> fp32).
 __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, uint32_t base, uint32_t d2) {
   const int rc = lora_chunks(p.r);
@@ -299,7 +352,7 @@ __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, uint32_t bas
 
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_xs,
-               const MmaParams p) {
+               const __grid_constant__ CUtensorMap tm_bl, const MmaParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -340,7 +393,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       mbar_init_a(ab_empty(s), 1);  // tcgen05.commit
     }
     mbar_init_a(ring_free, 1);
-    mbar_init_a(lora_full, 8);
+    // B^T TMA (expect_tx) + the t-tile builders: warp 11 (early) or warps 0-7 (late)
+    mbar_init_a(lora_full, p.lora_early ? 2 : 9);
     mbar_init_a(acc_full, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -352,6 +406,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_codes);
     tma_prefetch_desc(&tm_xs);
+    if (p.r > 0) tma_prefetch_desc(&tm_bl);
   }
   tc_fence_before();
   __syncthreads();
@@ -441,19 +496,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
       tc_commit(acc_full);  // always, so the epilogue's wait completes even after an abort
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ warps 0-7: dequant
     griddep_wait();  // row scales (and t) come from the preceding kernel
     {
       const float S = *p.tensor_scale;
       for (int i = threadIdx.x; i < p.n_tok; i += 256)
         stsf(smv + 4u * i, (m0 + i < p.M) ? S * __ldg(p.rinv + m0 + i) : 0.0f);
-    }
-    if (do_lora && p.lora_early) {
-      build_lora_tiles(p, lora_base, m0, n0, threadIdx.x);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_a(lora_full);
     }
     const int row = 16 * warp + (lane & 15);
     const int half = lane >> 4;
@@ -462,14 +511,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     for (int i = 0; i < nraw; ++i) {
       const int s = i % RS;
       const uint32_t ph = (i / RS) & 1;
-      if (!mbar_wait_a(raw_full(s), ph, abort_flag, p.status)) break;
+      if (!warp_wait(raw_full(s), ph, abort_flag, p.status, lane)) break;
       const uint32_t crow = sbase + p.off_codes + s * kCodesRawBytes + row * 128;
       const uint32_t srow = sbase + p.off_scales + s * kScalesRawBytes + row * 16 + half * 2;
       bool ok = true;
       for (int q = 0; q < kSub && j < nmma; ++q, ++j) {
         const int as = j % AS;
         const uint32_t aph = (j / AS) & 1;
-        if (!mbar_wait_a(ab_empty(as), aph ^ 1, abort_flag, p.status)) {
+        if (!warp_wait(ab_empty(as), aph ^ 1, abort_flag, p.status, lane)) {
           ok = false;
           break;
         }
@@ -499,17 +548,33 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (lane == 0) mbar_arrive_a(raw_empty(s));
     }
     if (do_lora && !p.lora_early) {
-      if (mbar_wait_a(ring_free, 0, abort_flag, p.status)) build_lora_tiles(p, lora_base, m0, n0, threadIdx.x);
+      if (warp_wait(ring_free, 0, abort_flag, p.status, lane)) build_t_tiles(p, lora_base, m0, threadIdx.x, 256);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive_a(lora_full);
+    }
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ LoRA operands
+    if (do_lora) {
+      if (p.lora_early) {
+        if (lane == 0) load_bt_tiles(p, &tm_bl, lora_base, n0, lora_full);
+        griddep_wait();  // t comes from the preceding kernel
+        build_t_tiles(p, lora_base, m0, lane, 32);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_a(lora_full);
+      } else if (warp_wait(ring_free, 0, abort_flag, p.status, lane)) {
+        if (lane == 0) load_bt_tiles(p, &tm_bl, lora_base, n0, lora_full);
+      } else if (lane == 0) {
+        mbar_arrive_a(lora_full);  // after an abort: keep the barrier count consistent
+      }
     }
   }
 
   // ---------------------------------------------------------------- epilogue
   const uint32_t part = sbase;  // [n_tok][128] fp32 scaled partial tile (split > 1), ring reused
   if (warp < 8) {
-    const bool ok = mbar_wait_a(acc_full, 0, abort_flag, p.status);
+    const bool ok = warp_wait(acc_full, 0, abort_flag, p.status, lane);
     tc_fence_after();
     const int q = warp & 3;
     const int nl = q * 32 + lane;
@@ -719,6 +784,15 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
                    static_cast<uint64_t>(K) * 2, kStageK, static_cast<uint32_t>(n_tok), CU_TENSOR_MAP_SWIZZLE_128B))
     return QERL_ERR_CUDA;
 
+  CUtensorMap tm_bl;
+  if (lora) {
+    if (!make_map_2d(&tm_bl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, static_cast<uint64_t>(r), static_cast<uint64_t>(N),
+                     static_cast<uint64_t>(r) * 2, kLoraChunkK, kTileN, CU_TENSOR_MAP_SWIZZLE_128B))
+      return QERL_ERR_CUDA;
+  } else {
+    std::memset(&tm_bl, 0, sizeof(tm_bl));
+  }
+
   // ---- prep: noise + fp16 staging (+ LoRA down-projection)
   PrepParams pp{};
   pp.x = static_cast<const __nv_bfloat16*>(a.x);
@@ -735,18 +809,19 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   int lora_blocks = 0;
   if (lora) {
     if (cudaMemsetAsync(t, 0, static_cast<size_t>(M) * r * 4, s) != cudaSuccess) return QERL_ERR_CUDA;
-    pp.lora_rows = std::min(kLoraMaxRows, kPrepThreads * kLoraOutPerThread / r);
-    pp.lora_row_tiles = (M + pp.lora_rows - 1) / pp.lora_rows;
-    const int k64 = K / 64;
-    const int target = 2 * sms;
-    int per = (k64 * pp.lora_row_tiles + target - 1) / target;
+    pp.lora_m_tiles = (M + kLoraTileM - 1) / kLoraTileM;
+    pp.lora_r_tiles = (r + kLoraTileR - 1) / kLoraTileR;
+    const int kc_total = K / kLoraKc;
+    const int tiles = pp.lora_m_tiles * pp.lora_r_tiles;
+    // Enough K slices for about two tasks per SM.
+    int per = (kc_total * tiles + 2 * sms - 1) / (2 * sms);
     per = std::max(per, 1);
-    pp.k64_per_chunk = per;
-    pp.lora_k_chunks = (k64 + per - 1) / per;
-    lora_blocks = pp.lora_row_tiles * pp.lora_k_chunks;
+    pp.kc_per_slice = per;
+    pp.lora_k_slices = (kc_total + per - 1) / per;
+    lora_blocks = tiles * pp.lora_k_slices;
   }
   size_t prep_smem = static_cast<size_t>(K) * 2;
-  if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>(pp.lora_rows * 64 + 64 * r) * 4);
+  if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>((kLoraTileM + kLoraTileR) * kLoraPad) * 4);
   if (prep_smem > static_cast<size_t>(kPrepSmemLimit)) return QERL_ERR_UNSUPPORTED_SHAPE;
   prep_kernel<<<M + lora_blocks, kPrepThreads, prep_smem, s>>>(pp);
   if (cudaGetLastError() != cudaSuccess) return QERL_ERR_CUDA;
@@ -794,7 +869,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, mma_kernel, tm_codes, tm_xs, mp) != cudaSuccess) return QERL_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, mma_kernel, tm_codes, tm_xs, tm_bl, mp) != cudaSuccess) return QERL_ERR_CUDA;
   return QERL_OK;
 }
 

@@ -37,8 +37,8 @@ def main():
         sets.append(q.quantize(W))
         del W
     x = torch.randn(a.m, a.k, device=dev).to(torch.bfloat16)
-    A = (torch.randn(a.k, a.r, device=dev) / a.k ** 0.5).to(torch.bfloat16) if a.r else None
-    B = (torch.randn(a.r, a.n, device=dev) * 0.01).to(torch.bfloat16) if a.r else None
+    A = (torch.randn(a.r, a.k, device=dev) / a.k ** 0.5).to(torch.bfloat16) if a.r else None
+    B = (torch.randn(a.n, a.r, device=dev) * 0.01).to(torch.bfloat16) if a.r else None
     z = torch.empty(a.k, dtype=torch.float32, device=dev)
     q.check(q.qerl_aqn_sample(z, a.sigma, 0))
     y = torch.empty(a.m, a.n, dtype=torch.bfloat16, device=dev)

@@ -203,7 +203,8 @@ def lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alph
     """fp64 y[m, len(cols)] of the NVFP4 + LoRA + AQN linear.
 
     x_bits: [m, k] uint16 bf16; codes [n, k/2]; scales [n, k/16]; S tensor scale;
-    z: [k] float32 or None; A_bits [k, r] uint16 bf16; B_bits [r, n] uint16 bf16.
+    z: [k] float32 or None; A_bits [r, k] uint16 bf16; B_bits [n, r] uint16 bf16
+    (the shapes of Eq. 2: A in R^{r x k}, B in R^{d x r}).
     """
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
@@ -215,8 +216,8 @@ def lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alph
     if A_bits is not None and B_bits is not None:
         A_bits = np.ascontiguousarray(A_bits, dtype=np.uint16)
         B_bits = np.ascontiguousarray(B_bits, dtype=np.uint16)
-        r = A_bits.shape[1]
-        assert A_bits.shape == (k, r) and B_bits.shape == (r, n)
+        r = A_bits.shape[0]
+        assert A_bits.shape == (r, k) and B_bits.shape == (n, r)
     else:
         A_bits = B_bits = None
     zz = None if z is None else np.ascontiguousarray(z, dtype=np.float32)

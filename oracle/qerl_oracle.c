@@ -350,10 +350,11 @@ void orc_noise_apply(const uint16_t* x, int64_t m, int64_t k, int64_t ldx, const
 /* ------------------------------------------------------------------------ */
 /* The linear layer, fp64 accumulation:                                      */
 /*   y[m][c] = sum_k xt[m][k] * W_hat[c][k]                                  */
-/*           + (alpha / r) * sum_j (sum_k xt[m][k] * A[k][j]) * B[j][c]      */
-/* ([QeRL] Eq. 2 forward, y = x W_hat + x B A, written in the x.A.B order    */
-/* of the library: A is k x r, B is r x n).  Both branches see the same      */
-/* noisy activation ([QeRL] "LoRA", interaction with AQN).                   */
+/*           + (alpha / r) * sum_j (sum_k xt[m][k] * A[j][k]) * B[c][j]      */
+/* ([QeRL] Eq. 2: W + BA with B in R^{d x r}, A in R^{r x k}; for an input   */
+/* row x the forward is x W^T + x A^T B^T.  A is r x k, B is n x r.)  Both   */
+/* branches see the same noisy activation ([QeRL] "LoRA", interaction with   */
+/* AQN).                                                                     */
 /* round_xt = 1: xt is the bf16 noisy activation (the reading above);        */
 /* round_xt = 0: xt = x * (1 + z) exactly in fp64 (used to check Eq. 12).    */
 /* Output columns are the ncols indices in cols[] (all n if cols == NULL).   */
@@ -388,7 +389,7 @@ int orc_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
         for (int64_t i = 0; i < m; ++i)
             for (int j = 0; j < r; ++j) {
                 double acc = 0.0;
-                for (int64_t kk = 0; kk < k; ++kk) acc += xt[i * k + kk] * (double)bf16_bits_to_f32(A[kk * r + j]);
+                for (int64_t kk = 0; kk < k; ++kk) acc += xt[i * k + kk] * (double)bf16_bits_to_f32(A[(int64_t)j * k + kk]);
                 t[i * r + j] = acc;
             }
 
@@ -406,7 +407,7 @@ int orc_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
             for (int64_t kk = 0; kk < k; ++kk) acc += xt[i * k + kk] * wrow[kk];
             if (use_lora) {
                 double l = 0.0;
-                for (int j = 0; j < r; ++j) l += t[i * r + j] * (double)bf16_bits_to_f32(B[(int64_t)j * n + c]);
+                for (int j = 0; j < r; ++j) l += t[i * r + j] * (double)bf16_bits_to_f32(B[c * r + j]);
                 acc += lora_scale * l;
             }
             y[i * ncols + ci] = acc;

@@ -48,8 +48,8 @@ class Case:
     def __init__(self, q, orc, m, n, k, r, sigma, seed=0, x_std=1.0):
         self.m, self.n, self.k, self.r = m, n, k, r
         self.x_bits = wl.activations_bits(m, k, seed, 1, std=x_std)
-        self.A_bits = wl.lora_A_bits(k, r, seed, 2) if r else None
-        self.B_bits = wl.lora_B_bits(r, n, seed, 3) if r else None
+        self.A_bits = wl.lora_A_bits(r, k, seed, 2) if r else None
+        self.B_bits = wl.lora_B_bits(n, r, seed, 3) if r else None
         self.z = wl.noise_vector(k, sigma, seed, 4) if sigma else None
         self.alpha = 2.0 * r
         self.codes, self.scales, self.S, self.oc, self.osc, self.oS = _quantized(q, orc, n, k, seed)

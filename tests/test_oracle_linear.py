@@ -1,7 +1,8 @@
-"""Pins for the oracle's linear layer y = x_tilde W_hat^T + (alpha/r) (x_tilde A) B.
+"""Pins for the oracle's linear layer y = x_tilde W_hat^T + (alpha/r) (x_tilde A^T) B^T.
 
-QeRL digest, section 3.4: "Low-Rank Adaptation" (Eq. 2 forward
-y = x W_hat + x B A, both branches on the same noisy activations), "Noise
+QeRL digest, section 3.4: "Low-Rank Adaptation" (Eq. 2, W + BA
+with A in R^{r x k}, B in R^{d x r}: forward x W^T + x A^T B^T, both branches on
+the same noisy activations), "Noise
 Merging" (Eq. 9-12: the merged noise is a per-input-channel factor (1 + z)),
 "NVFP4 Quantization" (Eq. 6).  Special cases reduce to a plain matmul, the
 LoRA term is checked through linearity in B, Eq. 12's weight-side form is
@@ -22,8 +23,8 @@ LEVELS = [float(v) for _, v in read_golden("e2m1_levels.txt")]
 def _case(m=3, n=40, k=96, r=4, seed=0, sigma=0.05):
     W = wl.weight_f32(n, k, seed, 0)
     x = wl.activations_bits(m, k, seed, 1)
-    A = wl.lora_A_bits(k, r, seed, 2)
-    B = wl.lora_B_bits(r, n, seed, 3, std=0.3)
+    A = wl.lora_A_bits(r, k, seed, 2)
+    B = wl.lora_B_bits(n, r, seed, 3, std=0.3)
     z = wl.noise_vector(k, sigma, seed, 4)
     return W, x, A, B, z
 
@@ -42,11 +43,11 @@ def test_no_noise_no_lora_is_plain_dequant_gemm(orc):
 def test_lora_term_is_linear_in_B(orc):
     W, x, A, B, z = _case()
     codes, scales, S = orc.quantize(W)
-    alpha, r = 8.0, A.shape[1]
+    alpha, r = 8.0, A.shape[0]
     y1 = orc.lora_linear(x, codes, scales, S, z=z, A_bits=A, B_bits=B, alpha=alpha)
     y0 = orc.lora_linear(x, codes, scales, S, z=z, A_bits=A, B_bits=np.zeros_like(B), alpha=alpha)
     xt = wl.bf16_bits_to_f32(orc.noise_apply(x, z)).astype(np.float64)
-    lora = (alpha / r) * ((xt @ wl.bf16_bits_to_f32(A).astype(np.float64)) @ wl.bf16_bits_to_f32(B).astype(np.float64))
+    lora = (alpha / r) * ((xt @ wl.bf16_bits_to_f32(A).astype(np.float64).T) @ wl.bf16_bits_to_f32(B).astype(np.float64).T)
     assert np.allclose(y1 - y0, lora, rtol=1e-10, atol=1e-12)
     assert np.abs(lora).max() > 1e-3  # the term is not trivially zero
 
@@ -105,10 +106,10 @@ def test_tiny_case_exact_rationals(orc):
         return Fraction(float(S)) * Fraction(float(e4[i, j // 16])) * v
 
     for mi in range(m):
-        t = [sum(Fraction(float(xt[mi, kk])) * Fraction(float(Af[kk, j])) for kk in range(k)) for j in range(r)]
+        t = [sum(Fraction(float(xt[mi, kk])) * Fraction(float(Af[j, kk])) for kk in range(k)) for j in range(r)]
         for c in range(n):
             base = sum(Fraction(float(xt[mi, kk])) * wv(c, kk) for kk in range(k))
-            lora = Fraction(alpha) / r * sum(t[j] * Fraction(float(Bf[j, c])) for j in range(r))
+            lora = Fraction(alpha) / r * sum(t[j] * Fraction(float(Bf[c, j])) for j in range(r))
             exact = float(base + lora)
             assert abs(y[mi, c] - exact) <= 1e-13 * max(1.0, abs(exact))
 

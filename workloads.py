@@ -104,14 +104,14 @@ def activations_bits(m: int, k: int, seed: int, *path: int, std: float = 1.0) ->
     return to_bf16_bits(rng(seed, *path, 3).standard_normal((m, k), dtype=np.float32) * np.float32(std))
 
 
-def lora_A_bits(k: int, r: int, seed: int, *path: int) -> np.ndarray:
-    """A [k, r] bf16 bits ~ N(0, 1/k)."""
-    return to_bf16_bits(rng(seed, *path, 4).standard_normal((k, r), dtype=np.float32) * np.float32(1.0 / np.sqrt(k)))
+def lora_A_bits(r: int, k: int, seed: int, *path: int) -> np.ndarray:
+    """A [r, k] bf16 bits ~ N(0, 1/k) (LoRA down-projection, r x in_features)."""
+    return to_bf16_bits(rng(seed, *path, 4).standard_normal((r, k), dtype=np.float32) * np.float32(1.0 / np.sqrt(k)))
 
 
-def lora_B_bits(r: int, n: int, seed: int, *path: int, std: float = 0.01) -> np.ndarray:
-    """B [r, n] bf16 bits ~ N(0, std^2)."""
-    return to_bf16_bits(rng(seed, *path, 5).standard_normal((r, n), dtype=np.float32) * np.float32(std))
+def lora_B_bits(n: int, r: int, seed: int, *path: int, std: float = 0.01) -> np.ndarray:
+    """B [n, r] bf16 bits ~ N(0, std^2) (LoRA up-projection, out_features x r)."""
+    return to_bf16_bits(rng(seed, *path, 5).standard_normal((n, r), dtype=np.float32) * np.float32(std))
 
 
 def noise_vector(k: int, sigma: float, seed: int, *path: int) -> np.ndarray:
