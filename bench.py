@@ -3,9 +3,9 @@
 
 One step = one rollout decode pass of a Qwen2.5-7B-shaped decoder layer's
 seven LoRA linears (q, k, v, o, gate, up, down; r = 32, alpha = 64) at each
-decode batch M in {1, 8, 32, 128}: per M, four AQN noise vectors (groups qkv,
-o, gate_up, down; sigma from the exponential-decay schedule, stage = step mod
-10) and seven qerl_lora_linear calls.  Inputs are synthetic and seeded; the
+decode batch M in {1, 8, 32, 128}: per M, the AQN noise of the four groups
+(qkv, o, gate_up, down; one sampler launch; sigma from the exponential-decay
+schedule, stage = step mod 10) and seven qerl_lora_linear calls.  Inputs are synthetic and seeded; the
 weights are NVFP4-quantized by the library from fp32 N(0, 0.02^2) with 0.5% of
 input channels scaled x10.  Weights rotate over 8 distinct layer copies
 (1.05 GB, far above the 129 MB L2), so every linear streams its weights from
@@ -76,7 +76,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -93,7 +93,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -163,7 +163,12 @@ class Activations:
         for lin in shapes:
             ks[lin.group] = lin.k
         self.x = {g: wl.normal_bf16_device((m, k), 1.0, seed, m, gi, 11) for gi, (g, k) in enumerate(ks.items())}
-        self.z = {g: torch.zeros(k, dtype=torch.float32, device="cuda") for g, k in ks.items()}
+        # one noise buffer for the layer; each AQN group is a 16-byte aligned slice of it
+        self.z_all = torch.zeros(sum(ks.values()), dtype=torch.float32, device="cuda")
+        self.z, off = {}, 0
+        for g, k in ks.items():
+            self.z[g] = self.z_all[off:off + k]
+            off += k
         self.y = [torch.empty((m, lin.n), dtype=torch.bfloat16, device="cuda") for lin in shapes]
         need = max(q.qerl_lora_linear_workspace_size(m, lin.n, lin.k, RANK_R) for lin in shapes)
         self.ws = q.workspace(need)
@@ -175,10 +180,9 @@ class Activations:
 
 
 def run_substep(q, layer, act, sigma, counter):
-    """One decode batch through the layer: 4 AQN samples + 7 linears (all on the current stream)."""
-    for gi, g in enumerate(wl.NOISE_GROUPS):
-        if g in act.z:
-            q.check(q.qerl_aqn_sample(act.z[g], sigma, 0, gi, counter), "qerl_aqn_sample")
+    """One decode batch through the layer: the AQN noise of all four groups (one sampler
+    launch over the concatenated channels) + 7 linears, all on the current stream."""
+    q.check(q.qerl_aqn_sample(act.z_all, sigma, 0, 0, counter), "qerl_aqn_sample")
     for ql, y in zip(layer, act.y):
         g = ql.lin.group
         q.check(q.qerl_lora_linear(act.x[g], ql.codes, ql.scales, ql.S, act.z[g], ql.A, ql.B, ALPHA, y, act.ws),
@@ -311,7 +315,7 @@ def bench_ours(args):
     # ---- end to end through the public API with host buffers (no graph)
     e2e = bench_e2e(q, layers, acts, args, copy_for, sigma_for, step_wbytes, world, barrier)
 
-    launches_per_step = len(DECODE_MS) * (len(wl.NOISE_GROUPS) + 2 * len(shapes))
+    launches_per_step = len(DECODE_MS) * (1 + 2 * len(shapes))
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -332,13 +336,13 @@ def bench_ours(args):
             "weight_bytes_per_step": int(step_wbytes),
             "l2": f"weights rotate over {N_COPIES} distinct layer copies "
                   f"({N_COPIES * layer_wbytes / 1e9:.2f} GB) > 129 MB L2; activations stay hot",
-            "launch": "one CUDA graph per (stage, M): 4 AQN samples + 7 linears",
+            "launch": "one CUDA graph per (stage, M): 1 AQN sampler launch (4 groups) + 7 linears",
             "parallelism": f"replicas x{world}",
         },
         "per_m": per_m,
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode linear path per (M, layer) sub-step: 7 x (prep + tcgen05 dequant-MMA) + 4 AQN samples",
+            "kernel": "decode linear path per (M, layer) sub-step: 7 x (prep + tcgen05 dequant-MMA) + AQN sampler",
             "achieved": round(sub_bytes_total / (sub_time_total * 1e-3) / 1e9, 1),
             "peak": hbm_peak,
             "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)",
@@ -557,7 +561,7 @@ def bench_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-extra", action="store_true", help="skip the prefill and quantizer measurements")
