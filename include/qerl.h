@@ -170,6 +170,25 @@ QERL_API qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64
                              const float* z, const void* A, const void* B, int r, float alpha,
                              void* y, int y_dtype, void* workspace, size_t ws_bytes, void* stream);
 
+/* The same linear for callers that cannot allocate device memory where they
+ * run it (a runtime with a fixed memory pool, a latency-critical loop that must
+ * not enter the CUDA allocator, a hard memory budget).  No counterpart in the
+ * paper: this is a library convenience.  Arguments as for qerl_lora_linear,
+ * without the workspace: the scratch lives in one library-owned device array
+ * of 8 MiB, held by every GPU that loads the library until exit.
+ *   - Problems whose scratch exceeds it (about m*k*2 + m*(r+1)*4 bytes) return
+ *     QERL_ERR_WORKSPACE; nothing is allocated, ever.
+ *   - All calls share the array: calls that may overlap on the GPU race, so
+ *     keep them ordered (e.g. on one stream).
+ *   - The first call on a device looks up the array's address on that device;
+ *     make it before any stream capture.
+ *   - Kernel-detected errors are not reported (the status word is private and
+ *     cleared per call); argument errors are returned as usual. */
+QERL_API qerl_status qerl_lora_linear_noalloc(const void* x, int64_t m, int64_t k, int64_t ldx,
+                                              const uint8_t* codes, const uint8_t* scales,
+                                              const float* tensor_scale, int64_t n, const float* z, const void* A,
+                                              const void* B, int r, float alpha, void* y, int y_dtype, void* stream);
+
 /* Synchronizes `stream`, returns the status word recorded in `workspace` by
  * the kernels of earlier calls (QERL_OK if none failed) and resets it to
  * QERL_OK.  A failing CUDA call returns QERL_ERR_CUDA. */

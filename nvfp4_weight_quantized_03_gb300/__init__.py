@@ -14,6 +14,7 @@ The functions named like the C entry points take torch tensors:
     qerl_aqn_stage(step, total_steps, num_stages)                   (host)
     qerl_aqn_sample(z, sigma, seed, stream_id, counter)
     qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, workspace)
+    qerl_lora_linear_noalloc(x, codes, scales, tensor_scale, z, A, B, alpha, y)
     qerl_read_status(workspace)
 
 and return the qerl_status integer (QERL_OK == 0).  `check()` turns a
@@ -33,7 +34,7 @@ __all__ = [
     "QERL_OK", "QERL_F32", "QERL_BF16", "QerlError", "check", "lib", "lib_path", "status_string",
     "qerl_nvfp4_quantize", "qerl_nvfp4_quantize_with_scale", "qerl_nvfp4_amax",
     "qerl_nvfp4_quantize_workspace_size", "qerl_aqn_sigma", "qerl_aqn_stage", "qerl_aqn_sample",
-    "qerl_lora_linear_workspace_size", "qerl_lora_linear", "qerl_read_status",
+    "qerl_lora_linear_workspace_size", "qerl_lora_linear", "qerl_lora_linear_noalloc", "qerl_read_status",
     "quantize", "lora_linear", "workspace",
 ]
 
@@ -94,6 +95,9 @@ def lib():
             L.qerl_lora_linear.restype = ctypes.c_int
             L.qerl_lora_linear.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_int,
                                            ctypes.c_float, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+            L.qerl_lora_linear_noalloc.restype = ctypes.c_int
+            L.qerl_lora_linear_noalloc.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp,
+                                                   ctypes.c_int, ctypes.c_float, _vp, ctypes.c_int, _vp]
             L.qerl_read_status.restype = ctypes.c_int
             L.qerl_read_status.argtypes = [_vp, _vp]
             _lib = L
@@ -188,6 +192,18 @@ def qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, workspac
     return lib().qerl_lora_linear(_p(x), m, k, x.stride(0), _p(codes), _p(scales), _p(tensor_scale), n, _p(z),
                                   _p(A), _p(B), r, float(alpha), _p(y), ydt, _p(workspace), _nbytes(workspace),
                                   _stream(stream))
+
+
+def qerl_lora_linear_noalloc(x, codes, scales, tensor_scale, z, A, B, alpha, y, stream=None) -> int:
+    """qerl_lora_linear without a workspace, for callers that cannot allocate
+    device memory at the call site; the library's own fixed scratch array is
+    used (shared by all calls: keep them ordered)."""
+    m, k = x.shape
+    n = codes.shape[0]
+    r = 0 if A is None else A.shape[0]
+    ydt = QERL_F32 if y.dtype == torch.float32 else QERL_BF16
+    return lib().qerl_lora_linear_noalloc(_p(x), m, k, x.stride(0), _p(codes), _p(scales), _p(tensor_scale), n,
+                                          _p(z), _p(A), _p(B), r, float(alpha), _p(y), ydt, _stream(stream))
 
 
 def qerl_read_status(workspace, stream=None) -> int:

@@ -1,0 +1,80 @@
+// noalloc.cu -- qerl_lora_linear_noalloc: the LoRA linear for callers that
+// cannot hand the library a workspace.
+//
+// Some callers are not allowed to allocate device memory where they run the
+// layer: an embedding runtime that owns a fixed memory pool and forbids new
+// allocations after start-up, a latency-critical host loop that must not
+// enter the CUDA allocator (cudaMalloc may synchronize the device and take
+// unbounded time), or a tool running under a hard memory budget.  For them
+// this entry point keeps its scratch (the staged noisy activations, the row
+// scales, the LoRA down-projection and the status word) in one file-scope
+// device array instead of a caller-provided workspace.  Inputs and outputs
+// are still the caller's buffers.
+//
+// Rules of use:
+//   - The array is kNoallocScratchBytes (8 MiB).  Every GPU that loads the
+//     library holds it until the process exits.  A problem whose scratch does
+//     not fit (about m*k*2 + m*(r+1)*4 bytes: decode-sized batches fit,
+//     e.g. m = 128 with k up to ~31000) is rejected with QERL_ERR_WORKSPACE;
+//     use qerl_lora_linear with a workspace for larger ones.
+//   - All calls share the array, which keeps the last call's contents.  Calls
+//     that may overlap on the GPU (different streams, or unordered host
+//     threads) race on it; keep the calls ordered, e.g. on one stream.
+//   - The first call on each device looks up the array's device address
+//     (cudaGetSymbolAddress, with that device current) and caches it.  Make
+//     that first call on a device before any stream capture.
+//   - The status word is cleared at the start of every call.  Errors that the
+//     kernels detect (a non-finite value, an expired bounded wait) are not
+//     reported through this entry point; argument errors are returned.
+#include <mutex>
+
+#include "qerl_internal.h"
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = size_t{8} << 20;
+constexpr int kMaxDevices = 64;
+
+// The scratch.  In host code this name is only a stand-in for the device
+// symbol, not a device address; the address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device.
+qerl_status scratch_for_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QERL_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return QERL_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return QERL_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return QERL_OK;
+}
+
+}  // namespace
+
+extern "C" qerl_status qerl_lora_linear_noalloc(const void* x, int64_t m, int64_t k, int64_t ldx,
+                                                const uint8_t* codes, const uint8_t* scales,
+                                                const float* tensor_scale, int64_t n, const float* z, const void* A,
+                                                const void* B, int r, float alpha, void* y, int y_dtype,
+                                                void* stream) {
+  if (m < 0 || n < 0 || k <= 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
+  const int r_eff = (A != nullptr && B != nullptr) ? r : 0;
+  if (qerl::linear_workspace_bytes(m, k, r_eff) > kNoallocScratchBytes) return QERL_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  qerl_status st = scratch_for_current_device(&scratch);
+  if (st != QERL_OK) return st;
+  if (m > 0 && n > 0) {
+    // The status word must start at zero for this call.
+    if (cudaMemsetAsync(scratch, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return QERL_ERR_CUDA;
+  }
+  return qerl_lora_linear(x, m, k, ldx, codes, scales, tensor_scale, n, z, A, B, r, alpha, y, y_dtype, scratch,
+                          kNoallocScratchBytes, stream);
+}
