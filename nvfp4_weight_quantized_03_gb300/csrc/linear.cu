@@ -52,10 +52,11 @@ namespace {
 // ------------------------------------------------------------------ prep
 
 constexpr int kPrepThreads = 256;
-constexpr int kLoraTileM = 64;   // token rows per LoRA task
-constexpr int kLoraTileR = 32;   // ranks per LoRA task
+constexpr int kLoraTileM = 16;   // token rows per LoRA tile
+constexpr int kLoraTileR = 32;   // ranks per LoRA tile
 constexpr int kLoraKc = 64;      // K per shared-memory chunk
 constexpr int kLoraPad = 68;     // padded row length (floats): conflict-free float4 reads
+constexpr int kPrepMaxCluster = 8;
 
 struct PrepParams {
   const __nv_bfloat16* x;
@@ -63,30 +64,54 @@ struct PrepParams {
   const __nv_bfloat16* A;  // [r][K]
   __half* xs;   // [M][K] staged x~ * 2^e_m
   float* rinv;  // [M] 2^-e_m
-  float* t;     // [M][r] (zero-initialised; tasks add their K-slice)
+  float* t;     // [groups][M][r] partial sums of x~ . A^T over K group g
   int64_t ldx;
   int M, K, r;
-  int row_tasks;        // = M
-  int lora_m_tiles;     // ceil(M / kLoraTileM)
-  int lora_r_tiles;     // ceil(r / kLoraTileR)
-  int lora_k_slices;    // number of K slices
-  int kc_per_slice;     // 64-wide K chunks per slice
+  int row_groups;    // blockIdx.y < row_groups: token rows blockIdx.y * cluster + blockIdx.x
+  int lora_m_tiles;  // ceil(M / kLoraTileM)
+  int lora_tiles;    // lora_m_tiles * ceil(r / kLoraTileR)
+  int cluster;       // CTAs per cluster (gridDim.x)
+  int groups;        // K groups; the cluster's CTAs split a group's K range
 };
+
+// K is cut into groups * cluster slices of 64-wide chunks, about two chunks
+// per CTA.  Each group's partial t is reduced inside its cluster; the MMA
+// kernel adds the groups.  Fewer groups for larger token tiles keep that last
+// sum small.
+struct LoraSplit {
+  int cluster, groups;
+};
+__host__ inline LoraSplit lora_split(int64_t m, int64_t k) {
+  const int kc_total = static_cast<int>(k / kLoraKc);
+  LoraSplit L;
+  L.cluster = std::max(1, std::min(kPrepMaxCluster, kc_total));
+  int g = (kc_total + 2 * L.cluster - 1) / (2 * L.cluster);
+  const int64_t n_tok = std::min<int64_t>(256, (m + 15) / 16 * 16);
+  g = std::min<int>(g, static_cast<int>(std::max<int64_t>(1, 256 / std::max<int64_t>(n_tok, 1))));
+  L.groups = std::max(1, std::min(16, g));
+  return L;
+}
 
 __device__ __forceinline__ float noisy(float xv, float zv) {
   // bf16_RN( x * (1 + z) ): one fp32 add, one fp32 multiply, one rounding.
   return __bfloat162float(__float2bfloat16_rn(__fmul_rn(xv, __fadd_rn(1.0f, zv))));
 }
 
+// Grid (cluster, row_groups + LoRA tiles), clusters of `cluster` CTAs along x.
+//   Row tasks: x~ for one token row, staged as fp16 * 2^e_m.
+//   LoRA tiles: t[16 rows][32 ranks] = x~ . A^T; the cluster's CTAs each sum
+//   one K slice and the partial tiles are added over distributed shared
+//   memory in a fixed order, so t is written once, deterministically.
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int tid = threadIdx.x;
   // The MMA kernel may start its prologue (barriers, TMEM, weight loads) now;
   // it waits for this grid's results before it reads them.
   griddep_launch_dependents();
-  if (blockIdx.x < p.row_tasks) {
+  if (static_cast<int>(blockIdx.y) < p.row_groups) {
     // ---- row task: x~ row -> smem (bf16), amax, then fp16 * 2^e
-    const int m = blockIdx.x;
+    const int m = blockIdx.y * p.cluster + blockIdx.x;
+    if (m >= p.M) return;
     __nv_bfloat16* xt = reinterpret_cast<__nv_bfloat16*>(sm);
     const uint4* xrow = reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(m) * p.ldx);
     unsigned amax = 0;
@@ -134,28 +159,27 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     }
     return;
   }
-  // ---- LoRA task: t[rows][ranks] += sum over a K slice of x~[row][k] * A[rank][k].
-  // 64 rows x 32 ranks per task; thread (tx, ty) owns rows {2ty, 2ty+1} and
-  // ranks {tx, tx+8, tx+16, tx+24}: 8 fp32 accumulators, float4 smem reads.
-  const int task = blockIdx.x - p.row_tasks;
-  const int mt = task % p.lora_m_tiles;
-  const int rt = (task / p.lora_m_tiles) % p.lora_r_tiles;
-  const int ks = task / (p.lora_m_tiles * p.lora_r_tiles);
+  // ---- LoRA tile: thread (rank = tid % 32, row pair = tid / 32): 2 accumulators.
+  const int lt = blockIdx.y - p.row_groups;
+  const int g = lt / p.lora_tiles;
+  const int tile = lt - g * p.lora_tiles;
+  const int mt = tile % p.lora_m_tiles;
+  const int rt = tile / p.lora_m_tiles;
+  const int ks = blockIdx.x;  // this CTA's rank in the cluster
   const int row0 = mt * kLoraTileM, rank0 = rt * kLoraTileR;
   float* xsm = reinterpret_cast<float*>(sm);     // [kLoraTileM][kLoraPad]
   float* asm_ = xsm + kLoraTileM * kLoraPad;     // [kLoraTileR][kLoraPad]
-  const int tx = tid & 7, ty = tid >> 3;
-  float acc[2][4];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-  const int kc_begin = ks * p.kc_per_slice;
-  const int kc_end = min(p.K / kLoraKc, kc_begin + p.kc_per_slice);
+  const int lr = tid & 31, rp = tid >> 5;
+  float acc0 = 0.0f, acc1 = 0.0f;
+  const int kc_total = p.K / kLoraKc;
+  const int slices = p.cluster * p.groups;
+  const int sl = g * p.cluster + ks;
+  const int kc_begin = static_cast<int>(static_cast<int64_t>(sl) * kc_total / slices);
+  const int kc_end = static_cast<int>(static_cast<int64_t>(sl + 1) * kc_total / slices);
   for (int kc = kc_begin; kc < kc_end; ++kc) {
     const int k0 = kc * kLoraKc;
     __syncthreads();
-    // x~ tile: 64 rows x 64 k, 8 bf16 per vector -> 512 vectors
+    // x~ tile: 16 rows x 64 k, 8 bf16 per vector -> 128 vectors
     for (int v = tid; v < kLoraTileM * kLoraKc / 8; v += kPrepThreads) {
       const int rr = v >> 3, kk = (v & 7) * 8;
       float f[8];
@@ -199,47 +223,56 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     __syncthreads();
 #pragma unroll 4
     for (int kk = 0; kk < kLoraKc; kk += 4) {
-      float4 xv[2], av[4];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) xv[i] = *reinterpret_cast<const float4*>(xsm + (2 * ty + i) * kLoraPad + kk);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) av[j] = *reinterpret_cast<const float4*>(asm_ + (tx + 8 * j) * kLoraPad + kk);
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[i][j] = fmaf(xv[i].x, av[j].x, acc[i][j]);
-          acc[i][j] = fmaf(xv[i].y, av[j].y, acc[i][j]);
-          acc[i][j] = fmaf(xv[i].z, av[j].z, acc[i][j]);
-          acc[i][j] = fmaf(xv[i].w, av[j].w, acc[i][j]);
-        }
+      const float4 x0 = *reinterpret_cast<const float4*>(xsm + (2 * rp) * kLoraPad + kk);
+      const float4 x1 = *reinterpret_cast<const float4*>(xsm + (2 * rp + 1) * kLoraPad + kk);
+      const float4 av = *reinterpret_cast<const float4*>(asm_ + lr * kLoraPad + kk);
+      acc0 = fmaf(x0.x, av.x, acc0);
+      acc0 = fmaf(x0.y, av.y, acc0);
+      acc0 = fmaf(x0.z, av.z, acc0);
+      acc0 = fmaf(x0.w, av.w, acc0);
+      acc1 = fmaf(x1.x, av.x, acc1);
+      acc1 = fmaf(x1.y, av.y, acc1);
+      acc1 = fmaf(x1.z, av.z, acc1);
+      acc1 = fmaf(x1.w, av.w, acc1);
     }
   }
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int row = row0 + 2 * ty + i, rank = rank0 + tx + 8 * j;
-      if (row < p.M && rank < p.r) atomicAdd(p.t + static_cast<int64_t>(row) * p.r + rank, acc[i][j]);
-    }
+  // Partial tile [kLoraTileM][kLoraTileR] of this K slice -> shared memory,
+  // then CTA q of the cluster sums entries q, q + cluster, ... over all slices.
+  __syncthreads();
+  float* part = reinterpret_cast<float*>(sm);
+  part[(2 * rp) * kLoraTileR + lr] = acc0;
+  part[(2 * rp + 1) * kLoraTileR + lr] = acc1;
+  cluster_sync_all();
+  const uint32_t part_s = smem_u32(part);
+  for (int idx = ks * kPrepThreads + tid; idx < kLoraTileM * kLoraTileR; idx += p.cluster * kPrepThreads) {
+    float v = 0.0f;
+    for (int q = 0; q < p.cluster; ++q) v += ld_shared_cluster_f32(mapa_shared(part_s + 4u * idx, q));
+    const int row = row0 + idx / kLoraTileR, rank = rank0 + idx % kLoraTileR;
+    if (row < p.M && rank < p.r) p.t[(static_cast<int64_t>(g) * p.M + row) * p.r + rank] = v;
+  }
+  cluster_sync_all();  // partners are done reading this CTA's partial tile
 }
 
 // ------------------------------------------------------------------ MMA kernel
 
-constexpr int kMmaThreads = 384;  // warps 0-7 dequant + epilogue, 8 weight producer, 9 MMA, 10 activation producer,
-                                  // 11 LoRA operands
+constexpr int kMmaThreads = 480;  // warps 0-7 dequant + epilogue, 8-11 MMA issuers, 12 weight producer,
+                                  // 13 activation producer, 14 LoRA operands
+constexpr int kIssuerWarp0 = 8, kMaxIssuers = 4;
+constexpr int kWeightWarp = 12, kActWarp = 13, kLoraWarp = 14;
 constexpr int kTileN = 128;       // output features per CTA (MMA M)
 constexpr int kStageK = 64;       // K per MMA stage (4 x K=16 instructions)
 constexpr int kRawK = 256;        // K per weight-load stage: 128 contiguous bytes of codes per row
 constexpr int kSub = kRawK / kStageK;                  // MMA stages per weight stage
 constexpr int kCodesRawBytes = kTileN * kRawK / 2;     // 16384
 constexpr int kScalesRawBytes = kTileN * kRawK / 16;   // 2048
-constexpr int kAStageBytes = kTileN * kStageK * 2;     // 16384 (fp16)
+constexpr int kAStageBytes = kTileN * kStageK * 2;     // 16384 (fp16, shared-memory A operand)
+constexpr int kAStageCols = kStageK / 2;               // 32 TMEM columns (fp16 pairs, tensor-memory A operand)
 constexpr int kLoraChunkK = 64;                        // r is processed in 64-wide chunks (one 128-B swizzle atom)
 constexpr int kBtChunkBytes = kTileN * 128;            // B^T chunk: 128 rows x 64 bf16
 constexpr int kMaxRaw = 8, kMaxAB = 8;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kBarBytes = 512;
+constexpr int kTmemCols = 512;
 
 struct MmaParams {
   const uint8_t* scales;
@@ -253,9 +286,11 @@ struct MmaParams {
   int n_tok;       // tokens per tile (MMA N), multiple of 16, <= 256
   int split;       // K split across the cluster (gridDim.x), in weight stages
   int raw_stages;  // weight-stage ring depth
-  int ab_stages;   // dequantized-A / activation-B ring depth
-  int tmem_cols;
-  uint32_t off_codes, off_a, off_b, off_scales, off_lora, off_sm, off_bars;
+  int ab_stages;   // dequantized-A / activation-B ring depth (a multiple of `issuers`)
+  int issuers;     // MMA-issuing threads, each with its own accumulator
+  int t_groups;    // t holds this many partial sums [t_groups][M][r], added in order
+  uint32_t off_codes, off_a, off_b, off_scales, off_lora, off_tstage, off_sm, off_bars;
+  uint32_t col_lora, col_a;  // TMEM columns of the LoRA accumulator and of the A stages
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
   float lora_scale;
   int y_f32;
@@ -298,7 +333,10 @@ __device__ void build_t_tiles(const MmaParams& p, uint32_t base, int m0, int tid
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int j = c * kLoraChunkK + g * 8 + e;
-      tv[e] = (m < p.M && j < p.r) ? __ldg(p.t + static_cast<int64_t>(m) * p.r + j) : 0.0f;
+      float v = 0.0f;
+      if (m < p.M && j < p.r)
+        for (int g = 0; g < p.t_groups; ++g) v += __ldg(p.t + (static_cast<int64_t>(g) * p.M + m) * p.r + j);
+      tv[e] = v;
     }
     uint32_t hw[4], lw[4];
 #pragma unroll
@@ -314,6 +352,49 @@ __device__ void build_t_tiles(const MmaParams& p, uint32_t base, int m0, int tid
   }
 }
 
+// Same tiles from the partial sums staged in shared memory by bulk copies:
+// tstage[g][ml][j] = t_part[g][m0 + ml][j] for ml < rows.
+__device__ void build_t_tiles_staged(const MmaParams& p, uint32_t base, uint32_t tstage, int rows, int tid,
+                                     int nthr) {
+  const int rc = lora_chunks(p.r);
+  const uint32_t thi = base + rc * kBtChunkBytes;
+  const uint32_t tlo = thi + rc * p.n_tok * 128;
+  const uint32_t gstride = static_cast<uint32_t>(p.n_tok * p.r * 4);
+  for (int idx = tid; idx < rc * p.n_tok * 8; idx += nthr) {
+    const int c = idx / (p.n_tok * 8), rem = idx - c * (p.n_tok * 8);
+    const int ml = rem >> 3, g8 = rem & 7;
+    const int j0 = c * kLoraChunkK + g8 * 8;
+    float tv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tv[e] = 0.0f;
+    if (ml < rows && j0 < p.r) {  // r is a multiple of 8: all eight ranks valid
+      const uint32_t src = tstage + static_cast<uint32_t>((ml * p.r + j0) * 4);
+      for (int g = 0; g < p.t_groups; ++g) {
+        const float4 a = lds128f(src + g * gstride), b = lds128f(src + g * gstride + 16);
+        tv[0] += a.x;
+        tv[1] += a.y;
+        tv[2] += a.z;
+        tv[3] += a.w;
+        tv[4] += b.x;
+        tv[5] += b.y;
+        tv[6] += b.z;
+        tv[7] += b.w;
+      }
+    }
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float h0 = __bfloat162float(__float2bfloat16_rn(tv[2 * e]));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(tv[2 * e + 1]));
+      hw[e] = pack_bf16x2(h0, h1);
+      lw[e] = pack_bf16x2(tv[2 * e] - h0, tv[2 * e + 1] - h1);
+    }
+    const uint32_t off = c * p.n_tok * 128 + ml * 128 + ((g8 ^ (ml & 7)) << 4);
+    sts128(thi + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    sts128(tlo + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+  }
+}
+
 // TMA of the B^T chunks (rows n0..n0+127 of B [N][r], 64 ranks per chunk,
 // zero-filled past N and r) into `base`, completing on `bar`.
 __device__ __forceinline__ void load_bt_tiles(const MmaParams& p, const CUtensorMap* tm_bl, uint32_t base, int n0,
@@ -323,15 +404,15 @@ __device__ __forceinline__ void load_bt_tiles(const MmaParams& p, const CUtensor
   for (int c = 0; c < rc; ++c) tma_load_2d(base + c * kBtChunkBytes, tm_bl, c * kLoraChunkK, n0, bar);
 }
 
-// Warp-cooperative bounded wait: lane 0 polls, the warp converges, then every
-// lane confirms the (already completed) phase for its own acquire.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                          int lane) {
-  int ok = 1;
-  if (lane == 0) ok = mbar_wait_a(bar, parity, abort_flag, status);
-  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-  if (ok) (void)mbar_try_wait_a(bar, parity);
-  return ok != 0;
+// Warp-cooperative bounded wait.  Every lane polls: one convergent try_wait
+// by the whole warp costs less than a single lane's poll inside a divergent
+// branch, and each lane then holds its own acquire.  The vote keeps the warp's
+// answer uniform when a bounded wait gives up.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  bool ok = mbar_try_wait_a(bar, parity);
+  if (__all_sync(0xFFFFFFFFu, ok)) return true;
+  if (!ok) ok = mbar_wait_a(bar, parity, abort_flag, status);
+  return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // D2 (+)= B^T . t_hi^T + B^T . t_lo^T over the rank dimension (bf16 x bf16 -> fp32).
@@ -350,6 +431,14 @@ __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, uint32_t bas
     }
 }
 
+// kTmemA: the dequantized weight operand goes to tensor memory (tcgen05.st),
+// each MMA reads it from there, and `issuers` threads issue MMAs for
+// interleaved stages into their own accumulators (an MMA occupies its issuing
+// thread for far longer than the tensor pipe needs for a 128 x n_tok x 16
+// product, so one issuer cannot keep the pipe busy at decode token counts).
+// Otherwise (256-token tiles) the operand is staged in shared memory and one
+// thread issues.
+template <bool kTmemA>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_xs,
                const __grid_constant__ CUtensorMap tm_bl, const MmaParams p) {
@@ -367,6 +456,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const uint32_t lora_full = bars + 8u * (kB2 + 1);
   const uint32_t acc_full = bars + 8u * (kB2 + 2);
   const uint32_t tmem_holder = bars + 8u * (kB2 + 3);
+  const uint32_t t_full = bars + 8u * (kB2 + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_gen + p.off_bars + 8 * (kB2 + 3) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -380,7 +470,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int kb_total = p.K / kStageK;
   const int mma_begin = kSub * rb;
   const int nmma = min(kSub * re, kb_total) - mma_begin;
-  const int RS = p.raw_stages, AS = p.ab_stages;
+  const int RS = p.raw_stages, AS = p.ab_stages, NI = p.issuers;
   const bool do_lora = p.r > 0 && split_idx == 0;  // one CTA of a K-split cluster adds the LoRA term
 
   if (threadIdx.x == 0) {
@@ -392,18 +482,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       mbar_init_a(ab_full(s), 9);   // 8 dequant warps + activation producer expect_tx
       mbar_init_a(ab_empty(s), 1);  // tcgen05.commit
     }
-    mbar_init_a(ring_free, 1);
-    // B^T TMA (expect_tx) + the t-tile builders: warp 11 (early) or warps 0-7 (late)
+    mbar_init_a(ring_free, NI);
+    // B^T TMA (expect_tx) + the t-tile builders: warp 14 (early) or warps 0-7 (late)
     mbar_init_a(lora_full, p.lora_early ? 2 : 9);
-    mbar_init_a(acc_full, 1);
+    mbar_init_a(acc_full, NI);
+    mbar_init_a(t_full, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 9) {
-    tmem_alloc(tmem_holder, p.tmem_cols);
+  if (warp == kIssuerWarp0) {
+    tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kWeightWarp && lane == 0) {
     tma_prefetch_desc(&tm_codes);
     tma_prefetch_desc(&tm_xs);
     if (p.r > 0) tma_prefetch_desc(&tm_bl);
@@ -412,12 +503,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem_gen + p.off_bars + 8 * (kB2 + 3));
-  const uint32_t d_acc = tmem_base;
-  const uint32_t d_lora = tmem_base + static_cast<uint32_t>(p.n_tok);
+  const uint32_t d_lora = tmem_base + p.col_lora;
   const uint32_t lora_base = p.lora_early ? sbase + p.off_lora : sbase;  // late: inside the idle ring
   const uint32_t smv = sbase + p.off_sm;
 
-  if (warp == 8) {
+  if (warp == kWeightWarp) {
     // ------------------------------------------------------------ weight producer
     const int kq = p.K / 16;  // scale bytes per row
     const bool vec_scales = (p.K % kRawK) == 0;
@@ -452,7 +542,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
       cp_async_mbar_arrive_noinc(raw_full(s));
     }
-  } else if (warp == 10) {
+  } else if (warp == kActWarp) {
     // ------------------------------------------------------------ activation producer
     griddep_wait();  // the staged activations are written by the preceding kernel
     if (lane == 0) {
@@ -464,32 +554,45 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         tma_load_2d(sbase + p.off_b + s * (p.n_tok * 128), &tm_xs, (mma_begin + j) * kStageK, m0, ab_full(s));
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      if (do_lora && p.lora_early) {
+  } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kMaxIssuers) {
+    // ------------------------------------------------------------ MMA issuers
+    const int ii = warp - kIssuerWarp0;
+    if (lane == 0 && ii < NI) {
+      const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
+      const uint32_t d_acc = tmem_base + static_cast<uint32_t>(ii * p.n_tok);
+      uint32_t acc = 0;
+      // Stage s is always served by issuer s % NI (AS is a multiple of NI), so
+      // each barrier has a single waiter that is never two phases ahead.
+      for (int j = ii; j < nmma; j += NI) {
+        const int s = j % AS;
+        const uint32_t ph = (j / AS) & 1;
+        if (!mbar_wait_a(ab_full(s), ph, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t b_addr = sbase + p.off_b + s * (p.n_tok * 128);
+#pragma unroll
+        for (int kk = 0; kk < kStageK / 16; ++kk) {
+          const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
+          if constexpr (kTmemA) {
+            tc_mma_f16_ts(d_acc, tmem_base + p.col_a + s * kAStageCols + kk * 8, bd, idesc, acc);
+          } else {
+            const uint32_t a_addr = sbase + p.off_a + s * kAStageBytes;
+            tc_mma_f16(d_acc, sw128_kmajor_desc(a_addr + kk * 32), bd, idesc, acc);
+          }
+          acc = 1;
+        }
+        tc_commit(ab_empty(s));
+      }
+      // The LoRA up-projection goes last, so a slow producer of t never
+      // holds up the weight stream.
+      if (ii == 0 && do_lora && p.lora_early) {
         if (mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
           tc_fence_after();
           issue_lora_mmas(p, lora_base, d_lora);
         }
       }
-      const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
-      for (int j = 0; j < nmma; ++j) {
-        const int s = j % AS;
-        const uint32_t ph = (j / AS) & 1;
-        if (!mbar_wait_a(ab_full(s), ph, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t a_addr = sbase + p.off_a + s * kAStageBytes;
-        const uint32_t b_addr = sbase + p.off_b + s * (p.n_tok * 128);
-#pragma unroll
-        for (int kk = 0; kk < kStageK / 16; ++kk)
-          tc_mma_f16(d_acc, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(ab_empty(s));
-      }
       if (do_lora && !p.lora_early) {
-        tc_commit(ring_free);  // the ring is idle once the mainloop MMAs are done
-        if (mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
+        tc_commit(ring_free);  // the ring is idle once every mainloop MMA is done
+        if (ii == 0 && mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
           tc_fence_after();
           issue_lora_mmas(p, lora_base, d_lora);
         }
@@ -498,72 +601,121 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ warps 0-7: dequant
-    griddep_wait();  // row scales (and t) come from the preceding kernel
-    {
-      const float S = *p.tensor_scale;
-      for (int i = threadIdx.x; i < p.n_tok; i += 256)
-        stsf(smv + 4u * i, (m0 + i < p.M) ? S * __ldg(p.rinv + m0 + i) : 0.0f);
-    }
-    const int row = 16 * warp + (lane & 15);
-    const int half = lane >> 4;
+    // kTmemA: warp w owns TMEM lane quadrant w % 4 (rows 32(w%4)..+31), one
+    // row per thread, and K-half w / 4 of every 64-wide stage.  Otherwise 16
+    // rows per warp, two K-halves per row pair.
+    const int row = kTmemA ? 32 * (warp & 3) + lane : 16 * warp + (lane & 15);
+    const int half = kTmemA ? warp >> 2 : lane >> 4;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t arow = static_cast<uint32_t>(row * 128);
-    int j = 0;
+    int j = 0, as = 0, s = 0;
+    uint32_t aph = 0, ph = 0;
     for (int i = 0; i < nraw; ++i) {
-      const int s = i % RS;
-      const uint32_t ph = (i / RS) & 1;
-      if (!warp_wait(raw_full(s), ph, abort_flag, p.status, lane)) break;
+      if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
       const uint32_t crow = sbase + p.off_codes + s * kCodesRawBytes + row * 128;
       const uint32_t srow = sbase + p.off_scales + s * kScalesRawBytes + row * 16 + half * 2;
+      // This thread's codes (16 B per 64-wide stage: chunk 2q + half of the
+      // row, 128-byte TMA swizzle) and scale pairs for the whole weight stage.
+      uint4 cw[kSub];
+      uint32_t sc[kSub];
+#pragma unroll
+      for (int q = 0; q < kSub; ++q) {
+        cw[q] = lds128(crow + (((2 * q + half) ^ (row & 7)) << 4));
+        sc[q] = lds16(srow + 4 * q);
+      }
+      // kTmemA: the weight stage's (up to) kSub MMA stages are converted back
+      // to back, their tensor-memory stores are awaited once and their full
+      // barriers signalled together (lane q arrives for stage q); the ring
+      // holds at least kSub stages.  Otherwise each stage is handed over as
+      // soon as it is written (the shared-memory ring may be shallower).
       bool ok = true;
-      for (int q = 0; q < kSub && j < nmma; ++q, ++j) {
-        const int as = j % AS;
-        const uint32_t aph = (j / AS) & 1;
-        if (!warp_wait(ab_empty(as), aph ^ 1, abort_flag, p.status, lane)) {
+      const int nq = min(kSub, nmma - j);
+      const int as0 = as;
+#pragma unroll
+      for (int q = 0; q < kSub; ++q) {
+        if (q >= nq) break;
+        if (!warp_wait(ab_empty(as), aph ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
-        // 32 codes (16 B) of this thread: 16-byte chunk (2q + half) of the row, 128-byte TMA swizzle
-        const uint4 cw = lds128(crow + (((2 * q + half) ^ (row & 7)) << 4));
-        const uint32_t sc2 = lds16(srow + 4 * q);
-        const __half2 s01 = e4m3x2_to_half2(sc2);
-        const __half2 sa = __low2half2(s01), sb = __high2half2(s01);
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-        const uint32_t a_s = sbase + p.off_a + as * kAStageBytes + arow;
+        const __half2 s01 = e4m3x2_to_half2(sc[q]);
+        const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
+        const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
+        const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
+        const uint32_t words[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+        uint32_t o[16];
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
-          const __half2 sq = qq < 2 ? sa : sb;
-          uint4 o;
-          __half2* oh = reinterpret_cast<__half2*>(&o);
+          uint32_t u[4];
+          e2m1x8_to_f16x2x4(words[qq], u);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) oh[b] = __hmul2(e2m1x2_to_half2((words[qq] >> (8 * b)) & 0xFFu), sq);
-          const int chunk = half * 4 + qq;
-          sts128(a_s + ((chunk ^ (row & 7)) << 4), o);
+          for (int b = 0; b < 4; ++b) o[4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_a(ab_full(as));
+        if constexpr (kTmemA) {
+          tmem_st_x16(tmem_base + lane_base + p.col_a + as * kAStageCols + 16 * half, o);
+        } else {
+          const uint32_t a_s = sbase + p.off_a + as * kAStageBytes + arow;
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const int chunk = half * 4 + qq;
+            sts128(a_s + ((chunk ^ (row & 7)) << 4), make_uint4(o[4 * qq], o[4 * qq + 1], o[4 * qq + 2], o[4 * qq + 3]));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_a(ab_full(as));
+        }
+        if (++as == AS) {
+          as = 0;
+          aph ^= 1;
+        }
       }
       if (!ok) break;
+      if constexpr (kTmemA) {
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane < nq) {
+          int st = as0 + lane;
+          while (st >= AS) st -= AS;
+          mbar_arrive_a(ab_full(st));
+        }
+      }
+      j += nq;
       __syncwarp();
       if (lane == 0) mbar_arrive_a(raw_empty(s));
+      if (++s == RS) {
+        s = 0;
+        ph ^= 1;
+      }
     }
     if (do_lora && !p.lora_early) {
-      if (warp_wait(ring_free, 0, abort_flag, p.status, lane)) build_t_tiles(p, lora_base, m0, threadIdx.x, 256);
+      if (warp_wait(ring_free, 0, abort_flag, p.status)) build_t_tiles(p, lora_base, m0, threadIdx.x, 256);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive_a(lora_full);
     }
-  } else if (warp == 11) {
+  } else if (warp == kLoraWarp) {
     // ------------------------------------------------------------ LoRA operands
     if (do_lora) {
       if (p.lora_early) {
         if (lane == 0) load_bt_tiles(p, &tm_bl, lora_base, n0, lora_full);
         griddep_wait();  // t comes from the preceding kernel
-        build_t_tiles(p, lora_base, m0, lane, 32);
+        // Bulk-copy this tile's rows of every partial sum, then convert from
+        // shared memory (scalar loads from L2 would serialize on latency).
+        const int rows = min(p.n_tok, p.M - m0);
+        const uint32_t bytes = static_cast<uint32_t>(rows * p.r * 4);
+        const uint32_t tstage = sbase + p.off_tstage;
+        if (lane == 0) {
+          mbar_arrive_expect_tx_a(t_full, bytes * static_cast<uint32_t>(p.t_groups));
+          for (int g = 0; g < p.t_groups; ++g)
+            bulk_load(tstage + static_cast<uint32_t>(g * p.n_tok * p.r * 4),
+                      p.t + (static_cast<int64_t>(g) * p.M + m0) * p.r, bytes, t_full);
+        }
+        if (warp_wait(t_full, 0, abort_flag, p.status)) build_t_tiles_staged(p, lora_base, tstage, rows, lane, 32);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive_a(lora_full);
-      } else if (warp_wait(ring_free, 0, abort_flag, p.status, lane)) {
+      } else if (warp_wait(ring_free, 0, abort_flag, p.status)) {
         if (lane == 0) load_bt_tiles(p, &tm_bl, lora_base, n0, lora_full);
       } else if (lane == 0) {
         mbar_arrive_a(lora_full);  // after an abort: keep the barrier count consistent
@@ -574,7 +726,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // ---------------------------------------------------------------- epilogue
   const uint32_t part = sbase;  // [n_tok][128] fp32 scaled partial tile (split > 1), ring reused
   if (warp < 8) {
-    const bool ok = warp_wait(acc_full, 0, abort_flag, p.status, lane);
+    // Row scales S * 2^-e_m come from the preceding kernel; the dequant above did not need them.
+    griddep_wait();
+    {
+      const float S = *p.tensor_scale;
+      for (int i = threadIdx.x; i < p.n_tok; i += 256)
+        stsf(smv + 4u * i, (m0 + i < p.M) ? S * __ldg(p.rinv + m0 + i) : 0.0f);
+    }
+    named_barrier_sync(1, 256);
+    const bool ok = warp_wait(acc_full, 0, abort_flag, p.status);
     tc_fence_after();
     const int q = warp & 3;
     const int nl = q * 32 + lane;
@@ -582,11 +742,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int cols = p.n_tok / 2;
     const int c0 = (warp >> 2) * cols;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int nacc = min(NI, nmma);
     for (int c = c0; c < c0 + cols; c += 8) {
       float v[8], l[8];
-      tmem_ld_x8(d_acc + lane_off + c, v);
+      tmem_ld_x8(tmem_base + lane_off + c, v);
       if (do_lora) tmem_ld_x8(d_lora + lane_off + c, l);
       tmem_ld_wait();
+      for (int a = 1; a < nacc; ++a) {
+        float w8[8];
+        tmem_ld_x8(tmem_base + static_cast<uint32_t>(a * p.n_tok) + lane_off + c, w8);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] += w8[e];
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         float out = ok ? v[e] * ldsf(smv + 4u * (c + e)) : 0.0f;
@@ -634,7 +802,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     cluster_sync_all();  // partners are done reading this CTA's partial tile
   }
-  if (warp == 9) tmem_dealloc(tmem_base, p.tmem_cols);
+  if (warp == kIssuerWarp0) tmem_dealloc(tmem_base, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -683,7 +851,8 @@ LinearLayout linear_layout(int64_t m, int64_t k, int r) {
   L.xs = kWsHeaderBytes;
   L.rinv = align_up(L.xs + static_cast<size_t>(m) * k * 2, 256);
   L.t = align_up(L.rinv + static_cast<size_t>(m) * 4, 256);
-  L.total = align_up(L.t + static_cast<size_t>(m) * (r > 0 ? r : 0) * 4, 256);
+  const size_t groups = r > 0 ? static_cast<size_t>(lora_split(m, k).groups) : 0;
+  L.total = align_up(L.t + groups * static_cast<size_t>(m) * (r > 0 ? r : 0) * 4, 256);
   return L;
 }
 
@@ -711,7 +880,9 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemLimit);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+      attr_err = cudaFuncSetAttribute(mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   });
   if (attr_err != cudaSuccess) return QERL_ERR_CUDA;
 
@@ -742,38 +913,59 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     }
   }
   const uint32_t lb = lora_bytes(r, n_tok);
+  const uint32_t tstage_bytes = r > 0 ? static_cast<uint32_t>(lora_split(M, K).groups * n_tok * r * 4) : 0u;
   const int lora_early = (r > 0 && n_tok <= 128) ? 1 : 0;
   const uint32_t part_bytes = split > 1 ? static_cast<uint32_t>(n_tok) * kTileN * 4u : 0u;
   const uint32_t b_stage = static_cast<uint32_t>(n_tok) * 128u;
+  // Decode-sized tiles (<= 128 tokens) keep the dequantized weights in tensor
+  // memory and spread MMA issue over several threads; 256-token tiles stage
+  // the weights in shared memory (their accumulators fill tensor memory).
+  const bool tmem_a = n_tok <= 128;
+  const int issuers = !tmem_a ? 1 : (n_tok <= 64 ? 4 : 2);
+  const uint32_t col_lora = static_cast<uint32_t>(issuers * n_tok);
+  const uint32_t col_a = static_cast<uint32_t>(align_up(col_lora + (r > 0 ? n_tok : 0), 32));
+  int ab_cap = kMaxAB;
+  if (tmem_a) {
+    if (col_a > static_cast<uint32_t>(kTmemCols)) return QERL_ERR_UNSUPPORTED_SHAPE;
+    ab_cap = std::min(kMaxAB, static_cast<int>((kTmemCols - col_a) / kAStageCols));
+    ab_cap -= ab_cap % issuers;  // stage s is always served by issuer s % issuers
+    if (ab_cap < std::max(2, issuers)) return QERL_ERR_UNSUPPORTED_SHAPE;
+  } else if (2 * n_tok > kTmemCols) {
+    return QERL_ERR_UNSUPPORTED_SHAPE;
+  }
   struct Plan {
-    uint32_t codes, a, b, scales, lora, sm, bars, total;
+    uint32_t codes, a, b, scales, lora, tstage, sm, bars, total;
   };
   auto plan_for = [&](int rs, int as) {
     Plan P;
     P.codes = 0;
     P.a = P.codes + rs * kCodesRawBytes;
-    P.b = P.a + as * kAStageBytes;
+    P.b = P.a + (tmem_a ? 0u : static_cast<uint32_t>(as) * kAStageBytes);
     P.scales = P.b + as * b_stage;
     uint32_t ring = P.scales + rs * kScalesRawBytes;
     if (!lora_early) ring = std::max(ring, lb);  // late LoRA tiles are built inside the ring
     ring = std::max(ring, part_bytes);
     P.lora = static_cast<uint32_t>(align_up(ring, 1024));
-    P.sm = P.lora + (lora_early ? lb : 0u);
+    P.tstage = P.lora + (lora_early ? lb : 0u);
+    P.sm = static_cast<uint32_t>(align_up(P.tstage + (lora_early ? tstage_bytes : 0u), 16));
     P.bars = static_cast<uint32_t>(align_up(P.sm + static_cast<uint32_t>(n_tok) * 4u, 16));
-    P.total = P.bars + kBarBytes + 1024u;  // + 1024-byte alignment slack
+    // + 1024-byte alignment slack; at least 116 KB so that two CTAs never share
+    // an SM (each allocates all of tensor memory, and partners in a cluster
+    // wait for one another).
+    P.total = std::max(P.bars + kBarBytes + 1024u, 118784u);
     return P;
   };
-  int ab_stages = n_tok <= 64 ? 6 : (n_tok <= 128 ? 4 : 3);
+  int ab_stages = tmem_a ? ab_cap : 3;
   int raw_stages = 0;
-  for (; ab_stages >= 2 && raw_stages < 2; --ab_stages) {
+  const int ab_step = issuers;
+  for (; ab_stages >= std::max(2, issuers) && raw_stages < 2; ab_stages -= ab_step) {
     for (raw_stages = kMaxRaw; raw_stages >= 2; --raw_stages)
       if (plan_for(raw_stages, ab_stages).total <= static_cast<uint32_t>(kSmemLimit)) break;
     if (raw_stages >= 2) break;
   }
-  if (raw_stages < 2 || ab_stages < 2) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (raw_stages < 2 || ab_stages < std::max(2, issuers)) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (tmem_a && ab_stages < kSub) return QERL_ERR_UNSUPPORTED_SHAPE;  // a weight stage is handed over at once
   const Plan P = plan_for(raw_stages, ab_stages);
-  int tmem_cols = 32;
-  while (tmem_cols < (r > 0 ? 2 * n_tok : n_tok)) tmem_cols *= 2;
 
   CUtensorMap tm_codes, tm_xs;
   if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, static_cast<uint64_t>(K) / 2,
@@ -805,26 +997,31 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   pp.M = M;
   pp.K = K;
   pp.r = r;
-  pp.row_tasks = M;
-  int lora_blocks = 0;
-  if (lora) {
-    if (cudaMemsetAsync(t, 0, static_cast<size_t>(M) * r * 4, s) != cudaSuccess) return QERL_ERR_CUDA;
-    pp.lora_m_tiles = (M + kLoraTileM - 1) / kLoraTileM;
-    pp.lora_r_tiles = (r + kLoraTileR - 1) / kLoraTileR;
-    const int kc_total = K / kLoraKc;
-    const int tiles = pp.lora_m_tiles * pp.lora_r_tiles;
-    // Enough K slices for about two tasks per SM.
-    int per = (kc_total * tiles + 2 * sms - 1) / (2 * sms);
-    per = std::max(per, 1);
-    pp.kc_per_slice = per;
-    pp.lora_k_slices = (kc_total + per - 1) / per;
-    lora_blocks = tiles * pp.lora_k_slices;
-  }
+  const LoraSplit ls = lora_split(M, K);
+  pp.cluster = lora ? ls.cluster : 1;
+  pp.groups = lora ? ls.groups : 0;
+  pp.row_groups = (M + pp.cluster - 1) / pp.cluster;
+  pp.lora_m_tiles = (M + kLoraTileM - 1) / kLoraTileM;
+  pp.lora_tiles = lora ? pp.lora_m_tiles * ((r + kLoraTileR - 1) / kLoraTileR) : 0;
+  const int lora_ctas_y = pp.lora_tiles * pp.groups;
   size_t prep_smem = static_cast<size_t>(K) * 2;
   if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>((kLoraTileM + kLoraTileR) * kLoraPad) * 4);
   if (prep_smem > static_cast<size_t>(kPrepSmemLimit)) return QERL_ERR_UNSUPPORTED_SHAPE;
-  prep_kernel<<<M + lora_blocks, kPrepThreads, prep_smem, s>>>(pp);
-  if (cudaGetLastError() != cudaSuccess) return QERL_ERR_CUDA;
+  {
+    cudaLaunchConfig_t pc{};
+    pc.gridDim = dim3(static_cast<unsigned>(pp.cluster), static_cast<unsigned>(pp.row_groups + lora_ctas_y), 1);
+    pc.blockDim = dim3(kPrepThreads, 1, 1);
+    pc.dynamicSmemBytes = prep_smem;
+    pc.stream = s;
+    cudaLaunchAttribute pa[1];
+    pa[0].id = cudaLaunchAttributeClusterDimension;
+    pa[0].val.clusterDim.x = static_cast<unsigned>(pp.cluster);
+    pa[0].val.clusterDim.y = 1;
+    pa[0].val.clusterDim.z = 1;
+    pc.attrs = pa;
+    pc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&pc, prep_kernel, pp) != cudaSuccess) return QERL_ERR_CUDA;
+  }
 
   MmaParams mp{};
   mp.scales = a.scales;
@@ -842,12 +1039,16 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.split = split;
   mp.raw_stages = raw_stages;
   mp.ab_stages = ab_stages;
-  mp.tmem_cols = tmem_cols;
+  mp.issuers = issuers;
+  mp.t_groups = pp.groups;
+  mp.col_lora = col_lora;
+  mp.col_a = col_a;
   mp.off_codes = P.codes;
   mp.off_a = P.a;
   mp.off_b = P.b;
   mp.off_scales = P.scales;
   mp.off_lora = P.lora;
+  mp.off_tstage = P.tstage;
   mp.off_sm = P.sm;
   mp.off_bars = P.bars;
   mp.lora_early = lora_early;
@@ -869,7 +1070,9 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, mma_kernel, tm_codes, tm_xs, tm_bl, mp) != cudaSuccess) return QERL_ERR_CUDA;
+  const cudaError_t le = tmem_a ? cudaLaunchKernelEx(&cfg, mma_kernel<true>, tm_codes, tm_xs, tm_bl, mp)
+                                : cudaLaunchKernelEx(&cfg, mma_kernel<false>, tm_codes, tm_xs, tm_bl, mp);
+  if (le != cudaSuccess) return QERL_ERR_CUDA;
   return QERL_OK;
 }
 
