@@ -269,12 +269,13 @@ constexpr int kAStageBytes = kTileN * kStageK * 2;     // 16384 (fp16, shared-me
 constexpr int kAStageCols = kStageK / 2;               // 32 TMEM columns (fp16 pairs, tensor-memory A operand)
 constexpr int kLoraChunkK = 64;                        // r is processed in 64-wide chunks (one 128-B swizzle atom)
 constexpr int kBtChunkBytes = kTileN * 128;            // B^T chunk: 128 rows x 64 bf16
-constexpr int kMaxRaw = 8, kMaxAB = 8;
+constexpr int kMaxRaw = 8, kMaxAB = 8, kMaxB = 16;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
-constexpr int kBarBytes = 512;
+constexpr int kBarBytes = 1024;
 constexpr int kTmemCols = 512;
 
 struct MmaParams {
+  const __half* xs;  // staged x~ [M][K] (fp16 * 2^e_m)
   const uint8_t* scales;
   const float* tensor_scale;
   const float* rinv;
@@ -286,10 +287,13 @@ struct MmaParams {
   int n_tok;       // tokens per tile (MMA N), multiple of 16, <= 256
   int split;       // K split across the cluster (gridDim.x), in weight stages
   int raw_stages;  // weight-stage ring depth
-  int ab_stages;   // dequantized-A / activation-B ring depth (a multiple of `issuers`)
+  int ab_stages;   // dequantized-A ring depth (also the activation ring's without kTmemA)
+  int b_stages;    // kTmemA, !coupled: activation ring depth (a multiple of kSub)
+  int coupled;     // kTmemA: a weight stage's activation slabs travel with its codes (same barrier, raw ring)
   int issuers;     // MMA-issuing threads, each with its own accumulator
   int t_groups;    // t holds this many partial sums [t_groups][M][r], added in order
   uint32_t off_codes, off_a, off_b, off_scales, off_lora, off_tstage, off_sm, off_bars;
+  uint32_t raw_b_bytes;  // coupled: activation bytes per weight stage (kSub slabs)
   uint32_t col_lora, col_a;  // TMEM columns of the LoRA accumulator and of the A stages
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
   float lora_scale;
@@ -457,6 +461,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const uint32_t acc_full = bars + 8u * (kB2 + 2);
   const uint32_t tmem_holder = bars + 8u * (kB2 + 3);
   const uint32_t t_full = bars + 8u * (kB2 + 4);
+  // kTmemA: the activation ring has its own depth and barriers.
+  auto b_full = [&](int s) { return bars + 8u * (kB2 + 8 + s); };
+  auto b_empty = [&](int s) { return bars + 8u * (kB2 + 8 + kMaxB + s); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_gen + p.off_bars + 8 * (kB2 + 3) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -470,18 +477,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int kb_total = p.K / kStageK;
   const int mma_begin = kSub * rb;
   const int nmma = min(kSub * re, kb_total) - mma_begin;
-  const int RS = p.raw_stages, AS = p.ab_stages, NI = p.issuers;
+  const int RS = p.raw_stages, AS = p.ab_stages, NI = p.issuers, BS = p.b_stages;
   const bool do_lora = p.r > 0 && split_idx == 0;  // one CTA of a K-split cluster adds the LoRA term
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
       mbar_init_a(raw_full(s), 33);  // producer expect_tx + 32 cp.async arrivals
-      mbar_init_a(raw_empty(s), 8);  // 8 dequant warps
+      mbar_init_a(raw_empty(s), kTmemA && p.coupled ? 8 + kSub : 8);  // 8 dequant warps (+ the stage's MMAs)
     }
     for (int s = 0; s < AS; ++s) {
-      mbar_init_a(ab_full(s), 9);   // 8 dequant warps + activation producer expect_tx
-      mbar_init_a(ab_empty(s), 1);  // tcgen05.commit
+      mbar_init_a(ab_full(s), kTmemA ? 8 : 9);  // 8 dequant warps (+ activation producer expect_tx)
+      mbar_init_a(ab_empty(s), 1);              // tcgen05.commit
     }
+    if (kTmemA)
+      for (int s = 0; s < BS; ++s) {
+        mbar_init_a(b_full(s), 1);   // producer: arrive after its copies landed, or expect_tx
+        mbar_init_a(b_empty(s), 1);  // tcgen05.commit
+      }
     mbar_init_a(ring_free, NI);
     // B^T TMA (expect_tx) + the t-tile builders: warp 14 (early) or warps 0-7 (late)
     mbar_init_a(lora_full, p.lora_early ? 2 : 9);
@@ -511,6 +523,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // ------------------------------------------------------------ weight producer
     const int kq = p.K / 16;  // scale bytes per row
     const bool vec_scales = (p.K % kRawK) == 0;
+    // Coupled: each weight stage's activation slabs are requested right after
+    // its codes, so they share the queue position instead of waiting behind
+    // every weight tile in flight; they come from the preceding kernel.
+    const bool coupled = kTmemA && p.coupled;
+    if (coupled) griddep_wait();
     for (int i = 0; i < nraw; ++i) {
       const int s = i % RS;
       const uint32_t ph = (i / RS) & 1;
@@ -520,8 +537,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (!ok) break;
       const int rst = rb + i;
       if (lane == 0) {
-        mbar_arrive_expect_tx_a(raw_full(s), kCodesRawBytes);
+        mbar_arrive_expect_tx_a(raw_full(s), kCodesRawBytes + (coupled ? p.raw_b_bytes : 0u));
         tma_load_2d(sbase + p.off_codes + s * kCodesRawBytes, &tm_codes, rst * (kRawK / 2), n0, raw_full(s));
+        if (coupled) tma_load_3d(sbase + p.off_b + s * p.raw_b_bytes, &tm_xs, 0, m0, rst * kSub, raw_full(s));
       }
       const uint32_t sdst = sbase + p.off_scales + s * kScalesRawBytes;
 #pragma unroll
@@ -545,7 +563,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp == kActWarp) {
     // ------------------------------------------------------------ activation producer
     griddep_wait();  // the staged activations are written by the preceding kernel
-    if (lane == 0) {
+    if constexpr (kTmemA) {
+      if (!p.coupled && lane == 0) {
+        // One 3D TMA per weight stage: kSub consecutive 64-wide K slabs of
+        // the n_tok x-rows land as kSub consecutive ring stages.
+        for (int i = 0; i < nraw; ++i) {
+          const int s0 = (i * kSub) % BS;
+          bool ok = true;
+          for (int q = 0; q < kSub && ok; ++q) {
+            const int jj = i * kSub + q;
+            ok = mbar_wait_a(b_empty(s0 + q), ((jj / BS) & 1) ^ 1, abort_flag, p.status);
+          }
+          if (!ok) break;
+          mbar_arrive_expect_tx_a(b_full(s0), static_cast<uint32_t>(kSub * p.n_tok * 128));
+          tma_load_3d(sbase + p.off_b + s0 * (p.n_tok * 128), &tm_xs, 0, m0, mma_begin + i * kSub, b_full(s0));
+        }
+      }
+    } else if (!kTmemA && lane == 0) {
       for (int j = 0; j < nmma; ++j) {
         const int s = j % AS;
         const uint32_t ph = (j / AS) & 1;
@@ -567,8 +601,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const int s = j % AS;
         const uint32_t ph = (j / AS) & 1;
         if (!mbar_wait_a(ab_full(s), ph, abort_flag, p.status)) break;
+        int sb = s;
+        uint32_t b_addr = sbase + p.off_b + s * (p.n_tok * 128);
+        if constexpr (kTmemA) {
+          if (p.coupled) {
+            // The activation slab sits in the weight stage's slot (already
+            // landed: the dequant warps waited for it; acquire it here too).
+            const int ri = j / kSub;
+            sb = ri % RS;
+            if (!mbar_wait_a(raw_full(sb), (ri / RS) & 1, abort_flag, p.status)) break;
+            b_addr = sbase + p.off_b + sb * p.raw_b_bytes + (j % kSub) * (p.n_tok * 128);
+          } else {
+            sb = j % BS;
+            if (!mbar_wait_a(b_full(sb - sb % kSub), (j / BS) & 1, abort_flag, p.status)) break;
+            b_addr = sbase + p.off_b + sb * (p.n_tok * 128);
+          }
+        }
         tc_fence_after();
-        const uint32_t b_addr = sbase + p.off_b + s * (p.n_tok * 128);
 #pragma unroll
         for (int kk = 0; kk < kStageK / 16; ++kk) {
           const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
@@ -581,6 +630,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           acc = 1;
         }
         tc_commit(ab_empty(s));
+        if constexpr (kTmemA) tc_commit(p.coupled ? raw_empty(sb) : b_empty(sb));
       }
       // The LoRA up-projection goes last, so a slow producer of t never
       // holds up the weight stream.
@@ -928,7 +978,10 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   if (tmem_a) {
     if (col_a > static_cast<uint32_t>(kTmemCols)) return QERL_ERR_UNSUPPORTED_SHAPE;
     ab_cap = std::min(kMaxAB, static_cast<int>((kTmemCols - col_a) / kAStageCols));
-    ab_cap -= ab_cap % issuers;  // stage s is always served by issuer s % issuers
+    // Stage s is always served by issuer s % issuers, and a weight stage's kSub
+    // MMA stages are consecutive ring stages: a multiple of kSub (which the
+    // issuer count divides).
+    ab_cap -= ab_cap % kSub;
     if (ab_cap < std::max(2, issuers)) return QERL_ERR_UNSUPPORTED_SHAPE;
   } else if (2 * n_tok > kTmemCols) {
     return QERL_ERR_UNSUPPORTED_SHAPE;
@@ -936,12 +989,17 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   struct Plan {
     uint32_t codes, a, b, scales, lora, tstage, sm, bars, total;
   };
-  auto plan_for = [&](int rs, int as) {
+  // Up to 64 tokens a weight stage's activation slabs ride in its raw-ring
+  // slot; above, a separate activation ring is filled by one 3D TMA per
+  // weight stage.
+  const int coupled = (tmem_a && n_tok <= 64) ? 1 : 0;
+  const uint32_t raw_b = coupled ? static_cast<uint32_t>(kSub) * b_stage : 0u;
+  auto plan_for = [&](int rs, int as, int bs) {
     Plan P;
     P.codes = 0;
     P.a = P.codes + rs * kCodesRawBytes;
     P.b = P.a + (tmem_a ? 0u : static_cast<uint32_t>(as) * kAStageBytes);
-    P.scales = P.b + as * b_stage;
+    P.scales = P.b + (coupled ? rs * raw_b : (tmem_a ? bs : as) * b_stage);
     uint32_t ring = P.scales + rs * kScalesRawBytes;
     if (!lora_early) ring = std::max(ring, lb);  // late LoRA tiles are built inside the ring
     ring = std::max(ring, part_bytes);
@@ -956,25 +1014,62 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     return P;
   };
   int ab_stages = tmem_a ? ab_cap : 3;
-  int raw_stages = 0;
-  const int ab_step = issuers;
-  for (; ab_stages >= std::max(2, issuers) && raw_stages < 2; ab_stages -= ab_step) {
-    for (raw_stages = kMaxRaw; raw_stages >= 2; --raw_stages)
-      if (plan_for(raw_stages, ab_stages).total <= static_cast<uint32_t>(kSmemLimit)) break;
-    if (raw_stages >= 2) break;
+  int raw_stages = 0, b_stages = 0;
+  if (tmem_a) {
+    // A lives in tensor memory: keep its depth; prefer >= 6 weight stages in
+    // flight (HBM latency), then the deepest activation ring that fits.
+    const int bs_pref = coupled ? kSub : 8;
+    int best_rs = 0, best_bs = 0;
+    for (int bs = bs_pref; bs >= kSub; bs -= kSub) {
+      int rs = kMaxRaw;
+      while (rs >= 2 && plan_for(rs, ab_stages, bs).total > static_cast<uint32_t>(kSmemLimit)) --rs;
+      if (rs > best_rs) {
+        best_rs = rs;
+        best_bs = bs;
+      }
+      if (rs >= 6) break;
+    }
+    raw_stages = best_rs;
+    b_stages = best_bs;
+  } else {
+    const int ab_step = issuers;
+    for (; ab_stages >= std::max(2, issuers) && raw_stages < 2; ab_stages -= ab_step) {
+      for (raw_stages = kMaxRaw; raw_stages >= 2; --raw_stages)
+        if (plan_for(raw_stages, ab_stages, 0).total <= static_cast<uint32_t>(kSmemLimit)) break;
+      if (raw_stages >= 2) break;
+    }
   }
   if (raw_stages < 2 || ab_stages < std::max(2, issuers)) return QERL_ERR_UNSUPPORTED_SHAPE;
-  if (tmem_a && ab_stages < kSub) return QERL_ERR_UNSUPPORTED_SHAPE;  // a weight stage is handed over at once
-  const Plan P = plan_for(raw_stages, ab_stages);
+  // A weight stage is handed over (and its activations loaded) at once.
+  if (tmem_a && (ab_stages < kSub || ab_stages % kSub != 0 || b_stages < kSub || b_stages % kSub != 0 ||
+                 (coupled && issuers != kSub)))
+    return QERL_ERR_UNSUPPORTED_SHAPE;
+  const Plan P = plan_for(raw_stages, ab_stages, b_stages);
 
   CUtensorMap tm_codes, tm_xs;
   if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, static_cast<uint64_t>(K) / 2,
                    static_cast<uint64_t>(N), static_cast<uint64_t>(K) / 2, kRawK / 2, kTileN,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return QERL_ERR_CUDA;
-  if (!make_map_2d(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xs, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
-                   static_cast<uint64_t>(K) * 2, kStageK, static_cast<uint32_t>(n_tok), CU_TENSOR_MAP_SWIZZLE_128B))
+  if (tmem_a) {
+    // x~ [M][K] viewed as (64 elements, M rows, K/64 slabs): box (64, n_tok, kSub).
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return QERL_ERR_CUDA;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kStageK), static_cast<cuuint64_t>(M),
+                                static_cast<cuuint64_t>(K / kStageK)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(kStageK) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(n_tok),
+                               static_cast<cuuint32_t>(kSub)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, xs, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QERL_ERR_CUDA;
+  } else if (!make_map_2d(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xs, static_cast<uint64_t>(K),
+                          static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2, kStageK,
+                          static_cast<uint32_t>(n_tok), CU_TENSOR_MAP_SWIZZLE_128B)) {
     return QERL_ERR_CUDA;
+  }
 
   CUtensorMap tm_bl;
   if (lora) {
@@ -1024,6 +1119,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   }
 
   MmaParams mp{};
+  mp.xs = xs;
   mp.scales = a.scales;
   mp.tensor_scale = a.tensor_scale;
   mp.rinv = rinv;
@@ -1039,6 +1135,9 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.split = split;
   mp.raw_stages = raw_stages;
   mp.ab_stages = ab_stages;
+  mp.b_stages = b_stages;
+  mp.coupled = coupled;
+  mp.raw_b_bytes = raw_b;
   mp.issuers = issuers;
   mp.t_groups = pp.groups;
   mp.col_lora = col_lora;
