@@ -140,7 +140,9 @@ class QLinear:
         if w_dtype == torch.bfloat16:
             W = W.to(torch.bfloat16)
         self.lin = lin
-        self.codes, self.scales, self.S = q.quantize(W)
+        codes, scales, self.S = q.quantize(W)
+        self.wp = q.pack(codes, scales)
+        del codes, scales
         del W
         self.A = wl.normal_bf16_device((r, lin.k), 1.0 / math.sqrt(lin.k), seed, *path, 2)
         self.B = wl.normal_bf16_device((lin.n, r), 0.01, seed, *path, 3)
@@ -185,7 +187,7 @@ def run_substep(q, layer, act, sigma, counter):
     q.check(q.qerl_aqn_sample(act.z_all, sigma, 0, 0, counter), "qerl_aqn_sample")
     for ql, y in zip(layer, act.y):
         g = ql.lin.group
-        q.check(q.qerl_lora_linear(act.x[g], ql.codes, ql.scales, ql.S, act.z[g], ql.A, ql.B, ALPHA, y, act.ws),
+        q.check(q.qerl_lora_linear(act.x[g], ql.wp, ql.S, act.z[g], ql.A, ql.B, ALPHA, y, act.ws),
                 "qerl_lora_linear")
 
 

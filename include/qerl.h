@@ -112,6 +112,32 @@ QERL_API qerl_status qerl_nvfp4_amax(const void* W, int w_dtype, int64_t n, int6
                             void* workspace, size_t ws_bytes, void* stream);
 
 /* ========================================================================
+ * Packed weights for the linear (a layout of the same codes and scales; no
+ * counterpart in the paper, which fixes the format, not its byte order).
+ *
+ * One contiguous 18432-byte block per (128-row tile t, 256-wide K stage g),
+ * blocks in row-tile-major order: block (t, g) at (t * ceil(k/256) + g) * 18432.
+ *   bytes [0, 16384): for row r (0..127) of the tile, the 128 code bytes of
+ *       K range [256 g, 256 g + 256) (two codes per byte, even k in the low
+ *       nibble, as qerl_nvfp4_quantize writes them) at r * 128, with 16-byte
+ *       chunk c stored at chunk position c XOR (r mod 8);
+ *   bytes [16384, 18432): the E4M3 scales of the stage as pairs: pair p
+ *       (16-element blocks 2p and 2p+1) of row r at 16384 + p * 256 + 2 r.
+ * Rows past n and columns past k are zero.  Each block is the exact image the
+ * linear's kernel stages in shared memory, so one bulk copy moves it.
+ *
+ * qerl_nvfp4_packed_size: bytes of the packed form of an n x k weight
+ * (ceil(n/128) * ceil(k/256) * 18432).
+ * qerl_nvfp4_pack: codes [n][k/2] (16-byte aligned) and scales [n][k/16]
+ * (4-byte aligned) as written by qerl_nvfp4_quantize -> packed (16-byte
+ * aligned, qerl_nvfp4_packed_size bytes, caller-allocated device memory).
+ * Requires k % 64 == 0 and k <= 65536.  Asynchronous on `stream`.
+ * ======================================================================== */
+QERL_API size_t qerl_nvfp4_packed_size(int64_t n, int64_t k);
+QERL_API qerl_status qerl_nvfp4_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
+                                     uint8_t* packed, void* stream);
+
+/* ========================================================================
  * AQN schedule ("Adaptive Quantization Noise", Eq. 8 and Algorithm 1).
  * Host functions, pure, no CUDA.
  *
@@ -141,14 +167,14 @@ QERL_API qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t 
  * The linear layer.
  *
  *   x~[m][k] = bf16_RN( float(x[m][k]) * (1.0f + z[k]) )       (z == NULL: x~ = x)
- *   y[m][n]  = out_RN( S * sum_k x~[m][k] * dec(scales[n][k/16]) * e2m1(codes[n][k])
+ *   y[m][n]  = out_RN( S * sum_k x~[m][k] * dec(scale[n][k/16]) * e2m1(code[n][k])
  *                     + (alpha / r) * sum_j (sum_k x~[m][k] * A[j][k]) * B[n][j] )
  *
  * x       device bf16, m x k, row stride ldx elements (ldx >= k, ldx % 8 == 0,
  *         16-byte aligned).
- * codes, scales, tensor_scale: as written by qerl_nvfp4_quantize for an
- *         n x k weight (n = output features, k = input features).  codes
- *         16-byte aligned, scales 4-byte aligned.
+ * wpacked the n x k weight's codes and scales (n = output features, k = input
+ *         features) as packed by qerl_nvfp4_pack, 16-byte aligned.
+ * tensor_scale device float, the S written by qerl_nvfp4_quantize.
  * z       device float[k] or NULL (no noise).
  * A       device bf16 r x k, B device bf16 n x r (row-major), or both NULL /
  *         r == 0 (no LoRA branch).  r % 8 == 0 and r <= 128; A and B
@@ -165,10 +191,10 @@ QERL_API qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t 
  * ======================================================================== */
 QERL_API size_t qerl_lora_linear_workspace_size(int64_t m, int64_t n, int64_t k, int r);
 
-QERL_API qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx,
-                             const uint8_t* codes, const uint8_t* scales, const float* tensor_scale, int64_t n,
-                             const float* z, const void* A, const void* B, int r, float alpha,
-                             void* y, int y_dtype, void* workspace, size_t ws_bytes, void* stream);
+QERL_API qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, const uint8_t* wpacked,
+                                      const float* tensor_scale, int64_t n, const float* z, const void* A,
+                                      const void* B, int r, float alpha, void* y, int y_dtype, void* workspace,
+                                      size_t ws_bytes, void* stream);
 
 /* The same linear for callers that cannot allocate device memory where they
  * run it (a runtime with a fixed memory pool, a latency-critical loop that must
@@ -176,7 +202,7 @@ QERL_API qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64
  * paper: this is a library convenience.  Arguments as for qerl_lora_linear,
  * without the workspace: the scratch lives in one library-owned device array
  * of 8 MiB, held by every GPU that loads the library until exit.
- *   - Problems whose scratch exceeds it (about m*k*2 + m*(r+1)*4 bytes) return
+ *   - Problems whose scratch exceeds it (about max(m, 16)*k*2 + m*(r+1)*4 bytes, more for the LoRA partial sums of small m) return
  *     QERL_ERR_WORKSPACE; nothing is allocated, ever.
  *   - All calls share the array: calls that may overlap on the GPU race, so
  *     keep them ordered (e.g. on one stream).
@@ -185,9 +211,9 @@ QERL_API qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64
  *   - Kernel-detected errors are not reported (the status word is private and
  *     cleared per call); argument errors are returned as usual. */
 QERL_API qerl_status qerl_lora_linear_noalloc(const void* x, int64_t m, int64_t k, int64_t ldx,
-                                              const uint8_t* codes, const uint8_t* scales,
-                                              const float* tensor_scale, int64_t n, const float* z, const void* A,
-                                              const void* B, int r, float alpha, void* y, int y_dtype, void* stream);
+                                              const uint8_t* wpacked, const float* tensor_scale, int64_t n,
+                                              const float* z, const void* A, const void* B, int r, float alpha,
+                                              void* y, int y_dtype, void* stream);
 
 /* Synchronizes `stream`, returns the status word recorded in `workspace` by
  * the kernels of earlier calls (QERL_OK if none failed) and resets it to

@@ -13,14 +13,16 @@ The functions named like the C entry points take torch tensors:
     qerl_aqn_sigma(stage, num_stages, sigma_start, sigma_end)       (host)
     qerl_aqn_stage(step, total_steps, num_stages)                   (host)
     qerl_aqn_sample(z, sigma, seed, stream_id, counter)
-    qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, workspace)
-    qerl_lora_linear_noalloc(x, codes, scales, tensor_scale, z, A, B, alpha, y)
+    qerl_nvfp4_packed_size(n, k)                                    (host)
+    qerl_nvfp4_pack(codes, scales, packed)
+    qerl_lora_linear(x, wpacked, tensor_scale, z, A, B, alpha, y, workspace)
+    qerl_lora_linear_noalloc(x, wpacked, tensor_scale, z, A, B, alpha, y)
     qerl_read_status(workspace)
 
 and return the qerl_status integer (QERL_OK == 0).  `check()` turns a
-non-zero status into an exception.  `quantize()` and `lora_linear()` are
-conveniences that allocate the outputs with torch (the library itself never
-allocates).
+non-zero status into an exception.  `quantize()`, `pack()` and
+`lora_linear()` are conveniences that allocate the outputs with torch (the
+library itself never allocates).
 """
 import ctypes
 import os
@@ -34,6 +36,7 @@ __all__ = [
     "QERL_OK", "QERL_F32", "QERL_BF16", "QerlError", "check", "lib", "lib_path", "status_string",
     "qerl_nvfp4_quantize", "qerl_nvfp4_quantize_with_scale", "qerl_nvfp4_amax",
     "qerl_nvfp4_quantize_workspace_size", "qerl_aqn_sigma", "qerl_aqn_stage", "qerl_aqn_sample",
+    "qerl_nvfp4_packed_size", "qerl_nvfp4_pack", "pack",
     "qerl_lora_linear_workspace_size", "qerl_lora_linear", "qerl_lora_linear_noalloc", "qerl_read_status",
     "quantize", "lora_linear", "workspace",
 ]
@@ -90,13 +93,17 @@ def lib():
             L.qerl_aqn_sample.restype = ctypes.c_int
             L.qerl_aqn_sample.argtypes = [_vp, _i64, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
                                           ctypes.c_uint64, _vp]
+            L.qerl_nvfp4_packed_size.restype = ctypes.c_size_t
+            L.qerl_nvfp4_packed_size.argtypes = [_i64, _i64]
+            L.qerl_nvfp4_pack.restype = ctypes.c_int
+            L.qerl_nvfp4_pack.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp]
             L.qerl_lora_linear_workspace_size.restype = ctypes.c_size_t
             L.qerl_lora_linear_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.c_int]
             L.qerl_lora_linear.restype = ctypes.c_int
-            L.qerl_lora_linear.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_int,
+            L.qerl_lora_linear.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_int,
                                            ctypes.c_float, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
             L.qerl_lora_linear_noalloc.restype = ctypes.c_int
-            L.qerl_lora_linear_noalloc.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp,
+            L.qerl_lora_linear_noalloc.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
                                                    ctypes.c_int, ctypes.c_float, _vp, ctypes.c_int, _vp]
             L.qerl_read_status.restype = ctypes.c_int
             L.qerl_read_status.argtypes = [_vp, _vp]
@@ -179,31 +186,42 @@ def qerl_aqn_sample(z, sigma: float, seed: int, stream_id: int = 0, counter: int
                                  int(stream_id) & 0xFFFFFFFF, int(counter) & (2**64 - 1), _stream(stream))
 
 
+def qerl_nvfp4_packed_size(n: int, k: int) -> int:
+    return lib().qerl_nvfp4_packed_size(int(n), int(k))
+
+
+def qerl_nvfp4_pack(codes, scales, packed, stream=None) -> int:
+    """codes [n, k/2], scales [n, k/16] (uint8) -> packed (uint8, qerl_nvfp4_packed_size(n, k) bytes)."""
+    n = codes.shape[0]
+    k = codes.shape[1] * 2
+    return lib().qerl_nvfp4_pack(_p(codes), _p(scales), n, k, _p(packed), _stream(stream))
+
+
 def qerl_lora_linear_workspace_size(m: int, n: int, k: int, r: int) -> int:
     return lib().qerl_lora_linear_workspace_size(int(m), int(n), int(k), int(r))
 
 
-def qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, workspace, stream=None) -> int:
-    """A: [r, k] bf16 (LoRA down-projection), B: [n, r] bf16 (LoRA up-projection)."""
+def qerl_lora_linear(x, wpacked, tensor_scale, z, A, B, alpha, y, workspace, stream=None) -> int:
+    """x [m, k] bf16; wpacked: the n x k weight packed by qerl_nvfp4_pack; y [m, n] (n taken from y);
+    A: [r, k] bf16 (LoRA down-projection), B: [n, r] bf16 (LoRA up-projection)."""
     m, k = x.shape
-    n = codes.shape[0]
+    n = y.shape[1]
     r = 0 if A is None else A.shape[0]
     ydt = QERL_F32 if y.dtype == torch.float32 else QERL_BF16
-    return lib().qerl_lora_linear(_p(x), m, k, x.stride(0), _p(codes), _p(scales), _p(tensor_scale), n, _p(z),
-                                  _p(A), _p(B), r, float(alpha), _p(y), ydt, _p(workspace), _nbytes(workspace),
-                                  _stream(stream))
+    return lib().qerl_lora_linear(_p(x), m, k, x.stride(0), _p(wpacked), _p(tensor_scale), n, _p(z), _p(A), _p(B),
+                                  r, float(alpha), _p(y), ydt, _p(workspace), _nbytes(workspace), _stream(stream))
 
 
-def qerl_lora_linear_noalloc(x, codes, scales, tensor_scale, z, A, B, alpha, y, stream=None) -> int:
+def qerl_lora_linear_noalloc(x, wpacked, tensor_scale, z, A, B, alpha, y, stream=None) -> int:
     """qerl_lora_linear without a workspace, for callers that cannot allocate
     device memory at the call site; the library's own fixed scratch array is
     used (shared by all calls: keep them ordered)."""
     m, k = x.shape
-    n = codes.shape[0]
+    n = y.shape[1]
     r = 0 if A is None else A.shape[0]
     ydt = QERL_F32 if y.dtype == torch.float32 else QERL_BF16
-    return lib().qerl_lora_linear_noalloc(_p(x), m, k, x.stride(0), _p(codes), _p(scales), _p(tensor_scale), n,
-                                          _p(z), _p(A), _p(B), r, float(alpha), _p(y), ydt, _stream(stream))
+    return lib().qerl_lora_linear_noalloc(_p(x), m, k, x.stride(0), _p(wpacked), _p(tensor_scale), n, _p(z),
+                                          _p(A), _p(B), r, float(alpha), _p(y), ydt, _stream(stream))
 
 
 def qerl_read_status(workspace, stream=None) -> int:
@@ -228,14 +246,21 @@ def quantize(W: torch.Tensor, ws: torch.Tensor = None):
     return codes, scales, ts
 
 
-def lora_linear(x, codes, scales, tensor_scale, z=None, A=None, B=None, alpha=0.0, out_dtype=torch.bfloat16,
+def pack(codes: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
+    """Packed (kernel-native) form of quantized weights, for qerl_lora_linear."""
+    n, k = codes.shape[0], codes.shape[1] * 2
+    packed = torch.empty(qerl_nvfp4_packed_size(n, k), dtype=torch.uint8, device=codes.device)
+    check(qerl_nvfp4_pack(codes, scales, packed), "qerl_nvfp4_pack")
+    return packed
+
+
+def lora_linear(x, wpacked, tensor_scale, n, z=None, A=None, B=None, alpha=0.0, out_dtype=torch.bfloat16,
                 ws=None):
     """y = x~ . dequant(W)^T + (alpha/r) (x~ A^T) B^T, x~ = bf16(x(1+z)), for bf16 x [m, k],
-    A [r, k], B [n, r]."""
+    W n x k packed by pack(), A [r, k], B [n, r]."""
     m, k = x.shape
-    n = codes.shape[0]
     r = 0 if A is None else A.shape[0]
     y = torch.empty((m, n), dtype=out_dtype, device=x.device)
     ws = workspace(qerl_lora_linear_workspace_size(m, n, k, r), x.device) if ws is None else ws
-    check(qerl_lora_linear(x, codes, scales, tensor_scale, z, A, B, alpha, y, ws), "qerl_lora_linear")
+    check(qerl_lora_linear(x, wpacked, tensor_scale, z, A, B, alpha, y, ws), "qerl_lora_linear")
     return y

@@ -107,16 +107,32 @@ qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, uin
   return qerl::launch_aqn_sample(z, k, sigma, seed, stream_id, counter, as_stream(stream));
 }
 
+size_t qerl_nvfp4_packed_size(int64_t n, int64_t k) {
+  if (n < 0 || k < 0) return 0;
+  return qerl::packed_weight_bytes(n, k);
+}
+
+qerl_status qerl_nvfp4_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
+                            void* stream) {
+  if (n < 0 || k < 0) return QERL_ERR_INVALID_ARGUMENT;
+  if (k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (n > INT32_MAX || k > 65536) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0 || k == 0) return QERL_OK;
+  if (codes == nullptr || scales == nullptr || packed == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(codes, 16) || !aligned(scales, 4) || !aligned(packed, 16)) return QERL_ERR_MISALIGNED;
+  return qerl::launch_pack(codes, scales, n, k, packed, as_stream(stream));
+}
+
 size_t qerl_lora_linear_workspace_size(int64_t m, int64_t n, int64_t k, int r) {
   (void)n;
   if (m < 0 || k < 0 || r < 0) return 0;
   return qerl::linear_workspace_bytes(m, k, r);
 }
 
-qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, const uint8_t* codes,
-                             const uint8_t* scales, const float* tensor_scale, int64_t n, const float* z,
-                             const void* A, const void* B, int r, float alpha, void* y, int y_dtype,
-                             void* workspace, size_t ws_bytes, void* stream) {
+qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, const uint8_t* wpacked,
+                             const float* tensor_scale, int64_t n, const float* z, const void* A, const void* B,
+                             int r, float alpha, void* y, int y_dtype, void* workspace, size_t ws_bytes,
+                             void* stream) {
   if (m < 0 || n < 0 || k <= 0 || ldx < k || r < 0) return QERL_ERR_INVALID_ARGUMENT;
   if (y_dtype != QERL_BF16 && y_dtype != QERL_F32) return QERL_ERR_INVALID_ARGUMENT;
   if ((A == nullptr) != (B == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
@@ -127,9 +143,8 @@ qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, c
   if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX || m * k > (int64_t{1} << 40))
     return QERL_ERR_UNSUPPORTED_SHAPE;
   if (m == 0 || n == 0) return QERL_OK;
-  if (x == nullptr || codes == nullptr || scales == nullptr || tensor_scale == nullptr || y == nullptr)
-    return QERL_ERR_INVALID_ARGUMENT;
-  if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(codes, 16) || !aligned(scales, 4)) return QERL_ERR_MISALIGNED;
+  if (x == nullptr || wpacked == nullptr || tensor_scale == nullptr || y == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wpacked, 16)) return QERL_ERR_MISALIGNED;
   if (z != nullptr && !aligned(z, 16)) return QERL_ERR_MISALIGNED;
   if (y_dtype == QERL_F32 ? !aligned(y, 4) : !aligned(y, 2)) return QERL_ERR_MISALIGNED;
   if (A != nullptr && (!aligned(A, 16) || !aligned(B, 16))) return QERL_ERR_MISALIGNED;
@@ -141,8 +156,7 @@ qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, c
   a.k = k;
   a.ldx = ldx;
   a.n = n;
-  a.codes = codes;
-  a.scales = scales;
+  a.wpacked = wpacked;
   a.tensor_scale = tensor_scale;
   a.z = z;
   a.A = A;

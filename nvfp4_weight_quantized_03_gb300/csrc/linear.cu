@@ -62,7 +62,7 @@ struct PrepParams {
   const __nv_bfloat16* x;
   const float* z;
   const __nv_bfloat16* A;  // [r][K]
-  __half* xs;   // [M][K] staged x~ * 2^e_m
+  __half* xs;   // staged x~ * 2^e_m: [M][K], or tiled (see xs_tile_offset)
   float* rinv;  // [M] 2^-e_m
   float* t;     // [groups][M][r] partial sums of x~ . A^T over K group g
   int64_t ldx;
@@ -72,7 +72,19 @@ struct PrepParams {
   int lora_tiles;    // lora_m_tiles * ceil(r / kLoraTileR)
   int cluster;       // CTAs per cluster (gridDim.x)
   int groups;        // K groups; the cluster's CTAs split a group's K range
+  int tiled_rows;    // > 0: x~ in the tiled layout for this many rows (>= M; rows past M are zero)
 };
+
+// Tiled x~ (token tiles of up to 128 rows, one tile): for each 256-wide K
+// stage g, four 64-wide slabs of tiled_rows rows x 128 bytes, each row's
+// 16-byte chunk c at position c ^ (row % 8) -- the shared-memory image of
+// the MMA's 128-byte-swizzled K-major operand, so one bulk copy per stage
+// moves it.  Byte offset of elements k .. k + 7 (k % 8 == 0) of row m:
+__host__ __device__ inline size_t xs_tile_offset(int m, int k, int rows) {
+  const int g = k >> 8, sl = (k >> 6) & 3, c = (k >> 3) & 7;
+  return static_cast<size_t>(g) * (4u * rows * 128u) + static_cast<size_t>(sl) * rows * 128u + m * 128u +
+         ((c ^ (m & 7)) << 4);
+}
 
 // K is cut into groups * cluster slices of 64-wide chunks, about two chunks
 // per CTA.  Each group's partial t is reduced inside its cluster; the MMA
@@ -111,7 +123,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   if (static_cast<int>(blockIdx.y) < p.row_groups) {
     // ---- row task: x~ row -> smem (bf16), amax, then fp16 * 2^e
     const int m = blockIdx.y * p.cluster + blockIdx.x;
-    if (m >= p.M) return;
+    if (m >= p.M) {
+      if (m < p.tiled_rows)  // padding row of the token tile: zeros
+        for (int v = tid; v < p.K / 8; v += kPrepThreads)
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.xs) + xs_tile_offset(m, 8 * v, p.tiled_rows)) =
+              make_uint4(0u, 0u, 0u, 0u);
+      return;
+    }
     __nv_bfloat16* xt = reinterpret_cast<__nv_bfloat16*>(sm);
     const uint4* xrow = reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(m) * p.ldx);
     unsigned amax = 0;
@@ -147,6 +165,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     const float scale = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
     if (tid == 0) p.rinv[m] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
     uint4* dst = reinterpret_cast<uint4*>(p.xs + static_cast<int64_t>(m) * p.K);
+    uint8_t* dst_t = reinterpret_cast<uint8_t*>(p.xs);
     for (int v = tid; v < p.K / 8; v += kPrepThreads) {
       uint4 raw = reinterpret_cast<const uint4*>(xt)[v];
       const __nv_bfloat16* e8 = reinterpret_cast<const __nv_bfloat16*>(&raw);
@@ -155,7 +174,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         o[j] = __floats2half2_rn(__bfloat162float(e8[2 * j]) * scale, __bfloat162float(e8[2 * j + 1]) * scale);
-      dst[v] = out;
+      if (p.tiled_rows > 0)
+        *reinterpret_cast<uint4*>(dst_t + xs_tile_offset(m, 8 * v, p.tiled_rows)) = out;
+      else
+        dst[v] = out;
     }
     return;
   }
@@ -264,7 +286,7 @@ constexpr int kStageK = 64;       // K per MMA stage (4 x K=16 instructions)
 constexpr int kRawK = 256;        // K per weight-load stage: 128 contiguous bytes of codes per row
 constexpr int kSub = kRawK / kStageK;                  // MMA stages per weight stage
 constexpr int kCodesRawBytes = kTileN * kRawK / 2;     // 16384
-constexpr int kScalesRawBytes = kTileN * kRawK / 16;   // 2048
+constexpr int kRawSlotBytes = kCodesRawBytes + kTileN * kRawK / 16;  // + 2048 scale bytes: one packed block
 constexpr int kAStageBytes = kTileN * kStageK * 2;     // 16384 (fp16, shared-memory A operand)
 constexpr int kAStageCols = kStageK / 2;               // 32 TMEM columns (fp16 pairs, tensor-memory A operand)
 constexpr int kLoraChunkK = 64;                        // r is processed in 64-wide chunks (one 128-B swizzle atom)
@@ -275,8 +297,8 @@ constexpr int kBarBytes = 1024;
 constexpr int kTmemCols = 512;
 
 struct MmaParams {
-  const __half* xs;  // staged x~ [M][K] (fp16 * 2^e_m)
-  const uint8_t* scales;
+  const __half* xs;        // staged x~ (fp16 * 2^e_m): tiled with kTmemA, else [M][K]
+  const uint8_t* wpacked;  // packed weight blocks (see qerl_nvfp4_pack)
   const float* tensor_scale;
   const float* rinv;
   const float* t;
@@ -292,7 +314,7 @@ struct MmaParams {
   int coupled;     // kTmemA: a weight stage's activation slabs travel with its codes (same barrier, raw ring)
   int issuers;     // MMA-issuing threads, each with its own accumulator
   int t_groups;    // t holds this many partial sums [t_groups][M][r], added in order
-  uint32_t off_codes, off_a, off_b, off_scales, off_lora, off_tstage, off_sm, off_bars;
+  uint32_t off_raw, off_a, off_b, off_lora, off_tstage, off_sm, off_bars;
   uint32_t raw_b_bytes;  // coupled: activation bytes per weight stage (kSub slabs)
   uint32_t col_lora, col_a;  // TMEM columns of the LoRA accumulator and of the A stages
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
@@ -444,8 +466,8 @@ __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, uint32_t bas
 // thread issues.
 template <bool kTmemA>
 __global__ void __launch_bounds__(kMmaThreads, 1)
-    mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_xs,
-               const __grid_constant__ CUtensorMap tm_bl, const MmaParams p) {
+    mma_kernel(const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_bl,
+               const MmaParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -482,7 +504,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
-      mbar_init_a(raw_full(s), 33);  // producer expect_tx + 32 cp.async arrivals
+      mbar_init_a(raw_full(s), 1);  // producer expect_tx
       mbar_init_a(raw_empty(s), kTmemA && p.coupled ? 8 + kSub : 8);  // 8 dequant warps (+ the stage's MMAs)
     }
     for (int s = 0; s < AS; ++s) {
@@ -507,8 +529,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWeightWarp && lane == 0) {
-    tma_prefetch_desc(&tm_codes);
-    tma_prefetch_desc(&tm_xs);
+    if (!kTmemA) tma_prefetch_desc(&tm_xs);
     if (p.r > 0) tma_prefetch_desc(&tm_bl);
   }
   tc_fence_before();
@@ -521,52 +542,50 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   if (warp == kWeightWarp) {
     // ------------------------------------------------------------ weight producer
-    const int kq = p.K / 16;  // scale bytes per row
-    const bool vec_scales = (p.K % kRawK) == 0;
-    // Coupled: each weight stage's activation slabs are requested right after
-    // its codes, so they share the queue position instead of waiting behind
-    // every weight tile in flight; they come from the preceding kernel.
+    // One bulk copy per weight stage: the packed block (codes in their
+    // swizzled image, then the scale pairs) is contiguous in memory.
+    // Coupled: the stage's activation slabs follow in the same queue
+    // position and complete on the same barrier; they come from the
+    // preceding kernel.
     const bool coupled = kTmemA && p.coupled;
+    const uint8_t* wtile = p.wpacked + static_cast<int64_t>(blockIdx.y) * raw_total * kRawSlotBytes;
+    const int kslabs = p.K / kStageK;
+    // The copies into the ring are held for a stage's whole dequant + MMA
+    // time, so the ring alone cannot cover HBM latency at full rate: the
+    // blocks kPrefetch stages ahead are prefetched into L2 (bounded by L2
+    // capacity, not shared memory) and the ring refills from L2.
+    constexpr int kPrefetch = 8;
+    if (lane == 0)
+      for (int i = 0; i < min(kPrefetch, nraw); ++i)
+        bulk_prefetch_l2(wtile + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes);
     if (coupled) griddep_wait();
-    for (int i = 0; i < nraw; ++i) {
-      const int s = i % RS;
-      const uint32_t ph = (i / RS) & 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status);
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) break;
-      const int rst = rb + i;
-      if (lane == 0) {
-        mbar_arrive_expect_tx_a(raw_full(s), kCodesRawBytes + (coupled ? p.raw_b_bytes : 0u));
-        tma_load_2d(sbase + p.off_codes + s * kCodesRawBytes, &tm_codes, rst * (kRawK / 2), n0, raw_full(s));
-        if (coupled) tma_load_3d(sbase + p.off_b + s * p.raw_b_bytes, &tm_xs, 0, m0, rst * kSub, raw_full(s));
+    if (lane == 0) {
+      for (int i = 0, s = 0; i < nraw; ++i) {
+        if (i + kPrefetch < nraw)
+          bulk_prefetch_l2(wtile + static_cast<int64_t>(rb + i + kPrefetch) * kRawSlotBytes, kRawSlotBytes);
+        const uint32_t ph = (i / RS) & 1;
+        if (!mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status)) break;
+        const int rst = rb + i;
+        const uint32_t xbytes =
+            coupled ? static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128) : 0u;
+        mbar_arrive_expect_tx_a(raw_full(s), kRawSlotBytes + xbytes);
+        bulk_load(sbase + p.off_raw + s * kRawSlotBytes, wtile + static_cast<int64_t>(rst) * kRawSlotBytes,
+                  kRawSlotBytes, raw_full(s));
+        if (coupled)
+          bulk_load(sbase + p.off_b + s * p.raw_b_bytes,
+                    reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rst) * p.raw_b_bytes, xbytes,
+                    raw_full(s));
+        if (++s == RS) s = 0;
       }
-      const uint32_t sdst = sbase + p.off_scales + s * kScalesRawBytes;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = lane * 4 + j;
-        const int n = n0 + row;
-        const bool in = n < p.N;
-        const uint8_t* src = p.scales + static_cast<int64_t>(in ? n : 0) * kq + rst * 16;
-        if (vec_scales) {
-          cp_async_16(sdst + row * 16, src, in ? 16u : 0u);
-        } else {
-#pragma unroll
-          for (int qq = 0; qq < kSub; ++qq) {
-            const bool v = in && (rst * kSub + qq) < kb_total;
-            cp_async_4(sdst + row * 16 + 4 * qq, v ? src + 4 * qq : p.scales, v ? 4u : 0u);
-          }
-        }
-      }
-      cp_async_mbar_arrive_noinc(raw_full(s));
     }
   } else if (warp == kActWarp) {
     // ------------------------------------------------------------ activation producer
     griddep_wait();  // the staged activations are written by the preceding kernel
     if constexpr (kTmemA) {
       if (!p.coupled && lane == 0) {
-        // One 3D TMA per weight stage: kSub consecutive 64-wide K slabs of
-        // the n_tok x-rows land as kSub consecutive ring stages.
+        // One bulk copy per weight stage: its kSub 64-wide K slabs (tiled
+        // layout) land as kSub consecutive ring stages.
+        const int kslabs = p.K / kStageK;
         for (int i = 0; i < nraw; ++i) {
           const int s0 = (i * kSub) % BS;
           bool ok = true;
@@ -575,8 +594,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             ok = mbar_wait_a(b_empty(s0 + q), ((jj / BS) & 1) ^ 1, abort_flag, p.status);
           }
           if (!ok) break;
-          mbar_arrive_expect_tx_a(b_full(s0), static_cast<uint32_t>(kSub * p.n_tok * 128));
-          tma_load_3d(sbase + p.off_b + s0 * (p.n_tok * 128), &tm_xs, 0, m0, mma_begin + i * kSub, b_full(s0));
+          const int rst = rb + i;
+          const uint32_t xbytes = static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128);
+          mbar_arrive_expect_tx_a(b_full(s0), xbytes);
+          bulk_load(sbase + p.off_b + s0 * (p.n_tok * 128),
+                    reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rst) * (kSub * p.n_tok * 128),
+                    xbytes, b_full(s0));
         }
       }
     } else if (!kTmemA && lane == 0) {
@@ -662,16 +685,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     uint32_t aph = 0, ph = 0;
     for (int i = 0; i < nraw; ++i) {
       if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
-      const uint32_t crow = sbase + p.off_codes + s * kCodesRawBytes + row * 128;
-      const uint32_t srow = sbase + p.off_scales + s * kScalesRawBytes + row * 16 + half * 2;
+      const uint32_t slot = sbase + p.off_raw + s * kRawSlotBytes;
+      const uint32_t crow = slot + row * 128;
+      const uint32_t srow = slot + kCodesRawBytes + half * 256 + row * 2;
       // This thread's codes (16 B per 64-wide stage: chunk 2q + half of the
-      // row, 128-byte TMA swizzle) and scale pairs for the whole weight stage.
+      // row, 128-byte swizzle) and scale pairs for the whole weight stage.
       uint4 cw[kSub];
       uint32_t sc[kSub];
 #pragma unroll
       for (int q = 0; q < kSub; ++q) {
         cw[q] = lds128(crow + (((2 * q + half) ^ (row & 7)) << 4));
-        sc[q] = lds16(srow + 4 * q);
+        sc[q] = lds16(srow + 2 * q * 256);  // scale pair 2q + half: blocks 4q + 2half, +1
       }
       // kTmemA: the weight stage's (up to) kSub MMA stages are converted back
       // to back, their tensor-memory stores are awaited once and their full
@@ -896,10 +920,17 @@ struct LinearLayout {
   size_t xs, rinv, t, total;
 };
 
+// Token tiles of up to 128 rows stage x~ in the tiled layout (one tile of
+// round_up(m, 16) rows); larger m keeps the row-major [m][k] layout.
+inline int tiled_rows_for(int64_t m) { return m <= 128 ? static_cast<int>((m + 15) / 16 * 16) : 0; }
+
 LinearLayout linear_layout(int64_t m, int64_t k, int r) {
   LinearLayout L;
   L.xs = kWsHeaderBytes;
-  L.rinv = align_up(L.xs + static_cast<size_t>(m) * k * 2, 256);
+  const int tr = tiled_rows_for(m);
+  const size_t xs_bytes =
+      tr > 0 ? static_cast<size_t>((k + kRawK - 1) / kRawK) * 4u * tr * 128u : static_cast<size_t>(m) * k * 2;
+  L.rinv = align_up(L.xs + xs_bytes, 256);
   L.t = align_up(L.rinv + static_cast<size_t>(m) * 4, 256);
   const size_t groups = r > 0 ? static_cast<size_t>(lora_split(m, k).groups) : 0;
   L.total = align_up(L.t + groups * static_cast<size_t>(m) * (r > 0 ? r : 0) * 4, 256);
@@ -987,20 +1018,19 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     return QERL_ERR_UNSUPPORTED_SHAPE;
   }
   struct Plan {
-    uint32_t codes, a, b, scales, lora, tstage, sm, bars, total;
+    uint32_t raw, a, b, lora, tstage, sm, bars, total;
   };
   // Up to 64 tokens a weight stage's activation slabs ride in its raw-ring
-  // slot; above, a separate activation ring is filled by one 3D TMA per
+  // slot; above, a separate activation ring is filled by one bulk copy per
   // weight stage.
   const int coupled = (tmem_a && n_tok <= 64) ? 1 : 0;
   const uint32_t raw_b = coupled ? static_cast<uint32_t>(kSub) * b_stage : 0u;
   auto plan_for = [&](int rs, int as, int bs) {
     Plan P;
-    P.codes = 0;
-    P.a = P.codes + rs * kCodesRawBytes;
+    P.raw = 0;  // packed weight blocks (codes + scale pairs); 18 KB slots keep 1024-byte alignment
+    P.a = P.raw + rs * kRawSlotBytes;
     P.b = P.a + (tmem_a ? 0u : static_cast<uint32_t>(as) * kAStageBytes);
-    P.scales = P.b + (coupled ? rs * raw_b : (tmem_a ? bs : as) * b_stage);
-    uint32_t ring = P.scales + rs * kScalesRawBytes;
+    uint32_t ring = P.b + (coupled ? rs * raw_b : (tmem_a ? bs : as) * b_stage);
     if (!lora_early) ring = std::max(ring, lb);  // late LoRA tiles are built inside the ring
     ring = std::max(ring, part_bytes);
     P.lora = static_cast<uint32_t>(align_up(ring, 1024));
@@ -1046,25 +1076,11 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     return QERL_ERR_UNSUPPORTED_SHAPE;
   const Plan P = plan_for(raw_stages, ab_stages, b_stages);
 
-  CUtensorMap tm_codes, tm_xs;
-  if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, static_cast<uint64_t>(K) / 2,
-                   static_cast<uint64_t>(N), static_cast<uint64_t>(K) / 2, kRawK / 2, kTileN,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
-    return QERL_ERR_CUDA;
+  // x~: tiled layout moved by bulk copies with kTmemA; the 256-token tiles
+  // read [M][K] through a 2D tensor map.
+  CUtensorMap tm_xs;
   if (tmem_a) {
-    // x~ [M][K] viewed as (64 elements, M rows, K/64 slabs): box (64, n_tok, kSub).
-    auto enc = tensor_map_encoder();
-    if (enc == nullptr) return QERL_ERR_CUDA;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kStageK), static_cast<cuuint64_t>(M),
-                                static_cast<cuuint64_t>(K / kStageK)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(kStageK) * 2};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(n_tok),
-                               static_cast<cuuint32_t>(kSub)};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, xs, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return QERL_ERR_CUDA;
+    std::memset(&tm_xs, 0, sizeof(tm_xs));
   } else if (!make_map_2d(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xs, static_cast<uint64_t>(K),
                           static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2, kStageK,
                           static_cast<uint32_t>(n_tok), CU_TENSOR_MAP_SWIZZLE_128B)) {
@@ -1095,7 +1111,8 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   const LoraSplit ls = lora_split(M, K);
   pp.cluster = lora ? ls.cluster : 1;
   pp.groups = lora ? ls.groups : 0;
-  pp.row_groups = (M + pp.cluster - 1) / pp.cluster;
+  pp.tiled_rows = tmem_a ? n_tok : 0;
+  pp.row_groups = (std::max(M, pp.tiled_rows) + pp.cluster - 1) / pp.cluster;
   pp.lora_m_tiles = (M + kLoraTileM - 1) / kLoraTileM;
   pp.lora_tiles = lora ? pp.lora_m_tiles * ((r + kLoraTileR - 1) / kLoraTileR) : 0;
   const int lora_ctas_y = pp.lora_tiles * pp.groups;
@@ -1120,7 +1137,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
 
   MmaParams mp{};
   mp.xs = xs;
-  mp.scales = a.scales;
+  mp.wpacked = a.wpacked;
   mp.tensor_scale = a.tensor_scale;
   mp.rinv = rinv;
   mp.t = t;
@@ -1142,10 +1159,9 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.t_groups = pp.groups;
   mp.col_lora = col_lora;
   mp.col_a = col_a;
-  mp.off_codes = P.codes;
+  mp.off_raw = P.raw;
   mp.off_a = P.a;
   mp.off_b = P.b;
-  mp.off_scales = P.scales;
   mp.off_lora = P.lora;
   mp.off_tstage = P.tstage;
   mp.off_sm = P.sm;
@@ -1169,8 +1185,8 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  const cudaError_t le = tmem_a ? cudaLaunchKernelEx(&cfg, mma_kernel<true>, tm_codes, tm_xs, tm_bl, mp)
-                                : cudaLaunchKernelEx(&cfg, mma_kernel<false>, tm_codes, tm_xs, tm_bl, mp);
+  const cudaError_t le = tmem_a ? cudaLaunchKernelEx(&cfg, mma_kernel<true>, tm_xs, tm_bl, mp)
+                                : cudaLaunchKernelEx(&cfg, mma_kernel<false>, tm_xs, tm_bl, mp);
   if (le != cudaSuccess) return QERL_ERR_CUDA;
   return QERL_OK;
 }

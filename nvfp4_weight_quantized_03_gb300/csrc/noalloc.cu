@@ -14,7 +14,7 @@
 // Rules of use:
 //   - The array is kNoallocScratchBytes (8 MiB).  Every GPU that loads the
 //     library holds it until the process exits.  A problem whose scratch does
-//     not fit (about m*k*2 + m*(r+1)*4 bytes: decode-sized batches fit,
+//     not fit (about max(m, 16)*k*2 + m*(r+1)*4 bytes: decode-sized batches fit,
 //     e.g. m = 128 with k up to ~31000) is rejected with QERL_ERR_WORKSPACE;
 //     use qerl_lora_linear with a workspace for larger ones.
 //   - All calls share the array, which keeps the last call's contents.  Calls
@@ -60,10 +60,9 @@ qerl_status scratch_for_current_device(void** out) {
 }  // namespace
 
 extern "C" qerl_status qerl_lora_linear_noalloc(const void* x, int64_t m, int64_t k, int64_t ldx,
-                                                const uint8_t* codes, const uint8_t* scales,
-                                                const float* tensor_scale, int64_t n, const float* z, const void* A,
-                                                const void* B, int r, float alpha, void* y, int y_dtype,
-                                                void* stream) {
+                                                const uint8_t* wpacked, const float* tensor_scale, int64_t n,
+                                                const float* z, const void* A, const void* B, int r, float alpha,
+                                                void* y, int y_dtype, void* stream) {
   if (m < 0 || n < 0 || k <= 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
   const int r_eff = (A != nullptr && B != nullptr) ? r : 0;
   if (qerl::linear_workspace_bytes(m, k, r_eff) > kNoallocScratchBytes) return QERL_ERR_WORKSPACE;
@@ -75,6 +74,6 @@ extern "C" qerl_status qerl_lora_linear_noalloc(const void* x, int64_t m, int64_
     if (cudaMemsetAsync(scratch, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return QERL_ERR_CUDA;
   }
-  return qerl_lora_linear(x, m, k, ldx, codes, scales, tensor_scale, n, z, A, B, r, alpha, y, y_dtype, scratch,
+  return qerl_lora_linear(x, m, k, ldx, wpacked, tensor_scale, n, z, A, B, r, alpha, y, y_dtype, scratch,
                           kNoallocScratchBytes, stream);
 }

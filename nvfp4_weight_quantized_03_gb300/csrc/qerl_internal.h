@@ -23,6 +23,12 @@ qerl_status launch_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_
                           uint8_t* scales, int* status, cudaStream_t s);
 qerl_status launch_amax_to_float(const unsigned* amax_bits, float* amax, cudaStream_t s);
 
+// Packed weights for the linear (quantize.cu): 128 rows x 256 K per block.
+constexpr size_t kPackedBlockBytes = 16384 + 2048;
+size_t packed_weight_bytes(int64_t n, int64_t k);
+qerl_status launch_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
+                        cudaStream_t s);
+
 // aqn.cu
 qerl_status launch_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, uint32_t stream_id,
                               uint64_t counter, cudaStream_t s);
@@ -31,8 +37,7 @@ qerl_status launch_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, u
 struct LinearArgs {
   const void* x;
   int64_t m, k, ldx, n;
-  const uint8_t* codes;
-  const uint8_t* scales;
+  const uint8_t* wpacked;
   const float* tensor_scale;
   const float* z;
   const void* A;

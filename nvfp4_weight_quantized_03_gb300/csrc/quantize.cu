@@ -152,7 +152,51 @@ int grid_for_rows(int64_t n) {
   return g < 1 ? 1 : static_cast<int>(g);
 }
 
+// Packed (kernel-native) weight layout for the linear: one contiguous
+// 18432-byte block per (128-row tile t, 256-wide K stage g), blocks in
+// (t, g) order.  Block bytes [0, 16384): row r's 128 code bytes (K range
+// g*256 .. +255, two codes per byte, even k in the low nibble) at r * 128,
+// 16-byte chunk c stored at chunk position c ^ (r % 8).  Bytes [16384, 18432):
+// E4M3 scale pair p (16-blocks 2p, 2p+1 of the stage) of row r at
+// 16384 + p * 256 + r * 2.  Rows >= n and K past k are zero.
+__global__ void __launch_bounds__(kThreads) pack_kernel(const uint8_t* __restrict__ codes,
+                                                         const uint8_t* __restrict__ scales, int n, int k,
+                                                         uint8_t* __restrict__ packed) {
+  const int g = blockIdx.x, t = blockIdx.y;
+  const int kg = gridDim.x;
+  uint8_t* blk = packed + (static_cast<int64_t>(t) * kg + g) * kPackedBlockBytes;
+  const int row_bytes = k / 2, srow_bytes = k / 16;
+  for (int idx = threadIdx.x; idx < 128 * 8; idx += kThreads) {
+    const int r = idx >> 3, c = idx & 7;
+    const int nrow = t * 128 + r;
+    const int off = g * 128 + c * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (nrow < n && off < row_bytes) v = __ldg(reinterpret_cast<const uint4*>(codes + static_cast<int64_t>(nrow) * row_bytes + off));
+    *reinterpret_cast<uint4*>(blk + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+  }
+  for (int idx = threadIdx.x; idx < 8 * 128; idx += kThreads) {
+    const int pr = idx >> 7, r = idx & 127;
+    const int nrow = t * 128 + r;
+    const int off = g * 16 + 2 * pr;
+    unsigned short v = 0;
+    if (nrow < n && off < srow_bytes)
+      v = __ldg(reinterpret_cast<const unsigned short*>(scales + static_cast<int64_t>(nrow) * srow_bytes + off));
+    *reinterpret_cast<unsigned short*>(blk + 16384 + pr * 256 + r * 2) = v;
+  }
+}
+
 }  // namespace
+
+size_t packed_weight_bytes(int64_t n, int64_t k) {
+  return static_cast<size_t>((n + 127) / 128) * static_cast<size_t>((k + 255) / 256) * kPackedBlockBytes;
+}
+
+qerl_status launch_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
+                        cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((k + 255) / 256), static_cast<unsigned>((n + 127) / 128));
+  pack_kernel<<<grid, kThreads, 0, s>>>(codes, scales, static_cast<int>(n), static_cast<int>(k), packed);
+  return cuda_status(cudaGetLastError());
+}
 
 qerl_status launch_amax(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w, unsigned* amax_bits,
                         cudaStream_t s) {

@@ -34,8 +34,9 @@ def main():
     sets = []
     for _ in range(a.copies):
         W = torch.randn(a.n, a.k, device=dev) * 0.02
-        sets.append(q.quantize(W))
-        del W
+        codes, scales, S = q.quantize(W)
+        sets.append((q.pack(codes, scales), S))
+        del W, codes, scales
     x = torch.randn(a.m, a.k, device=dev).to(torch.bfloat16)
     A = (torch.randn(a.r, a.k, device=dev) / a.k ** 0.5).to(torch.bfloat16) if a.r else None
     B = (torch.randn(a.n, a.r, device=dev) * 0.01).to(torch.bfloat16) if a.r else None
@@ -45,8 +46,8 @@ def main():
     ws = q.workspace(q.qerl_lora_linear_workspace_size(a.m, a.n, a.k, a.r))
 
     def call(i):
-        codes, scales, S = sets[i % a.copies]
-        q.check(q.qerl_lora_linear(x, codes, scales, S, z, A, B, a.alpha, y, ws))
+        wp, S = sets[i % a.copies]
+        q.check(q.qerl_lora_linear(x, wp, S, z, A, B, a.alpha, y, ws))
 
     for i in range(a.warmup):
         call(i)

@@ -67,11 +67,11 @@ no_gpu_only = pytest.mark.skipif(__import__("torch").cuda.is_available(),
 
 
 def _lin(L, **kw):
-    a = dict(x=0x1000, m=4, k=128, ldx=128, codes=0x2000, scales=0x3000, ts=0x4000, n=256, z=None, A=None,
+    a = dict(x=0x1000, m=4, k=128, ldx=128, w=0x2000, ts=0x4000, n=256, z=None, A=None,
              B=None, r=0, alpha=0.0, y=0x5000, ydt=q.QERL_BF16, ws=0x10000, wsb=1 << 30, stream=None)
     a.update(kw)
-    return L.qerl_lora_linear(a["x"], a["m"], a["k"], a["ldx"], a["codes"], a["scales"], a["ts"], a["n"], a["z"],
-                              a["A"], a["B"], a["r"], a["alpha"], a["y"], a["ydt"], a["ws"], a["wsb"], a["stream"])
+    return L.qerl_lora_linear(a["x"], a["m"], a["k"], a["ldx"], a["w"], a["ts"], a["n"], a["z"], a["A"], a["B"],
+                              a["r"], a["alpha"], a["y"], a["ydt"], a["ws"], a["wsb"], a["stream"])
 
 
 @no_gpu_only
@@ -89,14 +89,36 @@ def test_linear_validation(L):
     assert name(_lin(L, x=None)) == "QERL_ERR_INVALID_ARGUMENT"
     assert name(_lin(L, x=0x1008)) == "QERL_ERR_MISALIGNED"
     assert name(_lin(L, ldx=132)) == "QERL_ERR_MISALIGNED"
-    assert name(_lin(L, codes=0x2004)) == "QERL_ERR_MISALIGNED"
-    assert name(_lin(L, scales=0x3002)) == "QERL_ERR_MISALIGNED"
+    assert name(_lin(L, w=0x2004)) == "QERL_ERR_MISALIGNED"
+    assert name(_lin(L, w=None)) == "QERL_ERR_INVALID_ARGUMENT"
     assert name(_lin(L, z=0x8004)) == "QERL_ERR_MISALIGNED"
     assert name(_lin(L, ws=None)) == "QERL_ERR_WORKSPACE"
     need = L.qerl_lora_linear_workspace_size(4, 256, 128, 0)
     assert name(_lin(L, wsb=need - 1)) == "QERL_ERR_WORKSPACE"
     assert name(_lin(L, ws=0x10080)) == "QERL_ERR_MISALIGNED"
     assert _lin(L, m=0) == 0 and _lin(L, n=0) == 0  # empty problems are no-ops
+
+
+@no_gpu_only
+def test_pack_validation(L):
+    E = q.STATUS_NAMES
+    pk = lambda **kw: L.qerl_nvfp4_pack(kw.get("codes", 0x2000), kw.get("scales", 0x3000), kw.get("n", 4),
+                                        kw.get("k", 128), kw.get("packed", 0x8000), None)
+    assert E[pk(k=96)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[pk(n=-1)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[pk(packed=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[pk(codes=0x2008)] == "QERL_ERR_MISALIGNED"
+    assert E[pk(scales=0x3002)] == "QERL_ERR_MISALIGNED"
+    assert pk(n=0) == 0
+
+
+def test_packed_size(L):
+    # one 18432-byte block per 128 rows x 256 K, partial tiles rounded up
+    assert L.qerl_nvfp4_packed_size(128, 256) == 18432
+    assert L.qerl_nvfp4_packed_size(129, 256) == 2 * 18432
+    assert L.qerl_nvfp4_packed_size(3584, 3584) == 28 * 14 * 18432
+    assert L.qerl_nvfp4_packed_size(512, 320) == 4 * 2 * 18432
+    assert L.qerl_nvfp4_packed_size(0, 256) == 0
 
 
 def test_workspace_size_grows(L):

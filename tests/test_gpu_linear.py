@@ -37,7 +37,7 @@ def _quantized(q, orc, n, k, seed):
         assert np.array_equal(codes.cpu().numpy(), oc)
         assert np.array_equal(scales.cpu().numpy(), osc)
         assert S.item() == float(oS)
-        _QCACHE[key] = (codes, scales, S, oc, osc, oS)
+        _QCACHE[key] = (q.pack(codes, scales), S, oc, osc, oS)
     return _QCACHE[key]
 
 
@@ -52,7 +52,7 @@ class Case:
         self.B_bits = wl.lora_B_bits(n, r, seed, 3) if r else None
         self.z = wl.noise_vector(k, sigma, seed, 4) if sigma else None
         self.alpha = 2.0 * r
-        self.codes, self.scales, self.S, self.oc, self.osc, self.oS = _quantized(q, orc, n, k, seed)
+        self.wp, self.S, self.oc, self.osc, self.oS = _quantized(q, orc, n, k, seed)
         self.x = dev_bf16(self.x_bits)
         self.A = dev_bf16(self.A_bits) if r else None
         self.B = dev_bf16(self.B_bits) if r else None
@@ -61,8 +61,7 @@ class Case:
     def gpu(self, q, out_dtype=torch.bfloat16, ws=None):
         y = torch.full((self.m, self.n), float("nan"), dtype=out_dtype, device="cuda")
         ws = ws if ws is not None else q.workspace(q.qerl_lora_linear_workspace_size(self.m, self.n, self.k, self.r))
-        q.check(q.qerl_lora_linear(self.x, self.codes, self.scales, self.S, self.zd, self.A, self.B, self.alpha,
-                                   y, ws))
+        q.check(q.qerl_lora_linear(self.x, self.wp, self.S, self.zd, self.A, self.B, self.alpha, y, ws))
         assert q.qerl_read_status(ws) == 0
         return y
 
@@ -133,11 +132,10 @@ def test_linear_workspace_reuse_and_status(q, orc):
 def test_linear_empty(q):
     ws = q.workspace(256)
     x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
-    codes = torch.zeros((128, 32), dtype=torch.uint8, device="cuda")
-    scales = torch.zeros((128, 4), dtype=torch.uint8, device="cuda")
+    wp = torch.zeros(q.qerl_nvfp4_packed_size(128, 64), dtype=torch.uint8, device="cuda")
     S = torch.ones(1, device="cuda")
     y = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
-    assert q.qerl_lora_linear(x, codes, scales, S, None, None, None, 0.0, y, ws) == 0
+    assert q.qerl_lora_linear(x, wp, S, None, None, None, 0.0, y, ws) == 0
 
 
 def _sample_cols(n, cnt, seed):

@@ -31,7 +31,8 @@ class Problem:
     def __init__(self, q, m, n, k, r, sigma, seed):
         self.m, self.n, self.k, self.r = m, n, k, r
         self.W = wl.weight_f32(n, k, seed, 0)
-        self.codes, self.scales, self.S = q.quantize(torch.from_numpy(self.W).cuda())
+        codes, scales, self.S = q.quantize(torch.from_numpy(self.W).cuda())
+        self.wp = q.pack(codes, scales)
         self.x_bits = wl.activations_bits(m, k, seed, 1)
         self.A_bits = wl.lora_A_bits(r, k, seed, 2) if r else None
         self.B_bits = wl.lora_B_bits(n, r, seed, 3) if r else None
@@ -48,15 +49,13 @@ class Problem:
     def with_workspace(self, q, dtype):
         y = self.out(dtype)
         ws = q.workspace(q.qerl_lora_linear_workspace_size(self.m, self.n, self.k, self.r))
-        q.check(q.qerl_lora_linear(self.x, self.codes, self.scales, self.S, self.zd, self.A, self.B, self.alpha, y,
-                                   ws))
+        q.check(q.qerl_lora_linear(self.x, self.wp, self.S, self.zd, self.A, self.B, self.alpha, y, ws))
         assert q.qerl_read_status(ws) == 0
         return y
 
     def noalloc(self, q, dtype):
         y = self.out(dtype)
-        q.check(q.qerl_lora_linear_noalloc(self.x, self.codes, self.scales, self.S, self.zd, self.A, self.B,
-                                           self.alpha, y))
+        q.check(q.qerl_lora_linear_noalloc(self.x, self.wp, self.S, self.zd, self.A, self.B, self.alpha, y))
         torch.cuda.synchronize()
         return y
 
@@ -87,10 +86,9 @@ def test_noalloc_two_calls_match_workspace_entry_point(q, orc):
 def test_noalloc_rejects_oversize_problem(q):
     m, n, k = 1024, 128, 8192  # staged activations alone need 16 MiB
     x = torch.zeros((m, k), dtype=torch.bfloat16, device="cuda")
-    codes = torch.zeros((n, k // 2), dtype=torch.uint8, device="cuda")
-    scales = torch.zeros((n, k // 16), dtype=torch.uint8, device="cuda")
+    wp = torch.zeros(q.qerl_nvfp4_packed_size(n, k), dtype=torch.uint8, device="cuda")
     S = torch.ones(1, device="cuda")
     y = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
-    assert q.qerl_lora_linear_noalloc(x, codes, scales, S, None, None, None, 0.0, y) == QERL_ERR_WORKSPACE
+    assert q.qerl_lora_linear_noalloc(x, wp, S, None, None, None, 0.0, y) == QERL_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.isnan(y.float()).all()
