@@ -201,6 +201,68 @@ def linear_flops(lin, m, r=RANK_R):
     return 2.0 * m * lin.n * lin.k + 2.0 * m * lin.k * r + 2.0 * m * r * lin.n
 
 
+# Dominant launch of the decode step: the gate-shaped linear (the largest of
+# the seven, with up and down) at M = 8.  DRAM traffic of one such call
+# (mma_kernel + prep_kernel), from the ncu capture summarized in
+# profiles/mma_kernel_decode_gate_m8.md; None until a capture of the current
+# kernels exists.
+DOMINANT = ("gate", 8)
+DOMINANT_TRAFFIC_BYTES = 39942656  # 39.615 MB (mma_kernel) + 0.327 MB (prep_kernel) DRAM reads, 0 writes
+
+
+def dominant_call(q, layers, acts, hbm_peak, reps=64):
+    """Average per-call time of the dominant linear: a graph of back-to-back
+    calls timed with CUDA events on the replaying stream, weights rotating over
+    the layer copies (cold in L2)."""
+    names = [lin.name for lin in wl.QWEN_7B]
+    li, m = names.index(DOMINANT[0]), DOMINANT[1]
+    a = acts[DECODE_MS.index(m)]
+    lin = wl.QWEN_7B[li]
+    y = a.y[li]
+    g = lin.group
+
+    def call(i):
+        ql = layers[i % len(layers)][li]
+        q.check(q.qerl_lora_linear(a.x[g], ql.wp, ql.S, a.z[g], ql.A, ql.B, ALPHA, y, a.ws), "qerl_lora_linear")
+
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    # The calls are captured into one graph (no host gaps between them); the
+    # events on the replaying stream bracket all of them.
+    g_ = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    with torch.cuda.graph(g_, stream=cs):
+        for i in range(reps):
+            call(i)
+    g_.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g_.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    q.check(q.qerl_read_status(a.ws), "dominant call status")
+    t_ms = e0.elapsed_time(e1) / reps
+    alg = linear_algorithmic_bytes(lin, m)
+    achieved = alg / (t_ms * 1e-3) / 1e9
+    return {
+        "bound": "hbm",
+        "kernel": f"qerl_lora_linear call (prep_kernel + mma_kernel<1>), Qwen2.5-7B {lin.name} "
+                  f"{lin.n}x{lin.k}, M={m}, r={RANK_R}",
+        "achieved": round(achieved, 1),
+        "peak": hbm_peak,
+        "peak_source": "measured hbm_gbs (MEASURED_PEAKS.json)",
+        "unit": "GB/s",
+        "frac": round(achieved / hbm_peak, 4),
+        "traffic": DOMINANT_TRAFFIC_BYTES,
+        "algorithmic_bytes_per_call": int(alg),
+        "us_per_call": round(t_ms * 1e3, 3),
+        "timing": f"CUDA events around one graph replay of {reps} back-to-back calls on the launching "
+                  f"stream, weights rotating over {len(layers)} layer copies (> L2)",
+    }
+
+
 # ---------------------------------------------------------------- our arm
 
 def bench_ours(args):
@@ -314,6 +376,9 @@ def bench_ours(args):
     extra_prefill = bench_prefill(q, args, bf16_peak) if not args.skip_extra else None
     extra_quant = bench_quantize(q, hbm_peak) if not args.skip_extra else None
 
+    # ---- the dominant launch, timed per call
+    roofline = dominant_call(q, layers, acts, hbm_peak)
+
     # ---- end to end through the public API with host buffers (no graph)
     e2e = bench_e2e(q, layers, acts, args, copy_for, sigma_for, step_wbytes, world, barrier)
 
@@ -342,15 +407,12 @@ def bench_ours(args):
             "parallelism": f"replicas x{world}",
         },
         "per_m": per_m,
-        "roofline": {
-            "bound": "hbm",
-            "kernel": "decode linear path per (M, layer) sub-step: 7 x (prep + tcgen05 dequant-MMA) + AQN sampler",
+        "roofline": roofline,
+        "substep_roofline": {
+            "what": "whole decode sub-step (AQN sampler + 7 linears) per (M, layer), graph replay",
             "achieved": round(sub_bytes_total / (sub_time_total * 1e-3) / 1e9, 1),
-            "peak": hbm_peak,
-            "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)",
             "unit": "GB/s",
             "frac": round(sub_bytes_total / (sub_time_total * 1e-3) / 1e9 / hbm_peak, 4),
-            "traffic": None,
         },
         "gpu_launches": launches_per_step * K,
         "clocks": clk,

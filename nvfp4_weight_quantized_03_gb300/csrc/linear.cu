@@ -558,6 +558,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     if (lane == 0)
       for (int i = 0; i < min(kPrefetch, nraw); ++i)
         bulk_prefetch_l2(wtile + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes);
+    auto xbytes_of = [&](int rst) {
+      return coupled ? static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128) : 0u;
+    };
     if (coupled) griddep_wait();
     if (lane == 0) {
       for (int i = 0, s = 0; i < nraw; ++i) {
@@ -566,8 +569,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const uint32_t ph = (i / RS) & 1;
         if (!mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status)) break;
         const int rst = rb + i;
-        const uint32_t xbytes =
-            coupled ? static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128) : 0u;
+        const uint32_t xbytes = xbytes_of(rst);
         mbar_arrive_expect_tx_a(raw_full(s), kRawSlotBytes + xbytes);
         bulk_load(sbase + p.off_raw + s * kRawSlotBytes, wtile + static_cast<int64_t>(rst) * kRawSlotBytes,
                   kRawSlotBytes, raw_full(s));
@@ -818,16 +820,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int nacc = min(NI, nmma);
     for (int c = c0; c < c0 + cols; c += 8) {
-      float v[8], l[8];
-      tmem_ld_x8(tmem_base + lane_off + c, v);
+      // All accumulators' (and the LoRA accumulator's) columns first, one wait.
+      float w[kMaxIssuers][8], l[8];
+#pragma unroll
+      for (int a = 0; a < kMaxIssuers; ++a)
+        if (a < nacc) tmem_ld_x8(tmem_base + static_cast<uint32_t>(a * p.n_tok) + lane_off + c, w[a]);
       if (do_lora) tmem_ld_x8(d_lora + lane_off + c, l);
       tmem_ld_wait();
-      for (int a = 1; a < nacc; ++a) {
-        float w8[8];
-        tmem_ld_x8(tmem_base + static_cast<uint32_t>(a * p.n_tok) + lane_off + c, w8);
-        tmem_ld_wait();
+      float v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] += w8[e];
+      for (int e = 0; e < 8; ++e) {
+        v[e] = w[0][e];
+#pragma unroll
+        for (int a = 1; a < kMaxIssuers; ++a)
+          if (a < nacc) v[e] += w[a][e];
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
