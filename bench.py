@@ -173,6 +173,8 @@ class Activations:
             off += k
         self.y = [torch.empty((m, lin.n), dtype=torch.bfloat16, device="cuda") for lin in shapes]
         need = max(q.qerl_lora_linear_workspace_size(m, lin.n, lin.k, RANK_R) for lin in shapes)
+        # a group of up to three rank-RANK_R linears needs room for three LoRA partial sums
+        need += 2 * q.qerl_lora_linear_workspace_size(m, 0, max(lin.k for lin in shapes), RANK_R)
         self.ws = q.workspace(need)
 
     def io_bytes(self):
@@ -181,14 +183,24 @@ class Activations:
         return h2d, d2h
 
 
+# Linears of one input run as one grouped launch: {q,k,v}, {o}, {gate,up}, {down}.
+GROUPED = True
+
+
 def run_substep(q, layer, act, sigma, counter):
     """One decode batch through the layer: the AQN noise of all four groups (one sampler
-    launch over the concatenated channels) + 7 linears, all on the current stream."""
+    launch over the concatenated channels) + the 7 linears (4 grouped launches, or 7
+    single calls), all on the current stream."""
     q.check(q.qerl_aqn_sample(act.z_all, sigma, 0, 0, counter), "qerl_aqn_sample")
-    for ql, y in zip(layer, act.y):
-        g = ql.lin.group
-        q.check(q.qerl_lora_linear(act.x[g], ql.wp, ql.S, act.z[g], ql.A, ql.B, ALPHA, y, act.ws),
-                "qerl_lora_linear")
+    if not GROUPED:
+        for ql, y in zip(layer, act.y):
+            g = ql.lin.group
+            q.check(q.qerl_lora_linear(act.x[g], ql.wp, ql.S, act.z[g], ql.A, ql.B, ALPHA, y, act.ws),
+                    "qerl_lora_linear")
+        return
+    for g in wl.NOISE_GROUPS:
+        members = [(ql.wp, ql.S, ql.A, ql.B, ALPHA, y) for ql, y in zip(layer, act.y) if ql.lin.group == g]
+        q.check(q.qerl_lora_linear_group(act.x[g], act.z[g], members, act.ws), "qerl_lora_linear_group")
 
 
 def linear_algorithmic_bytes(lin, m, r=RANK_R):
@@ -382,7 +394,8 @@ def bench_ours(args):
     # ---- end to end through the public API with host buffers (no graph)
     e2e = bench_e2e(q, layers, acts, args, copy_for, sigma_for, step_wbytes, world, barrier)
 
-    launches_per_step = len(DECODE_MS) * (1 + 2 * len(shapes))
+    calls = len(wl.NOISE_GROUPS) if GROUPED else len(shapes)
+    launches_per_step = len(DECODE_MS) * (1 + 2 * calls)
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -403,7 +416,9 @@ def bench_ours(args):
             "weight_bytes_per_step": int(step_wbytes),
             "l2": f"weights rotate over {N_COPIES} distinct layer copies "
                   f"({N_COPIES * layer_wbytes / 1e9:.2f} GB) > 129 MB L2; activations stay hot",
-            "launch": "one CUDA graph per (stage, M): 1 AQN sampler launch (4 groups) + 7 linears",
+            "launch": ("one CUDA graph per (stage, M): 1 AQN sampler launch (4 groups) + "
+                       + ("4 grouped linear launches {q,k,v},{o},{gate,up},{down}" if GROUPED
+                          else "7 single-linear calls")),
             "parallelism": f"replicas x{world}",
         },
         "per_m": per_m,
@@ -631,7 +646,11 @@ def main():
     ap.add_argument("--skip-extra", action="store_true", help="skip the prefill and quantizer measurements")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ungrouped", action="store_true", help="seven single-linear calls per layer instead of four "
+                    "grouped launches")
     args = ap.parse_args()
+    global GROUPED
+    GROUPED = not args.ungrouped
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

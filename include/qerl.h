@@ -196,6 +196,38 @@ QERL_API qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64
                                       const void* B, int r, float alpha, void* y, int y_dtype, void* workspace,
                                       size_t ws_bytes, void* stream);
 
+/* ========================================================================
+ * Several linears of one input in one launch (q/k/v of an attention block,
+ * gate/up of an MLP; no counterpart in the pages, which describe one layer at
+ * a time).  Up to 4 linears share x, z and k; each has its own packed
+ * weights, tensor scale, LoRA adapters (A, B, r, alpha; A/B NULL or r == 0:
+ * none) and output y [m][n] of its y_dtype.  Every output equals what
+ * qerl_lora_linear gives for that linear alone (up to fp32 summation order).
+ * One noise/staging pass serves all of them and their weight tiles run in one
+ * grid, so small linears (k/v) do not pay a launch of their own.
+ * `linears` is a host array of `count` descriptors (1 <= count <= 4), read
+ * during the call.  Argument rules as for qerl_lora_linear, per linear; a
+ * linear with n == 0 is skipped.  workspace: at least
+ * qerl_lora_linear_group_workspace_size(m, k, linears, count) bytes.
+ * ======================================================================== */
+typedef struct qerl_linear_desc {
+  const uint8_t* wpacked;     /* qerl_nvfp4_pack output for this n x k weight */
+  const float* tensor_scale;  /* device float S */
+  int64_t n;                  /* output features */
+  const void* A;              /* bf16 [r][k] or NULL */
+  const void* B;              /* bf16 [n][r] or NULL */
+  int r;
+  float alpha;
+  void* y;                    /* device [m][n] */
+  int y_dtype;                /* QERL_BF16 or QERL_F32 */
+} qerl_linear_desc;
+
+QERL_API size_t qerl_lora_linear_group_workspace_size(int64_t m, int64_t k, const qerl_linear_desc* linears,
+                                                      int count);
+QERL_API qerl_status qerl_lora_linear_group(const void* x, int64_t m, int64_t k, int64_t ldx, const float* z,
+                                            const qerl_linear_desc* linears, int count, void* workspace,
+                                            size_t ws_bytes, void* stream);
+
 /* The same linear for callers that cannot allocate device memory where they
  * run it (a runtime with a fixed memory pool, a latency-critical loop that must
  * not enter the CUDA allocator, a hard memory budget).  No counterpart in the

@@ -17,6 +17,7 @@ The functions named like the C entry points take torch tensors:
     qerl_nvfp4_pack(codes, scales, packed)
     qerl_lora_linear(x, wpacked, tensor_scale, z, A, B, alpha, y, workspace)
     qerl_lora_linear_noalloc(x, wpacked, tensor_scale, z, A, B, alpha, y)
+    qerl_lora_linear_group(x, z, [(wpacked, tensor_scale, A, B, alpha, y), ...], workspace)
     qerl_read_status(workspace)
 
 and return the qerl_status integer (QERL_OK == 0).  `check()` turns a
@@ -38,8 +39,16 @@ __all__ = [
     "qerl_nvfp4_quantize_workspace_size", "qerl_aqn_sigma", "qerl_aqn_stage", "qerl_aqn_sample",
     "qerl_nvfp4_packed_size", "qerl_nvfp4_pack", "pack",
     "qerl_lora_linear_workspace_size", "qerl_lora_linear", "qerl_lora_linear_noalloc", "qerl_read_status",
+    "qerl_lora_linear_group", "qerl_lora_linear_group_workspace_size", "LinearDesc",
     "quantize", "lora_linear", "workspace",
 ]
+
+class LinearDesc(ctypes.Structure):
+    """Mirror of qerl_linear_desc (include/qerl.h)."""
+    _fields_ = [("wpacked", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p), ("n", ctypes.c_int64),
+                ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("r", ctypes.c_int), ("alpha", ctypes.c_float),
+                ("y", ctypes.c_void_p), ("y_dtype", ctypes.c_int)]
+
 
 QERL_OK = 0
 QERL_F32, QERL_BF16 = 0, 1
@@ -102,6 +111,11 @@ def lib():
             L.qerl_lora_linear.restype = ctypes.c_int
             L.qerl_lora_linear.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_int,
                                            ctypes.c_float, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+            L.qerl_lora_linear_group_workspace_size.restype = ctypes.c_size_t
+            L.qerl_lora_linear_group_workspace_size.argtypes = [_i64, _i64, ctypes.POINTER(LinearDesc), ctypes.c_int]
+            L.qerl_lora_linear_group.restype = ctypes.c_int
+            L.qerl_lora_linear_group.argtypes = [_vp, _i64, _i64, _i64, _vp, ctypes.POINTER(LinearDesc), ctypes.c_int,
+                                                 _vp, ctypes.c_size_t, _vp]
             L.qerl_lora_linear_noalloc.restype = ctypes.c_int
             L.qerl_lora_linear_noalloc.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
                                                    ctypes.c_int, ctypes.c_float, _vp, ctypes.c_int, _vp]
@@ -222,6 +236,31 @@ def qerl_lora_linear_noalloc(x, wpacked, tensor_scale, z, A, B, alpha, y, stream
     ydt = QERL_F32 if y.dtype == torch.float32 else QERL_BF16
     return lib().qerl_lora_linear_noalloc(_p(x), m, k, x.stride(0), _p(wpacked), _p(tensor_scale), n, _p(z),
                                           _p(A), _p(B), r, float(alpha), _p(y), ydt, _stream(stream))
+
+
+def _descs(linears):
+    """[(wpacked, tensor_scale, A, B, alpha, y), ...] -> ctypes array of LinearDesc."""
+    arr = (LinearDesc * len(linears))()
+    for d, (wp, ts, A, B, alpha, y) in zip(arr, linears):
+        d.wpacked, d.tensor_scale, d.n = _p(wp), _p(ts), y.shape[1]
+        d.A, d.B, d.r = _p(A), _p(B), 0 if A is None else A.shape[0]
+        d.alpha, d.y = float(alpha), _p(y)
+        d.y_dtype = QERL_F32 if y.dtype == torch.float32 else QERL_BF16
+    return arr
+
+
+def qerl_lora_linear_group_workspace_size(m: int, k: int, linears) -> int:
+    arr = _descs(linears)
+    return lib().qerl_lora_linear_group_workspace_size(int(m), int(k), arr, len(arr))
+
+
+def qerl_lora_linear_group(x, z, linears, workspace, stream=None) -> int:
+    """Up to four linears of one input x [m, k] (bf16) and noise z: linears is a list of
+    (wpacked, tensor_scale, A, B, alpha, y) with y [m, n_i]; one launch for all."""
+    m, k = x.shape
+    arr = _descs(linears)
+    return lib().qerl_lora_linear_group(_p(x), m, k, x.stride(0), _p(z), arr, len(arr), _p(workspace),
+                                        _nbytes(workspace), _stream(stream))
 
 
 def qerl_read_status(workspace, stream=None) -> int:

@@ -126,48 +126,94 @@ qerl_status qerl_nvfp4_pack(const uint8_t* codes, const uint8_t* scales, int64_t
 size_t qerl_lora_linear_workspace_size(int64_t m, int64_t n, int64_t k, int r) {
   (void)n;
   if (m < 0 || k < 0 || r < 0) return 0;
-  return qerl::linear_workspace_bytes(m, k, r);
+  return qerl::linear_workspace_bytes(m, k, &r, 1);
+}
+
+size_t qerl_lora_linear_group_workspace_size(int64_t m, int64_t k, const qerl_linear_desc* linears, int count) {
+  if (m < 0 || k < 0 || count < 1 || count > 4 || linears == nullptr) return 0;
+  int ranks[4] = {0, 0, 0, 0};
+  for (int i = 0; i < count; ++i) ranks[i] = linears[i].r > 0 ? linears[i].r : 0;
+  return qerl::linear_workspace_bytes(m, k, ranks, count);
+}
+
+qerl_status qerl_lora_linear_group(const void* x, int64_t m, int64_t k, int64_t ldx, const float* z,
+                                   const qerl_linear_desc* linears, int count, void* workspace, size_t ws_bytes,
+                                   void* stream) {
+  if (linears == nullptr || count < 1 || count > 4) return QERL_ERR_INVALID_ARGUMENT;
+  if (m < 0 || k <= 0 || ldx < k) return QERL_ERR_INVALID_ARGUMENT;
+  if (k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (k > 65536 || m > INT32_MAX || m * k > (int64_t{1} << 40)) return QERL_ERR_UNSUPPORTED_SHAPE;
+  qerl::LinearArgs a{};
+  int ranks[4] = {0, 0, 0, 0};
+  int64_t total_n = 0;
+  for (int i = 0; i < count; ++i) {
+    const qerl_linear_desc& d = linears[i];
+    int r = d.r;
+    if (d.n < 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
+    if (d.y_dtype != QERL_BF16 && d.y_dtype != QERL_F32) return QERL_ERR_INVALID_ARGUMENT;
+    if ((d.A == nullptr) != (d.B == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
+    if (r > 0 && d.A == nullptr) r = 0;
+    if (d.A != nullptr && r == 0) return QERL_ERR_INVALID_ARGUMENT;
+    if (r > 128 || r % 8 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+    if (d.n > INT32_MAX) return QERL_ERR_UNSUPPORTED_SHAPE;
+    total_n += d.n;
+    ranks[i] = r;
+    a.lin[i].wpacked = d.wpacked;
+    a.lin[i].tensor_scale = d.tensor_scale;
+    a.lin[i].n = d.n;
+    a.lin[i].A = r > 0 ? d.A : nullptr;
+    a.lin[i].B = r > 0 ? d.B : nullptr;
+    a.lin[i].r = r;
+    a.lin[i].alpha = d.alpha;
+    a.lin[i].y = d.y;
+    a.lin[i].y_f32 = d.y_dtype == QERL_F32;
+  }
+  if (m == 0 || total_n == 0) return QERL_OK;
+  if (x == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || ldx % 8 != 0) return QERL_ERR_MISALIGNED;
+  if (z != nullptr && !aligned(z, 16)) return QERL_ERR_MISALIGNED;
+  // Linears with no output features are dropped from the launch.
+  int nl = 0;
+  for (int i = 0; i < count; ++i) {
+    const qerl_linear_desc& d = linears[i];
+    if (d.n == 0) continue;
+    if (d.wpacked == nullptr || d.tensor_scale == nullptr || d.y == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+    if (!aligned(d.wpacked, 16)) return QERL_ERR_MISALIGNED;
+    if (d.y_dtype == QERL_F32 ? !aligned(d.y, 4) : !aligned(d.y, 2)) return QERL_ERR_MISALIGNED;
+    if (ranks[i] > 0 && (!aligned(d.A, 16) || !aligned(d.B, 16))) return QERL_ERR_MISALIGNED;
+    a.lin[nl] = a.lin[i];
+    ranks[nl] = ranks[i];
+    ++nl;
+  }
+  qerl_status st = check_ws(workspace, ws_bytes, qerl::linear_workspace_bytes(m, k, ranks, nl));
+  if (st != QERL_OK) return st;
+  a.nlin = nl;
+  a.x = x;
+  a.m = m;
+  a.k = k;
+  a.ldx = ldx;
+  a.z = z;
+  a.workspace = workspace;
+  a.ws_bytes = ws_bytes;
+  return qerl::launch_lora_linear(a, as_stream(stream));
 }
 
 qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, const uint8_t* wpacked,
                              const float* tensor_scale, int64_t n, const float* z, const void* A, const void* B,
                              int r, float alpha, void* y, int y_dtype, void* workspace, size_t ws_bytes,
                              void* stream) {
-  if (m < 0 || n < 0 || k <= 0 || ldx < k || r < 0) return QERL_ERR_INVALID_ARGUMENT;
-  if (y_dtype != QERL_BF16 && y_dtype != QERL_F32) return QERL_ERR_INVALID_ARGUMENT;
-  if ((A == nullptr) != (B == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
-  if (r > 0 && A == nullptr) r = 0;
-  if (A != nullptr && r == 0) return QERL_ERR_INVALID_ARGUMENT;
-  if (k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
-  if (r > 128 || r % 8 != 0 || k > 65536) return QERL_ERR_UNSUPPORTED_SHAPE;
-  if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX || m * k > (int64_t{1} << 40))
-    return QERL_ERR_UNSUPPORTED_SHAPE;
-  if (m == 0 || n == 0) return QERL_OK;
-  if (x == nullptr || wpacked == nullptr || tensor_scale == nullptr || y == nullptr) return QERL_ERR_INVALID_ARGUMENT;
-  if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wpacked, 16)) return QERL_ERR_MISALIGNED;
-  if (z != nullptr && !aligned(z, 16)) return QERL_ERR_MISALIGNED;
-  if (y_dtype == QERL_F32 ? !aligned(y, 4) : !aligned(y, 2)) return QERL_ERR_MISALIGNED;
-  if (A != nullptr && (!aligned(A, 16) || !aligned(B, 16))) return QERL_ERR_MISALIGNED;
-  qerl_status st = check_ws(workspace, ws_bytes, qerl::linear_workspace_bytes(m, k, r));
-  if (st != QERL_OK) return st;
-  qerl::LinearArgs a{};
-  a.x = x;
-  a.m = m;
-  a.k = k;
-  a.ldx = ldx;
-  a.n = n;
-  a.wpacked = wpacked;
-  a.tensor_scale = tensor_scale;
-  a.z = z;
-  a.A = A;
-  a.B = B;
-  a.r = r;
-  a.alpha = alpha;
-  a.y = y;
-  a.y_f32 = y_dtype == QERL_F32;
-  a.workspace = workspace;
-  a.ws_bytes = ws_bytes;
-  return qerl::launch_lora_linear(a, as_stream(stream));
+  if (n < 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
+  qerl_linear_desc d;
+  d.wpacked = wpacked;
+  d.tensor_scale = tensor_scale;
+  d.n = n;
+  d.A = A;
+  d.B = B;
+  d.r = r;
+  d.alpha = alpha;
+  d.y = y;
+  d.y_dtype = y_dtype;
+  return qerl_lora_linear_group(x, m, k, ldx, z, &d, 1, workspace, ws_bytes, stream);
 }
 
 qerl_status qerl_read_status(void* workspace, void* stream) {

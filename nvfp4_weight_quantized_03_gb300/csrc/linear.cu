@@ -5,35 +5,48 @@
 //      + (alpha / r) * (x~ . A) . B                         ("Low-Rank Adaptation", Eq. 2)
 //   (QeRL digest, section 3.4)
 //
-// Two kernels per call:
+// Two kernels per launch; one launch serves up to four linears that share x,
+// z and K (q/k/v, gate/up), their 128-row weight tiles concatenated on the
+// grid's y axis.
 //
-// prep_kernel  (CUDA cores, tiny): the noise step and the LoRA down-projection.
+// prep_kernel  (CUDA cores, latency-bound, tiny): the noise step and the LoRA
+//   down-projection.
 //   - row tasks: x~ for one token row, staged as fp16 times 2^e_m with e_m
 //     chosen so the row's largest |x~| lies in [2^14, 2^15).  bf16 values
 //     (8 significant bits) are exact in fp16 (11 bits) over that window, so
 //     the tensor cores see x~ exactly (up to entries below 2^-28 of the row
-//     maximum); 2^-e_m is undone in the epilogue.
-//   - LoRA tasks: t = x~ . A over a K-slice, fp32, reduced with atomics.
+//     maximum); 2^-e_m is undone in the epilogue.  For decode (<= 128
+//     tokens) the rows are written as swizzled 64-wide K slabs that one bulk
+//     copy moves per weight stage.
+//   - LoRA tasks: t = x~ . A^T for a 16-row x 32-rank tile over one K group;
+//     the CTAs of a thread-block cluster split the group and reduce through
+//     distributed shared memory.  Groups are summed in order by the consumer:
+//     no atomics, bit-reproducible.
 //
-// mma_kernel  (tcgen05 + TMA, the hot loop): a 128-output-feature tile of W
-//   is the MMA's M side, tokens are the MMA's N side (16..256).
-//     warp 8      weight producer: per 256-wide K stage, TMA of the packed
-//                 codes (128 rows x 128 contiguous bytes, 128-byte swizzle)
-//                 and cp.async of the E4M3 scales (128 rows x 16 bytes).
-//     warps 0..7  dequant: E2M1 pairs -> fp16 pairs (cvt.f16x2.e2m1x2), times
-//                 the block scale (cvt.f16x2.e4m3x2) -- exact products --
-//                 written per 64-wide K stage in the 128-byte-swizzled K-major
-//                 layout the MMA reads; they also build the LoRA operands.
-//     warp 10     activation producer: TMA of the staged x~ tile per 64-wide
-//                 K stage (n_tok x 64 fp16).
-//     warp 9      MMA issuer: 4 x tcgen05.mma kind::f16 (M=128, N=n_tok,
-//                 K=16) per stage into an fp32 TMEM accumulator D; the LoRA
-//                 up-projection runs on the tensor cores too, into a second
-//                 accumulator D2 = B^T . (t_hi + t_lo), bf16 x bf16 -> fp32.
+// mma_kernel  (tcgen05, the hot loop): a 128-output-feature tile of W is the
+//   MMA's M side, tokens are its N side (16..256).  Weights arrive in the
+//   packed layout (one 18432-byte block per 128 rows x 256 K: swizzled E2M1
+//   codes + interleaved E4M3 scale pairs), one 1-D bulk copy per block.
+//     warp 12      weight producer: L2 prefetch a few stages ahead, bulk copy
+//                  of each block (and, for <= 64 tokens, the x~ slabs of the
+//                  same K range on the same barrier).
+//     warp 13      activation producer (more than 64 tokens): x~ per stage,
+//                  bulk-copied slabs up to 128 tokens, 2-D TMA tiles beyond.
+//     warps 0..7   dequant: E2M1 pairs -> fp16 pairs, times the block scale
+//                  (exact products).  Decode writes them to tensor memory as
+//                  the MMA's A operand (tcgen05.st); prefill writes them to
+//                  shared memory in the 128-byte-swizzled K-major layout.
+//     warps 8..11  MMA issuers (lane 0 each): tcgen05.mma kind::f16, K=16,
+//                  round-robin over 64-K stages, each into its own fp32 TMEM
+//                  accumulator so issue latency overlaps; the epilogue adds
+//                  them.
+//     warp 14      LoRA: sums the down-projection groups, splits t into bf16
+//                  hi + lo and issues the up-projection B . (t_hi + t_lo)^T
+//                  into a separate accumulator (bf16 x bf16 -> fp32).
 //   Epilogue (warps 0..7): y = S * 2^-e_m * D + (alpha/r) * D2, rounded to
-//   bf16.  Small-N decode shapes split K across a thread-block cluster; each
-//   CTA writes its scaled partial tile to shared memory and partner CTAs sum
-//   them through distributed shared memory (no global scratch, no atomics).
+//   bf16 or kept fp32.  When the weight tiles leave SMs idle, K is split
+//   across a cluster; each CTA writes its scaled partial tile to shared
+//   memory and the partners sum them through distributed shared memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -51,6 +64,7 @@ namespace {
 
 // ------------------------------------------------------------------ prep
 
+constexpr int kMaxLinears = 4;  // linears sharing one launch (x, z and K)
 constexpr int kPrepThreads = 256;
 constexpr int kLoraTileM = 16;   // token rows per LoRA tile
 constexpr int kLoraTileR = 32;   // ranks per LoRA tile
@@ -61,15 +75,17 @@ constexpr int kPrepMaxCluster = 8;
 struct PrepParams {
   const __nv_bfloat16* x;
   const float* z;
-  const __nv_bfloat16* A;  // [r][K]
+  const __nv_bfloat16* A[kMaxLinears];  // [r][K] per linear (LoRA down-projections)
+  int r[kMaxLinears];
+  float* t[kMaxLinears];  // [groups][M][r] partial sums of x~ . A^T over K group g, per linear
+  int tile_begin[kMaxLinears + 1];  // LoRA tiles of linear l: [tile_begin[l], tile_begin[l+1])
   __half* xs;   // staged x~ * 2^e_m: [M][K], or tiled (see xs_tile_offset)
   float* rinv;  // [M] 2^-e_m
-  float* t;     // [groups][M][r] partial sums of x~ . A^T over K group g
   int64_t ldx;
-  int M, K, r;
+  int M, K;
   int row_groups;    // blockIdx.y < row_groups: token rows blockIdx.y * cluster + blockIdx.x
   int lora_m_tiles;  // ceil(M / kLoraTileM)
-  int lora_tiles;    // lora_m_tiles * ceil(r / kLoraTileR)
+  int lora_tiles;    // all linears' tiles: sum of lora_m_tiles * ceil(r / kLoraTileR)
   int cluster;       // CTAs per cluster (gridDim.x)
   int groups;        // K groups; the cluster's CTAs split a group's K range
   int tiled_rows;    // > 0: x~ in the tiled layout for this many rows (>= M; rows past M are zero)
@@ -184,7 +200,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   // ---- LoRA tile: thread (rank = tid % 32, row pair = tid / 32): 2 accumulators.
   const int lt = blockIdx.y - p.row_groups;
   const int g = lt / p.lora_tiles;
-  const int tile = lt - g * p.lora_tiles;
+  int tile = lt - g * p.lora_tiles;
+  int li = 0;
+  while (tile >= p.tile_begin[li + 1]) ++li;
+  tile -= p.tile_begin[li];
+  const __nv_bfloat16* Am = p.A[li];
+  const int rr_ = p.r[li];
+  float* tout = p.t[li];
   const int mt = tile % p.lora_m_tiles;
   const int rt = tile / p.lora_m_tiles;
   const int ks = blockIdx.x;  // this CTA's rank in the cluster
@@ -229,8 +251,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     for (int v = tid; v < kLoraTileR * kLoraKc / 8; v += kPrepThreads) {
       const int jj = v >> 3, kk = (v & 7) * 8;
       float f[8];
-      if (rank0 + jj < p.r) {
-        uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(rank0 + jj) * p.K + k0 + kk));
+      if (rank0 + jj < rr_) {
+        uint4 raw = __ldg(reinterpret_cast<const uint4*>(Am + static_cast<int64_t>(rank0 + jj) * p.K + k0 + kk));
         const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
 #pragma unroll
         for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
@@ -270,7 +292,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     float v = 0.0f;
     for (int q = 0; q < p.cluster; ++q) v += ld_shared_cluster_f32(mapa_shared(part_s + 4u * idx, q));
     const int row = row0 + idx / kLoraTileR, rank = rank0 + idx % kLoraTileR;
-    if (row < p.M && rank < p.r) p.t[(static_cast<int64_t>(g) * p.M + row) * p.r + rank] = v;
+    if (row < p.M && rank < rr_) tout[(static_cast<int64_t>(g) * p.M + row) * rr_ + rank] = v;
   }
   cluster_sync_all();  // partners are done reading this CTA's partial tile
 }
@@ -296,16 +318,25 @@ constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kBarBytes = 1024;
 constexpr int kTmemCols = 512;
 
+// One linear of a launch: several linears sharing x (and K) run in one grid,
+// their 128-row tiles concatenated along gridDim.y.
+struct LinearSlot {
+  const uint8_t* wpacked;     // packed weight blocks (see qerl_nvfp4_pack)
+  const float* tensor_scale;  // S
+  const float* t;             // LoRA partial sums [t_groups][M][r]
+  void* y;                    // [M][N]
+  int N, r, y_f32;
+  int tile_begin;             // first tile index (gridDim.y) of this linear
+  float lora_scale;           // alpha / r
+};
+
 struct MmaParams {
   const __half* xs;        // staged x~ (fp16 * 2^e_m): tiled with kTmemA, else [M][K]
-  const uint8_t* wpacked;  // packed weight blocks (see qerl_nvfp4_pack)
-  const float* tensor_scale;
   const float* rinv;
-  const float* t;
-  const __nv_bfloat16* B;
-  void* y;
+  LinearSlot lin[kMaxLinears];
+  int nlin;
   int* status;
-  int M, N, K, r;
+  int M, K;
   int n_tok;       // tokens per tile (MMA N), multiple of 16, <= 256
   int split;       // K split across the cluster (gridDim.x), in weight stages
   int raw_stages;  // weight-stage ring depth
@@ -318,8 +349,11 @@ struct MmaParams {
   uint32_t raw_b_bytes;  // coupled: activation bytes per weight stage (kSub slabs)
   uint32_t col_lora, col_a;  // TMEM columns of the LoRA accumulator and of the A stages
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
-  float lora_scale;
-  int y_f32;
+};
+
+// The LoRA up-projection's B matrices, one TMA map per linear of the launch.
+struct BtMaps {
+  CUtensorMap m[kMaxLinears];
 };
 
 __host__ __device__ inline int lora_chunks(int r) { return (r + kLoraChunkK - 1) / kLoraChunkK; }
@@ -327,12 +361,12 @@ __host__ __device__ inline uint32_t lora_bytes(int r, int n_tok) {
   return r > 0 ? static_cast<uint32_t>(lora_chunks(r)) * (kBtChunkBytes + 2u * n_tok * 128u) : 0u;
 }
 
-__device__ __forceinline__ void store_out(const MmaParams& p, int m, int n, float v) {
-  const int64_t idx = static_cast<int64_t>(m) * p.N + n;
-  if (p.y_f32)
-    reinterpret_cast<float*>(p.y)[idx] = v;
+__device__ __forceinline__ void store_out(const LinearSlot& L, int m, int n, float v) {
+  const int64_t idx = static_cast<int64_t>(m) * L.N + n;
+  if (L.y_f32)
+    reinterpret_cast<float*>(L.y)[idx] = v;
   else
-    reinterpret_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(v);
+    reinterpret_cast<__nv_bfloat16*>(L.y)[idx] = __float2bfloat16_rn(v);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -347,8 +381,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 //   t_lo chunk c: n_tok rows m x 64 j  bf16  = bf16(t - t_hi)
 // so B^T . t_hi + B^T . t_lo carries t to ~16 significant bits.  The t tiles
 // are built by `nthr` threads (tid < nthr); zero past M and r.
-__device__ void build_t_tiles(const MmaParams& p, uint32_t base, int m0, int tid, int nthr) {
-  const int rc = lora_chunks(p.r);
+__device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t base, int m0, int tid, int nthr) {
+  const int rc = lora_chunks(L.r);
   const uint32_t thi = base + rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
   for (int idx = tid; idx < rc * p.n_tok * 8; idx += nthr) {
@@ -360,8 +394,8 @@ __device__ void build_t_tiles(const MmaParams& p, uint32_t base, int m0, int tid
     for (int e = 0; e < 8; ++e) {
       const int j = c * kLoraChunkK + g * 8 + e;
       float v = 0.0f;
-      if (m < p.M && j < p.r)
-        for (int g = 0; g < p.t_groups; ++g) v += __ldg(p.t + (static_cast<int64_t>(g) * p.M + m) * p.r + j);
+      if (m < p.M && j < L.r)
+        for (int g = 0; g < p.t_groups; ++g) v += __ldg(L.t + (static_cast<int64_t>(g) * p.M + m) * L.r + j);
       tv[e] = v;
     }
     uint32_t hw[4], lw[4];
@@ -380,12 +414,12 @@ __device__ void build_t_tiles(const MmaParams& p, uint32_t base, int m0, int tid
 
 // Same tiles from the partial sums staged in shared memory by bulk copies:
 // tstage[g][ml][j] = t_part[g][m0 + ml][j] for ml < rows.
-__device__ void build_t_tiles_staged(const MmaParams& p, uint32_t base, uint32_t tstage, int rows, int tid,
-                                     int nthr) {
-  const int rc = lora_chunks(p.r);
+__device__ void build_t_tiles_staged(const MmaParams& p, const LinearSlot& L, uint32_t base, uint32_t tstage,
+                                     int rows, int tid, int nthr) {
+  const int rc = lora_chunks(L.r);
   const uint32_t thi = base + rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
-  const uint32_t gstride = static_cast<uint32_t>(p.n_tok * p.r * 4);
+  const uint32_t gstride = static_cast<uint32_t>(p.n_tok * L.r * 4);
   for (int idx = tid; idx < rc * p.n_tok * 8; idx += nthr) {
     const int c = idx / (p.n_tok * 8), rem = idx - c * (p.n_tok * 8);
     const int ml = rem >> 3, g8 = rem & 7;
@@ -393,8 +427,8 @@ __device__ void build_t_tiles_staged(const MmaParams& p, uint32_t base, uint32_t
     float tv[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) tv[e] = 0.0f;
-    if (ml < rows && j0 < p.r) {  // r is a multiple of 8: all eight ranks valid
-      const uint32_t src = tstage + static_cast<uint32_t>((ml * p.r + j0) * 4);
+    if (ml < rows && j0 < L.r) {  // r is a multiple of 8: all eight ranks valid
+      const uint32_t src = tstage + static_cast<uint32_t>((ml * L.r + j0) * 4);
       for (int g = 0; g < p.t_groups; ++g) {
         const float4 a = lds128f(src + g * gstride), b = lds128f(src + g * gstride + 16);
         tv[0] += a.x;
@@ -423,9 +457,9 @@ __device__ void build_t_tiles_staged(const MmaParams& p, uint32_t base, uint32_t
 
 // TMA of the B^T chunks (rows n0..n0+127 of B [N][r], 64 ranks per chunk,
 // zero-filled past N and r) into `base`, completing on `bar`.
-__device__ __forceinline__ void load_bt_tiles(const MmaParams& p, const CUtensorMap* tm_bl, uint32_t base, int n0,
+__device__ __forceinline__ void load_bt_tiles(const LinearSlot& L, const CUtensorMap* tm_bl, uint32_t base, int n0,
                                               uint32_t bar) {
-  const int rc = lora_chunks(p.r);
+  const int rc = lora_chunks(L.r);
   mbar_arrive_expect_tx_a(bar, static_cast<uint32_t>(rc) * kBtChunkBytes);
   for (int c = 0; c < rc; ++c) tma_load_2d(base + c * kBtChunkBytes, tm_bl, c * kLoraChunkK, n0, bar);
 }
@@ -442,14 +476,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // D2 (+)= B^T . t_hi^T + B^T . t_lo^T over the rank dimension (bf16 x bf16 -> fp32).
-__device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, uint32_t base, uint32_t d2) {
-  const int rc = lora_chunks(p.r);
+__device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, const LinearSlot& L, uint32_t base, uint32_t d2) {
+  const int rc = lora_chunks(L.r);
   const uint32_t idesc = idesc_bf16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
   const uint32_t thi = base + rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
   uint32_t acc = 0;
   for (int c = 0; c < rc; ++c)
-    for (int kk = 0; kk < kLoraChunkK / 16 && c * kLoraChunkK + kk * 16 < p.r; ++kk) {
+    for (int kk = 0; kk < kLoraChunkK / 16 && c * kLoraChunkK + kk * 16 < L.r; ++kk) {
       const uint64_t ad = sw128_kmajor_desc(base + c * kBtChunkBytes + kk * 32);
       tc_mma_f16(d2, ad, sw128_kmajor_desc(thi + c * p.n_tok * 128 + kk * 32), idesc, acc);
       tc_mma_f16(d2, ad, sw128_kmajor_desc(tlo + c * p.n_tok * 128 + kk * 32), idesc, 1u);
@@ -466,7 +500,7 @@ __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, uint32_t bas
 // thread issues.
 template <bool kTmemA>
 __global__ void __launch_bounds__(kMmaThreads, 1)
-    mma_kernel(const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_bl,
+    mma_kernel(const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ BtMaps tm_bls,
                const MmaParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -490,7 +524,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split_idx = blockIdx.x;
-  const int n0 = blockIdx.y * kTileN;
+  // This CTA's linear: the one whose tile range holds blockIdx.y.
+  int gi = 0;
+  while (gi + 1 < p.nlin && static_cast<int>(blockIdx.y) >= p.lin[gi + 1].tile_begin) ++gi;
+  const LinearSlot& L = p.lin[gi];
+  const CUtensorMap* tm_bl = &tm_bls.m[gi];
+  const int n0 = (static_cast<int>(blockIdx.y) - L.tile_begin) * kTileN;
   const int m0 = blockIdx.z * p.n_tok;
   const int raw_total = (p.K + kRawK - 1) / kRawK;
   const int rb = static_cast<int>(static_cast<int64_t>(split_idx) * raw_total / p.split);
@@ -500,7 +539,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int mma_begin = kSub * rb;
   const int nmma = min(kSub * re, kb_total) - mma_begin;
   const int RS = p.raw_stages, AS = p.ab_stages, NI = p.issuers, BS = p.b_stages;
-  const bool do_lora = p.r > 0 && split_idx == 0;  // one CTA of a K-split cluster adds the LoRA term
+  const bool do_lora = L.r > 0 && split_idx == 0;  // one CTA of a K-split cluster adds the LoRA term
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
@@ -530,7 +569,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   }
   if (warp == kWeightWarp && lane == 0) {
     if (!kTmemA) tma_prefetch_desc(&tm_xs);
-    if (p.r > 0) tma_prefetch_desc(&tm_bl);
+    if (L.r > 0) tma_prefetch_desc(tm_bl);
   }
   tc_fence_before();
   __syncthreads();
@@ -548,7 +587,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // position and complete on the same barrier; they come from the
     // preceding kernel.
     const bool coupled = kTmemA && p.coupled;
-    const uint8_t* wtile = p.wpacked + static_cast<int64_t>(blockIdx.y) * raw_total * kRawSlotBytes;
+    const uint8_t* wtile = L.wpacked + static_cast<int64_t>(n0 / kTileN) * raw_total * kRawSlotBytes;
     const int kslabs = p.K / kStageK;
     // The copies into the ring are held for a stage's whole dequant + MMA
     // time, so the ring alone cannot cover HBM latency at full rate: the
@@ -662,14 +701,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (ii == 0 && do_lora && p.lora_early) {
         if (mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
           tc_fence_after();
-          issue_lora_mmas(p, lora_base, d_lora);
+          issue_lora_mmas(p, L, lora_base, d_lora);
         }
       }
       if (do_lora && !p.lora_early) {
         tc_commit(ring_free);  // the ring is idle once every mainloop MMA is done
         if (ii == 0 && mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
           tc_fence_after();
-          issue_lora_mmas(p, lora_base, d_lora);
+          issue_lora_mmas(p, L, lora_base, d_lora);
         }
       }
       tc_commit(acc_full);  // always, so the epilogue's wait completes even after an abort
@@ -765,7 +804,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
     if (do_lora && !p.lora_early) {
-      if (warp_wait(ring_free, 0, abort_flag, p.status)) build_t_tiles(p, lora_base, m0, threadIdx.x, 256);
+      if (warp_wait(ring_free, 0, abort_flag, p.status)) build_t_tiles(p, L, lora_base, m0, threadIdx.x, 256);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive_a(lora_full);
@@ -774,25 +813,25 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // ------------------------------------------------------------ LoRA operands
     if (do_lora) {
       if (p.lora_early) {
-        if (lane == 0) load_bt_tiles(p, &tm_bl, lora_base, n0, lora_full);
+        if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full);
         griddep_wait();  // t comes from the preceding kernel
         // Bulk-copy this tile's rows of every partial sum, then convert from
         // shared memory (scalar loads from L2 would serialize on latency).
         const int rows = min(p.n_tok, p.M - m0);
-        const uint32_t bytes = static_cast<uint32_t>(rows * p.r * 4);
+        const uint32_t bytes = static_cast<uint32_t>(rows * L.r * 4);
         const uint32_t tstage = sbase + p.off_tstage;
         if (lane == 0) {
           mbar_arrive_expect_tx_a(t_full, bytes * static_cast<uint32_t>(p.t_groups));
           for (int g = 0; g < p.t_groups; ++g)
-            bulk_load(tstage + static_cast<uint32_t>(g * p.n_tok * p.r * 4),
-                      p.t + (static_cast<int64_t>(g) * p.M + m0) * p.r, bytes, t_full);
+            bulk_load(tstage + static_cast<uint32_t>(g * p.n_tok * L.r * 4),
+                      L.t + (static_cast<int64_t>(g) * p.M + m0) * L.r, bytes, t_full);
         }
-        if (warp_wait(t_full, 0, abort_flag, p.status)) build_t_tiles_staged(p, lora_base, tstage, rows, lane, 32);
+        if (warp_wait(t_full, 0, abort_flag, p.status)) build_t_tiles_staged(p, L, lora_base, tstage, rows, lane, 32);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive_a(lora_full);
       } else if (warp_wait(ring_free, 0, abort_flag, p.status)) {
-        if (lane == 0) load_bt_tiles(p, &tm_bl, lora_base, n0, lora_full);
+        if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full);
       } else if (lane == 0) {
         mbar_arrive_a(lora_full);  // after an abort: keep the barrier count consistent
       }
@@ -805,7 +844,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // Row scales S * 2^-e_m come from the preceding kernel; the dequant above did not need them.
     griddep_wait();
     {
-      const float S = *p.tensor_scale;
+      const float S = *L.tensor_scale;
       for (int i = threadIdx.x; i < p.n_tok; i += 256)
         stsf(smv + 4u * i, (m0 + i < p.M) ? S * __ldg(p.rinv + m0 + i) : 0.0f);
     }
@@ -838,11 +877,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         float out = ok ? v[e] * ldsf(smv + 4u * (c + e)) : 0.0f;
-        if (do_lora && ok) out = fmaf(p.lora_scale, l[e], out);
+        if (do_lora && ok) out = fmaf(L.lora_scale, l[e], out);
         if (p.split > 1)
           stsf(part + 4u * ((c + e) * kTileN + nl), out);
-        else if (m0 + c + e < p.M && n < p.N)
-          store_out(p, m0 + c + e, n, out);
+        else if (m0 + c + e < p.M && n < L.N)
+          store_out(L, m0 + c + e, n, out);
       }
     }
   }
@@ -877,7 +916,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const float out[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (n0 + nl4 + e < p.N) store_out(p, m0 + ml, n0 + nl4 + e, out[e]);
+          if (n0 + nl4 + e < L.N) store_out(L, m0 + ml, n0 + nl4 + e, out[e]);
       }
     }
     cluster_sync_all();  // partners are done reading this CTA's partial tile
@@ -923,40 +962,57 @@ int sm_count() {
 }
 
 struct LinearLayout {
-  size_t xs, rinv, t, total;
+  size_t xs, rinv, t[kMaxLinears], total;
 };
 
 // Token tiles of up to 128 rows stage x~ in the tiled layout (one tile of
 // round_up(m, 16) rows); larger m keeps the row-major [m][k] layout.
 inline int tiled_rows_for(int64_t m) { return m <= 128 ? static_cast<int>((m + 15) / 16 * 16) : 0; }
 
-LinearLayout linear_layout(int64_t m, int64_t k, int r) {
+LinearLayout linear_layout(int64_t m, int64_t k, const int* ranks, int nlin) {
   LinearLayout L;
   L.xs = kWsHeaderBytes;
   const int tr = tiled_rows_for(m);
   const size_t xs_bytes =
       tr > 0 ? static_cast<size_t>((k + kRawK - 1) / kRawK) * 4u * tr * 128u : static_cast<size_t>(m) * k * 2;
   L.rinv = align_up(L.xs + xs_bytes, 256);
-  L.t = align_up(L.rinv + static_cast<size_t>(m) * 4, 256);
-  const size_t groups = r > 0 ? static_cast<size_t>(lora_split(m, k).groups) : 0;
-  L.total = align_up(L.t + groups * static_cast<size_t>(m) * (r > 0 ? r : 0) * 4, 256);
+  size_t off = align_up(L.rinv + static_cast<size_t>(m) * 4, 256);
+  const size_t groups = static_cast<size_t>(lora_split(m, k).groups);
+  for (int i = 0; i < kMaxLinears; ++i) {
+    L.t[i] = off;
+    const int r = i < nlin && ranks[i] > 0 ? ranks[i] : 0;
+    off = align_up(off + groups * static_cast<size_t>(m) * r * 4, 256);
+  }
+  L.total = off;
   return L;
 }
 
 }  // namespace
 
-size_t linear_workspace_bytes(int64_t m, int64_t k, int r) { return linear_layout(m, k, r).total; }
+size_t linear_workspace_bytes(int64_t m, int64_t k, const int* ranks, int nlin) {
+  return linear_layout(m, k, ranks, nlin).total;
+}
 
 qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
-  const int M = static_cast<int>(a.m), N = static_cast<int>(a.n), K = static_cast<int>(a.k);
-  const bool lora = a.r > 0 && a.A != nullptr && a.B != nullptr;
-  const int r = lora ? a.r : 0;
-  const LinearLayout WL = linear_layout(a.m, a.k, r);
+  const int M = static_cast<int>(a.m), K = static_cast<int>(a.k);
+  const int nlin = a.nlin;
+  if (nlin < 1 || nlin > kMaxLinears) return QERL_ERR_INVALID_ARGUMENT;
+  int ranks[kMaxLinears] = {0, 0, 0, 0};
+  int tile_begin[kMaxLinears + 1] = {0, 0, 0, 0, 0};
+  int r = 0;  // the largest rank: sizes the LoRA operand region
+  for (int i = 0; i < nlin; ++i) {
+    const LinearDesc& d = a.lin[i];
+    ranks[i] = (d.r > 0 && d.A != nullptr && d.B != nullptr) ? d.r : 0;
+    r = std::max(r, ranks[i]);
+    tile_begin[i + 1] = tile_begin[i] + static_cast<int>((d.n + kTileN - 1) / kTileN);
+  }
+  const bool lora = r > 0;
+  const int n_tiles = tile_begin[nlin];
+  const LinearLayout WL = linear_layout(a.m, a.k, ranks, nlin);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   int* status = reinterpret_cast<int*>(ws);
   __half* xs = reinterpret_cast<__half*>(ws + WL.xs);
   float* rinv = reinterpret_cast<float*>(ws + WL.rinv);
-  float* t = reinterpret_cast<float*>(ws + WL.t);
   const int sms = sm_count();
 
   // Kernel attributes are set once per process (not per call), so calls can be
@@ -982,7 +1038,6 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     n_tok = 256;
     m_tiles = (M + 255) / 256;
   }
-  const int n_tiles = (N + kTileN - 1) / kTileN;
   const int raw_total = (K + kRawK - 1) / kRawK;
   int split = 1;
   if (n_tok <= 128) {
@@ -1093,34 +1148,39 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     return QERL_ERR_CUDA;
   }
 
-  CUtensorMap tm_bl;
-  if (lora) {
-    if (!make_map_2d(&tm_bl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, static_cast<uint64_t>(r), static_cast<uint64_t>(N),
-                     static_cast<uint64_t>(r) * 2, kLoraChunkK, kTileN, CU_TENSOR_MAP_SWIZZLE_128B))
+  BtMaps tm_bls;
+  std::memset(&tm_bls, 0, sizeof(tm_bls));
+  for (int i = 0; i < nlin; ++i)
+    if (ranks[i] > 0 &&
+        !make_map_2d(&tm_bls.m[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.lin[i].B, static_cast<uint64_t>(ranks[i]),
+                     static_cast<uint64_t>(a.lin[i].n), static_cast<uint64_t>(ranks[i]) * 2, kLoraChunkK, kTileN,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
       return QERL_ERR_CUDA;
-  } else {
-    std::memset(&tm_bl, 0, sizeof(tm_bl));
-  }
 
   // ---- prep: noise + fp16 staging (+ LoRA down-projection)
   PrepParams pp{};
   pp.x = static_cast<const __nv_bfloat16*>(a.x);
   pp.z = a.z;
-  pp.A = static_cast<const __nv_bfloat16*>(a.A);
   pp.xs = xs;
   pp.rinv = rinv;
-  pp.t = t;
   pp.ldx = a.ldx;
   pp.M = M;
   pp.K = K;
-  pp.r = r;
   const LoraSplit ls = lora_split(M, K);
   pp.cluster = lora ? ls.cluster : 1;
   pp.groups = lora ? ls.groups : 0;
   pp.tiled_rows = tmem_a ? n_tok : 0;
   pp.row_groups = (std::max(M, pp.tiled_rows) + pp.cluster - 1) / pp.cluster;
   pp.lora_m_tiles = (M + kLoraTileM - 1) / kLoraTileM;
-  pp.lora_tiles = lora ? pp.lora_m_tiles * ((r + kLoraTileR - 1) / kLoraTileR) : 0;
+  pp.tile_begin[0] = 0;
+  for (int i = 0; i < kMaxLinears; ++i) {
+    const bool on = i < nlin && ranks[i] > 0;
+    pp.A[i] = on ? static_cast<const __nv_bfloat16*>(a.lin[i].A) : nullptr;
+    pp.r[i] = on ? ranks[i] : 0;
+    pp.t[i] = reinterpret_cast<float*>(ws + WL.t[i]);
+    pp.tile_begin[i + 1] = pp.tile_begin[i] + (on ? pp.lora_m_tiles * ((ranks[i] + kLoraTileR - 1) / kLoraTileR) : 0);
+  }
+  pp.lora_tiles = pp.tile_begin[kMaxLinears];
   const int lora_ctas_y = pp.lora_tiles * pp.groups;
   size_t prep_smem = static_cast<size_t>(K) * 2;
   if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>((kLoraTileM + kLoraTileR) * kLoraPad) * 4);
@@ -1143,17 +1203,23 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
 
   MmaParams mp{};
   mp.xs = xs;
-  mp.wpacked = a.wpacked;
-  mp.tensor_scale = a.tensor_scale;
   mp.rinv = rinv;
-  mp.t = t;
-  mp.B = static_cast<const __nv_bfloat16*>(a.B);
-  mp.y = a.y;
+  mp.nlin = nlin;
+  for (int i = 0; i < nlin; ++i) {
+    LinearSlot& L = mp.lin[i];
+    L.wpacked = a.lin[i].wpacked;
+    L.tensor_scale = a.lin[i].tensor_scale;
+    L.t = pp.t[i];
+    L.y = a.lin[i].y;
+    L.N = static_cast<int>(a.lin[i].n);
+    L.r = ranks[i];
+    L.y_f32 = a.lin[i].y_f32 ? 1 : 0;
+    L.tile_begin = tile_begin[i];
+    L.lora_scale = ranks[i] > 0 ? a.lin[i].alpha / static_cast<float>(ranks[i]) : 0.0f;
+  }
   mp.status = status;
   mp.M = M;
-  mp.N = N;
   mp.K = K;
-  mp.r = r;
   mp.n_tok = n_tok;
   mp.split = split;
   mp.raw_stages = raw_stages;
@@ -1173,8 +1239,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.off_sm = P.sm;
   mp.off_bars = P.bars;
   mp.lora_early = lora_early;
-  mp.lora_scale = lora ? a.alpha / static_cast<float>(r) : 0.0f;
-  mp.y_f32 = a.y_f32 ? 1 : 0;
+
   const uint32_t smem_bytes = P.total;
 
   cudaLaunchConfig_t cfg{};
@@ -1191,8 +1256,8 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  const cudaError_t le = tmem_a ? cudaLaunchKernelEx(&cfg, mma_kernel<true>, tm_xs, tm_bl, mp)
-                                : cudaLaunchKernelEx(&cfg, mma_kernel<false>, tm_xs, tm_bl, mp);
+  const cudaError_t le = tmem_a ? cudaLaunchKernelEx(&cfg, mma_kernel<true>, tm_xs, tm_bls, mp)
+                                : cudaLaunchKernelEx(&cfg, mma_kernel<false>, tm_xs, tm_bls, mp);
   if (le != cudaSuccess) return QERL_ERR_CUDA;
   return QERL_OK;
 }

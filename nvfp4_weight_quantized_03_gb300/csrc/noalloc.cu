@@ -65,7 +65,7 @@ extern "C" qerl_status qerl_lora_linear_noalloc(const void* x, int64_t m, int64_
                                                 void* y, int y_dtype, void* stream) {
   if (m < 0 || n < 0 || k <= 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
   const int r_eff = (A != nullptr && B != nullptr) ? r : 0;
-  if (qerl::linear_workspace_bytes(m, k, r_eff) > kNoallocScratchBytes) return QERL_ERR_WORKSPACE;
+  if (qerl::linear_workspace_bytes(m, k, &r_eff, 1) > kNoallocScratchBytes) return QERL_ERR_WORKSPACE;
   void* scratch = nullptr;
   qerl_status st = scratch_for_current_device(&scratch);
   if (st != QERL_OK) return st;

@@ -34,22 +34,27 @@ qerl_status launch_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, u
                               uint64_t counter, cudaStream_t s);
 
 // linear.cu
-struct LinearArgs {
-  const void* x;
-  int64_t m, k, ldx, n;
+struct LinearDesc {
   const uint8_t* wpacked;
   const float* tensor_scale;
-  const float* z;
+  int64_t n;
   const void* A;
   const void* B;
   int r;
   float alpha;
   void* y;
   bool y_f32;
+};
+struct LinearArgs {  // up to 4 linears sharing x, z and k
+  const void* x;
+  int64_t m, k, ldx;
+  const float* z;
+  LinearDesc lin[4];
+  int nlin;
   void* workspace;
   size_t ws_bytes;
 };
-size_t linear_workspace_bytes(int64_t m, int64_t k, int r);
+size_t linear_workspace_bytes(int64_t m, int64_t k, const int* ranks, int nlin);
 qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s);
 
 }  // namespace qerl

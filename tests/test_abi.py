@@ -99,6 +99,50 @@ def test_linear_validation(L):
     assert _lin(L, m=0) == 0 and _lin(L, n=0) == 0  # empty problems are no-ops
 
 
+def _desc(**kw):
+    a = dict(wpacked=0x2000, tensor_scale=0x4000, n=256, A=None, B=None, r=0, alpha=0.0, y=0x5000,
+             y_dtype=q.QERL_BF16)
+    a.update(kw)
+    d = q.LinearDesc()
+    for f, v in a.items():
+        setattr(d, f, v)
+    return d
+
+
+def _group(L, descs, **kw):
+    a = dict(x=0x1000, m=4, k=128, ldx=128, z=None, ws=0x10000, wsb=1 << 30)
+    a.update(kw)
+    arr = (q.LinearDesc * max(len(descs), 1))(*descs)
+    return L.qerl_lora_linear_group(a["x"], a["m"], a["k"], a["ldx"], a["z"], arr if descs else None,
+                                    len(descs), a["ws"], a["wsb"], None)
+
+
+@no_gpu_only
+def test_group_validation(L):
+    E = q.STATUS_NAMES
+    ok = _desc()
+    assert E[_group(L, [])] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[_group(L, [ok] * 5)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[_group(L, [ok, _desc(y_dtype=5)])] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[_group(L, [ok, _desc(A=0x6000)])] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[_group(L, [ok, _desc(A=0x6000, B=0x7000, r=12)])] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[_group(L, [ok, _desc(wpacked=0x2008)])] == "QERL_ERR_MISALIGNED"
+    assert E[_group(L, [ok, _desc(wpacked=None)])] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[_group(L, [ok, _desc(y=0x5001)])] == "QERL_ERR_MISALIGNED"
+    assert E[_group(L, [ok, _desc(y=0x5002, y_dtype=q.QERL_F32)])] == "QERL_ERR_MISALIGNED"
+    assert E[_group(L, [ok], k=96, ldx=96)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    # a member with n == 0 is dropped before its pointers are checked; all empty: no-op
+    assert _group(L, [_desc(n=0, wpacked=None, y=None)], m=4) == 0
+    assert _group(L, [ok, ok], m=0) == 0
+    # the group workspace covers every member's LoRA partials
+    lo = L.qerl_lora_linear_group_workspace_size(4, 128, (q.LinearDesc * 1)(ok), 1)
+    hi = L.qerl_lora_linear_group_workspace_size(
+        4, 128, (q.LinearDesc * 2)(ok, _desc(A=0x6000, B=0x7000, r=64)), 2)
+    assert 0 < lo < hi
+    assert E[_group(L, [ok, _desc(A=0x6000, B=0x7000, r=64)], wsb=hi - 1)] == "QERL_ERR_WORKSPACE"
+    assert L.qerl_lora_linear_group_workspace_size(4, 128, (q.LinearDesc * 1)(ok), 5) == 0
+
+
 @no_gpu_only
 def test_pack_validation(L):
     E = q.STATUS_NAMES

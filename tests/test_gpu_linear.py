@@ -167,3 +167,42 @@ def test_linear_14b_prefill_sampled(q, orc, lin):
     cols = _sample_cols(lin.n, 24, 2)
     sub = y[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()]
     assert_linear_close(sub, c.oracle(orc, rows=rows, cols=cols), orc, what=f"14B {lin.name} prefill")
+
+
+@pytest.mark.parametrize("m", [1, 8, 128])
+def test_linear_group_matches_single_calls(q, orc, m):
+    """q/k/v-like group (three linears of one input, different N, ranks and alphas, one without
+    LoRA): every output matches its own qerl_lora_linear call and the oracle."""
+    k = 1024
+    shapes = [(768, 16, 32.0), (256, 8, 24.0), (384, 0, 0.0)]
+    cases = [Case(q, orc, m, n, k, r, 1e-2, seed=40 + i) for i, (n, r, _) in enumerate(shapes)]
+    x = cases[0].x
+    for c, (_, _, alpha) in zip(cases, shapes):
+        c.x, c.x_bits, c.z, c.zd = x, cases[0].x_bits, cases[0].z, cases[0].zd
+        c.alpha = alpha
+    ys = [torch.full((m, c.n), float("nan"), dtype=torch.bfloat16, device="cuda") for c in cases]
+    lin = [(c.wp, c.S, c.A, c.B, c.alpha, y) for c, y in zip(cases, ys)]
+    ws = q.workspace(q.qerl_lora_linear_group_workspace_size(m, k, lin))
+    q.check(q.qerl_lora_linear_group(x, cases[0].zd, lin, ws))
+    assert q.qerl_read_status(ws) == 0
+    for c, y in zip(cases, ys):
+        assert_linear_close(y, c.oracle(orc), orc, what=f"group n{c.n} r{c.r}")
+        single = c.gpu(q)
+        assert torch.allclose(y.float(), single.float(), rtol=1e-2, atol=1e-3)
+
+
+def test_linear_group_four_with_an_empty_member(q, orc):
+    m, k = 8, 512
+    cases = [Case(q, orc, m, n, k, 16, 0.0, seed=50 + i) for i, n in enumerate([256, 128, 512])]
+    x = cases[0].x
+    for c in cases:
+        c.x, c.x_bits = x, cases[0].x_bits
+    ys = [torch.full((m, c.n), float("nan"), dtype=torch.bfloat16, device="cuda") for c in cases]
+    empty_y = torch.empty((m, 0), dtype=torch.bfloat16, device="cuda")
+    lin = [(c.wp, c.S, c.A, c.B, c.alpha, y) for c, y in zip(cases, ys)]
+    lin.insert(1, (cases[0].wp, cases[0].S, None, None, 0.0, empty_y))
+    ws = q.workspace(q.qerl_lora_linear_group_workspace_size(m, k, lin))
+    q.check(q.qerl_lora_linear_group(x, None, lin, ws))
+    assert q.qerl_read_status(ws) == 0
+    for c, y in zip(cases, ys):
+        assert_linear_close(y, c.oracle(orc), orc, what=f"group4 n{c.n}")
