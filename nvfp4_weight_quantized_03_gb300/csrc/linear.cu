@@ -27,24 +27,29 @@
 //   MMA's M side, tokens are its N side (16..256).  Weights arrive in the
 //   packed layout (one 18432-byte block per 128 rows x 256 K: swizzled E2M1
 //   codes + interleaved E4M3 scale pairs), one 1-D bulk copy per block.
-//     warp 12      weight producer: L2 prefetch a few stages ahead, bulk copy
+//   Nineteen warps; the light roles take the low (older) warp numbers so the
+//   scheduler does not starve them behind the ALU-bound dequant warps:
+//     warp 0       weight producer: L2 prefetch a few stages ahead, bulk copy
 //                  of each block (and, for <= 64 tokens, the x~ slabs of the
-//                  same K range on the same barrier).
-//     warp 13      activation producer (more than 64 tokens): x~ per stage,
+//                  same K range on the same barrier; the first ring of blocks
+//                  is requested before waiting for the preceding kernel).
+//     warp 1       activation producer (more than 64 tokens): x~ per stage,
 //                  bulk-copied slabs up to 128 tokens, 2-D TMA tiles beyond.
-//     warps 0..7   dequant: E2M1 pairs -> fp16 pairs, times the block scale
+//     warp 2       LoRA operands: sums the down-projection groups, scales each
+//                  token row and splits t into bf16 hi + lo.
+//     warps 3..10  MMA issuers (1, 2, 4 or 8 of them; lane 0 issues):
+//                  tcgen05.mma kind::f16, K=16, each into its own fp32 TMEM
+//                  accumulator, so that the ~150-cycle issue cost of an MMA
+//                  overlaps across threads; the epilogue adds them.  Issuer 0
+//                  also adds the LoRA up-projection B . (t_hi + t_lo)^T into
+//                  its accumulator.
+//     warps 11..18 dequant: E2M1 pairs -> fp16 pairs, times the block scale
 //                  (exact products).  Decode writes them to tensor memory as
-//                  the MMA's A operand (tcgen05.st); prefill writes them to
-//                  shared memory in the 128-byte-swizzled K-major layout.
-//     warps 8..11  MMA issuers (lane 0 each): tcgen05.mma kind::f16, K=16,
-//                  round-robin over 64-K stages, each into its own fp32 TMEM
-//                  accumulator so issue latency overlaps; the epilogue adds
-//                  them.
-//     warp 14      LoRA: sums the down-projection groups, splits t into bf16
-//                  hi + lo and issues the up-projection B . (t_hi + t_lo)^T
-//                  into a separate accumulator (bf16 x bf16 -> fp32).
-//   Epilogue (warps 0..7): y = S * 2^-e_m * D + (alpha/r) * D2, rounded to
-//   bf16 or kept fp32.  When the weight tiles leave SMs idle, K is split
+//                  the MMA's A operand (tcgen05.st), a weight stage per
+//                  hand-over; prefill writes them to shared memory in the
+//                  128-byte-swizzled K-major layout.
+//   Epilogue (dequant warps): y = S * 2^-e_m * (sum of accumulators), rounded
+//   to bf16 or kept fp32.  When the weight tiles leave SMs idle, K is split
 //   across a cluster; each CTA writes its scaled partial tile to shared
 //   memory and the partners sum them through distributed shared memory.
 #include <cuda.h>
@@ -299,10 +304,16 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
 
 // ------------------------------------------------------------------ MMA kernel
 
-constexpr int kMmaThreads = 480;  // warps 0-7 dequant + epilogue, 8-11 MMA issuers, 12 weight producer,
-                                  // 13 activation producer, 14 LoRA operands
-constexpr int kIssuerWarp0 = 8, kMaxIssuers = 4;
-constexpr int kWeightWarp = 12, kActWarp = 13, kLoraWarp = 14;
+// Warp roles.  The issue scheduler favours older (lower-numbered) warps, so
+// the light, latency-critical roles come first and the eight ALU-bound
+// dequant warps last: otherwise the MMA issuers starve behind them.  Each
+// group of four consecutive dequant warps covers the four tensor-memory lane
+// quadrants (warp % 4).
+constexpr int kMmaThreads = 608;  // 19 warps
+constexpr int kWeightWarp = 0, kActWarp = 1, kLoraWarp = 2;
+constexpr int kIssuerWarp0 = 3, kMaxIssuers = 8;
+constexpr int kDeqWarp0 = kIssuerWarp0 + kMaxIssuers;  // dequant + epilogue: warps 11..18
+static_assert(kDeqWarp0 + 8 == kMmaThreads / 32, "warp roles");
 constexpr int kTileN = 128;       // output features per CTA (MMA M)
 constexpr int kStageK = 64;       // K per MMA stage (4 x K=16 instructions)
 constexpr int kRawK = 256;        // K per weight-load stage: 128 contiguous bytes of codes per row
@@ -347,7 +358,7 @@ struct MmaParams {
   int t_groups;    // t holds this many partial sums [t_groups][M][r], added in order
   uint32_t off_raw, off_a, off_b, off_lora, off_tstage, off_sm, off_bars;
   uint32_t raw_b_bytes;  // coupled: activation bytes per weight stage (kSub slabs)
-  uint32_t col_lora, col_a;  // TMEM columns of the LoRA accumulator and of the A stages
+  uint32_t col_a;  // TMEM column of the A stages (accumulators: issuer i at i * n_tok)
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
 };
 
@@ -381,6 +392,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 //   t_lo chunk c: n_tok rows m x 64 j  bf16  = bf16(t - t_hi)
 // so B^T . t_hi + B^T . t_lo carries t to ~16 significant bits.  The t tiles
 // are built by `nthr` threads (tid < nthr); zero past M and r.
+// The up-projection accumulates into the main accumulator, which the epilogue
+// scales by S * 2^-e_m per token row m; so row m of t enters pre-scaled by
+// (alpha / r) / (S * 2^-e_m) (fp32, before the hi/lo split: a relative change
+// of a few fp32 ulps).  S must be positive and finite; otherwise the row
+// factor is 0 and the call records QERL_ERR_NONFINITE.
+__device__ __forceinline__ float lora_row_factor(const MmaParams& p, const LinearSlot& L, int m) {
+  if (m >= p.M) return 0.0f;
+  const float sr = *L.tensor_scale * __ldg(p.rinv + m);
+  if (!(sr > 0.0f) || sr > 3.0e38f) {
+    record_error(p.status, 6);
+    return 0.0f;
+  }
+  return L.lora_scale / sr;
+}
 __device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t base, int m0, int tid, int nthr) {
   const int rc = lora_chunks(L.r);
   const uint32_t thi = base + rc * kBtChunkBytes;
@@ -389,6 +414,7 @@ __device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t 
     const int c = idx / (p.n_tok * 8), rem = idx - c * (p.n_tok * 8);
     const int ml = rem >> 3, g = rem & 7;
     const int m = m0 + ml;
+    const float f = lora_row_factor(p, L, m);
     float tv[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -396,7 +422,7 @@ __device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t 
       float v = 0.0f;
       if (m < p.M && j < L.r)
         for (int g = 0; g < p.t_groups; ++g) v += __ldg(L.t + (static_cast<int64_t>(g) * p.M + m) * L.r + j);
-      tv[e] = v;
+      tv[e] = v * f;
     }
     uint32_t hw[4], lw[4];
 #pragma unroll
@@ -415,7 +441,7 @@ __device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t 
 // Same tiles from the partial sums staged in shared memory by bulk copies:
 // tstage[g][ml][j] = t_part[g][m0 + ml][j] for ml < rows.
 __device__ void build_t_tiles_staged(const MmaParams& p, const LinearSlot& L, uint32_t base, uint32_t tstage,
-                                     int rows, int tid, int nthr) {
+                                     int rows, int m0, int tid, int nthr) {
   const int rc = lora_chunks(L.r);
   const uint32_t thi = base + rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
@@ -440,6 +466,9 @@ __device__ void build_t_tiles_staged(const MmaParams& p, const LinearSlot& L, ui
         tv[6] += b.z;
         tv[7] += b.w;
       }
+      const float f = lora_row_factor(p, L, m0 + ml);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tv[e] *= f;
     }
     uint32_t hw[4], lw[4];
 #pragma unroll
@@ -469,25 +498,24 @@ __device__ __forceinline__ void load_bt_tiles(const LinearSlot& L, const CUtenso
 // branch, and each lane then holds its own acquire.  The vote keeps the warp's
 // answer uniform when a bounded wait gives up.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-  bool ok = mbar_try_wait_a(bar, parity);
+  bool ok = mbar_probe_a(bar, parity);
   if (__all_sync(0xFFFFFFFFu, ok)) return true;
   if (!ok) ok = mbar_wait_a(bar, parity, abort_flag, status);
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// D2 (+)= B^T . t_hi^T + B^T . t_lo^T over the rank dimension (bf16 x bf16 -> fp32).
+// D += B^T . t_hi^T + B^T . t_lo^T over the rank dimension (bf16 x bf16 ->
+// fp32), into an accumulator that already holds this thread's main-loop sum.
 __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, const LinearSlot& L, uint32_t base, uint32_t d2) {
   const int rc = lora_chunks(L.r);
   const uint32_t idesc = idesc_bf16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
   const uint32_t thi = base + rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
-  uint32_t acc = 0;
   for (int c = 0; c < rc; ++c)
     for (int kk = 0; kk < kLoraChunkK / 16 && c * kLoraChunkK + kk * 16 < L.r; ++kk) {
       const uint64_t ad = sw128_kmajor_desc(base + c * kBtChunkBytes + kk * 32);
-      tc_mma_f16(d2, ad, sw128_kmajor_desc(thi + c * p.n_tok * 128 + kk * 32), idesc, acc);
+      tc_mma_f16(d2, ad, sw128_kmajor_desc(thi + c * p.n_tok * 128 + kk * 32), idesc, 1u);
       tc_mma_f16(d2, ad, sw128_kmajor_desc(tlo + c * p.n_tok * 128 + kk * 32), idesc, 1u);
-      acc = 1;
     }
 }
 
@@ -544,11 +572,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
       mbar_init_a(raw_full(s), 1);  // producer expect_tx
-      mbar_init_a(raw_empty(s), kTmemA && p.coupled ? 8 + kSub : 8);  // 8 dequant warps (+ the stage's MMAs)
+      mbar_init_a(raw_empty(s), kTmemA && p.coupled ? 8 + NI : 8);  // 8 dequant warps (+ each issuer's commit)
     }
-    for (int s = 0; s < AS; ++s) {
-      mbar_init_a(ab_full(s), kTmemA ? 8 : 9);  // 8 dequant warps (+ activation producer expect_tx)
-      mbar_init_a(ab_empty(s), 1);              // tcgen05.commit
+    if (kTmemA) {
+      // One barrier pair per weight stage of the tensor-memory ring (kSub MMA
+      // stages): every dequant warp arrives once, every issuer commits once.
+      for (int w = 0; w < AS / kSub; ++w) {
+        mbar_init_a(ab_full(w), 8);
+        mbar_init_a(ab_empty(w), NI);
+      }
+    } else {
+      for (int s = 0; s < AS; ++s) {
+        mbar_init_a(ab_full(s), 9);   // 8 dequant warps + activation producer expect_tx
+        mbar_init_a(ab_empty(s), 1);  // tcgen05.commit
+      }
     }
     if (kTmemA)
       for (int s = 0; s < BS; ++s) {
@@ -575,7 +612,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem_gen + p.off_bars + 8 * (kB2 + 3));
-  const uint32_t d_lora = tmem_base + p.col_lora;
   const uint32_t lora_base = p.lora_early ? sbase + p.off_lora : sbase;  // late: inside the idle ring
   const uint32_t smv = sbase + p.off_sm;
 
@@ -600,18 +636,33 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     auto xbytes_of = [&](int rst) {
       return coupled ? static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128) : 0u;
     };
+    // Coupled: the first ring's weight blocks do not depend on the preceding
+    // kernel (the weights were written before it started), so they are
+    // requested before waiting for it; their activation slabs, and the
+    // arrivals that let those stages complete, follow once it has finished.
+    const int early = coupled ? min(RS, nraw) : 0;
+    if (lane == 0)
+      for (int i = 0; i < early; ++i) {
+        mbar_expect_tx_a(raw_full(i), kRawSlotBytes);
+        bulk_load(sbase + p.off_raw + i * kRawSlotBytes, wtile + static_cast<int64_t>(rb + i) * kRawSlotBytes,
+                  kRawSlotBytes, raw_full(i));
+      }
     if (coupled) griddep_wait();
     if (lane == 0) {
       for (int i = 0, s = 0; i < nraw; ++i) {
         if (i + kPrefetch < nraw)
           bulk_prefetch_l2(wtile + static_cast<int64_t>(rb + i + kPrefetch) * kRawSlotBytes, kRawSlotBytes);
-        const uint32_t ph = (i / RS) & 1;
-        if (!mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status)) break;
         const int rst = rb + i;
         const uint32_t xbytes = xbytes_of(rst);
-        mbar_arrive_expect_tx_a(raw_full(s), kRawSlotBytes + xbytes);
-        bulk_load(sbase + p.off_raw + s * kRawSlotBytes, wtile + static_cast<int64_t>(rst) * kRawSlotBytes,
-                  kRawSlotBytes, raw_full(s));
+        if (i < early) {
+          mbar_arrive_expect_tx_a(raw_full(s), xbytes);
+        } else {
+          const uint32_t ph = (i / RS) & 1;
+          if (!mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status)) break;
+          mbar_arrive_expect_tx_a(raw_full(s), kRawSlotBytes + xbytes);
+          bulk_load(sbase + p.off_raw + s * kRawSlotBytes, wtile + static_cast<int64_t>(rst) * kRawSlotBytes,
+                    kRawSlotBytes, raw_full(s));
+        }
         if (coupled)
           bulk_load(sbase + p.off_b + s * p.raw_b_bytes,
                     reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rst) * p.raw_b_bytes, xbytes,
@@ -655,71 +706,125 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kMaxIssuers) {
     // ------------------------------------------------------------ MMA issuers
     const int ii = warp - kIssuerWarp0;
-    if (lane == 0 && ii < NI) {
+    if (ii < NI) {
       const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
       const uint32_t d_acc = tmem_base + static_cast<uint32_t>(ii * p.n_tok);
       uint32_t acc = 0;
-      // Stage s is always served by issuer s % NI (AS is a multiple of NI), so
-      // each barrier has a single waiter that is never two phases ahead.
-      for (int j = ii; j < nmma; j += NI) {
-        const int s = j % AS;
-        const uint32_t ph = (j / AS) & 1;
-        if (!mbar_wait_a(ab_full(s), ph, abort_flag, p.status)) break;
-        int sb = s;
-        uint32_t b_addr = sbase + p.off_b + s * (p.n_tok * 128);
-        if constexpr (kTmemA) {
+      if constexpr (kTmemA) {
+        // The whole warp runs the loop (waits, addresses and descriptors are
+        // warp-uniform); lane 0 issues the MMAs and their commits.  A weight
+        // stage holds kSub x 4 MMAs (u = 4 q + kk: MMA stage q, K step kk);
+        // issuer ii takes the contiguous block of `per` of them starting at
+        // ii * per, into its own accumulator (with <= 4 issuers an MMA stage
+        // therefore has a single issuer).  Every issuer waits for the slot's
+        // full barrier and commits once to its empty barrier (and, coupled,
+        // to the raw slot whose activation slabs it read), so a slot cannot
+        // be refilled before all of them are done and no waiter falls two
+        // phases behind.  Coupled, the activation slabs landed with the
+        // weight stage on its raw barrier, which the dequant warps waited for
+        // before arriving on the slot's full barrier: waiting for that barrier
+        // orders the slabs before these MMAs too.
+        const int AW = AS / kSub;
+        const int per = kSub * 4 / NI;
+        const int u0 = ii * per;
+        const uint32_t b_slab = static_cast<uint32_t>(p.n_tok * 128);
+        int w = 0, rs = 0;
+        uint32_t wph = 0;
+        for (int wi = 0; wi < nraw; ++wi) {
+          if (!warp_wait(ab_full(w), wph, abort_flag, p.status)) break;
+          const int nq = min(kSub, nmma - wi * kSub);
+          const int u1 = min(u0 + per, 4 * nq);  // this issuer's MMAs in this weight stage: [u0, u1)
+          const uint32_t a_st = tmem_base + p.col_a + static_cast<uint32_t>(w * kSub * kAStageCols);
+          tc_fence_after();
           if (p.coupled) {
-            // The activation slab sits in the weight stage's slot (already
-            // landed: the dequant warps waited for it; acquire it here too).
-            const int ri = j / kSub;
-            sb = ri % RS;
-            if (!mbar_wait_a(raw_full(sb), (ri / RS) & 1, abort_flag, p.status)) break;
-            b_addr = sbase + p.off_b + sb * p.raw_b_bytes + (j % kSub) * (p.n_tok * 128);
+            const uint32_t b_st = sbase + p.off_b + static_cast<uint32_t>(rs) * p.raw_b_bytes;
+            if (lane == 0) {
+              for (int u = u0; u < u1; ++u)
+                tc_mma_f16_ts(d_acc, a_st + (u >> 2) * kAStageCols + (u & 3) * 8,
+                              sw128_kmajor_desc(b_st + (u >> 2) * b_slab + (u & 3) * 32), idesc,
+                              (u > u0 || wi > 0) ? 1u : acc);
+              tc_commit(ab_empty(w));
+              tc_commit(raw_empty(rs));
+            }
+            if (u1 > u0) acc = 1;
           } else {
-            sb = j % BS;
-            if (!mbar_wait_a(b_full(sb - sb % kSub), (j / BS) & 1, abort_flag, p.status)) break;
-            b_addr = sbase + p.off_b + sb * (p.n_tok * 128);
-          }
-        }
-        tc_fence_after();
+            // Separate activation ring: each MMA stage's slab has its own
+            // full (per weight stage) and empty (per MMA stage) barriers;
+            // with <= kSub issuers an MMA stage has a single issuer.
+            bool ok = true;
+            for (int q = u0 >> 2; q < (u1 + 3) >> 2; ++q) {
+              const int j = wi * kSub + q;
+              const int sb = j % BS;
+              if (!warp_wait(b_full(sb - sb % kSub), (j / BS) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t b_addr = sbase + p.off_b + sb * b_slab;
+              if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < kStageK / 16; ++kk) {
-          const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
-          if constexpr (kTmemA) {
-            tc_mma_f16_ts(d_acc, tmem_base + p.col_a + s * kAStageCols + kk * 8, bd, idesc, acc);
-          } else {
-            const uint32_t a_addr = sbase + p.off_a + s * kAStageBytes;
-            tc_mma_f16(d_acc, sw128_kmajor_desc(a_addr + kk * 32), bd, idesc, acc);
+                for (int kk = 0; kk < 4; ++kk)
+                  tc_mma_f16_ts(d_acc, a_st + q * kAStageCols + kk * 8, sw128_kmajor_desc(b_addr + kk * 32), idesc,
+                                kk > 0 ? 1u : acc);
+                tc_commit(b_empty(sb));
+              }
+              acc = 1;
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(ab_empty(w));
           }
-          acc = 1;
+          __syncwarp();
+          if (++w == AW) {
+            w = 0;
+            wph ^= 1;
+          }
+          if (++rs == RS) rs = 0;
         }
-        tc_commit(ab_empty(s));
-        if constexpr (kTmemA) tc_commit(p.coupled ? raw_empty(sb) : b_empty(sb));
-      }
-      // The LoRA up-projection goes last, so a slow producer of t never
-      // holds up the weight stream.
-      if (ii == 0 && do_lora && p.lora_early) {
-        if (mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
+      } else if (lane == 0) {
+        // Stage s is always served by issuer s % NI (AS is a multiple of NI),
+        // so each barrier has a single waiter that is never two phases ahead.
+        for (int j = ii; j < nmma; j += NI) {
+          const int s = j % AS;
+          const uint32_t ph = (j / AS) & 1;
+          if (!mbar_wait_a(ab_full(s), ph, abort_flag, p.status)) break;
+          const uint32_t b_addr = sbase + p.off_b + s * (p.n_tok * 128);
           tc_fence_after();
-          issue_lora_mmas(p, L, lora_base, d_lora);
+          const uint32_t a_addr = sbase + p.off_a + s * kAStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < kStageK / 16; ++kk) {
+            tc_mma_f16(d_acc, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc, acc);
+            acc = 1;
+          }
+          tc_commit(ab_empty(s));
         }
       }
-      if (do_lora && !p.lora_early) {
-        tc_commit(ring_free);  // the ring is idle once every mainloop MMA is done
-        if (ii == 0 && mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
-          tc_fence_after();
-          issue_lora_mmas(p, L, lora_base, d_lora);
+      if (lane == 0) {
+        // The LoRA up-projection goes last, so a slow producer of t never
+        // holds up the weight stream.
+        if (ii == 0 && do_lora && p.lora_early) {
+          if (mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
+            tc_fence_after();
+            issue_lora_mmas(p, L, lora_base, d_acc);
+          }
         }
+        if (do_lora && !p.lora_early) {
+          tc_commit(ring_free);  // the ring is idle once every mainloop MMA is done
+          if (ii == 0 && mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
+            tc_fence_after();
+            issue_lora_mmas(p, L, lora_base, d_acc);
+          }
+        }
+        tc_commit(acc_full);  // always, so the epilogue's wait completes even after an abort
       }
-      tc_commit(acc_full);  // always, so the epilogue's wait completes even after an abort
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ warps 0-7: dequant
+  } else if (warp >= kDeqWarp0) {
+    // ------------------------------------------------------------ dequant warps
     // kTmemA: warp w owns TMEM lane quadrant w % 4 (rows 32(w%4)..+31), one
     // row per thread, and K-half w / 4 of every 64-wide stage.  Otherwise 16
     // rows per warp, two K-halves per row pair.
-    const int row = kTmemA ? 32 * (warp & 3) + lane : 16 * warp + (lane & 15);
-    const int half = kTmemA ? warp >> 2 : lane >> 4;
+    const int dw = warp - kDeqWarp0;
+    const int row = kTmemA ? 32 * (warp & 3) + lane : 16 * dw + (lane & 15);
+    const int half = kTmemA ? dw >> 2 : lane >> 4;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t arow = static_cast<uint32_t>(row * 128);
     int j = 0, as = 0, s = 0;
@@ -738,62 +843,69 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         cw[q] = lds128(crow + (((2 * q + half) ^ (row & 7)) << 4));
         sc[q] = lds16(srow + 2 * q * 256);  // scale pair 2q + half: blocks 4q + 2half, +1
       }
-      // kTmemA: the weight stage's (up to) kSub MMA stages are converted back
-      // to back, their tensor-memory stores are awaited once and their full
-      // barriers signalled together (lane q arrives for stage q); the ring
-      // holds at least kSub stages.  Otherwise each stage is handed over as
-      // soon as it is written (the shared-memory ring may be shallower).
-      bool ok = true;
-      const int nq = min(kSub, nmma - j);
-      const int as0 = as;
+      // The whole weight stage is converted first, with no waits in between,
+      // so the conversions of its (up to) kSub MMA stages overlap.  kTmemA:
+      // the ring is handed over a weight stage (kSub MMA stages) at a time.
+      // Otherwise each MMA stage is handed over as soon as it is written (the
+      // shared-memory ring may be shallower).
+      uint32_t o[kSub][16];
 #pragma unroll
       for (int q = 0; q < kSub; ++q) {
-        if (q >= nq) break;
-        if (!warp_wait(ab_empty(as), aph ^ 1, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
         const __half2 s01 = e4m3x2_to_half2(sc[q]);
         const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
         const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
         const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
         const uint32_t words[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
-        uint32_t o[16];
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
           uint32_t u[4];
           e2m1x8_to_f16x2x4(words[qq], u);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) o[4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
+          for (int b = 0; b < 4; ++b) o[q][4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
         }
-        if constexpr (kTmemA) {
-          tmem_st_x16(tmem_base + lane_base + p.col_a + as * kAStageCols + 16 * half, o);
-        } else {
+      }
+      const int nq = min(kSub, nmma - j);
+      if constexpr (kTmemA) {
+        // One wait for the weight stage's tensor-memory slot (as is a multiple
+        // of kSub here), its MMA stages stored back to back, one arrival.
+        if (!warp_wait(ab_empty(as / kSub), aph ^ 1, abort_flag, p.status)) break;
+#pragma unroll
+        for (int q = 0; q < kSub; ++q)
+          if (q < nq) tmem_st_x16(tmem_base + lane_base + p.col_a + (as + q) * kAStageCols + 16 * half, o[q]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_a(ab_full(as / kSub));
+        as += kSub;
+        if (as == AS) {
+          as = 0;
+          aph ^= 1;
+        }
+      } else {
+        bool ok = true;
+#pragma unroll
+        for (int q = 0; q < kSub; ++q) {
+          if (q >= nq) break;
+          if (!warp_wait(ab_empty(as), aph ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           const uint32_t a_s = sbase + p.off_a + as * kAStageBytes + arow;
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
             const int chunk = half * 4 + qq;
-            sts128(a_s + ((chunk ^ (row & 7)) << 4), make_uint4(o[4 * qq], o[4 * qq + 1], o[4 * qq + 2], o[4 * qq + 3]));
+            sts128(a_s + ((chunk ^ (row & 7)) << 4),
+                   make_uint4(o[q][4 * qq], o[q][4 * qq + 1], o[q][4 * qq + 2], o[q][4 * qq + 3]));
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive_a(ab_full(as));
+          if (++as == AS) {
+            as = 0;
+            aph ^= 1;
+          }
         }
-        if (++as == AS) {
-          as = 0;
-          aph ^= 1;
-        }
-      }
-      if (!ok) break;
-      if constexpr (kTmemA) {
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane < nq) {
-          int st = as0 + lane;
-          while (st >= AS) st -= AS;
-          mbar_arrive_a(ab_full(st));
-        }
+        if (!ok) break;
       }
       j += nq;
       __syncwarp();
@@ -804,7 +916,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
     if (do_lora && !p.lora_early) {
-      if (warp_wait(ring_free, 0, abort_flag, p.status)) build_t_tiles(p, L, lora_base, m0, threadIdx.x, 256);
+      if (warp_wait(ring_free, 0, abort_flag, p.status)) build_t_tiles(p, L, lora_base, m0, threadIdx.x - 32 * kDeqWarp0, 256);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive_a(lora_full);
@@ -826,7 +938,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             bulk_load(tstage + static_cast<uint32_t>(g * p.n_tok * L.r * 4),
                       L.t + (static_cast<int64_t>(g) * p.M + m0) * L.r, bytes, t_full);
         }
-        if (warp_wait(t_full, 0, abort_flag, p.status)) build_t_tiles_staged(p, L, lora_base, tstage, rows, lane, 32);
+        if (warp_wait(t_full, 0, abort_flag, p.status)) build_t_tiles_staged(p, L, lora_base, tstage, rows, m0, lane, 32);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive_a(lora_full);
@@ -840,12 +952,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   // ---------------------------------------------------------------- epilogue
   const uint32_t part = sbase;  // [n_tok][128] fp32 scaled partial tile (split > 1), ring reused
-  if (warp < 8) {
+  const int dt = static_cast<int>(threadIdx.x) - 32 * kDeqWarp0;  // dequant-warp thread index
+  if (warp >= kDeqWarp0) {
     // Row scales S * 2^-e_m come from the preceding kernel; the dequant above did not need them.
     griddep_wait();
     {
       const float S = *L.tensor_scale;
-      for (int i = threadIdx.x; i < p.n_tok; i += 256)
+      for (int i = dt; i < p.n_tok; i += 256)
         stsf(smv + 4u * i, (m0 + i < p.M) ? S * __ldg(p.rinv + m0 + i) : 0.0f);
     }
     named_barrier_sync(1, 256);
@@ -855,29 +968,33 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int nl = q * 32 + lane;
     const int n = n0 + nl;
     const int cols = p.n_tok / 2;
-    const int c0 = (warp >> 2) * cols;
+    const int c0 = ((warp - kDeqWarp0) >> 2) * cols;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const int nacc = min(NI, nmma);
+    // Issuer a holds a sum iff its first MMA falls in the first weight
+    // stage's (up to kSub) MMA stages: a prefix of the issuers.
+    const int nq0 = min(kSub, nmma);
+    const int nacc = min(NI, (nq0 * NI + 3) / 4);
     for (int c = c0; c < c0 + cols; c += 8) {
-      // All accumulators' (and the LoRA accumulator's) columns first, one wait.
-      float w[kMaxIssuers][8], l[8];
-#pragma unroll
-      for (int a = 0; a < kMaxIssuers; ++a)
-        if (a < nacc) tmem_ld_x8(tmem_base + static_cast<uint32_t>(a * p.n_tok) + lane_off + c, w[a]);
-      if (do_lora) tmem_ld_x8(d_lora + lane_off + c, l);
-      tmem_ld_wait();
       float v[8];
+      // Four accumulators' columns per wait (issuer 0's holds the LoRA term).
+      for (int a0 = 0; a0 < nacc; a0 += 4) {
+        float w[4][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        v[e] = w[0][e];
+        for (int a = 0; a < 4; ++a)
+          if (a0 + a < nacc) tmem_ld_x8(tmem_base + static_cast<uint32_t>((a0 + a) * p.n_tok) + lane_off + c, w[a]);
+        tmem_ld_wait();
 #pragma unroll
-        for (int a = 1; a < kMaxIssuers; ++a)
-          if (a < nacc) v[e] += w[a][e];
+        for (int e = 0; e < 8; ++e) {
+          float t = a0 == 0 ? w[0][e] : v[e] + w[0][e];
+#pragma unroll
+          for (int a = 1; a < 4; ++a)
+            if (a0 + a < nacc) t += w[a][e];
+          v[e] = t;
+        }
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        float out = ok ? v[e] * ldsf(smv + 4u * (c + e)) : 0.0f;
-        if (do_lora && ok) out = fmaf(L.lora_scale, l[e], out);
+        const float out = ok ? v[e] * ldsf(smv + 4u * (c + e)) : 0.0f;
         if (p.split > 1)
           stsf(part + 4u * ((c + e) * kTileN + nl), out);
         else if (m0 + c + e < p.M && n < L.N)
@@ -896,12 +1013,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   if (p.split > 1) {
     cluster_sync_all();  // every partner's scaled partial tile is in its shared memory
-    if (warp < 8) {
+    if (warp >= kDeqWarp0) {
       const int rank = static_cast<int>(cluster_ctarank());
       const int per = (p.n_tok + p.split - 1) / p.split;
       const int mb = rank * per;
       const int me = min(min(p.n_tok, mb + per), p.M - m0);
-      for (int it = threadIdx.x; it < (me - mb) * (kTileN / 4); it += 256) {
+      for (int it = dt; it < (me - mb) * (kTileN / 4); it += 256) {
         const int ml = mb + it / (kTileN / 4);
         const int nl4 = 4 * (it % (kTileN / 4));
         const uint32_t off = 4u * static_cast<uint32_t>(ml * kTileN + nl4);
@@ -1022,6 +1139,11 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemLimit);
+    // The prep grid runs beside the MMA kernel's CTAs (which start early and
+    // hold most of shared memory): the same carveout lets them share an SM.
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      cudaSharedmemCarveoutMaxShared);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (attr_err == cudaSuccess)
@@ -1063,18 +1185,19 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // memory and spread MMA issue over several threads; 256-token tiles stage
   // the weights in shared memory (their accumulators fill tensor memory).
   const bool tmem_a = n_tok <= 128;
-  const int issuers = !tmem_a ? 1 : (n_tok <= 64 ? 4 : 2);
-  const uint32_t col_lora = static_cast<uint32_t>(issuers * n_tok);
-  const uint32_t col_a = static_cast<uint32_t>(align_up(col_lora + (r > 0 ? n_tok : 0), 32));
+  // Each MMA occupies its issuing thread for ~150 cycles whatever the token
+  // count, so small tiles take more issuers (each with its own accumulator,
+  // which tensor memory must hold next to the A ring).
+  const int issuers = !tmem_a ? 1 : (n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2));
+  const uint32_t col_a = static_cast<uint32_t>(align_up(issuers * n_tok, 32));
   int ab_cap = kMaxAB;
   if (tmem_a) {
     if (col_a > static_cast<uint32_t>(kTmemCols)) return QERL_ERR_UNSUPPORTED_SHAPE;
     ab_cap = std::min(kMaxAB, static_cast<int>((kTmemCols - col_a) / kAStageCols));
-    // Stage s is always served by issuer s % issuers, and a weight stage's kSub
-    // MMA stages are consecutive ring stages: a multiple of kSub (which the
-    // issuer count divides).
+    // The ring is handed over a weight stage (kSub consecutive MMA stages) at
+    // a time: a multiple of kSub.
     ab_cap -= ab_cap % kSub;
-    if (ab_cap < std::max(2, issuers)) return QERL_ERR_UNSUPPORTED_SHAPE;
+    if (ab_cap < kSub) return QERL_ERR_UNSUPPORTED_SHAPE;
   } else if (2 * n_tok > kTmemCols) {
     return QERL_ERR_UNSUPPORTED_SHAPE;
   }
@@ -1130,10 +1253,10 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
       if (raw_stages >= 2) break;
     }
   }
-  if (raw_stages < 2 || ab_stages < std::max(2, issuers)) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (raw_stages < 2 || ab_stages < (tmem_a ? kSub : std::max(2, issuers))) return QERL_ERR_UNSUPPORTED_SHAPE;
   // A weight stage is handed over (and its activations loaded) at once.
   if (tmem_a && (ab_stages < kSub || ab_stages % kSub != 0 || b_stages < kSub || b_stages % kSub != 0 ||
-                 (coupled && issuers != kSub)))
+                 (kSub * 4) % issuers != 0 || (!coupled && issuers > kSub)))
     return QERL_ERR_UNSUPPORTED_SHAPE;
   const Plan P = plan_for(raw_stages, ab_stages, b_stages);
 
@@ -1229,7 +1352,6 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.raw_b_bytes = raw_b;
   mp.issuers = issuers;
   mp.t_groups = pp.groups;
-  mp.col_lora = col_lora;
   mp.col_a = col_a;
   mp.off_raw = P.raw;
   mp.off_a = P.a;

@@ -81,6 +81,11 @@ __device__ __forceinline__ void mbar_init_a(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive_a(uint32_t bar) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
 }
+// Raises the barrier's pending transaction count without arriving: the phase
+// cannot complete before the (later) arrive, however early the bytes land.
+__device__ __forceinline__ void mbar_expect_tx_a(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx_a(uint32_t bar, uint32_t bytes) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
                "r"(bytes)
@@ -90,6 +95,16 @@ __device__ __forceinline__ bool mbar_try_wait_a(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait_a(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
@@ -111,12 +126,24 @@ __device__ __forceinline__ bool mbar_try_wait_hint_a(uint32_t bar, uint32_t pari
 #ifndef QERL_WAIT_HINT_NS
 #define QERL_WAIT_HINT_NS 20000
 #endif
+// First look at a phase before a bounded wait.
+__device__ __forceinline__ bool mbar_probe_a(uint32_t bar, uint32_t parity) {
+#ifdef QERL_WAIT_POLL
+  return mbar_test_wait_a(bar, parity);
+#else
+  return mbar_try_wait_a(bar, parity);
+#endif
+}
 __device__ __forceinline__ bool mbar_wait_a(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-  if (mbar_try_wait_a(bar, parity)) return true;
+  if (mbar_probe_a(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
+#ifdef QERL_WAIT_POLL
+    if (mbar_test_wait_a(bar, parity)) return true;
+#else
     if (QERL_WAIT_HINT_NS > 0 ? mbar_try_wait_hint_a(bar, parity, QERL_WAIT_HINT_NS) : mbar_try_wait_a(bar, parity))
       return true;
+#endif
     if ((i & (QERL_WAIT_HINT_NS > 0 ? 15u : 1023u)) == 0) {
       if (*abort_flag) return false;
       if (clock64() - t0 > kWaitLimitCycles) {
