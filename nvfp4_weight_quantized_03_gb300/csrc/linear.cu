@@ -75,6 +75,10 @@ constexpr int kLoraTileM = 16;   // token rows per LoRA tile
 constexpr int kLoraTileR = 32;   // ranks per LoRA tile
 constexpr int kLoraKc = 64;      // K per shared-memory chunk
 constexpr int kLoraPad = 68;     // padded row length (floats): conflict-free float4 reads
+constexpr int kLoraStages = 3;   // chunks in flight (cp.async ring)
+// One ring stage: x [16][64] bf16, A [32][64] bf16, z [64] fp32.
+constexpr int kLoraStageBytes = (kLoraTileM + kLoraTileR) * kLoraKc * 2 + kLoraKc * 4;
+constexpr int kLoraSmemBytes = kLoraStages * kLoraStageBytes + (kLoraTileM + kLoraTileR) * kLoraPad * 4;
 constexpr int kPrepMaxCluster = 8;
 
 struct PrepParams {
@@ -154,19 +158,39 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     __nv_bfloat16* xt = reinterpret_cast<__nv_bfloat16*>(sm);
     const uint4* xrow = reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(m) * p.ldx);
     unsigned amax = 0;
-    for (int v = tid; v < p.K / 8; v += kPrepThreads) {
-      uint4 raw = __ldg(xrow + v);
-      __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&raw);
-      if (p.z != nullptr) {
-        const float4 z0 = __ldg(reinterpret_cast<const float4*>(p.z) + 2 * v);
-        const float4 z1 = __ldg(reinterpret_cast<const float4*>(p.z) + 2 * v + 1);
-        const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+    // Four vectors per thread per round: their loads are all in flight
+    // before the first is used.
+    const int nv = p.K / 8;
+    const float4* z4 = reinterpret_cast<const float4*>(p.z);
+    for (int v0 = tid; v0 < nv; v0 += 4 * kPrepThreads) {
+      uint4 raw[4];
+      float4 za[4], zb[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) e[j] = __float2bfloat16_rn(__fmul_rn(__bfloat162float(e[j]), __fadd_rn(1.0f, zz[j])));
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * kPrepThreads;
+        if (v < nv) {
+          raw[u] = __ldg(xrow + v);
+          if (p.z != nullptr) {
+            za[u] = __ldg(z4 + 2 * v);
+            zb[u] = __ldg(z4 + 2 * v + 1);
+          }
+        }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = max(amax, static_cast<unsigned>(__bfloat16_as_ushort(e[j]) & 0x7FFFu));
-      reinterpret_cast<uint4*>(xt)[v] = raw;
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * kPrepThreads;
+        if (v >= nv) break;
+        __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&raw[u]);
+        if (p.z != nullptr) {
+          const float zz[8] = {za[u].x, za[u].y, za[u].z, za[u].w, zb[u].x, zb[u].y, zb[u].z, zb[u].w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            e[j] = __float2bfloat16_rn(__fmul_rn(__bfloat162float(e[j]), __fadd_rn(1.0f, zz[j])));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = max(amax, static_cast<unsigned>(__bfloat16_as_ushort(e[j]) & 0x7FFFu));
+        reinterpret_cast<uint4*>(xt)[v] = raw[u];
+      }
     }
     amax = __reduce_max_sync(0xFFFFFFFFu, amax);
     __shared__ unsigned red[kPrepThreads / 32];
@@ -216,8 +240,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   const int rt = tile / p.lora_m_tiles;
   const int ks = blockIdx.x;  // this CTA's rank in the cluster
   const int row0 = mt * kLoraTileM, rank0 = rt * kLoraTileR;
-  float* xsm = reinterpret_cast<float*>(sm);     // [kLoraTileM][kLoraPad]
-  float* asm_ = xsm + kLoraTileM * kLoraPad;     // [kLoraTileR][kLoraPad]
+  // The slice's 64-wide chunks stream through a kLoraStages-deep cp.async
+  // ring (raw bf16 x, A and fp32 z; rows past M and ranks past r zero-filled)
+  // so that their loads overlap; each chunk is then converted once into the
+  // fp32 tiles below (x~ with the noise applied, A) that the FMA loop reads.
+  float* xsm = reinterpret_cast<float*>(sm + kLoraStages * kLoraStageBytes);  // [kLoraTileM][kLoraPad]
+  float* asm_ = xsm + kLoraTileM * kLoraPad;                                   // [kLoraTileR][kLoraPad]
+  const uint32_t ring = smem_u32(sm);
   const int lr = tid & 31, rp = tid >> 5;
   float acc0 = 0.0f, acc1 = 0.0f;
   const int kc_total = p.K / kLoraKc;
@@ -225,51 +254,61 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   const int sl = g * p.cluster + ks;
   const int kc_begin = static_cast<int>(static_cast<int64_t>(sl) * kc_total / slices);
   const int kc_end = static_cast<int>(static_cast<int64_t>(sl + 1) * kc_total / slices);
-  for (int kc = kc_begin; kc < kc_end; ++kc) {
+  auto issue_chunk = [&](int kc, int st) {
+    const uint32_t base = ring + st * kLoraStageBytes;
     const int k0 = kc * kLoraKc;
-    __syncthreads();
-    // x~ tile: 16 rows x 64 k, 8 bf16 per vector -> 128 vectors
-    for (int v = tid; v < kLoraTileM * kLoraKc / 8; v += kPrepThreads) {
-      const int rr = v >> 3, kk = (v & 7) * 8;
-      float f[8];
-      if (row0 + rr < p.M) {
-        uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(row0 + rr) * p.ldx + k0 + kk));
-        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
-        if (p.z != nullptr) {
-          const float4 z0 = __ldg(reinterpret_cast<const float4*>(p.z + k0 + kk));
-          const float4 z1 = __ldg(reinterpret_cast<const float4*>(p.z + k0 + kk) + 1);
-          const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = noisy(f[j], zz[j]);
-        }
+    constexpr int kXv = kLoraTileM * kLoraKc / 8, kAv = kLoraTileR * kLoraKc / 8, kZv = kLoraKc / 4;
+    for (int v = tid; v < kXv + kAv + kZv; v += kPrepThreads) {
+      if (v < kXv) {
+        const int rr = v >> 3, c = v & 7;
+        const bool in = row0 + rr < p.M;
+        cp_async_16(base + v * 16, in ? p.x + static_cast<int64_t>(row0 + rr) * p.ldx + k0 + c * 8 : p.x, in ? 16u : 0u);
+      } else if (v < kXv + kAv) {
+        const int jj = (v - kXv) >> 3, c = (v - kXv) & 7;
+        const bool in = rank0 + jj < rr_;
+        cp_async_16(base + v * 16, in ? Am + static_cast<int64_t>(rank0 + jj) * p.K + k0 + c * 8 : Am,
+                    in ? 16u : 0u);
       } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = 0.0f;
+        const int c = v - kXv - kAv;
+        cp_async_16(base + v * 16, p.z != nullptr ? p.z + k0 + c * 4 : reinterpret_cast<const float*>(p.x),
+                    p.z != nullptr ? 16u : 0u);
       }
-      float4* d = reinterpret_cast<float4*>(xsm + rr * kLoraPad + kk);
-      d[0] = make_float4(f[0], f[1], f[2], f[3]);
-      d[1] = make_float4(f[4], f[5], f[6], f[7]);
     }
-    // A tile: 32 ranks x 64 k -> 256 vectors
-    for (int v = tid; v < kLoraTileR * kLoraKc / 8; v += kPrepThreads) {
-      const int jj = v >> 3, kk = (v & 7) * 8;
-      float f[8];
-      if (rank0 + jj < rr_) {
-        uint4 raw = __ldg(reinterpret_cast<const uint4*>(Am + static_cast<int64_t>(rank0 + jj) * p.K + k0 + kk));
+  };
+  for (int st = 0; st < kLoraStages; ++st) {
+    if (kc_begin + st < kc_end) issue_chunk(kc_begin + st, st);
+    cp_async_commit();  // one group per chunk slot, empty past the slice
+  }
+  for (int kc = kc_begin, st = 0; kc < kc_end; ++kc) {
+    cp_async_wait_group<kLoraStages - 1>();  // this chunk's group has landed
+    __syncthreads();                          // ... for every thread; the FMA loop above is done
+    {
+      const uint8_t* stg = sm + st * kLoraStageBytes;
+      const __nv_bfloat16* xr = reinterpret_cast<const __nv_bfloat16*>(stg);
+      const __nv_bfloat16* ar = xr + kLoraTileM * kLoraKc;
+      const float* zr = reinterpret_cast<const float*>(ar + kLoraTileR * kLoraKc);
+      {
+        const int rr = tid >> 4, k4 = (tid & 15) * 4;  // 16 rows x 64 k, four per thread
+        float4 f;
+        f.x = noisy(__bfloat162float(xr[rr * kLoraKc + k4]), zr[k4]);
+        f.y = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 1]), zr[k4 + 1]);
+        f.z = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 2]), zr[k4 + 2]);
+        f.w = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 3]), zr[k4 + 3]);
+        *reinterpret_cast<float4*>(xsm + rr * kLoraPad + k4) = f;
+      }
+      {
+        const int jj = tid >> 3, k8 = (tid & 7) * 8;  // 32 ranks x 64 k, eight per thread
+        const uint4 raw = *reinterpret_cast<const uint4*>(ar + jj * kLoraKc + k8);
         const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = 0.0f;
+        float4* d = reinterpret_cast<float4*>(asm_ + jj * kLoraPad + k8);
+        d[0] = make_float4(__bfloat162float(e[0]), __bfloat162float(e[1]), __bfloat162float(e[2]), __bfloat162float(e[3]));
+        d[1] = make_float4(__bfloat162float(e[4]), __bfloat162float(e[5]), __bfloat162float(e[6]), __bfloat162float(e[7]));
       }
-      float4* d = reinterpret_cast<float4*>(asm_ + jj * kLoraPad + kk);
-      d[0] = make_float4(f[0], f[1], f[2], f[3]);
-      d[1] = make_float4(f[4], f[5], f[6], f[7]);
     }
-    __syncthreads();
+    __syncthreads();  // fp32 tiles ready; the raw stage is free
+    if (kc + kLoraStages < kc_end) issue_chunk(kc + kLoraStages, st);
+    cp_async_commit();
+    if (++st == kLoraStages) st = 0;
 #pragma unroll 4
     for (int kk = 0; kk < kLoraKc; kk += 4) {
       const float4 x0 = *reinterpret_cast<const float4*>(xsm + (2 * rp) * kLoraPad + kk);
@@ -285,6 +324,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
       acc1 = fmaf(x1.w, av.w, acc1);
     }
   }
+  cp_async_wait_group<0>();
   // Partial tile [kLoraTileM][kLoraTileR] of this K slice -> shared memory,
   // then CTA q of the cluster sums entries q, q + cluster, ... over all slices.
   __syncthreads();
@@ -380,33 +420,57 @@ __device__ __forceinline__ void store_out(const LinearSlot& L, int m, int n, flo
     reinterpret_cast<__nv_bfloat16*>(L.y)[idx] = __float2bfloat16_rn(v);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+// (a, b) -> bf16 pairs hi = (trunc(a), trunc(b)) and lo = (trunc(a - hi_a),
+// trunc(b - hi_b)), element a in the low half.  hi + lo carries each value to
+// ~15 significant bits (relative error < 2^-14); a - hi is exact in fp32.
+// Integer ops only: the conversion pipe is kept busy by the dequant warps.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  const float ra = a - __uint_as_float(ua & 0xFFFF0000u), rb = b - __uint_as_float(ub & 0xFFFF0000u);
+  hi = __byte_perm(ua, ub, 0x7632);
+  lo = __byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x7632);
 }
 
 // LoRA up-projection operands, in the 128-byte-swizzled K-major layout (the
 // rank index j is the MMA's K):
 //   B^T chunk c:  128 rows n  x 64 j   bf16  = B[n0 + n][c*64 + j]   (TMA from B [N][r])
-//   t_hi chunk c: n_tok rows m x 64 j  bf16  = bf16(t[m0 + m][c*64 + j])
-//   t_lo chunk c: n_tok rows m x 64 j  bf16  = bf16(t - t_hi)
-// so B^T . t_hi + B^T . t_lo carries t to ~16 significant bits.  The t tiles
+//   t_hi chunk c: n_tok rows m x 64 j  bf16  = t[m0 + m][c*64 + j] truncated
+//   t_lo chunk c: n_tok rows m x 64 j  bf16  = (t - t_hi) truncated
+// so B^T . t_hi + B^T . t_lo carries t to ~15 significant bits.  The t tiles
 // are built by `nthr` threads (tid < nthr); zero past M and r.
 // The up-projection accumulates into the main accumulator, which the epilogue
 // scales by S * 2^-e_m per token row m; so row m of t enters pre-scaled by
 // (alpha / r) / (S * 2^-e_m) (fp32, before the hi/lo split: a relative change
 // of a few fp32 ulps).  S must be positive and finite; otherwise the row
 // factor is 0 and the call records QERL_ERR_NONFINITE.
-__device__ __forceinline__ float lora_row_factor(const MmaParams& p, const LinearSlot& L, int m) {
-  if (m >= p.M) return 0.0f;
-  const float sr = *L.tensor_scale * __ldg(p.rinv + m);
-  if (!(sr > 0.0f) || sr > 3.0e38f) {
-    record_error(p.status, 6);
-    return 0.0f;
+// Row factors for tokens m0 .. m0 + n_tok - 1 into shared memory `fac`
+// (n_tok floats), computed by `nthr` threads with their loads issued together.
+__device__ __forceinline__ void fill_lora_factors(const MmaParams& p, const LinearSlot& L, uint32_t fac, int m0,
+                                                  int tid, int nthr) {
+  float rv[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = tid + u * nthr;
+    rv[u] = (i < p.n_tok && m0 + i < p.M) ? __ldg(p.rinv + m0 + i) : 0.0f;
   }
-  return L.lora_scale / sr;
+  const float S = *L.tensor_scale;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = tid + u * nthr;
+    if (i >= p.n_tok) break;
+    float f = 0.0f;
+    if (m0 + i < p.M) {
+      const float sr = S * rv[u];
+      if (!(sr > 0.0f) || sr > 3.0e38f)
+        record_error(p.status, 6);
+      else
+        f = L.lora_scale / sr;
+    }
+    stsf(fac + 4u * i, f);
+  }
 }
-__device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t base, int m0, int tid, int nthr) {
+__device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t base, uint32_t fac, int m0, int tid,
+                              int nthr) {
   const int rc = lora_chunks(L.r);
   const uint32_t thi = base + rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
@@ -414,7 +478,7 @@ __device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t 
     const int c = idx / (p.n_tok * 8), rem = idx - c * (p.n_tok * 8);
     const int ml = rem >> 3, g = rem & 7;
     const int m = m0 + ml;
-    const float f = lora_row_factor(p, L, m);
+    const float f = ldsf(fac + 4u * ml);
     float tv[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -426,12 +490,7 @@ __device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t 
     }
     uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float h0 = __bfloat162float(__float2bfloat16_rn(tv[2 * e]));
-      const float h1 = __bfloat162float(__float2bfloat16_rn(tv[2 * e + 1]));
-      hw[e] = pack_bf16x2(h0, h1);
-      lw[e] = pack_bf16x2(tv[2 * e] - h0, tv[2 * e + 1] - h1);
-    }
+    for (int e = 0; e < 4; ++e) split_bf16x2(tv[2 * e], tv[2 * e + 1], hw[e], lw[e]);
     const uint32_t off = c * p.n_tok * 128 + ml * 128 + ((g ^ (ml & 7)) << 4);
     sts128(thi + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
     sts128(tlo + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
@@ -441,7 +500,7 @@ __device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t 
 // Same tiles from the partial sums staged in shared memory by bulk copies:
 // tstage[g][ml][j] = t_part[g][m0 + ml][j] for ml < rows.
 __device__ void build_t_tiles_staged(const MmaParams& p, const LinearSlot& L, uint32_t base, uint32_t tstage,
-                                     int rows, int m0, int tid, int nthr) {
+                                     uint32_t fac, int rows, int tid, int nthr) {
   const int rc = lora_chunks(L.r);
   const uint32_t thi = base + rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
@@ -466,18 +525,13 @@ __device__ void build_t_tiles_staged(const MmaParams& p, const LinearSlot& L, ui
         tv[6] += b.z;
         tv[7] += b.w;
       }
-      const float f = lora_row_factor(p, L, m0 + ml);
+      const float f = ldsf(fac + 4u * ml);
 #pragma unroll
       for (int e = 0; e < 8; ++e) tv[e] *= f;
     }
     uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float h0 = __bfloat162float(__float2bfloat16_rn(tv[2 * e]));
-      const float h1 = __bfloat162float(__float2bfloat16_rn(tv[2 * e + 1]));
-      hw[e] = pack_bf16x2(h0, h1);
-      lw[e] = pack_bf16x2(tv[2 * e] - h0, tv[2 * e + 1] - h1);
-    }
+    for (int e = 0; e < 4; ++e) split_bf16x2(tv[2 * e], tv[2 * e + 1], hw[e], lw[e]);
     const uint32_t off = c * p.n_tok * 128 + ml * 128 + ((g8 ^ (ml & 7)) << 4);
     sts128(thi + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
     sts128(tlo + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
@@ -593,8 +647,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         mbar_init_a(b_empty(s), 1);  // tcgen05.commit
       }
     mbar_init_a(ring_free, NI);
-    // B^T TMA (expect_tx) + the t-tile builders: warp 14 (early) or warps 0-7 (late)
-    mbar_init_a(lora_full, p.lora_early ? 2 : 9);
+    // B^T TMA (expect_tx) + the eight dequant warps, which build the t tiles
+    mbar_init_a(lora_full, 9);
     mbar_init_a(acc_full, NI);
     mbar_init_a(t_full, 1);
     *abort_flag = 0;
@@ -915,8 +969,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         ph ^= 1;
       }
     }
-    if (do_lora && !p.lora_early) {
-      if (warp_wait(ring_free, 0, abort_flag, p.status)) build_t_tiles(p, L, lora_base, m0, threadIdx.x - 32 * kDeqWarp0, 256);
+    if (do_lora) {
+      // The LoRA operand's t tiles, by all 256 dequant threads once their
+      // stream is done: from the rows the LoRA warp staged (early), or from
+      // global memory into the idle ring (late).
+      const int dtid = static_cast<int>(threadIdx.x) - 32 * kDeqWarp0;
+      griddep_wait();  // the row exponents come from the preceding kernel
+      fill_lora_factors(p, L, smv + 4u * p.n_tok, m0, dtid, 256);
+      named_barrier_sync(1, 256);
+      if (p.lora_early) {
+        if (warp_wait(t_full, 0, abort_flag, p.status))
+          build_t_tiles_staged(p, L, lora_base, sbase + p.off_tstage, smv + 4u * p.n_tok, min(p.n_tok, p.M - m0),
+                               dtid, 256);
+      } else if (warp_wait(ring_free, 0, abort_flag, p.status)) {
+        build_t_tiles(p, L, lora_base, smv + 4u * p.n_tok, m0, dtid, 256);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive_a(lora_full);
@@ -938,14 +1005,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             bulk_load(tstage + static_cast<uint32_t>(g * p.n_tok * L.r * 4),
                       L.t + (static_cast<int64_t>(g) * p.M + m0) * L.r, bytes, t_full);
         }
-        if (warp_wait(t_full, 0, abort_flag, p.status)) build_t_tiles_staged(p, L, lora_base, tstage, rows, m0, lane, 32);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_a(lora_full);
+        // The dequant warps build the t tiles from these rows after their main loop.
       } else if (warp_wait(ring_free, 0, abort_flag, p.status)) {
         if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full);
       } else if (lane == 0) {
-        mbar_arrive_a(lora_full);  // after an abort: keep the barrier count consistent
+        mbar_arrive_expect_tx_a(lora_full, 0);  // after an abort: keep the barrier count consistent
       }
     }
   }
@@ -1220,7 +1284,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     P.lora = static_cast<uint32_t>(align_up(ring, 1024));
     P.tstage = P.lora + (lora_early ? lb : 0u);
     P.sm = static_cast<uint32_t>(align_up(P.tstage + (lora_early ? tstage_bytes : 0u), 16));
-    P.bars = static_cast<uint32_t>(align_up(P.sm + static_cast<uint32_t>(n_tok) * 4u, 16));
+    P.bars = static_cast<uint32_t>(align_up(P.sm + static_cast<uint32_t>(n_tok) * 8u, 16));  // row scales, LoRA factors
     // + 1024-byte alignment slack; at least 116 KB so that two CTAs never share
     // an SM (each allocates all of tensor memory, and partners in a cluster
     // wait for one another).
@@ -1306,7 +1370,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   pp.lora_tiles = pp.tile_begin[kMaxLinears];
   const int lora_ctas_y = pp.lora_tiles * pp.groups;
   size_t prep_smem = static_cast<size_t>(K) * 2;
-  if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>((kLoraTileM + kLoraTileR) * kLoraPad) * 4);
+  if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>(kLoraSmemBytes));
   if (prep_smem > static_cast<size_t>(kPrepSmemLimit)) return QERL_ERR_UNSUPPORTED_SHAPE;
   {
     cudaLaunchConfig_t pc{};
