@@ -213,34 +213,41 @@ def linear_flops(lin, m, r=RANK_R):
     return 2.0 * m * lin.n * lin.k + 2.0 * m * lin.k * r + 2.0 * m * r * lin.n
 
 
-# Dominant launch of the decode step: the gate-shaped linear (the largest of
-# the seven, with up and down) at M = 8.  DRAM traffic of one such call
-# (mma_kernel + prep_kernel), from the ncu capture summarized in
-# profiles/mma_kernel_decode_gate_m8.md; None until a capture of the current
-# kernels exists.
-DOMINANT = ("gate", 8)
-DOMINANT_TRAFFIC_BYTES = 39942656  # 39.615 MB (mma_kernel) + 0.327 MB (prep_kernel) DRAM reads, 0 writes
+def group_algorithmic_bytes(lins, m, r=RANK_R):
+    """Minimum HBM/L2 bytes of one grouped launch: every member's weights, output and
+    LoRA adapters, plus the shared input x and noise z once."""
+    k = lins[0].k
+    return (sum(l.n * l.k * BYTES_PER_WEIGHT + m * l.n * 2 + l.k * r * 2 + r * l.n * 2 for l in lins)
+            + m * k * 2 + k * 4)
+
+
+# Dominant launch of the decode step: the grouped gate + up launch (two
+# 18944 x 3584 linears sharing x; the largest of the step's four launches) at
+# M = 8.  DRAM traffic of one such launch (prep_kernel + mma_kernel), from the
+# ncu capture summarized in profiles/mma_kernel_decode_gateup_m8.md; None
+# while no capture of the current kernels exists.
+DOMINANT = ("gate_up", 8)
+DOMINANT_TRAFFIC_BYTES = 79662336  # prep 565,504 + mma 79,033,856 read + 62,976 written (ncu, 1 pass)
 
 
 def dominant_call(q, layers, acts, hbm_peak, reps=64):
-    """Average per-call time of the dominant linear: a graph of back-to-back
-    calls timed with CUDA events on the replaying stream, weights rotating over
-    the layer copies (cold in L2)."""
-    names = [lin.name for lin in wl.QWEN_7B]
-    li, m = names.index(DOMINANT[0]), DOMINANT[1]
+    """Average per-launch time of the dominant grouped launch: a graph of
+    back-to-back launches timed with CUDA events on the replaying stream,
+    weights rotating over the layer copies (cold in L2)."""
+    g, m = DOMINANT
+    idx = [i for i, lin in enumerate(wl.QWEN_7B) if lin.group == g]
+    lins = [wl.QWEN_7B[i] for i in idx]
     a = acts[DECODE_MS.index(m)]
-    lin = wl.QWEN_7B[li]
-    y = a.y[li]
-    g = lin.group
 
     def call(i):
-        ql = layers[i % len(layers)][li]
-        q.check(q.qerl_lora_linear(a.x[g], ql.wp, ql.S, a.z[g], ql.A, ql.B, ALPHA, y, a.ws), "qerl_lora_linear")
+        layer = layers[i % len(layers)]
+        members = [(layer[j].wp, layer[j].S, layer[j].A, layer[j].B, ALPHA, a.y[j]) for j in idx]
+        q.check(q.qerl_lora_linear_group(a.x[g], a.z[g], members, a.ws), "qerl_lora_linear_group")
 
     for i in range(3):
         call(i)
     torch.cuda.synchronize()
-    # The calls are captured into one graph (no host gaps between them); the
+    # The launches are captured into one graph (no host gaps between them); the
     # events on the replaying stream bracket all of them.
     g_ = torch.cuda.CUDAGraph()
     cs = torch.cuda.Stream()
@@ -254,14 +261,15 @@ def dominant_call(q, layers, acts, hbm_peak, reps=64):
     g_.replay()
     e1.record()
     torch.cuda.synchronize()
-    q.check(q.qerl_read_status(a.ws), "dominant call status")
+    q.check(q.qerl_read_status(a.ws), "dominant launch status")
     t_ms = e0.elapsed_time(e1) / reps
-    alg = linear_algorithmic_bytes(lin, m)
+    alg = group_algorithmic_bytes(lins, m)
     achieved = alg / (t_ms * 1e-3) / 1e9
+    names = " + ".join(f"{l.name} {l.n}x{l.k}" for l in lins)
     return {
         "bound": "hbm",
-        "kernel": f"qerl_lora_linear call (prep_kernel + mma_kernel<1>), Qwen2.5-7B {lin.name} "
-                  f"{lin.n}x{lin.k}, M={m}, r={RANK_R}",
+        "kernel": f"qerl_lora_linear_group launch (prep_kernel + mma_kernel<1>), Qwen2.5-7B {names}, "
+                  f"M={m}, r={RANK_R}",
         "achieved": round(achieved, 1),
         "peak": hbm_peak,
         "peak_source": "measured hbm_gbs (MEASURED_PEAKS.json)",
@@ -270,7 +278,7 @@ def dominant_call(q, layers, acts, hbm_peak, reps=64):
         "traffic": DOMINANT_TRAFFIC_BYTES,
         "algorithmic_bytes_per_call": int(alg),
         "us_per_call": round(t_ms * 1e3, 3),
-        "timing": f"CUDA events around one graph replay of {reps} back-to-back calls on the launching "
+        "timing": f"CUDA events around one graph replay of {reps} back-to-back launches on the launching "
                   f"stream, weights rotating over {len(layers)} layer copies (> L2)",
     }
 

@@ -174,7 +174,10 @@ QERL_API qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t 
  *         16-byte aligned).
  * wpacked the n x k weight's codes and scales (n = output features, k = input
  *         features) as packed by qerl_nvfp4_pack, 16-byte aligned.
- * tensor_scale device float, the S written by qerl_nvfp4_quantize.
+ * tensor_scale device float, the S written by qerl_nvfp4_quantize (finite
+ *         and > 0).  With a LoRA branch, a non-positive or non-finite S drops
+ *         the LoRA term and records QERL_ERR_NONFINITE in the status word (the
+ *         up-projection is accumulated pre-divided by S).
  * z       device float[k] or NULL (no noise).
  * A       device bf16 r x k, B device bf16 n x r (row-major), or both NULL /
  *         r == 0 (no LoRA branch).  r % 8 == 0 and r <= 128; A and B
