@@ -5,7 +5,8 @@ One step = one rollout decode pass of a Qwen2.5-7B-shaped decoder layer's
 seven LoRA linears (q, k, v, o, gate, up, down; r = 32, alpha = 64) at each
 decode batch M in {1, 8, 32, 128}: per M, the AQN noise of the four groups
 (qkv, o, gate_up, down; one sampler launch; sigma from the exponential-decay
-schedule, stage = step mod 10) and seven qerl_lora_linear calls.  Inputs are synthetic and seeded; the
+schedule, stage = step mod 10) and the seven linears as four grouped launches
+({q,k,v}, {o}, {gate,up}, {down}; --ungrouped: seven single calls).  Inputs are synthetic and seeded; the
 weights are NVFP4-quantized by the library from fp32 N(0, 0.02^2) with 0.5% of
 input channels scaled x10.  Weights rotate over 8 distinct layer copies
 (1.05 GB, far above the 129 MB L2), so every linear streams its weights from
@@ -15,8 +16,12 @@ HBM.  Each (stage, M) sub-step is one CUDA graph replay.
 weight: E2M1 code + E4M3 scale share) over the timed steps.  Also reported:
 prefill TFLOP/s (Qwen2.5-14B-shaped layer, M = 4096), quantizer GB/s, an
 end-to-end figure through the public API with host buffers, the roofline of
-the decode path, the oracle timed on host cores, and SM clocks sampled during
-the timed region.
+the decode path's largest launch, the oracle timed on host cores, and SM
+clocks sampled during the timed region.  Unless --skip-extra: a single
+Qwen2.5-3B q_proj at M = 4 (weights hot and cold in L2), 8192-step sustained
+decode on the 7B stack at M in {8, 64, 128} with sigma decaying over the run,
+and the Qwen2.5-32B-shaped 64-layer weight stream (one M = 16 step through all
+448 linears, whose quantization from heavy-tailed bf16 is timed too).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -395,6 +400,11 @@ def bench_ours(args):
     # ---- prefill (14B-shaped layer, M = 4096) and quantizer throughput
     extra_prefill = bench_prefill(q, args, bf16_peak) if not args.skip_extra else None
     extra_quant = bench_quantize(q, hbm_peak) if not args.skip_extra else None
+    # ---- the other workloads: single 3B q_proj (hot/cold L2), 32B 64-layer stream (+ its
+    # quantization), long sustained decode on the 7B stack
+    extra_qproj = bench_qproj_3b(q, hbm_peak) if not args.skip_extra else None
+    extra_sustained = bench_sustained(q, layers, hbm_peak) if not args.skip_extra else None
+    extra_32b = bench_32b_stream(q, hbm_peak) if not args.skip_extra else None
 
     # ---- the dominant launch, timed per call
     roofline = dominant_call(q, layers, acts, hbm_peak)
@@ -445,6 +455,13 @@ def bench_ours(args):
         out["prefill"] = extra_prefill
     if extra_quant:
         out["quantize"] = extra_quant
+    if extra_qproj:
+        out["qproj_3b_m4"] = extra_qproj
+    if extra_sustained:
+        out["sustained_decode"] = extra_sustained
+    if extra_32b:
+        out["decode_32b_64layers_m16"] = extra_32b["decode"]
+        out["quantize_32b_all"] = extra_32b["quantize"]
     if rank == 0 and not args.skip_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_oracle(seconds_budget=args.cpu_budget)
     if rank == 0:
@@ -520,6 +537,162 @@ def bench_quantize(q, hbm_peak):
            "bytes_note": "4.5625 B/weight: bf16 read twice (amax pass + encode pass) + 0.5625 B written"}
     del Ws, outs
     torch.cuda.empty_cache()
+    return res
+
+
+def _graph_time_ms(fn, reps, warm=2):
+    """Capture fn() into one CUDA graph, replay `warm` times, then time `reps` replays."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps, g
+
+
+def bench_qproj_3b(q, hbm_peak):
+    """Single Qwen2.5-3B q_proj (2048 x 2048), M = 4, r = 16, alpha = 32, AQN sigma = 1e-2: per-call
+    time with the weights hot in L2 (one copy) and cold (64 rotating copies, 151 MB > L2)."""
+    lin = wl.QWEN_3B_QPROJ
+    m, r, alpha = 4, 16, 32.0
+    copies = [QLinear(q, lin, 3, c, r=r) for c in range(64)]
+    x = wl.normal_bf16_device((m, lin.k), 1.0, 3, 0, 11)
+    z = torch.empty(lin.k, dtype=torch.float32, device="cuda")
+    q.check(q.qerl_aqn_sample(z, 1e-2, 3), "qerl_aqn_sample")
+    y = torch.empty((m, lin.n), dtype=torch.bfloat16, device="cuda")
+    ws = q.workspace(q.qerl_lora_linear_workspace_size(m, lin.n, lin.k, r))
+    reps = 64
+    res = {"workload": "Qwen2.5-3B q_proj 2048x2048, M=4, LoRA r=16 alpha=32, AQN sigma=1e-2"}
+    for name, ncp in (("l2_hot", 1), ("l2_cold", 64)):
+        def calls():
+            for i in range(reps):
+                ql = copies[i % ncp]
+                q.check(q.qerl_lora_linear(x, ql.wp, ql.S, z, ql.A, ql.B, alpha, y, ws), "qerl_lora_linear")
+        t_ms, _ = _graph_time_ms(calls, 5)
+        us = t_ms * 1e3 / reps
+        alg = linear_algorithmic_bytes(lin, m, r)
+        res[name] = {"us_per_call": round(us, 3), "GBps": round(alg / (us * 1e-6) / 1e9, 1),
+                     "frac_of_hbm_peak": round(alg / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+    q.check(q.qerl_read_status(ws), "qproj status")
+    del copies
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_32b_stream(q, hbm_peak):
+    """Qwen2.5-32B-shaped 64-layer weight stream: every linear quantized by the library from bf16
+    ~N(0, 0.02^2) with Student-t(3) outlier channels (each quantize call timed), then one decode
+    step at M = 16 through all 448 linears (64 x (AQN sampler + 4 grouped launches)), one graph."""
+    shapes = wl.QWEN_32B
+    nl = wl.QWEN_32B_LAYERS
+    m = 16
+    ws_q = q.workspace(256)
+    layers = []
+    qt_ms, n_weights = 0.0, 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for li in range(nl):
+        layer = []
+        for j, lin in enumerate(shapes):
+            W = wl.weight_heavy_tail_bf16_device(lin.n, lin.k, 32, li, j)
+            codes = torch.empty((lin.n, lin.k // 2), dtype=torch.uint8, device="cuda")
+            scales = torch.empty((lin.n, lin.k // 16), dtype=torch.uint8, device="cuda")
+            S = torch.empty(1, dtype=torch.float32, device="cuda")
+            e0.record()
+            q.check(q.qerl_nvfp4_quantize(W, codes, scales, S, ws_q), "qerl_nvfp4_quantize")
+            e1.record()
+            e1.synchronize()
+            qt_ms += e0.elapsed_time(e1)
+            n_weights += lin.n * lin.k
+            ql = QLinear.__new__(QLinear)
+            ql.lin, ql.S, ql.wp = lin, S, q.pack(codes, scales)
+            ql.A = wl.normal_bf16_device((RANK_R, lin.k), 1.0 / math.sqrt(lin.k), 32, li, j, 2)
+            ql.B = wl.normal_bf16_device((lin.n, RANK_R), 0.01, 32, li, j, 3)
+            layer.append(ql)
+            del W, codes, scales
+        layers.append(layer)
+    q.check(q.qerl_read_status(ws_q), "quantize status")
+    act = Activations(q, shapes, m, 32)
+
+    def step():
+        for li, layer in enumerate(layers):
+            run_substep(q, layer, act, 5e-3, li)
+
+    reps = 5
+    t_ms, g = _graph_time_ms(step, reps)
+    q.check(q.qerl_read_status(act.ws), "32B step status")
+    wbytes = sum(ql.weight_bytes for layer in layers for ql in layer)
+    alg = nl * sum(linear_algorithmic_bytes(lin, m) for lin in shapes)
+    two_pass = n_weights * (2 + 2 + BYTES_PER_WEIGHT)
+    res = {
+        "decode": {"workload": "Qwen2.5-32B-shaped 64 decoder layers (448 linears, hidden 5120, intermediate 27648, "
+                               "kv 1024), one decode step at M=16, LoRA r=32 alpha=64, per-layer AQN noise",
+                   "weight_bytes": int(wbytes), "ms_per_step": round(t_ms, 3),
+                   "weight_GBps": round(wbytes / (t_ms * 1e-3) / 1e9, 1),
+                   "frac_of_hbm_peak": round(wbytes / (t_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                   "all_bytes_GBps": round(alg / (t_ms * 1e-3) / 1e9, 1),
+                   "timing": f"one CUDA graph of the whole step (320 launches), {reps} timed replays"},
+        "quantize": {"workload": "nvfp4 quantization of all 448 Qwen2.5-32B-shaped matrices from bf16 "
+                                 "N(0,0.02^2) with Student-t(3) outlier channels (0.5%)",
+                     "weights": int(n_weights), "ms_total": round(qt_ms, 3),
+                     "GBps_two_pass_bytes": round(two_pass / (qt_ms * 1e-3) / 1e9, 1),
+                     "frac_of_hbm_peak": round(two_pass / (qt_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                     "timing": "CUDA events around each quantize call, summed"},
+    }
+    del layers, act, g
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_sustained(q, layers, hbm_peak, steps=8192):
+    """Long-rollout decode: `steps` back-to-back layer passes on the 7B-shaped stack (the 8 layer
+    copies in turn) at M in {8, 64, 128}, AQN sigma decaying over 10 equal stages of the run."""
+    shapes = wl.QWEN_7B
+    res = {"workload": f"{steps} back-to-back decode steps (one 7B-shaped layer pass each, weights rotating "
+                       f"over {len(layers)} copies) per M, AQN sigma 1e-2 -> 5e-4 over 10 stages"}
+    per = len(layers)
+    assert steps % (NUM_STAGES * per) == 0 or steps % per == 0
+    layer_wbytes = sum(ql.weight_bytes for ql in layers[0])
+    for m in (8, 64, 128):
+        act = Activations(q, shapes, m, 7)
+        graphs = []
+        cs = torch.cuda.Stream()
+        for st in range(NUM_STAGES):
+            sigma = q.qerl_aqn_sigma(st, NUM_STAGES, SIGMA_START, SIGMA_END)
+            for c in range(per):
+                run_substep(q, layers[c], act, sigma, st)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cs):
+                for c in range(per):
+                    run_substep(q, layers[c], act, sigma, st)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        n_rep = steps // per
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n_rep):
+            graphs[min(NUM_STAGES - 1, i * NUM_STAGES // n_rep)].replay()
+        e1.record()
+        torch.cuda.synchronize()
+        q.check(q.qerl_read_status(act.ws), "sustained status")
+        t_ms = e0.elapsed_time(e1)
+        n_steps = n_rep * per
+        res[str(m)] = {"steps": n_steps, "ms_total": round(t_ms, 2),
+                       "weight_GBps": round(layer_wbytes * n_steps / (t_ms * 1e-3) / 1e9, 1),
+                       "frac_of_hbm_peak": round(layer_wbytes * n_steps / (t_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                       "tokens_per_s_per_layer": round(m * n_steps / (t_ms * 1e-3), 1)}
+        del graphs, act
+        torch.cuda.empty_cache()
     return res
 
 
@@ -651,7 +824,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--skip-extra", action="store_true", help="skip the prefill and quantizer measurements")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="skip the prefill, quantizer, 3B q_proj, sustained and 32B-stream measurements")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ungrouped", action="store_true", help="seven single-linear calls per layer instead of four "

@@ -141,6 +141,22 @@ def weight_f32_device(n: int, k: int, seed: int, *path: int, std: float = 0.02, 
     return W
 
 
+def weight_heavy_tail_bf16_device(n: int, k: int, seed: int, *path: int, std: float = 0.02,
+                                  outlier_frac: float = 0.005, nu: int = 3, device="cuda") -> torch.Tensor:
+    """Device bf16 W [n, k] ~ N(0, std^2), with round(outlier_frac * k) input channels drawn
+    from std * Student-t(nu) instead (t = Z / sqrt(chi2_nu / nu), chi2_nu a sum of nu squared
+    normals; integer nu)."""
+    g = torch_generator(seed, *path, 2, device=device)
+    W = torch.randn((n, k), generator=g, device=device, dtype=torch.float32) * std
+    cols = torch.from_numpy(outlier_channels(k, seed, *path, frac=outlier_frac)).to(device)
+    z = torch.randn((n, cols.numel()), generator=g, device=device, dtype=torch.float32)
+    chi2 = torch.zeros_like(z)
+    for _ in range(nu):
+        chi2 += torch.randn(z.shape, generator=g, device=device, dtype=torch.float32) ** 2
+    W[:, cols] = z / torch.sqrt(chi2 / nu) * std
+    return W.to(torch.bfloat16)
+
+
 def normal_bf16_device(shape, std: float, seed: int, *path: int, device="cuda") -> torch.Tensor:
     g = torch_generator(seed, *path, 3, device=device)
     return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
