@@ -400,6 +400,7 @@ struct MmaParams {
   uint32_t raw_b_bytes;  // coupled: activation bytes per weight stage (kSub slabs)
   uint32_t col_a;  // TMEM column of the A stages (accumulators: issuer i at i * n_tok)
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
+  int wave;        // CTAs per wave (one per SM) when split == 1, else 0
 };
 
 // The LoRA up-projection's B matrices, one TMA map per linear of the launch.
@@ -703,6 +704,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     if (coupled) griddep_wait();
     if (lane == 0) {
+      uint32_t ph = 0;
       for (int i = 0, s = 0; i < nraw; ++i) {
         if (i + kPrefetch < nraw)
           bulk_prefetch_l2(wtile + static_cast<int64_t>(rb + i + kPrefetch) * kRawSlotBytes, kRawSlotBytes);
@@ -711,7 +713,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if (i < early) {
           mbar_arrive_expect_tx_a(raw_full(s), xbytes);
         } else {
-          const uint32_t ph = (i / RS) & 1;
           if (!mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status)) break;
           mbar_arrive_expect_tx_a(raw_full(s), kRawSlotBytes + xbytes);
           bulk_load(sbase + p.off_raw + s * kRawSlotBytes, wtile + static_cast<int64_t>(rst) * kRawSlotBytes,
@@ -721,7 +722,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           bulk_load(sbase + p.off_b + s * p.raw_b_bytes,
                     reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rst) * p.raw_b_bytes, xbytes,
                     raw_full(s));
-        if (++s == RS) s = 0;
+        if (++s == RS) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+      // The tile the next wave runs (one CTA per SM: `wave` CTAs later) gets
+      // its first blocks prefetched into L2 now, so that CTA does not start
+      // on a cold stream.
+      if (kTmemA && p.split == 1 && p.wave > 0) {
+        const int ty = static_cast<int>(blockIdx.y) + p.wave;
+        int gj = 0;
+        while (gj + 1 < p.nlin && ty >= p.lin[gj + 1].tile_begin) ++gj;
+        if (ty < p.lin[p.nlin - 1].tile_begin + (p.lin[p.nlin - 1].N + kTileN - 1) / kTileN) {
+          const uint8_t* nt = p.lin[gj].wpacked + static_cast<int64_t>(ty - p.lin[gj].tile_begin) * raw_total *
+                                                      kRawSlotBytes;
+          for (int i = 0; i < min(kPrefetch, raw_total); ++i)
+            bulk_prefetch_l2(nt + static_cast<int64_t>(i) * kRawSlotBytes, kRawSlotBytes);
+        }
       }
     }
   } else if (warp == kActWarp) {
@@ -1425,6 +1443,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.off_sm = P.sm;
   mp.off_bars = P.bars;
   mp.lora_early = lora_early;
+  mp.wave = split == 1 ? sm_count() : 0;
 
   const uint32_t smem_bytes = P.total;
 
