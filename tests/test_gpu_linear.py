@@ -206,3 +206,27 @@ def test_linear_group_four_with_an_empty_member(q, orc):
     assert q.qerl_read_status(ws) == 0
     for c, y in zip(cases, ys):
         assert_linear_close(y, c.oracle(orc), orc, what=f"group4 n{c.n}")
+
+
+def test_linear_full_wave_separate_activation_ring(q, orc):
+    """100 tokens (separate activation ring) over 152 tiles of 128 rows: one CTA per tile,
+    no K split, a full wave.  Full output against the oracle."""
+    c = Case(q, orc, 100, 152 * 128, 512, 16, 1e-2, seed=31)
+    assert_linear_close(c.gpu(q), c.oracle(orc), orc, what="full wave")
+
+
+def test_linear_group_full_wave_two_members(q, orc):
+    """A grouped launch of 75 + 77 tiles at 96 tokens (ragged last tile): the members' tiles
+    are consecutive on the grid, no K split."""
+    m, k = 96, 512
+    cases = [Case(q, orc, m, n, k, 16, 1e-2, seed=60 + i) for i, n in enumerate([75 * 128, 77 * 128 - 40])]
+    x = cases[0].x
+    for c in cases:
+        c.x, c.x_bits, c.z, c.zd = x, cases[0].x_bits, cases[0].z, cases[0].zd
+    ys = [torch.full((m, c.n), float("nan"), dtype=torch.bfloat16, device="cuda") for c in cases]
+    lin = [(c.wp, c.S, c.A, c.B, c.alpha, y) for c, y in zip(cases, ys)]
+    ws = q.workspace(q.qerl_lora_linear_group_workspace_size(m, k, lin))
+    q.check(q.qerl_lora_linear_group(x, cases[0].zd, lin, ws))
+    assert q.qerl_read_status(ws) == 0
+    for c, y in zip(cases, ys):
+        assert_linear_close(y, c.oracle(orc), orc, what=f"wave group n{c.n}")
