@@ -401,6 +401,7 @@ struct MmaParams {
   uint32_t col_a;  // TMEM column of the A stages (accumulators: issuer i at i * n_tok)
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
   int wave;        // CTAs per wave (one per SM) when split == 1, else 0
+  int stage_out;   // the widest output tile (fp32) fits in the idle ring: staged stores
 };
 
 // The LoRA up-projection's B matrices, one TMA map per linear of the launch.
@@ -1079,8 +1080,52 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const float out = ok ? v[e] * ldsf(smv + 4u * (c + e)) : 0.0f;
         if (p.split > 1)
           stsf(part + 4u * ((c + e) * kTileN + nl), out);
-        else if (m0 + c + e < p.M && n < L.N)
-          store_out(L, m0 + c + e, n, out);
+        else if (!p.stage_out) {
+          if (m0 + c + e < p.M && n < L.N) store_out(L, m0 + c + e, n, out);
+        } else if (L.y_f32) {
+          stsf(sbase + 4u * ((c + e) * kTileN + nl), out);  // staged: [token][128 rows]
+        } else {
+          sts16(sbase + 2u * ((c + e) * kTileN + nl), __bfloat16_as_ushort(__float2bfloat16_rn(out)));
+        }
+      }
+    }
+    if (p.split == 1 && p.stage_out) {
+      // The output tile leaves shared memory (the idle ring) a token row at a
+      // time in 16-byte vectors: far fewer store instructions than one 2- or
+      // 4-byte store per thread and token.
+      fence_proxy_async_smem();  // the staged tile is read by bulk copies below
+      named_barrier_sync(1, 256);
+      const int rows = min(p.n_tok, p.M - m0);
+      const int nvalid = min(kTileN, L.N - n0);
+      const int es = L.y_f32 ? 4 : 2;
+      uint8_t* ybase = reinterpret_cast<uint8_t*>(L.y);
+      const bool vec = (reinterpret_cast<uintptr_t>(ybase) & 15u) == 0 && (static_cast<int64_t>(L.N) * es) % 16 == 0;
+      if (vec && (nvalid * es) % 16 == 0) {
+        // One bulk copy per token row; the writes drain after this CTA has
+        // moved on (it only waits for shared memory to have been read).
+        if (dt < rows) {
+          bulk_store(ybase + (static_cast<int64_t>(m0 + dt) * L.N + n0) * es,
+                     sbase + static_cast<uint32_t>(dt * kTileN * es), static_cast<uint32_t>(nvalid * es));
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+      } else {
+      const int chunks = vec ? nvalid * es / 16 : 0;  // whole 16-byte chunks per token row
+      for (int it = dt; it < rows * chunks; it += 256) {
+        const int ml = it / chunks, ch = it - ml * chunks;
+        const uint4 val = lds128(sbase + static_cast<uint32_t>(ml * kTileN * es + ch * 16));
+        *reinterpret_cast<uint4*>(ybase + (static_cast<int64_t>(m0 + ml) * L.N + n0) * es + ch * 16) = val;
+      }
+      const int e0 = chunks * 16 / es;  // the rest element by element
+      const int rest = nvalid - e0;
+      for (int it = dt; it < rows * rest; it += 256) {
+        const int ml = it / rest, nn = e0 + (it - ml * rest);
+        const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0 + nn;
+        if (L.y_f32)
+          reinterpret_cast<float*>(ybase)[gi] = ldsf(sbase + 4u * (ml * kTileN + nn));
+        else
+          reinterpret_cast<uint16_t*>(ybase)[gi] = lds16(sbase + 2u * (ml * kTileN + nn));
+      }
       }
     }
   }
@@ -1100,6 +1145,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const int per = (p.n_tok + p.split - 1) / p.split;
       const int mb = rank * per;
       const int me = min(min(p.n_tok, mb + per), p.M - m0);
+      // Four consecutive outputs per thread: one 8- (bf16) or 16-byte (f32)
+      // store when the row pitch and base allow it.
+      const bool vec4 = (reinterpret_cast<uintptr_t>(L.y) & 15u) == 0 && L.N % 4 == 0;
       for (int it = dt; it < (me - mb) * (kTileN / 4); it += 256) {
         const int ml = mb + it / (kTileN / 4);
         const int nl4 = 4 * (it % (kTileN / 4));
@@ -1113,9 +1161,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           acc.w += v.w;
         }
         const float out[4] = {acc.x, acc.y, acc.z, acc.w};
+        const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0 + nl4;
+        if (vec4 && n0 + nl4 + 3 < L.N) {
+          if (L.y_f32) {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(L.y) + gi) = acc;
+          } else {
+            uint2 pk;
+            pk.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
+            pk.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(L.y) + gi) = pk;
+          }
+        } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (n0 + nl4 + e < L.N) store_out(L, m0 + ml, n0 + nl4 + e, out[e]);
+          for (int e = 0; e < 4; ++e)
+            if (n0 + nl4 + e < L.N) store_out(L, m0 + ml, n0 + nl4 + e, out[e]);
+        }
       }
     }
     cluster_sync_all();  // partners are done reading this CTA's partial tile
@@ -1444,6 +1506,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.off_bars = P.bars;
   mp.lora_early = lora_early;
   mp.wave = split == 1 ? sm_count() : 0;
+  mp.stage_out = static_cast<uint32_t>(n_tok) * kTileN * 4u <= P.lora ? 1 : 0;
 
   const uint32_t smem_bytes = P.total;
 
