@@ -232,7 +232,7 @@ def group_algorithmic_bytes(lins, m, r=RANK_R):
 # ncu capture summarized in profiles/mma_kernel_decode_gateup_m8.md; None
 # while no capture of the current kernels exists.
 DOMINANT = ("gate_up", 8)
-DOMINANT_TRAFFIC_BYTES = 79662336  # prep 565,504 + mma 79,033,856 read + 62,976 written (ncu, 1 pass)
+DOMINANT_TRAFFIC_BYTES = 79609600  # prep 565,248 + mma 79,023,872 read + 20,480 written (ncu, 1 pass)
 
 
 def dominant_call(q, layers, acts, hbm_peak, reps=64):
