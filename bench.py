@@ -18,8 +18,9 @@ prefill TFLOP/s (Qwen2.5-14B-shaped layer, M = 4096), quantizer GB/s, an
 end-to-end figure through the public API with host buffers, the roofline of
 the decode path's largest launch, the oracle timed on host cores, and SM
 clocks sampled during the timed region.  Unless --skip-extra: a single
-Qwen2.5-3B q_proj at M = 4 (weights hot and cold in L2), 8192-step sustained
-decode on the 7B stack at M in {8, 64, 128} with sigma decaying over the run,
+Qwen2.5-3B q_proj at M = 4 (weights hot and cold in L2), 8192 sustained
+decode steps through a 28-layer 7B-shaped stack at M in {8, 64, 128} (z
+resampled every step, sigma decaying over the run),
 and the Qwen2.5-32B-shaped 64-layer weight stream (one M = 16 step through all
 448 linears, whose quantization from heavy-tailed bf16 is timed too).
 
@@ -403,7 +404,7 @@ def bench_ours(args):
     # ---- the other workloads: single 3B q_proj (hot/cold L2), 32B 64-layer stream (+ its
     # quantization), long sustained decode on the 7B stack
     extra_qproj = bench_qproj_3b(q, hbm_peak) if not args.skip_extra else None
-    extra_sustained = bench_sustained(q, layers, hbm_peak) if not args.skip_extra else None
+    extra_sustained = bench_sustained(q, hbm_peak, dev_index) if not args.skip_extra else None
     extra_32b = bench_32b_stream(q, hbm_peak) if not args.skip_extra else None
 
     # ---- the dominant launch, timed per call
@@ -653,46 +654,83 @@ def bench_32b_stream(q, hbm_peak):
     return res
 
 
-def bench_sustained(q, layers, hbm_peak, steps=8192):
-    """Long-rollout decode: `steps` back-to-back layer passes on the 7B-shaped stack (the 8 layer
-    copies in turn) at M in {8, 64, 128}, AQN sigma decaying over 10 equal stages of the run."""
+def bench_sustained(q, hbm_peak, dev_index, steps=8192):
+    """Long-rollout decode on a 28-layer Qwen2.5-7B-shaped stack (3.67 GB NVFP4): `steps`
+    back-to-back decode steps per M in {8, 64, 128}, a step being one token pass through all
+    28 layers (per layer: one AQN sampler launch for the four noise groups, then the four
+    grouped linear launches).  z is resampled every step (sampler counter = step) and sigma
+    follows qerl_aqn_stage(step, steps, 10).  Launches are eager (the counter changes every
+    step) and go straight to the C entry points with argument lists built once.  Reported:
+    GB/s over the run and min / median over consecutive windows of >= 1 s, clocks sampled."""
     shapes = wl.QWEN_7B
-    res = {"workload": f"{steps} back-to-back decode steps (one 7B-shaped layer pass each, weights rotating "
-                       f"over {len(layers)} copies) per M, AQN sigma 1e-2 -> 5e-4 over 10 stages"}
-    per = len(layers)
-    assert steps % (NUM_STAGES * per) == 0 or steps % per == 0
-    layer_wbytes = sum(ql.weight_bytes for ql in layers[0])
+    nl = wl.QWEN_7B_LAYERS
+    layers = [layer_weights(q, shapes, 47, li) for li in range(nl)]
+    lib = q.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    step_wbytes = nl * sum(ql.weight_bytes for ql in layers[0])
+    sigmas = [q.qerl_aqn_sigma(s, NUM_STAGES, SIGMA_START, SIGMA_END) for s in range(NUM_STAGES)]
+    res = {"workload": f"{steps} back-to-back decode steps per M through a {nl}-layer Qwen2.5-7B-shaped stack "
+                       f"({step_wbytes / 1e9:.2f} GB NVFP4 + LoRA r=32), AQN z resampled every step, sigma "
+                       f"1e-2 -> 5e-4 over 10 stages (qerl_aqn_stage)",
+           "launch": "eager: per layer 1 AQN sampler + 4 grouped linear launches"}
     for m in (8, 64, 128):
         act = Activations(q, shapes, m, 7)
-        graphs = []
-        cs = torch.cuda.Stream()
-        for st in range(NUM_STAGES):
-            sigma = q.qerl_aqn_sigma(st, NUM_STAGES, SIGMA_START, SIGMA_END)
-            for c in range(per):
-                run_substep(q, layers[c], act, sigma, st)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cs):
-                for c in range(per):
-                    run_substep(q, layers[c], act, sigma, st)
-            graphs.append(g)
+        ws_p, ws_n = act.ws.data_ptr(), act.ws.numel() * act.ws.element_size()
+        z_p, z_n = act.z_all.data_ptr(), act.z_all.numel()
+        calls = []
+        for layer in layers:
+            per = []
+            for g in wl.NOISE_GROUPS:
+                members = [(ql.wp, ql.S, ql.A, ql.B, ALPHA, y) for ql, y in zip(layer, act.y) if ql.lin.group == g]
+                arr = q._descs(members)
+                x = act.x[g]
+                per.append((x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), act.z[g].data_ptr(), arr, len(arr)))
+            calls.append(per)
+
+        def step(i):
+            sg = sigmas[q.qerl_aqn_stage(i, steps, NUM_STAGES)]
+            for li, per in enumerate(calls):
+                lib.qerl_aqn_sample(z_p, z_n, sg, 7, li, i, stream)
+                for xp, mm, kk, ld, zp, arr, cnt in per:
+                    lib.qerl_lora_linear_group(xp, mm, kk, ld, zp, arr, cnt, ws_p, ws_n, stream)
+
+        for i in range(2):
+            step(i)
         torch.cuda.synchronize()
-        n_rep = steps // per
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(n_rep):
-            graphs[min(NUM_STAGES - 1, i * NUM_STAGES // n_rep)].replay()
-        e1.record()
+        q.check(q.qerl_read_status(act.ws), "sustained warm-up status")
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        clocks = ClockSampler(dev_index)
+        clocks.start()
+        ev[0].record()
+        h0 = time.perf_counter()
+        for i in range(steps):
+            step(i)
+            ev[i + 1].record()
+        host_s = time.perf_counter() - h0
         torch.cuda.synchronize()
+        clk = clocks.stop()
         q.check(q.qerl_read_status(act.ws), "sustained status")
-        t_ms = e0.elapsed_time(e1)
-        n_steps = n_rep * per
-        res[str(m)] = {"steps": n_steps, "ms_total": round(t_ms, 2),
-                       "weight_GBps": round(layer_wbytes * n_steps / (t_ms * 1e-3) / 1e9, 1),
-                       "frac_of_hbm_peak": round(layer_wbytes * n_steps / (t_ms * 1e-3) / 1e9 / hbm_peak, 4),
-                       "tokens_per_s_per_layer": round(m * n_steps / (t_ms * 1e-3), 1)}
-        del graphs, act
+        dts = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+        total = sum(dts)
+        windows, acc_ms, acc_n = [], 0.0, 0
+        for d in dts:
+            acc_ms += d
+            acc_n += 1
+            if acc_ms >= 1000.0:
+                windows.append(step_wbytes * acc_n / (acc_ms * 1e-3) / 1e9)
+                acc_ms, acc_n = 0.0, 0
+        gbps = step_wbytes * steps / (total * 1e-3) / 1e9
+        res[str(m)] = {"steps": steps, "s_total": round(total / 1e3, 2), "ms_per_step": round(total / steps, 3),
+                       "weight_GBps": round(gbps, 1), "frac_of_hbm_peak": round(gbps / hbm_peak, 4),
+                       "window_GBps_min": round(min(windows), 1) if windows else None,
+                       "window_GBps_median": round(statistics.median(windows), 1) if windows else None,
+                       "windows": len(windows), "tokens_per_s": round(m * steps / (total * 1e-3), 1),
+                       "host_enqueue_ms_per_step": round(host_s * 1e3 / steps, 3),
+                       "clocks": clk}
+        del calls, act
         torch.cuda.empty_cache()
+    del layers
+    torch.cuda.empty_cache()
     return res
 
 
