@@ -163,30 +163,47 @@ def layer_weights(q, shapes, seed, copy):
 
 
 class Activations:
-    """Per-M inputs (one x and one z per AQN group), outputs and a workspace."""
+    """Per-M inputs (one x and one z per AQN group), outputs and a workspace.  The
+    inputs are views of one buffer and the outputs views of another, so a step's
+    host copies are one transfer each way."""
 
     def __init__(self, q, shapes, m, seed):
         self.m = m
         ks = {}
         for lin in shapes:
             ks[lin.group] = lin.k
-        self.x = {g: wl.normal_bf16_device((m, k), 1.0, seed, m, gi, 11) for gi, (g, k) in enumerate(ks.items())}
+        self.x_all = torch.empty(m * sum(ks.values()), dtype=torch.bfloat16, device="cuda")
+        self.x, off = {}, 0
+        for gi, (g, k) in enumerate(ks.items()):
+            self.x[g] = self.x_all[off:off + m * k].view(m, k)
+            self.x[g].copy_(wl.normal_bf16_device((m, k), 1.0, seed, m, gi, 11))
+            off += m * k
         # one noise buffer for the layer; each AQN group is a 16-byte aligned slice of it
         self.z_all = torch.zeros(sum(ks.values()), dtype=torch.float32, device="cuda")
         self.z, off = {}, 0
         for g, k in ks.items():
             self.z[g] = self.z_all[off:off + k]
             off += k
-        self.y = [torch.empty((m, lin.n), dtype=torch.bfloat16, device="cuda") for lin in shapes]
+        self.y_all = torch.empty(m * sum(lin.n for lin in shapes), dtype=torch.bfloat16, device="cuda")
+        self.y, off = [], 0
+        for lin in shapes:
+            self.y.append(self.y_all[off:off + m * lin.n].view(m, lin.n))
+            off += m * lin.n
         need = max(q.qerl_lora_linear_workspace_size(m, lin.n, lin.k, RANK_R) for lin in shapes)
         # a group of up to three rank-RANK_R linears needs room for three LoRA partial sums
         need += 2 * q.qerl_lora_linear_workspace_size(m, 0, max(lin.k for lin in shapes), RANK_R)
         self.ws = q.workspace(need)
 
     def io_bytes(self):
-        h2d = sum(t.numel() * t.element_size() for t in self.x.values())
-        d2h = sum(t.numel() * t.element_size() for t in self.y)
-        return h2d, d2h
+        return self.x_all.numel() * self.x_all.element_size(), self.y_all.numel() * self.y_all.element_size()
+
+    def group_descs(self, q, layer):
+        """Per AQN group: (x, z, descriptor array) of its grouped launch on this layer."""
+        out = []
+        for g in wl.NOISE_GROUPS:
+            members = [(ql.wp, ql.S, ql.A, ql.B, ALPHA, y) for ql, y in zip(layer, self.y) if ql.lin.group == g]
+            out.append((self.x[g], self.z[g], q.linear_descs(members)))
+        return out
 
 
 # Linears of one input run as one grouped launch: {q,k,v}, {o}, {gate,up}, {down}.
@@ -682,7 +699,7 @@ def bench_sustained(q, hbm_peak, dev_index, steps=8192):
             per = []
             for g in wl.NOISE_GROUPS:
                 members = [(ql.wp, ql.S, ql.A, ql.B, ALPHA, y) for ql, y in zip(layer, act.y) if ql.lin.group == g]
-                arr = q._descs(members)
+                arr = q.linear_descs(members)
                 x = act.x[g]
                 per.append((x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), act.z[g].data_ptr(), arr, len(arr)))
             calls.append(per)
@@ -698,6 +715,13 @@ def bench_sustained(q, hbm_peak, dev_index, steps=8192):
             step(i)
         torch.cuda.synchronize()
         q.check(q.qerl_read_status(act.ws), "sustained warm-up status")
+        # host cost of enqueuing a step while the launch queue still has room (two steps
+        # after a sync); in the long run below the queue is full and the host waits on it
+        h0 = time.perf_counter()
+        step(0)
+        step(1)
+        host_free_ms = (time.perf_counter() - h0) * 1e3 / 2
+        torch.cuda.synchronize()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
         clocks = ClockSampler(dev_index)
         clocks.start()
@@ -726,6 +750,7 @@ def bench_sustained(q, hbm_peak, dev_index, steps=8192):
                        "window_GBps_median": round(statistics.median(windows), 1) if windows else None,
                        "windows": len(windows), "tokens_per_s": round(m * steps / (total * 1e-3), 1),
                        "host_enqueue_ms_per_step": round(host_s * 1e3 / steps, 3),
+                       "host_enqueue_ms_per_step_queue_free": round(host_free_ms, 3),
                        "clocks": clk}
         del calls, act
         torch.cuda.empty_cache()
@@ -737,19 +762,26 @@ def bench_sustained(q, hbm_peak, dev_index, steps=8192):
 def bench_e2e(q, layers, acts, args, copy_for, sigma_for, step_wbytes, world, barrier):
     """Same decode step through the public API, eager calls, inputs copied from pinned host
     memory and outputs copied back to pinned host memory inside the timed region."""
-    host_x = [{g: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for g, t in a.x.items()}
-              for a in acts]
-    host_y = [[torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in a.y] for a in acts]
+    host_x = [torch.empty(a.x_all.shape, dtype=a.x_all.dtype, pin_memory=True).copy_(a.x_all.cpu()) for a in acts]
+    host_y = [torch.empty(a.y_all.shape, dtype=a.y_all.dtype, pin_memory=True) for a in acts]
     h2d = sum(a.io_bytes()[0] for a in acts)
     d2h = sum(a.io_bytes()[1] for a in acts)
+    # each (layer copy, M) pair's descriptor arrays, built once
+    descs = {}
 
     def e2e_step(i):
         for j, a in enumerate(acts):
-            for g, t in a.x.items():
-                t.copy_(host_x[j][g], non_blocking=True)
-            run_substep(q, layers[copy_for(i, j)], a, sigma_for(i), i % NUM_STAGES)
-            for y, hy in zip(a.y, host_y[j]):
-                hy.copy_(y, non_blocking=True)
+            a.x_all.copy_(host_x[j], non_blocking=True)
+            c = copy_for(i, j)
+            if not GROUPED:
+                run_substep(q, layers[c], a, sigma_for(i), i % NUM_STAGES)
+            else:
+                if (c, j) not in descs:
+                    descs[(c, j)] = a.group_descs(q, layers[c])
+                q.check(q.qerl_aqn_sample(a.z_all, sigma_for(i), 0, 0, i % NUM_STAGES), "qerl_aqn_sample")
+                for x, z, arr in descs[(c, j)]:
+                    q.check(q.qerl_lora_linear_group(x, z, arr, a.ws), "qerl_lora_linear_group")
+            host_y[j].copy_(a.y_all, non_blocking=True)
 
     for i in range(max(2, args.warmup)):
         e2e_step(i)

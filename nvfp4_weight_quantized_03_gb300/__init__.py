@@ -20,6 +20,9 @@ The functions named like the C entry points take torch tensors:
     qerl_lora_linear_group(x, z, [(wpacked, tensor_scale, A, B, alpha, y), ...], workspace)
     qerl_read_status(workspace)
 
+`linear_descs()` builds the descriptor array of a group once; passing it
+instead of the list skips that marshalling on every call.
+
 and return the qerl_status integer (QERL_OK == 0).  `check()` turns a
 non-zero status into an exception.  `quantize()`, `pack()` and
 `lora_linear()` are conveniences that allocate the outputs with torch (the
@@ -39,7 +42,7 @@ __all__ = [
     "qerl_nvfp4_quantize_workspace_size", "qerl_aqn_sigma", "qerl_aqn_stage", "qerl_aqn_sample",
     "qerl_nvfp4_packed_size", "qerl_nvfp4_pack", "pack",
     "qerl_lora_linear_workspace_size", "qerl_lora_linear", "qerl_lora_linear_noalloc", "qerl_read_status",
-    "qerl_lora_linear_group", "qerl_lora_linear_group_workspace_size", "LinearDesc",
+    "qerl_lora_linear_group", "qerl_lora_linear_group_workspace_size", "LinearDesc", "linear_descs",
     "quantize", "lora_linear", "workspace",
 ]
 
@@ -239,7 +242,10 @@ def qerl_lora_linear_noalloc(x, wpacked, tensor_scale, z, A, B, alpha, y, stream
 
 
 def _descs(linears):
-    """[(wpacked, tensor_scale, A, B, alpha, y), ...] -> ctypes array of LinearDesc."""
+    """[(wpacked, tensor_scale, A, B, alpha, y), ...] -> ctypes array of LinearDesc
+    (an array built before is passed through)."""
+    if isinstance(linears, ctypes.Array):
+        return linears
     arr = (LinearDesc * len(linears))()
     for d, (wp, ts, A, B, alpha, y) in zip(arr, linears):
         d.wpacked, d.tensor_scale, d.n = _p(wp), _p(ts), y.shape[1]
@@ -249,6 +255,12 @@ def _descs(linears):
     return arr
 
 
+def linear_descs(linears):
+    """The qerl_linear_desc array of a group, [(wpacked, tensor_scale, A, B, alpha, y), ...],
+    built once: the array holds raw pointers, so the tensors must outlive it."""
+    return _descs(linears)
+
+
 def qerl_lora_linear_group_workspace_size(m: int, k: int, linears) -> int:
     arr = _descs(linears)
     return lib().qerl_lora_linear_group_workspace_size(int(m), int(k), arr, len(arr))
@@ -256,7 +268,8 @@ def qerl_lora_linear_group_workspace_size(m: int, k: int, linears) -> int:
 
 def qerl_lora_linear_group(x, z, linears, workspace, stream=None) -> int:
     """Up to four linears of one input x [m, k] (bf16) and noise z: linears is a list of
-    (wpacked, tensor_scale, A, B, alpha, y) with y [m, n_i]; one launch for all."""
+    (wpacked, tensor_scale, A, B, alpha, y) with y [m, n_i], or its linear_descs() array;
+    one launch for all."""
     m, k = x.shape
     arr = _descs(linears)
     return lib().qerl_lora_linear_group(_p(x), m, k, x.stride(0), _p(z), arr, len(arr), _p(workspace),

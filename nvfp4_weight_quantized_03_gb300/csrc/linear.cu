@@ -1215,10 +1215,19 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uin
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// SM count of the current device, queried once per device.
 int sm_count() {
-  int dev = 0, sms = 148;
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices] = {};
+  int dev = 0;
   cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 148;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < kMaxDevices && sms > 0) cached[dev].store(sms, std::memory_order_relaxed);
   return sms;
 }
 
@@ -1505,7 +1514,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.off_sm = P.sm;
   mp.off_bars = P.bars;
   mp.lora_early = lora_early;
-  mp.wave = split == 1 ? sm_count() : 0;
+  mp.wave = split == 1 ? sms : 0;
   mp.stage_out = static_cast<uint32_t>(n_tok) * kTileN * 4u <= P.lora ? 1 : 0;
 
   const uint32_t smem_bytes = P.total;

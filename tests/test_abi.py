@@ -8,6 +8,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 from conftest import ROOT
 
@@ -141,6 +142,21 @@ def test_group_validation(L):
     assert 0 < lo < hi
     assert E[_group(L, [ok, _desc(A=0x6000, B=0x7000, r=64)], wsb=hi - 1)] == "QERL_ERR_WORKSPACE"
     assert L.qerl_lora_linear_group_workspace_size(4, 128, (q.LinearDesc * 1)(ok), 5) == 0
+
+
+def test_linear_descs_built_once():
+    """A group's descriptor array, built once, carries each member's fields and is passed
+    through unchanged by the group call's marshalling."""
+    y = torch.empty((4, 256), dtype=torch.bfloat16)
+    y32 = torch.empty((4, 128), dtype=torch.float32)
+    A = torch.empty((16, 128), dtype=torch.bfloat16)
+    B = torch.empty((256, 16), dtype=torch.bfloat16)
+    arr = q.linear_descs([(0x2000, 0x3000, A, B, 32.0, y), (0x4000, 0x3010, None, None, 0.0, y32)])
+    assert q._descs(arr) is arr
+    d0, d1 = arr[0], arr[1]
+    assert (d0.wpacked, d0.tensor_scale, d0.n, d0.r, d0.alpha) == (0x2000, 0x3000, 256, 16, 32.0)
+    assert (d0.A, d0.B, d0.y, d0.y_dtype) == (A.data_ptr(), B.data_ptr(), y.data_ptr(), q.QERL_BF16)
+    assert (d1.wpacked, d1.n, d1.r, d1.A, d1.B, d1.y_dtype) == (0x4000, 128, 0, None, None, q.QERL_F32)
 
 
 @no_gpu_only

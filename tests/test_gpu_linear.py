@@ -189,6 +189,14 @@ def test_linear_group_matches_single_calls(q, orc, m):
         assert_linear_close(y, c.oracle(orc), orc, what=f"group n{c.n} r{c.r}")
         single = c.gpu(q)
         assert torch.allclose(y.float(), single.float(), rtol=1e-2, atol=1e-3)
+    # the same group through a descriptor array built once: the same launch, bit for bit
+    ys2 = [torch.full_like(y, float("nan")) for y in ys]
+    arr = q.linear_descs([(c.wp, c.S, c.A, c.B, c.alpha, y) for c, y in zip(cases, ys2)])
+    for _ in range(2):
+        q.check(q.qerl_lora_linear_group(x, cases[0].zd, arr, ws))
+    assert q.qerl_read_status(ws) == 0
+    for y, y2 in zip(ys, ys2):
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
 def test_linear_group_four_with_an_empty_member(q, orc):
