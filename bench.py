@@ -397,7 +397,8 @@ def bench_ours(args):
     per_m = {}
     sub_bytes_total, sub_time_total = 0.0, 0.0
     for j, m in enumerate(DECODE_MS):
-        t_ms = sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K
+        ts = sorted(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+        t_ms = sum(ts) / K
         alg = sum(linear_algorithmic_bytes(lin, m) for lin in shapes)
         sub_bytes_total += alg
         sub_time_total += t_ms
@@ -412,6 +413,7 @@ def bench_ours(args):
             "roofline_frac_max_bw_tc": round(max(t_bw, t_tc) / t_ms, 4),
             "TFLOPs": round(flops / (t_ms * 1e-3) / 1e12, 2),
             "tokens_per_s_per_layer": round(m / (t_ms * 1e-3), 1),
+            "us_per_layer_p10_median_p90": [round(_pct(ts, p) * 1e3, 2) for p in (10, 50, 90)],
         }
     value = world * step_wbytes * K / (elapsed_ms * 1e-3) / 1e9
 
@@ -489,6 +491,12 @@ def bench_ours(args):
         dist.destroy_process_group()
 
 
+def _pct(sorted_vals, p):
+    """p-th percentile (nearest rank) of an ascending list."""
+    i = min(len(sorted_vals) - 1, max(0, int(round(p / 100.0 * (len(sorted_vals) - 1)))))
+    return sorted_vals[i]
+
+
 def bench_prefill(q, args, bf16_peak):
     shapes = wl.QWEN_14B
     m = 4096
@@ -504,20 +512,43 @@ def bench_prefill(q, args, bf16_peak):
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
-    reps = 10
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
+    reps = 50
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for i in range(reps):
         g.replay()
-    e1.record()
+        ev[i + 1].record()
     torch.cuda.synchronize()
-    t_ms = e0.elapsed_time(e1) / reps
+    ts = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
+    t_ms = sum(ts) / reps
     q.check(q.qerl_read_status(act.ws), "prefill status")
     flops = sum(linear_flops(lin, m) for lin in shapes)
     tf = flops / (t_ms * 1e-3) / 1e12
+    # each grouped launch alone (eager, back to back; a launch is ~1 ms, so launch cost is noise)
+    per_launch = {}
+    for g_name, (x, z, arr) in zip(wl.NOISE_GROUPS, act.group_descs(q, layer)):
+        lins = [ql.lin for ql in layer if ql.lin.group == g_name]
+        for _ in range(2):
+            q.check(q.qerl_lora_linear_group(x, z, arr, act.ws), "qerl_lora_linear_group")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_rep = 20
+        e0.record()
+        for _ in range(n_rep):
+            q.check(q.qerl_lora_linear_group(x, z, arr, act.ws), "qerl_lora_linear_group")
+        e1.record()
+        torch.cuda.synchronize()
+        lt = e0.elapsed_time(e1) / n_rep
+        lf = sum(linear_flops(lin, m) for lin in lins)
+        per_launch[g_name] = {"ms": round(lt, 4), "TFLOPs": round(lf / (lt * 1e-3) / 1e12, 1),
+                              "frac_of_bf16_peak": round(lf / (lt * 1e-3) / 1e12 / bf16_peak, 4)}
+    q.check(q.qerl_read_status(act.ws), "prefill status")
     res = {"workload": "Qwen2.5-14B decoder-layer linears, M=4096 (8 x 512 prompt tokens), r=32 alpha=64, "
                        "AQN sigma=5e-3", "ms_per_layer": round(t_ms, 4), "TFLOPs": round(tf, 1),
            "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_TFLOPs": bf16_peak,
+           "ms_per_layer_p10_median_p90": [round(_pct(ts, p), 4) for p in (10, 50, 90)],
+           "per_launch": per_launch,
+           "timing": f"{reps} graph replays of the layer (AQN sampler + 4 grouped launches), one event pair "
+                     "each; per_launch: each grouped launch {q,k,v}, {o}, {gate,up}, {down} 20x back to back",
            "note": "fp16 operands run at the bf16 dense rate; peak = measured cuBLAS bf16 burst"}
     del layer, act
     torch.cuda.empty_cache()
@@ -552,7 +583,9 @@ def bench_quantize(q, hbm_peak):
     res = {"workload": "NVFP4 quantization of one Qwen2.5-7B layer's 7 matrices from bf16 (233 M weights)",
            "ms": round(t_ms, 4), "GBps_two_pass_bytes": round(two_pass / (t_ms * 1e-3) / 1e9, 1),
            "frac_of_hbm_peak": round(two_pass / (t_ms * 1e-3) / 1e9 / hbm_peak, 4),
-           "bytes_note": "4.5625 B/weight: bf16 read twice (amax pass + encode pass) + 0.5625 B written"}
+           "GBps_single_pass_bytes": round(nw * (2 + BYTES_PER_WEIGHT) / (t_ms * 1e-3) / 1e9, 1),
+           "bytes_note": "4.5625 B/weight: bf16 read twice (amax pass + encode pass) + 0.5625 B written; "
+                         "single-pass lower bound 2.5625 B/weight"}
     del Ws, outs
     torch.cuda.empty_cache()
     return res
@@ -658,12 +691,14 @@ def bench_32b_stream(q, hbm_peak):
                    "weight_GBps": round(wbytes / (t_ms * 1e-3) / 1e9, 1),
                    "frac_of_hbm_peak": round(wbytes / (t_ms * 1e-3) / 1e9 / hbm_peak, 4),
                    "all_bytes_GBps": round(alg / (t_ms * 1e-3) / 1e9, 1),
+                   "tokens_per_s": round(m / (t_ms * 1e-3), 1),
                    "timing": f"one CUDA graph of the whole step (320 launches), {reps} timed replays"},
         "quantize": {"workload": "nvfp4 quantization of all 448 Qwen2.5-32B-shaped matrices from bf16 "
                                  "N(0,0.02^2) with Student-t(3) outlier channels (0.5%)",
                      "weights": int(n_weights), "ms_total": round(qt_ms, 3),
                      "GBps_two_pass_bytes": round(two_pass / (qt_ms * 1e-3) / 1e9, 1),
                      "frac_of_hbm_peak": round(two_pass / (qt_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                     "GBps_single_pass_bytes": round(n_weights * (2 + BYTES_PER_WEIGHT) / (qt_ms * 1e-3) / 1e9, 1),
                      "timing": "CUDA events around each quantize call, summed"},
     }
     del layers, act, g
