@@ -72,6 +72,17 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x, returned on every rank (x itself for one process):
+    the job's time is its slowest replica's."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -385,12 +396,7 @@ def bench_ours(args):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = tt.item()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, "cuda")
     for act in acts:
         q.check(q.qerl_read_status(act.ws), "status after timed region")
 
@@ -833,7 +839,7 @@ def bench_e2e(q, layers, acts, args, copy_for, sigma_for, step_wbytes, world, ba
     wall = time.perf_counter() - t
     barrier()
     dev_ms = e0.elapsed_time(e1)
-    t_s = max(wall, dev_ms * 1e-3)
+    t_s = max_over_ranks(max(wall, dev_ms * 1e-3), world, "cuda")
     return {"value": round(world * step_wbytes * steps / t_s / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": round(t_s * 1e3 / steps, 4),

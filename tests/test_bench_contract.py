@@ -54,3 +54,29 @@ def test_reference_arm_two_ranks_rank0_reports():
     assert len(lines) == 1, r.stdout[-2000:]
     _check(lines[0])
     assert lines[0]["n_gpus"] == 2
+
+
+_RANKS_SCRIPT = r"""
+import os, sys
+import torch.distributed as dist
+sys.path.insert(0, os.environ["QERL_ROOT"])
+import bench
+world, rank, _ = bench.dist_env()
+dist.init_process_group("gloo")
+got = bench.max_over_ranks(1.5 + rank, world, "cpu")
+print(f"RANK {rank} {world} {got}", flush=True)
+dist.destroy_process_group()
+"""
+
+
+def test_timing_is_max_over_two_gloo_ranks(tmp_path):
+    """The replica path's job time is the slowest rank's, and every rank sees it (two gloo ranks)."""
+    script = tmp_path / "ranks.py"
+    script.write_text(_RANKS_SCRIPT)
+    env = dict(os.environ, QERL_ROOT=str(ROOT))
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", "29541", str(script)],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    got = sorted(l.split()[1:] for l in r.stdout.splitlines() if l.startswith("RANK "))
+    assert got == [["0", "2", "2.5"], ["1", "2", "2.5"]], r.stdout
