@@ -64,7 +64,8 @@ import bench
 world, rank, _ = bench.dist_env()
 dist.init_process_group("gloo")
 got = bench.max_over_ranks(1.5 + rank, world, "cpu")
-print(f"RANK {rank} {world} {got}", flush=True)
+with open(os.path.join(os.environ["QERL_OUT"], f"rank{rank}.txt"), "w") as f:
+    f.write(f"{rank} {world} {got}")
 dist.destroy_process_group()
 """
 
@@ -73,10 +74,10 @@ def test_timing_is_max_over_two_gloo_ranks(tmp_path):
     """The replica path's job time is the slowest rank's, and every rank sees it (two gloo ranks)."""
     script = tmp_path / "ranks.py"
     script.write_text(_RANKS_SCRIPT)
-    env = dict(os.environ, QERL_ROOT=str(ROOT))
+    env = dict(os.environ, QERL_ROOT=str(ROOT), QERL_OUT=str(tmp_path))
     r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
                         "--master-addr", "127.0.0.1", "--master-port", "29541", str(script)],
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
-    got = sorted(l.split()[1:] for l in r.stdout.splitlines() if l.startswith("RANK "))
-    assert got == [["0", "2", "2.5"], ["1", "2", "2.5"]], r.stdout
+    got = [(tmp_path / f"rank{i}.txt").read_text().split() for i in range(2)]
+    assert got == [["0", "2", "2.5"], ["1", "2", "2.5"]]
