@@ -485,6 +485,8 @@ def bench_ours(args):
         out["qproj_3b_m4"] = extra_qproj
     if extra_sustained:
         out["sustained_decode"] = extra_sustained
+    if not args.skip_extra:
+        out["aqn_schedules"] = aqn_schedule_table(q)
     if extra_32b:
         out["decode_32b_64layers_m16"] = extra_32b["decode"]
         out["quantize_32b_all"] = extra_32b["quantize"]
@@ -495,6 +497,23 @@ def bench_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def aqn_schedule_table(q, num_stages=NUM_STAGES, calls=20000):
+    """The four sigma decay schedules of the library (host functions) per stage, and their host
+    cost per call (the schedule is evaluated once per training step)."""
+    names = {q.QERL_SCHEDULE_EXPONENTIAL: "exponential", q.QERL_SCHEDULE_LINEAR: "linear",
+             q.QERL_SCHEDULE_COSINE: "cosine", q.QERL_SCHEDULE_LOGARITHMIC: "logarithmic"}
+    lib = q.lib()
+    out = {"num_stages": num_stages, "sigma_start": SIGMA_START, "sigma_end": SIGMA_END}
+    for sch, name in names.items():
+        out[name] = [float(f"{q.qerl_aqn_sigma_schedule(sch, st, num_stages, SIGMA_START, SIGMA_END):.6e}")
+                     for st in range(num_stages)]
+    t = time.perf_counter()
+    for i in range(calls):
+        lib.qerl_aqn_sigma_schedule(i & 3, i % num_stages, num_stages, SIGMA_START, SIGMA_END)
+    out["host_ns_per_call_incl_ctypes"] = round((time.perf_counter() - t) * 1e9 / calls, 1)
+    return out
 
 
 def _pct(sorted_vals, p):

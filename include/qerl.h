@@ -153,6 +153,25 @@ QERL_API qerl_status qerl_nvfp4_pack(const uint8_t* codes, const uint8_t* scales
 QERL_API double qerl_aqn_sigma(int stage, int num_stages, double sigma_start, double sigma_end);
 QERL_API int qerl_aqn_stage(int64_t step, int64_t total_steps, int num_stages);
 
+/* The decay schedules the digest's AQN section compares ("Why exponential
+ * decay"; the ablation's Figures 9 and 15), over the same stages as
+ * qerl_aqn_sigma: with k = stage + 1 and u = (k-1)/(K-1),
+ *   QERL_SCHEDULE_EXPONENTIAL  sigma_start * (sigma_end/sigma_start)^u  (Eq. 8,
+ *                              identical to qerl_aqn_sigma)
+ *   QERL_SCHEDULE_LINEAR       sigma_start - (sigma_start - sigma_end) * u
+ *   QERL_SCHEDULE_COSINE       sigma_end + (sigma_start - sigma_end) * (1 + cos(pi u)) / 2
+ *   QERL_SCHEDULE_LOGARITHMIC  sigma_start - (sigma_start - sigma_end) * ln(k) / ln(K)
+ * stage < 0 returns 0, stage >= K clamps to K-1, num_stages <= 1 returns
+ * sigma_start.  An unknown schedule returns NaN.  Host, pure, no CUDA. */
+typedef enum {
+  QERL_SCHEDULE_EXPONENTIAL = 0,
+  QERL_SCHEDULE_LINEAR = 1,
+  QERL_SCHEDULE_COSINE = 2,
+  QERL_SCHEDULE_LOGARITHMIC = 3
+} qerl_schedule;
+QERL_API double qerl_aqn_sigma_schedule(int schedule, int stage, int num_stages, double sigma_start,
+                                        double sigma_end);
+
 /* AQN noise vector ("Adaptive Quantization Noise", Eq. 7: Z ~ N(0, sigma^2 I),
  * one value per input channel, resampled per forward pass).  Generator (the
  * digest only says Gaussian): channels 4i..4i+3 come from Philox4x32-10

@@ -12,6 +12,7 @@ The functions named like the C entry points take torch tensors:
     qerl_nvfp4_amax(W, amax, workspace)
     qerl_aqn_sigma(stage, num_stages, sigma_start, sigma_end)       (host)
     qerl_aqn_stage(step, total_steps, num_stages)                   (host)
+    qerl_aqn_sigma_schedule(schedule, stage, num_stages, ...)       (host)
     qerl_aqn_sample(z, sigma, seed, stream_id, counter)
     qerl_nvfp4_packed_size(n, k)                                    (host)
     qerl_nvfp4_pack(codes, scales, packed)
@@ -40,6 +41,8 @@ __all__ = [
     "QERL_OK", "QERL_F32", "QERL_BF16", "QerlError", "check", "lib", "lib_path", "status_string",
     "qerl_nvfp4_quantize", "qerl_nvfp4_quantize_with_scale", "qerl_nvfp4_amax",
     "qerl_nvfp4_quantize_workspace_size", "qerl_aqn_sigma", "qerl_aqn_stage", "qerl_aqn_sample",
+    "qerl_aqn_sigma_schedule", "QERL_SCHEDULE_EXPONENTIAL", "QERL_SCHEDULE_LINEAR", "QERL_SCHEDULE_COSINE",
+    "QERL_SCHEDULE_LOGARITHMIC",
     "qerl_nvfp4_packed_size", "qerl_nvfp4_pack", "pack",
     "qerl_lora_linear_workspace_size", "qerl_lora_linear", "qerl_lora_linear_noalloc", "qerl_read_status",
     "qerl_lora_linear_group", "qerl_lora_linear_group_workspace_size", "LinearDesc", "linear_descs",
@@ -55,6 +58,7 @@ class LinearDesc(ctypes.Structure):
 
 QERL_OK = 0
 QERL_F32, QERL_BF16 = 0, 1
+QERL_SCHEDULE_EXPONENTIAL, QERL_SCHEDULE_LINEAR, QERL_SCHEDULE_COSINE, QERL_SCHEDULE_LOGARITHMIC = 0, 1, 2, 3
 STATUS_NAMES = {0: "QERL_OK", 1: "QERL_ERR_INVALID_ARGUMENT", 2: "QERL_ERR_UNSUPPORTED_SHAPE",
                 3: "QERL_ERR_MISALIGNED", 4: "QERL_ERR_CUDA", 5: "QERL_ERR_TIMEOUT", 6: "QERL_ERR_NONFINITE",
                 7: "QERL_ERR_WORKSPACE"}
@@ -100,6 +104,9 @@ def lib():
             L.qerl_nvfp4_amax.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, ctypes.c_size_t, _vp]
             L.qerl_aqn_sigma.restype = ctypes.c_double
             L.qerl_aqn_sigma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double]
+            L.qerl_aqn_sigma_schedule.restype = ctypes.c_double
+            L.qerl_aqn_sigma_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                  ctypes.c_double]
             L.qerl_aqn_stage.restype = ctypes.c_int
             L.qerl_aqn_stage.argtypes = [_i64, _i64, ctypes.c_int]
             L.qerl_aqn_sample.restype = ctypes.c_int
@@ -192,6 +199,12 @@ def qerl_nvfp4_amax(W, amax, workspace, stream=None) -> int:
 
 def qerl_aqn_sigma(stage: int, num_stages: int, sigma_start: float = 1e-2, sigma_end: float = 5e-4) -> float:
     return lib().qerl_aqn_sigma(int(stage), int(num_stages), float(sigma_start), float(sigma_end))
+
+
+def qerl_aqn_sigma_schedule(schedule: int, stage: int, num_stages: int, sigma_start: float = 1e-2,
+                            sigma_end: float = 5e-4) -> float:
+    return lib().qerl_aqn_sigma_schedule(int(schedule), int(stage), int(num_stages), float(sigma_start),
+                                         float(sigma_end))
 
 
 def qerl_aqn_stage(step: int, total_steps: int, num_stages: int) -> int:

@@ -78,6 +78,33 @@ extern "C" double qerl_aqn_sigma(int stage, int num_stages, double sigma_start, 
   return sigma_start * std::pow(sigma_end / sigma_start, expo);
 }
 
+// The four decay schedules the digest compares in section 3.4 ("Why
+// exponential decay") and in its ablation (Figures 9 and 15), over the same
+// stages: with k = stage + 1 and u = (k-1)/(K-1),
+//   exponential  sigma_start * (sigma_end / sigma_start)^u           (Eq. 8)
+//   linear       sigma_start - (sigma_start - sigma_end) * u
+//   cosine       sigma_end + (sigma_start - sigma_end) * (1 + cos(pi u)) / 2
+//   logarithmic  sigma_start - (sigma_start - sigma_end) * log(k) / log(K)
+extern "C" double qerl_aqn_sigma_schedule(int schedule, int stage, int num_stages, double sigma_start,
+                                          double sigma_end) {
+  if (schedule < QERL_SCHEDULE_EXPONENTIAL || schedule > QERL_SCHEDULE_LOGARITHMIC) return std::nan("");
+  if (stage < 0) return 0.0;
+  if (num_stages <= 1) return sigma_start;
+  if (stage >= num_stages) stage = num_stages - 1;
+  const double span = sigma_start - sigma_end;
+  const double u = static_cast<double>(stage) / static_cast<double>(num_stages - 1);
+  switch (schedule) {
+    case QERL_SCHEDULE_LINEAR:
+      return sigma_start - span * u;
+    case QERL_SCHEDULE_COSINE:
+      return sigma_end + span * (1.0 + std::cos(M_PI * u)) / 2.0;
+    case QERL_SCHEDULE_LOGARITHMIC:
+      return sigma_start - span * std::log(static_cast<double>(stage + 1)) / std::log(static_cast<double>(num_stages));
+    default:
+      return qerl_aqn_sigma(stage, num_stages, sigma_start, sigma_end);
+  }
+}
+
 extern "C" int qerl_aqn_stage(int64_t step, int64_t total_steps, int num_stages) {
   if (num_stages <= 0 || step < 0) return -1;
   int64_t steps_per_stage = total_steps / num_stages;

@@ -68,6 +68,9 @@ def lib():
             L.orc_nvfp4_dequant.argtypes = [_u8p, _u8p, ctypes.c_float, _i64, _i64, _f64p]
             L.orc_aqn_sigma.restype = ctypes.c_double
             L.orc_aqn_sigma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double]
+            L.orc_aqn_sigma_schedule.restype = ctypes.c_double
+            L.orc_aqn_sigma_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                 ctypes.c_double]
             L.orc_aqn_stage.restype = ctypes.c_int
             L.orc_aqn_stage.argtypes = [_i64, _i64, ctypes.c_int]
             L.orc_philox4x32_10.restype = None
@@ -165,6 +168,13 @@ def dequant(codes: np.ndarray, scales: np.ndarray, S: float) -> np.ndarray:
 
 def aqn_sigma(stage: int, num_stages: int, sigma_start: float = 1e-2, sigma_end: float = 5e-4) -> float:
     return lib().orc_aqn_sigma(int(stage), int(num_stages), float(sigma_start), float(sigma_end))
+
+
+def aqn_sigma_schedule(schedule: int, stage: int, num_stages: int, sigma_start: float = 1e-2,
+                       sigma_end: float = 5e-4) -> float:
+    """Decay schedule 0 exponential (Eq. 8), 1 linear, 2 cosine, 3 logarithmic (digest, AQN section)."""
+    return lib().orc_aqn_sigma_schedule(int(schedule), int(stage), int(num_stages), float(sigma_start),
+                                        float(sigma_end))
 
 
 def aqn_stage(step: int, total_steps: int, num_stages: int) -> int:

@@ -264,6 +264,33 @@ double orc_aqn_sigma(int stage, int num_stages, double sigma_start, double sigma
     return sigma_start * pow(sigma_end / sigma_start, (double)stage / (double)(num_stages - 1));
 }
 
+/* The digest's four decay schedules (AQN section, "Why exponential decay";
+   ablation Figures 9 and 15), stage k = 1..K (library stage + 1):
+   0 exponential: Eq. 8;
+   1 linear:      s_start - (s_start - s_end) (k-1)/(K-1);
+   2 cosine:      s_end + 1/2 (s_start - s_end) (1 + cos(pi (k-1)/(K-1)));
+   3 logarithmic: s_start - (s_start - s_end) log(k) / log(K).
+   Same special stages as Eq. 8 above; an unknown schedule gives NaN. */
+double orc_aqn_sigma_schedule(int schedule, int stage, int num_stages, double s_start, double s_end)
+{
+    if (schedule < 0 || schedule > 3) return NAN;
+    if (stage < 0) return 0.0;
+    if (num_stages <= 1) return s_start;
+    if (stage > num_stages - 1) stage = num_stages - 1;
+    const int k = stage + 1, K = num_stages;
+    const double frac = (double)(k - 1) / (double)(K - 1);
+    switch (schedule) {
+    case 0:
+        return orc_aqn_sigma(stage, num_stages, s_start, s_end);
+    case 1:
+        return s_start - (s_start - s_end) * frac;
+    case 2:
+        return s_end + 0.5 * (s_start - s_end) * (1.0 + cos(acos(-1.0) * frac));
+    default:
+        return s_start - (s_start - s_end) * log((double)k) / log((double)K);
+    }
+}
+
 /* Algorithm 1: total steps split into K stages of floor(total/K) steps. */
 int orc_aqn_stage(int64_t step, int64_t total_steps, int num_stages)
 {

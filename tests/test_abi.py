@@ -54,6 +54,19 @@ def test_host_schedule_matches_oracle(L, orc):
         for stage in range(-2, K + 3):
             for s0, s1 in ((1e-2, 5e-4), (0.1, 1e-3)):
                 assert q.qerl_aqn_sigma(stage, K, s0, s1) == orc.aqn_sigma(stage, K, s0, s1)
+    for sch in range(4):
+        for K in (1, 2, 5, 10):
+            for stage in range(-2, K + 3):
+                lib_v = q.qerl_aqn_sigma_schedule(sch, stage, K, 1e-2, 5e-4)
+                orc_v = orc.aqn_sigma_schedule(sch, stage, K, 1e-2, 5e-4)
+                assert abs(lib_v - orc_v) <= 4e-16 * abs(orc_v), (sch, K, stage)
+    import math
+    assert math.isnan(q.qerl_aqn_sigma_schedule(4, 1, 10, 1e-2, 5e-4))
+    header = open(os.path.join(ROOT, "include", "qerl.h")).read()
+    enum = dict(re.findall(r"QERL_SCHEDULE_(\w+) = (\d+)", header))
+    assert len(enum) == 4
+    for name, val in enum.items():
+        assert getattr(q, "QERL_SCHEDULE_" + name) == int(val)
     for total in (1, 7, 600, 8192):
         for K in (1, 3, 10):
             for step in list(range(-2, 30)) + [total - 1, total, 5 * total]:

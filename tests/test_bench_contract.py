@@ -81,3 +81,18 @@ def test_timing_is_max_over_two_gloo_ranks(tmp_path):
     assert r.returncode == 0, r.stderr[-2000:]
     got = [(tmp_path / f"rank{i}.txt").read_text().split() for i in range(2)]
     assert got == [["0", "2", "2.5"], ["1", "2", "2.5"]]
+
+
+def test_aqn_schedule_table():
+    """The bench's schedule table: every schedule starts at sigma_start, ends at sigma_end and
+    decreases; the host cost is reported."""
+    import importlib
+    sys.path.insert(0, str(ROOT))
+    bench = importlib.import_module("bench")
+    import nvfp4_weight_quantized_03_gb300 as q
+    t = bench.aqn_schedule_table(q, calls=100)
+    for name in ("exponential", "linear", "cosine", "logarithmic"):
+        sig = t[name]
+        assert len(sig) == t["num_stages"] and sig[0] == t["sigma_start"]
+        assert abs(sig[-1] - t["sigma_end"]) <= 1e-9 and all(b < a for a, b in zip(sig, sig[1:]))
+    assert t["host_ns_per_call_incl_ctypes"] > 0

@@ -91,3 +91,58 @@ def test_sampler_scales_by_sigma(orc, sigma):
     zs = orc.aqn_sample(4097, sigma, 9, 0, 0).astype(np.float64)
     # two fp32 roundings (of n and of sigma * n) separate the two sides
     assert np.all(np.abs(zs - s32 * z1) <= np.abs(s32 * z1) * 2 ** -23 + 1e-45)
+
+
+# The digest's four decay schedules (AQN section, "Why exponential decay"; ablation Figures 9
+# and 15): 0 exponential (Eq. 8), 1 linear, 2 cosine, 3 logarithmic.  Pinned by properties
+# each closed form implies, not by retyping it.
+SCHEDULES = (0, 1, 2, 3)
+
+
+def _sched(orc, sch, k_stages=K):
+    return [orc.aqn_sigma_schedule(sch, i, k_stages, S0, S1) for i in range(k_stages)]
+
+
+def test_decay_schedules_share_stages_and_endpoints(orc):
+    for sch in SCHEDULES:
+        sig = _sched(orc, sch)
+        assert sig[0] == S0
+        assert abs(sig[-1] - S1) <= 1e-15 * S0
+        assert all(b < a for a, b in zip(sig, sig[1:])), sch
+        assert orc.aqn_sigma_schedule(sch, -1, K, S0, S1) == 0.0
+        assert orc.aqn_sigma_schedule(sch, K + 3, K, S0, S1) == sig[-1]
+        assert orc.aqn_sigma_schedule(sch, 2, 1, S0, S1) == S0
+    assert np.isnan(orc.aqn_sigma_schedule(4, 1, K, S0, S1))
+    assert np.isnan(orc.aqn_sigma_schedule(-1, 1, K, S0, S1))
+    assert _sched(orc, 0) == [orc.aqn_sigma(i, K, S0, S1) for i in range(K)]
+
+
+def test_linear_schedule_takes_equal_steps(orc):
+    for k_stages in (2, 5, K):
+        sig = _sched(orc, 1, k_stages)
+        for a, b in zip(sig, sig[1:]):
+            assert abs((a - b) - (S0 - S1) / (k_stages - 1)) <= 1e-17
+
+
+def test_cosine_schedule_is_point_symmetric_and_s_shaped(orc):
+    for k_stages in (9, K):
+        sig = _sched(orc, 2, k_stages)
+        for i in range(k_stages):
+            assert abs(sig[i] + sig[k_stages - 1 - i] - (S0 + S1)) <= 1e-17
+        if k_stages % 2:
+            assert abs(sig[k_stages // 2] - (S0 + S1) / 2) <= 1e-17
+        steps = [a - b for a, b in zip(sig, sig[1:])]
+        mid = len(steps) // 2
+        assert steps[0] < steps[mid] and steps[-1] < steps[mid]
+
+
+def test_logarithmic_schedule_product_rule(orc):
+    """The drop below sigma_start at stage k is proportional to log k: drop(k1 k2) = drop(k1) +
+    drop(k2), and the drops per stage shrink (sharp start, long tail)."""
+    def drop(k):
+        return S0 - orc.aqn_sigma_schedule(3, k - 1, K, S0, S1)
+
+    for k1, k2 in ((2, 2), (2, 3), (2, 4), (2, 5), (3, 3)):
+        assert abs(drop(k1 * k2) - (drop(k1) + drop(k2))) <= 1e-17
+    steps = [drop(k + 1) - drop(k) for k in range(1, K)]
+    assert all(b < a for a, b in zip(steps, steps[1:]))
