@@ -200,7 +200,10 @@ QERL_API qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t 
  * z       device float[k] or NULL (no noise).
  * A       device bf16 r x k, B device bf16 n x r (row-major), or both NULL /
  *         r == 0 (no LoRA branch).  r % 8 == 0 and r <= 128; A and B
- *         16-byte aligned.
+ *         16-byte aligned.  Ranks above 64 with 33..128 tokens (m) can need
+ *         more shared memory than a CTA has: the call then returns
+ *         QERL_ERR_UNSUPPORTED_SHAPE before launching anything.  Every
+ *         r <= 64 is supported at every m.
  * y       device, m x n (row stride n), y_dtype QERL_BF16 (round to nearest
  *         even) or QERL_F32.
  * workspace device, >= qerl_lora_linear_workspace_size(m, n, k, r) bytes,
