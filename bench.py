@@ -617,7 +617,8 @@ def bench_quantize(q, hbm_peak):
 
 
 def _graph_time_ms(fn, reps, warm=2):
-    """Capture fn() into one CUDA graph, replay `warm` times, then time `reps` replays."""
+    """Capture fn() into one CUDA graph, replay `warm` times, then time `reps` back-to-back replays
+    with an event between consecutive ones: (mean ms, graph, [p10, median, p90] ms)."""
     fn()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
@@ -627,13 +628,14 @@ def _graph_time_ms(fn, reps, warm=2):
     for _ in range(warm):
         g.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for i in range(reps):
         g.replay()
-    e1.record()
+        ev[i + 1].record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps, g
+    ts = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
+    return ev[0].elapsed_time(ev[-1]) / reps, g, [_pct(ts, p) for p in (10, 50, 90)]
 
 
 def bench_qproj_3b(q, hbm_peak):
@@ -654,11 +656,13 @@ def bench_qproj_3b(q, hbm_peak):
             for i in range(reps):
                 ql = copies[i % ncp]
                 q.check(q.qerl_lora_linear(x, ql.wp, ql.S, z, ql.A, ql.B, alpha, y, ws), "qerl_lora_linear")
-        t_ms, _ = _graph_time_ms(calls, 5)
+        t_ms, _, pct = _graph_time_ms(calls, 50)
         us = t_ms * 1e3 / reps
         alg = linear_algorithmic_bytes(lin, m, r)
         res[name] = {"us_per_call": round(us, 3), "GBps": round(alg / (us * 1e-6) / 1e9, 1),
-                     "frac_of_hbm_peak": round(alg / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+                     "frac_of_hbm_peak": round(alg / (us * 1e-6) / 1e9 / hbm_peak, 4),
+                     "us_per_call_p10_median_p90": [round(v * 1e3 / reps, 3) for v in pct],
+                     "timing": f"50 graph replays of {reps} back-to-back calls, one event pair per replay"}
     q.check(q.qerl_read_status(ws), "qproj status")
     del copies
     torch.cuda.empty_cache()
@@ -703,8 +707,8 @@ def bench_32b_stream(q, hbm_peak):
         for li, layer in enumerate(layers):
             run_substep(q, layer, act, 5e-3, li)
 
-    reps = 5
-    t_ms, g = _graph_time_ms(step, reps)
+    reps = 50
+    t_ms, g, pct = _graph_time_ms(step, reps)
     q.check(q.qerl_read_status(act.ws), "32B step status")
     wbytes = sum(ql.weight_bytes for layer in layers for ql in layer)
     alg = nl * sum(linear_algorithmic_bytes(lin, m) for lin in shapes)
@@ -717,6 +721,7 @@ def bench_32b_stream(q, hbm_peak):
                    "frac_of_hbm_peak": round(wbytes / (t_ms * 1e-3) / 1e9 / hbm_peak, 4),
                    "all_bytes_GBps": round(alg / (t_ms * 1e-3) / 1e9, 1),
                    "tokens_per_s": round(m / (t_ms * 1e-3), 1),
+                   "ms_per_step_p10_median_p90": [round(v, 3) for v in pct],
                    "timing": f"one CUDA graph of the whole step (320 launches), {reps} timed replays"},
         "quantize": {"workload": "nvfp4 quantization of all 448 Qwen2.5-32B-shaped matrices from bf16 "
                                  "N(0,0.02^2) with Student-t(3) outlier channels (0.5%)",
