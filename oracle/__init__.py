@@ -78,6 +78,8 @@ def lib():
             L.orc_aqn_sample.restype = None
             L.orc_aqn_sample.argtypes = [_f32p, _i64, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
                                          ctypes.c_uint64]
+            L.orc_rmsnorm_noise.restype = None
+            L.orc_rmsnorm_noise.argtypes = [_u16p, _i64, _i64, _i64, _u16p, _f32p, ctypes.c_double, _f64p, _u16p]
             L.orc_noise_apply.restype = None
             L.orc_noise_apply.argtypes = [_u16p, _i64, _i64, _i64, _f32p, _u16p]
             L.orc_lora_linear.restype = ctypes.c_int
@@ -206,6 +208,22 @@ def noise_apply(x_bits: np.ndarray, z) -> np.ndarray:
     out = np.empty((m, k), dtype=np.uint16)
     lib().orc_noise_apply(_ptr(x_bits, _u16p), m, k, k, _ptr(zz, _f32p), _ptr(out, _u16p))
     return out
+
+
+def rmsnorm_noise(h_bits, w_bits, Z=None, delta=1e-6):
+    """Eq. 10 (digest, "Noise Merging"): (w + Z) * h / sqrt(mean(h^2) + delta) per row, fp64.
+    h_bits [m, k] and w_bits [k] uint16 (bf16), Z [k] float32 or None.  Returns (fp64 values,
+    their bf16 bits)."""
+    h_bits = np.ascontiguousarray(h_bits, dtype=np.uint16)
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    m, k = h_bits.shape
+    assert w_bits.shape == (k,)
+    zz = None if Z is None else np.ascontiguousarray(Z, dtype=np.float32)
+    out64 = np.empty((m, k), dtype=np.float64)
+    bits = np.empty((m, k), dtype=np.uint16)
+    lib().orc_rmsnorm_noise(_ptr(h_bits, _u16p), m, k, k, _ptr(w_bits, _u16p), _ptr(zz, _f32p), float(delta),
+                            _ptr(out64, _f64p), _ptr(bits, _u16p))
+    return out64, bits
 
 
 def lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alpha=0.0,

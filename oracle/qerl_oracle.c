@@ -375,6 +375,37 @@ void orc_noise_apply(const uint16_t* x, int64_t m, int64_t k, int64_t ldx, const
 }
 
 /* ------------------------------------------------------------------------ */
+/* RMSNorm with the noise merged into its scale.  [QeRL] "Noise Merging",    */
+/* Eq. 10:                                                                   */
+/*   out[i][j] = (w_j + Z_j) * h[i][j] / sqrt((1/k) sum_l h[i][l]^2 + delta) */
+/* h bf16 [m][k] (row stride ldh), w bf16 [k], Z fp32 [k] or NULL (plain     */
+/* RMSNorm, Z = 0).  Everything in fp64; out64 (if not NULL) receives the    */
+/* values, out_bits (if not NULL) their single rounding to bf16 (reading:    */
+/* the digest leaves the output precision open; the linear consumes bf16).   */
+/* delta is the caller's (the digest: "a small constant").  A zero row with  */
+/* delta == 0 gives NaN (0 / 0), as the definition does.                     */
+/* ------------------------------------------------------------------------ */
+void orc_rmsnorm_noise(const uint16_t* h, int64_t m, int64_t k, int64_t ldh, const uint16_t* w, const float* Z,
+                       double delta, double* out64, uint16_t* out_bits)
+{
+    for (int64_t i = 0; i < m; ++i) {
+        const uint16_t* row = h + i * ldh;
+        double ss = 0.0;
+        for (int64_t j = 0; j < k; ++j) {
+            const double v = (double)bf16_bits_to_f32(row[j]);
+            ss += v * v;
+        }
+        const double denom = sqrt(ss / (double)k + delta);
+        for (int64_t j = 0; j < k; ++j) {
+            const double w_noise = (double)bf16_bits_to_f32(w[j]) + (Z ? (double)Z[j] : 0.0);
+            const double v = w_noise * ((double)bf16_bits_to_f32(row[j]) / denom);
+            if (out64) out64[i * k + j] = v;
+            if (out_bits) out_bits[i * k + j] = orc_f64_to_bf16(v);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* The linear layer, fp64 accumulation:                                      */
 /*   y[m][c] = sum_k xt[m][k] * W_hat[c][k]                                  */
 /*           + (alpha / r) * sum_j (sum_k xt[m][k] * A[j][k]) * B[c][j]      */

@@ -114,6 +114,13 @@ def lora_B_bits(n: int, r: int, seed: int, *path: int, std: float = 0.01) -> np.
     return to_bf16_bits(rng(seed, *path, 5).standard_normal((n, r), dtype=np.float32) * np.float32(std))
 
 
+def rmsnorm_weight_bits(k: int, seed: int, *path: int, mean: float = 1.0, std: float = 0.1) -> np.ndarray:
+    """An RMSNorm scale w [k] bf16 bits ~ |N(mean, std^2)| (positive, around 1, as trained
+    norm scales are; synthetic)."""
+    return to_bf16_bits(np.abs(rng(seed, *path, 8).standard_normal(k, dtype=np.float32) * np.float32(std)
+                               + np.float32(mean)))
+
+
 def noise_vector(k: int, sigma: float, seed: int, *path: int) -> np.ndarray:
     """A channel-wise noise vector z [k] fp32 = sigma * N(0, 1), drawn on the host.
     (Used as a plain input of the linear; the library's own sampler is separate.)"""
