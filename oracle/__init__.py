@@ -78,6 +78,9 @@ def lib():
             L.orc_aqn_sample.restype = None
             L.orc_aqn_sample.argtypes = [_f32p, _i64, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
                                          ctypes.c_uint64]
+            L.orc_lora_linear_backward.restype = ctypes.c_int
+            L.orc_lora_linear_backward.argtypes = [_u16p, _i64, _i64, _u8p, _u8p, ctypes.c_float, _i64, _u16p, _u16p,
+                                                   ctypes.c_int, ctypes.c_float, _f64p, _f64p, _f64p, _f64p]
             L.orc_rmsnorm_noise.restype = None
             L.orc_rmsnorm_noise.argtypes = [_u16p, _i64, _i64, _i64, _u16p, _f32p, ctypes.c_double, _f64p, _u16p]
             L.orc_noise_apply.restype = None
@@ -208,6 +211,29 @@ def noise_apply(x_bits: np.ndarray, z) -> np.ndarray:
     out = np.empty((m, k), dtype=np.uint16)
     lib().orc_noise_apply(_ptr(x_bits, _u16p), m, k, k, _ptr(zz, _f32p), _ptr(out, _u16p))
     return out
+
+
+def lora_linear_backward(xt_bits, codes, scales, S, A_bits, B_bits, alpha, dy):
+    """Gradients of the linear through the frozen NVFP4 weight, fp64: (d_xt [m, k], dA [r, k],
+    dB [n, r]) for y = xt W_hat^T + (alpha/r)(xt A^T) B^T and the output gradient dy [m, n].
+    xt_bits is the bf16 noisy activation; A_bits/B_bits None: no LoRA term (dA, dB None)."""
+    xt_bits = np.ascontiguousarray(xt_bits, dtype=np.uint16)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    dy = np.ascontiguousarray(dy, dtype=np.float64)
+    m, k = xt_bits.shape
+    n = codes.shape[0]
+    assert dy.shape == (m, n)
+    r = 0 if A_bits is None else A_bits.shape[0]
+    A = None if A_bits is None else np.ascontiguousarray(A_bits, dtype=np.uint16)
+    B = None if B_bits is None else np.ascontiguousarray(B_bits, dtype=np.uint16)
+    dxt = np.empty((m, k), dtype=np.float64)
+    dA = np.zeros((max(r, 1), k), dtype=np.float64)
+    dB = np.zeros((n, max(r, 1)), dtype=np.float64)
+    _check(lib().orc_lora_linear_backward(_ptr(xt_bits, _u16p), m, k, _ptr(codes, _u8p), _ptr(scales, _u8p),
+                                          float(S), n, _ptr(A, _u16p), _ptr(B, _u16p), r, float(alpha),
+                                          _ptr(dy, _f64p), _ptr(dxt, _f64p), _ptr(dA, _f64p), _ptr(dB, _f64p)))
+    return dxt, (dA[:r] if r else None), (dB[:, :r] if r else None)
 
 
 def rmsnorm_noise(h_bits, w_bits, Z=None, delta=1e-6):

@@ -474,3 +474,76 @@ int orc_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
     free(xt); free(t); free(wrow);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* LoRA backward through the frozen NVFP4 weight ([QeRL] "Low-Rank          */
+/* Adaptation (LoRA) Within Quantized Layers", gradient flow: only A and B  */
+/* are trained, the quantized base weight is frozen and only passes the     */
+/* input gradient).  For the forward above with the noisy activation xt,    */
+/*   y = xt W_hat^T + s (xt A^T) B^T,   s = alpha / r,   t = xt A^T:         */
+/*   d_xt = dy W_hat + s (dy B) A      [m][k]                                */
+/*   dA   = s (dy B)^T xt              [r][k]                                */
+/*   dB   = s dy^T t                   [n][r]                                */
+/* fp64 throughout.  xt: [m][k] bf16 bits (the forward's input to both      */
+/* branches); dy: [m][n] fp64.  A or B NULL, or r == 0: no LoRA term (dA    */
+/* and dB untouched).                                                        */
+/* ------------------------------------------------------------------------ */
+int orc_lora_linear_backward(const uint16_t* xt, int64_t m, int64_t k, const uint8_t* codes, const uint8_t* scales,
+                             float S, int64_t n, const uint16_t* A, const uint16_t* B, int r, float alpha,
+                             const double* dy, double* dxt, double* dA, double* dB)
+{
+    if (m < 0 || k < 0 || n < 0 || r < 0) return ORC_ERR_ARG;
+    if (k % 32 != 0) return ORC_ERR_SHAPE;
+    const int use_lora = (A != NULL && B != NULL && r > 0);
+    const double s = use_lora ? (double)alpha / (double)r : 0.0;
+    double* W_hat = (double*)malloc(sizeof(double) * (size_t)(n * k + 1));
+    double* dyB = (double*)malloc(sizeof(double) * (size_t)(m * (r > 0 ? r : 1) + 1));
+    double* t = (double*)malloc(sizeof(double) * (size_t)(m * (r > 0 ? r : 1) + 1));
+    if (!W_hat || !dyB || !t) { free(W_hat); free(dyB); free(t); return ORC_ERR_ARG; }
+    orc_nvfp4_dequant(codes, scales, S, n, k, W_hat);
+
+    /* d_xt = dy W_hat */
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t kk = 0; kk < k; ++kk) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < n; ++c) acc += dy[i * n + c] * W_hat[c * k + kk];
+            dxt[i * k + kk] = acc;
+        }
+    if (use_lora) {
+        /* dy B and t = xt A^T */
+        for (int64_t i = 0; i < m; ++i)
+            for (int j = 0; j < r; ++j) {
+                double a = 0.0, b = 0.0;
+                for (int64_t c = 0; c < n; ++c) a += dy[i * n + c] * (double)bf16_bits_to_f32(B[c * r + j]);
+                for (int64_t kk = 0; kk < k; ++kk)
+                    b += (double)bf16_bits_to_f32(xt[i * k + kk]) * (double)bf16_bits_to_f32(A[(int64_t)j * k + kk]);
+                dyB[i * r + j] = a;
+                t[i * r + j] = b;
+            }
+        /* d_xt += s (dy B) A */
+        for (int64_t i = 0; i < m; ++i)
+            for (int64_t kk = 0; kk < k; ++kk) {
+                double acc = 0.0;
+                for (int j = 0; j < r; ++j) acc += dyB[i * r + j] * (double)bf16_bits_to_f32(A[(int64_t)j * k + kk]);
+                dxt[i * k + kk] += s * acc;
+            }
+        /* dA = s (dy B)^T xt */
+        for (int j = 0; j < r; ++j)
+            for (int64_t kk = 0; kk < k; ++kk) {
+                double acc = 0.0;
+                for (int64_t i = 0; i < m; ++i) acc += dyB[i * r + j] * (double)bf16_bits_to_f32(xt[i * k + kk]);
+                dA[(int64_t)j * k + kk] = s * acc;
+            }
+        /* dB = s dy^T t */
+        for (int64_t c = 0; c < n; ++c)
+            for (int j = 0; j < r; ++j) {
+                double acc = 0.0;
+                for (int64_t i = 0; i < m; ++i) acc += dy[i * n + c] * t[i * r + j];
+                dB[c * r + j] = s * acc;
+            }
+    }
+    free(W_hat);
+    free(dyB);
+    free(t);
+    return ORC_OK;
+}
