@@ -234,3 +234,17 @@ def test_product_and_oracle_are_independent():
             text = open(os.path.join(ROOT, "oracle", fn)).read()
             assert "nvfp4_weight_quantized_03_gb300" not in re.findall(r"(?:import|from)\s+([\w.]+)", text), fn
             assert "#include" not in text or ("qerl_ptx" not in text and "qerl.h" not in text), fn
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_header_is_plain_c_and_cpp(lang, std):
+    """include/qerl.h is a C ABI: it compiles as pedantic C99 and as C++11 on its own."""
+    import shutil
+    cc = shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no gcc")
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            r = subprocess.run([cc, "-fsyntax-only", "-x", lang, std, "-Wall", "-Wextra", "-pedantic", "-Werror",
+                                os.path.join(ROOT, "include", fn)], capture_output=True, text=True)
+            assert r.returncode == 0, r.stderr
