@@ -84,10 +84,10 @@ def lib():
             L.orc_rmsnorm_noise.restype = None
             L.orc_rmsnorm_noise.argtypes = [_u16p, _i64, _i64, _i64, _u16p, _f32p, ctypes.c_double, _f64p, _u16p]
             L.orc_noise_apply.restype = None
-            L.orc_noise_apply.argtypes = [_u16p, _i64, _i64, _i64, _f32p, _u16p]
+            L.orc_noise_apply.argtypes = [_u16p, _i64, _i64, _i64, _f32p, _i64, _u16p]
             L.orc_lora_linear.restype = ctypes.c_int
             L.orc_lora_linear.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p, ctypes.c_float, _i64,
-                                          _f32p, _u16p, _u16p, ctypes.c_int, ctypes.c_float,
+                                          _f32p, _i64, _u16p, _u16p, ctypes.c_int, ctypes.c_float,
                                           ctypes.c_int, _i64p, _i64, _f64p]
             _lib = L
     return _lib
@@ -203,13 +203,26 @@ def aqn_sample(k: int, sigma: float, seed: int, stream_id: int = 0, counter: int
 
 # ---- linear ----------------------------------------------------------------
 
+def _noise_rows(z, m, k):
+    """z: None, [k] (one vector for every row) or [m, k] (one per row) -> (array, row stride)."""
+    if z is None:
+        return None, 0
+    zz = np.ascontiguousarray(z, dtype=np.float32)
+    if zz.ndim == 1:
+        assert zz.shape == (k,)
+        return zz, 0
+    assert zz.shape == (m, k)
+    return zz, k
+
+
 def noise_apply(x_bits: np.ndarray, z) -> np.ndarray:
-    """x_bits [m, k] uint16 (bf16); returns the bf16 bits of bf16(x * (1 + z))."""
+    """x_bits [m, k] uint16 (bf16); z [k] or [m, k] float32; returns the bf16 bits of
+    bf16(x * (1 + z))."""
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     m, k = x_bits.shape
-    zz = None if z is None else np.ascontiguousarray(z, dtype=np.float32)
+    zz, ldz = _noise_rows(z, m, k)
     out = np.empty((m, k), dtype=np.uint16)
-    lib().orc_noise_apply(_ptr(x_bits, _u16p), m, k, k, _ptr(zz, _f32p), _ptr(out, _u16p))
+    lib().orc_noise_apply(_ptr(x_bits, _u16p), m, k, k, _ptr(zz, _f32p), ldz, _ptr(out, _u16p))
     return out
 
 
@@ -257,7 +270,8 @@ def lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alph
     """fp64 y[m, len(cols)] of the NVFP4 + LoRA + AQN linear.
 
     x_bits: [m, k] uint16 bf16; codes [n, k/2]; scales [n, k/16]; S tensor scale;
-    z: [k] float32 or None; A_bits [r, k] uint16 bf16; B_bits [n, r] uint16 bf16
+    z: [k] float32 (one vector for every row), [m, k] (one per row) or None;
+    A_bits [r, k] uint16 bf16; B_bits [n, r] uint16 bf16
     (the shapes of Eq. 2: A in R^{r x k}, B in R^{d x r}).
     """
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
@@ -274,7 +288,7 @@ def lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alph
         assert A_bits.shape == (r, k) and B_bits.shape == (n, r)
     else:
         A_bits = B_bits = None
-    zz = None if z is None else np.ascontiguousarray(z, dtype=np.float32)
+    zz, ldz = _noise_rows(z, m, k)
     if cols is None:
         cols_arr, ncols = None, n
     else:
@@ -282,7 +296,7 @@ def lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alph
         ncols = cols_arr.size
     y = np.empty((m, ncols), dtype=np.float64)
     _check(lib().orc_lora_linear(_ptr(x_bits, _u16p), m, k, k, _ptr(codes, _u8p), _ptr(scales, _u8p),
-                                 float(S), n, _ptr(zz, _f32p), _ptr(A_bits, _u16p), _ptr(B_bits, _u16p),
+                                 float(S), n, _ptr(zz, _f32p), ldz, _ptr(A_bits, _u16p), _ptr(B_bits, _u16p),
                                  r, float(alpha), 1 if round_xt else 0, _ptr(cols_arr, _i64p), ncols,
                                  _ptr(y, _f64p)))
     return y

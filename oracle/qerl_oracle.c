@@ -359,15 +359,18 @@ void orc_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, uint32_t st
 /* into the RMSNorm scale acts as a per-input-channel factor (1 + z) on the  */
 /* activations, which the quantized kernel receives as bf16.  Reading:       */
 /*   x_tilde = bf16_RN( float(x) * (1.0f + z) )   (fp32 ops)                 */
-/* z == NULL means no noise (x_tilde = x).                                   */
+/* z == NULL means no noise (x_tilde = x).  Row i uses z + i * ldz: ldz = 0  */
+/* is one vector for every row (the broadcast of Eq. 9), ldz = k one vector  */
+/* per row (per rollout).                                                    */
 /* ------------------------------------------------------------------------ */
-void orc_noise_apply(const uint16_t* x, int64_t m, int64_t k, int64_t ldx, const float* z, uint16_t* xt)
+void orc_noise_apply(const uint16_t* x, int64_t m, int64_t k, int64_t ldx, const float* z, int64_t ldz,
+                     uint16_t* xt)
 {
     for (int64_t i = 0; i < m; ++i)
         for (int64_t j = 0; j < k; ++j) {
             uint16_t h = x[i * ldx + j];
             if (z) {
-                float f = bf16_bits_to_f32(h) * (1.0f + z[j]);
+                float f = bf16_bits_to_f32(h) * (1.0f + z[i * ldz + j]);
                 h = f32_to_bf16_rn(f);
             }
             xt[i * k + j] = h;
@@ -415,15 +418,16 @@ void orc_rmsnorm_noise(const uint16_t* h, int64_t m, int64_t k, int64_t ldh, con
 /* AQN).                                                                     */
 /* round_xt = 1: xt is the bf16 noisy activation (the reading above);        */
 /* round_xt = 0: xt = x * (1 + z) exactly in fp64 (used to check Eq. 12).    */
+/* Row i of x uses noise row z + i * ldz (ldz = 0: one vector for all rows).  */
 /* Output columns are the ncols indices in cols[] (all n if cols == NULL).   */
 /* A or B NULL, or r == 0: no LoRA term.                                     */
 /* ------------------------------------------------------------------------ */
 int orc_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
                     const uint8_t* codes, const uint8_t* scales, float S, int64_t n,
-                    const float* z, const uint16_t* A, const uint16_t* B, int r, float alpha,
+                    const float* z, int64_t ldz, const uint16_t* A, const uint16_t* B, int r, float alpha,
                     int round_xt, const int64_t* cols, int64_t ncols, double* y)
 {
-    if (m < 0 || k < 0 || n < 0 || ldx < k || r < 0) return ORC_ERR_ARG;
+    if (m < 0 || k < 0 || n < 0 || ldx < k || r < 0 || ldz < 0) return ORC_ERR_ARG;
     if (k % 32 != 0) return ORC_ERR_SHAPE;
     int use_lora = (A != NULL && B != NULL && r > 0);
     if (cols == NULL) ncols = n;
@@ -438,8 +442,8 @@ int orc_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
             uint16_t h = x[i * ldx + j];
             double v;
             if (z == NULL) v = (double)bf16_bits_to_f32(h);
-            else if (round_xt) v = (double)bf16_bits_to_f32(f32_to_bf16_rn(bf16_bits_to_f32(h) * (1.0f + z[j])));
-            else v = (double)bf16_bits_to_f32(h) * (1.0 + (double)z[j]);
+            else if (round_xt) v = (double)bf16_bits_to_f32(f32_to_bf16_rn(bf16_bits_to_f32(h) * (1.0f + z[i * ldz + j])));
+            else v = (double)bf16_bits_to_f32(h) * (1.0 + (double)z[i * ldz + j]);
             xt[i * k + j] = v;
         }
 

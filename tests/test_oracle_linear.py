@@ -120,3 +120,45 @@ def test_output_rounding_to_bf16(orc):
     back = (b.astype(np.uint32) << 16).view(np.float32)
     assert back[0] == 1.0 and back[1] == 1.0  # tie to even
     assert np.isinf(back[4])
+
+
+# Per-row (per-rollout) noise: the digest's AQN section says each rollout may see a different
+# epsilon; the broadcast of Eq. 9 is the case where every row gets the same vector.
+
+
+def test_per_row_noise_with_identical_rows_is_the_broadcast(orc):
+    W, x, A, B, z = _case()
+    codes, scales, S = orc.quantize(W)
+    zz = np.tile(z, (x.shape[0], 1))
+    a = orc.lora_linear(x, codes, scales, S, z=z, A_bits=A, B_bits=B, alpha=4.0)
+    b = orc.lora_linear(x, codes, scales, S, z=zz, A_bits=A, B_bits=B, alpha=4.0)
+    assert np.array_equal(a, b)
+    assert np.array_equal(orc.noise_apply(x, z), orc.noise_apply(x, zz))
+
+
+def test_per_row_noise_reaches_only_its_row(orc):
+    W, x, A, B, z = _case(m=4)
+    codes, scales, S = orc.quantize(W)
+    zz = np.tile(z, (4, 1))
+    zz[2] = wl.noise_vector(z.size, 0.05, 0, 9)
+    base = orc.lora_linear(x, codes, scales, S, z=z, A_bits=A, B_bits=B, alpha=4.0)
+    y = orc.lora_linear(x, codes, scales, S, z=zz, A_bits=A, B_bits=B, alpha=4.0)
+    for i in (0, 1, 3):
+        assert np.array_equal(y[i], base[i])
+    assert not np.array_equal(y[2], base[2])
+    # and row 2 is the broadcast linear of its own noise vector
+    alone = orc.lora_linear(x[2:3], codes, scales, S, z=zz[2], A_bits=A, B_bits=B, alpha=4.0)
+    assert np.array_equal(y[2:3], alone)
+
+
+def test_per_row_noise_eq12_each_row(orc):
+    """Eq. 12 per row: row i of x (1 + z_i) W_hat^T equals x_i (W_hat (.) (1 + z_i))^T."""
+    W, x, A, B, z = _case(n=24, k=64, m=3)
+    codes, scales, S = orc.quantize(W)
+    Wh = orc.dequant(codes, scales, S)
+    zz = np.stack([wl.noise_vector(64, 0.05, 0, 20 + i) for i in range(3)])
+    y = orc.lora_linear(x, codes, scales, S, z=zz, round_xt=False)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    for i in range(3):
+        ref = xf[i] @ (Wh * (1.0 + zz[i].astype(np.float64))[None, :]).T
+        assert np.allclose(y[i], ref, rtol=1e-12, atol=1e-13)
