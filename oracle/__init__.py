@@ -78,6 +78,12 @@ def lib():
             L.orc_aqn_sample.restype = None
             L.orc_aqn_sample.argtypes = [_f32p, _i64, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
                                          ctypes.c_uint64]
+            L.orc_e8m0_decode.restype = ctypes.c_double
+            L.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
+            L.orc_mxfp4_quantize.restype = ctypes.c_int
+            L.orc_mxfp4_quantize.argtypes = [_f32p, _i64, _i64, _i64, _u8p, _u8p]
+            L.orc_mxfp4_dequant.restype = None
+            L.orc_mxfp4_dequant.argtypes = [_u8p, _u8p, _i64, _i64, _f64p]
             L.orc_lora_linear_backward.restype = ctypes.c_int
             L.orc_lora_linear_backward.argtypes = [_u16p, _i64, _i64, _u8p, _u8p, ctypes.c_float, _i64, _u16p, _u16p,
                                                    ctypes.c_int, ctypes.c_float, _f64p, _f64p, _f64p, _f64p]
@@ -166,6 +172,30 @@ def dequant(codes: np.ndarray, scales: np.ndarray, S: float) -> np.ndarray:
     k = 2 * k2
     out = np.empty((n, k), dtype=np.float64)
     lib().orc_nvfp4_dequant(_ptr(codes, _u8p), _ptr(scales, _u8p), float(S), n, k, _ptr(out, _f64p))
+    return out
+
+
+def e8m0_decode(code: int) -> float:
+    return lib().orc_e8m0_decode(int(code))
+
+
+def mxfp4_quantize(W: np.ndarray):
+    """MXFP4 (E2M1 elements, one E8M0 power-of-two scale per 32 along K): W [n, k] fp32 ->
+    (codes [n, k/2] u8, scales [n, k/32] u8)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    n, k = W.shape
+    codes = np.zeros((n, k // 2), dtype=np.uint8)
+    scales = np.zeros((n, k // 32), dtype=np.uint8)
+    _check(lib().orc_mxfp4_quantize(_ptr(W, _f32p), n, k, k, _ptr(codes, _u8p), _ptr(scales, _u8p)))
+    return codes, scales
+
+
+def mxfp4_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    n, k2 = codes.shape
+    out = np.empty((n, 2 * k2), dtype=np.float64)
+    lib().orc_mxfp4_dequant(_ptr(codes, _u8p), _ptr(scales, _u8p), n, 2 * k2, _ptr(out, _f64p))
     return out
 
 

@@ -251,6 +251,64 @@ void orc_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float S, int
 }
 
 /* ------------------------------------------------------------------------ */
+/* MXFP4, the format the digest compares with NVFP4 ([QeRL] "NVFP4           */
+/* Quantization", other 4-bit formats): E2M1 elements with one shared E8M0   */
+/* scale (a power of two) per block of 32 along K; no tensor scale.  The     */
+/* digest does not say how the scale is chosen.  Reading: the OCP MX rule,   */
+/* X = 2^(floor(log2(amax_b)) - 2), 2 being the largest E2M1 exponent, so    */
+/* the block max lands in [4, 8) * X (values above 6 X saturate); E8M0 code  */
+/* = log2(X) + 127, clamped to [0, 254]; an all-zero block gets code 0.      */
+/* Elements: the E2M1 encoder above on w / X (exact: X is a power of two).   */
+/* Layout: codes [n][k/2] (element 2j low nibble), scales [n][k/32].         */
+/* ------------------------------------------------------------------------ */
+double orc_e8m0_decode(uint8_t code)
+{
+    if (code == 0xFF) return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+int orc_mxfp4_quantize(const float* W, int64_t n, int64_t k, int64_t ldw, uint8_t* codes, uint8_t* scales)
+{
+    if (n < 0 || k < 0 || ldw < k) return ORC_ERR_ARG;
+    if (k % 32 != 0) return ORC_ERR_SHAPE;
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t b = 0; b < k / 32; ++b) {
+            const float* blk = W + i * ldw + b * 32;
+            float amax = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                if (!isfinite(blk[j])) return ORC_ERR_NONFINITE;
+                if (fabsf(blk[j]) > amax) amax = fabsf(blk[j]);
+            }
+            int e = -127;
+            if (amax > 0.0f) {
+                int ex;
+                frexp((double)amax, &ex); /* amax in [2^(ex-1), 2^ex): floor(log2(amax)) = ex - 1 */
+                e = ex - 1 - 2;
+                if (e < -127) e = -127;
+                if (e > 127) e = 127;
+            }
+            scales[i * (k / 32) + b] = (uint8_t)(e + 127);
+            const double X = ldexp(1.0, e);
+            for (int j = 0; j < 32; j += 2) {
+                const uint8_t lo = orc_e2m1_encode((float)((double)blk[j] / X));
+                const uint8_t hi = orc_e2m1_encode((float)((double)blk[j + 1] / X));
+                codes[i * (k / 2) + (b * 32 + j) / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    return ORC_OK;
+}
+
+void orc_mxfp4_dequant(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, double* W_hat)
+{
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < k; ++j) {
+            const uint8_t byte = codes[i * (k / 2) + j / 2];
+            const uint8_t c = (j & 1) ? (byte >> 4) : (byte & 0xF);
+            W_hat[i * k + j] = orc_e8m0_decode(scales[i * (k / 32) + j / 32]) * orc_e2m1_decode(c);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
 /* AQN schedule: [QeRL] Eq. 8, sigma(k) = s0 * (s1/s0)^((k-1)/(K-1)),        */
 /* k = 1..K.  Library stage index `stage` = k - 1 (0..K-1); a negative stage */
 /* is the warm-up stage of Algorithm 1 with sigma = 0; stages past the last  */
