@@ -72,6 +72,20 @@ def dist_env():
     return ws, rank, local
 
 
+def host_cpu_model():
+    """The host CPU's model name (best effort: /proc/cpuinfo, else the platform string)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def max_over_ranks(x, world, device):
     """The largest of every rank's x, returned on every rank (x itself for one process):
     the job's time is its slowest replica's."""
@@ -923,7 +937,8 @@ def cpu_baseline_oracle(seconds_budget=15.0):
     dt = time.perf_counter() - t
     return {"value": round(wbytes / dt / 1e9, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"full 7B-shaped layer (7 linears + 4 AQN samples) at decode M in {ms_done}, one pass each; "
-                      f"{dt:.1f} s; plain C fp64, single thread", "host_cpus": os.cpu_count()}
+                      f"{dt:.1f} s; plain C fp64, single thread", "host_cpus": os.cpu_count(),
+            "host_cpu_model": host_cpu_model()}
 
 
 def bench_reference(args):
@@ -947,7 +962,8 @@ def bench_reference(args):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "sample": sample},
-           "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+           "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                            "host_cpus": os.cpu_count(), "host_cpu_model": host_cpu_model()},
            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
            "gpu_launches": 0}
     print(json.dumps(out), flush=True)
