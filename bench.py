@@ -72,16 +72,35 @@ def dist_env():
     return ws, rank, local
 
 
+# Arm CPU identification: (implementer, part) from /proc/cpuinfo -> core name
+# (Arm's published MIDR part numbers).
+ARM_PARTS = {(0x41, 0xD0C): "Neoverse-N1", (0x41, 0xD40): "Neoverse-V1", (0x41, 0xD49): "Neoverse-N2",
+             (0x41, 0xD4F): "Neoverse-V2", (0x41, 0xD8E): "Neoverse-N3", (0x41, 0xD84): "Neoverse-V3"}
+
+
+EXTRAS = ("prefill", "quantize", "qproj", "sustained", "32b")
+
+
 def host_cpu_model():
-    """The host CPU's model name (best effort: /proc/cpuinfo, else the platform string)."""
+    """The host CPU's model name: /proc/cpuinfo's "model name" (x86), else the Arm core named
+    from its "CPU implementer" / "CPU part" fields (raw values kept), else the platform string."""
+    impl = part = None
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                key = line.split(":")[0].strip().lower()
-                if key in ("model name", "cpu model", "hardware"):
-                    return line.split(":", 1)[1].strip()
-    except OSError:
+                key, _, val = line.partition(":")
+                key, val = key.strip().lower(), val.strip()
+                if key in ("model name", "cpu model"):
+                    return val
+                if key == "cpu implementer" and impl is None:
+                    impl = int(val, 0)
+                elif key == "cpu part" and part is None:
+                    part = int(val, 0)
+    except (OSError, ValueError):
         pass
+    if impl is not None and part is not None:
+        name = ARM_PARTS.get((impl, part), "Arm core")
+        return f"{name} (CPU implementer {impl:#x}, part {part:#05x})"
     import platform
     return platform.processor() or platform.machine()
 
@@ -438,13 +457,14 @@ def bench_ours(args):
     value = world * step_wbytes * K / (elapsed_ms * 1e-3) / 1e9
 
     # ---- prefill (14B-shaped layer, M = 4096) and quantizer throughput
-    extra_prefill = bench_prefill(q, args, bf16_peak) if not args.skip_extra else None
-    extra_quant = bench_quantize(q, hbm_peak) if not args.skip_extra else None
+    want = set(EXTRAS) if not args.skip_extra else set(args.extras.split(",")) - {""}
+    extra_prefill = bench_prefill(q, args, bf16_peak) if "prefill" in want else None
+    extra_quant = bench_quantize(q, hbm_peak) if "quantize" in want else None
     # ---- the other workloads: single 3B q_proj (hot/cold L2), 32B 64-layer stream (+ its
     # quantization), long sustained decode on the 7B stack
-    extra_qproj = bench_qproj_3b(q, hbm_peak) if not args.skip_extra else None
-    extra_sustained = bench_sustained(q, hbm_peak, dev_index) if not args.skip_extra else None
-    extra_32b = bench_32b_stream(q, hbm_peak) if not args.skip_extra else None
+    extra_qproj = bench_qproj_3b(q, hbm_peak) if "qproj" in want else None
+    extra_sustained = bench_sustained(q, hbm_peak, dev_index) if "sustained" in want else None
+    extra_32b = bench_32b_stream(q, hbm_peak) if "32b" in want else None
 
     # ---- the dominant launch, timed per call
     roofline = dominant_call(q, layers, acts, hbm_peak)
@@ -977,6 +997,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-extra", action="store_true",
                     help="skip the prefill, quantizer, 3B q_proj, sustained and 32B-stream measurements")
+    ap.add_argument("--extras", default="", help="with --skip-extra: a comma-separated subset of "
+                    + ",".join(EXTRAS) + " to run anyway")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ungrouped", action="store_true", help="seven single-linear calls per layer instead of four "

@@ -259,14 +259,18 @@ QERL_API qerl_status qerl_lora_linear_group(const void* x, int64_t m, int64_t k,
  * paper: this is a library convenience.  Arguments as for qerl_lora_linear,
  * without the workspace: the scratch lives in one library-owned device array
  * of 8 MiB, held by every GPU that loads the library until exit.
- *   - Problems whose scratch exceeds it (about max(m, 16)*k*2 + m*(r+1)*4 bytes, more for the LoRA partial sums of small m) return
+ *   - A problem fits exactly when qerl_lora_linear_workspace_size(m, n, k, r)
+ *     <= 8 MiB (e.g. m = 128 with k up to ~28000 at r = 32); a larger one returns
  *     QERL_ERR_WORKSPACE; nothing is allocated, ever.
  *   - All calls share the array: calls that may overlap on the GPU race, so
  *     keep them ordered (e.g. on one stream).
  *   - The first call on a device looks up the array's address on that device;
  *     make it before any stream capture.
- *   - Kernel-detected errors are not reported (the status word is private and
- *     cleared per call); argument errors are returned as usual. */
+ *   - Argument errors are returned as by qerl_lora_linear (same checks, same
+ *     order).  Kernel-detected errors are not reported: the status word is
+ *     private and cleared per call.  An expired bounded wait leaves zeros in
+ *     the output tile it hit; a non-positive or non-finite tensor scale gives
+ *     non-finite outputs. */
 QERL_API qerl_status qerl_lora_linear_noalloc(const void* x, int64_t m, int64_t k, int64_t ldx,
                                               const uint8_t* wpacked, const float* tensor_scale, int64_t n,
                                               const float* z, const void* A, const void* B, int r, float alpha,

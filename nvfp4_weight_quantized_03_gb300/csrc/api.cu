@@ -32,6 +32,73 @@ qerl_status check_ws(void* workspace, size_t ws_bytes, size_t need) {
 
 }  // namespace
 
+namespace qerl {
+
+// Argument checks of a grouped linear call (the order every linear entry point
+// uses), filling `a` with the linears that have output features.  *empty is
+// set when there is nothing to compute (m == 0 or every n == 0): the call is
+// then a no-op and needs no workspace.
+qerl_status prepare_linear_group(const void* x, int64_t m, int64_t k, int64_t ldx, const float* z,
+                                 const qerl_linear_desc* linears, int count, LinearArgs* out, bool* empty) {
+  *empty = false;
+  if (linears == nullptr || count < 1 || count > 4) return QERL_ERR_INVALID_ARGUMENT;
+  if (m < 0 || k <= 0 || ldx < k) return QERL_ERR_INVALID_ARGUMENT;
+  if (k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (k > 65536 || m > INT32_MAX || m * k > (int64_t{1} << 40)) return QERL_ERR_UNSUPPORTED_SHAPE;
+  LinearArgs a{};
+  int64_t total_n = 0;
+  for (int i = 0; i < count; ++i) {
+    const qerl_linear_desc& d = linears[i];
+    int r = d.r;
+    if (d.n < 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
+    if (d.y_dtype != QERL_BF16 && d.y_dtype != QERL_F32) return QERL_ERR_INVALID_ARGUMENT;
+    if ((d.A == nullptr) != (d.B == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
+    if (r > 0 && d.A == nullptr) r = 0;
+    if (d.A != nullptr && r == 0) return QERL_ERR_INVALID_ARGUMENT;
+    if (r > 128 || r % 8 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+    if (d.n > INT32_MAX) return QERL_ERR_UNSUPPORTED_SHAPE;
+    total_n += d.n;
+    a.lin[i].wpacked = d.wpacked;
+    a.lin[i].tensor_scale = d.tensor_scale;
+    a.lin[i].n = d.n;
+    a.lin[i].A = r > 0 ? d.A : nullptr;
+    a.lin[i].B = r > 0 ? d.B : nullptr;
+    a.lin[i].r = r;
+    a.lin[i].alpha = d.alpha;
+    a.lin[i].y = d.y;
+    a.lin[i].y_f32 = d.y_dtype == QERL_F32;
+  }
+  if (m == 0 || total_n == 0) {
+    *empty = true;
+    return QERL_OK;
+  }
+  if (x == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || ldx % 8 != 0) return QERL_ERR_MISALIGNED;
+  if (z != nullptr && !aligned(z, 16)) return QERL_ERR_MISALIGNED;
+  // Linears with no output features are dropped from the launch.
+  int nl = 0;
+  for (int i = 0; i < count; ++i) {
+    const qerl_linear_desc& d = linears[i];
+    if (d.n == 0) continue;
+    if (d.wpacked == nullptr || d.tensor_scale == nullptr || d.y == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+    if (!aligned(d.wpacked, 16)) return QERL_ERR_MISALIGNED;
+    if (d.y_dtype == QERL_F32 ? !aligned(d.y, 4) : !aligned(d.y, 2)) return QERL_ERR_MISALIGNED;
+    if (a.lin[i].r > 0 && (!aligned(d.A, 16) || !aligned(d.B, 16))) return QERL_ERR_MISALIGNED;
+    a.lin[nl] = a.lin[i];
+    ++nl;
+  }
+  a.nlin = nl;
+  a.x = x;
+  a.m = m;
+  a.k = k;
+  a.ldx = ldx;
+  a.z = z;
+  *out = a;
+  return QERL_OK;
+}
+
+}  // namespace qerl
+
 extern "C" {
 
 const char* qerl_status_string(int status) {
@@ -139,60 +206,14 @@ size_t qerl_lora_linear_group_workspace_size(int64_t m, int64_t k, const qerl_li
 qerl_status qerl_lora_linear_group(const void* x, int64_t m, int64_t k, int64_t ldx, const float* z,
                                    const qerl_linear_desc* linears, int count, void* workspace, size_t ws_bytes,
                                    void* stream) {
-  if (linears == nullptr || count < 1 || count > 4) return QERL_ERR_INVALID_ARGUMENT;
-  if (m < 0 || k <= 0 || ldx < k) return QERL_ERR_INVALID_ARGUMENT;
-  if (k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
-  if (k > 65536 || m > INT32_MAX || m * k > (int64_t{1} << 40)) return QERL_ERR_UNSUPPORTED_SHAPE;
   qerl::LinearArgs a{};
+  bool empty = false;
+  qerl_status st = qerl::prepare_linear_group(x, m, k, ldx, z, linears, count, &a, &empty);
+  if (st != QERL_OK || empty) return st;
   int ranks[4] = {0, 0, 0, 0};
-  int64_t total_n = 0;
-  for (int i = 0; i < count; ++i) {
-    const qerl_linear_desc& d = linears[i];
-    int r = d.r;
-    if (d.n < 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
-    if (d.y_dtype != QERL_BF16 && d.y_dtype != QERL_F32) return QERL_ERR_INVALID_ARGUMENT;
-    if ((d.A == nullptr) != (d.B == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
-    if (r > 0 && d.A == nullptr) r = 0;
-    if (d.A != nullptr && r == 0) return QERL_ERR_INVALID_ARGUMENT;
-    if (r > 128 || r % 8 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
-    if (d.n > INT32_MAX) return QERL_ERR_UNSUPPORTED_SHAPE;
-    total_n += d.n;
-    ranks[i] = r;
-    a.lin[i].wpacked = d.wpacked;
-    a.lin[i].tensor_scale = d.tensor_scale;
-    a.lin[i].n = d.n;
-    a.lin[i].A = r > 0 ? d.A : nullptr;
-    a.lin[i].B = r > 0 ? d.B : nullptr;
-    a.lin[i].r = r;
-    a.lin[i].alpha = d.alpha;
-    a.lin[i].y = d.y;
-    a.lin[i].y_f32 = d.y_dtype == QERL_F32;
-  }
-  if (m == 0 || total_n == 0) return QERL_OK;
-  if (x == nullptr) return QERL_ERR_INVALID_ARGUMENT;
-  if (!aligned(x, 16) || ldx % 8 != 0) return QERL_ERR_MISALIGNED;
-  if (z != nullptr && !aligned(z, 16)) return QERL_ERR_MISALIGNED;
-  // Linears with no output features are dropped from the launch.
-  int nl = 0;
-  for (int i = 0; i < count; ++i) {
-    const qerl_linear_desc& d = linears[i];
-    if (d.n == 0) continue;
-    if (d.wpacked == nullptr || d.tensor_scale == nullptr || d.y == nullptr) return QERL_ERR_INVALID_ARGUMENT;
-    if (!aligned(d.wpacked, 16)) return QERL_ERR_MISALIGNED;
-    if (d.y_dtype == QERL_F32 ? !aligned(d.y, 4) : !aligned(d.y, 2)) return QERL_ERR_MISALIGNED;
-    if (ranks[i] > 0 && (!aligned(d.A, 16) || !aligned(d.B, 16))) return QERL_ERR_MISALIGNED;
-    a.lin[nl] = a.lin[i];
-    ranks[nl] = ranks[i];
-    ++nl;
-  }
-  qerl_status st = check_ws(workspace, ws_bytes, qerl::linear_workspace_bytes(m, k, ranks, nl));
+  for (int i = 0; i < a.nlin; ++i) ranks[i] = a.lin[i].r;
+  st = check_ws(workspace, ws_bytes, qerl::linear_workspace_bytes(m, k, ranks, a.nlin));
   if (st != QERL_OK) return st;
-  a.nlin = nl;
-  a.x = x;
-  a.m = m;
-  a.k = k;
-  a.ldx = ldx;
-  a.z = z;
   a.workspace = workspace;
   a.ws_bytes = ws_bytes;
   return qerl::launch_lora_linear(a, as_stream(stream));

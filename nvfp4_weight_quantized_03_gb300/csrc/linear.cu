@@ -392,7 +392,7 @@ struct MmaParams {
   int split;       // K split across the cluster (gridDim.x), in weight stages
   int raw_stages;  // weight-stage ring depth
   int ab_stages;   // dequantized-A ring depth (also the activation ring's without kTmemA)
-  int b_stages;    // kTmemA, !coupled: activation ring depth (a multiple of kSub)
+  int b_stages;    // kTmemA, !coupled: activation ring depth in 64-wide slabs (one barrier pair each; a multiple of kSub)
   int coupled;     // kTmemA: a weight stage's activation slabs travel with its codes (same barrier, raw ring)
   int issuers;     // MMA-issuing threads, each with its own accumulator
   int t_groups;    // t holds this many partial sums [t_groups][M][r], added in order
@@ -628,13 +628,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
       mbar_init_a(raw_full(s), 1);  // producer expect_tx
-      mbar_init_a(raw_empty(s), kTmemA && p.coupled ? 8 + NI : 8);  // 8 dequant warps (+ each issuer's commit)
+      // kTmemA: the four dequant warps of the stage's group (+ each issuer's
+      // commit when the activation slabs ride in the slot); else all eight.
+      mbar_init_a(raw_empty(s), kTmemA ? 4 + (p.coupled ? NI : 0) : 8);
     }
     if (kTmemA) {
       // One barrier pair per weight stage of the tensor-memory ring (kSub MMA
-      // stages): every dequant warp arrives once, every issuer commits once.
+      // stages): the four warps of the dequant group that wrote it arrive
+      // once each, every issuer commits once.
       for (int w = 0; w < AS / kSub; ++w) {
-        mbar_init_a(ab_full(w), 8);
+        mbar_init_a(ab_full(w), 4);
         mbar_init_a(ab_empty(w), NI);
       }
     } else {
@@ -748,23 +751,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     griddep_wait();  // the staged activations are written by the preceding kernel
     if constexpr (kTmemA) {
       if (!p.coupled && lane == 0) {
-        // One bulk copy per weight stage: its kSub 64-wide K slabs (tiled
-        // layout) land as kSub consecutive ring stages.
-        const int kslabs = p.K / kStageK;
-        for (int i = 0; i < nraw; ++i) {
-          const int s0 = (i * kSub) % BS;
-          bool ok = true;
-          for (int q = 0; q < kSub && ok; ++q) {
-            const int jj = i * kSub + q;
-            ok = mbar_wait_a(b_empty(s0 + q), ((jj / BS) & 1) ^ 1, abort_flag, p.status);
+        // One bulk copy per 64-wide K slab (tiled layout: the slabs of
+        // consecutive MMA stages are contiguous), each slot with its own full
+        // and empty barrier, so a slot is refilled as soon as the MMAs that
+        // read it are done -- the copy of the next slabs overlaps the MMAs of
+        // the current ones.
+        const uint32_t slab = static_cast<uint32_t>(p.n_tok) * 128u;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(mma_begin) * slab;
+        int sb = 0;
+        uint32_t bph = 0;
+        for (int j = 0; j < nmma; ++j) {
+          if (!mbar_wait_a(b_empty(sb), bph ^ 1, abort_flag, p.status)) break;
+          mbar_arrive_expect_tx_a(b_full(sb), slab);
+          bulk_load(sbase + p.off_b + sb * slab, src + static_cast<int64_t>(j) * slab, slab, b_full(sb));
+          if (++sb == BS) {
+            sb = 0;
+            bph ^= 1;
           }
-          if (!ok) break;
-          const int rst = rb + i;
-          const uint32_t xbytes = static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128);
-          mbar_arrive_expect_tx_a(b_full(s0), xbytes);
-          bulk_load(sbase + p.off_b + s0 * (p.n_tok * 128),
-                    reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rst) * (kSub * p.n_tok * 128),
-                    xbytes, b_full(s0));
         }
       }
     } else if (!kTmemA && lane == 0) {
@@ -803,6 +806,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const uint32_t b_slab = static_cast<uint32_t>(p.n_tok * 128);
         int w = 0, rs = 0;
         uint32_t wph = 0;
+        int js = 0, jsb = 0;  // separate activation ring: slab 0 is in slot 0, phase 0
+        uint32_t jph = 0;
         for (int wi = 0; wi < nraw; ++wi) {
           if (!warp_wait(ab_full(w), wph, abort_flag, p.status)) break;
           const int nq = min(kSub, nmma - wi * kSub);
@@ -822,13 +827,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             if (u1 > u0) acc = 1;
           } else {
             // Separate activation ring: each MMA stage's slab has its own
-            // full (per weight stage) and empty (per MMA stage) barriers;
-            // with <= kSub issuers an MMA stage has a single issuer.
+            // full and empty barrier; with <= kSub issuers an MMA stage has a
+            // single issuer.  (js, jsb, jph) track this issuer's slab index,
+            // its ring slot and phase incrementally (no division in the loop).
             bool ok = true;
             for (int q = u0 >> 2; q < (u1 + 3) >> 2; ++q) {
               const int j = wi * kSub + q;
-              const int sb = j % BS;
-              if (!warp_wait(b_full(sb - sb % kSub), (j / BS) & 1, abort_flag, p.status)) {
+              while (js < j) {
+                ++js;
+                if (++jsb == BS) {
+                  jsb = 0;
+                  jph ^= 1;
+                }
+              }
+              const int sb = jsb;
+              if (!warp_wait(b_full(sb), jph, abort_flag, p.status)) {
                 ok = false;
                 break;
               }
@@ -892,69 +905,119 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
   } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------------------ dequant warps
-    // kTmemA: warp w owns TMEM lane quadrant w % 4 (rows 32(w%4)..+31), one
-    // row per thread, and K-half w / 4 of every 64-wide stage.  Otherwise 16
-    // rows per warp, two K-halves per row pair.
     const int dw = warp - kDeqWarp0;
-    const int row = kTmemA ? 32 * (warp & 3) + lane : 16 * dw + (lane & 15);
-    const int half = kTmemA ? dw >> 2 : lane >> 4;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t arow = static_cast<uint32_t>(row * 128);
-    int j = 0, as = 0, s = 0;
-    uint32_t aph = 0, ph = 0;
-    for (int i = 0; i < nraw; ++i) {
-      if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
-      const uint32_t slot = sbase + p.off_raw + s * kRawSlotBytes;
-      const uint32_t crow = slot + row * 128;
-      const uint32_t srow = slot + kCodesRawBytes + half * 256 + row * 2;
-      // This thread's codes (16 B per 64-wide stage: chunk 2q + half of the
-      // row, 128-byte swizzle) and scale pairs for the whole weight stage.
-      uint4 cw[kSub];
-      uint32_t sc[kSub];
+    if constexpr (kTmemA) {
+      // Two groups of four warps (one per TMEM lane quadrant, warp % 4) take
+      // alternate weight stages: group g = dw / 4 dequantizes stages g, g + 2,
+      // ...  A thread is one weight row (its lane of the quadrant) and covers
+      // the stage's whole 256-wide K range, one MMA stage (64 K = 32 TMEM
+      // columns of fp16 pairs) at a time: convert, store to tensor memory,
+      // next.  While one group stores and hands a stage over, the other
+      // converts the next one, so the conversion units stay busy.
+      const int grp = dw >> 2;
+      const int row = 32 * (warp & 3) + lane;
+      const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+      const int AW = AS / kSub;  // tensor-memory slots, one weight stage each (>= 2)
+      int s = grp, w = grp;      // this group's first stage (index grp): raw slot grp, A slot grp (RS, AW >= 2)
+      uint32_t ph = 0, aph = 0;
+      for (int i = grp; i < nraw; i += 2) {
+        if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
+        const uint32_t slot = sbase + p.off_raw + s * kRawSlotBytes;
+        const uint32_t crow = slot + row * 128;
+        const uint32_t srow = slot + kCodesRawBytes + row * 2;
+        const int nq = min(kSub, nmma - i * kSub);
+        const uint32_t a_slot = tmem_base + lane_base + p.col_a + static_cast<uint32_t>(w * kSub * kAStageCols);
+        bool ok = true;
 #pragma unroll
-      for (int q = 0; q < kSub; ++q) {
-        cw[q] = lds128(crow + (((2 * q + half) ^ (row & 7)) << 4));
-        sc[q] = lds16(srow + 2 * q * 256);  // scale pair 2q + half: blocks 4q + 2half, +1
-      }
-      // The whole weight stage is converted first, with no waits in between,
-      // so the conversions of its (up to) kSub MMA stages overlap.  kTmemA:
-      // the ring is handed over a weight stage (kSub MMA stages) at a time.
-      // Otherwise each MMA stage is handed over as soon as it is written (the
-      // shared-memory ring may be shallower).
-      uint32_t o[kSub][16];
+        for (int q = 0; q < kSub; ++q) {
+          if (q >= nq) break;
+          // MMA stage q: 16-byte code chunks 2q, 2q + 1 of the row (128-byte
+          // swizzle) and the scale pairs of the same K range.
+          uint32_t o[32];
 #pragma unroll
-      for (int q = 0; q < kSub; ++q) {
-        const __half2 s01 = e4m3x2_to_half2(sc[q]);
-        const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
-        const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
-        const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
-        const uint32_t words[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+          for (int h = 0; h < 2; ++h) {
+            const uint4 cw = lds128(crow + (((2 * q + h) ^ (row & 7)) << 4));
+            const __half2 s01 = e4m3x2_to_half2(lds16(srow + (2 * q + h) * 256));
+            const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
+            const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
+            const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          uint32_t u[4];
-          e2m1x8_to_f16x2x4(words[qq], u);
+            for (int qq = 0; qq < 4; ++qq) {
+              uint32_t u[4];
+              e2m1x8_to_f16x2x4(words[qq], u);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) o[q][4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
+              for (int b = 0; b < 4; ++b) o[16 * h + 4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
+            }
+          }
+          // The slot's previous MMAs must be done before the first store
+          // (the first conversion overlaps that wait).
+          if (q == 0 && !warp_wait(ab_empty(w), aph ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tmem_st_x32(a_slot + q * kAStageCols, o);
         }
-      }
-      const int nq = min(kSub, nmma - j);
-      if constexpr (kTmemA) {
-        // One wait for the weight stage's tensor-memory slot (as is a multiple
-        // of kSub here), its MMA stages stored back to back, one arrival.
-        if (!warp_wait(ab_empty(as / kSub), aph ^ 1, abort_flag, p.status)) break;
-#pragma unroll
-        for (int q = 0; q < kSub; ++q)
-          if (q < nq) tmem_st_x16(tmem_base + lane_base + p.col_a + (as + q) * kAStageCols + 16 * half, o[q]);
+        if (!ok) break;
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_a(ab_full(as / kSub));
-        as += kSub;
-        if (as == AS) {
-          as = 0;
+        if (lane == 0) {
+          mbar_arrive_a(ab_full(w));
+          mbar_arrive_a(raw_empty(s));
+        }
+        s += 2;
+        if (s >= RS) {
+          s -= RS;
+          ph ^= 1;
+        }
+        w += 2;
+        if (w >= AW) {
+          w -= AW;
           aph ^= 1;
         }
-      } else {
+      }
+    } else {
+      // 16 rows per warp, two K-halves per row pair; every MMA stage is
+      // handed over as soon as it is written to shared memory.
+      const int row = 16 * dw + (lane & 15);
+      const int half = lane >> 4;
+      const uint32_t arow = static_cast<uint32_t>(row * 128);
+      int j = 0, as = 0, s = 0;
+      uint32_t aph = 0, ph = 0;
+      for (int i = 0; i < nraw; ++i) {
+        if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
+        const uint32_t slot = sbase + p.off_raw + s * kRawSlotBytes;
+        const uint32_t crow = slot + row * 128;
+        const uint32_t srow = slot + kCodesRawBytes + half * 256 + row * 2;
+        // This thread's codes (16 B per 64-wide stage: chunk 2q + half of the
+        // row, 128-byte swizzle) and scale pairs for the whole weight stage.
+        uint4 cw[kSub];
+        uint32_t sc[kSub];
+#pragma unroll
+        for (int q = 0; q < kSub; ++q) {
+          cw[q] = lds128(crow + (((2 * q + half) ^ (row & 7)) << 4));
+          sc[q] = lds16(srow + 2 * q * 256);  // scale pair 2q + half: blocks 4q + 2half, +1
+        }
+        // The whole weight stage is converted first, with no waits in between,
+        // so the conversions of its (up to) kSub MMA stages overlap.
+        uint32_t o[kSub][16];
+#pragma unroll
+        for (int q = 0; q < kSub; ++q) {
+          const __half2 s01 = e4m3x2_to_half2(sc[q]);
+          const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
+          const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
+          const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
+          const uint32_t words[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            uint32_t u[4];
+            e2m1x8_to_f16x2x4(words[qq], u);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) o[q][4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
+          }
+        }
+        const int nq = min(kSub, nmma - j);
         bool ok = true;
 #pragma unroll
         for (int q = 0; q < kSub; ++q) {
@@ -979,13 +1042,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           }
         }
         if (!ok) break;
-      }
-      j += nq;
-      __syncwarp();
-      if (lane == 0) mbar_arrive_a(raw_empty(s));
-      if (++s == RS) {
-        s = 0;
-        ph ^= 1;
+        j += nq;
+        __syncwarp();
+        if (lane == 0) mbar_arrive_a(raw_empty(s));
+        if (++s == RS) {
+          s = 0;
+          ph ^= 1;
+        }
       }
     }
     if (do_lora) {
@@ -1383,18 +1446,33 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   int ab_stages = tmem_a ? ab_cap : 3;
   int raw_stages = 0, b_stages = 0;
   if (tmem_a) {
-    // A lives in tensor memory: keep its depth; prefer >= 6 weight stages in
-    // flight (HBM latency), then the deepest activation ring that fits.
-    const int bs_pref = coupled ? kSub : 8;
-    int best_rs = 0, best_bs = 0;
-    for (int bs = bs_pref; bs >= kSub; bs -= kSub) {
+    // A lives in tensor memory: keep its depth.  Mbarrier waits test a phase
+    // parity, so every ring slot must always be waited on by the same thread
+    // group in phase order (a waiter that is two phases ahead would pass
+    // early): the weight ring has an even number of slots (the two dequant
+    // groups take alternate stages, so each group owns the slots of its
+    // parity) and the activation ring a multiple of kSub slabs (each issuer
+    // owns fixed MMA stages of every weight stage).  Coupled: the deepest
+    // weight ring.  Separate activation ring: at least four weight stages if
+    // possible (blocks further ahead are prefetched into L2), then the
+    // deepest activation ring.
+    auto max_rs = [&](int bs) {
       int rs = kMaxRaw;
       while (rs >= 2 && plan_for(rs, ab_stages, bs).total > static_cast<uint32_t>(kSmemLimit)) --rs;
-      if (rs > best_rs) {
-        best_rs = rs;
-        best_bs = bs;
+      return rs & ~1;
+    };
+    int best_rs = 0, best_bs = 0;
+    if (coupled) {
+      best_bs = kSub;
+      best_rs = max_rs(kSub);
+    } else {
+      for (int bs = 2 * kSub; bs >= kSub; bs -= kSub) {
+        const int rs = max_rs(bs);
+        if (rs >= 2 && (best_rs == 0 || std::min(rs, 4) > std::min(best_rs, 4))) {
+          best_rs = rs;
+          best_bs = bs;
+        }
       }
-      if (rs >= 6) break;
     }
     raw_stages = best_rs;
     b_stages = best_bs;
@@ -1408,8 +1486,8 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   }
   if (raw_stages < 2 || ab_stages < (tmem_a ? kSub : std::max(2, issuers))) return QERL_ERR_UNSUPPORTED_SHAPE;
   // A weight stage is handed over (and its activations loaded) at once.
-  if (tmem_a && (ab_stages < kSub || ab_stages % kSub != 0 || b_stages < kSub || b_stages % kSub != 0 ||
-                 (kSub * 4) % issuers != 0 || (!coupled && issuers > kSub)))
+  if (tmem_a && (ab_stages < 2 * kSub || ab_stages % kSub != 0 || b_stages < kSub || b_stages % kSub != 0 ||
+                 raw_stages % 2 != 0 || (kSub * 4) % issuers != 0 || (!coupled && issuers > kSub)))
     return QERL_ERR_UNSUPPORTED_SHAPE;
   const Plan P = plan_for(raw_stages, ab_stages, b_stages);
 

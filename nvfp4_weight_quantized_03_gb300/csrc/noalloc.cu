@@ -13,10 +13,11 @@
 //
 // Rules of use:
 //   - The array is kNoallocScratchBytes (8 MiB).  Every GPU that loads the
-//     library holds it until the process exits.  A problem whose scratch does
-//     not fit (about max(m, 16)*k*2 + m*(r+1)*4 bytes: decode-sized batches fit,
-//     e.g. m = 128 with k up to ~31000) is rejected with QERL_ERR_WORKSPACE;
-//     use qerl_lora_linear with a workspace for larger ones.
+//     library holds it until the process exits.  A problem fits exactly when
+//     qerl_lora_linear_workspace_size(m, n, k, r) <= 8 MiB (decode-sized
+//     batches do, e.g. m = 128 with k up to ~28000 at r = 32); a larger one is
+//     rejected with QERL_ERR_WORKSPACE -- use qerl_lora_linear with a
+//     workspace for it.
 //   - All calls share the array, which keeps the last call's contents.  Calls
 //     that may overlap on the GPU (different streams, or unordered host
 //     threads) race on it; keep the calls ordered, e.g. on one stream.
@@ -24,8 +25,10 @@
 //     (cudaGetSymbolAddress, with that device current) and caches it.  Make
 //     that first call on a device before any stream capture.
 //   - The status word is cleared at the start of every call.  Errors that the
-//     kernels detect (a non-finite value, an expired bounded wait) are not
-//     reported through this entry point; argument errors are returned.
+//     kernels detect are not reported through this entry point (argument
+//     errors are returned as usual): an expired bounded wait leaves zeros in
+//     the output tile it hit, and a non-positive or non-finite tensor scale
+//     gives non-finite outputs.
 #include <mutex>
 
 #include "qerl_internal.h"
@@ -63,17 +66,23 @@ extern "C" qerl_status qerl_lora_linear_noalloc(const void* x, int64_t m, int64_
                                                 const uint8_t* wpacked, const float* tensor_scale, int64_t n,
                                                 const float* z, const void* A, const void* B, int r, float alpha,
                                                 void* y, int y_dtype, void* stream) {
-  if (m < 0 || n < 0 || k <= 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
-  const int r_eff = (A != nullptr && B != nullptr) ? r : 0;
-  if (qerl::linear_workspace_bytes(m, k, &r_eff, 1) > kNoallocScratchBytes) return QERL_ERR_WORKSPACE;
+  // The same argument checks, in the same order, as qerl_lora_linear: a call
+  // that the workspace entry point rejects is rejected here with the same
+  // code, before anything is enqueued.
+  if (n < 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
+  const qerl_linear_desc d{wpacked, tensor_scale, n, A, B, r, alpha, y, y_dtype};
+  qerl::LinearArgs a{};
+  bool empty = false;
+  qerl_status st = qerl::prepare_linear_group(x, m, k, ldx, z, &d, 1, &a, &empty);
+  if (st != QERL_OK || empty) return st;
+  // The scratch this problem needs is exactly qerl_lora_linear_workspace_size(m, n, k, r).
+  if (qerl::linear_workspace_bytes(m, k, &a.lin[0].r, 1) > kNoallocScratchBytes) return QERL_ERR_WORKSPACE;
   void* scratch = nullptr;
-  qerl_status st = scratch_for_current_device(&scratch);
-  if (st != QERL_OK) return st;
-  if (m > 0 && n > 0) {
-    // The status word must start at zero for this call.
-    if (cudaMemsetAsync(scratch, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-      return QERL_ERR_CUDA;
-  }
-  return qerl_lora_linear(x, m, k, ldx, wpacked, tensor_scale, n, z, A, B, r, alpha, y, y_dtype, scratch,
-                          kNoallocScratchBytes, stream);
+  if ((st = scratch_for_current_device(&scratch)) != QERL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The status word must start at zero for this call.
+  if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess) return QERL_ERR_CUDA;
+  a.workspace = scratch;
+  a.ws_bytes = kNoallocScratchBytes;
+  return qerl::launch_lora_linear(a, s);
 }

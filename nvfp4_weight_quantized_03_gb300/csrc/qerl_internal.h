@@ -55,6 +55,10 @@ struct LinearArgs {  // up to 4 linears sharing x, z and k
   size_t ws_bytes;
 };
 size_t linear_workspace_bytes(int64_t m, int64_t k, const int* ranks, int nlin);
+
+// api.cu: the argument checks shared by every linear entry point.
+qerl_status prepare_linear_group(const void* x, int64_t m, int64_t k, int64_t ldx, const float* z,
+                                 const qerl_linear_desc* linears, int count, LinearArgs* out, bool* empty);
 qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s);
 
 }  // namespace qerl

@@ -92,3 +92,30 @@ def test_noalloc_rejects_oversize_problem(q):
     assert q.qerl_lora_linear_noalloc(x, wp, S, None, None, None, 0.0, y) == QERL_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.isnan(y.float()).all()
+
+
+def test_noalloc_rejects_like_workspace_entry_point(q):
+    """Calls the workspace entry point rejects are rejected here with the same code,
+    before anything is enqueued (the output stays untouched): a rank that is not a
+    multiple of 8, a rank above 128, and a misaligned x."""
+    m, n, k = 4, 128, 256
+    x_full = torch.zeros((m, k + 8), dtype=torch.bfloat16, device="cuda")
+    x = x_full[:, :k]
+    wp = torch.zeros(q.qerl_nvfp4_packed_size(n, k), dtype=torch.uint8, device="cuda")
+    S = torch.ones(1, device="cuda")
+    ws = q.workspace(q.qerl_lora_linear_workspace_size(m, n, k, 136))
+    cases = [
+        ("rank 12", x, torch.zeros((12, k), dtype=torch.bfloat16, device="cuda"),
+         torch.zeros((n, 12), dtype=torch.bfloat16, device="cuda")),
+        ("rank 136", x, torch.zeros((136, k), dtype=torch.bfloat16, device="cuda"),
+         torch.zeros((n, 136), dtype=torch.bfloat16, device="cuda")),
+        ("misaligned x", x_full.view(-1)[1:1 + m * k].view(m, k), None, None),
+    ]
+    for what, xx, A, B in cases:
+        y = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+        want = q.qerl_lora_linear(xx, wp, S, None, A, B, 1.0, y, ws)
+        got = q.qerl_lora_linear_noalloc(xx, wp, S, None, A, B, 1.0, y)
+        torch.cuda.synchronize()
+        assert want != 0, what
+        assert got == want, f"{what}: noalloc {got}, workspace entry point {want}"
+        assert torch.isnan(y.float()).all(), f"{what}: output written by a rejected call"
