@@ -86,7 +86,10 @@ struct PrepParams {
   const float* z;
   const __nv_bfloat16* A[kMaxLinears];  // [r][K] per linear (LoRA down-projections)
   int r[kMaxLinears];
-  float* t[kMaxLinears];  // [groups][M][r] partial sums of x~ . A^T over K group g, per linear
+  float* t[kMaxLinears];   // [groups][M][r] partial sums of x~ . A^T over K group g, per linear
+  float* tf[kMaxLinears];  // [M][r] their sum (written by the last cluster to finish a LoRA tile)
+  unsigned* tile_count;    // per LoRA tile (lora_tiles of them): clusters done; reset by the last one
+  int sum_groups;          // 1: sum the groups into tf (the consumer reads one sum); 0: the consumer adds them
   int tile_begin[kMaxLinears + 1];  // LoRA tiles of linear l: [tile_begin[l], tile_begin[l+1])
   __half* xs;   // staged x~ * 2^e_m: [M][K], or tiled (see xs_tile_offset)
   float* rinv;  // [M] 2^-e_m
@@ -118,13 +121,32 @@ __host__ __device__ inline size_t xs_tile_offset(int m, int k, int rows) {
 struct LoraSplit {
   int cluster, groups;
 };
-__host__ inline LoraSplit lora_split(int64_t m, int64_t k) {
+// The last cluster to finish a tile sums the groups (see prep_kernel), so the
+// group count only trades prep parallelism against that final sum.  Tiles
+// count their finished clusters in a fixed region of the workspace
+// (kMaxLoraCounters); a call with more LoRA tiles uses one group per tile.
+constexpr int kMaxLoraCounters = 4096;
+__host__ inline int lora_tile_count(int64_t m, const int* ranks, int nlin) {
+  int64_t tiles = 0;
+  for (int i = 0; i < nlin; ++i)
+    if (ranks[i] > 0) tiles += ((m + kLoraTileM - 1) / kLoraTileM) * ((ranks[i] + kLoraTileR - 1) / kLoraTileR);
+  return static_cast<int>(std::min<int64_t>(tiles, INT32_MAX));
+}
+// Pair-mode token tiles (65..128 rows) have the prep kernel sum the groups;
+// other tiles stage every group's partial sums and add them, so their group
+// count is bounded by that staging buffer (256 / n_tok groups).
+__host__ inline bool lora_sum_in_prep(int64_t m) { return m > 64 && m <= 128; }
+__host__ inline LoraSplit lora_split(int64_t m, int64_t k, const int* ranks, int nlin) {
   const int kc_total = static_cast<int>(k / kLoraKc);
   LoraSplit L;
   L.cluster = std::max(1, std::min(kPrepMaxCluster, kc_total));
   int g = (kc_total + 2 * L.cluster - 1) / (2 * L.cluster);
-  const int64_t n_tok = std::min<int64_t>(256, (m + 15) / 16 * 16);
-  g = std::min<int>(g, static_cast<int>(std::max<int64_t>(1, 256 / std::max<int64_t>(n_tok, 1))));
+  if (lora_sum_in_prep(m)) {
+    if (lora_tile_count(m, ranks, nlin) > kMaxLoraCounters) g = 1;
+  } else {
+    const int64_t n_tok = std::min<int64_t>(256, (m + 15) / 16 * 16);
+    g = std::min<int>(g, static_cast<int>(std::max<int64_t>(1, 256 / std::max<int64_t>(n_tok, 1))));
+  }
   L.groups = std::max(1, std::min(16, g));
   return L;
 }
@@ -230,6 +252,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   const int lt = blockIdx.y - p.row_groups;
   const int g = lt / p.lora_tiles;
   int tile = lt - g * p.lora_tiles;
+  const int tile_lin = tile;  // this LoRA tile over all linears (its counter)
   int li = 0;
   while (tile >= p.tile_begin[li + 1]) ++li;
   tile -= p.tile_begin[li];
@@ -247,8 +270,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   float* xsm = reinterpret_cast<float*>(sm + kLoraStages * kLoraStageBytes);  // [kLoraTileM][kLoraPad]
   float* asm_ = xsm + kLoraTileM * kLoraPad;                                   // [kLoraTileR][kLoraPad]
   const uint32_t ring = smem_u32(sm);
-  const int lr = tid & 31, rp = tid >> 5;
-  float acc0 = 0.0f, acc1 = 0.0f;
+  constexpr int kRowsPerThread = kLoraTileM * kLoraTileR / kPrepThreads;
+  static_assert(kRowsPerThread * (kPrepThreads / 32) == kLoraTileM, "LoRA tile map");
+  const int lr = tid & 31, rq = tid >> 5;
+  float acc[kRowsPerThread];
+#pragma unroll
+  for (int i = 0; i < kRowsPerThread; ++i) acc[i] = 0.0f;
   const int kc_total = p.K / kLoraKc;
   const int slices = p.cluster * p.groups;
   const int sl = g * p.cluster + ks;
@@ -287,8 +314,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
       const __nv_bfloat16* xr = reinterpret_cast<const __nv_bfloat16*>(stg);
       const __nv_bfloat16* ar = xr + kLoraTileM * kLoraKc;
       const float* zr = reinterpret_cast<const float*>(ar + kLoraTileR * kLoraKc);
-      {
-        const int rr = tid >> 4, k4 = (tid & 15) * 4;  // 16 rows x 64 k, four per thread
+      for (int i = tid; i < kLoraTileM * kLoraKc / 4; i += kPrepThreads) {
+        const int rr = i >> 4, k4 = (i & 15) * 4;  // 16 rows x 64 k, four per item
         float4 f;
         f.x = noisy(__bfloat162float(xr[rr * kLoraKc + k4]), zr[k4]);
         f.y = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 1]), zr[k4 + 1]);
@@ -296,8 +323,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
         f.w = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 3]), zr[k4 + 3]);
         *reinterpret_cast<float4*>(xsm + rr * kLoraPad + k4) = f;
       }
-      {
-        const int jj = tid >> 3, k8 = (tid & 7) * 8;  // 32 ranks x 64 k, eight per thread
+      for (int i = tid; i < kLoraTileR * kLoraKc / 8; i += kPrepThreads) {
+        const int jj = i >> 3, k8 = (i & 7) * 8;  // 32 ranks x 64 k, eight per item
         const uint4 raw = *reinterpret_cast<const uint4*>(ar + jj * kLoraKc + k8);
         const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
         float4* d = reinterpret_cast<float4*>(asm_ + jj * kLoraPad + k8);
@@ -311,17 +338,15 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     if (++st == kLoraStages) st = 0;
 #pragma unroll 4
     for (int kk = 0; kk < kLoraKc; kk += 4) {
-      const float4 x0 = *reinterpret_cast<const float4*>(xsm + (2 * rp) * kLoraPad + kk);
-      const float4 x1 = *reinterpret_cast<const float4*>(xsm + (2 * rp + 1) * kLoraPad + kk);
       const float4 av = *reinterpret_cast<const float4*>(asm_ + lr * kLoraPad + kk);
-      acc0 = fmaf(x0.x, av.x, acc0);
-      acc0 = fmaf(x0.y, av.y, acc0);
-      acc0 = fmaf(x0.z, av.z, acc0);
-      acc0 = fmaf(x0.w, av.w, acc0);
-      acc1 = fmaf(x1.x, av.x, acc1);
-      acc1 = fmaf(x1.y, av.y, acc1);
-      acc1 = fmaf(x1.z, av.z, acc1);
-      acc1 = fmaf(x1.w, av.w, acc1);
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i) {
+        const float4 xv = *reinterpret_cast<const float4*>(xsm + (kRowsPerThread * rq + i) * kLoraPad + kk);
+        acc[i] = fmaf(xv.x, av.x, acc[i]);
+        acc[i] = fmaf(xv.y, av.y, acc[i]);
+        acc[i] = fmaf(xv.z, av.z, acc[i]);
+        acc[i] = fmaf(xv.w, av.w, acc[i]);
+      }
     }
   }
   cp_async_wait_group<0>();
@@ -329,17 +354,49 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   // then CTA q of the cluster sums entries q, q + cluster, ... over all slices.
   __syncthreads();
   float* part = reinterpret_cast<float*>(sm);
-  part[(2 * rp) * kLoraTileR + lr] = acc0;
-  part[(2 * rp + 1) * kLoraTileR + lr] = acc1;
+#pragma unroll
+  for (int i = 0; i < kRowsPerThread; ++i) part[(kRowsPerThread * rq + i) * kLoraTileR + lr] = acc[i];
   cluster_sync_all();
   const uint32_t part_s = smem_u32(part);
   for (int idx = ks * kPrepThreads + tid; idx < kLoraTileM * kLoraTileR; idx += p.cluster * kPrepThreads) {
     float v = 0.0f;
     for (int q = 0; q < p.cluster; ++q) v += ld_shared_cluster_f32(mapa_shared(part_s + 4u * idx, q));
     const int row = row0 + idx / kLoraTileR, rank = rank0 + idx % kLoraTileR;
-    if (row < p.M && rank < rr_) tout[(static_cast<int64_t>(g) * p.M + row) * rr_ + rank] = v;
+    if (row < p.M && rank < rr_) {
+      if (p.sum_groups && p.groups == 1)
+        p.tf[li][static_cast<int64_t>(row) * rr_ + rank] = v;  // one group: already the sum
+      else
+        tout[(static_cast<int64_t>(g) * p.M + row) * rr_ + rank] = v;
+    }
   }
-  cluster_sync_all();  // partners are done reading this CTA's partial tile
+  cluster_sync_all();  // partners are done reading this CTA's partial tile; the group's writes are ordered
+  if (!p.sum_groups || p.groups == 1) return;
+  // The last cluster to finish this LoRA tile (one per K group) adds the
+  // groups' partial sums in group order -- deterministic -- into tf, so the
+  // MMA kernel reads one sum per element.  It resets the counter for the next
+  // call.  (Release: the cluster barrier above orders the group's writes
+  // before this CTA's fence and atomic; acquire: the fence after it.)
+  if (ks != 0) return;
+  __shared__ unsigned last;
+  if (tid == 0) {
+    __threadfence();
+    const unsigned done = atomicAdd(p.tile_count + tile_lin, 1u);
+    last = done == static_cast<unsigned>(p.groups - 1) ? 1u : 0u;
+    if (last) {
+      __threadfence();
+      p.tile_count[tile_lin] = 0u;
+    }
+  }
+  __syncthreads();
+  if (!last) return;
+  float* tfin = p.tf[li];
+  for (int idx = tid; idx < kLoraTileM * kLoraTileR; idx += kPrepThreads) {
+    const int row = row0 + idx / kLoraTileR, rank = rank0 + idx % kLoraTileR;
+    if (row >= p.M || rank >= rr_) continue;
+    float v = 0.0f;
+    for (int gg = 0; gg < p.groups; ++gg) v += __ldcg(tout + (static_cast<int64_t>(gg) * p.M + row) * rr_ + rank);
+    tfin[static_cast<int64_t>(row) * rr_ + rank] = v;
+  }
 }
 
 // ------------------------------------------------------------------ MMA kernel
@@ -365,6 +422,14 @@ constexpr int kAStageCols = kStageK / 2;               // 32 TMEM columns (fp16 
 constexpr int kLoraChunkK = 64;                        // r is processed in 64-wide chunks (one 128-B swizzle atom)
 constexpr int kBtChunkBytes = kTileN * 128;            // B^T chunk: 128 rows x 64 bf16
 constexpr int kMaxRaw = 8, kMaxAB = 8, kMaxB = 16;
+constexpr int kMaxSplit = 8;  // CTAs of a K-split cluster (portable cluster size)
+// Weight blocks prefetched into L2 ahead of the ring: the ring's copies are
+// held for a stage's whole dequant + MMA time, so the ring alone cannot cover
+// HBM latency at full rate; the ring refills from L2.
+constexpr int kPrefetchStages = 8;
+// Pair mode uses two issuer warps; the other six build the LoRA operand's t
+// tiles while the weights stream.
+constexpr int kPairLoraWarps = kMaxIssuers - 2;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kBarBytes = 1024;
 constexpr int kTmemCols = 512;
@@ -402,6 +467,12 @@ struct MmaParams {
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
   int wave;        // CTAs per wave (one per SM) when split == 1, else 0
   int stage_out;   // the widest output tile (fp32) fits in the idle ring: staged stores
+  // kTmemA, more than 64 tokens: a CTA takes a pair of adjacent 128-row tiles
+  // of one linear (grid y counts pairs), so every activation slab it receives
+  // serves 256 weight rows.  Dequant group g and issuer g own tile g; the
+  // tensor-memory A slots are handed over per MMA stage (one per tile and
+  // stage of the weight stage), the LoRA operands are built in the idle ring.
+  int pair;
 };
 
 // The LoRA up-projection's B matrices, one TMA map per linear of the launch.
@@ -410,8 +481,10 @@ struct BtMaps {
 };
 
 __host__ __device__ inline int lora_chunks(int r) { return (r + kLoraChunkK - 1) / kLoraChunkK; }
-__host__ __device__ inline uint32_t lora_bytes(int r, int n_tok) {
-  return r > 0 ? static_cast<uint32_t>(lora_chunks(r)) * (kBtChunkBytes + 2u * n_tok * 128u) : 0u;
+// LoRA operand region: `nbt` sets of B^T chunks (one per weight tile of the
+// CTA), then the t_hi and t_lo chunks shared by them.
+__host__ __device__ inline uint32_t lora_bytes(int r, int n_tok, int nbt = 1) {
+  return r > 0 ? static_cast<uint32_t>(lora_chunks(r)) * (nbt * kBtChunkBytes + 2u * n_tok * 128u) : 0u;
 }
 
 __device__ __forceinline__ void store_out(const LinearSlot& L, int m, int n, float v) {
@@ -472,9 +545,9 @@ __device__ __forceinline__ void fill_lora_factors(const MmaParams& p, const Line
   }
 }
 __device__ void build_t_tiles(const MmaParams& p, const LinearSlot& L, uint32_t base, uint32_t fac, int m0, int tid,
-                              int nthr) {
+                              int nthr, int nbt = 1) {
   const int rc = lora_chunks(L.r);
-  const uint32_t thi = base + rc * kBtChunkBytes;
+  const uint32_t thi = base + nbt * rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
   for (int idx = tid; idx < rc * p.n_tok * 8; idx += nthr) {
     const int c = idx / (p.n_tok * 8), rem = idx - c * (p.n_tok * 8);
@@ -541,12 +614,15 @@ __device__ void build_t_tiles_staged(const MmaParams& p, const LinearSlot& L, ui
 }
 
 // TMA of the B^T chunks (rows n0..n0+127 of B [N][r], 64 ranks per chunk,
-// zero-filled past N and r) into `base`, completing on `bar`.
+// zero-filled past N and r) into `base`, completing on `bar`; for `ntl` tiles
+// (rows n0 + 128 i, chunk set i at base + i * rc * kBtChunkBytes), one arrival.
 __device__ __forceinline__ void load_bt_tiles(const LinearSlot& L, const CUtensorMap* tm_bl, uint32_t base, int n0,
-                                              uint32_t bar) {
+                                              uint32_t bar, int ntl = 1) {
   const int rc = lora_chunks(L.r);
-  mbar_arrive_expect_tx_a(bar, static_cast<uint32_t>(rc) * kBtChunkBytes);
-  for (int c = 0; c < rc; ++c) tma_load_2d(base + c * kBtChunkBytes, tm_bl, c * kLoraChunkK, n0, bar);
+  mbar_arrive_expect_tx_a(bar, static_cast<uint32_t>(rc * ntl) * kBtChunkBytes);
+  for (int i = 0; i < ntl; ++i)
+    for (int c = 0; c < rc; ++c)
+      tma_load_2d(base + (i * rc + c) * kBtChunkBytes, tm_bl, c * kLoraChunkK, n0 + i * kTileN, bar);
 }
 
 // Warp-cooperative bounded wait.  Every lane polls: one convergent try_wait
@@ -562,14 +638,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 // D += B^T . t_hi^T + B^T . t_lo^T over the rank dimension (bf16 x bf16 ->
 // fp32), into an accumulator that already holds this thread's main-loop sum.
-__device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, const LinearSlot& L, uint32_t base, uint32_t d2) {
+// `bt` is this tile's B^T chunk set, `thi` the t_hi chunks (t_lo follows).
+__device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, const LinearSlot& L, uint32_t bt, uint32_t thi,
+                                                uint32_t d2) {
   const int rc = lora_chunks(L.r);
   const uint32_t idesc = idesc_bf16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
-  const uint32_t thi = base + rc * kBtChunkBytes;
   const uint32_t tlo = thi + rc * p.n_tok * 128;
   for (int c = 0; c < rc; ++c)
     for (int kk = 0; kk < kLoraChunkK / 16 && c * kLoraChunkK + kk * 16 < L.r; ++kk) {
-      const uint64_t ad = sw128_kmajor_desc(base + c * kBtChunkBytes + kk * 32);
+      const uint64_t ad = sw128_kmajor_desc(bt + c * kBtChunkBytes + kk * 32);
       tc_mma_f16(d2, ad, sw128_kmajor_desc(thi + c * p.n_tok * 128 + kk * 32), idesc, 1u);
       tc_mma_f16(d2, ad, sw128_kmajor_desc(tlo + c * p.n_tok * 128 + kk * 32), idesc, 1u);
     }
@@ -613,7 +690,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   while (gi + 1 < p.nlin && static_cast<int>(blockIdx.y) >= p.lin[gi + 1].tile_begin) ++gi;
   const LinearSlot& L = p.lin[gi];
   const CUtensorMap* tm_bl = &tm_bls.m[gi];
-  const int n0 = (static_cast<int>(blockIdx.y) - L.tile_begin) * kTileN;
+  const int n0 = (static_cast<int>(blockIdx.y) - L.tile_begin) * kTileN * (p.pair ? 2 : 1);
+  // Weight tiles this CTA streams: 1, or 2 in pair mode (1 for an odd last tile).
+  const int ntl = p.pair ? min(2, (L.N - n0 + kTileN - 1) / kTileN) : 1;
+  const uint32_t rslot = static_cast<uint32_t>(p.pair ? 2 : 1) * kRawSlotBytes;  // raw-ring slot size
   const int m0 = blockIdx.z * p.n_tok;
   const int raw_total = (p.K + kRawK - 1) / kRawK;
   const int rb = static_cast<int>(static_cast<int64_t>(split_idx) * raw_total / p.split);
@@ -624,15 +704,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int nmma = min(kSub * re, kb_total) - mma_begin;
   const int RS = p.raw_stages, AS = p.ab_stages, NI = p.issuers, BS = p.b_stages;
   const bool do_lora = L.r > 0 && split_idx == 0;  // one CTA of a K-split cluster adds the LoRA term
+  const int n_iss = p.pair ? ntl : NI;              // issuers with work (each commits once to the barriers below)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
       mbar_init_a(raw_full(s), 1);  // producer expect_tx
       // kTmemA: the four dequant warps of the stage's group (+ each issuer's
-      // commit when the activation slabs ride in the slot); else all eight.
-      mbar_init_a(raw_empty(s), kTmemA ? 4 + (p.coupled ? NI : 0) : 8);
+      // commit when the activation slabs ride in the slot); pair mode: the
+      // groups of both tiles; else all eight.
+      mbar_init_a(raw_empty(s), kTmemA ? (p.pair ? 4 * ntl : 4 + (p.coupled ? NI : 0)) : 8);
     }
-    if (kTmemA) {
+    if (kTmemA && p.pair) {
+      // One barrier pair per (tile, MMA stage) slot of tensor memory: the
+      // tile's four dequant warps arrive, its issuer commits.
+      for (int w = 0; w < 2 * kSub; ++w) {
+        mbar_init_a(ab_full(w), 4);
+        mbar_init_a(ab_empty(w), 1);
+      }
+    } else if (kTmemA) {
       // One barrier pair per weight stage of the tensor-memory ring (kSub MMA
       // stages): the four warps of the dequant group that wrote it arrive
       // once each, every issuer commits once.
@@ -648,13 +737,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     if (kTmemA)
       for (int s = 0; s < BS; ++s) {
-        mbar_init_a(b_full(s), 1);   // producer: arrive after its copies landed, or expect_tx
-        mbar_init_a(b_empty(s), 1);  // tcgen05.commit
+        mbar_init_a(b_full(s), 1);                  // producer expect_tx
+        mbar_init_a(b_empty(s), p.pair ? ntl : 1);  // tcgen05.commit of each issuer reading the slab
       }
-    mbar_init_a(ring_free, NI);
-    // B^T TMA (expect_tx) + the eight dequant warps, which build the t tiles
-    mbar_init_a(lora_full, 9);
-    mbar_init_a(acc_full, NI);
+    mbar_init_a(ring_free, n_iss);
+    // B^T TMA (expect_tx) + the warps that build the t tiles: the eight
+    // dequant warps, or in pair mode the six issuer warps without a tile.
+    mbar_init_a(lora_full, p.pair ? 1 + kPairLoraWarps : 9);
+    mbar_init_a(acc_full, n_iss);
     mbar_init_a(t_full, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -683,44 +773,58 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // preceding kernel.
     const bool coupled = kTmemA && p.coupled;
     const uint8_t* wtile = L.wpacked + static_cast<int64_t>(n0 / kTileN) * raw_total * kRawSlotBytes;
+    const int64_t tile_stride = static_cast<int64_t>(raw_total) * kRawSlotBytes;  // next tile's blocks (pair mode)
     const int kslabs = p.K / kStageK;
     // The copies into the ring are held for a stage's whole dequant + MMA
     // time, so the ring alone cannot cover HBM latency at full rate: the
     // blocks kPrefetch stages ahead are prefetched into L2 (bounded by L2
     // capacity, not shared memory) and the ring refills from L2.
-    constexpr int kPrefetch = 8;
-    if (lane == 0)
+    constexpr int kPrefetch = kPrefetchStages;
+    if (!kTmemA && lane == 0)
       for (int i = 0; i < min(kPrefetch, nraw); ++i)
         bulk_prefetch_l2(wtile + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes);
     auto xbytes_of = [&](int rst) {
       return coupled ? static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128) : 0u;
     };
-    // Coupled: the first ring's weight blocks do not depend on the preceding
-    // kernel (the weights were written before it started), so they are
-    // requested before waiting for it; their activation slabs, and the
-    // arrivals that let those stages complete, follow once it has finished.
-    const int early = coupled ? min(RS, nraw) : 0;
-    if (lane == 0)
+    // kTmemA: the first ring of weight blocks (and L2 prefetches further
+    // ahead) is requested at once: the weights were written before the
+    // preceding kernel of this call started.  Coupled: the stages' activation
+    // slabs, and the arrivals that let them complete, follow once that kernel
+    // has finished.
+    const int early = kTmemA ? min(RS, nraw) : 0;
+    if (kTmemA && lane == 0) {
+      for (int i = 0; i < min(kPrefetch, nraw); ++i)
+        for (int t = 0; t < ntl; ++t)
+          bulk_prefetch_l2(wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes);
       for (int i = 0; i < early; ++i) {
-        mbar_expect_tx_a(raw_full(i), kRawSlotBytes);
-        bulk_load(sbase + p.off_raw + i * kRawSlotBytes, wtile + static_cast<int64_t>(rb + i) * kRawSlotBytes,
-                  kRawSlotBytes, raw_full(i));
+        if (coupled)
+          mbar_expect_tx_a(raw_full(i), kRawSlotBytes);
+        else
+          mbar_arrive_expect_tx_a(raw_full(i), ntl * kRawSlotBytes);
+        for (int t = 0; t < ntl; ++t)
+          bulk_load(sbase + p.off_raw + i * rslot + t * kRawSlotBytes,
+                    wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes,
+                    raw_full(i));
       }
+    }
     if (coupled) griddep_wait();
     if (lane == 0) {
       uint32_t ph = 0;
       for (int i = 0, s = 0; i < nraw; ++i) {
         if (i + kPrefetch < nraw)
-          bulk_prefetch_l2(wtile + static_cast<int64_t>(rb + i + kPrefetch) * kRawSlotBytes, kRawSlotBytes);
+          for (int t = 0; t < ntl; ++t)
+            bulk_prefetch_l2(wtile + t * tile_stride + static_cast<int64_t>(rb + i + kPrefetch) * kRawSlotBytes,
+                             kRawSlotBytes);
         const int rst = rb + i;
         const uint32_t xbytes = xbytes_of(rst);
         if (i < early) {
-          mbar_arrive_expect_tx_a(raw_full(s), xbytes);
+          if (coupled) mbar_arrive_expect_tx_a(raw_full(s), xbytes);
         } else {
           if (!mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status)) break;
-          mbar_arrive_expect_tx_a(raw_full(s), kRawSlotBytes + xbytes);
-          bulk_load(sbase + p.off_raw + s * kRawSlotBytes, wtile + static_cast<int64_t>(rst) * kRawSlotBytes,
-                    kRawSlotBytes, raw_full(s));
+          mbar_arrive_expect_tx_a(raw_full(s), ntl * kRawSlotBytes + xbytes);
+          for (int t = 0; t < ntl; ++t)
+            bulk_load(sbase + p.off_raw + s * rslot + t * kRawSlotBytes,
+                      wtile + t * tile_stride + static_cast<int64_t>(rst) * kRawSlotBytes, kRawSlotBytes, raw_full(s));
         }
         if (coupled)
           bulk_load(sbase + p.off_b + s * p.raw_b_bytes,
@@ -782,11 +886,48 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kMaxIssuers) {
     // ------------------------------------------------------------ MMA issuers
     const int ii = warp - kIssuerWarp0;
-    if (ii < NI) {
+    if (ii < n_iss) {
       const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
       const uint32_t d_acc = tmem_base + static_cast<uint32_t>(ii * p.n_tok);
       uint32_t acc = 0;
-      if constexpr (kTmemA) {
+      if (kTmemA && p.pair) {
+        // Pair mode: this issuer owns tile ii of the pair (its accumulator,
+        // its tensor-memory A slot per MMA stage q: ab_*(ii * kSub + q)) and
+        // reads every activation slab in order; each slab's empty barrier
+        // takes the commits of both issuers.
+        const uint32_t b_slab = static_cast<uint32_t>(p.n_tok * 128);
+        int jsb = 0;
+        uint32_t jph = 0;
+        for (int wi = 0; wi < nraw; ++wi) {
+          const int nq = min(kSub, nmma - wi * kSub);
+          bool ok = true;
+          for (int q = 0; q < nq; ++q) {
+            const int sl = ii * kSub + q;
+            if (!warp_wait(ab_full(sl), wi & 1, abort_flag, p.status) ||
+                !warp_wait(b_full(jsb), jph, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_st = tmem_base + p.col_a + static_cast<uint32_t>(sl * kAStageCols);
+            const uint32_t b_addr = sbase + p.off_b + jsb * b_slab;
+            if (lane == 0) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16_ts(d_acc, a_st + kk * 8, sw128_kmajor_desc(b_addr + kk * 32), idesc,
+                              (wi > 0 || q > 0 || kk > 0) ? 1u : 0u);
+              tc_commit(ab_empty(sl));
+              tc_commit(b_empty(jsb));
+            }
+            if (++jsb == BS) {
+              jsb = 0;
+              jph ^= 1;
+            }
+          }
+          __syncwarp();
+          if (!ok) break;
+        }
+      } else if constexpr (kTmemA) {
         // The whole warp runs the loop (waits, addresses and descriptors are
         // warp-uniform); lane 0 issues the MMAs and their commits.  A weight
         // stage holds kSub x 4 MMAs (u = 4 q + kk: MMA stage q, K step kk);
@@ -887,26 +1028,110 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (lane == 0) {
         // The LoRA up-projection goes last, so a slow producer of t never
         // holds up the weight stream.
-        if (ii == 0 && do_lora && p.lora_early) {
+        if ((p.pair || ii == 0) && do_lora && p.lora_early) {
+          // Pair mode: each issuer adds its own tile's up-projection (its B^T
+          // chunk set; the t tiles are shared).  Otherwise issuer 0 does.
           if (mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
             tc_fence_after();
-            issue_lora_mmas(p, L, lora_base, d_acc);
+            const int rc = lora_chunks(L.r);
+            const int nbt = p.pair ? 2 : 1;
+            issue_lora_mmas(p, L, lora_base + static_cast<uint32_t>((p.pair ? ii : 0) * rc * kBtChunkBytes),
+                            lora_base + static_cast<uint32_t>(nbt * rc * kBtChunkBytes), d_acc);
           }
         }
         if (do_lora && !p.lora_early) {
           tc_commit(ring_free);  // the ring is idle once every mainloop MMA is done
-          if (ii == 0 && mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
+          // Pair mode: each issuer adds its own tile's up-projection (its B^T
+          // chunk set; the t tiles are shared).  Otherwise issuer 0 does.
+          if ((p.pair || ii == 0) && mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
             tc_fence_after();
-            issue_lora_mmas(p, L, lora_base, d_acc);
+            const int rc = lora_chunks(L.r);
+            const int nbt = p.pair ? 2 : 1;
+            issue_lora_mmas(p, L, lora_base + static_cast<uint32_t>((p.pair ? ii : 0) * rc * kBtChunkBytes),
+                            lora_base + static_cast<uint32_t>(nbt * rc * kBtChunkBytes), d_acc);
           }
         }
         tc_commit(acc_full);  // always, so the epilogue's wait completes even after an abort
       }
+    } else if (p.pair && do_lora && ii >= 2) {
+      // Pair mode: the issuer warps without a tile build the LoRA operand's
+      // t tiles (shared by both tiles) from the partial sums in global
+      // memory while the weights stream, into the dedicated LoRA region.
+      const int ltid = static_cast<int>(threadIdx.x) - 32 * (kIssuerWarp0 + 2);
+      const int lthr = 32 * kPairLoraWarps;
+      griddep_wait();  // t and the row exponents come from the preceding kernel
+      fill_lora_factors(p, L, smv + 4u * p.n_tok, m0, ltid, lthr);
+      named_barrier_sync(2, lthr);
+      // Without room for a dedicated region (large ranks) the operand is
+      // built in the ring once the mainloop has left it.
+      if (p.lora_early || warp_wait(ring_free, 0, abort_flag, p.status))
+        build_t_tiles(p, L, lora_base, smv + 4u * p.n_tok, m0, ltid, lthr, 2);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_a(lora_full);
     }
   } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------------------ dequant warps
     const int dw = warp - kDeqWarp0;
-    if constexpr (kTmemA) {
+    if (kTmemA && p.pair) {
+      // Pair mode: group g = dw / 4 dequantizes tile g of the pair (a thread
+      // is one weight row of it), every weight stage, and hands each MMA
+      // stage's 32 TMEM columns over as soon as they are stored, so the next
+      // stage's conversion overlaps the current stage's remaining MMAs.
+      const int g = dw >> 2;
+      if (g < ntl) {
+        const int row = 32 * (warp & 3) + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        int s = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < nraw; ++i) {
+          if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
+          const uint32_t slot = sbase + p.off_raw + s * rslot + g * kRawSlotBytes;
+          const uint32_t crow = slot + row * 128;
+          const uint32_t srow = slot + kCodesRawBytes + row * 2;
+          const int nq = min(kSub, nmma - i * kSub);
+          bool ok = true;
+#pragma unroll
+          for (int q = 0; q < kSub; ++q) {
+            if (q >= nq) break;
+            uint32_t o[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 cw = lds128(crow + (((2 * q + h) ^ (row & 7)) << 4));
+              const __half2 s01 = e4m3x2_to_half2(lds16(srow + (2 * q + h) * 256));
+              const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
+              const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
+              const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
+              const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                uint32_t u[4];
+                e2m1x8_to_f16x2x4(words[qq], u);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) o[16 * h + 4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
+              }
+            }
+            const int sl = g * kSub + q;
+            if (!warp_wait(ab_empty(sl), (i & 1) ^ 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tmem_st_x32(tmem_base + lane_base + p.col_a + static_cast<uint32_t>(sl * kAStageCols), o);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_a(ab_full(sl));
+          }
+          if (!ok) break;
+          __syncwarp();
+          if (lane == 0) mbar_arrive_a(raw_empty(s));
+          if (++s == RS) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    } else if constexpr (kTmemA) {
       // Two groups of four warps (one per TMEM lane quadrant, warp % 4) take
       // alternate weight stages: group g = dw / 4 dequantizes stages g, g + 2,
       // ...  A thread is one weight row (its lane of the quadrant) and covers
@@ -1051,7 +1276,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
       }
     }
-    if (do_lora) {
+    if (do_lora && !p.pair) {
       // The LoRA operand's t tiles, by all 256 dequant threads once their
       // stream is done: from the rows the LoRA warp staged (early), or from
       // global memory into the idle ring (late).
@@ -1064,7 +1289,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           build_t_tiles_staged(p, L, lora_base, sbase + p.off_tstage, smv + 4u * p.n_tok, min(p.n_tok, p.M - m0),
                                dtid, 256);
       } else if (warp_wait(ring_free, 0, abort_flag, p.status)) {
-        build_t_tiles(p, L, lora_base, smv + 4u * p.n_tok, m0, dtid, 256);
+        build_t_tiles(p, L, lora_base, smv + 4u * p.n_tok, m0, dtid, 256, p.pair ? 2 : 1);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -1073,7 +1298,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp == kLoraWarp) {
     // ------------------------------------------------------------ LoRA operands
     if (do_lora) {
-      if (p.lora_early) {
+      if (p.lora_early && p.pair) {
+        // Both tiles' B^T chunk sets (a missing second tile: zeros); the
+        // idle issuer warps build the t tiles.
+        if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full, 2);
+      } else if (p.lora_early) {
         if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full);
         griddep_wait();  // t comes from the preceding kernel
         // Bulk-copy this tile's rows of every partial sum, then convert from
@@ -1089,7 +1318,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         // The dequant warps build the t tiles from these rows after their main loop.
       } else if (warp_wait(ring_free, 0, abort_flag, p.status)) {
-        if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full);
+        // Pair mode: both tiles' B^T chunk sets (the second one's rows past N
+        // read as zeros); otherwise this tile's.
+        if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full, p.pair ? ntl : 1);
       } else if (lane == 0) {
         mbar_arrive_expect_tx_a(lora_full, 0);  // after an abort: keep the barrier count consistent
       }
@@ -1097,8 +1328,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   }
 
   // ---------------------------------------------------------------- epilogue
-  const uint32_t part = sbase;  // [n_tok][128] fp32 scaled partial tile (split > 1), ring reused
+  const uint32_t part = sbase;  // [tile][n_tok][128] fp32 scaled partial tiles (split > 1), ring reused
   const int dt = static_cast<int>(threadIdx.x) - 32 * kDeqWarp0;  // dequant-warp thread index
+  const int ntl_e = p.pair ? ntl : 1;                              // weight tiles of this CTA
   if (warp >= kDeqWarp0) {
     // Row scales S * 2^-e_m come from the preceding kernel; the dequant above did not need them.
     griddep_wait();
@@ -1112,22 +1344,61 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     tc_fence_after();
     const int q = warp & 3;
     const int nl = q * 32 + lane;
-    const int n = n0 + nl;
-    const int cols = p.n_tok / 2;
-    const int c0 = ((warp - kDeqWarp0) >> 2) * cols;
+    // Pair mode: warp group eg reads tile eg's accumulator, all token columns;
+    // otherwise the two groups split the token columns of the one tile.
+    const int eg = p.pair ? (warp - kDeqWarp0) >> 2 : 0;
+    const bool live = eg < ntl_e;
+    const int n = n0 + eg * kTileN + nl;
+    const int cols = p.pair ? p.n_tok : p.n_tok / 2;
+    const int c0 = p.pair ? 0 : ((warp - kDeqWarp0) >> 2) * cols;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t acc0 = static_cast<uint32_t>(eg * p.n_tok);       // first accumulator column
+    const uint32_t tile_out = static_cast<uint32_t>(eg * p.n_tok * kTileN);  // element offset of its staged tile
     // Issuer a holds a sum iff its first MMA falls in the first weight
-    // stage's (up to kSub) MMA stages: a prefix of the issuers.
+    // stage's (up to kSub) MMA stages: a prefix of the issuers.  Pair mode:
+    // one accumulator per tile.
     const int nq0 = min(kSub, nmma);
-    const int nacc = min(NI, (nq0 * NI + 3) / 4);
-    for (int c = c0; c < c0 + cols; c += 8) {
+    const int nacc = p.pair ? 1 : min(NI, (nq0 * NI + 3) / 4);
+    if (p.pair && live) {
+      // One accumulator per tile: 32 token columns per TMEM load and wait
+      // (columns past n_tok are read -- they lie inside tensor memory -- but
+      // not stored).  The row scales come in as vectors; an unsplit tile is
+      // stored straight from registers (a warp writes 32 consecutive outputs
+      // of one token row per store), a split one goes to its partial tile.
+      const int rows = min(p.n_tok, p.M - m0);
+      for (int c = 0; c < p.n_tok; c += 32) {
+        float w[32], sc[32];
+        tmem_ld_x32(tmem_base + acc0 + lane_off + c, w);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 s4 = lds128f(smv + 4u * (c + e));
+          sc[e] = s4.x;
+          sc[e + 1] = s4.y;
+          sc[e + 2] = s4.z;
+          sc[e + 3] = s4.w;
+        }
+        tmem_ld_wait();
+        if (p.split > 1) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c + e < p.n_tok)
+              stsf(part + 4u * (tile_out + static_cast<uint32_t>((c + e) * kTileN + nl)), ok ? w[e] * sc[e] : 0.0f);
+        } else if (n < L.N) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c + e < rows) store_out(L, m0 + c + e, n, ok ? w[e] * sc[e] : 0.0f);
+        }
+      }
+    }
+    for (int c = c0; !p.pair && c < c0 + cols; c += 8) {
       float v[8];
       // Four accumulators' columns per wait (issuer 0's holds the LoRA term).
       for (int a0 = 0; a0 < nacc; a0 += 4) {
         float w[4][8];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
-          if (a0 + a < nacc) tmem_ld_x8(tmem_base + static_cast<uint32_t>((a0 + a) * p.n_tok) + lane_off + c, w[a]);
+          if (a0 + a < nacc)
+            tmem_ld_x8(tmem_base + acc0 + static_cast<uint32_t>((a0 + a) * p.n_tok) + lane_off + c, w[a]);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -1141,21 +1412,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float out = ok ? v[e] * ldsf(smv + 4u * (c + e)) : 0.0f;
+        const uint32_t el = tile_out + static_cast<uint32_t>((c + e) * kTileN + nl);
         if (p.split > 1)
-          stsf(part + 4u * ((c + e) * kTileN + nl), out);
+          stsf(part + 4u * el, out);
         else if (!p.stage_out) {
           if (m0 + c + e < p.M && n < L.N) store_out(L, m0 + c + e, n, out);
         } else if (L.y_f32) {
-          stsf(sbase + 4u * ((c + e) * kTileN + nl), out);  // staged: [token][128 rows]
+          stsf(sbase + 4u * el, out);  // staged: [tile][token][128 rows]
         } else {
-          sts16(sbase + 2u * ((c + e) * kTileN + nl), __bfloat16_as_ushort(__float2bfloat16_rn(out)));
+          sts16(sbase + 2u * el, __bfloat16_as_ushort(__float2bfloat16_rn(out)));
         }
       }
     }
-    if (p.split == 1 && p.stage_out) {
+    if (p.split == 1 && p.stage_out && !p.pair) {
       // The output tile leaves shared memory (the idle ring) a token row at a
-      // time in 16-byte vectors: far fewer store instructions than one 2- or
-      // 4-byte store per thread and token.
+      // time: one bulk copy per row when rows are 16-byte aligned (the writes
+      // drain after the CTA has moved on), else 16-byte vectors.
       fence_proxy_async_smem();  // the staged tile is read by bulk copies below
       named_barrier_sync(1, 256);
       const int rows = min(p.n_tok, p.M - m0);
@@ -1164,8 +1436,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       uint8_t* ybase = reinterpret_cast<uint8_t*>(L.y);
       const bool vec = (reinterpret_cast<uintptr_t>(ybase) & 15u) == 0 && (static_cast<int64_t>(L.N) * es) % 16 == 0;
       if (vec && (nvalid * es) % 16 == 0) {
-        // One bulk copy per token row; the writes drain after this CTA has
-        // moved on (it only waits for shared memory to have been read).
         if (dt < rows) {
           bulk_store(ybase + (static_cast<int64_t>(m0 + dt) * L.N + n0) * es,
                      sbase + static_cast<uint32_t>(dt * kTileN * es), static_cast<uint32_t>(nvalid * es));
@@ -1173,22 +1443,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           bulk_wait_group_read0();
         }
       } else {
-      const int chunks = vec ? nvalid * es / 16 : 0;  // whole 16-byte chunks per token row
-      for (int it = dt; it < rows * chunks; it += 256) {
-        const int ml = it / chunks, ch = it - ml * chunks;
-        const uint4 val = lds128(sbase + static_cast<uint32_t>(ml * kTileN * es + ch * 16));
-        *reinterpret_cast<uint4*>(ybase + (static_cast<int64_t>(m0 + ml) * L.N + n0) * es + ch * 16) = val;
-      }
-      const int e0 = chunks * 16 / es;  // the rest element by element
-      const int rest = nvalid - e0;
-      for (int it = dt; it < rows * rest; it += 256) {
-        const int ml = it / rest, nn = e0 + (it - ml * rest);
-        const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0 + nn;
-        if (L.y_f32)
-          reinterpret_cast<float*>(ybase)[gi] = ldsf(sbase + 4u * (ml * kTileN + nn));
-        else
-          reinterpret_cast<uint16_t*>(ybase)[gi] = lds16(sbase + 2u * (ml * kTileN + nn));
-      }
+        const int chunks = vec ? nvalid * es / 16 : 0;  // whole 16-byte chunks per token row
+        for (int it = dt; it < rows * chunks; it += 256) {
+          const int ml = it / chunks, ch = it - ml * chunks;
+          const uint4 val = lds128(sbase + static_cast<uint32_t>(ml * kTileN * es + ch * 16));
+          *reinterpret_cast<uint4*>(ybase + (static_cast<int64_t>(m0 + ml) * L.N + n0) * es + ch * 16) = val;
+        }
+        const int e0 = chunks * 16 / es;  // the rest element by element
+        const int rest = nvalid - e0;
+        for (int it = dt; it < rows * rest; it += 256) {
+          const int ml = it / rest, nn = e0 + (it - ml * rest);
+          const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0 + nn;
+          if (L.y_f32)
+            reinterpret_cast<float*>(ybase)[gi] = ldsf(sbase + 4u * (ml * kTileN + nn));
+          else
+            reinterpret_cast<uint16_t*>(ybase)[gi] = lds16(sbase + 2u * (ml * kTileN + nn));
+        }
       }
     }
   }
@@ -1211,35 +1481,65 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // Four consecutive outputs per thread: one 8- (bf16) or 16-byte (f32)
       // store when the row pitch and base allow it.
       const bool vec4 = (reinterpret_cast<uintptr_t>(L.y) & 15u) == 0 && L.N % 4 == 0;
-      for (int it = dt; it < (me - mb) * (kTileN / 4); it += 256) {
-        const int ml = mb + it / (kTileN / 4);
-        const int nl4 = 4 * (it % (kTileN / 4));
-        const uint32_t off = 4u * static_cast<uint32_t>(ml * kTileN + nl4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int qq = 0; qq < p.split; ++qq) {
-          const float4 v = ld_shared_cluster_f32x4(mapa_shared(part + off, qq));
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
-        }
-        const float out[4] = {acc.x, acc.y, acc.z, acc.w};
-        const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0 + nl4;
-        if (vec4 && n0 + nl4 + 3 < L.N) {
-          if (L.y_f32) {
-            *reinterpret_cast<float4*>(reinterpret_cast<float*>(L.y) + gi) = acc;
-          } else {
-            uint2 pk;
-            pk.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
-                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
-            pk.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
-                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
-            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(L.y) + gi) = pk;
-          }
-        } else {
+      const int per_tile = max(0, me - mb) * (kTileN / 4);
+      // Every partner's partial tile, mapped once.  Each thread sums two
+      // 4-column groups at a time and issues all their remote loads (up to
+      // 2 x 8) before the first add, so the distributed-shared-memory latency
+      // is paid once per group pair, not once per partner.
+      uint32_t rpart[kMaxSplit];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (n0 + nl4 + e < L.N) store_out(L, m0 + ml, n0 + nl4 + e, out[e]);
+      for (int qq = 0; qq < kMaxSplit; ++qq) rpart[qq] = qq < p.split ? mapa_shared(part, qq) : 0u;
+      for (int it0 = dt; it0 < ntl_e * per_tile; it0 += 512) {
+        float4 v[2][kMaxSplit];
+        uint32_t off[2];
+        bool have[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int it = it0 + u * 256;
+          have[u] = it < ntl_e * per_tile;
+          const int t = have[u] ? it / per_tile : 0, rem = have[u] ? it - t * per_tile : 0;
+          const int ml = mb + rem / (kTileN / 4);
+          off[u] = 4u * static_cast<uint32_t>(t * p.n_tok * kTileN + ml * kTileN + 4 * (rem % (kTileN / 4)));
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int qq = 0; qq < kMaxSplit; ++qq)
+            if (have[u] && qq < p.split) v[u][qq] = ld_shared_cluster_f32x4(rpart[qq] + off[u]);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (!have[u]) continue;
+          const int it = it0 + u * 256;
+          const int t = it / per_tile, rem = it - t * per_tile;
+          const int ml = mb + rem / (kTileN / 4);
+          const int nl4 = 4 * (rem % (kTileN / 4)) + t * kTileN;  // column within this CTA's tiles
+          float4 acc = v[u][0];
+#pragma unroll
+          for (int qq = 1; qq < kMaxSplit; ++qq)
+            if (qq < p.split) {
+              acc.x += v[u][qq].x;
+              acc.y += v[u][qq].y;
+              acc.z += v[u][qq].z;
+              acc.w += v[u][qq].w;
+            }
+          const float out[4] = {acc.x, acc.y, acc.z, acc.w};
+          const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0 + nl4;
+          if (vec4 && n0 + nl4 + 3 < L.N) {
+            if (L.y_f32) {
+              *reinterpret_cast<float4*>(reinterpret_cast<float*>(L.y) + gi) = acc;
+            } else {
+              uint2 pk;
+              pk.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
+                     (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
+              pk.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
+                     (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
+              *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(L.y) + gi) = pk;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (n0 + nl4 + e < L.N) store_out(L, m0 + ml, n0 + nl4 + e, out[e]);
+          }
         }
       }
     }
@@ -1294,8 +1594,45 @@ int sm_count() {
   return sms;
 }
 
+// How many clusters of `sp` decode-kernel CTAs (maximal shared memory, one
+// per SM) can be resident on the current device at once; queried once per
+// device and cluster size.  sp == 1: the SM count.
+int resident_clusters(int sp) {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices][kMaxSplit + 1] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool cacheable = dev >= 0 && dev < kMaxDevices && sp >= 1 && sp <= kMaxSplit;
+  if (cacheable) {
+    const int c = cached[dev][sp].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (sp == 1) {
+    n = sm_count();
+  } else {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(sp), 1, 1);
+    cfg.blockDim = dim3(kMmaThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemLimit;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(sp);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // the query failed: fall back to whole SMs
+      n = sm_count() / sp;
+    }
+  }
+  if (cacheable && n > 0) cached[dev][sp].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 struct LinearLayout {
-  size_t xs, rinv, t[kMaxLinears], total;
+  size_t xs, rinv, t[kMaxLinears], tf[kMaxLinears], count, total;
 };
 
 // Token tiles of up to 128 rows stage x~ in the tiled layout (one tile of
@@ -1304,17 +1641,22 @@ inline int tiled_rows_for(int64_t m) { return m <= 128 ? static_cast<int>((m + 1
 
 LinearLayout linear_layout(int64_t m, int64_t k, const int* ranks, int nlin) {
   LinearLayout L;
-  L.xs = kWsHeaderBytes;
+  // Fixed offset, whatever the shape: the LoRA tiles' completion counters,
+  // zero between calls (each is reset by the cluster that finishes its tile).
+  L.count = kWsHeaderBytes;
+  L.xs = align_up(L.count + kMaxLoraCounters * sizeof(unsigned), 256);
   const int tr = tiled_rows_for(m);
   const size_t xs_bytes =
       tr > 0 ? static_cast<size_t>((k + kRawK - 1) / kRawK) * 4u * tr * 128u : static_cast<size_t>(m) * k * 2;
   L.rinv = align_up(L.xs + xs_bytes, 256);
   size_t off = align_up(L.rinv + static_cast<size_t>(m) * 4, 256);
-  const size_t groups = static_cast<size_t>(lora_split(m, k).groups);
+  const size_t groups = static_cast<size_t>(lora_split(m, k, ranks, nlin).groups);
   for (int i = 0; i < kMaxLinears; ++i) {
     L.t[i] = off;
     const int r = i < nlin && ranks[i] > 0 ? ranks[i] : 0;
     off = align_up(off + groups * static_cast<size_t>(m) * r * 4, 256);
+    L.tf[i] = off;
+    off = align_up(off + static_cast<size_t>(m) * r * 4, 256);
   }
   L.total = off;
   return L;
@@ -1330,17 +1672,51 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   const int M = static_cast<int>(a.m), K = static_cast<int>(a.k);
   const int nlin = a.nlin;
   if (nlin < 1 || nlin > kMaxLinears) return QERL_ERR_INVALID_ARGUMENT;
+  // Token tiles: one of round_up(M, 16) rows up to 256 tokens, else 256-row tiles.
+  const int n_tok = M <= 256 ? (M + 15) / 16 * 16 : 256;
+  const int m_tiles = M <= 256 ? 1 : (M + 255) / 256;
+  const int raw_total = (K + kRawK - 1) / kRawK;
   int ranks[kMaxLinears] = {0, 0, 0, 0};
-  int tile_begin[kMaxLinears + 1] = {0, 0, 0, 0, 0};
+  int tiles[kMaxLinears] = {0, 0, 0, 0};
   int r = 0;  // the largest rank: sizes the LoRA operand region
+  int all_pairs = 0;
   for (int i = 0; i < nlin; ++i) {
     const LinearDesc& d = a.lin[i];
     ranks[i] = (d.r > 0 && d.A != nullptr && d.B != nullptr) ? d.r : 0;
     r = std::max(r, ranks[i]);
-    tile_begin[i + 1] = tile_begin[i] + static_cast<int>((d.n + kTileN - 1) / kTileN);
+    tiles[i] = static_cast<int>((d.n + kTileN - 1) / kTileN);
+    all_pairs += (tiles[i] + 1) / 2;
   }
+  // K split across a cluster when the CTAs alone leave SMs idle: minimise
+  // waves x weight stages per CTA, with a small per-CTA fixed cost.  A wave is
+  // as many clusters as can be resident at once (clusters live inside one
+  // GPC, so e.g. 7-CTA clusters leave SMs unused).
+  auto best_split = [&](int units) {
+    if (n_tok > 128) return 1;
+    int sp_best = 1;
+    double best = 1e30;
+    for (int sp = 1; sp <= kMaxSplit && sp <= raw_total; ++sp) {
+      const int resident = resident_clusters(sp);
+      if (resident <= 0) continue;
+      const int waves = (units * m_tiles + resident - 1) / resident;
+      const double cost = waves * (static_cast<double>((raw_total + sp - 1) / sp) + 1.5);
+      if (cost < best - 1e-9) {
+        best = cost;
+        sp_best = sp;
+      }
+    }
+    return sp_best;
+  };
+  // Decode tiles above 64 tokens run in pair mode -- one CTA per two adjacent
+  // 128-row weight tiles of a linear, sharing the activation slabs -- when
+  // each CTA then streams at least 6 weight stages: its mainloop is about
+  // twice as fast per tile, its fixed costs (two tiles' epilogue) higher.
+  const int split_pair = n_tok > 64 && n_tok <= 128 ? best_split(all_pairs) : 1;
+  const bool pair = n_tok > 64 && n_tok <= 128 && (raw_total + split_pair - 1) / split_pair >= 6;
+  int tile_begin[kMaxLinears + 1] = {0, 0, 0, 0, 0};  // in grid-y units: tiles, or pairs of tiles
+  for (int i = 0; i < nlin; ++i) tile_begin[i + 1] = tile_begin[i] + (pair ? (tiles[i] + 1) / 2 : tiles[i]);
   const bool lora = r > 0;
-  const int n_tiles = tile_begin[nlin];
+  const int n_tiles = tile_begin[nlin];  // grid-y units
   const LinearLayout WL = linear_layout(a.m, a.k, ranks, nlin);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   int* status = reinterpret_cast<int*>(ws);
@@ -1368,34 +1744,16 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   if (attr_err != cudaSuccess) return QERL_ERR_CUDA;
 
   // ---- tile shape and pipeline depth (host-side checks before any launch)
-  int n_tok, m_tiles;
-  if (M <= 256) {
-    n_tok = (M + 15) / 16 * 16;
-    m_tiles = 1;
-  } else {
-    n_tok = 256;
-    m_tiles = (M + 255) / 256;
-  }
-  const int raw_total = (K + kRawK - 1) / kRawK;
-  int split = 1;
-  if (n_tok <= 128) {
-    // K split across a cluster when the tiles alone leave SMs idle: minimise
-    // waves x weight stages per CTA, with a small per-CTA fixed cost.
-    double best = 1e30;
-    for (int sp = 1; sp <= 8 && sp <= raw_total; ++sp) {
-      const int ctas = n_tiles * m_tiles * sp;
-      const int waves = (ctas + sms - 1) / sms;
-      const double cost = waves * (static_cast<double>((raw_total + sp - 1) / sp) + 1.5);
-      if (cost < best - 1e-9) {
-        best = cost;
-        split = sp;
-      }
-    }
-  }
-  const uint32_t lb = lora_bytes(r, n_tok);
-  const uint32_t tstage_bytes = r > 0 ? static_cast<uint32_t>(lora_split(M, K).groups * n_tok * r * 4) : 0u;
-  const int lora_early = (r > 0 && n_tok <= 128) ? 1 : 0;
-  const uint32_t part_bytes = split > 1 ? static_cast<uint32_t>(n_tok) * kTileN * 4u : 0u;
+  const int split = best_split(n_tiles);
+  const int tpc = pair ? 2 : 1;  // weight tiles per CTA
+  const uint32_t lb = lora_bytes(r, n_tok, tpc);
+  // The LoRA operand is built early (its own region) up to 128 tokens: from
+  // partial sums staged in shared memory, or in pair mode straight from
+  // global memory by the idle issuer warps.
+  const int t_groups = lora_sum_in_prep(M) ? 1 : lora_split(M, K, ranks, nlin).groups;  // partial sums the MMA kernel adds
+  const uint32_t tstage_bytes = (r > 0 && !pair) ? static_cast<uint32_t>(t_groups * n_tok * r * 4) : 0u;
+  int lora_early = (r > 0 && n_tok <= 128) ? 1 : 0;
+  const uint32_t part_bytes = split > 1 ? static_cast<uint32_t>(tpc * n_tok) * kTileN * 4u : 0u;
   const uint32_t b_stage = static_cast<uint32_t>(n_tok) * 128u;
   // Decode-sized tiles (<= 128 tokens) keep the dequantized weights in tensor
   // memory and spread MMA issue over several threads; 256-token tiles stage
@@ -1404,6 +1762,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // Each MMA occupies its issuing thread for ~150 cycles whatever the token
   // count, so small tiles take more issuers (each with its own accumulator,
   // which tensor memory must hold next to the A ring).
+  // Pair mode: one issuer per tile.
   const int issuers = !tmem_a ? 1 : (n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2));
   const uint32_t col_a = static_cast<uint32_t>(align_up(issuers * n_tok, 32));
   int ab_cap = kMaxAB;
@@ -1428,7 +1787,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   auto plan_for = [&](int rs, int as, int bs) {
     Plan P;
     P.raw = 0;  // packed weight blocks (codes + scale pairs); 18 KB slots keep 1024-byte alignment
-    P.a = P.raw + rs * kRawSlotBytes;
+    P.a = P.raw + rs * tpc * kRawSlotBytes;
     P.b = P.a + (tmem_a ? 0u : static_cast<uint32_t>(as) * kAStageBytes);
     uint32_t ring = P.b + (coupled ? rs * raw_b : (tmem_a ? bs : as) * b_stage);
     if (!lora_early) ring = std::max(ring, lb);  // late LoRA tiles are built inside the ring
@@ -1456,19 +1815,24 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     // weight ring.  Separate activation ring: at least four weight stages if
     // possible (blocks further ahead are prefetched into L2), then the
     // deepest activation ring.
+    // (Pair mode: both dequant groups visit every weight slot in order, so
+    // any depth >= 2 works.)
     auto max_rs = [&](int bs) {
       int rs = kMaxRaw;
       while (rs >= 2 && plan_for(rs, ab_stages, bs).total > static_cast<uint32_t>(kSmemLimit)) --rs;
-      return rs & ~1;
+      return pair ? rs : rs & ~1;
     };
     int best_rs = 0, best_bs = 0;
     if (coupled) {
       best_bs = kSub;
       best_rs = max_rs(kSub);
     } else {
+      // Pair mode: each slab waits for both tiles' MMAs before it is
+      // refilled, so two weight stages of activations come first.
+      const int rs_pref = pair ? 2 : 4;
       for (int bs = 2 * kSub; bs >= kSub; bs -= kSub) {
         const int rs = max_rs(bs);
-        if (rs >= 2 && (best_rs == 0 || std::min(rs, 4) > std::min(best_rs, 4))) {
+        if (rs >= 2 && (best_rs == 0 || std::min(rs, rs_pref) > std::min(best_rs, rs_pref))) {
           best_rs = rs;
           best_bs = bs;
         }
@@ -1484,10 +1848,25 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
       if (raw_stages >= 2) break;
     }
   }
+  if (tmem_a && lora_early && raw_stages < 2) {
+    // Large rank: no room for a dedicated LoRA region; build the operand in
+    // the idle ring after the mainloop instead.
+    lora_early = 0;
+    for (int bs = coupled ? kSub : 2 * kSub; bs >= kSub && raw_stages < 2; bs -= kSub) {
+      int rs = kMaxRaw;
+      while (rs >= 2 && plan_for(rs, ab_stages, bs).total > static_cast<uint32_t>(kSmemLimit)) --rs;
+      if (!pair) rs &= ~1;
+      if (rs >= 2) {
+        raw_stages = rs;
+        b_stages = bs;
+      }
+    }
+  }
   if (raw_stages < 2 || ab_stages < (tmem_a ? kSub : std::max(2, issuers))) return QERL_ERR_UNSUPPORTED_SHAPE;
   // A weight stage is handed over (and its activations loaded) at once.
   if (tmem_a && (ab_stages < 2 * kSub || ab_stages % kSub != 0 || b_stages < kSub || b_stages % kSub != 0 ||
-                 raw_stages % 2 != 0 || (kSub * 4) % issuers != 0 || (!coupled && issuers > kSub)))
+                 (!pair && raw_stages % 2 != 0) || (kSub * 4) % issuers != 0 || (!coupled && issuers > kSub) ||
+                 (pair && (issuers != 2 || ab_stages != 2 * kSub))))
     return QERL_ERR_UNSUPPORTED_SHAPE;
   const Plan P = plan_for(raw_stages, ab_stages, b_stages);
 
@@ -1520,7 +1899,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   pp.ldx = a.ldx;
   pp.M = M;
   pp.K = K;
-  const LoraSplit ls = lora_split(M, K);
+  const LoraSplit ls = lora_split(M, K, ranks, nlin);
   pp.cluster = lora ? ls.cluster : 1;
   pp.groups = lora ? ls.groups : 0;
   pp.tiled_rows = tmem_a ? n_tok : 0;
@@ -1532,11 +1911,14 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     pp.A[i] = on ? static_cast<const __nv_bfloat16*>(a.lin[i].A) : nullptr;
     pp.r[i] = on ? ranks[i] : 0;
     pp.t[i] = reinterpret_cast<float*>(ws + WL.t[i]);
+    pp.tf[i] = reinterpret_cast<float*>(ws + WL.tf[i]);
     pp.tile_begin[i + 1] = pp.tile_begin[i] + (on ? pp.lora_m_tiles * ((ranks[i] + kLoraTileR - 1) / kLoraTileR) : 0);
   }
   pp.lora_tiles = pp.tile_begin[kMaxLinears];
+  pp.tile_count = reinterpret_cast<unsigned*>(ws + WL.count);
+  pp.sum_groups = lora_sum_in_prep(M) ? 1 : 0;
   const int lora_ctas_y = pp.lora_tiles * pp.groups;
-  size_t prep_smem = static_cast<size_t>(K) * 2;
+  size_t prep_smem = static_cast<size_t>(K) * 2;  // row tasks stage the row
   if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>(kLoraSmemBytes));
   if (prep_smem > static_cast<size_t>(kPrepSmemLimit)) return QERL_ERR_UNSUPPORTED_SHAPE;
   {
@@ -1563,7 +1945,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     LinearSlot& L = mp.lin[i];
     L.wpacked = a.lin[i].wpacked;
     L.tensor_scale = a.lin[i].tensor_scale;
-    L.t = pp.t[i];
+    L.t = pp.sum_groups ? pp.tf[i] : pp.t[i];  // the summed down-projection, or its group partials
     L.y = a.lin[i].y;
     L.N = static_cast<int>(a.lin[i].n);
     L.r = ranks[i];
@@ -1582,7 +1964,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.coupled = coupled;
   mp.raw_b_bytes = raw_b;
   mp.issuers = issuers;
-  mp.t_groups = pp.groups;
+  mp.t_groups = pp.sum_groups ? 1 : pp.groups;  // == t_groups
   mp.col_a = col_a;
   mp.off_raw = P.raw;
   mp.off_a = P.a;
@@ -1592,8 +1974,9 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.off_sm = P.sm;
   mp.off_bars = P.bars;
   mp.lora_early = lora_early;
-  mp.wave = split == 1 ? sms : 0;
-  mp.stage_out = static_cast<uint32_t>(n_tok) * kTileN * 4u <= P.lora ? 1 : 0;
+  mp.wave = (split == 1 && !pair) ? sms : 0;
+  mp.stage_out = static_cast<uint32_t>(tpc * n_tok) * kTileN * 4u <= P.lora ? 1 : 0;
+  mp.pair = pair ? 1 : 0;
 
   const uint32_t smem_bytes = P.total;
 

@@ -86,6 +86,13 @@ SMALL = [
     (600, 256, 256, 128, 1e-2),
     (8, 512, 3584, 32, 1e-2),  # 7B k/v shape at decode (K split across a cluster)
     (32, 1024, 4096, 16, 0.0),
+    # pair mode (65..128 tokens: two 128-row tiles per CTA sharing the activation slabs)
+    (100, 384, 2048, 128, 1e-2),  # 3 tiles: the second CTA has one; rank 128 (late LoRA operand)
+    (72, 1000, 1024, 32, 1e-2),   # ragged N inside the last pair
+    (128, 256, 6144, 32, 1e-2),   # one pair, K split across a cluster
+    (65, 128, 512, 8, 0.0),       # a single tile in pair mode
+    (48, 384, 3584, 128, 1e-2),   # rank 128 at 33..64 tokens: the LoRA operand built late, in the idle ring
+    (128, 512, 18944, 128, 5e-3), # rank 128 at 128 tokens, long K (pair mode, summed LoRA groups)
 ]
 
 
