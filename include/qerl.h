@@ -253,6 +253,51 @@ QERL_API qerl_status qerl_lora_linear_group(const void* x, int64_t m, int64_t k,
                                             const qerl_linear_desc* linears, int count, void* workspace,
                                             size_t ws_bytes, void* stream);
 
+/* ========================================================================
+ * Per-rollout noise ("Adaptive Quantization Noise", noise injection: each
+ * rollout sees its own noise sample).  As qerl_lora_linear_group, with a row
+ * stride for z: z == NULL: no noise; ldz == 0: one vector z[k] for every row
+ * (the batch broadcast of Eq. 9); ldz >= k: row i of x uses z + i * ldz (one
+ * vector per rollout / token row).  ldz % 4 == 0 (16-byte aligned rows).
+ * Workspace: qerl_lora_linear_group_workspace_size(m, k, linears, count).
+ * ======================================================================== */
+QERL_API qerl_status qerl_lora_linear_group_rowz(const void* x, int64_t m, int64_t k, int64_t ldx, const float* z,
+                                                 int64_t ldz, const qerl_linear_desc* linears, int count,
+                                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* ========================================================================
+ * RMSNorm with the noise merged into its scale, feeding the linears
+ * ("Noise Merging", Eq. 10-11: the noise Z is added to the RMSNorm weight w,
+ * which is equivalent to the per-input-channel factor (1 + Z/w) on the
+ * normalised activation):
+ *
+ *   x~[i][j] = bf16_RN( (w[j] + Z[j]) * (h[i][j] / sqrt((1/k) sum_l h[i][l]^2 + delta)) )
+ *
+ * computed in fp64 in that order with one rounding, then the grouped linear of
+ * qerl_lora_linear_group on x~ (no further noise; both branches see x~).
+ * h       device bf16 [m][ldh] (the pre-norm hidden state), 16-byte aligned,
+ *         ldh % 8 == 0.
+ * w_norm  device bf16 [k] (the RMSNorm weight), 16-byte aligned.
+ * Z       device fp32 [k] (the AQN noise of this norm's consumers) or NULL
+ *         (plain RMSNorm), 16-byte aligned.
+ * delta   the RMSNorm epsilon, finite and >= 0 (delta == 0 on an all-zero row
+ *         gives NaN, as the definition does).
+ * Requires k % 64 == 0, m <= 65535.  workspace: at least
+ * qerl_rmsnorm_lora_linear_group_workspace_size(m, k, linears, count) bytes
+ * (it also holds x~ when a linear has a LoRA branch).
+ * ======================================================================== */
+QERL_API size_t qerl_rmsnorm_lora_linear_group_workspace_size(int64_t m, int64_t k, const qerl_linear_desc* linears,
+                                                              int count);
+QERL_API qerl_status qerl_rmsnorm_lora_linear_group(const void* h, int64_t m, int64_t k, int64_t ldh,
+                                                    const void* w_norm, const float* Z, double delta,
+                                                    const qerl_linear_desc* linears, int count, void* workspace,
+                                                    size_t ws_bytes, void* stream);
+
+/* The normalisation step above on its own: out device bf16 [m][ldo] receives
+ * x~ (16-byte aligned, ldo % 8 == 0).  k % 8 == 0, m <= 65535.  No workspace. */
+QERL_API qerl_status qerl_rmsnorm_noise(const void* h, int64_t m, int64_t k, int64_t ldh, const void* w_norm,
+                                        const float* Z, double delta, void* out, int64_t ldo, void* stream);
+
 /* The same linear for callers that cannot allocate device memory where they
  * run it (a runtime with a fixed memory pool, a latency-critical loop that must
  * not enter the CUDA allocator, a hard memory budget).  No counterpart in the

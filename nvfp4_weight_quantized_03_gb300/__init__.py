@@ -126,6 +126,18 @@ def lib():
             L.qerl_lora_linear_group.restype = ctypes.c_int
             L.qerl_lora_linear_group.argtypes = [_vp, _i64, _i64, _i64, _vp, ctypes.POINTER(LinearDesc), ctypes.c_int,
                                                  _vp, ctypes.c_size_t, _vp]
+            L.qerl_lora_linear_group_rowz.restype = ctypes.c_int
+            L.qerl_lora_linear_group_rowz.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, ctypes.POINTER(LinearDesc),
+                                                      ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+            L.qerl_rmsnorm_lora_linear_group_workspace_size.restype = ctypes.c_size_t
+            L.qerl_rmsnorm_lora_linear_group_workspace_size.argtypes = [_i64, _i64, ctypes.POINTER(LinearDesc),
+                                                                        ctypes.c_int]
+            L.qerl_rmsnorm_lora_linear_group.restype = ctypes.c_int
+            L.qerl_rmsnorm_lora_linear_group.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, ctypes.c_double,
+                                                         ctypes.POINTER(LinearDesc), ctypes.c_int, _vp,
+                                                         ctypes.c_size_t, _vp]
+            L.qerl_rmsnorm_noise.restype = ctypes.c_int
+            L.qerl_rmsnorm_noise.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, ctypes.c_double, _vp, _i64, _vp]
             L.qerl_lora_linear_noalloc.restype = ctypes.c_int
             L.qerl_lora_linear_noalloc.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
                                                    ctypes.c_int, ctypes.c_float, _vp, ctypes.c_int, _vp]
@@ -287,6 +299,37 @@ def qerl_lora_linear_group(x, z, linears, workspace, stream=None) -> int:
     arr = _descs(linears)
     return lib().qerl_lora_linear_group(_p(x), m, k, x.stride(0), _p(z), arr, len(arr), _p(workspace),
                                         _nbytes(workspace), _stream(stream))
+
+
+def qerl_lora_linear_group_rowz(x, z, linears, workspace, stream=None) -> int:
+    """The grouped linear with per-row noise: z is None, a [k] vector (every row), or [m, k]
+    float32 (row i of x uses z[i]; its row stride is passed)."""
+    m, k = x.shape
+    arr = _descs(linears)
+    ldz = 0 if z is None or z.dim() == 1 else z.stride(0)
+    return lib().qerl_lora_linear_group_rowz(_p(x), m, k, x.stride(0), _p(z), ldz, arr, len(arr), _p(workspace),
+                                             _nbytes(workspace), _stream(stream))
+
+
+def qerl_rmsnorm_lora_linear_group_workspace_size(m: int, k: int, linears) -> int:
+    arr = _descs(linears)
+    return lib().qerl_rmsnorm_lora_linear_group_workspace_size(int(m), int(k), arr, len(arr))
+
+
+def qerl_rmsnorm_lora_linear_group(h, w_norm, Z, delta, linears, workspace, stream=None) -> int:
+    """RMSNorm of h [m, k] (bf16) with the noise Z [k] (float32, or None) merged into its
+    weight w_norm [k] (bf16), then the grouped linear of the result."""
+    m, k = h.shape
+    arr = _descs(linears)
+    return lib().qerl_rmsnorm_lora_linear_group(_p(h), m, k, h.stride(0), _p(w_norm), _p(Z), float(delta), arr,
+                                                len(arr), _p(workspace), _nbytes(workspace), _stream(stream))
+
+
+def qerl_rmsnorm_noise(h, w_norm, Z, delta, out, stream=None) -> int:
+    """The normalisation step alone: out [m, k] bf16 = bf16((w_norm + Z) * h / rms(h))."""
+    m, k = h.shape
+    return lib().qerl_rmsnorm_noise(_p(h), m, k, h.stride(0), _p(w_norm), _p(Z), float(delta), _p(out),
+                                    out.stride(0), _stream(stream))
 
 
 def qerl_read_status(workspace, stream=None) -> int:

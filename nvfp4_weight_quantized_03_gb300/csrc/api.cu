@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" entry points declared in include/qerl.h: argument
 // validation on the host, workspace layout, and the kernel launches.
+#include <cmath>
 #include <cstdint>
 
 #include "qerl_internal.h"
@@ -217,6 +218,79 @@ qerl_status qerl_lora_linear_group(const void* x, int64_t m, int64_t k, int64_t 
   a.workspace = workspace;
   a.ws_bytes = ws_bytes;
   return qerl::launch_lora_linear(a, as_stream(stream));
+}
+
+qerl_status qerl_lora_linear_group_rowz(const void* x, int64_t m, int64_t k, int64_t ldx, const float* z, int64_t ldz,
+                                        const qerl_linear_desc* linears, int count, void* workspace, size_t ws_bytes,
+                                        void* stream) {
+  qerl::LinearArgs a{};
+  bool empty = false;
+  qerl_status st = qerl::prepare_linear_group(x, m, k, ldx, z, linears, count, &a, &empty);
+  if (st != QERL_OK || empty) return st;
+  if (z != nullptr && ldz != 0) {
+    if (ldz < k) return QERL_ERR_INVALID_ARGUMENT;
+    if (ldz % 4 != 0) return QERL_ERR_MISALIGNED;  // every row 16-byte aligned
+  }
+  int ranks[4] = {0, 0, 0, 0};
+  for (int i = 0; i < a.nlin; ++i) ranks[i] = a.lin[i].r;
+  st = check_ws(workspace, ws_bytes, qerl::linear_workspace_bytes(m, k, ranks, a.nlin));
+  if (st != QERL_OK) return st;
+  a.ldz = z != nullptr ? ldz : 0;
+  a.workspace = workspace;
+  a.ws_bytes = ws_bytes;
+  return qerl::launch_lora_linear(a, as_stream(stream));
+}
+
+size_t qerl_rmsnorm_lora_linear_group_workspace_size(int64_t m, int64_t k, const qerl_linear_desc* linears,
+                                                     int count) {
+  if (m < 0 || k < 0 || count < 1 || count > 4 || linears == nullptr) return 0;
+  int ranks[4] = {0, 0, 0, 0};
+  for (int i = 0; i < count; ++i) ranks[i] = linears[i].r > 0 && linears[i].A != nullptr ? linears[i].r : 0;
+  return qerl::linear_workspace_bytes(m, k, ranks, count, true);
+}
+
+namespace {
+qerl_status check_rmsnorm_args(int64_t m, int64_t k, const void* w_norm, const float* Z, double delta) {
+  if (!(delta >= 0.0) || !std::isfinite(delta)) return QERL_ERR_INVALID_ARGUMENT;
+  if (m > 65535) return QERL_ERR_UNSUPPORTED_SHAPE;  // one CTA per row on the grid's y axis
+  if (k % 8 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (m > 0 && k > 0 && w_norm == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(w_norm, 16) || (Z != nullptr && !aligned(Z, 16))) return QERL_ERR_MISALIGNED;
+  return QERL_OK;
+}
+}  // namespace
+
+qerl_status qerl_rmsnorm_lora_linear_group(const void* h, int64_t m, int64_t k, int64_t ldh, const void* w_norm,
+                                           const float* Z, double delta, const qerl_linear_desc* linears, int count,
+                                           void* workspace, size_t ws_bytes, void* stream) {
+  qerl::LinearArgs a{};
+  bool empty = false;
+  qerl_status st = qerl::prepare_linear_group(h, m, k, ldh, nullptr, linears, count, &a, &empty);
+  if (st != QERL_OK || empty) return st;
+  if ((st = check_rmsnorm_args(m, k, w_norm, Z, delta)) != QERL_OK) return st;
+  int ranks[4] = {0, 0, 0, 0};
+  for (int i = 0; i < a.nlin; ++i) ranks[i] = a.lin[i].r;
+  st = check_ws(workspace, ws_bytes, qerl::linear_workspace_bytes(m, k, ranks, a.nlin, true));
+  if (st != QERL_OK) return st;
+  a.rmsnorm = true;
+  a.w_norm = w_norm;
+  a.Zn = Z;
+  a.delta = delta;
+  a.workspace = workspace;
+  a.ws_bytes = ws_bytes;
+  return qerl::launch_lora_linear(a, as_stream(stream));
+}
+
+qerl_status qerl_rmsnorm_noise(const void* h, int64_t m, int64_t k, int64_t ldh, const void* w_norm, const float* Z,
+                               double delta, void* out, int64_t ldo, void* stream) {
+  if (m < 0 || k < 0 || ldh < k || ldo < k) return QERL_ERR_INVALID_ARGUMENT;
+  qerl_status st = check_rmsnorm_args(m, k, w_norm, Z, delta);
+  if (st != QERL_OK) return st;
+  if (m == 0 || k == 0) return QERL_OK;
+  if (h == nullptr || out == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(h, 16) || !aligned(out, 16) || ldh % 8 != 0 || ldo % 8 != 0) return QERL_ERR_MISALIGNED;
+  if (k > INT32_MAX) return QERL_ERR_UNSUPPORTED_SHAPE;
+  return qerl::launch_rmsnorm_noise(h, m, k, ldh, w_norm, Z, delta, out, ldo, as_stream(stream));
 }
 
 qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, const uint8_t* wpacked,

@@ -76,14 +76,26 @@ constexpr int kLoraTileR = 32;   // ranks per LoRA tile
 constexpr int kLoraKc = 64;      // K per shared-memory chunk
 constexpr int kLoraPad = 68;     // padded row length (floats): conflict-free float4 reads
 constexpr int kLoraStages = 3;   // chunks in flight (cp.async ring)
-// One ring stage: x [16][64] bf16, A [32][64] bf16, z [64] fp32.
-constexpr int kLoraStageBytes = (kLoraTileM + kLoraTileR) * kLoraKc * 2 + kLoraKc * 4;
+// One ring stage: x [16][64] bf16, A [32][64] bf16, z [16][64] fp32 (one
+// row of it when the noise is shared by all rows).
+constexpr int kLoraStageBytes = (kLoraTileM + kLoraTileR) * kLoraKc * 2 + kLoraTileM * kLoraKc * 4;
 constexpr int kLoraSmemBytes = kLoraStages * kLoraStageBytes + (kLoraTileM + kLoraTileR) * kLoraPad * 4;
 constexpr int kPrepMaxCluster = 8;
 
 struct PrepParams {
   const __nv_bfloat16* x;
   const float* z;
+  int64_t ldz;  // noise row stride: 0 = one vector z[K] for every row, else row m uses z + m * ldz
+  // RMSNorm with merged noise (row tasks; "Noise Merging", Eq. 10-11): x holds
+  // h, and x~ = bf16((w_norm + Zn) * (h / sqrt(mean(h^2) + delta))) in fp64
+  // with one rounding.  xt_out (row stride ldo) receives x~ when not null;
+  // the staged copy (xs) is skipped when xs is null.
+  const __nv_bfloat16* w_norm;
+  const float* Zn;
+  double delta;
+  __nv_bfloat16* xt_out;
+  int64_t ldo;
+  int rmsnorm;
   const __nv_bfloat16* A[kMaxLinears];  // [r][K] per linear (LoRA down-projections)
   int r[kMaxLinears];
   float* t[kMaxLinears];   // [groups][M][r] partial sums of x~ . A^T over K group g, per linear
@@ -151,6 +163,16 @@ __host__ inline LoraSplit lora_split(int64_t m, int64_t k, const int* ranks, int
   return L;
 }
 
+// fp64 -> bf16, round to nearest even, one rounding: the value is first
+// rounded to fp32 toward zero with the inexact bit kept in the last place
+// (round to odd; fp32 carries 16 more bits than bf16, so the final rounding
+// sees the exact tie/half-way situation), then rounded to bf16.
+__device__ __forceinline__ __nv_bfloat16 f64_to_bf16_rn(double v) {
+  float f = __double2float_rz(v);
+  if (static_cast<double>(f) != v && isfinite(f)) f = __uint_as_float(__float_as_uint(f) | 1u);
+  return __float2bfloat16_rn(f);
+}
+
 __device__ __forceinline__ float noisy(float xv, float zv) {
   // bf16_RN( x * (1 + z) ): one fp32 add, one fp32 multiply, one rounding.
   return __bfloat162float(__float2bfloat16_rn(__fmul_rn(xv, __fadd_rn(1.0f, zv))));
@@ -180,10 +202,59 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     __nv_bfloat16* xt = reinterpret_cast<__nv_bfloat16*>(sm);
     const uint4* xrow = reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(m) * p.ldx);
     unsigned amax = 0;
+    const int nv = p.K / 8;
+    if (p.rmsnorm) {
+      // x~ = (w + Z) * (h / sqrt(mean(h^2) + delta)), fp64, one rounding to
+      // bf16 (the op order of the definition; the mean's summation order is
+      // the only difference from a sequential sum: ~1e-16 relative).
+      __shared__ double red_d[kPrepThreads / 32];
+      double ss = 0.0;
+      for (int v = tid; v < nv; v += kPrepThreads) {
+        const uint4 raw = __ldg(xrow + v);
+        reinterpret_cast<uint4*>(xt)[v] = raw;
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const double hv = static_cast<double>(__bfloat162float(e[j]));
+          ss = fma(hv, hv, ss);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+      if ((tid & 31) == 0) red_d[tid >> 5] = ss;
+      __syncthreads();
+      double tot = 0.0;
+#pragma unroll
+      for (int i = 0; i < kPrepThreads / 32; ++i) tot += red_d[i];
+      const double denom = sqrt(tot / static_cast<double>(p.K) + p.delta);
+      const uint4* w4 = reinterpret_cast<const uint4*>(p.w_norm);
+      const float4* Z4 = reinterpret_cast<const float4*>(p.Zn);
+      __nv_bfloat16* orow = p.xt_out != nullptr ? p.xt_out + static_cast<int64_t>(m) * p.ldo : nullptr;
+      for (int v = tid; v < nv; v += kPrepThreads) {
+        uint4 raw = reinterpret_cast<const uint4*>(xt)[v];
+        const uint4 wr = __ldg(w4 + v);
+        float zz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (p.Zn != nullptr) {
+          const float4 za = __ldg(Z4 + 2 * v), zb = __ldg(Z4 + 2 * v + 1);
+          zz[0] = za.x; zz[1] = za.y; zz[2] = za.z; zz[3] = za.w;
+          zz[4] = zb.x; zz[5] = zb.y; zz[6] = zb.z; zz[7] = zb.w;
+        }
+        __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&raw);
+        const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wr);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const double wn = static_cast<double>(__bfloat162float(we[j])) + static_cast<double>(zz[j]);
+          e[j] = f64_to_bf16_rn(wn * (static_cast<double>(__bfloat162float(e[j])) / denom));
+          amax = max(amax, static_cast<unsigned>(__bfloat16_as_ushort(e[j]) & 0x7FFFu));
+        }
+        reinterpret_cast<uint4*>(xt)[v] = raw;
+        if (orow != nullptr) reinterpret_cast<uint4*>(orow)[v] = raw;
+      }
+      if (p.xs == nullptr) return;  // the normalisation step alone
+    } else {
     // Four vectors per thread per round: their loads are all in flight
     // before the first is used.
-    const int nv = p.K / 8;
-    const float4* z4 = reinterpret_cast<const float4*>(p.z);
+    const float4* z4 = reinterpret_cast<const float4*>(p.z != nullptr ? p.z + m * p.ldz : nullptr);
     for (int v0 = tid; v0 < nv; v0 += 4 * kPrepThreads) {
       uint4 raw[4];
       float4 za[4], zb[4];
@@ -213,6 +284,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
         for (int j = 0; j < 8; ++j) amax = max(amax, static_cast<unsigned>(__bfloat16_as_ushort(e[j]) & 0x7FFFu));
         reinterpret_cast<uint4*>(xt)[v] = raw[u];
       }
+    }
     }
     amax = __reduce_max_sync(0xFFFFFFFFu, amax);
     __shared__ unsigned red[kPrepThreads / 32];
@@ -284,7 +356,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   auto issue_chunk = [&](int kc, int st) {
     const uint32_t base = ring + st * kLoraStageBytes;
     const int k0 = kc * kLoraKc;
-    constexpr int kXv = kLoraTileM * kLoraKc / 8, kAv = kLoraTileR * kLoraKc / 8, kZv = kLoraKc / 4;
+    constexpr int kXv = kLoraTileM * kLoraKc / 8, kAv = kLoraTileR * kLoraKc / 8;
+    const int kZv = (p.ldz > 0 ? kLoraTileM : 1) * kLoraKc / 4;  // z rows staged
     for (int v = tid; v < kXv + kAv + kZv; v += kPrepThreads) {
       if (v < kXv) {
         const int rr = v >> 3, c = v & 7;
@@ -296,9 +369,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
         cp_async_16(base + v * 16, in ? Am + static_cast<int64_t>(rank0 + jj) * p.K + k0 + c * 8 : Am,
                     in ? 16u : 0u);
       } else {
-        const int c = v - kXv - kAv;
-        cp_async_16(base + v * 16, p.z != nullptr ? p.z + k0 + c * 4 : reinterpret_cast<const float*>(p.x),
-                    p.z != nullptr ? 16u : 0u);
+        const int c = v - kXv - kAv;                          // 16 per z row
+        const int zr = c >> 4, zc = c & 15;
+        const bool in = p.z != nullptr && (p.ldz == 0 || row0 + zr < p.M);
+        cp_async_16(base + v * 16, in ? p.z + (row0 + zr) * p.ldz + k0 + zc * 4 : reinterpret_cast<const float*>(p.x),
+                    in ? 16u : 0u);
       }
     }
   };
@@ -317,10 +392,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
       for (int i = tid; i < kLoraTileM * kLoraKc / 4; i += kPrepThreads) {
         const int rr = i >> 4, k4 = (i & 15) * 4;  // 16 rows x 64 k, four per item
         float4 f;
-        f.x = noisy(__bfloat162float(xr[rr * kLoraKc + k4]), zr[k4]);
-        f.y = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 1]), zr[k4 + 1]);
-        f.z = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 2]), zr[k4 + 2]);
-        f.w = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 3]), zr[k4 + 3]);
+        const float* zrow = zr + (p.ldz > 0 ? rr * kLoraKc : 0);
+        f.x = noisy(__bfloat162float(xr[rr * kLoraKc + k4]), zrow[k4]);
+        f.y = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 1]), zrow[k4 + 1]);
+        f.z = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 2]), zrow[k4 + 2]);
+        f.w = noisy(__bfloat162float(xr[rr * kLoraKc + k4 + 3]), zrow[k4 + 3]);
         *reinterpret_cast<float4*>(xsm + rr * kLoraPad + k4) = f;
       }
       for (int i = tid; i < kLoraTileR * kLoraKc / 8; i += kPrepThreads) {
@@ -1632,14 +1708,14 @@ int resident_clusters(int sp) {
 }
 
 struct LinearLayout {
-  size_t xs, rinv, t[kMaxLinears], tf[kMaxLinears], count, total;
+  size_t xs, rinv, t[kMaxLinears], tf[kMaxLinears], count, xt, total;
 };
 
 // Token tiles of up to 128 rows stage x~ in the tiled layout (one tile of
 // round_up(m, 16) rows); larger m keeps the row-major [m][k] layout.
 inline int tiled_rows_for(int64_t m) { return m <= 128 ? static_cast<int>((m + 15) / 16 * 16) : 0; }
 
-LinearLayout linear_layout(int64_t m, int64_t k, const int* ranks, int nlin) {
+LinearLayout linear_layout(int64_t m, int64_t k, const int* ranks, int nlin, bool rmsnorm) {
   LinearLayout L;
   // Fixed offset, whatever the shape: the LoRA tiles' completion counters,
   // zero between calls (each is reset by the cluster that finishes its tile).
@@ -1658,14 +1734,51 @@ LinearLayout linear_layout(int64_t m, int64_t k, const int* ranks, int nlin) {
     L.tf[i] = off;
     off = align_up(off + static_cast<size_t>(m) * r * 4, 256);
   }
+  // RMSNorm mode with a LoRA branch: the normalised x~ (bf16 [m][k]) for the
+  // LoRA down-projection.
+  L.xt = off;
+  bool lora = false;
+  for (int i = 0; i < nlin; ++i) lora = lora || ranks[i] > 0;
+  if (rmsnorm && lora) off = align_up(off + static_cast<size_t>(m) * k * 2, 256);
   L.total = off;
   return L;
 }
 
 }  // namespace
 
-size_t linear_workspace_bytes(int64_t m, int64_t k, const int* ranks, int nlin) {
-  return linear_layout(m, k, ranks, nlin).total;
+size_t linear_workspace_bytes(int64_t m, int64_t k, const int* ranks, int nlin, bool rmsnorm) {
+  return linear_layout(m, k, ranks, nlin, rmsnorm).total;
+}
+
+qerl_status launch_rmsnorm_noise(const void* h, int64_t m, int64_t k, int64_t ldh, const void* w_norm, const float* Zn,
+                                 double delta, void* out, int64_t ldo, cudaStream_t s) {
+  if (m == 0 || k == 0) return QERL_OK;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit - 1024);
+  });
+  if (err != cudaSuccess) return QERL_ERR_CUDA;
+  if (k * 2 > kSmemLimit - 1024) return QERL_ERR_UNSUPPORTED_SHAPE;
+  PrepParams q{};
+  q.x = static_cast<const __nv_bfloat16*>(h);
+  q.ldx = ldh;
+  q.M = static_cast<int>(m);
+  q.K = static_cast<int>(k);
+  q.rmsnorm = 1;
+  q.w_norm = static_cast<const __nv_bfloat16*>(w_norm);
+  q.Zn = Zn;
+  q.delta = delta;
+  q.xt_out = static_cast<__nv_bfloat16*>(out);
+  q.ldo = ldo;
+  q.cluster = 1;
+  q.row_groups = static_cast<int>(m);
+  cudaLaunchConfig_t pc{};
+  pc.gridDim = dim3(1, static_cast<unsigned>(m), 1);
+  pc.blockDim = dim3(kPrepThreads, 1, 1);
+  pc.dynamicSmemBytes = static_cast<size_t>(k) * 2;
+  pc.stream = s;
+  return cudaLaunchKernelEx(&pc, prep_kernel, q) == cudaSuccess ? QERL_OK : QERL_ERR_CUDA;
 }
 
 qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
@@ -1717,7 +1830,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   for (int i = 0; i < nlin; ++i) tile_begin[i + 1] = tile_begin[i] + (pair ? (tiles[i] + 1) / 2 : tiles[i]);
   const bool lora = r > 0;
   const int n_tiles = tile_begin[nlin];  // grid-y units
-  const LinearLayout WL = linear_layout(a.m, a.k, ranks, nlin);
+  const LinearLayout WL = linear_layout(a.m, a.k, ranks, nlin, a.rmsnorm);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   int* status = reinterpret_cast<int*>(ws);
   __half* xs = reinterpret_cast<__half*>(ws + WL.xs);
@@ -1894,6 +2007,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   PrepParams pp{};
   pp.x = static_cast<const __nv_bfloat16*>(a.x);
   pp.z = a.z;
+  pp.ldz = a.z != nullptr ? a.ldz : 0;
   pp.xs = xs;
   pp.rinv = rinv;
   pp.ldx = a.ldx;
@@ -1917,24 +2031,52 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   pp.lora_tiles = pp.tile_begin[kMaxLinears];
   pp.tile_count = reinterpret_cast<unsigned*>(ws + WL.count);
   pp.sum_groups = lora_sum_in_prep(M) ? 1 : 0;
-  const int lora_ctas_y = pp.lora_tiles * pp.groups;
   size_t prep_smem = static_cast<size_t>(K) * 2;  // row tasks stage the row
   if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>(kLoraSmemBytes));
   if (prep_smem > static_cast<size_t>(kPrepSmemLimit)) return QERL_ERR_UNSUPPORTED_SHAPE;
-  {
+  auto launch_prep = [&](const PrepParams& q, int row_groups, int lora_ctas_y, int cluster) {
     cudaLaunchConfig_t pc{};
-    pc.gridDim = dim3(static_cast<unsigned>(pp.cluster), static_cast<unsigned>(pp.row_groups + lora_ctas_y), 1);
+    pc.gridDim = dim3(static_cast<unsigned>(cluster), static_cast<unsigned>(row_groups + lora_ctas_y), 1);
     pc.blockDim = dim3(kPrepThreads, 1, 1);
     pc.dynamicSmemBytes = prep_smem;
     pc.stream = s;
     cudaLaunchAttribute pa[1];
     pa[0].id = cudaLaunchAttributeClusterDimension;
-    pa[0].val.clusterDim.x = static_cast<unsigned>(pp.cluster);
+    pa[0].val.clusterDim.x = static_cast<unsigned>(cluster);
     pa[0].val.clusterDim.y = 1;
     pa[0].val.clusterDim.z = 1;
     pc.attrs = pa;
     pc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&pc, prep_kernel, pp) != cudaSuccess) return QERL_ERR_CUDA;
+    return cudaLaunchKernelEx(&pc, prep_kernel, q) == cudaSuccess;
+  };
+  if (a.rmsnorm) {
+    // RMSNorm with merged noise: the row tasks normalise h into x~ (staged for
+    // the MMA kernel, and written out for the LoRA down-projection), then a
+    // second launch runs the LoRA tiles on that x~ with no further noise.
+    PrepParams rq = pp;
+    rq.rmsnorm = 1;
+    rq.w_norm = static_cast<const __nv_bfloat16*>(a.w_norm);
+    rq.Zn = a.Zn;
+    rq.delta = a.delta;
+    rq.xt_out = lora ? reinterpret_cast<__nv_bfloat16*>(ws + WL.xt) : nullptr;
+    rq.ldo = K;
+    rq.z = nullptr;
+    rq.ldz = 0;
+    rq.cluster = 1;
+    rq.row_groups = std::max(M, pp.tiled_rows);
+    rq.lora_tiles = 0;
+    if (!launch_prep(rq, rq.row_groups, 0, 1)) return QERL_ERR_CUDA;
+    if (lora) {
+      PrepParams lq = pp;
+      lq.x = rq.xt_out;
+      lq.ldx = K;
+      lq.z = nullptr;
+      lq.ldz = 0;
+      lq.row_groups = 0;
+      if (!launch_prep(lq, 0, pp.lora_tiles * pp.groups, pp.cluster)) return QERL_ERR_CUDA;
+    }
+  } else if (!launch_prep(pp, pp.row_groups, pp.lora_tiles * pp.groups, pp.cluster)) {
+    return QERL_ERR_CUDA;
   }
 
   MmaParams mp{};

@@ -49,12 +49,22 @@ struct LinearArgs {  // up to 4 linears sharing x, z and k
   const void* x;
   int64_t m, k, ldx;
   const float* z;
+  int64_t ldz;  // noise row stride: 0 = one vector for every row
+  // RMSNorm with merged noise in front of the linears (x holds h): x~ =
+  // bf16((w_norm + Zn) * h / sqrt(mean(h^2) + delta)); z is then unused.
+  bool rmsnorm;
+  const void* w_norm;
+  const float* Zn;
+  double delta;
   LinearDesc lin[4];
   int nlin;
   void* workspace;
   size_t ws_bytes;
 };
-size_t linear_workspace_bytes(int64_t m, int64_t k, const int* ranks, int nlin);
+size_t linear_workspace_bytes(int64_t m, int64_t k, const int* ranks, int nlin, bool rmsnorm = false);
+// The normalisation step alone: out [m][ldo] bf16 (linear.cu).
+qerl_status launch_rmsnorm_noise(const void* h, int64_t m, int64_t k, int64_t ldh, const void* w_norm, const float* Zn,
+                                 double delta, void* out, int64_t ldo, cudaStream_t s);
 
 // api.cu: the argument checks shared by every linear entry point.
 qerl_status prepare_linear_group(const void* x, int64_t m, int64_t k, int64_t ldx, const float* z,

@@ -248,3 +248,36 @@ def test_header_is_plain_c_and_cpp(lang, std):
             r = subprocess.run([cc, "-fsyntax-only", "-x", lang, std, "-Wall", "-Wextra", "-pedantic", "-Werror",
                                 os.path.join(ROOT, "include", fn)], capture_output=True, text=True)
             assert r.returncode == 0, r.stderr
+
+
+@no_gpu_only
+def test_rowz_and_rmsnorm_validation(L):
+    """Argument checks of the per-row-noise and RMSNorm entry points (no device work)."""
+    E = q.STATUS_NAMES
+    arr = (q.LinearDesc * 1)(_desc())
+    rowz = lambda z, ldz: L.qerl_lora_linear_group_rowz(0x1000, 4, 128, 128, z, ldz, arr, 1, 0x10000, 1 << 30, None)
+    assert E[rowz(0x8000, 64)] == "QERL_ERR_INVALID_ARGUMENT"      # a row stride shorter than a row
+    assert E[rowz(0x8000, 130)] == "QERL_ERR_MISALIGNED"           # rows not 16-byte aligned
+    assert E[rowz(0x8004, 0)] == "QERL_ERR_MISALIGNED"
+    rms = lambda **kw: L.qerl_rmsnorm_lora_linear_group(
+        kw.get("h", 0x1000), kw.get("m", 4), 128, 128, kw.get("w", 0x3000), kw.get("Z", None),
+        kw.get("delta", 1e-6), arr, 1, 0x10000, kw.get("wsb", 1 << 30), None)
+    assert E[rms(delta=-1.0)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[rms(delta=float("nan"))] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[rms(w=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[rms(w=0x3008)] == "QERL_ERR_MISALIGNED"
+    assert E[rms(Z=0x3004)] == "QERL_ERR_MISALIGNED"
+    assert E[rms(m=70000)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    need = L.qerl_rmsnorm_lora_linear_group_workspace_size(4, 128, arr, 1)
+    assert E[rms(wsb=need - 1)] == "QERL_ERR_WORKSPACE"
+    # with a LoRA branch the workspace also holds the normalised activations
+    arr2 = (q.LinearDesc * 1)(_desc(A=0x6000, B=0x7000, r=16))
+    assert (L.qerl_rmsnorm_lora_linear_group_workspace_size(4, 128, arr2, 1)
+            >= L.qerl_lora_linear_group_workspace_size(4, 128, arr2, 1) + 4 * 128 * 2)
+    norm = lambda **kw: L.qerl_rmsnorm_noise(kw.get("h", 0x1000), 4, kw.get("k", 128), kw.get("ldh", 128), 0x3000,
+                                             None, 1e-6, kw.get("out", 0x5000), kw.get("ldo", 128), None)
+    assert E[norm(k=124)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[norm(ldh=100)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[norm(out=0x5008)] == "QERL_ERR_MISALIGNED"
+    assert E[norm(ldo=132)] == "QERL_ERR_MISALIGNED"
+    assert E[norm(out=None)] == "QERL_ERR_INVALID_ARGUMENT"
