@@ -111,6 +111,15 @@ QERL_API qerl_status qerl_nvfp4_quantize_with_scale(const void* W, int w_dtype, 
 QERL_API qerl_status qerl_nvfp4_amax(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w, float* amax,
                             void* workspace, size_t ws_bytes, void* stream);
 
+/* The tensor scale of a weight from its amax: S = amax / 2688 in fp32 (S = 1
+ * if that is 0), the rule qerl_nvfp4_quantize applies.  amax and tensor_scale
+ * are device floats.  For a weight sharded across devices (a column- or
+ * row-parallel linear): each shard's qerl_nvfp4_amax, an all-reduce(max) of
+ * those, this call, then qerl_nvfp4_quantize_with_scale on every shard gives
+ * codes and scales bit-identical to quantizing the whole tensor.  A negative
+ * or non-finite amax gives S = NaN (which _with_scale then rejects). */
+QERL_API qerl_status qerl_nvfp4_tensor_scale(const float* amax, float* tensor_scale, void* stream);
+
 /* ========================================================================
  * Packed weights for the linear (a layout of the same codes and scales; no
  * counterpart in the paper, which fixes the format, not its byte order).

@@ -126,6 +126,8 @@ def lib():
             L.qerl_lora_linear_group.restype = ctypes.c_int
             L.qerl_lora_linear_group.argtypes = [_vp, _i64, _i64, _i64, _vp, ctypes.POINTER(LinearDesc), ctypes.c_int,
                                                  _vp, ctypes.c_size_t, _vp]
+            L.qerl_nvfp4_tensor_scale.restype = ctypes.c_int
+            L.qerl_nvfp4_tensor_scale.argtypes = [_vp, _vp, _vp]
             L.qerl_lora_linear_group_rowz.restype = ctypes.c_int
             L.qerl_lora_linear_group_rowz.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, ctypes.POINTER(LinearDesc),
                                                       ctypes.c_int, _vp, ctypes.c_size_t, _vp]
@@ -207,6 +209,21 @@ def qerl_nvfp4_amax(W, amax, workspace, stream=None) -> int:
     n, k = W.shape
     return lib().qerl_nvfp4_amax(_p(W), _wdtype(W), n, k, W.stride(0), _p(amax), _p(workspace),
                                  _nbytes(workspace), _stream(stream))
+
+
+def qerl_nvfp4_tensor_scale(amax, tensor_scale, stream=None) -> int:
+    return lib().qerl_nvfp4_tensor_scale(_p(amax), _p(tensor_scale), _stream(stream))
+
+
+def global_amax(amax, group=None):
+    """All-reduce(max) of a shard's amax (a one-element float tensor, in place) over the
+    process group: with it, qerl_nvfp4_tensor_scale and qerl_nvfp4_quantize_with_scale give
+    every shard the codes and scales of the whole tensor.  Plain torch.distributed
+    plumbing (any backend: gloo for CPU tensors, NCCL for device tensors)."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.all_reduce(amax, op=dist.ReduceOp.MAX, group=group)
+    return amax
 
 
 def qerl_aqn_sigma(stage: int, num_stages: int, sigma_start: float = 1e-2, sigma_end: float = 5e-4) -> float:

@@ -36,18 +36,26 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+# A test-only variant (QERL_TEST_HOOKS: settable wait limit and a barrier
+# arrival that never comes), loaded only by the failure-detection test.
+LIB_TEST_HOOKS = os.path.join(HERE, "libqerl_testhooks.so")
+
+
+def build(force: bool = False, verbose: bool = False, test_hooks: bool = False) -> str:
     nvcc = nvcc_path()
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD + ("_hooks" if test_hooks else "")
+    lib_out = LIB_TEST_HOOKS if test_hooks else LIB
+    extra = ["-DQERL_TEST_HOOKS"] if test_hooks else []
+    os.makedirs(build_dir, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS]
     jobs = []
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s, *hdrs]):
-            jobs.append([nvcc, *GENCODE, *NVCC_FLAGS, "-c", s, "-o", o])
+            jobs.append([nvcc, *GENCODE, *NVCC_FLAGS, *extra, "-c", s, "-o", o])
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
             results = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), jobs))
@@ -56,15 +64,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
                 sys.stderr.write(res.stdout + res.stderr)
             if res.returncode != 0:
                 raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib_out, objs):
+        tmp = lib_out + f".tmp{os.getpid()}"
         cmd = [nvcc, *GENCODE, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lpthread", "-lrt"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             sys.stderr.write(res.stdout + res.stderr)
             raise RuntimeError("link failed")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_out)
+    return lib_out
 
 
 if __name__ == "__main__":

@@ -166,6 +166,11 @@ qerl_status qerl_nvfp4_quantize_with_scale(const void* W, int w_dtype, int64_t n
                              &hdr->status, as_stream(stream));
 }
 
+qerl_status qerl_nvfp4_tensor_scale(const float* amax, float* tensor_scale, void* stream) {
+  if (amax == nullptr || tensor_scale == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  return qerl::launch_tensor_scale(amax, tensor_scale, as_stream(stream));
+}
+
 qerl_status qerl_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, uint32_t stream_id, uint64_t counter,
                             void* stream) {
   if (k < 0) return QERL_ERR_INVALID_ARGUMENT;

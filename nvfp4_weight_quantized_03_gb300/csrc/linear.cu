@@ -820,7 +820,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // B^T TMA (expect_tx) + the warps that build the t tiles: the eight
     // dequant warps, or in pair mode the six issuer warps without a tile.
     mbar_init_a(lora_full, p.pair ? 1 + kPairLoraWarps : 9);
+#ifdef QERL_TEST_HOOKS
+    mbar_init_a(acc_full, n_iss + (g_test_extra_arrival ? 1 : 0));
+#else
     mbar_init_a(acc_full, n_iss);
+#endif
     mbar_init_a(t_full, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -2143,3 +2147,16 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
 }
 
 }  // namespace qerl
+
+#ifdef QERL_TEST_HOOKS
+// Test-only entry point of the hooks build: the bounded waits' limit in clock
+// cycles, and whether the accumulator barrier gets an arrival that never comes
+// (the epilogue's wait then runs out after every MMA and copy has completed).
+extern "C" __attribute__((visibility("default"))) int qerl_test_set_hooks(long long wait_limit_cycles,
+                                                                         int extra_arrival) {
+  if (cudaMemcpyToSymbol(qerl::g_test_wait_limit, &wait_limit_cycles, sizeof(wait_limit_cycles)) != cudaSuccess)
+    return 1;
+  if (cudaMemcpyToSymbol(qerl::g_test_extra_arrival, &extra_arrival, sizeof(extra_arrival)) != cudaSuccess) return 1;
+  return 0;
+}
+#endif

@@ -22,6 +22,7 @@ qerl_status launch_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_
                           const unsigned* amax_bits, const float* s_in, float* s_out, uint8_t* codes,
                           uint8_t* scales, int* status, cudaStream_t s);
 qerl_status launch_amax_to_float(const unsigned* amax_bits, float* amax, cudaStream_t s);
+qerl_status launch_tensor_scale(const float* amax, float* S, cudaStream_t s);
 
 // Packed weights for the linear (quantize.cu): 128 rows x 256 K per block.
 constexpr size_t kPackedBlockBytes = 16384 + 2048;

@@ -33,6 +33,16 @@ __device__ __forceinline__ void fence_mbarrier_init() {
 // GB300 clocks): they record QERL_ERR_TIMEOUT (5), raise the CTA's abort flag
 // so its other roles stop waiting, and return false.  Never trap.
 constexpr long long kWaitLimitCycles = 4000000000ll;
+#ifdef QERL_TEST_HOOKS
+// Test-only build (never the shipped library): the wait limit and one extra,
+// never-arriving count on a chosen barrier are set from the host, so a test
+// can make a bounded wait run out (see qerl_test_set_hooks in linear.cu).
+static __device__ long long g_test_wait_limit = kWaitLimitCycles;
+static __device__ int g_test_extra_arrival = 0;  // 1: the accumulator barrier expects one more arrival
+#define QERL_WAIT_LIMIT g_test_wait_limit
+#else
+#define QERL_WAIT_LIMIT kWaitLimitCycles
+#endif
 
 // u32 shared-address forms (the hot loops keep every shared access in the
 // shared state space; a generic pointer would cost a generic load/store).
@@ -107,7 +117,7 @@ __device__ __forceinline__ bool mbar_wait_a(uint32_t bar, uint32_t parity, volat
 #endif
     if ((i & (QERL_WAIT_HINT_NS > 0 ? 15u : 1023u)) == 0) {
       if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > QERL_WAIT_LIMIT) {
         *abort_flag = 1;
         record_error(status, 5);
         return false;

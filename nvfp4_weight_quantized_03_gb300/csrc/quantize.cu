@@ -143,6 +143,19 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(const uint8_t* __restr
 
 __global__ void amax_to_float_kernel(const unsigned* amax_bits, float* amax) { *amax = __uint_as_float(*amax_bits); }
 
+// S from an amax the caller combined (e.g. the max over the shards of a
+// tensor): the rule of the quantizer's own prologue, bit for bit.
+__global__ void tensor_scale_kernel(const float* amax, float* S) {
+  const float a = *amax;
+  if (!(a >= 0.0f) || !isfinite(a)) {
+    *S = __uint_as_float(0x7FC00000u);
+    return;
+  }
+  float s = __fdiv_rn(a, 2688.0f);  // amax / (6 * 448)
+  if (s == 0.0f) s = 1.0f;
+  *S = s;
+}
+
 int grid_for_rows(int64_t n) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -214,6 +227,11 @@ qerl_status launch_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_
   encode_kernel<<<grid_for_rows(n > 0 ? n : 1), kThreads, 0, s>>>(static_cast<const uint8_t*>(W), n, k,
                                                                    ld_w * esz, bf16, amax_bits, s_in, s_out,
                                                                    codes, scales, status);
+  return cuda_status(cudaGetLastError());
+}
+
+qerl_status launch_tensor_scale(const float* amax, float* S, cudaStream_t s) {
+  tensor_scale_kernel<<<1, 1, 0, s>>>(amax, S);
   return cuda_status(cudaGetLastError());
 }
 

@@ -245,3 +245,51 @@ def test_linear_group_full_wave_two_members(q, orc):
     assert q.qerl_read_status(ws) == 0
     for c, y in zip(cases, ys):
         assert_linear_close(y, c.oracle(orc), orc, what=f"wave group n{c.n}")
+
+
+GUARD = 4096
+GUARD_BYTE = 0xA5
+
+
+def _guarded(nbytes):
+    """A device byte buffer of nbytes followed by GUARD bytes of a pattern."""
+    buf = torch.full((nbytes + GUARD,), GUARD_BYTE, dtype=torch.uint8, device="cuda")
+    return buf
+
+
+def _guard_intact(buf, nbytes):
+    return bool((buf[nbytes:] == GUARD_BYTE).all().item())
+
+
+@pytest.mark.parametrize("m,n,k,r", [(8, 384, 1024, 32), (100, 384, 2048, 32), (300, 256, 576, 16)])
+def test_no_writes_past_the_buffers(q, orc, m, n, k, r):
+    """Guard regions after y, the workspace and the packed weights stay untouched by the
+    quantizer, the packer and the linear (decode, pair and prefill paths; ragged N)."""
+    W = wl.weight_f32(n, k, 91, 0)
+    codes, scales, S = q.quantize(torch.from_numpy(W).cuda())
+    pbytes = q.qerl_nvfp4_packed_size(n, k)
+    pbuf = _guarded(pbytes)
+    q.check(q.qerl_nvfp4_pack(codes, scales, pbuf[:pbytes]))
+    torch.cuda.synchronize()
+    assert _guard_intact(pbuf, pbytes), "pack wrote past the packed weights"
+    x = dev_bf16(wl.activations_bits(m, k, 92, 1))
+    A, B = dev_bf16(wl.lora_A_bits(r, k, 93, 2)), dev_bf16(wl.lora_B_bits(n, r, 94, 3))
+    zd = torch.from_numpy(wl.noise_vector(k, 1e-2, 95)).cuda()
+    wsb = q.qerl_lora_linear_workspace_size(m, n, k, r)
+    wsb = (wsb + 255) // 256 * 256
+    wbuf = _guarded(wsb)
+    wbuf[:wsb].zero_()
+    ybytes = m * n * 2
+    ybuf = _guarded(ybytes)
+    y = ybuf[:ybytes].view(torch.bfloat16).view(m, n)
+    for _ in range(2):
+        q.check(q.qerl_lora_linear(x, pbuf[:pbytes], S, zd, A, B, 2.0 * r, y, wbuf[:wsb]))
+    assert q.qerl_read_status(wbuf[:wsb]) == 0
+    assert _guard_intact(ybuf, ybytes), "the linear wrote past y"
+    assert _guard_intact(wbuf, wsb), "the linear wrote past its workspace"
+    assert _guard_intact(pbuf, pbytes), "the linear wrote into the packed weights' guard"
+    rows = None if m <= 128 else np.arange(0, m, 9)
+    ref = orc.lora_linear(wl.activations_bits(m, k, 92, 1) if rows is None else wl.activations_bits(m, k, 92, 1)[rows],
+                          *orc.quantize(W), z=wl.noise_vector(k, 1e-2, 95), A_bits=wl.lora_A_bits(r, k, 93, 2),
+                          B_bits=wl.lora_B_bits(n, r, 94, 3), alpha=2.0 * r)
+    assert_linear_close(y if rows is None else y[torch.from_numpy(rows).cuda()], ref, orc, what="guarded")
