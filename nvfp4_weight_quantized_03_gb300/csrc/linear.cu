@@ -144,10 +144,10 @@ __host__ inline int lora_tile_count(int64_t m, const int* ranks, int nlin) {
     if (ranks[i] > 0) tiles += ((m + kLoraTileM - 1) / kLoraTileM) * ((ranks[i] + kLoraTileR - 1) / kLoraTileR);
   return static_cast<int>(std::min<int64_t>(tiles, INT32_MAX));
 }
-// Pair-mode token tiles (65..128 rows) have the prep kernel sum the groups;
-// other tiles stage every group's partial sums and add them, so their group
-// count is bounded by that staging buffer (256 / n_tok groups).
-__host__ inline bool lora_sum_in_prep(int64_t m) { return m > 64 && m <= 128; }
+// Above 64 tokens (pair-mode-sized tiles, prefill) the prep kernel sums the
+// groups; smaller tiles stage every group's partial sums and add them, so
+// their group count is bounded by that staging buffer (256 / n_tok groups).
+__host__ inline bool lora_sum_in_prep(int64_t m) { return m > 64; }
 __host__ inline LoraSplit lora_split(int64_t m, int64_t k, const int* ranks, int nlin) {
   const int kc_total = static_cast<int>(k / kLoraKc);
   LoraSplit L;
@@ -549,6 +549,7 @@ struct MmaParams {
   // tensor-memory A slots are handed over per MMA stage (one per tile and
   // stage of the weight stage), the LoRA operands are built in the idle ring.
   int pair;
+  int xs_rowmajor;  // x~ staged as [M][K] (more than 128 tokens: several token tiles), read by 2-D TMA
 };
 
 // The LoRA up-projection's B matrices, one TMA map per linear of the launch.
@@ -834,7 +835,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWeightWarp && lane == 0) {
-    if (!kTmemA) tma_prefetch_desc(&tm_xs);
+    if (!kTmemA || p.xs_rowmajor) tma_prefetch_desc(&tm_xs);
     if (L.r > 0) tma_prefetch_desc(tm_bl);
   }
   tc_fence_before();
@@ -940,14 +941,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // and empty barrier, so a slot is refilled as soon as the MMAs that
         // read it are done -- the copy of the next slabs overlaps the MMAs of
         // the current ones.
+        // One token tile (up to 128 tokens): the slabs are contiguous in the
+        // tiled layout (one bulk copy each); several token tiles read [M][K]
+        // through the 2-D tensor map (rows past M are zero-filled).
         const uint32_t slab = static_cast<uint32_t>(p.n_tok) * 128u;
         const uint8_t* src = reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(mma_begin) * slab;
+        const bool rowmajor = p.xs_rowmajor != 0;
         int sb = 0;
         uint32_t bph = 0;
         for (int j = 0; j < nmma; ++j) {
           if (!mbar_wait_a(b_empty(sb), bph ^ 1, abort_flag, p.status)) break;
           mbar_arrive_expect_tx_a(b_full(sb), slab);
-          bulk_load(sbase + p.off_b + sb * slab, src + static_cast<int64_t>(j) * slab, slab, b_full(sb));
+          if (rowmajor)
+            tma_load_2d(sbase + p.off_b + sb * slab, &tm_xs, (mma_begin + j) * kStageK, m0, b_full(sb));
+          else
+            bulk_load(sbase + p.off_b + sb * slab, src + static_cast<int64_t>(j) * slab, slab, b_full(sb));
           if (++sb == BS) {
             sb = 0;
             bph ^= 1;
@@ -1463,6 +1471,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (c + e < p.n_tok)
               stsf(part + 4u * (tile_out + static_cast<uint32_t>((c + e) * kTileN + nl)), ok ? w[e] * sc[e] : 0.0f);
+        } else if (p.stage_out) {
+          // staged [tile][token][128 rows], stored below as 16-byte vectors
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (c + e >= p.n_tok) break;
+            const uint32_t el = tile_out + static_cast<uint32_t>((c + e) * kTileN + nl);
+            const float val = ok ? w[e] * sc[e] : 0.0f;
+            if (L.y_f32)
+              stsf(sbase + 4u * el, val);
+            else
+              sts16(sbase + 2u * el, __bfloat16_as_ushort(__float2bfloat16_rn(val)));
+          }
         } else if (n < L.N) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
@@ -1470,6 +1490,40 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
       }
     }
+    // One accumulator (one issuer, e.g. 256-token tiles): 32 token columns
+    // per TMEM load and wait.  Several: 8 columns of up to four of them per
+    // wait.  The row scales arrive as vectors (one shared-memory load per
+    // four values, not one per value).
+    auto emit = [&](int c, int e, float val) {
+      const uint32_t el = tile_out + static_cast<uint32_t>((c + e) * kTileN + nl);
+      if (p.split > 1)
+        stsf(part + 4u * el, val);
+      else if (!p.stage_out) {
+        if (m0 + c + e < p.M && n < L.N) store_out(L, m0 + c + e, n, val);
+      } else if (L.y_f32) {
+        stsf(sbase + 4u * el, val);  // staged: [tile][token][128 rows]
+      } else {
+        sts16(sbase + 2u * el, __bfloat16_as_ushort(__float2bfloat16_rn(val)));
+      }
+    };
+    if (!p.pair && nacc == 1 && cols % 32 == 0) {
+      for (int c = c0; c < c0 + cols; c += 32) {
+        float w[32];
+        tmem_ld_x32(tmem_base + acc0 + lane_off + c, w);
+        float sc[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 s4 = lds128f(smv + 4u * (c + e));
+          sc[e] = s4.x;
+          sc[e + 1] = s4.y;
+          sc[e + 2] = s4.z;
+          sc[e + 3] = s4.w;
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) emit(c, e, ok ? w[e] * sc[e] : 0.0f);
+      }
+    } else {
     for (int c = c0; !p.pair && c < c0 + cols; c += 8) {
       float v[8];
       // Four accumulators' columns per wait (issuer 0's holds the LoRA term).
@@ -1489,36 +1543,32 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           v[e] = t;
         }
       }
+      const float4 s0 = lds128f(smv + 4u * c), s1 = lds128f(smv + 4u * (c + 4));
+      const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float out = ok ? v[e] * ldsf(smv + 4u * (c + e)) : 0.0f;
-        const uint32_t el = tile_out + static_cast<uint32_t>((c + e) * kTileN + nl);
-        if (p.split > 1)
-          stsf(part + 4u * el, out);
-        else if (!p.stage_out) {
-          if (m0 + c + e < p.M && n < L.N) store_out(L, m0 + c + e, n, out);
-        } else if (L.y_f32) {
-          stsf(sbase + 4u * el, out);  // staged: [tile][token][128 rows]
-        } else {
-          sts16(sbase + 2u * el, __bfloat16_as_ushort(__float2bfloat16_rn(out)));
-        }
-      }
+      for (int e = 0; e < 8; ++e) emit(c, e, ok ? v[e] * sc[e] : 0.0f);
     }
-    if (p.split == 1 && p.stage_out && !p.pair) {
+    }
+    if (p.split == 1 && p.stage_out) {
       // The output tile leaves shared memory (the idle ring) a token row at a
       // time: one bulk copy per row when rows are 16-byte aligned (the writes
       // drain after the CTA has moved on), else 16-byte vectors.
       fence_proxy_async_smem();  // the staged tile is read by bulk copies below
       named_barrier_sync(1, 256);
       const int rows = min(p.n_tok, p.M - m0);
-      const int nvalid = min(kTileN, L.N - n0);
       const int es = L.y_f32 ? 4 : 2;
       uint8_t* ybase = reinterpret_cast<uint8_t*>(L.y);
       const bool vec = (reinterpret_cast<uintptr_t>(ybase) & 15u) == 0 && (static_cast<int64_t>(L.N) * es) % 16 == 0;
-      if (vec && (nvalid * es) % 16 == 0) {
+      for (int t = 0; t < ntl_e; ++t) {
+      const int n0t = n0 + t * kTileN;
+      const int nvalid = min(kTileN, L.N - n0t);
+      const uint32_t stile = sbase + static_cast<uint32_t>(t * p.n_tok * kTileN * es);
+      // (Bulk copies are processed one after another: many token rows go out
+      // as coalesced vector stores instead.)
+      if (vec && (nvalid * es) % 16 == 0 && p.n_tok <= 64) {
         if (dt < rows) {
-          bulk_store(ybase + (static_cast<int64_t>(m0 + dt) * L.N + n0) * es,
-                     sbase + static_cast<uint32_t>(dt * kTileN * es), static_cast<uint32_t>(nvalid * es));
+          bulk_store(ybase + (static_cast<int64_t>(m0 + dt) * L.N + n0t) * es,
+                     stile + static_cast<uint32_t>(dt * kTileN * es), static_cast<uint32_t>(nvalid * es));
           bulk_commit_group();
           bulk_wait_group_read0();
         }
@@ -1526,19 +1576,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const int chunks = vec ? nvalid * es / 16 : 0;  // whole 16-byte chunks per token row
         for (int it = dt; it < rows * chunks; it += 256) {
           const int ml = it / chunks, ch = it - ml * chunks;
-          const uint4 val = lds128(sbase + static_cast<uint32_t>(ml * kTileN * es + ch * 16));
-          *reinterpret_cast<uint4*>(ybase + (static_cast<int64_t>(m0 + ml) * L.N + n0) * es + ch * 16) = val;
+          const uint4 val = lds128(stile + static_cast<uint32_t>(ml * kTileN * es + ch * 16));
+          *reinterpret_cast<uint4*>(ybase + (static_cast<int64_t>(m0 + ml) * L.N + n0t) * es + ch * 16) = val;
         }
         const int e0 = chunks * 16 / es;  // the rest element by element
         const int rest = nvalid - e0;
         for (int it = dt; it < rows * rest; it += 256) {
           const int ml = it / rest, nn = e0 + (it - ml * rest);
-          const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0 + nn;
+          const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0t + nn;
           if (L.y_f32)
-            reinterpret_cast<float*>(ybase)[gi] = ldsf(sbase + 4u * (ml * kTileN + nn));
+            reinterpret_cast<float*>(ybase)[gi] = ldsf(stile + 4u * (ml * kTileN + nn));
           else
-            reinterpret_cast<uint16_t*>(ybase)[gi] = lds16(sbase + 2u * (ml * kTileN + nn));
+            reinterpret_cast<uint16_t*>(ybase)[gi] = lds16(stile + 2u * (ml * kTileN + nn));
         }
+      }
       }
     }
   }
@@ -1789,9 +1840,14 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   const int M = static_cast<int>(a.m), K = static_cast<int>(a.k);
   const int nlin = a.nlin;
   if (nlin < 1 || nlin > kMaxLinears) return QERL_ERR_INVALID_ARGUMENT;
-  // Token tiles: one of round_up(M, 16) rows up to 256 tokens, else 256-row tiles.
-  const int n_tok = M <= 256 ? (M + 15) / 16 * 16 : 256;
-  const int m_tiles = M <= 256 ? 1 : (M + 255) / 256;
+  // Token tiles: one of round_up(M, 16) rows up to 128 tokens, else 128-row
+  // tiles (prefill: in pair mode each CTA's activation slab then serves 256
+  // weight rows; a 256-token tile of one weight tile would need 1.5x the
+  // activation bytes per MAC, and activation ingress into an SM is what
+  // bounds these tiles).
+  const int n_tok = M <= 128 ? (M + 15) / 16 * 16 : 128;
+  const int m_tiles = M <= 128 ? 1 : (M + 127) / 128;
+  const bool xs_rowmajor = M > 128;
   const int raw_total = (K + kRawK - 1) / kRawK;
   int ranks[kMaxLinears] = {0, 0, 0, 0};
   int tiles[kMaxLinears] = {0, 0, 0, 0};
@@ -1809,7 +1865,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // as many clusters as can be resident at once (clusters live inside one
   // GPC, so e.g. 7-CTA clusters leave SMs unused).
   auto best_split = [&](int units) {
-    if (n_tok > 128) return 1;
+    if (m_tiles > 1) return 1;  // several token tiles fill the GPU without a K split
     int sp_best = 1;
     double best = 1e30;
     for (int sp = 1; sp <= kMaxSplit && sp <= raw_total; ++sp) {
@@ -1872,15 +1928,16 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   int lora_early = (r > 0 && n_tok <= 128) ? 1 : 0;
   const uint32_t part_bytes = split > 1 ? static_cast<uint32_t>(tpc * n_tok) * kTileN * 4u : 0u;
   const uint32_t b_stage = static_cast<uint32_t>(n_tok) * 128u;
-  // Decode-sized tiles (<= 128 tokens) keep the dequantized weights in tensor
-  // memory and spread MMA issue over several threads; 256-token tiles stage
-  // the weights in shared memory (their accumulators fill tensor memory).
-  const bool tmem_a = n_tok <= 128;
+  // The dequantized weights go to tensor memory as the MMA's A operand at
+  // every tile size: 256-token tiles (prefill) keep one 256-column
+  // accumulator and a two-weight-stage A ring beside it, with one MMA issuer
+  // (an N = 256 MMA outlasts its issue cost).
+  const bool tmem_a = true;
   // Each MMA occupies its issuing thread for ~150 cycles whatever the token
   // count, so small tiles take more issuers (each with its own accumulator,
   // which tensor memory must hold next to the A ring).
   // Pair mode: one issuer per tile.
-  const int issuers = !tmem_a ? 1 : (n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2));
+  const int issuers = n_tok > 128 ? 1 : (n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2));
   const uint32_t col_a = static_cast<uint32_t>(align_up(issuers * n_tok, 32));
   int ab_cap = kMaxAB;
   if (tmem_a) {
@@ -1946,8 +2003,11 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     } else {
       // Pair mode: each slab waits for both tiles' MMAs before it is
       // refilled, so two weight stages of activations come first.
-      const int rs_pref = pair ? 2 : 4;
-      for (int bs = 2 * kSub; bs >= kSub; bs -= kSub) {
+      // One issuer (256-token tiles) consumes every slab itself, so any ring
+      // depth keeps slot ownership fixed; otherwise multiples of kSub.
+      const int rs_pref = pair || issuers == 1 ? 2 : 4;
+      const int bs_step = issuers == 1 ? 1 : kSub;
+      for (int bs = 2 * kSub; bs >= kSub; bs -= bs_step) {
         const int rs = max_rs(bs);
         if (rs >= 2 && (best_rs == 0 || std::min(rs, rs_pref) > std::min(best_rs, rs_pref))) {
           best_rs = rs;
@@ -1981,7 +2041,8 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   }
   if (raw_stages < 2 || ab_stages < (tmem_a ? kSub : std::max(2, issuers))) return QERL_ERR_UNSUPPORTED_SHAPE;
   // A weight stage is handed over (and its activations loaded) at once.
-  if (tmem_a && (ab_stages < 2 * kSub || ab_stages % kSub != 0 || b_stages < kSub || b_stages % kSub != 0 ||
+  if (tmem_a && (ab_stages < 2 * kSub || ab_stages % kSub != 0 || b_stages < kSub ||
+                 (issuers > 1 && b_stages % kSub != 0) ||
                  (!pair && raw_stages % 2 != 0) || (kSub * 4) % issuers != 0 || (!coupled && issuers > kSub) ||
                  (pair && (issuers != 2 || ab_stages != 2 * kSub))))
     return QERL_ERR_UNSUPPORTED_SHAPE;
@@ -1990,7 +2051,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // x~: tiled layout moved by bulk copies with kTmemA; the 256-token tiles
   // read [M][K] through a 2D tensor map.
   CUtensorMap tm_xs;
-  if (tmem_a) {
+  if (!xs_rowmajor) {
     std::memset(&tm_xs, 0, sizeof(tm_xs));
   } else if (!make_map_2d(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xs, static_cast<uint64_t>(K),
                           static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2, kStageK,
@@ -2020,7 +2081,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   const LoraSplit ls = lora_split(M, K, ranks, nlin);
   pp.cluster = lora ? ls.cluster : 1;
   pp.groups = lora ? ls.groups : 0;
-  pp.tiled_rows = tmem_a ? n_tok : 0;
+  pp.tiled_rows = xs_rowmajor ? 0 : n_tok;
   pp.row_groups = (std::max(M, pp.tiled_rows) + pp.cluster - 1) / pp.cluster;
   pp.lora_m_tiles = (M + kLoraTileM - 1) / kLoraTileM;
   pp.tile_begin[0] = 0;
@@ -2123,6 +2184,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.wave = (split == 1 && !pair) ? sms : 0;
   mp.stage_out = static_cast<uint32_t>(tpc * n_tok) * kTileN * 4u <= P.lora ? 1 : 0;
   mp.pair = pair ? 1 : 0;
+  mp.xs_rowmajor = xs_rowmajor ? 1 : 0;
 
   const uint32_t smem_bytes = P.total;
 
