@@ -95,6 +95,10 @@ def lib():
             L.orc_lora_linear.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p, ctypes.c_float, _i64,
                                           _f32p, _i64, _u16p, _u16p, ctypes.c_int, ctypes.c_float,
                                           ctypes.c_int, _i64p, _i64, _f64p]
+            L.orc_mxfp4_lora_linear.restype = ctypes.c_int
+            L.orc_mxfp4_lora_linear.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p, _i64,
+                                                _f32p, _i64, _u16p, _u16p, ctypes.c_int, ctypes.c_float,
+                                                ctypes.c_int, _i64p, _i64, _f64p]
             _lib = L
     return _lib
 
@@ -304,12 +308,22 @@ def lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alph
     A_bits [r, k] uint16 bf16; B_bits [n, r] uint16 bf16
     (the shapes of Eq. 2: A in R^{r x k}, B in R^{d x r}).
     """
+    return _linear(False, x_bits, codes, scales, S, z, A_bits, B_bits, alpha, round_xt, cols)
+
+
+def mxfp4_lora_linear(x_bits, codes, scales, z=None, A_bits=None, B_bits=None, alpha=0.0,
+                      round_xt=True, cols=None) -> np.ndarray:
+    """The same linear over an MXFP4 weight: codes [n, k/2], E8M0 scales [n, k/32]."""
+    return _linear(True, x_bits, codes, scales, 1.0, z, A_bits, B_bits, alpha, round_xt, cols)
+
+
+def _linear(mx, x_bits, codes, scales, S, z, A_bits, B_bits, alpha, round_xt, cols):
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scales = np.ascontiguousarray(scales, dtype=np.uint8)
     m, k = x_bits.shape
     n = codes.shape[0]
-    assert codes.shape == (n, k // 2) and scales.shape == (n, k // 16)
+    assert codes.shape == (n, k // 2) and scales.shape == (n, k // (32 if mx else 16))
     r = 0
     if A_bits is not None and B_bits is not None:
         A_bits = np.ascontiguousarray(A_bits, dtype=np.uint16)
@@ -325,8 +339,12 @@ def lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alph
         cols_arr = np.ascontiguousarray(cols, dtype=np.int64)
         ncols = cols_arr.size
     y = np.empty((m, ncols), dtype=np.float64)
-    _check(lib().orc_lora_linear(_ptr(x_bits, _u16p), m, k, k, _ptr(codes, _u8p), _ptr(scales, _u8p),
-                                 float(S), n, _ptr(zz, _f32p), ldz, _ptr(A_bits, _u16p), _ptr(B_bits, _u16p),
-                                 r, float(alpha), 1 if round_xt else 0, _ptr(cols_arr, _i64p), ncols,
-                                 _ptr(y, _f64p)))
+    rest = (_ptr(zz, _f32p), ldz, _ptr(A_bits, _u16p), _ptr(B_bits, _u16p), r, float(alpha),
+            1 if round_xt else 0, _ptr(cols_arr, _i64p), ncols, _ptr(y, _f64p))
+    if mx:
+        _check(lib().orc_mxfp4_lora_linear(_ptr(x_bits, _u16p), m, k, k, _ptr(codes, _u8p), _ptr(scales, _u8p),
+                                           n, *rest))
+    else:
+        _check(lib().orc_lora_linear(_ptr(x_bits, _u16p), m, k, k, _ptr(codes, _u8p), _ptr(scales, _u8p),
+                                     float(S), n, *rest))
     return y

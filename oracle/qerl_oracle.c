@@ -480,10 +480,35 @@ void orc_rmsnorm_noise(const uint16_t* h, int64_t m, int64_t k, int64_t ldh, con
 /* Output columns are the ncols indices in cols[] (all n if cols == NULL).   */
 /* A or B NULL, or r == 0: no LoRA term.                                     */
 /* ------------------------------------------------------------------------ */
-int orc_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
-                    const uint8_t* codes, const uint8_t* scales, float S, int64_t n,
-                    const float* z, int64_t ldz, const uint16_t* A, const uint16_t* B, int r, float alpha,
-                    int round_xt, const int64_t* cols, int64_t ncols, double* y)
+/* One dequantized weight row c (k values) of a 4-bit format, for the linear. */
+typedef void (*orc_row_dequant)(const uint8_t* codes, const uint8_t* scales, float S, int64_t k, int64_t c,
+                                double* wrow);
+
+/* Eq. 6: W_hat[c][j] = S * dec_E4M3(scale[c][j/16]) * e2m1(code[c][j]). */
+static void nvfp4_row(const uint8_t* codes, const uint8_t* scales, float S, int64_t k, int64_t c, double* wrow)
+{
+    for (int64_t kk = 0; kk < k; ++kk) {
+        uint8_t byte = codes[c * (k / 2) + kk / 2];
+        uint8_t code = (kk & 1) ? (byte >> 4) : (byte & 0xF);
+        wrow[kk] = (double)S * (orc_e4m3_decode(scales[c * (k / 16) + kk / 16]) * orc_e2m1_decode(code));
+    }
+}
+
+/* MXFP4: W_hat[c][j] = dec_E8M0(scale[c][j/32]) * e2m1(code[c][j]) (no tensor scale). */
+static void mxfp4_row(const uint8_t* codes, const uint8_t* scales, float S, int64_t k, int64_t c, double* wrow)
+{
+    (void)S;
+    for (int64_t kk = 0; kk < k; ++kk) {
+        uint8_t byte = codes[c * (k / 2) + kk / 2];
+        uint8_t code = (kk & 1) ? (byte >> 4) : (byte & 0xF);
+        wrow[kk] = orc_e8m0_decode(scales[c * (k / 32) + kk / 32]) * orc_e2m1_decode(code);
+    }
+}
+
+static int lora_linear_core(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
+                            const uint8_t* codes, const uint8_t* scales, float S, orc_row_dequant deq, int64_t n,
+                            const float* z, int64_t ldz, const uint16_t* A, const uint16_t* B, int r, float alpha,
+                            int round_xt, const int64_t* cols, int64_t ncols, double* y)
 {
     if (m < 0 || k < 0 || n < 0 || ldx < k || r < 0 || ldz < 0) return ORC_ERR_ARG;
     if (k % 32 != 0) return ORC_ERR_SHAPE;
@@ -517,11 +542,7 @@ int orc_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
     for (int64_t ci = 0; ci < ncols; ++ci) {
         int64_t c = cols ? cols[ci] : ci;
         if (c < 0 || c >= n) { free(xt); free(t); free(wrow); return ORC_ERR_ARG; }
-        for (int64_t kk = 0; kk < k; ++kk) {
-            uint8_t byte = codes[c * (k / 2) + kk / 2];
-            uint8_t code = (kk & 1) ? (byte >> 4) : (byte & 0xF);
-            wrow[kk] = (double)S * (orc_e4m3_decode(scales[c * (k / 16) + kk / 16]) * orc_e2m1_decode(code));
-        }
+        deq(codes, scales, S, k, c, wrow);
         for (int64_t i = 0; i < m; ++i) {
             double acc = 0.0;
             for (int64_t kk = 0; kk < k; ++kk) acc += xt[i * k + kk] * wrow[kk];
@@ -535,6 +556,27 @@ int orc_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
     }
     free(xt); free(t); free(wrow);
     return ORC_OK;
+}
+
+int orc_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
+                    const uint8_t* codes, const uint8_t* scales, float S, int64_t n,
+                    const float* z, int64_t ldz, const uint16_t* A, const uint16_t* B, int r, float alpha,
+                    int round_xt, const int64_t* cols, int64_t ncols, double* y)
+{
+    return lora_linear_core(x, m, k, ldx, codes, scales, S, nvfp4_row, n, z, ldz, A, B, r, alpha, round_xt,
+                            cols, ncols, y);
+}
+
+/* The same linear over an MXFP4 weight (codes [n][k/2], E8M0 scales        */
+/* [n][k/32], as orc_mxfp4_quantize writes them): the format variant of the */
+/* digest's 4-bit format comparison, with every other step unchanged.       */
+int orc_mxfp4_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
+                          const uint8_t* codes, const uint8_t* scales, int64_t n,
+                          const float* z, int64_t ldz, const uint16_t* A, const uint16_t* B, int r, float alpha,
+                          int round_xt, const int64_t* cols, int64_t ncols, double* y)
+{
+    return lora_linear_core(x, m, k, ldx, codes, scales, 1.0f, mxfp4_row, n, z, ldz, A, B, r, alpha, round_xt,
+                            cols, ncols, y);
 }
 
 /* ------------------------------------------------------------------------ */

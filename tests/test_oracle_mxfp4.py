@@ -99,3 +99,48 @@ def test_zero_block_and_bad_input(orc):
         orc.mxfp4_quantize(W)
     with pytest.raises(Exception):
         orc.mxfp4_quantize(np.ones((1, 48), np.float32))
+
+
+# ---- the MXFP4 linear (orc_mxfp4_lora_linear) --------------------------------------------
+
+def _mx_weights(orc, n, k, seed):
+    W = wl.weight_f32(n, k, seed, 0)
+    return orc.mxfp4_quantize(W)
+
+
+def test_mx_linear_is_the_plain_matmul_of_the_dequantized_weight(orc):
+    """No noise, no LoRA: y = x . W_hat^T with W_hat from the MXFP4 decoder, checked against a
+    numpy fp64 matmul (only the summation order differs)."""
+    m, n, k = 5, 96, 256
+    codes, scales = _mx_weights(orc, n, k, 201)
+    x_bits = wl.activations_bits(m, k, 202, 1)
+    x = (x_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = x @ orc.mxfp4_dequant(codes, scales).T
+    got = orc.mxfp4_lora_linear(x_bits, codes, scales)
+    assert np.max(np.abs(got - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_mx_linear_equals_the_nvfp4_linear_on_a_shared_weight(orc):
+    """An NVFP4 weight whose tensor scale and block scales are powers of two, equal over each pair of
+    16-blocks, is also an MXFP4 weight (E8M0 code = log2(S * dec(s)) + 127).  Both oracle linears
+    must then agree bit for bit, noise, per-row noise, LoRA and column subsets included (this pins
+    the 32-block scale index and the absence of a tensor scale in the MXFP4 row decoder)."""
+    rng = np.random.default_rng(203)
+    m, n, k, r = 6, 40, 192, 8
+    codes = rng.integers(0, 256, size=(n, k // 2), dtype=np.uint8)
+    exps = rng.integers(-9, 9, size=(n, k // 32))                      # E4M3 holds 2^-9 .. 2^8 exactly
+    e4m3 = np.where(exps >= -6, (exps + 7) << 3, 1 << (exps + 9)).astype(np.uint8)
+    nv_scales = np.repeat(e4m3, 2, axis=1)
+    assert all(orc.e4m3_decode(int(e4m3[i, j])) == 2.0 ** int(exps[i, j]) for i in range(n) for j in range(k // 32))
+    S_exp = -3
+    mx_scales = (exps + S_exp + 127).astype(np.uint8)
+    x_bits = wl.activations_bits(m, k, 204, 1)
+    z = (rng.standard_normal((m, k)) * 1e-2).astype(np.float32)
+    A_bits, B_bits = wl.lora_A_bits(r, k, 205, 2), wl.lora_B_bits(n, r, 206, 3)
+    cols = np.array([0, 3, 17, 39, 5])
+    for zz in (None, z[0], z):
+        nv = orc.lora_linear(x_bits, codes, nv_scales, 2.0 ** S_exp, z=zz, A_bits=A_bits, B_bits=B_bits,
+                             alpha=16.0, cols=cols)
+        mx = orc.mxfp4_lora_linear(x_bits, codes, mx_scales, z=zz, A_bits=A_bits, B_bits=B_bits, alpha=16.0,
+                                   cols=cols)
+        assert np.array_equal(nv, mx)
