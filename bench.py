@@ -78,7 +78,7 @@ ARM_PARTS = {(0x41, 0xD0C): "Neoverse-N1", (0x41, 0xD40): "Neoverse-V1", (0x41, 
              (0x41, 0xD4F): "Neoverse-V2", (0x41, 0xD8E): "Neoverse-N3", (0x41, 0xD84): "Neoverse-V3"}
 
 
-EXTRAS = ("prefill", "quantize", "qproj", "sustained", "32b")
+EXTRAS = ("prefill", "quantize", "qproj", "sustained", "32b", "mxfp4")
 
 
 def host_cpu_model():
@@ -185,13 +185,17 @@ class ClockSampler:
 class QLinear:
     """One NVFP4-quantized linear with its LoRA adapters (device)."""
 
-    def __init__(self, q, lin, seed, *path, r=RANK_R, w_dtype=torch.float32):
+    def __init__(self, q, lin, seed, *path, r=RANK_R, w_dtype=torch.float32, fmt="nvfp4"):
         W = wl.weight_f32_device(lin.n, lin.k, seed, *path)
         if w_dtype == torch.bfloat16:
             W = W.to(torch.bfloat16)
         self.lin = lin
-        codes, scales, self.S = q.quantize(W)
-        self.wp = q.pack(codes, scales)
+        if fmt == "mxfp4":
+            codes, scales = q.mxfp4_quantize(W)
+            self.wp, self.S = q.mxfp4_pack(codes, scales)
+        else:
+            codes, scales, self.S = q.quantize(W)
+            self.wp = q.pack(codes, scales)
         del codes, scales
         del W
         self.A = wl.normal_bf16_device((r, lin.k), 1.0 / math.sqrt(lin.k), seed, *path, 2)
@@ -465,6 +469,7 @@ def bench_ours(args):
     extra_qproj = bench_qproj_3b(q, hbm_peak) if "qproj" in want else None
     extra_sustained = bench_sustained(q, hbm_peak, dev_index) if "sustained" in want else None
     extra_32b = bench_32b_stream(q, hbm_peak) if "32b" in want else None
+    extra_mx = bench_mxfp4(q, hbm_peak) if "mxfp4" in want else None
 
     # ---- the dominant launch, timed per call
     roofline = dominant_call(q, layers, acts, hbm_peak)
@@ -524,6 +529,8 @@ def bench_ours(args):
     if extra_32b:
         out["decode_32b_64layers_m16"] = extra_32b["decode"]
         out["quantize_32b_all"] = extra_32b["quantize"]
+    if extra_mx:
+        out["mxfp4"] = extra_mx
     if rank == 0 and not args.skip_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_oracle(seconds_budget=args.cpu_budget)
     if rank == 0:
@@ -646,6 +653,63 @@ def bench_quantize(q, hbm_peak):
            "bytes_note": "4.5625 B/weight: bf16 read twice (amax pass + encode pass) + 0.5625 B written; "
                          "single-pass lower bound 2.5625 B/weight"}
     del Ws, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+MXFP4_BYTES_PER_WEIGHT = 0.5 + 1.0 / 32  # E2M1 + one E8M0 per 32
+
+
+def bench_mxfp4(q, hbm_peak, ms=(8, 32)):
+    """The format variant: the 7B-shaped layer quantized to MXFP4 by the library (timed), packed,
+    then decode through the same grouped launches as the headline (graph replay, weights rotating
+    over N_COPIES layer copies).  GB/s on MXFP4's own bytes (0.53125 B/weight) and on the bytes the
+    kernels move (the packed layout keeps one scale byte per 16, 0.5625 B/weight)."""
+    shapes = wl.QWEN_7B
+    Ws = [wl.weight_f32_device(lin.n, lin.k, 5, 0, li).to(torch.bfloat16) for li, lin in enumerate(shapes)]
+    outs = [(torch.empty((lin.n, lin.k // 2), dtype=torch.uint8, device="cuda"),
+             torch.empty((lin.n, lin.k // 32), dtype=torch.uint8, device="cuda")) for lin in shapes]
+    ws = q.workspace(256)
+
+    def quant():
+        for W, (c, sc) in zip(Ws, outs):
+            q.check(q.qerl_mxfp4_quantize(W, c, sc, ws), "qerl_mxfp4_quantize")
+
+    quant()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        quant()
+    e1.record()
+    torch.cuda.synchronize()
+    tq = e0.elapsed_time(e1) / 5
+    q.check(q.qerl_read_status(ws), "mxfp4 quantize status")
+    nw = sum(lin.n * lin.k for lin in shapes)
+    res = {"workload": "Qwen2.5-7B-shaped layer in MXFP4 (E2M1 + E8M0 per 32), LoRA r=32, AQN",
+           "quantize": {"ms": round(tq, 4), "GBps": round(nw * (2 + MXFP4_BYTES_PER_WEIGHT) / (tq * 1e-3) / 1e9, 1),
+                        "bytes_note": "one pass: bf16 read + 0.53125 B/weight written"}}
+    del Ws, outs
+    layers = [[QLinear(q, lin, 5, c, li, fmt="mxfp4") for li, lin in enumerate(shapes)] for c in range(N_COPIES)]
+    mx_bytes = nw * MXFP4_BYTES_PER_WEIGHT
+    for m in ms:
+        act = Activations(q, shapes, m, 5)
+        q.check(q.qerl_aqn_sample(act.z_all, 1e-2, 5), "qerl_aqn_sample")
+
+        def step():
+            for c in range(N_COPIES):
+                run_substep(q, layers[c], act, 1e-2, c)
+
+        t_ms, _, pct = _graph_time_ms(step, 20)
+        q.check(q.qerl_read_status(act.ws), "mxfp4 decode status")
+        per_layer_us = t_ms * 1e3 / N_COPIES
+        res[f"decode_m{m}"] = {
+            "us_per_layer": round(per_layer_us, 2),
+            "GBps_mxfp4_bytes": round(mx_bytes / (per_layer_us * 1e-6) / 1e9, 1),
+            "GBps_packed_bytes": round(nw * BYTES_PER_WEIGHT / (per_layer_us * 1e-6) / 1e9, 1),
+            "frac_of_hbm_peak_packed": round(nw * BYTES_PER_WEIGHT / (per_layer_us * 1e-6) / 1e9 / hbm_peak, 4)}
+        del act
+    del layers
     torch.cuda.empty_cache()
     return res
 

@@ -57,7 +57,8 @@ typedef enum {
     QERL_ERR_CUDA = 4,              /* a CUDA runtime call failed (the CUDA error is not cleared) */
     QERL_ERR_TIMEOUT = 5,           /* a kernel's bounded wait expired (recorded in the status word) */
     QERL_ERR_NONFINITE = 6,         /* NaN or Inf in the weights (recorded in the status word) */
-    QERL_ERR_WORKSPACE = 7          /* workspace missing or smaller than the *_workspace_size() */
+    QERL_ERR_WORKSPACE = 7,         /* workspace missing or smaller than the *_workspace_size() */
+    QERL_ERR_RANGE = 8              /* a weight the packed layout cannot hold (MXFP4 scale span; status word) */
 } qerl_status;
 
 typedef enum { QERL_F32 = 0, QERL_BF16 = 1 } qerl_dtype;
@@ -145,6 +146,45 @@ QERL_API qerl_status qerl_nvfp4_tensor_scale(const float* amax, float* tensor_sc
 QERL_API size_t qerl_nvfp4_packed_size(int64_t n, int64_t k);
 QERL_API qerl_status qerl_nvfp4_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
                                      uint8_t* packed, void* stream);
+
+/* ========================================================================
+ * MXFP4, the 4-bit format the digest's "NVFP4 Quantization" section compares
+ * NVFP4 with: E2M1 elements with one shared E8M0 (power-of-two) scale per 32
+ * contiguous elements along K, no tensor scale.  The same linear kernels run
+ * it: qerl_mxfp4_pack writes the linear's packed layout plus a tensor scale,
+ * and qerl_lora_linear / _group take those exactly as for NVFP4.
+ *
+ * qerl_mxfp4_quantize: W [n][ld_w] f32 or bf16 (device, 16-byte aligned rows)
+ *   -> codes [n][k/2] (two per byte, even k in the low nibble; device,
+ *   16-byte aligned) and scales [n][k/32] (E8M0 codes, 127 = 2^0).  The
+ *   scale rule (the digest does not give one; the OCP MX rule):
+ *   e = floor(log2(amax_b)) - 2 clamped to [-127, 127], code e + 127, so the
+ *   block max lands in [4, 8) * 2^e and values above 6 * 2^e saturate; an
+ *   all-zero block gets code 0.  Elements: E2M1 of w / 2^e, round to nearest,
+ *   ties to the even code, saturating at 6, -0 written as 0.  workspace:
+ *   qerl_nvfp4_quantize_workspace_size() bytes, 256-byte aligned, zero-filled
+ *   before first use.  Requires k % 32 == 0, ld_w >= k.  A non-finite weight
+ *   records QERL_ERR_NONFINITE in the workspace status word (that block's
+ *   codes and scale are then not written).
+ *
+ * qerl_mxfp4_pack: codes and scales as above -> packed (the layout described
+ *   for qerl_nvfp4_pack, qerl_nvfp4_packed_size(n, k) bytes) and
+ *   *tensor_scale (device float).  The layout holds E4M3 block scales times
+ *   an fp32 tensor scale; an E8M0 scale 2^(e-127) is stored as
+ *   S = 2^(e_max - 135) (e_max: the largest code over blocks with a non-zero
+ *   element) times the E4M3 code of 2^(e - e_max + 8), exact for every block
+ *   scale down to 2^-17 of the largest (E4M3 holds 2^-9 .. 2^8 exactly).  A
+ *   non-zero block further below is packed as zeros and records
+ *   QERL_ERR_RANGE in the workspace status word.  An all-zero weight gives
+ *   S = 1.  Same shape rules and alignment as qerl_nvfp4_pack; scales need
+ *   no alignment.  workspace as for qerl_mxfp4_quantize.
+ * ======================================================================== */
+QERL_API qerl_status qerl_mxfp4_quantize(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w,
+                                         uint8_t* codes, uint8_t* scales, void* workspace, size_t ws_bytes,
+                                         void* stream);
+QERL_API qerl_status qerl_mxfp4_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
+                                     uint8_t* packed, float* tensor_scale, void* workspace, size_t ws_bytes,
+                                     void* stream);
 
 /* ========================================================================
  * AQN schedule ("Adaptive Quantization Noise", Eq. 8 and Algorithm 1).

@@ -61,7 +61,7 @@ QERL_F32, QERL_BF16 = 0, 1
 QERL_SCHEDULE_EXPONENTIAL, QERL_SCHEDULE_LINEAR, QERL_SCHEDULE_COSINE, QERL_SCHEDULE_LOGARITHMIC = 0, 1, 2, 3
 STATUS_NAMES = {0: "QERL_OK", 1: "QERL_ERR_INVALID_ARGUMENT", 2: "QERL_ERR_UNSUPPORTED_SHAPE",
                 3: "QERL_ERR_MISALIGNED", 4: "QERL_ERR_CUDA", 5: "QERL_ERR_TIMEOUT", 6: "QERL_ERR_NONFINITE",
-                7: "QERL_ERR_WORKSPACE"}
+                7: "QERL_ERR_WORKSPACE", 8: "QERL_ERR_RANGE"}
 
 _lib = None
 _lock = threading.Lock()
@@ -100,6 +100,11 @@ def lib():
             L.qerl_nvfp4_quantize_with_scale.restype = ctypes.c_int
             L.qerl_nvfp4_quantize_with_scale.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                                          ctypes.c_size_t, _vp]
+            L.qerl_mxfp4_quantize.restype = ctypes.c_int
+            L.qerl_mxfp4_quantize.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_size_t,
+                                              _vp]
+            L.qerl_mxfp4_pack.restype = ctypes.c_int
+            L.qerl_mxfp4_pack.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, ctypes.c_size_t, _vp]
             L.qerl_nvfp4_amax.restype = ctypes.c_int
             L.qerl_nvfp4_amax.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, ctypes.c_size_t, _vp]
             L.qerl_aqn_sigma.restype = ctypes.c_double
@@ -256,6 +261,22 @@ def qerl_nvfp4_pack(codes, scales, packed, stream=None) -> int:
     return lib().qerl_nvfp4_pack(_p(codes), _p(scales), n, k, _p(packed), _stream(stream))
 
 
+def qerl_mxfp4_quantize(W, codes, scales, workspace, stream=None) -> int:
+    """W [n, k] f32/bf16 -> codes [n, k/2], E8M0 scales [n, k/32] (uint8)."""
+    n, k = W.shape
+    return lib().qerl_mxfp4_quantize(_p(W), _wdtype(W), n, k, W.stride(0), _p(codes), _p(scales), _p(workspace),
+                                     _nbytes(workspace), _stream(stream))
+
+
+def qerl_mxfp4_pack(codes, scales, packed, tensor_scale, workspace, stream=None) -> int:
+    """codes [n, k/2], E8M0 scales [n, k/32] -> packed (qerl_nvfp4_packed_size(n, k) bytes) and the
+    power-of-two tensor scale the linear applies."""
+    n = codes.shape[0]
+    k = codes.shape[1] * 2
+    return lib().qerl_mxfp4_pack(_p(codes), _p(scales), n, k, _p(packed), _p(tensor_scale), _p(workspace),
+                                 _nbytes(workspace), _stream(stream))
+
+
 def qerl_lora_linear_workspace_size(m: int, n: int, k: int, r: int) -> int:
     return lib().qerl_lora_linear_workspace_size(int(m), int(n), int(k), int(r))
 
@@ -377,6 +398,26 @@ def pack(codes: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
     packed = torch.empty(qerl_nvfp4_packed_size(n, k), dtype=torch.uint8, device=codes.device)
     check(qerl_nvfp4_pack(codes, scales, packed), "qerl_nvfp4_pack")
     return packed
+
+
+def mxfp4_quantize(W: torch.Tensor, ws: torch.Tensor = None):
+    """MXFP4-quantize an n x k float32/bfloat16 CUDA tensor -> (codes, E8M0 scales)."""
+    n, k = W.shape
+    codes = torch.empty((n, k // 2), dtype=torch.uint8, device=W.device)
+    scales = torch.empty((n, k // 32), dtype=torch.uint8, device=W.device)
+    ws = workspace(qerl_nvfp4_quantize_workspace_size(), W.device) if ws is None else ws
+    check(qerl_mxfp4_quantize(W, codes, scales, ws), "qerl_mxfp4_quantize")
+    return codes, scales
+
+
+def mxfp4_pack(codes: torch.Tensor, scales: torch.Tensor, ws: torch.Tensor = None):
+    """Packed form of an MXFP4 weight for qerl_lora_linear -> (packed, tensor_scale)."""
+    n, k = codes.shape[0], codes.shape[1] * 2
+    packed = torch.empty(qerl_nvfp4_packed_size(n, k), dtype=torch.uint8, device=codes.device)
+    ts = torch.empty(1, dtype=torch.float32, device=codes.device)
+    ws = workspace(qerl_nvfp4_quantize_workspace_size(), codes.device) if ws is None else ws
+    check(qerl_mxfp4_pack(codes, scales, packed, ts, ws), "qerl_mxfp4_pack")
+    return packed, ts
 
 
 def lora_linear(x, wpacked, tensor_scale, n, z=None, A=None, B=None, alpha=0.0, out_dtype=torch.bfloat16,

@@ -112,6 +112,7 @@ const char* qerl_status_string(int status) {
     case QERL_ERR_TIMEOUT: return "QERL_ERR_TIMEOUT";
     case QERL_ERR_NONFINITE: return "QERL_ERR_NONFINITE";
     case QERL_ERR_WORKSPACE: return "QERL_ERR_WORKSPACE";
+    case QERL_ERR_RANGE: return "QERL_ERR_RANGE";
     default: return "QERL_ERR_UNKNOWN";
   }
 }
@@ -194,6 +195,35 @@ qerl_status qerl_nvfp4_pack(const uint8_t* codes, const uint8_t* scales, int64_t
   if (codes == nullptr || scales == nullptr || packed == nullptr) return QERL_ERR_INVALID_ARGUMENT;
   if (!aligned(codes, 16) || !aligned(scales, 4) || !aligned(packed, 16)) return QERL_ERR_MISALIGNED;
   return qerl::launch_pack(codes, scales, n, k, packed, as_stream(stream));
+}
+
+qerl_status qerl_mxfp4_quantize(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w, uint8_t* codes,
+                                uint8_t* scales, void* workspace, size_t ws_bytes, void* stream) {
+  qerl_status st = check_weight_args(W, w_dtype, n, k, ld_w);
+  if (st != QERL_OK) return st;
+  if (n > 0 && k > 0 && (codes == nullptr || scales == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(codes, 16)) return QERL_ERR_MISALIGNED;
+  if ((st = check_ws(workspace, ws_bytes, kWsHeaderBytes)) != QERL_OK) return st;
+  auto* hdr = static_cast<qerl::WsHeader*>(workspace);
+  return qerl::launch_mx_encode(W, w_dtype == QERL_BF16, n, k, ld_w, codes, scales, &hdr->status,
+                                as_stream(stream));
+}
+
+qerl_status qerl_mxfp4_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
+                            float* tensor_scale, void* workspace, size_t ws_bytes, void* stream) {
+  if (n < 0 || k < 0) return QERL_ERR_INVALID_ARGUMENT;
+  if (k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (n > INT32_MAX || k > 65536) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (tensor_scale == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (n > 0 && k > 0 && (codes == nullptr || scales == nullptr || packed == nullptr))
+    return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(codes, 16) || !aligned(packed, 16)) return QERL_ERR_MISALIGNED;
+  qerl_status st = check_ws(workspace, ws_bytes, kWsHeaderBytes);
+  if (st != QERL_OK) return st;
+  auto* hdr = static_cast<qerl::WsHeader*>(workspace);
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemsetAsync(&hdr->amax_bits, 0, sizeof(unsigned), s) != cudaSuccess) return QERL_ERR_CUDA;
+  return qerl::launch_mx_pack(codes, scales, n, k, packed, tensor_scale, &hdr->amax_bits, &hdr->status, s);
 }
 
 size_t qerl_lora_linear_workspace_size(int64_t m, int64_t n, int64_t k, int r) {

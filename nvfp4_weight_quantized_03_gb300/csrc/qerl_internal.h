@@ -29,6 +29,12 @@ constexpr size_t kPackedBlockBytes = 16384 + 2048;
 size_t packed_weight_bytes(int64_t n, int64_t k);
 qerl_status launch_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
                         cudaStream_t s);
+// MXFP4 (quantize.cu): the encoder, and the pack into the same layout with a
+// power-of-two tensor scale (emax1: a zeroed device word of the workspace).
+qerl_status launch_mx_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w, uint8_t* codes,
+                             uint8_t* scales, int* status, cudaStream_t s);
+qerl_status launch_mx_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
+                           float* tensor_scale, unsigned* emax1, int* status, cudaStream_t s);
 
 // aqn.cu
 qerl_status launch_aqn_sample(float* z, int64_t k, float sigma, uint64_t seed, uint32_t stream_id,

@@ -198,7 +198,166 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const uint8_t* __restric
   }
 }
 
+// ---------------------------------------------------------------------------
+// MXFP4 (the 4-bit format the digest's "NVFP4 Quantization" section compares
+// with): E2M1 elements and one E8M0 scale X = 2^e per 32 contiguous elements,
+// no tensor scale.  The digest does not fix the scale rule; this follows the
+// OCP MX one, e = floor(log2(amax_b)) - 2 clamped to [-127, 127] (2 is the
+// largest E2M1 exponent, so the block max lands in [4, 8) X and values above
+// 6 X saturate), code e + 127, an all-zero block code 0.  w / X is exact
+// (a power-of-two scaling; a result below 2^-126 encodes to 0 either way).
+// One thread per 32-element block; a warp covers consecutive blocks of a row.
+__global__ void __launch_bounds__(kThreads) mx_encode_kernel(const uint8_t* __restrict__ W, int64_t n, int64_t k,
+                                                             int64_t ld_bytes, bool bf16,
+                                                             uint8_t* __restrict__ codes,
+                                                             uint8_t* __restrict__ scales, int* __restrict__ status) {
+  const int64_t nb = k / 32;
+  for (int64_t row = blockIdx.x; row < n; row += gridDim.x) {
+    const uint8_t* rowp = W + row * ld_bytes;
+    for (int64_t b = threadIdx.x; b < nb; b += kThreads) {
+      float w[32];
+      if (bf16) {
+        const uint4* p = reinterpret_cast<const uint4*>(rowp) + 4 * b;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = __ldg(p + q);
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            w[8 * q + 2 * i] = __uint_as_float(u[i] << 16);
+            w[8 * q + 2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+          }
+        }
+      } else {
+        const float4* p = reinterpret_cast<const float4*>(rowp) + 8 * b;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 v = __ldg(p + q);
+          w[4 * q] = v.x;
+          w[4 * q + 1] = v.y;
+          w[4 * q + 2] = v.z;
+          w[4 * q + 3] = v.w;
+        }
+      }
+      unsigned mb = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mb = max(mb, __float_as_uint(w[i]) & 0x7FFFFFFFu);
+      if (mb >= 0x7F800000u) {
+        record_error(status, 6);
+        continue;
+      }
+      int e = -127;
+      if (mb != 0u) {
+        const int bexp = static_cast<int>(mb >> 23);
+        const int fl = bexp > 0 ? bexp - 127 : (31 - __clz(static_cast<int>(mb))) - 149;  // floor(log2(amax))
+        e = min(max(fl - 2, -127), 127);
+      }
+      // 2^-e for e in [-127, 125] is a normal float.
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      uint32_t packed[4] = {0u, 0u, 0u, 0u};
+      if (mb != 0u) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          uint32_t byte = f32x2_to_e2m1x2_satfinite(__fmul_rn(w[2 * i], inv), __fmul_rn(w[2 * i + 1], inv));
+          if ((byte & 0x07u) == 0u) byte &= 0xF0u;  // a zero magnitude is +0 (code 0x0)
+          if ((byte & 0x70u) == 0u) byte &= 0x0Fu;
+          packed[i >> 2] |= byte << (8 * (i & 3));
+        }
+      }
+      *reinterpret_cast<uint4*>(codes + row * (k / 2) + b * 16) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      scales[row * nb + b] = static_cast<uint8_t>(e + 127);
+    }
+  }
+}
+
+__device__ __forceinline__ bool any_magnitude(uint4 v) { return ((v.x | v.y | v.z | v.w) & 0x77777777u) != 0u; }
+
+// Largest E8M0 code over the 32-blocks holding a non-zero code, plus one (0:
+// no such block), into *emax1 (zeroed by the caller).
+__global__ void __launch_bounds__(kThreads) mx_emax_kernel(const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ scales, int64_t n, int64_t k,
+                                                           unsigned* __restrict__ emax1) {
+  const int64_t nb = k / 32;
+  unsigned m = 0;
+  for (int64_t row = blockIdx.x; row < n; row += gridDim.x)
+    for (int64_t b = threadIdx.x; b < nb; b += kThreads)
+      if (any_magnitude(__ldg(reinterpret_cast<const uint4*>(codes + row * (k / 2) + b * 16))))
+        m = max(m, static_cast<unsigned>(scales[row * nb + b]) + 1u);
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31) == 0 && m != 0u) atomicMax(emax1, m);
+}
+
+// MXFP4 -> the linear's packed layout.  The kernel decodes E4M3 block scales
+// times one fp32 tensor scale, so a power-of-two block scale 2^(e-127) is
+// written as S * 2^d with S = 2^(e_ref - 127), e_ref = e_max - 8, and the E4M3
+// code of 2^d (d = e - e_ref in [-9, 8]: E4M3 holds those powers exactly,
+// 2^-9 .. 2^-7 as subnormals), the same code in both 16-element slots of the
+// 32-block.  The product is the MXFP4 value exactly.  A non-zero block with
+// d < -9 (a block scale more than 2^17 below the weight's largest) does not
+// fit: it is written as zero and the call records QERL_ERR_RANGE.
+__global__ void __launch_bounds__(kThreads) mx_pack_kernel(const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ scales, int n, int k,
+                                                           const unsigned* __restrict__ emax1,
+                                                           uint8_t* __restrict__ packed, float* __restrict__ S_out,
+                                                           int* __restrict__ status) {
+  const int g = blockIdx.x, t = blockIdx.y;
+  const int kg = gridDim.x;
+  const unsigned em1 = *emax1;
+  const int e_ref = em1 == 0u ? 127 : static_cast<int>(em1) - 1 - 8;
+  if (g == 0 && t == 0 && threadIdx.x == 0) {
+    const int se = e_ref - 127;  // in [-135, 119]
+    *S_out = em1 == 0u ? 1.0f
+                       : __uint_as_float(se >= -126 ? static_cast<uint32_t>(se + 127) << 23 : 1u << (se + 149));
+  }
+  if (n == 0 || k == 0) return;  // an empty weight: only S
+  uint8_t* blk = packed + (static_cast<int64_t>(t) * kg + g) * kPackedBlockBytes;
+  const int row_bytes = k / 2, srow = k / 32;
+  for (int idx = threadIdx.x; idx < 128 * 8; idx += kThreads) {
+    const int r = idx >> 3, c = idx & 7;
+    const int nrow = t * 128 + r;
+    const int off = g * 128 + c * 16;  // chunk c is 32-block g * 8 + c
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    unsigned short sv = 0;
+    if (nrow < n && off < row_bytes) {
+      v = __ldg(reinterpret_cast<const uint4*>(codes + static_cast<int64_t>(nrow) * row_bytes + off));
+      if (any_magnitude(v)) {
+        const int d = static_cast<int>(scales[static_cast<int64_t>(nrow) * srow + g * 8 + c]) - e_ref;
+        if (d < -9) {
+          record_error(status, QERL_ERR_RANGE);
+          v = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          const unsigned c4 = d >= -6 ? static_cast<unsigned>(d + 7) << 3 : 1u << (d + 9);
+          sv = static_cast<unsigned short>(c4 | (c4 << 8));
+        }
+      }
+    }
+    *reinterpret_cast<uint4*>(blk + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+    *reinterpret_cast<unsigned short*>(blk + 16384 + c * 256 + r * 2) = sv;
+  }
+}
+
 }  // namespace
+
+qerl_status launch_mx_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w, uint8_t* codes,
+                             uint8_t* scales, int* status, cudaStream_t s) {
+  if (n == 0 || k == 0) return QERL_OK;
+  const int64_t esz = bf16 ? 2 : 4;
+  mx_encode_kernel<<<grid_for_rows(n), kThreads, 0, s>>>(static_cast<const uint8_t*>(W), n, k, ld_w * esz, bf16,
+                                                          codes, scales, status);
+  return cuda_status(cudaGetLastError());
+}
+
+qerl_status launch_mx_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
+                           float* tensor_scale, unsigned* emax1, int* status, cudaStream_t s) {
+  mx_emax_kernel<<<grid_for_rows(n), kThreads, 0, s>>>(codes, scales, n, k, emax1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return QERL_ERR_CUDA;
+  const dim3 grid(static_cast<unsigned>(n > 0 && k > 0 ? (k + 255) / 256 : 1),
+                  static_cast<unsigned>(n > 0 && k > 0 ? (n + 127) / 128 : 1));
+  mx_pack_kernel<<<grid, kThreads, 0, s>>>(codes, scales, static_cast<int>(n), static_cast<int>(k), emax1, packed,
+                                           tensor_scale, status);
+  return cuda_status(cudaGetLastError());
+}
 
 size_t packed_weight_bytes(int64_t n, int64_t k) {
   return static_cast<size_t>((n + 127) / 128) * static_cast<size_t>((k + 255) / 256) * kPackedBlockBytes;

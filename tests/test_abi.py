@@ -221,6 +221,34 @@ def test_quantize_validation(L):
     assert L.qerl_aqn_sample(None, 0, 1.0, 0, 0, 0, None) == 0
 
 
+def test_mxfp4_validation(L):
+    """The MXFP4 entry points reject bad arguments on the host, before any device work."""
+    E = q.STATUS_NAMES
+    qz = lambda **kw: L.qerl_mxfp4_quantize(
+        kw.get("W", 0x1000), kw.get("dt", q.QERL_BF16), kw.get("n", 4), kw.get("k", 64), kw.get("ld", 64),
+        kw.get("codes", 0x2000), kw.get("scales", 0x3000), kw.get("ws", 0x10000), kw.get("wsb", 256), None)
+    assert E[qz(k=48, ld=48)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[qz(dt=7)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[qz(ld=32)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[qz(W=0x1002)] == "QERL_ERR_MISALIGNED"
+    assert E[qz(codes=0x2004)] == "QERL_ERR_MISALIGNED"
+    assert E[qz(scales=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[qz(wsb=128)] == "QERL_ERR_WORKSPACE"
+    assert E[qz(ws=0x10080)] == "QERL_ERR_MISALIGNED"
+    pk = lambda **kw: L.qerl_mxfp4_pack(
+        kw.get("codes", 0x2000), kw.get("scales", 0x3001), kw.get("n", 4), kw.get("k", kw.get("k", 128)),
+        kw.get("packed", 0x4000), kw.get("ts", 0x5000), kw.get("ws", 0x10000), kw.get("wsb", 256), None)
+    assert E[pk(k=96)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[pk(k=65536 + 64)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[pk(n=-1)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[pk(ts=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[pk(packed=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[pk(packed=0x4008)] == "QERL_ERR_MISALIGNED"
+    assert E[pk(codes=0x2001)] == "QERL_ERR_MISALIGNED"
+    assert E[pk(wsb=0)] == "QERL_ERR_WORKSPACE"
+    assert L.qerl_status_string(8) == b"QERL_ERR_RANGE"
+
+
 def test_product_and_oracle_are_independent():
     pkg = os.path.join(ROOT, "nvfp4_weight_quantized_03_gb300")
     for dirpath, _, files in os.walk(pkg):
