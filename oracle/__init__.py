@@ -260,10 +260,11 @@ def noise_apply(x_bits: np.ndarray, z) -> np.ndarray:
     return out
 
 
-def lora_linear_backward(xt_bits, codes, scales, S, A_bits, B_bits, alpha, dy):
+def lora_linear_backward(xt_bits, codes, scales, S, A_bits, B_bits, alpha, dy, want_dxt=True):
     """Gradients of the linear through the frozen NVFP4 weight, fp64: (d_xt [m, k], dA [r, k],
     dB [n, r]) for y = xt W_hat^T + (alpha/r)(xt A^T) B^T and the output gradient dy [m, n].
-    xt_bits is the bf16 noisy activation; A_bits/B_bits None: no LoRA term (dA, dB None)."""
+    xt_bits is the bf16 noisy activation; A_bits/B_bits None: no LoRA term (dA, dB None).
+    want_dxt False: d_xt is not computed (None), only the adapters' gradients."""
     xt_bits = np.ascontiguousarray(xt_bits, dtype=np.uint16)
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scales = np.ascontiguousarray(scales, dtype=np.uint8)
@@ -274,7 +275,7 @@ def lora_linear_backward(xt_bits, codes, scales, S, A_bits, B_bits, alpha, dy):
     r = 0 if A_bits is None else A_bits.shape[0]
     A = None if A_bits is None else np.ascontiguousarray(A_bits, dtype=np.uint16)
     B = None if B_bits is None else np.ascontiguousarray(B_bits, dtype=np.uint16)
-    dxt = np.empty((m, k), dtype=np.float64)
+    dxt = np.empty((m, k), dtype=np.float64) if want_dxt else None
     dA = np.zeros((max(r, 1), k), dtype=np.float64)
     dB = np.zeros((n, max(r, 1)), dtype=np.float64)
     _check(lib().orc_lora_linear_backward(_ptr(xt_bits, _u16p), m, k, _ptr(codes, _u8p), _ptr(scales, _u8p),

@@ -600,19 +600,21 @@ int orc_lora_linear_backward(const uint16_t* xt, int64_t m, int64_t k, const uin
     if (k % 32 != 0) return ORC_ERR_SHAPE;
     const int use_lora = (A != NULL && B != NULL && r > 0);
     const double s = use_lora ? (double)alpha / (double)r : 0.0;
-    double* W_hat = (double*)malloc(sizeof(double) * (size_t)(n * k + 1));
+    double* W_hat = dxt != NULL ? (double*)malloc(sizeof(double) * (size_t)(n * k + 1)) : NULL;
     double* dyB = (double*)malloc(sizeof(double) * (size_t)(m * (r > 0 ? r : 1) + 1));
     double* t = (double*)malloc(sizeof(double) * (size_t)(m * (r > 0 ? r : 1) + 1));
-    if (!W_hat || !dyB || !t) { free(W_hat); free(dyB); free(t); return ORC_ERR_ARG; }
-    orc_nvfp4_dequant(codes, scales, S, n, k, W_hat);
+    if ((dxt != NULL && !W_hat) || !dyB || !t) { free(W_hat); free(dyB); free(t); return ORC_ERR_ARG; }
 
-    /* d_xt = dy W_hat */
-    for (int64_t i = 0; i < m; ++i)
-        for (int64_t kk = 0; kk < k; ++kk) {
-            double acc = 0.0;
-            for (int64_t c = 0; c < n; ++c) acc += dy[i * n + c] * W_hat[c * k + kk];
-            dxt[i * k + kk] = acc;
-        }
+    /* d_xt = dy W_hat (skipped when dxt is NULL: only the adapters' gradients) */
+    if (dxt != NULL) {
+        orc_nvfp4_dequant(codes, scales, S, n, k, W_hat);
+        for (int64_t i = 0; i < m; ++i)
+            for (int64_t kk = 0; kk < k; ++kk) {
+                double acc = 0.0;
+                for (int64_t c = 0; c < n; ++c) acc += dy[i * n + c] * W_hat[c * k + kk];
+                dxt[i * k + kk] = acc;
+            }
+    }
     if (use_lora) {
         /* dy B and t = xt A^T */
         for (int64_t i = 0; i < m; ++i)
@@ -625,7 +627,7 @@ int orc_lora_linear_backward(const uint16_t* xt, int64_t m, int64_t k, const uin
                 t[i * r + j] = b;
             }
         /* d_xt += s (dy B) A */
-        for (int64_t i = 0; i < m; ++i)
+        for (int64_t i = 0; i < (dxt != NULL ? m : 0); ++i)
             for (int64_t kk = 0; kk < k; ++kk) {
                 double acc = 0.0;
                 for (int j = 0; j < r; ++j) acc += dyB[i * r + j] * (double)bf16_bits_to_f32(A[(int64_t)j * k + kk]);

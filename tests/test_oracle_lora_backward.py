@@ -83,3 +83,12 @@ def test_base_part_is_the_adjoint_of_the_forward(orc):
     lhs = float(np.sum(dy * y))
     rhs = float(np.sum(dxt * wl.bf16_bits_to_f32(xt).astype(np.float64)))
     assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+
+
+def test_adapter_gradients_alone_match_the_full_call(orc):
+    """want_dxt=False skips only the input gradient: dA and dB are bit-identical to the full call."""
+    codes, scales, S, xt, A, B, dy = _setup(orc, seed=5)
+    _, dA, dB = orc.lora_linear_backward(xt, codes, scales, S, A, B, ALPHA, dy)
+    dxt2, dA2, dB2 = orc.lora_linear_backward(xt, codes, scales, S, A, B, ALPHA, dy, want_dxt=False)
+    assert dxt2 is None
+    assert np.array_equal(dA, dA2) and np.array_equal(dB, dB2)
