@@ -78,7 +78,7 @@ ARM_PARTS = {(0x41, 0xD0C): "Neoverse-N1", (0x41, 0xD40): "Neoverse-V1", (0x41, 
              (0x41, 0xD4F): "Neoverse-V2", (0x41, 0xD8E): "Neoverse-N3", (0x41, 0xD84): "Neoverse-V3"}
 
 
-EXTRAS = ("prefill", "quantize", "qproj", "sustained", "32b", "mxfp4")
+EXTRAS = ("prefill", "quantize", "qproj", "sustained", "32b", "mxfp4", "backward")
 
 
 def host_cpu_model():
@@ -470,6 +470,7 @@ def bench_ours(args):
     extra_sustained = bench_sustained(q, hbm_peak, dev_index) if "sustained" in want else None
     extra_32b = bench_32b_stream(q, hbm_peak) if "32b" in want else None
     extra_mx = bench_mxfp4(q, hbm_peak) if "mxfp4" in want else None
+    extra_bwd = bench_backward(q, bf16_peak) if "backward" in want else None
 
     # ---- the dominant launch, timed per call
     roofline = dominant_call(q, layers, acts, hbm_peak)
@@ -531,6 +532,8 @@ def bench_ours(args):
         out["quantize_32b_all"] = extra_32b["quantize"]
     if extra_mx:
         out["mxfp4"] = extra_mx
+    if extra_bwd:
+        out["backward"] = extra_bwd
     if rank == 0 and not args.skip_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_oracle(seconds_budget=args.cpu_budget)
     if rank == 0:
@@ -653,6 +656,61 @@ def bench_quantize(q, hbm_peak):
            "bytes_note": "4.5625 B/weight: bf16 read twice (amax pass + encode pass) + 0.5625 B written; "
                          "single-pass lower bound 2.5625 B/weight"}
     del Ws, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+def backward_flops(lin, m, r=RANK_R):
+    """dx~ = dy W_hat (2mnk) + s (dy B) A (u: 2mnr, u A: 2mrk); t = x~ A^T (2mkr); dA (2mrk); dB (2mnr)."""
+    return 2.0 * m * lin.n * lin.k + 4.0 * m * lin.n * r + 6.0 * m * lin.k * r
+
+
+def bench_backward(q, bf16_peak, m=4096):
+    """The policy-update half: the backward of the 14B-shaped layer's seven linears at M = 4096 (dx~,
+    dA, dB per linear; the weights packed transposed once), graph replay."""
+    shapes = wl.QWEN_14B
+    r = RANK_R
+    items = []
+    for li, lin in enumerate(shapes):
+        W = wl.weight_f32_device(lin.n, lin.k, 6, 0, li)
+        codes, scales, S = q.quantize(W)
+        del W
+        wpt = q.pack_transposed(codes, scales)
+        del codes, scales
+        A = wl.normal_bf16_device((r, lin.k), 1.0 / math.sqrt(lin.k), 6, li, 2)
+        B = wl.normal_bf16_device((lin.n, r), 0.01, 6, li, 3)
+        xt = wl.normal_bf16_device((m, lin.k), 1.0, 6, li, 4)
+        dy = wl.normal_bf16_device((m, lin.n), 0.01, 6, li, 5)
+        dxt = torch.empty((m, lin.k), dtype=torch.bfloat16, device="cuda")
+        dA = torch.empty((r, lin.k), dtype=torch.float32, device="cuda")
+        dB = torch.empty((lin.n, r), dtype=torch.float32, device="cuda")
+        items.append((lin, wpt, S, A, B, xt, dy, dxt, dA, dB))
+    ws = q.workspace(max(q.qerl_lora_linear_backward_workspace_size(m, lin.n, lin.k, r) for lin in shapes))
+
+    def layer_bwd():
+        for lin, wpt, S, A, B, xt, dy, dxt, dA, dB in items:
+            q.check(q.qerl_lora_linear_backward(xt, dy, wpt, S, A, B, ALPHA, dxt, dA, dB, ws),
+                    "qerl_lora_linear_backward")
+
+    t_ms, _, pct = _graph_time_ms(layer_bwd, 20)
+    q.check(q.qerl_read_status(ws), "backward status")
+    flops = sum(backward_flops(lin, m, r) for lin in shapes)
+    per = {}
+    for lin, wpt, S, A, B, xt, dy, dxt, dA, dB in items:
+        def one():
+            q.check(q.qerl_lora_linear_backward(xt, dy, wpt, S, A, B, ALPHA, dxt, dA, dB, ws),
+                    "qerl_lora_linear_backward")
+        lt, _, _ = _graph_time_ms(one, 10)
+        lf = backward_flops(lin, m, r)
+        per[lin.name] = {"ms": round(lt, 4), "TFLOPs": round(lf / (lt * 1e-3) / 1e12, 1),
+                         "frac_of_bf16_peak": round(lf / (lt * 1e-3) / 1e12 / bf16_peak, 4)}
+    res = {"workload": "backward of the Qwen2.5-14B-shaped layer's 7 linears, M=4096, r=32 alpha=64: dx~ (bf16), "
+                       "dA, dB (fp32)",
+           "ms_per_layer": round(t_ms, 4), "TFLOPs": round(flops / (t_ms * 1e-3) / 1e12, 1),
+           "frac_of_bf16_peak": round(flops / (t_ms * 1e-3) / 1e12 / bf16_peak, 4),
+           "ms_per_layer_p10_median_p90": [round(v, 4) for v in pct], "per_linear": per,
+           "flops_note": "2mnk + 4mnr + 6mkr per linear (dx~ base, dy B, (dy B) A, x~ A^T, dA, dB)"}
+    del items
     torch.cuda.empty_cache()
     return res
 

@@ -147,6 +147,21 @@ QERL_API size_t qerl_nvfp4_packed_size(int64_t n, int64_t k);
 QERL_API qerl_status qerl_nvfp4_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
                                      uint8_t* packed, void* stream);
 
+/* The transposed packed layout, for the input gradient of the linear
+ * (qerl_lora_linear_backward): the n x k weight's k x n transpose, its
+ * contraction running along n.  Same block size and code bytes as
+ * qerl_nvfp4_pack's layout with the roles of n and k exchanged (blocks per
+ * 128-row tile over k and 256-wide stage over n; row kk of a tile holds the
+ * codes of W[n][k] for the stage's n, two per byte, n even in the low
+ * nibble); the 2048 scale bytes of a block hold the E4M3 scale of (n, k),
+ * scales[n][k/16], for each of the tile's eight 16-row groups and the
+ * stage's 256 n, at 16384 + (kk / 16) * 256 + (n mod 256).  Size:
+ * qerl_nvfp4_packed_size(k, n) bytes.  Requires n % 64 == 0, n <= 65536,
+ * k % 32 == 0; codes and packed_t 16-byte aligned.  Weights are frozen in
+ * LoRA training, so this runs once per weight, beside qerl_nvfp4_pack. */
+QERL_API qerl_status qerl_nvfp4_pack_transposed(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
+                                                uint8_t* packed_t, void* stream);
+
 /* ========================================================================
  * MXFP4, the 4-bit format the digest's "NVFP4 Quantization" section compares
  * NVFP4 with: E2M1 elements with one shared E8M0 (power-of-two) scale per 32
@@ -346,6 +361,43 @@ QERL_API qerl_status qerl_rmsnorm_lora_linear_group(const void* h, int64_t m, in
  * x~ (16-byte aligned, ldo % 8 == 0).  k % 8 == 0, m <= 65535.  No workspace. */
 QERL_API qerl_status qerl_rmsnorm_noise(const void* h, int64_t m, int64_t k, int64_t ldh, const void* w_norm,
                                         const float* Z, double delta, void* out, int64_t ldo, void* stream);
+
+/* ========================================================================
+ * The backward pass of the linear ("Low-Rank Adaptation (LoRA) Within
+ * Quantized Layers", gradient flow: the quantized base weight is frozen and
+ * only carries the input gradient; A and B are trained).  For the forward
+ * y = x~ W_hat^T + s (x~ A^T) B^T, s = alpha / r:
+ *
+ *   dx~ = dy W_hat + s (dy B) A        [m][k]  (bf16 or fp32, row stride k)
+ *   dA  = s (dy B)^T x~                [r][k]  fp32
+ *   dB  = s dy^T (x~ A^T)              [n][r]  fp32
+ *
+ * xt      device bf16 [m][ldxt]: the forward's input to both branches, x~
+ *         (needed for dA and dB; may be NULL when both are NULL or r == 0).
+ * dy      device bf16 [m][lddy].
+ * wpacked_t  the weight in the transposed packed layout
+ *         (qerl_nvfp4_pack_transposed), tensor_scale its S (device float).
+ * A, B    the adapters as in the forward (bf16 [r][k], [n][r]), or both NULL
+ *         (r ignored: no LoRA terms; dA, dB untouched).
+ * dxt     device [m][k], dxt_dtype QERL_BF16 or QERL_F32; dA, dB device fp32
+ *         or NULL to skip.
+ * workspace  >= qerl_lora_linear_backward_workspace_size(m, n, k, r) bytes,
+ *         256-byte aligned, zero-filled before first use; its status word
+ *         (qerl_read_status) records kernel-detected errors as for the linear.
+ * Requires n % 64 == 0 (n <= 65536), k % 64 == 0 (as the forward does),
+ * r % 8 == 0 (r <= 128),
+ * 16-byte aligned xt, dy, A, B and packed weights, ldxt and lddy multiples
+ * of 8.  m == 0 zero-fills dA and dB.  dx~ runs on the forward's
+ * tensor-core kernel (the transposed problem: dy contracts with W_hat along
+ * n; u = dy B is its LoRA down-projection and A its up-projection); dA and
+ * dB are rank-r reductions over the m tokens on CUDA cores, deterministic.
+ * ======================================================================== */
+QERL_API size_t qerl_lora_linear_backward_workspace_size(int64_t m, int64_t n, int64_t k, int r);
+QERL_API qerl_status qerl_lora_linear_backward(const void* xt, int64_t m, int64_t k, int64_t ldxt, const void* dy,
+                                               int64_t n, int64_t lddy, const uint8_t* wpacked_t,
+                                               const float* tensor_scale, const void* A, const void* B, int r,
+                                               float alpha, void* dxt, int dxt_dtype, float* dA, float* dB,
+                                               void* workspace, size_t ws_bytes, void* stream);
 
 /* The same linear for callers that cannot allocate device memory where they
  * run it (a runtime with a fixed memory pool, a latency-critical loop that must

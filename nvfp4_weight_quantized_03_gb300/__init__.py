@@ -100,6 +100,14 @@ def lib():
             L.qerl_nvfp4_quantize_with_scale.restype = ctypes.c_int
             L.qerl_nvfp4_quantize_with_scale.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                                          ctypes.c_size_t, _vp]
+            L.qerl_nvfp4_pack_transposed.restype = ctypes.c_int
+            L.qerl_nvfp4_pack_transposed.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp]
+            L.qerl_lora_linear_backward_workspace_size.restype = ctypes.c_size_t
+            L.qerl_lora_linear_backward_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.c_int]
+            L.qerl_lora_linear_backward.restype = ctypes.c_int
+            L.qerl_lora_linear_backward.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _vp,
+                                                    ctypes.c_int, ctypes.c_float, _vp, ctypes.c_int, _vp, _vp, _vp,
+                                                    ctypes.c_size_t, _vp]
             L.qerl_mxfp4_quantize.restype = ctypes.c_int
             L.qerl_mxfp4_quantize.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_size_t,
                                               _vp]
@@ -261,6 +269,31 @@ def qerl_nvfp4_pack(codes, scales, packed, stream=None) -> int:
     return lib().qerl_nvfp4_pack(_p(codes), _p(scales), n, k, _p(packed), _stream(stream))
 
 
+def qerl_nvfp4_pack_transposed(codes, scales, packed_t, stream=None) -> int:
+    """codes [n, k/2], scales [n, k/16] -> the transposed packed layout (qerl_nvfp4_packed_size(k, n) bytes)."""
+    n = codes.shape[0]
+    k = codes.shape[1] * 2
+    return lib().qerl_nvfp4_pack_transposed(_p(codes), _p(scales), n, k, _p(packed_t), _stream(stream))
+
+
+def qerl_lora_linear_backward_workspace_size(m: int, n: int, k: int, r: int) -> int:
+    return lib().qerl_lora_linear_backward_workspace_size(int(m), int(n), int(k), int(r))
+
+
+def qerl_lora_linear_backward(xt, dy, wpacked_t, tensor_scale, A, B, alpha, dxt, dA, dB, workspace,
+                              stream=None) -> int:
+    """xt [m, k] bf16 (the forward's x~), dy [m, n] bf16, wpacked_t from qerl_nvfp4_pack_transposed;
+    dxt [m, k] bf16/fp32; dA [r, k], dB [n, r] fp32 or None."""
+    m, n = dy.shape
+    k = dxt.shape[1]
+    r = 0 if A is None else A.shape[0]
+    ddt = QERL_F32 if dxt.dtype == torch.float32 else QERL_BF16
+    ldxt = xt.stride(0) if xt is not None else k
+    return lib().qerl_lora_linear_backward(_p(xt), m, k, ldxt, _p(dy), n, dy.stride(0), _p(wpacked_t),
+                                           _p(tensor_scale), _p(A), _p(B), r, float(alpha), _p(dxt), ddt, _p(dA),
+                                           _p(dB), _p(workspace), _nbytes(workspace), _stream(stream))
+
+
 def qerl_mxfp4_quantize(W, codes, scales, workspace, stream=None) -> int:
     """W [n, k] f32/bf16 -> codes [n, k/2], E8M0 scales [n, k/32] (uint8)."""
     n, k = W.shape
@@ -397,6 +430,14 @@ def pack(codes: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
     n, k = codes.shape[0], codes.shape[1] * 2
     packed = torch.empty(qerl_nvfp4_packed_size(n, k), dtype=torch.uint8, device=codes.device)
     check(qerl_nvfp4_pack(codes, scales, packed), "qerl_nvfp4_pack")
+    return packed
+
+
+def pack_transposed(codes: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
+    """The transposed packed layout of quantized weights, for qerl_lora_linear_backward."""
+    n, k = codes.shape[0], codes.shape[1] * 2
+    packed = torch.empty(qerl_nvfp4_packed_size(k, n), dtype=torch.uint8, device=codes.device)
+    check(qerl_nvfp4_pack_transposed(codes, scales, packed), "qerl_nvfp4_pack_transposed")
     return packed
 
 

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqerl.so")
-SOURCES = ["api.cu", "quantize.cu", "aqn.cu", "linear.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quantize.cu", "aqn.cu", "linear.cu", "backward.cu", "noalloc.cu"]
 HEADERS = ["qerl_ptx.cuh", "qerl_internal.h", os.path.join("..", "..", "include", "qerl.h")]
 
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -226,6 +226,78 @@ qerl_status qerl_mxfp4_pack(const uint8_t* codes, const uint8_t* scales, int64_t
   return qerl::launch_mx_pack(codes, scales, n, k, packed, tensor_scale, &hdr->amax_bits, &hdr->status, s);
 }
 
+qerl_status qerl_nvfp4_pack_transposed(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
+                                       uint8_t* packed_t, void* stream) {
+  if (n < 0 || k < 0) return QERL_ERR_INVALID_ARGUMENT;
+  if (n % 64 != 0 || k % 32 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (n > 65536 || k > INT32_MAX) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0 || k == 0) return QERL_OK;
+  if (codes == nullptr || scales == nullptr || packed_t == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(codes, 16) || !aligned(packed_t, 16)) return QERL_ERR_MISALIGNED;
+  return qerl::launch_pack_t(codes, scales, n, k, packed_t, as_stream(stream));
+}
+
+size_t qerl_lora_linear_backward_workspace_size(int64_t m, int64_t n, int64_t k, int r) {
+  if (m < 0 || n < 0 || k < 0 || r < 0) return 0;
+  return qerl::backward_workspace_bytes(m, n, k, r);
+}
+
+qerl_status qerl_lora_linear_backward(const void* xt, int64_t m, int64_t k, int64_t ldxt, const void* dy, int64_t n,
+                                      int64_t lddy, const uint8_t* wpacked_t, const float* tensor_scale,
+                                      const void* A, const void* B, int r, float alpha, void* dxt, int dxt_dtype,
+                                      float* dA, float* dB, void* workspace, size_t ws_bytes, void* stream) {
+  if (m < 0 || n <= 0 || k <= 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
+  if (ldxt < k || lddy < n) return QERL_ERR_INVALID_ARGUMENT;
+  if (dxt_dtype != QERL_BF16 && dxt_dtype != QERL_F32) return QERL_ERR_INVALID_ARGUMENT;
+  if ((A == nullptr) != (B == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
+  if (A == nullptr) r = 0;
+  if (A != nullptr && r == 0) return QERL_ERR_INVALID_ARGUMENT;
+  if (r > 128 || r % 8 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  // The input gradient is a linear contracting over n (the transposed layout's
+  // K); t = x~ A^T contracts over k as the forward does (k % 64 == 0 there too).
+  if (n % 64 != 0 || k % 64 != 0) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (n > 65536 || k > INT32_MAX || m > INT32_MAX || m * n > (int64_t{1} << 40)) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (!std::isfinite(alpha)) return QERL_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = as_stream(stream);
+  if (m == 0) {  // empty sums: zero gradients for the adapters
+    if (r > 0 && dA != nullptr && cudaMemsetAsync(dA, 0, static_cast<size_t>(r) * k * 4, s) != cudaSuccess)
+      return QERL_ERR_CUDA;
+    if (r > 0 && dB != nullptr && cudaMemsetAsync(dB, 0, static_cast<size_t>(n) * r * 4, s) != cudaSuccess)
+      return QERL_ERR_CUDA;
+    return QERL_OK;
+  }
+  if (dy == nullptr || wpacked_t == nullptr || tensor_scale == nullptr || dxt == nullptr)
+    return QERL_ERR_INVALID_ARGUMENT;
+  if (r > 0 && (dA != nullptr || dB != nullptr) && xt == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(dy, 16) || lddy % 8 != 0 || !aligned(wpacked_t, 16)) return QERL_ERR_MISALIGNED;
+  if (xt != nullptr && (!aligned(xt, 16) || ldxt % 8 != 0)) return QERL_ERR_MISALIGNED;
+  if (dxt_dtype == QERL_F32 ? !aligned(dxt, 4) : !aligned(dxt, 2)) return QERL_ERR_MISALIGNED;
+  if (r > 0 && (!aligned(A, 16) || !aligned(B, 16) || !aligned(dA, 4) || !aligned(dB, 4)))
+    return QERL_ERR_MISALIGNED;
+  qerl_status st = check_ws(workspace, ws_bytes, qerl::backward_workspace_bytes(m, n, k, r));
+  if (st != QERL_OK) return st;
+  qerl::BackwardArgs b{};
+  b.xt = xt;
+  b.m = m;
+  b.k = k;
+  b.ldxt = ldxt;
+  b.dy = dy;
+  b.n = n;
+  b.lddy = lddy;
+  b.wpacked_t = wpacked_t;
+  b.tensor_scale = tensor_scale;
+  b.A = r > 0 ? A : nullptr;
+  b.B = r > 0 ? B : nullptr;
+  b.r = r;
+  b.alpha = alpha;
+  b.dxt = dxt;
+  b.dxt_f32 = dxt_dtype == QERL_F32;
+  b.dA = r > 0 ? dA : nullptr;
+  b.dB = r > 0 ? dB : nullptr;
+  b.workspace = workspace;
+  return qerl::launch_lora_linear_backward(b, s);
+}
+
 size_t qerl_lora_linear_workspace_size(int64_t m, int64_t n, int64_t k, int r) {
   (void)n;
   if (m < 0 || k < 0 || r < 0) return 0;

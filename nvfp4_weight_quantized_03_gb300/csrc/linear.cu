@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     // Four vectors per thread per round: their loads are all in flight
     // before the first is used.
     const float4* z4 = reinterpret_cast<const float4*>(p.z != nullptr ? p.z + m * p.ldz : nullptr);
+    uint4* xo = p.xt_out != nullptr ? reinterpret_cast<uint4*>(p.xt_out + static_cast<int64_t>(m) * p.ldo) : nullptr;
     for (int v0 = tid; v0 < nv; v0 += 4 * kPrepThreads) {
       uint4 raw[4];
       float4 za[4], zb[4];
@@ -283,6 +284,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) amax = max(amax, static_cast<unsigned>(__bfloat16_as_ushort(e[j]) & 0x7FFFu));
         reinterpret_cast<uint4*>(xt)[v] = raw[u];
+        if (xo != nullptr) xo[v] = raw[u];
       }
     }
     }
@@ -550,6 +552,7 @@ struct MmaParams {
   // stage of the weight stage), the LoRA operands are built in the idle ring.
   int pair;
   int xs_rowmajor;  // x~ staged as [M][K] (more than 128 tokens: several token tiles), read by 2-D TMA
+  int wt;           // the weights are in the transposed packed layout (input gradient of the linear)
 };
 
 // The LoRA up-projection's B matrices, one TMA map per linear of the launch.
@@ -736,6 +739,49 @@ __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, const Linear
 // product, so one issuer cannot keep the pipe busy at decode token counts).
 // Otherwise (256-token tiles) the operand is staged in shared memory and one
 // thread issues.
+// One MMA stage (64 K) of weight row `row` of a staged packed block at
+// `slot` -> 32 fp16 pairs o[] (element pairs along K), exact: an E2M1 value
+// times an E4M3 scale fits fp16.  Forward layout: one scale per 16 K, as
+// pairs at kCodesRawBytes + p * 256 + 2 * row.  Transposed layout (wt; the
+// weight's transpose for the input gradient, K being the original output
+// dimension): a scale per element along K, shared by the 16 rows of a row
+// group, at kCodesRawBytes + (row / 16) * 256 + k.
+__device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q, bool wt, uint32_t (&o)[32]) {
+  const uint32_t crow = slot + row * 128;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 cw = lds128(crow + (((2 * q + h) ^ (row & 7)) << 4));
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    if (!wt) {
+      const __half2 s01 = e4m3x2_to_half2(lds16(slot + kCodesRawBytes + row * 2 + (2 * q + h) * 256));
+      const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
+      const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
+      const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        uint32_t u[4];
+        e2m1x8_to_f16x2x4(words[qq], u);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) o[16 * h + 4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
+      }
+    } else {
+      const uint32_t sbase = slot + kCodesRawBytes + (row >> 4) * 256 + (2 * q + h) * 32;
+      const uint4 s0 = lds128(sbase), s1 = lds128(sbase + 16);
+      const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        uint32_t u[4];
+        e2m1x8_to_f16x2x4(words[qq], u);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const __half2 sc = e4m3x2_to_half2((sw[2 * qq + (b >> 1)] >> (16 * (b & 1))) & 0xFFFFu);
+          o[16 * h + 4 * qq + b] = hmul2_bits(u[b], *reinterpret_cast<const uint32_t*>(&sc));
+        }
+      }
+    }
+  }
+}
+
 template <bool kTmemA>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ BtMaps tm_bls,
@@ -1161,6 +1207,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------------------ dequant warps
     const int dw = warp - kDeqWarp0;
+    const bool wt = p.wt != 0;
     if (kTmemA && p.pair) {
       // Pair mode: group g = dw / 4 dequantizes tile g of the pair (a thread
       // is one weight row of it), every weight stage, and hands each MMA
@@ -1175,30 +1222,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int i = 0; i < nraw; ++i) {
           if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
           const uint32_t slot = sbase + p.off_raw + s * rslot + g * kRawSlotBytes;
-          const uint32_t crow = slot + row * 128;
-          const uint32_t srow = slot + kCodesRawBytes + row * 2;
           const int nq = min(kSub, nmma - i * kSub);
           bool ok = true;
 #pragma unroll
           for (int q = 0; q < kSub; ++q) {
             if (q >= nq) break;
             uint32_t o[32];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint4 cw = lds128(crow + (((2 * q + h) ^ (row & 7)) << 4));
-              const __half2 s01 = e4m3x2_to_half2(lds16(srow + (2 * q + h) * 256));
-              const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
-              const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
-              const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
-              const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-              for (int qq = 0; qq < 4; ++qq) {
-                uint32_t u[4];
-                e2m1x8_to_f16x2x4(words[qq], u);
-#pragma unroll
-                for (int b = 0; b < 4; ++b) o[16 * h + 4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
-              }
-            }
+            dequant_mma_stage(slot, row, q, wt, o);
             const int sl = g * kSub + q;
             if (!warp_wait(ab_empty(sl), (i & 1) ^ 1, abort_flag, p.status)) {
               ok = false;
@@ -1236,8 +1266,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int i = grp; i < nraw; i += 2) {
         if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
         const uint32_t slot = sbase + p.off_raw + s * kRawSlotBytes;
-        const uint32_t crow = slot + row * 128;
-        const uint32_t srow = slot + kCodesRawBytes + row * 2;
         const int nq = min(kSub, nmma - i * kSub);
         const uint32_t a_slot = tmem_base + lane_base + p.col_a + static_cast<uint32_t>(w * kSub * kAStageCols);
         bool ok = true;
@@ -1245,24 +1273,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int q = 0; q < kSub; ++q) {
           if (q >= nq) break;
           // MMA stage q: 16-byte code chunks 2q, 2q + 1 of the row (128-byte
-          // swizzle) and the scale pairs of the same K range.
+          // swizzle) and the scales of the same K range.
           uint32_t o[32];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint4 cw = lds128(crow + (((2 * q + h) ^ (row & 7)) << 4));
-            const __half2 s01 = e4m3x2_to_half2(lds16(srow + (2 * q + h) * 256));
-            const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
-            const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
-            const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
-            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              uint32_t u[4];
-              e2m1x8_to_f16x2x4(words[qq], u);
-#pragma unroll
-              for (int b = 0; b < 4; ++b) o[16 * h + 4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
-            }
-          }
+          dequant_mma_stage(slot, row, q, wt, o);
           // The slot's previous MMAs must be done before the first store
           // (the first conversion overlaps that wait).
           if (q == 0 && !warp_wait(ab_empty(w), aph ^ 1, abort_flag, p.status)) {
@@ -1697,6 +1710,179 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return f;
 }
 
+// ---------------------------------------------------------------------------
+// The LoRA down-projection on the tensor cores, for more than 128 tokens
+// ("Low-Rank Adaptation (LoRA) Within Quantized Layers", Eq. 2: the branch's
+// first factor, t = x~ A^T, which the up-projection in the linear's epilogue
+// consumes):  t_i[m][j] = sum_k X[m][k] A_i[j][k],  X bf16 [M][K] (x~),
+// A_i bf16 [r_i][K], t_i fp32 [M][r_i].
+// A CTA: 128 token rows x round16(r_i) ranks over a K range; grid (split,
+// token tiles, linears), clusters of `split` CTAs along K whose fp32
+// accumulators are added over distributed shared memory in rank order
+// (deterministic).  Warp 0 lane 0 streams (X, A) 64-wide K stages by TMA
+// (128-byte swizzle; rows past M and ranks past r read as zeros); warp 1
+// lane 0 issues kind::f16 MMAs with bf16 operands (products exact, fp32
+// accumulation) into tensor memory; all four warps read the accumulator back.
+constexpr int kLdThreads = 128;
+constexpr int kLdStages = 4;
+constexpr int kLdMaxSplit = 8;
+
+struct LdMaps {
+  CUtensorMap x;
+  CUtensorMap a[kMaxLinears];
+};
+struct LdParams {
+  int M, K;
+  int r[kMaxLinears];
+  float* t[kMaxLinears];
+  int lin_of[kMaxLinears];  // blockIdx.z -> linear
+  int split;
+  int* status;
+};
+
+__host__ __device__ constexpr uint32_t ld_stage_bytes(int r16) { return 16384u + static_cast<uint32_t>(r16) * 128u; }
+__host__ __device__ constexpr uint32_t ld_smem_bytes(int r16) {
+  return 1024u + kLdStages * ld_stage_bytes(r16) + 8u * (2 * kLdStages + 2) + 8u;
+}
+
+__global__ void __launch_bounds__(kLdThreads, 1)
+    lora_down_tc_kernel(const __grid_constant__ LdMaps maps, const LdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem_gen = smem_raw + (sbase - raw_addr);
+  const int li = p.lin_of[blockIdx.z];
+  const int r = p.r[li];
+  const int r16 = (r + 15) & ~15;
+  const uint32_t stage_bytes = ld_stage_bytes(r16);  // a multiple of 2048: stages stay 1024-byte aligned
+  const uint32_t ring_bytes = kLdStages * stage_bytes;
+  const uint32_t bars = sbase + ring_bytes;
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (kLdStages + s); };
+  const uint32_t acc_full = bars + 8u * (2 * kLdStages);
+  const uint32_t tmem_holder = bars + 8u * (2 * kLdStages + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_gen + ring_bytes + 8 * (2 * kLdStages + 1) + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = p.split, sidx = static_cast<int>(blockIdx.x);
+  const int m0 = static_cast<int>(blockIdx.y) * 128;
+  const int nk = p.K / 64;
+  const int kc0 = sidx * nk / split, kc1 = (sidx + 1) * nk / split;  // >= 1 chunk each (split <= nk)
+  const uint32_t tcols = r16 <= 32 ? 32u : (r16 <= 64 ? 64u : 128u);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLdStages; ++s) {
+      mbar_init_a(full(s), 1);
+      mbar_init_a(empty(s), 1);
+    }
+    mbar_init_a(acc_full, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, tcols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.x);
+    tma_prefetch_desc(&maps.a[li]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem_gen + ring_bytes + 8 * (2 * kLdStages + 1));
+
+  if (warp == 0 && lane == 0) {
+    int issued = 0;
+    for (int kc = kc0; kc < kc1; ++kc) {
+      const int i = kc - kc0, s = i % kLdStages;
+      if (i >= kLdStages && !mbar_wait_a(empty(s), ((i / kLdStages) & 1) ^ 1, abort_flag, p.status)) break;
+      mbar_arrive_expect_tx_a(full(s), stage_bytes);
+      const uint32_t st = sbase + s * stage_bytes;
+      tma_load_2d(st, &maps.x, kc * 64, m0, full(s));
+      tma_load_2d(st + 16384u, &maps.a[li], kc * 64, 0, full(s));
+      issued = i + 1;
+    }
+    // Every issued copy lands before the ring is reused or the CTA exits
+    // (after an expired wait too): wait for each slot's last copy, bounded.
+    volatile int no_abort = 0;
+    for (int s = 0; s < min(issued, kLdStages); ++s) {
+      const int last = issued - 1 - ((issued - 1 - s) % kLdStages);
+      mbar_wait_a(full(s), (last / kLdStages) & 1, &no_abort, p.status);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(r16));
+    for (int kc = kc0; kc < kc1; ++kc) {
+      const int i = kc - kc0, s = i % kLdStages;
+      if (!mbar_wait_a(full(s), (i / kLdStages) & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t st = sbase + s * stage_bytes;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_f16(tmem, sw128_kmajor_desc(st + kk * 32), sw128_kmajor_desc(st + 16384u + kk * 32), idesc,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(empty(s));
+    }
+    tc_commit(acc_full);  // also after an expired wait: arrives once the issued MMAs are done
+  }
+  __syncwarp();
+  const bool ok = mbar_wait_a(acc_full, 0, abort_flag, p.status);
+  tc_fence_after();
+  __syncthreads();  // the producer's copies have landed: the ring is free
+  const int row = 32 * warp + lane;
+  const int m = m0 + row;
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+  float* tout = p.t[li];
+  if (split == 1) {
+    for (int c = 0; c < r16; c += 8) {
+      float v[8];
+      tmem_ld_x8(lane_addr + c, v);
+      tmem_ld_wait();
+      if (ok && m < p.M)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (c + e < r) tout[static_cast<int64_t>(m) * r + c + e] = v[e];
+    }
+  } else {
+    // Partial tile -> this CTA's shared memory ([128][r16] fp32 in the idle
+    // ring), then rank c of the cluster adds rows c, c + split, ... over all
+    // partners in rank order.
+    const uint32_t red = sbase;
+    for (int c = 0; c < r16; c += 8) {
+      float v[8];
+      tmem_ld_x8(lane_addr + c, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 8; ++e) stsf(red + static_cast<uint32_t>((row * r16 + c + e) * 4), v[e]);
+    }
+    cluster_sync_all();
+    const int q4 = r16 / 4;
+    for (int it = threadIdx.x; it < 128 * q4; it += kLdThreads) {
+      const int rr = it / q4, c4 = (it % q4) * 4;
+      if (rr % split != sidx) continue;
+      const uint32_t off = red + static_cast<uint32_t>((rr * r16 + c4) * 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < split; ++q) {
+        const float4 v = ld_shared_cluster_f32x4(mapa_shared(off, static_cast<uint32_t>(q)));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      const int mm = m0 + rr;
+      if (ok && mm < p.M) {
+        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (c4 + e < r) tout[static_cast<int64_t>(mm) * r + c4 + e] = a4[e];
+      }
+    }
+    cluster_sync_all();  // partners are done reading this CTA's partial tile
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, tcols);
+}
+
 bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
   auto enc = tensor_map_encoder();
@@ -1762,6 +1948,64 @@ int resident_clusters(int sp) {
   return n;
 }
 
+// The tensor-core LoRA down-projection (lora_down_tc_kernel) of up to four
+// linears sharing X (bf16 [M][ldx]): t[i] fp32 [M][r[i]] (r[i] == 0: skipped).
+qerl_status lora_down_tc(const void* x, int64_t ldx, int64_t M, int64_t K, const void* const* A, const int* r,
+                         float* const* t, int nlin, int* status, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(lora_down_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(ld_smem_bytes(128)));
+  });
+  if (err != cudaSuccess) return QERL_ERR_CUDA;
+  LdMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  if (!make_map_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(ldx) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return QERL_ERR_CUDA;
+  LdParams lp{};
+  lp.M = static_cast<int>(M);
+  lp.K = static_cast<int>(K);
+  lp.status = status;
+  int nz = 0, r16max = 0;
+  for (int i = 0; i < nlin; ++i) {
+    if (r[i] <= 0) continue;
+    const int r16 = (r[i] + 15) & ~15;
+    if (!make_map_2d(&maps.a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A[i], static_cast<uint64_t>(K),
+                     static_cast<uint64_t>(r[i]), static_cast<uint64_t>(K) * 2, 64, static_cast<uint32_t>(r16),
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return QERL_ERR_CUDA;
+    lp.r[i] = r[i];
+    lp.t[i] = t[i];
+    lp.lin_of[nz++] = i;
+    r16max = std::max(r16max, r16);
+  }
+  if (nz == 0 || M == 0) return QERL_OK;
+  const int m_tiles = static_cast<int>((M + 127) / 128);
+  const int nk = static_cast<int>(K / 64);
+  // Split K over a cluster until the grid covers the SMs once.
+  int split = (sm_count() + m_tiles * nz - 1) / (m_tiles * nz);
+  split = std::max(1, std::min(split, std::min(kLdMaxSplit, nk)));
+  lp.split = split;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(split), static_cast<unsigned>(m_tiles), static_cast<unsigned>(nz));
+  cfg.blockDim = dim3(kLdThreads, 1, 1);
+  cfg.dynamicSmemBytes = ld_smem_bytes(r16max);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = static_cast<unsigned>(split);
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lora_down_tc_kernel, maps, lp) == cudaSuccess ? QERL_OK : QERL_ERR_CUDA;
+}
+
+// Above this many tokens the LoRA down-projection runs on the tensor cores.
+__host__ inline bool lora_down_on_tc(int64_t m) { return m > 128; }
+
 struct LinearLayout {
   size_t xs, rinv, t[kMaxLinears], tf[kMaxLinears], count, xt, total;
 };
@@ -1789,17 +2033,129 @@ LinearLayout linear_layout(int64_t m, int64_t k, const int* ranks, int nlin, boo
     L.tf[i] = off;
     off = align_up(off + static_cast<size_t>(m) * r * 4, 256);
   }
-  // RMSNorm mode with a LoRA branch: the normalised x~ (bf16 [m][k]) for the
-  // LoRA down-projection.
+  // x~ in bf16 [m][k] for the LoRA down-projection when it does not read x
+  // itself: RMSNorm mode, and (with noise) the tensor-core down-projection.
   L.xt = off;
   bool lora = false;
   for (int i = 0; i < nlin; ++i) lora = lora || ranks[i] > 0;
-  if (rmsnorm && lora) off = align_up(off + static_cast<size_t>(m) * k * 2, 256);
+  if ((rmsnorm || lora_down_on_tc(m)) && lora) off = align_up(off + static_cast<size_t>(m) * k * 2, 256);
   L.total = off;
   return L;
 }
 
+constexpr int kPrepSmemLimit = kSmemLimit - 1024;  // leaves room for the kernel's static shared memory
+
+// Kernel attributes are set once per process (not per call), so calls can be
+// captured into CUDA graphs.
+bool kernel_attrs_ok() {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemLimit);
+    // The prep grid runs beside the MMA kernel's CTAs (which start early and
+    // hold most of shared memory): the same carveout lets them share an SM.
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      cudaSharedmemCarveoutMaxShared);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  });
+  return attr_err == cudaSuccess;
+}
+
+// The prep kernel's LoRA tiles for one linear (rank r, down-projection A
+// [r][k]) over x (bf16 [m][ldx], no noise): fills the fields of `pp` they use.
+void lora_prep_params(PrepParams& pp, int64_t m, int64_t k, int r, const void* A, uint8_t* ws,
+                      const LinearLayout& WL) {
+  const int ranks[1] = {r};
+  const LoraSplit ls = lora_split(m, k, ranks, 1);
+  pp.M = static_cast<int>(m);
+  pp.K = static_cast<int>(k);
+  pp.cluster = ls.cluster;
+  pp.groups = ls.groups;
+  pp.lora_m_tiles = static_cast<int>((m + kLoraTileM - 1) / kLoraTileM);
+  pp.tile_begin[0] = 0;
+  for (int i = 0; i < kMaxLinears; ++i) {
+    const bool on = i == 0;
+    pp.A[i] = on ? static_cast<const __nv_bfloat16*>(A) : nullptr;
+    pp.r[i] = on ? r : 0;
+    pp.t[i] = reinterpret_cast<float*>(ws + WL.t[i]);
+    pp.tf[i] = reinterpret_cast<float*>(ws + WL.tf[i]);
+    pp.tile_begin[i + 1] = pp.tile_begin[i] + (on ? pp.lora_m_tiles * ((r + kLoraTileR - 1) / kLoraTileR) : 0);
+  }
+  pp.lora_tiles = pp.tile_begin[kMaxLinears];
+  pp.tile_count = reinterpret_cast<unsigned*>(ws + WL.count);
+  pp.sum_groups = lora_sum_in_prep(m) ? 1 : 0;
+}
+
 }  // namespace
+
+LoraDown linear_lora_down(const LinearArgs& a, int i) {
+  int ranks[kMaxLinears] = {0, 0, 0, 0};
+  for (int j = 0; j < a.nlin; ++j)
+    ranks[j] = (a.lin[j].r > 0 && a.lin[j].A != nullptr && a.lin[j].B != nullptr) ? a.lin[j].r : 0;
+  const LinearLayout WL = linear_layout(a.m, a.k, ranks, a.nlin, a.rmsnorm);
+  const uint8_t* ws = static_cast<const uint8_t*>(a.workspace);
+  LoraDown d;
+  if (lora_sum_in_prep(a.m)) {
+    d.t = reinterpret_cast<const float*>(ws + WL.tf[i]);
+    d.parts = 1;
+  } else {
+    d.t = reinterpret_cast<const float*>(ws + WL.t[i]);
+    d.parts = lora_split(a.m, a.k, ranks, a.nlin).groups;
+  }
+  d.part_stride = a.m * ranks[i];
+  return d;
+}
+
+size_t lora_down_workspace_bytes(int64_t m, int64_t k, int r) {
+  const LinearLayout WL = linear_layout(m, k, &r, 1, false);
+  // Only the counters and t / tf of the layout are used; xs and rinv are not.
+  return WL.total - (WL.t[0] - WL.xs);
+}
+
+qerl_status launch_lora_down(const void* x, int64_t m, int64_t k, int64_t ldx, const void* A, int r, void* workspace,
+                             LoraDown* out, int* status, cudaStream_t s) {
+  if (!kernel_attrs_ok()) return QERL_ERR_CUDA;
+  LinearLayout WL = linear_layout(m, k, &r, 1, false);
+  // Drop the unused staging regions: t / tf follow the counters directly.
+  const size_t shift = WL.t[0] - WL.xs;
+  for (int i = 0; i < kMaxLinears; ++i) {
+    WL.t[i] -= shift;
+    WL.tf[i] -= shift;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PrepParams pp{};
+  pp.x = static_cast<const __nv_bfloat16*>(x);
+  pp.ldx = ldx;
+  lora_prep_params(pp, m, k, r, A, ws, WL);
+  pp.row_groups = 0;
+  out->t = pp.sum_groups ? pp.tf[0] : pp.t[0];
+  out->parts = pp.sum_groups ? 1 : pp.groups;
+  out->part_stride = m * r;
+  if (m == 0 || r == 0) return QERL_OK;
+  if (lora_down_on_tc(m)) {  // the sum lands in tf (sum_groups holds for these m)
+    const void* As[1] = {A};
+    const int rs[1] = {r};
+    float* ts[1] = {pp.tf[0]};
+    return lora_down_tc(x, ldx, m, k, As, rs, ts, 1, status, s);
+  }
+  cudaLaunchConfig_t pc{};
+  pc.gridDim = dim3(static_cast<unsigned>(pp.cluster), static_cast<unsigned>(pp.lora_tiles * pp.groups), 1);
+  pc.blockDim = dim3(kPrepThreads, 1, 1);
+  pc.dynamicSmemBytes = kLoraSmemBytes;
+  pc.stream = s;
+  cudaLaunchAttribute pa[1];
+  pa[0].id = cudaLaunchAttributeClusterDimension;
+  pa[0].val.clusterDim.x = static_cast<unsigned>(pp.cluster);
+  pa[0].val.clusterDim.y = 1;
+  pa[0].val.clusterDim.z = 1;
+  pc.attrs = pa;
+  pc.numAttrs = 1;
+  return cudaLaunchKernelEx(&pc, prep_kernel, pp) == cudaSuccess ? QERL_OK : QERL_ERR_CUDA;
+}
 
 size_t linear_workspace_bytes(int64_t m, int64_t k, const int* ranks, int nlin, bool rmsnorm) {
   return linear_layout(m, k, ranks, nlin, rmsnorm).total;
@@ -1897,24 +2253,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   float* rinv = reinterpret_cast<float*>(ws + WL.rinv);
   const int sms = sm_count();
 
-  // Kernel attributes are set once per process (not per call), so calls can be
-  // captured into CUDA graphs.
-  constexpr int kPrepSmemLimit = kSmemLimit - 1024;  // leaves room for the kernel's static shared memory
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemLimit);
-    // The prep grid runs beside the MMA kernel's CTAs (which start early and
-    // hold most of shared memory): the same carveout lets them share an SM.
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                      cudaSharedmemCarveoutMaxShared);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-  });
-  if (attr_err != cudaSuccess) return QERL_ERR_CUDA;
+  if (!kernel_attrs_ok()) return QERL_ERR_CUDA;
 
   // ---- tile shape and pipeline depth (host-side checks before any launch)
   const int split = best_split(n_tiles);
@@ -2114,7 +2453,35 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     pc.numAttrs = 1;
     return cudaLaunchKernelEx(&pc, prep_kernel, q) == cudaSuccess;
   };
-  if (a.rmsnorm) {
+  const bool tc_lora = lora && lora_down_on_tc(M);
+  auto down_tc = [&](const void* xsrc, int64_t ld) {
+    const void* As[kMaxLinears] = {nullptr, nullptr, nullptr, nullptr};
+    for (int i = 0; i < nlin; ++i) As[i] = a.lin[i].A;
+    return lora_down_tc(xsrc, ld, M, K, As, ranks, pp.tf, nlin, status, s);
+  };
+  if (tc_lora) {
+    // Row tasks (noise or RMSNorm, fp16 staging; x~ in bf16 when it differs
+    // from x), then the down-projection on the tensor cores; its sums go
+    // where the consumers of summed partials read them (tf).
+    PrepParams rq = pp;
+    rq.lora_tiles = 0;
+    if (a.rmsnorm) {
+      rq.rmsnorm = 1;
+      rq.w_norm = static_cast<const __nv_bfloat16*>(a.w_norm);
+      rq.Zn = a.Zn;
+      rq.delta = a.delta;
+      rq.z = nullptr;
+      rq.ldz = 0;
+      rq.cluster = 1;
+      rq.row_groups = std::max(M, pp.tiled_rows);
+    }
+    const bool own_xt = a.rmsnorm || a.z != nullptr;
+    rq.xt_out = own_xt ? reinterpret_cast<__nv_bfloat16*>(ws + WL.xt) : nullptr;
+    rq.ldo = K;
+    if (!launch_prep(rq, rq.row_groups, 0, rq.cluster)) return QERL_ERR_CUDA;
+    const qerl_status st = own_xt ? down_tc(ws + WL.xt, K) : down_tc(a.x, a.ldx);
+    if (st != QERL_OK) return st;
+  } else if (a.rmsnorm) {
     // RMSNorm with merged noise: the row tasks normalise h into x~ (staged for
     // the MMA kernel, and written out for the LoRA down-projection), then a
     // second launch runs the LoRA tiles on that x~ with no further noise.
@@ -2185,6 +2552,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.stage_out = static_cast<uint32_t>(tpc * n_tok) * kTileN * 4u <= P.lora ? 1 : 0;
   mp.pair = pair ? 1 : 0;
   mp.xs_rowmajor = xs_rowmajor ? 1 : 0;
+  mp.wt = a.wt ? 1 : 0;
 
   const uint32_t smem_bytes = P.total;
 

@@ -29,6 +29,10 @@ constexpr size_t kPackedBlockBytes = 16384 + 2048;
 size_t packed_weight_bytes(int64_t n, int64_t k);
 qerl_status launch_pack(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
                         cudaStream_t s);
+// The transposed packed layout of an n x k weight (its k x n transpose, the
+// contraction along n), for the input gradient (quantize.cu).
+qerl_status launch_pack_t(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
+                          cudaStream_t s);
 // MXFP4 (quantize.cu): the encoder, and the pack into the same layout with a
 // power-of-two tensor scale (emax1: a zeroed device word of the workspace).
 qerl_status launch_mx_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w, uint8_t* codes,
@@ -65,6 +69,9 @@ struct LinearArgs {  // up to 4 linears sharing x, z and k
   double delta;
   LinearDesc lin[4];
   int nlin;
+  // The weights are packed transposed (qerl_nvfp4_pack_transposed): the
+  // linear then multiplies by W_hat instead of W_hat^T (k is W's n).
+  bool wt;
   void* workspace;
   size_t ws_bytes;
 };
@@ -72,6 +79,41 @@ size_t linear_workspace_bytes(int64_t m, int64_t k, const int* ranks, int nlin, 
 // The normalisation step alone: out [m][ldo] bf16 (linear.cu).
 qerl_status launch_rmsnorm_noise(const void* h, int64_t m, int64_t k, int64_t ldh, const void* w_norm, const float* Zn,
                                  double delta, void* out, int64_t ldo, cudaStream_t s);
+
+// The LoRA down-projection t = x~ . A^T of a linear ([m][r] fp32), as the
+// sum of `parts` partial arrays part_stride floats apart (linear.cu).
+struct LoraDown {
+  const float* t;
+  int parts;
+  int64_t part_stride;
+};
+// Where linear i's down-projection lies in the workspace after launch_lora_linear(a).
+LoraDown linear_lora_down(const LinearArgs& a, int i);
+// The down-projection alone, of x (bf16 [m][ldx], no noise) with A [r][k].
+size_t lora_down_workspace_bytes(int64_t m, int64_t k, int r);
+qerl_status launch_lora_down(const void* x, int64_t m, int64_t k, int64_t ldx, const void* A, int r, void* workspace,
+                             LoraDown* out, int* status, cudaStream_t s);
+
+// The backward pass (backward.cu): dx~, dA, dB of the LoRA linear.
+struct BackwardArgs {
+  const void* xt;  // bf16 [m][ldxt]: the forward's x~
+  int64_t m, k, ldxt;
+  const void* dy;  // bf16 [m][lddy]
+  int64_t n, lddy;
+  const uint8_t* wpacked_t;  // the weight in the transposed packed layout
+  const float* tensor_scale;
+  const void* A;  // bf16 [r][k]
+  const void* B;  // bf16 [n][r]
+  int r;
+  float alpha;
+  void* dxt;  // [m][k]
+  bool dxt_f32;
+  float* dA;  // [r][k] or null
+  float* dB;  // [n][r] or null
+  void* workspace;
+};
+size_t backward_workspace_bytes(int64_t m, int64_t n, int64_t k, int r);
+qerl_status launch_lora_linear_backward(const BackwardArgs& b, cudaStream_t s);
 
 // api.cu: the argument checks shared by every linear entry point.
 qerl_status prepare_linear_group(const void* x, int64_t m, int64_t k, int64_t ldx, const float* z,

@@ -336,7 +336,61 @@ __global__ void __launch_bounds__(kThreads) mx_pack_kernel(const uint8_t* __rest
   }
 }
 
+// The transposed packed layout (the weight's transpose, for the input
+// gradient dx~ = dy . W_hat, whose contraction runs along W's n): one
+// 18432-byte block per (128-row tile t over k, 256-wide stage g over n),
+// blocks in (t, g) order.  Bytes [0, 16384): for row kk of the tile (k =
+// 128 t + kk), the 128 code bytes of n in [256 g, 256 g + 256), n even in the
+// low nibble, 16-byte chunk c at position c ^ (kk % 8).  Bytes [16384,
+// 18432): the E4M3 scale of (n, k) -- scales[n][k / 16], shared by the 16
+// rows of a row group -- at 16384 + (kk / 16) * 256 + (n - 256 g).  Rows
+// past k and n past the weight are zero.  The codes of the stage are first
+// gathered into shared memory (256 n x 64 bytes), then re-paired along n.
+__global__ void __launch_bounds__(kThreads) pack_t_kernel(const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ scales, int n, int k,
+                                                           uint8_t* __restrict__ packed) {
+  __shared__ __align__(16) uint8_t sm[256 * 64];
+  const int g = blockIdx.x, t = blockIdx.y;
+  const int kg = gridDim.x;
+  uint8_t* blk = packed + (static_cast<int64_t>(t) * kg + g) * kPackedBlockBytes;
+  const int row_bytes = k / 2, srow = k / 16;
+  for (int idx = threadIdx.x; idx < 256 * 4; idx += kThreads) {
+    const int nl = idx >> 2, c = idx & 3;
+    const int nn = g * 256 + nl;
+    const int off = t * 64 + c * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (nn < n && off < row_bytes)
+      v = __ldg(reinterpret_cast<const uint4*>(codes + static_cast<int64_t>(nn) * row_bytes + off));
+    *reinterpret_cast<uint4*>(sm + nl * 64 + c * 16) = v;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < 128 * 8; idx += kThreads) {
+    const int kk = idx >> 3, c = idx & 7;
+    const int shift = 4 * (kk & 1);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {  // output byte j of the chunk: n = 32 c + 2 j, 2 j + 1
+      const uint32_t lo = (sm[(32 * c + 2 * j) * 64 + (kk >> 1)] >> shift) & 0xFu;
+      const uint32_t hi = (sm[(32 * c + 2 * j + 1) * 64 + (kk >> 1)] >> shift) & 0xFu;
+      w[j >> 2] |= (lo | (hi << 4)) << (8 * (j & 3));
+    }
+    *reinterpret_cast<uint4*>(blk + kk * 128 + ((c ^ (kk & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  for (int idx = threadIdx.x; idx < 8 * 256; idx += kThreads) {
+    const int rg = idx >> 8, nl = idx & 255;
+    const int nn = g * 256 + nl, sc = t * 8 + rg;
+    blk[16384 + rg * 256 + nl] = (nn < n && sc < srow) ? scales[static_cast<int64_t>(nn) * srow + sc] : 0;
+  }
+}
+
 }  // namespace
+
+qerl_status launch_pack_t(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, uint8_t* packed,
+                          cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((n + 255) / 256), static_cast<unsigned>((k + 127) / 128));
+  pack_t_kernel<<<grid, kThreads, 0, s>>>(codes, scales, static_cast<int>(n), static_cast<int>(k), packed);
+  return cuda_status(cudaGetLastError());
+}
 
 qerl_status launch_mx_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w, uint8_t* codes,
                              uint8_t* scales, int* status, cudaStream_t s) {

@@ -249,6 +249,38 @@ def test_mxfp4_validation(L):
     assert L.qerl_status_string(8) == b"QERL_ERR_RANGE"
 
 
+def test_backward_validation(L):
+    """The backward and the transposed pack reject bad arguments on the host."""
+    E = q.STATUS_NAMES
+    bw = lambda **kw: L.qerl_lora_linear_backward(
+        kw.get("xt", 0x1000), kw.get("m", 4), kw.get("k", 512), kw.get("ldxt", 512), kw.get("dy", 0x2000),
+        kw.get("n", 256), kw.get("lddy", 256), kw.get("wp", 0x3000), kw.get("ts", 0x4000), kw.get("A", 0x5000),
+        kw.get("B", 0x6000), kw.get("r", 16), 32.0, kw.get("dxt", 0x7000), kw.get("dt", q.QERL_BF16),
+        kw.get("dA", 0x8000), kw.get("dB", 0x9000), kw.get("ws", 0x10000), kw.get("wsb", 0), None)
+    assert E[bw(n=96, lddy=96)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[bw(k=48, ldxt=48)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[bw(k=96, ldxt=96)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[bw(r=12)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[bw(r=136)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[bw(B=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[bw(dt=9)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[bw(lddy=128)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[bw(dy=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[bw(xt=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[bw(dy=0x2008)] == "QERL_ERR_MISALIGNED"
+    assert E[bw(ldxt=516)] == "QERL_ERR_MISALIGNED"
+    assert E[bw(wp=0x3004)] == "QERL_ERR_MISALIGNED"
+    assert E[bw()] == "QERL_ERR_WORKSPACE"
+    assert L.qerl_lora_linear_backward_workspace_size(4, 256, 512, 16) > 0
+    pt = lambda **kw: L.qerl_nvfp4_pack_transposed(kw.get("codes", 0x1000), kw.get("scales", 0x2000),
+                                                   kw.get("n", 256), kw.get("k", 512), kw.get("out", 0x3000), None)
+    assert E[pt(n=96)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[pt(k=48)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[pt(n=65536 + 64)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[pt(out=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[pt(codes=0x1008)] == "QERL_ERR_MISALIGNED"
+
+
 def test_product_and_oracle_are_independent():
     pkg = os.path.join(ROOT, "nvfp4_weight_quantized_03_gb300")
     for dirpath, _, files in os.walk(pkg):
