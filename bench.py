@@ -536,6 +536,7 @@ def bench_ours(args):
         out["backward"] = extra_bwd
     if rank == 0 and not args.skip_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_oracle(seconds_budget=args.cpu_budget)
+        out["cpu_baseline"]["all_cores"] = cpu_baseline_oracle_all_cores()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -1083,6 +1084,48 @@ def cpu_baseline_oracle(seconds_budget=15.0):
             "host_cpu_model": host_cpu_model()}
 
 
+def _oracle_slice_worker(idx, nproc, ms, barrier, out_q):
+    """All-cores baseline worker: output rows idx::nproc of every linear of the 7B-shaped layer
+    (oracle-quantized slices), timed after a common barrier on the system-wide monotonic clock."""
+    import oracle
+    layer = []
+    for li, lin in enumerate(wl.QWEN_7B):
+        rows = np.arange(idx, lin.n, nproc)
+        W = wl.weight_f32(lin.n, lin.k, 0, 100, li)[rows]
+        codes, scales, S = oracle.quantize(W)
+        A = wl.lora_A_bits(RANK_R, lin.k, 0, 100, li)
+        B = wl.lora_B_bits(lin.n, RANK_R, 0, 100, li)[rows]
+        layer.append((lin, len(rows), codes, scales, S, A, B))
+    xs = _oracle_inputs(layer, ms, 0)
+    barrier.wait()
+    t0 = time.monotonic()
+    wbytes = _oracle_step(layer, xs, ms, 0)
+    out_q.put((t0, time.monotonic(), wbytes))
+
+
+def cpu_baseline_oracle_all_cores(ms=(1, 8)):
+    """The same oracle on every host core: one spawned process per core, each owning an
+    interleaved slice of every linear's output rows; wall time from the common start to the
+    last finish."""
+    import multiprocessing as mp
+    nproc = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(nproc)
+    out_q = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_slice_worker, args=(i, nproc, tuple(ms), barrier, out_q))
+             for i in range(nproc)]
+    for pr in procs:
+        pr.start()
+    res = [out_q.get() for _ in procs]
+    for pr in procs:
+        pr.join()
+    wall = max(r[1] for r in res) - min(r[0] for r in res)
+    wbytes = sum(r[2] for r in res)
+    return {"value": round(wbytes / wall / 1e9, 5), "unit": UNIT, "cores": nproc, "kind": "oracle",
+            "sample": f"full 7B-shaped layer at decode M in {list(ms)}, output rows split over {nproc} "
+                      f"processes; {wall:.2f} s wall", "host_cpu_model": host_cpu_model()}
+
+
 def bench_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -1111,6 +1154,89 @@ def bench_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def bench_case(args):
+    """One linear shape on its own (the command profilers wrap): `--case M,N,K,R` with N a '+'-joined
+    list for one grouped launch (e.g. 8,18944+18944,3584,32 for gate + up), `--case-kind backward`
+    for the backward of a single linear.  `--case-copies` weight sets (fp32 N(0, 0.02^2) quantized by
+    the library) rotate over `--steps` timed calls after `--warmup` untimed ones, CUDA events on the
+    current stream (or one graph replay with --case-graph).  Prints one JSON line."""
+    m_s, n_s, k_s, r_s = args.case.split(",")
+    m, k, r = int(m_s), int(k_s), int(r_s)
+    ns = [int(v) for v in n_s.split("+")]
+    import nvfp4_weight_quantized_03_gb300 as q
+    q.lib()
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    bwd = args.case_kind == "backward"
+    if bwd and len(ns) != 1:
+        raise SystemExit("--case-kind backward takes one linear")
+    sets = []
+    for _ in range(args.case_copies):
+        members = []
+        for n in ns:
+            W = torch.randn(n, k, device=dev, generator=gen) * 0.02
+            codes, scales, S = q.quantize(W)
+            members.append((q.pack_transposed(codes, scales) if bwd else q.pack(codes, scales), S))
+            del W, codes, scales
+        sets.append(members)
+    x = torch.randn(m, k, device=dev, generator=gen).to(torch.bfloat16)
+    As = [(torch.randn(r, k, device=dev, generator=gen) / k ** 0.5).to(torch.bfloat16) if r else None for _ in ns]
+    Bs = [(torch.randn(n, r, device=dev, generator=gen) * 0.01).to(torch.bfloat16) if r else None for n in ns]
+    z = torch.empty(k, dtype=torch.float32, device=dev)
+    q.check(q.qerl_aqn_sample(z, 1e-2, 0))
+    ys = [torch.empty(m, n, dtype=torch.bfloat16, device=dev) for n in ns]
+    if bwd:
+        dy = (torch.randn(m, ns[0], device=dev, generator=gen) * 0.01).to(torch.bfloat16)
+        dxt = torch.empty(m, k, dtype=torch.bfloat16, device=dev)
+        dA = torch.empty(r, k, dtype=torch.float32, device=dev) if r else None
+        dB = torch.empty(ns[0], r, dtype=torch.float32, device=dev) if r else None
+        ws = q.workspace(q.qerl_lora_linear_backward_workspace_size(m, ns[0], k, r))
+    else:
+        ws = q.workspace(q.qerl_lora_linear_group_workspace_size(
+            m, k, [(wp, S, A_, B_, ALPHA, y) for (wp, S), A_, B_, y in zip(sets[0], As, Bs, ys)]))
+
+    def call(i):
+        members = sets[i % args.case_copies]
+        if bwd:
+            wpt, S = members[0]
+            q.check(q.qerl_lora_linear_backward(x, dy, wpt, S, As[0], Bs[0], ALPHA, dxt, dA, dB, ws))
+        else:
+            q.check(q.qerl_lora_linear_group(
+                x, z, [(wp, S, A_, B_, ALPHA, y) for (wp, S), A_, B_, y in zip(members, As, Bs, ys)], ws))
+
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.case_graph:
+        g = torch.cuda.CUDAGraph()
+        st = torch.cuda.Stream()
+        with torch.cuda.graph(g, stream=st):
+            for i in range(args.steps):
+                call(i)
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+    else:
+        e0.record()
+        for i in range(args.steps):
+            call(i)
+        e1.record()
+    torch.cuda.synchronize()
+    q.check(q.qerl_read_status(ws), "case status")
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    wbytes = sum(ns) * k * BYTES_PER_WEIGHT
+    flops = sum(2.0 * m * n * k + 2.0 * m * r * (k + n) * (2 if bwd else 1) + (2.0 * m * k * r if bwd else 0.0)
+                for n in ns)
+    print(json.dumps({"case": args.case, "kind": args.case_kind, "us_per_call": round(us, 3),
+                      "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
+                      "TFLOPs": round(flops / (us * 1e-6) / 1e12, 2), "graph": args.case_graph,
+                      "calls": args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1125,7 +1251,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ungrouped", action="store_true", help="seven single-linear calls per layer instead of four "
                     "grouped launches")
+    ap.add_argument("--case", default="", help="time one shape instead: M,N,K,R (N '+'-joined for a grouped "
+                    "launch), e.g. 8,18944+18944,3584,32")
+    ap.add_argument("--case-kind", choices=["forward", "backward"], default="forward")
+    ap.add_argument("--case-copies", type=int, default=4, help="weight sets the timed calls rotate over")
+    ap.add_argument("--case-graph", action="store_true", help="replay the timed calls as one CUDA graph")
     args = ap.parse_args()
+    if args.case:
+        bench_case(args)
+        return
     global GROUPED
     GROUPED = not args.ungrouped
     if args.warmup < 3:

@@ -1737,6 +1737,13 @@ struct LdParams {
   float* t[kMaxLinears];
   int lin_of[kMaxLinears];  // blockIdx.z -> linear
   int split;
+  // groups > 1: K is cut into groups * split slices; each cluster (one
+  // group) writes its partial sum to tpart[i] + g * M * r, and the last
+  // cluster of a token tile to finish (counted in counters[], reset by it)
+  // adds the groups in group order into t[i].
+  int groups, m_tiles;
+  float* tpart[kMaxLinears];
+  unsigned* counters;
   int* status;
 };
 
@@ -1764,9 +1771,11 @@ __global__ void __launch_bounds__(kLdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_gen + ring_bytes + 8 * (2 * kLdStages + 1) + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = p.split, sidx = static_cast<int>(blockIdx.x);
-  const int m0 = static_cast<int>(blockIdx.y) * 128;
+  const int mt = static_cast<int>(blockIdx.y) / p.groups, g = static_cast<int>(blockIdx.y) % p.groups;
+  const int m0 = mt * 128;
   const int nk = p.K / 64;
-  const int kc0 = sidx * nk / split, kc1 = (sidx + 1) * nk / split;  // >= 1 chunk each (split <= nk)
+  const int pieces = p.groups * split, piece = g * split + sidx;
+  const int kc0 = piece * nk / pieces, kc1 = (piece + 1) * nk / pieces;  // >= 1 chunk each (pieces <= nk)
   const uint32_t tcols = r16 <= 32 ? 32u : (r16 <= 64 ? 64u : 128u);
 
   if (threadIdx.x == 0) {
@@ -1790,6 +1799,10 @@ __global__ void __launch_bounds__(kLdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem_gen + ring_bytes + 8 * (2 * kLdStages + 1));
+  // Every CTA of this grid is resident and holds its tensor memory: the
+  // linear's MMA kernel may start its prologue (it waits for this grid's
+  // completion before it reads t).
+  griddep_launch_dependents();
 
   if (warp == 0 && lane == 0) {
     int issued = 0;
@@ -1831,7 +1844,7 @@ __global__ void __launch_bounds__(kLdThreads, 1)
   const int row = 32 * warp + lane;
   const int m = m0 + row;
   const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-  float* tout = p.t[li];
+  float* tout = p.groups > 1 ? p.tpart[li] + static_cast<int64_t>(g) * p.M * r : p.t[li];
   if (split == 1) {
     for (int c = 0; c < r16; c += 8) {
       float v[8];
@@ -1856,18 +1869,23 @@ __global__ void __launch_bounds__(kLdThreads, 1)
     }
     cluster_sync_all();
     const int q4 = r16 / 4;
-    for (int it = threadIdx.x; it < 128 * q4; it += kLdThreads) {
-      const int rr = it / q4, c4 = (it % q4) * 4;
-      if (rr % split != sidx) continue;
+    const int my_rows = (128 - sidx + split - 1) / split;
+    for (int it = threadIdx.x; it < my_rows * q4; it += kLdThreads) {
+      const int rr = sidx + split * (it / q4), c4 = (it % q4) * 4;
       const uint32_t off = red + static_cast<uint32_t>((rr * r16 + c4) * 4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q = 0; q < split; ++q) {
-        const float4 v = ld_shared_cluster_f32x4(mapa_shared(off, static_cast<uint32_t>(q)));
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-      }
+      float4 v[kLdMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kLdMaxSplit; ++q)
+        if (q < split) v[q] = ld_shared_cluster_f32x4(mapa_shared(off, static_cast<uint32_t>(q)));
+      float4 acc = v[0];
+#pragma unroll
+      for (int q = 1; q < kLdMaxSplit; ++q)
+        if (q < split) {
+          acc.x += v[q].x;
+          acc.y += v[q].y;
+          acc.z += v[q].z;
+          acc.w += v[q].w;
+        }
       const int mm = m0 + rr;
       if (ok && mm < p.M) {
         const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
@@ -1877,6 +1895,52 @@ __global__ void __launch_bounds__(kLdThreads, 1)
       }
     }
     cluster_sync_all();  // partners are done reading this CTA's partial tile
+  }
+  if (p.groups > 1) {
+    // Rank sidx of every group's cluster wrote rows sidx, sidx + split, ...:
+    // the last of them to finish adds those rows over the groups in group
+    // order (release: this CTA's barrier orders its writes before the fence
+    // and atomic of thread 0; acquire: the fence after it).
+    __shared__ unsigned last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned* cnt = p.counters + (static_cast<int>(blockIdx.z) * p.m_tiles + mt) * split + sidx;
+      __threadfence();
+      const unsigned done = atomicAdd(cnt, 1u);
+      last = done == static_cast<unsigned>(p.groups - 1) ? 1u : 0u;
+      if (last) {
+        __threadfence();
+        *cnt = 0u;
+      }
+    }
+    __syncthreads();
+    if (last && ok) {
+      const float* tp = p.tpart[li];
+      const int r4 = r / 4;
+      const int my_rows = (128 - sidx + split - 1) / split;
+      const int64_t gstride = static_cast<int64_t>(p.M) * r;
+      for (int it = threadIdx.x; it < my_rows * r4; it += kLdThreads) {
+        const int mm = m0 + sidx + split * (it / r4), c4 = (it % r4) * 4;
+        if (mm >= p.M) break;
+        const float* src = tp + static_cast<int64_t>(mm) * r + c4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int g0 = 0; g0 < p.groups; g0 += 4) {
+          float4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (g0 + u < p.groups) v[u] = __ldcg(reinterpret_cast<const float4*>(src + (g0 + u) * gstride));
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (g0 + u < p.groups) {
+              acc.x += v[u].x;
+              acc.y += v[u].y;
+              acc.z += v[u].z;
+              acc.w += v[u].w;
+            }
+        }
+        *reinterpret_cast<float4*>(p.t[li] + static_cast<int64_t>(mm) * r + c4) = acc;
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1951,7 +2015,8 @@ int resident_clusters(int sp) {
 // The tensor-core LoRA down-projection (lora_down_tc_kernel) of up to four
 // linears sharing X (bf16 [M][ldx]): t[i] fp32 [M][r[i]] (r[i] == 0: skipped).
 qerl_status lora_down_tc(const void* x, int64_t ldx, int64_t M, int64_t K, const void* const* A, const int* r,
-                         float* const* t, int nlin, int* status, cudaStream_t s) {
+                         float* const* t, float* const* tpart, int max_groups, unsigned* counters, int nlin,
+                         int* status, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
@@ -1984,12 +2049,21 @@ qerl_status lora_down_tc(const void* x, int64_t ldx, int64_t M, int64_t K, const
   if (nz == 0 || M == 0) return QERL_OK;
   const int m_tiles = static_cast<int>((M + 127) / 128);
   const int nk = static_cast<int>(K / 64);
-  // Split K over a cluster until the grid covers the SMs once.
-  int split = (sm_count() + m_tiles * nz - 1) / (m_tiles * nz);
-  split = std::max(1, std::min(split, std::min(kLdMaxSplit, nk)));
+  // Split K over a cluster, then over groups of clusters, until the grid
+  // covers the SMs once (a CTA streams 20 KB per K chunk into one SM, so few
+  // CTAs over a long K are bound by that SM's ingress).
+  const int want = (sm_count() + m_tiles * nz - 1) / (m_tiles * nz);
+  int split = std::max(1, std::min(want, std::min(kLdMaxSplit, nk)));
+  int groups = (want + split - 1) / split;
+  groups = std::max(1, std::min({groups, max_groups, nk / split}));
+  if (m_tiles * nz * split > kMaxLoraCounters) groups = 1;  // one completion counter per (tile, cluster rank)
   lp.split = split;
+  lp.groups = groups;
+  lp.m_tiles = m_tiles;
+  lp.counters = counters;
+  for (int i = 0; i < nlin; ++i) lp.tpart[i] = tpart != nullptr ? tpart[i] : nullptr;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(split), static_cast<unsigned>(m_tiles), static_cast<unsigned>(nz));
+  cfg.gridDim = dim3(static_cast<unsigned>(split), static_cast<unsigned>(m_tiles * groups), static_cast<unsigned>(nz));
   cfg.blockDim = dim3(kLdThreads, 1, 1);
   cfg.dynamicSmemBytes = ld_smem_bytes(r16max);
   cfg.stream = s;
@@ -2003,8 +2077,10 @@ qerl_status lora_down_tc(const void* x, int64_t ldx, int64_t M, int64_t K, const
   return cudaLaunchKernelEx(&cfg, lora_down_tc_kernel, maps, lp) == cudaSuccess ? QERL_OK : QERL_ERR_CUDA;
 }
 
-// Above this many tokens the LoRA down-projection runs on the tensor cores.
-__host__ inline bool lora_down_on_tc(int64_t m) { return m > 128; }
+// Above 64 tokens (where the consumers read one summed t) the LoRA
+// down-projection runs on the tensor cores: on CUDA cores its cost grows with
+// M * K and dominated the 65-128-token launches.
+__host__ inline bool lora_down_on_tc(int64_t m) { return lora_sum_in_prep(m); }
 
 struct LinearLayout {
   size_t xs, rinv, t[kMaxLinears], tf[kMaxLinears], count, xt, total;
@@ -2140,7 +2216,8 @@ qerl_status launch_lora_down(const void* x, int64_t m, int64_t k, int64_t ldx, c
     const void* As[1] = {A};
     const int rs[1] = {r};
     float* ts[1] = {pp.tf[0]};
-    return lora_down_tc(x, ldx, m, k, As, rs, ts, 1, status, s);
+    float* tps[1] = {pp.t[0]};
+    return lora_down_tc(x, ldx, m, k, As, rs, ts, tps, pp.groups, pp.tile_count, 1, status, s);
   }
   cudaLaunchConfig_t pc{};
   pc.gridDim = dim3(static_cast<unsigned>(pp.cluster), static_cast<unsigned>(pp.lora_tiles * pp.groups), 1);
@@ -2457,7 +2534,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   auto down_tc = [&](const void* xsrc, int64_t ld) {
     const void* As[kMaxLinears] = {nullptr, nullptr, nullptr, nullptr};
     for (int i = 0; i < nlin; ++i) As[i] = a.lin[i].A;
-    return lora_down_tc(xsrc, ld, M, K, As, ranks, pp.tf, nlin, status, s);
+    return lora_down_tc(xsrc, ld, M, K, As, ranks, pp.tf, pp.t, pp.groups, pp.tile_count, nlin, status, s);
   };
   if (tc_lora) {
     // Row tasks (noise or RMSNorm, fp16 staging; x~ in bf16 when it differs
