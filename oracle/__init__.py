@@ -95,6 +95,18 @@ def lib():
             L.orc_lora_linear.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p, ctypes.c_float, _i64,
                                           _f32p, _i64, _u16p, _u16p, ctypes.c_int, ctypes.c_float,
                                           ctypes.c_int, _i64p, _i64, _f64p]
+            L.orc_nf4_levels.restype = None
+            L.orc_nf4_levels.argtypes = [_f64p]
+            L.orc_nf4_encode.restype = ctypes.c_uint8
+            L.orc_nf4_encode.argtypes = [ctypes.c_float]
+            L.orc_nf4_quantize.restype = ctypes.c_int
+            L.orc_nf4_quantize.argtypes = [_f32p, _i64, _i64, _i64, _u8p, _u8p, _f32p]
+            L.orc_nf4_dequant.restype = None
+            L.orc_nf4_dequant.argtypes = [_u8p, _u8p, ctypes.c_float, _i64, _i64, _f64p]
+            L.orc_nf4_lora_linear.restype = ctypes.c_int
+            L.orc_nf4_lora_linear.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p, ctypes.c_float, _i64,
+                                              _f32p, _i64, _u16p, _u16p, ctypes.c_int, ctypes.c_float,
+                                              ctypes.c_int, _i64p, _i64, _f64p]
             L.orc_mxfp4_lora_linear.restype = ctypes.c_int
             L.orc_mxfp4_lora_linear.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p, _i64,
                                                 _f32p, _i64, _u16p, _u16p, ctypes.c_int, ctypes.c_float,
@@ -309,16 +321,55 @@ def lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alph
     A_bits [r, k] uint16 bf16; B_bits [n, r] uint16 bf16
     (the shapes of Eq. 2: A in R^{r x k}, B in R^{d x r}).
     """
-    return _linear(False, x_bits, codes, scales, S, z, A_bits, B_bits, alpha, round_xt, cols)
+    return _linear("nvfp4", x_bits, codes, scales, S, z, A_bits, B_bits, alpha, round_xt, cols)
+
+
+def nf4_levels() -> np.ndarray:
+    """The 16 NF4 levels, ascending (code c -> level c; code 7 is 0)."""
+    out = np.empty(16, dtype=np.float64)
+    lib().orc_nf4_levels(_ptr(out, _f64p))
+    return out
+
+
+def nf4_encode(q: float) -> int:
+    return int(lib().orc_nf4_encode(float(q)))
+
+
+def nf4_quantize(W: np.ndarray):
+    """NF4 levels with NVFP4-style dual scaling: W [n, k] fp32 -> (codes [n, k/2], E4M3 scales
+    [n, k/16], tensor scale S)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    n, k = W.shape
+    codes = np.zeros((n, k // 2), dtype=np.uint8)
+    scales = np.zeros((n, k // 16), dtype=np.uint8)
+    S = np.zeros(1, dtype=np.float32)
+    _check(lib().orc_nf4_quantize(_ptr(W, _f32p), n, k, k, _ptr(codes, _u8p), _ptr(scales, _u8p), _ptr(S, _f32p)))
+    return codes, scales, float(S[0])
+
+
+def nf4_dequant(codes: np.ndarray, scales: np.ndarray, S: float) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    n, k2 = codes.shape
+    out = np.empty((n, 2 * k2), dtype=np.float64)
+    lib().orc_nf4_dequant(_ptr(codes, _u8p), _ptr(scales, _u8p), float(S), n, 2 * k2, _ptr(out, _f64p))
+    return out
+
+
+def nf4_lora_linear(x_bits, codes, scales, S, z=None, A_bits=None, B_bits=None, alpha=0.0,
+                    round_xt=True, cols=None) -> np.ndarray:
+    """The same linear over an NF4 weight (codes [n, k/2], E4M3 scales [n, k/16], tensor scale S)."""
+    return _linear("nf4", x_bits, codes, scales, S, z, A_bits, B_bits, alpha, round_xt, cols)
 
 
 def mxfp4_lora_linear(x_bits, codes, scales, z=None, A_bits=None, B_bits=None, alpha=0.0,
                       round_xt=True, cols=None) -> np.ndarray:
     """The same linear over an MXFP4 weight: codes [n, k/2], E8M0 scales [n, k/32]."""
-    return _linear(True, x_bits, codes, scales, 1.0, z, A_bits, B_bits, alpha, round_xt, cols)
+    return _linear("mxfp4", x_bits, codes, scales, 1.0, z, A_bits, B_bits, alpha, round_xt, cols)
 
 
-def _linear(mx, x_bits, codes, scales, S, z, A_bits, B_bits, alpha, round_xt, cols):
+def _linear(fmt, x_bits, codes, scales, S, z, A_bits, B_bits, alpha, round_xt, cols):
+    mx = fmt == "mxfp4"
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scales = np.ascontiguousarray(scales, dtype=np.uint8)
@@ -345,6 +396,9 @@ def _linear(mx, x_bits, codes, scales, S, z, A_bits, B_bits, alpha, round_xt, co
     if mx:
         _check(lib().orc_mxfp4_lora_linear(_ptr(x_bits, _u16p), m, k, k, _ptr(codes, _u8p), _ptr(scales, _u8p),
                                            n, *rest))
+    elif fmt == "nf4":
+        _check(lib().orc_nf4_lora_linear(_ptr(x_bits, _u16p), m, k, k, _ptr(codes, _u8p), _ptr(scales, _u8p),
+                                         float(S), n, *rest))
     else:
         _check(lib().orc_lora_linear(_ptr(x_bits, _u16p), m, k, k, _ptr(codes, _u8p), _ptr(scales, _u8p),
                                      float(S), n, *rest))

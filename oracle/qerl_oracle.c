@@ -309,6 +309,111 @@ void orc_mxfp4_dequant(const uint8_t* codes, const uint8_t* scales, int64_t n, i
 }
 
 /* ------------------------------------------------------------------------ */
+/* NF4, the QLoRA format the digest sets against NVFP4 ([QeRL] "NVFP4      */
+/* Quantization", other 4-bit formats, and the QLoRA discussion: levels at   */
+/* quantiles of the Gaussian, recovered through a lookup table).  The digest */
+/* gives no construction; reading (the QLoRA one): 16 levels, ascending, are */
+/* standard-normal quantiles at evenly spaced probabilities with an exact    */
+/* zero -- 8 positive levels Phi^-1(1/2 + (i/8)(p - 1/2)), i = 1..8, 7       */
+/* negative levels -Phi^-1(1/2 + (i/7)(p - 1/2)), i = 1..7, and 0, with      */
+/* p = ((1 - 1/32) + (1 - 1/30)) / 2 -- each divided by the largest, so they */
+/* span [-1, 1]; code c (0..15) is the c-th level (code 7 = 0).  Scaling     */
+/* (reading): NVFP4's dual scaling with a level range of 1 instead of 6:     */
+/* S = amax_t / 448 (1 if 0), block scale s = E4M3_RNE_SAT(amax_b / S) per   */
+/* 16, element code = the level nearest to q = w / (S dec(s)) (one fp32     */
+/* division), decided against the fp32-rounded midpoints m_c of adjacent    */
+/* levels: c = #{ m_c <= q } (a quotient on a midpoint goes up).             */
+/* Phi^-1 here: bisection of Phi(x) = erfc(-x / sqrt 2) / 2 to the last bit. */
+/* ------------------------------------------------------------------------ */
+static double norm_ppf_bisect(double prob)
+{
+    double lo = -40.0, hi = 40.0;
+    for (int it = 0; it < 4000; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        if (mid == lo || mid == hi) break;
+        if (0.5 * erfc(-mid / sqrt(2.0)) < prob) lo = mid; else hi = mid;
+    }
+    return 0.5 * (lo + hi);
+}
+
+void orc_nf4_levels(double* out16)
+{
+    const double p = ((1.0 - 1.0 / 32.0) + (1.0 - 1.0 / 30.0)) / 2.0;
+    const double top = norm_ppf_bisect(p);
+    for (int i = 1; i <= 7; ++i) out16[7 - i] = -norm_ppf_bisect(0.5 + (i / 7.0) * (p - 0.5)) / top;
+    out16[7] = 0.0;
+    for (int i = 1; i <= 8; ++i) out16[7 + i] = norm_ppf_bisect(0.5 + (i / 8.0) * (p - 0.5)) / top;
+}
+
+uint8_t orc_nf4_encode(float q)
+{
+    double lv[16];
+    orc_nf4_levels(lv);
+    uint8_t c = 0;
+    for (int i = 0; i < 15; ++i) {
+        const float mid = (float)((lv[i] + lv[i + 1]) / 2.0);
+        if (mid <= q) c = (uint8_t)(i + 1);
+    }
+    return c;
+}
+
+int orc_nf4_quantize(const float* W, int64_t n, int64_t k, int64_t ldw, uint8_t* codes, uint8_t* scales,
+                     float* S_out)
+{
+    if (n < 0 || k < 0 || ldw < k) return ORC_ERR_ARG;
+    if (k % 32 != 0) return ORC_ERR_SHAPE;
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < k; ++j) {
+            if (!isfinite(W[i * ldw + j])) return ORC_ERR_NONFINITE;
+            if (fabsf(W[i * ldw + j]) > amax) amax = fabsf(W[i * ldw + j]);
+        }
+    float S = amax / 448.0f;
+    if (S == 0.0f) S = 1.0f;
+    *S_out = S;
+    double lv[16];
+    orc_nf4_levels(lv);
+    float mids[15];
+    for (int i = 0; i < 15; ++i) mids[i] = (float)((lv[i] + lv[i + 1]) / 2.0);
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t b = 0; b < k / 16; ++b) {
+            const float* wb = W + i * ldw + b * 16;
+            float amax_b = 0.0f;
+            for (int t = 0; t < 16; ++t)
+                if (fabsf(wb[t]) > amax_b) amax_b = fabsf(wb[t]);
+            const uint8_t s = orc_e4m3_encode_pos(amax_b / S);
+            const float sc = S * (float)orc_e4m3_decode(s);
+            scales[i * (k / 16) + b] = s;
+            for (int t = 0; t < 16; t += 2) {
+                uint8_t cc[2] = {7, 7};
+                for (int u = 0; u < 2; ++u) {
+                    if (sc == 0.0f) continue;
+                    const float q = wb[t + u] / sc;
+                    uint8_t c = 0;
+                    for (int m = 0; m < 15; ++m)
+                        if (mids[m] <= q) c = (uint8_t)(m + 1);
+                    cc[u] = c;
+                }
+                codes[i * (k / 2) + (b * 16 + t) / 2] = (uint8_t)(cc[0] | (cc[1] << 4));
+            }
+        }
+    return ORC_OK;
+}
+
+/* W_hat[i][j] = S * dec(scale[i][j/16]) * level(code[i][j]), fp64. */
+void orc_nf4_dequant(const uint8_t* codes, const uint8_t* scales, float S, int64_t n, int64_t k, double* W_hat)
+{
+    double lv[16];
+    orc_nf4_levels(lv);
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < k; ++j) {
+            const uint8_t byte = codes[i * (k / 2) + j / 2];
+            const uint8_t c = (j & 1) ? (byte >> 4) : (byte & 0xF);
+            W_hat[i * k + j] = (double)S * (orc_e4m3_decode(scales[i * (k / 16) + j / 16]) * lv[c]);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
 /* AQN schedule: [QeRL] Eq. 8, sigma(k) = s0 * (s1/s0)^((k-1)/(K-1)),        */
 /* k = 1..K.  Library stage index `stage` = k - 1 (0..K-1); a negative stage */
 /* is the warm-up stage of Algorithm 1 with sigma = 0; stages past the last  */
@@ -505,6 +610,18 @@ static void mxfp4_row(const uint8_t* codes, const uint8_t* scales, float S, int6
     }
 }
 
+/* NF4: W_hat[c][j] = S * dec_E4M3(scale[c][j/16]) * level(code[c][j]). */
+static void nf4_row(const uint8_t* codes, const uint8_t* scales, float S, int64_t k, int64_t c, double* wrow)
+{
+    double lv[16];
+    orc_nf4_levels(lv);
+    for (int64_t kk = 0; kk < k; ++kk) {
+        uint8_t byte = codes[c * (k / 2) + kk / 2];
+        uint8_t code = (kk & 1) ? (byte >> 4) : (byte & 0xF);
+        wrow[kk] = (double)S * (orc_e4m3_decode(scales[c * (k / 16) + kk / 16]) * lv[code]);
+    }
+}
+
 static int lora_linear_core(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
                             const uint8_t* codes, const uint8_t* scales, float S, orc_row_dequant deq, int64_t n,
                             const float* z, int64_t ldz, const uint16_t* A, const uint16_t* B, int r, float alpha,
@@ -576,6 +693,17 @@ int orc_mxfp4_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
                           int round_xt, const int64_t* cols, int64_t ncols, double* y)
 {
     return lora_linear_core(x, m, k, ldx, codes, scales, 1.0f, mxfp4_row, n, z, ldz, A, B, r, alpha, round_xt,
+                            cols, ncols, y);
+}
+
+/* The same linear over an NF4 weight (codes [n][k/2], E4M3 scales [n][k/16], */
+/* tensor scale S, as orc_nf4_quantize writes them).                          */
+int orc_nf4_lora_linear(const uint16_t* x, int64_t m, int64_t k, int64_t ldx,
+                        const uint8_t* codes, const uint8_t* scales, float S, int64_t n,
+                        const float* z, int64_t ldz, const uint16_t* A, const uint16_t* B, int r, float alpha,
+                        int round_xt, const int64_t* cols, int64_t ncols, double* y)
+{
+    return lora_linear_core(x, m, k, ldx, codes, scales, S, nf4_row, n, z, ldz, A, B, r, alpha, round_xt,
                             cols, ncols, y);
 }
 
