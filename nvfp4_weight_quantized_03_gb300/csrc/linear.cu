@@ -495,7 +495,6 @@ constexpr int kRawK = 256;        // K per weight-load stage: 128 contiguous byt
 constexpr int kSub = kRawK / kStageK;                  // MMA stages per weight stage
 constexpr int kCodesRawBytes = kTileN * kRawK / 2;     // 16384
 constexpr int kRawSlotBytes = kCodesRawBytes + kTileN * kRawK / 16;  // + 2048 scale bytes: one packed block
-constexpr int kAStageBytes = kTileN * kStageK * 2;     // 16384 (fp16, shared-memory A operand)
 constexpr int kAStageCols = kStageK / 2;               // 32 TMEM columns (fp16 pairs, tensor-memory A operand)
 constexpr int kLoraChunkK = 64;                        // r is processed in 64-wide chunks (one 128-B swizzle atom)
 constexpr int kBtChunkBytes = kTileN * 128;            // B^T chunk: 128 rows x 64 bf16
@@ -525,7 +524,7 @@ struct LinearSlot {
 };
 
 struct MmaParams {
-  const __half* xs;        // staged x~ (fp16 * 2^e_m): tiled with kTmemA, else [M][K]
+  const __half* xs;        // staged x~ (fp16 * 2^e_m): tiled up to 128 tokens, else [M][K]
   const float* rinv;
   LinearSlot lin[kMaxLinears];
   int nlin;
@@ -534,18 +533,18 @@ struct MmaParams {
   int n_tok;       // tokens per tile (MMA N), multiple of 16, <= 256
   int split;       // K split across the cluster (gridDim.x), in weight stages
   int raw_stages;  // weight-stage ring depth
-  int ab_stages;   // dequantized-A ring depth (also the activation ring's without kTmemA)
-  int b_stages;    // kTmemA, !coupled: activation ring depth in 64-wide slabs (one barrier pair each; a multiple of kSub)
-  int coupled;     // kTmemA: a weight stage's activation slabs travel with its codes (same barrier, raw ring)
+  int ab_stages;   // tensor-memory A ring depth, in MMA stages
+  int b_stages;    // !coupled: activation ring depth in 64-wide slabs (one barrier pair each; a multiple of kSub)
+  int coupled;     // a weight stage's activation slabs travel with its codes (same barrier, raw ring)
   int issuers;     // MMA-issuing threads, each with its own accumulator
   int t_groups;    // t holds this many partial sums [t_groups][M][r], added in order
-  uint32_t off_raw, off_a, off_b, off_lora, off_tstage, off_sm, off_bars;
+  uint32_t off_raw, off_b, off_lora, off_tstage, off_sm, off_bars;
   uint32_t raw_b_bytes;  // coupled: activation bytes per weight stage (kSub slabs)
   uint32_t col_a;  // TMEM column of the A stages (accumulators: issuer i at i * n_tok)
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
   int wave;        // CTAs per wave (one per SM) when split == 1, else 0
   int stage_out;   // the widest output tile (fp32) fits in the idle ring: staged stores
-  // kTmemA, more than 64 tokens: a CTA takes a pair of adjacent 128-row tiles
+  // More than 64 tokens: a CTA takes a pair of adjacent 128-row tiles
   // of one linear (grid y counts pairs), so every activation slab it receives
   // serves 256 weight rows.  Dequant group g and issuer g own tile g; the
   // tensor-memory A slots are handed over per MMA stage (one per tile and
@@ -732,13 +731,11 @@ __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, const Linear
     }
 }
 
-// kTmemA: the dequantized weight operand goes to tensor memory (tcgen05.st),
-// each MMA reads it from there, and `issuers` threads issue MMAs for
-// interleaved stages into their own accumulators (an MMA occupies its issuing
-// thread for far longer than the tensor pipe needs for a 128 x n_tok x 16
-// product, so one issuer cannot keep the pipe busy at decode token counts).
-// Otherwise (256-token tiles) the operand is staged in shared memory and one
-// thread issues.
+// The dequantized weight operand goes to tensor memory (tcgen05.st), each MMA
+// reads it from there, and `issuers` threads issue MMAs for interleaved
+// stages into their own accumulators (an MMA occupies its issuing thread for
+// far longer than the tensor pipe needs for a 128 x n_tok x 16 product, so
+// one issuer cannot keep the pipe busy at decode token counts).
 // One MMA stage (64 K) of weight row `row` of a staged packed block at
 // `slot` -> 32 fp16 pairs o[] (element pairs along K), exact: an E2M1 value
 // times an E4M3 scale fits fp16.  Forward layout: one scale per 16 K, as
@@ -782,7 +779,6 @@ __device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q,
   }
 }
 
-template <bool kTmemA>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ BtMaps tm_bls,
                const MmaParams p) {
@@ -801,7 +797,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const uint32_t acc_full = bars + 8u * (kB2 + 2);
   const uint32_t tmem_holder = bars + 8u * (kB2 + 3);
   const uint32_t t_full = bars + 8u * (kB2 + 4);
-  // kTmemA: the activation ring has its own depth and barriers.
+  // The activation ring has its own depth and barriers.
   auto b_full = [&](int s) { return bars + 8u * (kB2 + 8 + s); };
   auto b_empty = [&](int s) { return bars + 8u * (kB2 + 8 + kMaxB + s); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_gen + p.off_bars + 8 * (kB2 + 3) + 4);
@@ -832,19 +828,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
       mbar_init_a(raw_full(s), 1);  // producer expect_tx
-      // kTmemA: the four dequant warps of the stage's group (+ each issuer's
+      // The four dequant warps of the stage's group (+ each issuer's
       // commit when the activation slabs ride in the slot); pair mode: the
       // groups of both tiles; else all eight.
-      mbar_init_a(raw_empty(s), kTmemA ? (p.pair ? 4 * ntl : 4 + (p.coupled ? NI : 0)) : 8);
+      mbar_init_a(raw_empty(s), p.pair ? 4 * ntl : 4 + (p.coupled ? NI : 0));
     }
-    if (kTmemA && p.pair) {
+    if (p.pair) {
       // One barrier pair per (tile, MMA stage) slot of tensor memory: the
       // tile's four dequant warps arrive, its issuer commits.
       for (int w = 0; w < 2 * kSub; ++w) {
         mbar_init_a(ab_full(w), 4);
         mbar_init_a(ab_empty(w), 1);
       }
-    } else if (kTmemA) {
+    } else {
       // One barrier pair per weight stage of the tensor-memory ring (kSub MMA
       // stages): the four warps of the dequant group that wrote it arrive
       // once each, every issuer commits once.
@@ -852,14 +848,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         mbar_init_a(ab_full(w), 4);
         mbar_init_a(ab_empty(w), NI);
       }
-    } else {
-      for (int s = 0; s < AS; ++s) {
-        mbar_init_a(ab_full(s), 9);   // 8 dequant warps + activation producer expect_tx
-        mbar_init_a(ab_empty(s), 1);  // tcgen05.commit
-      }
     }
-    if (kTmemA)
-      for (int s = 0; s < BS; ++s) {
+    for (int s = 0; s < BS; ++s) {
         mbar_init_a(b_full(s), 1);                  // producer expect_tx
         mbar_init_a(b_empty(s), p.pair ? ntl : 1);  // tcgen05.commit of each issuer reading the slab
       }
@@ -881,7 +871,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWeightWarp && lane == 0) {
-    if (!kTmemA || p.xs_rowmajor) tma_prefetch_desc(&tm_xs);
+    if (p.xs_rowmajor) tma_prefetch_desc(&tm_xs);
     if (L.r > 0) tma_prefetch_desc(tm_bl);
   }
   tc_fence_before();
@@ -898,7 +888,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // Coupled: the stage's activation slabs follow in the same queue
     // position and complete on the same barrier; they come from the
     // preceding kernel.
-    const bool coupled = kTmemA && p.coupled;
+    const bool coupled = p.coupled != 0;
     const uint8_t* wtile = L.wpacked + static_cast<int64_t>(n0 / kTileN) * raw_total * kRawSlotBytes;
     const int64_t tile_stride = static_cast<int64_t>(raw_total) * kRawSlotBytes;  // next tile's blocks (pair mode)
     const int kslabs = p.K / kStageK;
@@ -907,19 +897,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // blocks kPrefetch stages ahead are prefetched into L2 (bounded by L2
     // capacity, not shared memory) and the ring refills from L2.
     constexpr int kPrefetch = kPrefetchStages;
-    if (!kTmemA && lane == 0)
-      for (int i = 0; i < min(kPrefetch, nraw); ++i)
-        bulk_prefetch_l2(wtile + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes);
     auto xbytes_of = [&](int rst) {
       return coupled ? static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128) : 0u;
     };
-    // kTmemA: the first ring of weight blocks (and L2 prefetches further
+    // The first ring of weight blocks (and L2 prefetches further
     // ahead) is requested at once: the weights were written before the
     // preceding kernel of this call started.  Coupled: the stages' activation
     // slabs, and the arrivals that let them complete, follow once that kernel
     // has finished.
-    const int early = kTmemA ? min(RS, nraw) : 0;
-    if (kTmemA && lane == 0) {
+    const int early = min(RS, nraw);
+    if (lane == 0) {
       for (int i = 0; i < min(kPrefetch, nraw); ++i)
         for (int t = 0; t < ntl; ++t)
           bulk_prefetch_l2(wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes);
@@ -965,7 +952,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // The tile the next wave runs (one CTA per SM: `wave` CTAs later) gets
       // its first blocks prefetched into L2 now, so that CTA does not start
       // on a cold stream.
-      if (kTmemA && p.split == 1 && p.wave > 0) {
+      if (p.split == 1 && p.wave > 0) {
         const int ty = static_cast<int>(blockIdx.y) + p.wave;
         int gj = 0;
         while (gj + 1 < p.nlin && ty >= p.lin[gj + 1].tile_begin) ++gj;
@@ -980,7 +967,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp == kActWarp) {
     // ------------------------------------------------------------ activation producer
     griddep_wait();  // the staged activations are written by the preceding kernel
-    if constexpr (kTmemA) {
+    {
       if (!p.coupled && lane == 0) {
         // One bulk copy per 64-wide K slab (tiled layout: the slabs of
         // consecutive MMA stages are contiguous), each slot with its own full
@@ -1008,14 +995,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           }
         }
       }
-    } else if (!kTmemA && lane == 0) {
-      for (int j = 0; j < nmma; ++j) {
-        const int s = j % AS;
-        const uint32_t ph = (j / AS) & 1;
-        if (!mbar_wait_a(ab_empty(s), ph ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx_a(ab_full(s), static_cast<uint32_t>(p.n_tok) * 128u);
-        tma_load_2d(sbase + p.off_b + s * (p.n_tok * 128), &tm_xs, (mma_begin + j) * kStageK, m0, ab_full(s));
-      }
     }
   } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kMaxIssuers) {
     // ------------------------------------------------------------ MMA issuers
@@ -1024,7 +1003,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
       const uint32_t d_acc = tmem_base + static_cast<uint32_t>(ii * p.n_tok);
       uint32_t acc = 0;
-      if (kTmemA && p.pair) {
+      if (p.pair) {
         // Pair mode: this issuer owns tile ii of the pair (its accumulator,
         // its tensor-memory A slot per MMA stage q: ab_*(ii * kSub + q)) and
         // reads every activation slab in order; each slab's empty barrier
@@ -1061,7 +1040,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           __syncwarp();
           if (!ok) break;
         }
-      } else if constexpr (kTmemA) {
+      } else {
         // The whole warp runs the loop (waits, addresses and descriptors are
         // warp-uniform); lane 0 issues the MMAs and their commits.  A weight
         // stage holds kSub x 4 MMAs (u = 4 q + kk: MMA stage q, K step kk);
@@ -1141,23 +1120,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           }
           if (++rs == RS) rs = 0;
         }
-      } else if (lane == 0) {
-        // Stage s is always served by issuer s % NI (AS is a multiple of NI),
-        // so each barrier has a single waiter that is never two phases ahead.
-        for (int j = ii; j < nmma; j += NI) {
-          const int s = j % AS;
-          const uint32_t ph = (j / AS) & 1;
-          if (!mbar_wait_a(ab_full(s), ph, abort_flag, p.status)) break;
-          const uint32_t b_addr = sbase + p.off_b + s * (p.n_tok * 128);
-          tc_fence_after();
-          const uint32_t a_addr = sbase + p.off_a + s * kAStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < kStageK / 16; ++kk) {
-            tc_mma_f16(d_acc, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc, acc);
-            acc = 1;
-          }
-          tc_commit(ab_empty(s));
-        }
       }
       if (lane == 0) {
         // The LoRA up-projection goes last, so a slow producer of t never
@@ -1208,7 +1170,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // ------------------------------------------------------------ dequant warps
     const int dw = warp - kDeqWarp0;
     const bool wt = p.wt != 0;
-    if (kTmemA && p.pair) {
+    if (p.pair) {
       // Pair mode: group g = dw / 4 dequantizes tile g of the pair (a thread
       // is one weight row of it), every weight stage, and hands each MMA
       // stage's 32 TMEM columns over as soon as they are stored, so the next
@@ -1249,7 +1211,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           }
         }
       }
-    } else if constexpr (kTmemA) {
+    } else {
       // Two groups of four warps (one per TMEM lane quadrant, warp % 4) take
       // alternate weight stages: group g = dw / 4 dequantizes stages g, g + 2,
       // ...  A thread is one weight row (its lane of the quadrant) and covers
@@ -1301,79 +1263,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if (w >= AW) {
           w -= AW;
           aph ^= 1;
-        }
-      }
-    } else {
-      // 16 rows per warp, two K-halves per row pair; every MMA stage is
-      // handed over as soon as it is written to shared memory.
-      const int row = 16 * dw + (lane & 15);
-      const int half = lane >> 4;
-      const uint32_t arow = static_cast<uint32_t>(row * 128);
-      int j = 0, as = 0, s = 0;
-      uint32_t aph = 0, ph = 0;
-      for (int i = 0; i < nraw; ++i) {
-        if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
-        const uint32_t slot = sbase + p.off_raw + s * kRawSlotBytes;
-        const uint32_t crow = slot + row * 128;
-        const uint32_t srow = slot + kCodesRawBytes + half * 256 + row * 2;
-        // This thread's codes (16 B per 64-wide stage: chunk 2q + half of the
-        // row, 128-byte swizzle) and scale pairs for the whole weight stage.
-        uint4 cw[kSub];
-        uint32_t sc[kSub];
-#pragma unroll
-        for (int q = 0; q < kSub; ++q) {
-          cw[q] = lds128(crow + (((2 * q + half) ^ (row & 7)) << 4));
-          sc[q] = lds16(srow + 2 * q * 256);  // scale pair 2q + half: blocks 4q + 2half, +1
-        }
-        // The whole weight stage is converted first, with no waits in between,
-        // so the conversions of its (up to) kSub MMA stages overlap.
-        uint32_t o[kSub][16];
-#pragma unroll
-        for (int q = 0; q < kSub; ++q) {
-          const __half2 s01 = e4m3x2_to_half2(sc[q]);
-          const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
-          const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
-          const uint32_t sb = *reinterpret_cast<const uint32_t*>(&sb2);
-          const uint32_t words[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            uint32_t u[4];
-            e2m1x8_to_f16x2x4(words[qq], u);
-#pragma unroll
-            for (int b = 0; b < 4; ++b) o[q][4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
-          }
-        }
-        const int nq = min(kSub, nmma - j);
-        bool ok = true;
-#pragma unroll
-        for (int q = 0; q < kSub; ++q) {
-          if (q >= nq) break;
-          if (!warp_wait(ab_empty(as), aph ^ 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t a_s = sbase + p.off_a + as * kAStageBytes + arow;
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const int chunk = half * 4 + qq;
-            sts128(a_s + ((chunk ^ (row & 7)) << 4),
-                   make_uint4(o[q][4 * qq], o[q][4 * qq + 1], o[q][4 * qq + 2], o[q][4 * qq + 3]));
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_a(ab_full(as));
-          if (++as == AS) {
-            as = 0;
-            aph ^= 1;
-          }
-        }
-        if (!ok) break;
-        j += nq;
-        __syncwarp();
-        if (lane == 0) mbar_arrive_a(raw_empty(s));
-        if (++s == RS) {
-          s = 0;
-          ph ^= 1;
         }
       }
     }
@@ -2003,7 +1892,7 @@ int resident_clusters(int sp) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel, &cfg) != cudaSuccess) {
       cudaGetLastError();  // the query failed: fall back to whole SMs
       n = sm_count() / sp;
     }
@@ -2134,9 +2023,7 @@ bool kernel_attrs_ok() {
       attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                       cudaSharedmemCarveoutMaxShared);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+      attr_err = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   });
   return attr_err == cudaSuccess;
 }
@@ -2344,42 +2231,32 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   int lora_early = (r > 0 && n_tok <= 128) ? 1 : 0;
   const uint32_t part_bytes = split > 1 ? static_cast<uint32_t>(tpc * n_tok) * kTileN * 4u : 0u;
   const uint32_t b_stage = static_cast<uint32_t>(n_tok) * 128u;
-  // The dequantized weights go to tensor memory as the MMA's A operand at
-  // every tile size: 256-token tiles (prefill) keep one 256-column
-  // accumulator and a two-weight-stage A ring beside it, with one MMA issuer
-  // (an N = 256 MMA outlasts its issue cost).
-  const bool tmem_a = true;
+  // The dequantized weights go to tensor memory as the MMA's A operand.
   // Each MMA occupies its issuing thread for ~150 cycles whatever the token
   // count, so small tiles take more issuers (each with its own accumulator,
   // which tensor memory must hold next to the A ring).
   // Pair mode: one issuer per tile.
-  const int issuers = n_tok > 128 ? 1 : (n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2));
+  const int issuers = n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2);
   const uint32_t col_a = static_cast<uint32_t>(align_up(issuers * n_tok, 32));
-  int ab_cap = kMaxAB;
-  if (tmem_a) {
-    if (col_a > static_cast<uint32_t>(kTmemCols)) return QERL_ERR_UNSUPPORTED_SHAPE;
-    ab_cap = std::min(kMaxAB, static_cast<int>((kTmemCols - col_a) / kAStageCols));
-    // The ring is handed over a weight stage (kSub consecutive MMA stages) at
-    // a time: a multiple of kSub.
-    ab_cap -= ab_cap % kSub;
-    if (ab_cap < kSub) return QERL_ERR_UNSUPPORTED_SHAPE;
-  } else if (2 * n_tok > kTmemCols) {
-    return QERL_ERR_UNSUPPORTED_SHAPE;
-  }
+  if (col_a > static_cast<uint32_t>(kTmemCols)) return QERL_ERR_UNSUPPORTED_SHAPE;
+  int ab_cap = std::min(kMaxAB, static_cast<int>((kTmemCols - col_a) / kAStageCols));
+  // The ring is handed over a weight stage (kSub consecutive MMA stages) at
+  // a time: a multiple of kSub.
+  ab_cap -= ab_cap % kSub;
+  if (ab_cap < kSub) return QERL_ERR_UNSUPPORTED_SHAPE;
   struct Plan {
-    uint32_t raw, a, b, lora, tstage, sm, bars, total;
+    uint32_t raw, b, lora, tstage, sm, bars, total;
   };
   // Up to 64 tokens a weight stage's activation slabs ride in its raw-ring
   // slot; above, a separate activation ring is filled by one bulk copy per
   // weight stage.
-  const int coupled = (tmem_a && n_tok <= 64) ? 1 : 0;
+  const int coupled = n_tok <= 64 ? 1 : 0;
   const uint32_t raw_b = coupled ? static_cast<uint32_t>(kSub) * b_stage : 0u;
-  auto plan_for = [&](int rs, int as, int bs) {
+  auto plan_for = [&](int rs, int bs) {
     Plan P;
     P.raw = 0;  // packed weight blocks (codes + scale pairs); 18 KB slots keep 1024-byte alignment
-    P.a = P.raw + rs * tpc * kRawSlotBytes;
-    P.b = P.a + (tmem_a ? 0u : static_cast<uint32_t>(as) * kAStageBytes);
-    uint32_t ring = P.b + (coupled ? rs * raw_b : (tmem_a ? bs : as) * b_stage);
+    P.b = P.raw + rs * tpc * kRawSlotBytes;
+    uint32_t ring = P.b + (coupled ? rs * raw_b : bs * b_stage);
     if (!lora_early) ring = std::max(ring, lb);  // late LoRA tiles are built inside the ring
     ring = std::max(ring, part_bytes);
     P.lora = static_cast<uint32_t>(align_up(ring, 1024));
@@ -2392,9 +2269,9 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     P.total = std::max(P.bars + kBarBytes + 1024u, 118784u);
     return P;
   };
-  int ab_stages = tmem_a ? ab_cap : 3;
+  const int ab_stages = ab_cap;
   int raw_stages = 0, b_stages = 0;
-  if (tmem_a) {
+  {
     // A lives in tensor memory: keep its depth.  Mbarrier waits test a phase
     // parity, so every ring slot must always be waited on by the same thread
     // group in phase order (a waiter that is two phases ahead would pass
@@ -2409,7 +2286,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     // any depth >= 2 works.)
     auto max_rs = [&](int bs) {
       int rs = kMaxRaw;
-      while (rs >= 2 && plan_for(rs, ab_stages, bs).total > static_cast<uint32_t>(kSmemLimit)) --rs;
+      while (rs >= 2 && plan_for(rs, bs).total > static_cast<uint32_t>(kSmemLimit)) --rs;
       return pair ? rs : rs & ~1;
     };
     int best_rs = 0, best_bs = 0;
@@ -2418,12 +2295,10 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
       best_rs = max_rs(kSub);
     } else {
       // Pair mode: each slab waits for both tiles' MMAs before it is
-      // refilled, so two weight stages of activations come first.
-      // One issuer (256-token tiles) consumes every slab itself, so any ring
-      // depth keeps slot ownership fixed; otherwise multiples of kSub.
-      const int rs_pref = pair || issuers == 1 ? 2 : 4;
-      const int bs_step = issuers == 1 ? 1 : kSub;
-      for (int bs = 2 * kSub; bs >= kSub; bs -= bs_step) {
+      // refilled, so two weight stages of activations come first.  The ring
+      // holds multiples of kSub slabs (each issuer owns fixed MMA stages).
+      const int rs_pref = pair ? 2 : 4;
+      for (int bs = 2 * kSub; bs >= kSub; bs -= kSub) {
         const int rs = max_rs(bs);
         if (rs >= 2 && (best_rs == 0 || std::min(rs, rs_pref) > std::min(best_rs, rs_pref))) {
           best_rs = rs;
@@ -2433,21 +2308,14 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     }
     raw_stages = best_rs;
     b_stages = best_bs;
-  } else {
-    const int ab_step = issuers;
-    for (; ab_stages >= std::max(2, issuers) && raw_stages < 2; ab_stages -= ab_step) {
-      for (raw_stages = kMaxRaw; raw_stages >= 2; --raw_stages)
-        if (plan_for(raw_stages, ab_stages, 0).total <= static_cast<uint32_t>(kSmemLimit)) break;
-      if (raw_stages >= 2) break;
-    }
   }
-  if (tmem_a && lora_early && raw_stages < 2) {
+  if (lora_early && raw_stages < 2) {
     // Large rank: no room for a dedicated LoRA region; build the operand in
     // the idle ring after the mainloop instead.
     lora_early = 0;
     for (int bs = coupled ? kSub : 2 * kSub; bs >= kSub && raw_stages < 2; bs -= kSub) {
       int rs = kMaxRaw;
-      while (rs >= 2 && plan_for(rs, ab_stages, bs).total > static_cast<uint32_t>(kSmemLimit)) --rs;
+      while (rs >= 2 && plan_for(rs, bs).total > static_cast<uint32_t>(kSmemLimit)) --rs;
       if (!pair) rs &= ~1;
       if (rs >= 2) {
         raw_stages = rs;
@@ -2455,16 +2323,15 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
       }
     }
   }
-  if (raw_stages < 2 || ab_stages < (tmem_a ? kSub : std::max(2, issuers))) return QERL_ERR_UNSUPPORTED_SHAPE;
+  if (raw_stages < 2) return QERL_ERR_UNSUPPORTED_SHAPE;
   // A weight stage is handed over (and its activations loaded) at once.
-  if (tmem_a && (ab_stages < 2 * kSub || ab_stages % kSub != 0 || b_stages < kSub ||
-                 (issuers > 1 && b_stages % kSub != 0) ||
-                 (!pair && raw_stages % 2 != 0) || (kSub * 4) % issuers != 0 || (!coupled && issuers > kSub) ||
-                 (pair && (issuers != 2 || ab_stages != 2 * kSub))))
+  if (ab_stages < 2 * kSub || ab_stages % kSub != 0 || b_stages < kSub || b_stages % kSub != 0 ||
+      (!pair && raw_stages % 2 != 0) || (kSub * 4) % issuers != 0 || (!coupled && issuers > kSub) ||
+      (pair && (issuers != 2 || ab_stages != 2 * kSub)))
     return QERL_ERR_UNSUPPORTED_SHAPE;
-  const Plan P = plan_for(raw_stages, ab_stages, b_stages);
+  const Plan P = plan_for(raw_stages, b_stages);
 
-  // x~: tiled layout moved by bulk copies with kTmemA; the 256-token tiles
+  // x~: tiled layout moved by bulk copies; several 128-token tiles
   // read [M][K] through a 2D tensor map.
   CUtensorMap tm_xs;
   if (!xs_rowmajor) {
@@ -2618,7 +2485,6 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.t_groups = pp.sum_groups ? 1 : pp.groups;  // == t_groups
   mp.col_a = col_a;
   mp.off_raw = P.raw;
-  mp.off_a = P.a;
   mp.off_b = P.b;
   mp.off_lora = P.lora;
   mp.off_tstage = P.tstage;
@@ -2647,8 +2513,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  const cudaError_t le = tmem_a ? cudaLaunchKernelEx(&cfg, mma_kernel<true>, tm_xs, tm_bls, mp)
-                                : cudaLaunchKernelEx(&cfg, mma_kernel<false>, tm_xs, tm_bls, mp);
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, mma_kernel, tm_xs, tm_bls, mp);
   if (le != cudaSuccess) return QERL_ERR_CUDA;
   return QERL_OK;
 }
