@@ -78,7 +78,7 @@ ARM_PARTS = {(0x41, 0xD0C): "Neoverse-N1", (0x41, 0xD40): "Neoverse-V1", (0x41, 
              (0x41, 0xD4F): "Neoverse-V2", (0x41, 0xD8E): "Neoverse-N3", (0x41, 0xD84): "Neoverse-V3"}
 
 
-EXTRAS = ("prefill", "quantize", "qproj", "sustained", "32b", "mxfp4", "backward")
+EXTRAS = ("prefill", "quantize", "qproj", "sustained", "32b", "mxfp4", "nf4", "backward")
 
 
 def host_cpu_model():
@@ -190,9 +190,13 @@ class QLinear:
         if w_dtype == torch.bfloat16:
             W = W.to(torch.bfloat16)
         self.lin = lin
+        self.w_format = q.QERL_W_NF4 if fmt == "nf4" else q.QERL_W_NVFP4
         if fmt == "mxfp4":
             codes, scales = q.mxfp4_quantize(W)
             self.wp, self.S = q.mxfp4_pack(codes, scales)
+        elif fmt == "nf4":
+            codes, scales, self.S = q.nf4_quantize(W)
+            self.wp = q.pack(codes, scales)
         else:
             codes, scales, self.S = q.quantize(W)
             self.wp = q.pack(codes, scales)
@@ -270,7 +274,8 @@ def run_substep(q, layer, act, sigma, counter):
                     "qerl_lora_linear")
         return
     for g in wl.NOISE_GROUPS:
-        members = [(ql.wp, ql.S, ql.A, ql.B, ALPHA, y) for ql, y in zip(layer, act.y) if ql.lin.group == g]
+        members = [(ql.wp, ql.S, ql.A, ql.B, ALPHA, y, ql.w_format) for ql, y in zip(layer, act.y)
+                   if ql.lin.group == g]
         q.check(q.qerl_lora_linear_group(act.x[g], act.z[g], members, act.ws), "qerl_lora_linear_group")
 
 
@@ -471,6 +476,7 @@ def bench_ours(args):
     extra_32b = bench_32b_stream(q, hbm_peak) if "32b" in want else None
     extra_mx = bench_mxfp4(q, hbm_peak) if "mxfp4" in want else None
     extra_bwd = bench_backward(q, bf16_peak) if "backward" in want else None
+    extra_nf4 = bench_nf4(q, hbm_peak) if "nf4" in want else None
 
     # ---- the dominant launch, timed per call
     roofline = dominant_call(q, layers, acts, hbm_peak)
@@ -534,6 +540,8 @@ def bench_ours(args):
         out["mxfp4"] = extra_mx
     if extra_bwd:
         out["backward"] = extra_bwd
+    if extra_nf4:
+        out["nf4"] = extra_nf4
     if rank == 0 and not args.skip_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_oracle(seconds_budget=args.cpu_budget)
         out["cpu_baseline"]["all_cores"] = cpu_baseline_oracle_all_cores()
@@ -767,6 +775,34 @@ def bench_mxfp4(q, hbm_peak, ms=(8, 32)):
             "GBps_mxfp4_bytes": round(mx_bytes / (per_layer_us * 1e-6) / 1e9, 1),
             "GBps_packed_bytes": round(nw * BYTES_PER_WEIGHT / (per_layer_us * 1e-6) / 1e9, 1),
             "frac_of_hbm_peak_packed": round(nw * BYTES_PER_WEIGHT / (per_layer_us * 1e-6) / 1e9 / hbm_peak, 4)}
+        del act
+    del layers
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_nf4(q, hbm_peak, ms=(8, 32)):
+    """The QLoRA format through the same kernels: the 7B-shaped layer NF4-quantized by the library
+    (levels recovered by table lookup in the dequantization), decode through the grouped launches,
+    weights rotating over N_COPIES layer copies; the same bytes per weight as NVFP4."""
+    shapes = wl.QWEN_7B
+    layers = [[QLinear(q, lin, 7, c, li, fmt="nf4") for li, lin in enumerate(shapes)] for c in range(N_COPIES)]
+    nw = sum(lin.n * lin.k for lin in shapes)
+    res = {"workload": "Qwen2.5-7B-shaped layer in NF4 (QLoRA levels, E4M3 per 16 + FP32 tensor scale), LoRA r=32, "
+                       "AQN"}
+    for m in ms:
+        act = Activations(q, shapes, m, 7)
+
+        def step():
+            for c in range(N_COPIES):
+                run_substep(q, layers[c], act, 1e-2, c)
+
+        t_ms, _, _ = _graph_time_ms(step, 20)
+        q.check(q.qerl_read_status(act.ws), "nf4 decode status")
+        us = t_ms * 1e3 / N_COPIES
+        res[f"decode_m{m}"] = {"us_per_layer": round(us, 2),
+                               "weight_GBps": round(nw * BYTES_PER_WEIGHT / (us * 1e-6) / 1e9, 1),
+                               "frac_of_hbm_peak": round(nw * BYTES_PER_WEIGHT / (us * 1e-6) / 1e9 / hbm_peak, 4)}
         del act
     del layers
     torch.cuda.empty_cache()

@@ -62,6 +62,9 @@ typedef enum {
 } qerl_status;
 
 typedef enum { QERL_F32 = 0, QERL_BF16 = 1 } qerl_dtype;
+/* Element code of a packed weight (qerl_linear_desc.w_format): E2M1
+ * (NVFP4, and MXFP4 after qerl_mxfp4_pack) or the NF4 level table. */
+typedef enum { QERL_W_NVFP4 = 0, QERL_W_NF4 = 1 } qerl_w_format;
 
 /* Human-readable name of a status code (static string, never NULL). */
 QERL_API const char* qerl_status_string(int status);
@@ -161,6 +164,28 @@ QERL_API qerl_status qerl_nvfp4_pack(const uint8_t* codes, const uint8_t* scales
  * LoRA training, so this runs once per weight, beside qerl_nvfp4_pack. */
 QERL_API qerl_status qerl_nvfp4_pack_transposed(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
                                                 uint8_t* packed_t, void* stream);
+
+/* ========================================================================
+ * NF4, the QLoRA format the digest sets against NVFP4 (its levels sit at
+ * quantiles of the Gaussian and are recovered through a lookup table, the
+ * "unpacking" cost the digest ascribes to QLoRA).  Levels (the QLoRA
+ * construction; the digest gives none): standard-normal quantiles at evenly
+ * spaced probabilities with an exact zero -- Phi^-1(1/2 + (i/8)(p - 1/2)),
+ * i = 1..8, their 7-point negative counterpart and 0, p = (1 - 1/32 + 1 -
+ * 1/30) / 2 -- divided by the largest (range [-1, 1]); code c is the c-th
+ * level in ascending order (code 7 = 0).  Scaling: NVFP4's dual scaling with a
+ * level range of 1: S = amax / 448 (1 if 0), block scale E4M3(amax_b / S) per
+ * 16, element code = the level nearest to w / (S dec(s)) (fp32 quotient
+ * compared with the fp32 midpoints of adjacent levels; on a midpoint, the
+ * upper level).  Codes and scales have qerl_nvfp4_quantize's layout, so
+ * qerl_nvfp4_pack packs them; the linear takes them with w_format =
+ * QERL_W_NF4 (its dequantization looks each code byte up in a table; the
+ * product with the block scale is rounded once to fp16).  Arguments, errors
+ * and workspace as qerl_nvfp4_quantize.
+ * ======================================================================== */
+QERL_API qerl_status qerl_nf4_quantize(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w,
+                                       uint8_t* codes, uint8_t* scales, float* tensor_scale, void* workspace,
+                                       size_t ws_bytes, void* stream);
 
 /* ========================================================================
  * MXFP4, the 4-bit format the digest's "NVFP4 Quantization" section compares
@@ -309,6 +334,7 @@ typedef struct qerl_linear_desc {
   float alpha;
   void* y;                    /* device [m][n] */
   int y_dtype;                /* QERL_BF16 or QERL_F32 */
+  int w_format;               /* QERL_W_NVFP4 (also MXFP4 packed by qerl_mxfp4_pack; 0) or QERL_W_NF4 */
 } qerl_linear_desc;
 
 QERL_API size_t qerl_lora_linear_group_workspace_size(int64_t m, int64_t k, const qerl_linear_desc* linears,

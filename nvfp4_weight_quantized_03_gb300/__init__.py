@@ -53,11 +53,12 @@ class LinearDesc(ctypes.Structure):
     """Mirror of qerl_linear_desc (include/qerl.h)."""
     _fields_ = [("wpacked", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p), ("n", ctypes.c_int64),
                 ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("r", ctypes.c_int), ("alpha", ctypes.c_float),
-                ("y", ctypes.c_void_p), ("y_dtype", ctypes.c_int)]
+                ("y", ctypes.c_void_p), ("y_dtype", ctypes.c_int), ("w_format", ctypes.c_int)]
 
 
 QERL_OK = 0
 QERL_F32, QERL_BF16 = 0, 1
+QERL_W_NVFP4, QERL_W_NF4 = 0, 1
 QERL_SCHEDULE_EXPONENTIAL, QERL_SCHEDULE_LINEAR, QERL_SCHEDULE_COSINE, QERL_SCHEDULE_LOGARITHMIC = 0, 1, 2, 3
 STATUS_NAMES = {0: "QERL_OK", 1: "QERL_ERR_INVALID_ARGUMENT", 2: "QERL_ERR_UNSUPPORTED_SHAPE",
                 3: "QERL_ERR_MISALIGNED", 4: "QERL_ERR_CUDA", 5: "QERL_ERR_TIMEOUT", 6: "QERL_ERR_NONFINITE",
@@ -108,6 +109,9 @@ def lib():
             L.qerl_lora_linear_backward.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _vp,
                                                     ctypes.c_int, ctypes.c_float, _vp, ctypes.c_int, _vp, _vp, _vp,
                                                     ctypes.c_size_t, _vp]
+            L.qerl_nf4_quantize.restype = ctypes.c_int
+            L.qerl_nf4_quantize.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                            ctypes.c_size_t, _vp]
             L.qerl_mxfp4_quantize.restype = ctypes.c_int
             L.qerl_mxfp4_quantize.argtypes = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_size_t,
                                               _vp]
@@ -294,6 +298,14 @@ def qerl_lora_linear_backward(xt, dy, wpacked_t, tensor_scale, A, B, alpha, dxt,
                                            _p(dB), _p(workspace), _nbytes(workspace), _stream(stream))
 
 
+def qerl_nf4_quantize(W, codes, scales, tensor_scale, workspace, stream=None) -> int:
+    """W [n, k] f32/bf16 -> NF4 codes [n, k/2], E4M3 scales [n, k/16], tensor scale (the layout of
+    qerl_nvfp4_quantize, so qerl_nvfp4_pack packs it; the linear takes w_format QERL_W_NF4)."""
+    n, k = W.shape
+    return lib().qerl_nf4_quantize(_p(W), _wdtype(W), n, k, W.stride(0), _p(codes), _p(scales), _p(tensor_scale),
+                                   _p(workspace), _nbytes(workspace), _stream(stream))
+
+
 def qerl_mxfp4_quantize(W, codes, scales, workspace, stream=None) -> int:
     """W [n, k] f32/bf16 -> codes [n, k/2], E8M0 scales [n, k/32] (uint8)."""
     n, k = W.shape
@@ -338,12 +350,14 @@ def qerl_lora_linear_noalloc(x, wpacked, tensor_scale, z, A, B, alpha, y, stream
 
 
 def _descs(linears):
-    """[(wpacked, tensor_scale, A, B, alpha, y), ...] -> ctypes array of LinearDesc
+    """[(wpacked, tensor_scale, A, B, alpha, y[, w_format]), ...] -> ctypes array of LinearDesc
     (an array built before is passed through)."""
     if isinstance(linears, ctypes.Array):
         return linears
     arr = (LinearDesc * len(linears))()
-    for d, (wp, ts, A, B, alpha, y) in zip(arr, linears):
+    for d, item in zip(arr, linears):
+        wp, ts, A, B, alpha, y = item[:6]
+        d.w_format = int(item[6]) if len(item) > 6 else QERL_W_NVFP4
         d.wpacked, d.tensor_scale, d.n = _p(wp), _p(ts), y.shape[1]
         d.A, d.B, d.r = _p(A), _p(B), 0 if A is None else A.shape[0]
         d.alpha, d.y = float(alpha), _p(y)
@@ -439,6 +453,17 @@ def pack_transposed(codes: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
     packed = torch.empty(qerl_nvfp4_packed_size(k, n), dtype=torch.uint8, device=codes.device)
     check(qerl_nvfp4_pack_transposed(codes, scales, packed), "qerl_nvfp4_pack_transposed")
     return packed
+
+
+def nf4_quantize(W: torch.Tensor, ws: torch.Tensor = None):
+    """NF4-quantize an n x k float32/bfloat16 CUDA tensor -> (codes, scales, tensor_scale)."""
+    n, k = W.shape
+    codes = torch.empty((n, k // 2), dtype=torch.uint8, device=W.device)
+    scales = torch.empty((n, k // 16), dtype=torch.uint8, device=W.device)
+    ts = torch.empty(1, dtype=torch.float32, device=W.device)
+    ws = workspace(qerl_nvfp4_quantize_workspace_size(), W.device) if ws is None else ws
+    check(qerl_nf4_quantize(W, codes, scales, ts, ws), "qerl_nf4_quantize")
+    return codes, scales, ts
 
 
 def mxfp4_quantize(W: torch.Tensor, ws: torch.Tensor = None):

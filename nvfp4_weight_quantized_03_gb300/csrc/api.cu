@@ -53,6 +53,7 @@ qerl_status prepare_linear_group(const void* x, int64_t m, int64_t k, int64_t ld
     int r = d.r;
     if (d.n < 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
     if (d.y_dtype != QERL_BF16 && d.y_dtype != QERL_F32) return QERL_ERR_INVALID_ARGUMENT;
+    if (d.w_format != QERL_W_NVFP4 && d.w_format != QERL_W_NF4) return QERL_ERR_INVALID_ARGUMENT;
     if ((d.A == nullptr) != (d.B == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
     if (r > 0 && d.A == nullptr) r = 0;
     if (d.A != nullptr && r == 0) return QERL_ERR_INVALID_ARGUMENT;
@@ -68,6 +69,7 @@ qerl_status prepare_linear_group(const void* x, int64_t m, int64_t k, int64_t ld
     a.lin[i].alpha = d.alpha;
     a.lin[i].y = d.y;
     a.lin[i].y_f32 = d.y_dtype == QERL_F32;
+    a.lin[i].nf4 = d.w_format == QERL_W_NF4;
   }
   if (m == 0 || total_n == 0) {
     *empty = true;
@@ -150,6 +152,23 @@ qerl_status qerl_nvfp4_quantize(const void* W, int w_dtype, int64_t n, int64_t k
   if ((st = qerl::launch_amax(W, bf16, n, k, ld_w, &hdr->amax_bits, s)) != QERL_OK) return st;
   return qerl::launch_encode(W, bf16, n, k, ld_w, &hdr->amax_bits, nullptr, tensor_scale, codes, scales,
                              &hdr->status, s);
+}
+
+qerl_status qerl_nf4_quantize(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w, uint8_t* codes,
+                              uint8_t* scales, float* tensor_scale, void* workspace, size_t ws_bytes, void* stream) {
+  qerl_status st = check_weight_args(W, w_dtype, n, k, ld_w);
+  if (st != QERL_OK) return st;
+  if (tensor_scale == nullptr) return QERL_ERR_INVALID_ARGUMENT;
+  if (n > 0 && k > 0 && (codes == nullptr || scales == nullptr)) return QERL_ERR_INVALID_ARGUMENT;
+  if (!aligned(codes, 16)) return QERL_ERR_MISALIGNED;
+  if ((st = check_ws(workspace, ws_bytes, kWsHeaderBytes)) != QERL_OK) return st;
+  auto* hdr = static_cast<qerl::WsHeader*>(workspace);
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemsetAsync(&hdr->amax_bits, 0, sizeof(unsigned), s) != cudaSuccess) return QERL_ERR_CUDA;
+  const bool bf16 = w_dtype == QERL_BF16;
+  if ((st = qerl::launch_amax(W, bf16, n, k, ld_w, &hdr->amax_bits, s)) != QERL_OK) return st;
+  return qerl::launch_encode(W, bf16, n, k, ld_w, &hdr->amax_bits, nullptr, tensor_scale, codes, scales,
+                             &hdr->status, s, true);
 }
 
 qerl_status qerl_nvfp4_quantize_with_scale(const void* W, int w_dtype, int64_t n, int64_t k, int64_t ld_w,
@@ -405,7 +424,7 @@ qerl_status qerl_lora_linear(const void* x, int64_t m, int64_t k, int64_t ldx, c
                              int r, float alpha, void* y, int y_dtype, void* workspace, size_t ws_bytes,
                              void* stream) {
   if (n < 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
-  qerl_linear_desc d;
+  qerl_linear_desc d{};
   d.wpacked = wpacked;
   d.tensor_scale = tensor_scale;
   d.n = n;

@@ -60,6 +60,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "qerl_internal.h"
 #include "qerl_ptx.cuh"
@@ -521,6 +522,7 @@ struct LinearSlot {
   int N, r, y_f32;
   int tile_begin;             // first tile index (gridDim.y) of this linear
   float lora_scale;           // alpha / r
+  int nf4;                    // NF4 element codes: dequantized through the level table
 };
 
 struct MmaParams {
@@ -552,6 +554,11 @@ struct MmaParams {
   int pair;
   int xs_rowmajor;  // x~ staged as [M][K] (more than 128 tokens: several token tiles), read by 2-D TMA
   int wt;           // the weights are in the transposed packed layout (input gradient of the linear)
+  // NF4 (a linear with nf4 set): the 16 levels as fp16 bits; the dequant
+  // warps expand them into a 256-entry table of fp16 pairs (one per code
+  // byte) at off_lut.
+  unsigned short nf4_half[16];
+  uint32_t off_lut;
 };
 
 // The LoRA up-projection's B matrices, one TMA map per linear of the launch.
@@ -743,7 +750,27 @@ __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, const Linear
 // weight's transpose for the input gradient, K being the original output
 // dimension): a scale per element along K, shared by the 16 rows of a row
 // group, at kCodesRawBytes + (row / 16) * 256 + k.
-__device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q, bool wt, uint32_t (&o)[32]) {
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// Element pairs of 8 codes (a 32-bit word): E2M1 by conversion, or (kLut)
+// NF4 by the byte-indexed table of fp16 pairs at `lut`.
+template <bool kLut>
+__device__ __forceinline__ void codes8_to_f16x2x4(uint32_t w, uint32_t lut, uint32_t (&u)[4]) {
+  if constexpr (!kLut) {
+    e2m1x8_to_f16x2x4(w, u);
+  } else {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) u[b] = lds32(lut + 4u * ((w >> (8 * b)) & 0xFFu));
+  }
+}
+
+template <bool kLut>
+__device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q, bool wt, uint32_t lut,
+                                                  uint32_t (&o)[32]) {
   const uint32_t crow = slot + row * 128;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -757,7 +784,7 @@ __device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q,
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
         uint32_t u[4];
-        e2m1x8_to_f16x2x4(words[qq], u);
+        codes8_to_f16x2x4<kLut>(words[qq], lut, u);
 #pragma unroll
         for (int b = 0; b < 4; ++b) o[16 * h + 4 * qq + b] = hmul2_bits(u[b], qq < 2 ? sa : sb);
       }
@@ -768,7 +795,7 @@ __device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q,
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
         uint32_t u[4];
-        e2m1x8_to_f16x2x4(words[qq], u);
+        codes8_to_f16x2x4<kLut>(words[qq], lut, u);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const __half2 sc = e4m3x2_to_half2((sw[2 * qq + (b >> 1)] >> (16 * (b & 1))) & 0xFFFFu);
@@ -1170,102 +1197,120 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // ------------------------------------------------------------ dequant warps
     const int dw = warp - kDeqWarp0;
     const bool wt = p.wt != 0;
-    if (p.pair) {
-      // Pair mode: group g = dw / 4 dequantizes tile g of the pair (a thread
-      // is one weight row of it), every weight stage, and hands each MMA
-      // stage's 32 TMEM columns over as soon as they are stored, so the next
-      // stage's conversion overlaps the current stage's remaining MMAs.
-      const int g = dw >> 2;
-      if (g < ntl) {
+    uint32_t lut = 0u;
+    if (L.nf4) {
+      // The NF4 table: entry e (a code byte) = the fp16 pair (level[e & 15],
+      // level[e >> 4]), low element in the low half as the E2M1 conversion.
+      lut = sbase + p.off_lut;
+      const int e = static_cast<int>(threadIdx.x) - 32 * kDeqWarp0;  // 0..255
+      sts32(lut + 4u * e, static_cast<uint32_t>(p.nf4_half[e & 15]) | (static_cast<uint32_t>(p.nf4_half[e >> 4]) << 16));
+      named_barrier_sync(3, 256);
+    }
+    // The loops are instantiated with and without the NF4 table, so the E2M1
+    // path carries no per-word branch.
+    auto dequant_loops = [&](auto lut_on) {
+      constexpr bool kLut = decltype(lut_on)::value;
+      if (p.pair) {
+        // Pair mode: group g = dw / 4 dequantizes tile g of the pair (a thread
+        // is one weight row of it), every weight stage, and hands each MMA
+        // stage's 32 TMEM columns over as soon as they are stored, so the next
+        // stage's conversion overlaps the current stage's remaining MMAs.
+        const int g = dw >> 2;
+        if (g < ntl) {
+          const int row = 32 * (warp & 3) + lane;
+          const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+          int s = 0;
+          uint32_t ph = 0;
+          for (int i = 0; i < nraw; ++i) {
+            if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
+            const uint32_t slot = sbase + p.off_raw + s * rslot + g * kRawSlotBytes;
+            const int nq = min(kSub, nmma - i * kSub);
+            bool ok = true;
+#pragma unroll
+            for (int q = 0; q < kSub; ++q) {
+              if (q >= nq) break;
+              uint32_t o[32];
+              dequant_mma_stage<kLut>(slot, row, q, wt, lut, o);
+              const int sl = g * kSub + q;
+              if (!warp_wait(ab_empty(sl), (i & 1) ^ 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              tmem_st_x32(tmem_base + lane_base + p.col_a + static_cast<uint32_t>(sl * kAStageCols), o);
+              tmem_st_wait();
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_a(ab_full(sl));
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive_a(raw_empty(s));
+            if (++s == RS) {
+              s = 0;
+              ph ^= 1;
+            }
+          }
+        }
+      } else {
+        // Two groups of four warps (one per TMEM lane quadrant, warp % 4) take
+        // alternate weight stages: group g = dw / 4 dequantizes stages g, g + 2,
+        // ...  A thread is one weight row (its lane of the quadrant) and covers
+        // the stage's whole 256-wide K range, one MMA stage (64 K = 32 TMEM
+        // columns of fp16 pairs) at a time: convert, store to tensor memory,
+        // next.  While one group stores and hands a stage over, the other
+        // converts the next one, so the conversion units stay busy.
+        const int grp = dw >> 2;
         const int row = 32 * (warp & 3) + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        int s = 0;
-        uint32_t ph = 0;
-        for (int i = 0; i < nraw; ++i) {
+        const int AW = AS / kSub;  // tensor-memory slots, one weight stage each (>= 2)
+        int s = grp, w = grp;      // this group's first stage (index grp): raw slot grp, A slot grp (RS, AW >= 2)
+        uint32_t ph = 0, aph = 0;
+        for (int i = grp; i < nraw; i += 2) {
           if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
-          const uint32_t slot = sbase + p.off_raw + s * rslot + g * kRawSlotBytes;
+          const uint32_t slot = sbase + p.off_raw + s * kRawSlotBytes;
           const int nq = min(kSub, nmma - i * kSub);
+          const uint32_t a_slot = tmem_base + lane_base + p.col_a + static_cast<uint32_t>(w * kSub * kAStageCols);
           bool ok = true;
 #pragma unroll
           for (int q = 0; q < kSub; ++q) {
             if (q >= nq) break;
+            // MMA stage q: 16-byte code chunks 2q, 2q + 1 of the row (128-byte
+            // swizzle) and the scales of the same K range.
             uint32_t o[32];
-            dequant_mma_stage(slot, row, q, wt, o);
-            const int sl = g * kSub + q;
-            if (!warp_wait(ab_empty(sl), (i & 1) ^ 1, abort_flag, p.status)) {
+            dequant_mma_stage<kLut>(slot, row, q, wt, lut, o);
+            // The slot's previous MMAs must be done before the first store
+            // (the first conversion overlaps that wait).
+            if (q == 0 && !warp_wait(ab_empty(w), aph ^ 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
-            tmem_st_x32(tmem_base + lane_base + p.col_a + static_cast<uint32_t>(sl * kAStageCols), o);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_a(ab_full(sl));
+            tmem_st_x32(a_slot + q * kAStageCols, o);
           }
           if (!ok) break;
+          tmem_st_wait();
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_a(raw_empty(s));
-          if (++s == RS) {
-            s = 0;
+          if (lane == 0) {
+            mbar_arrive_a(ab_full(w));
+            mbar_arrive_a(raw_empty(s));
+          }
+          s += 2;
+          if (s >= RS) {
+            s -= RS;
             ph ^= 1;
           }
-        }
-      }
-    } else {
-      // Two groups of four warps (one per TMEM lane quadrant, warp % 4) take
-      // alternate weight stages: group g = dw / 4 dequantizes stages g, g + 2,
-      // ...  A thread is one weight row (its lane of the quadrant) and covers
-      // the stage's whole 256-wide K range, one MMA stage (64 K = 32 TMEM
-      // columns of fp16 pairs) at a time: convert, store to tensor memory,
-      // next.  While one group stores and hands a stage over, the other
-      // converts the next one, so the conversion units stay busy.
-      const int grp = dw >> 2;
-      const int row = 32 * (warp & 3) + lane;
-      const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-      const int AW = AS / kSub;  // tensor-memory slots, one weight stage each (>= 2)
-      int s = grp, w = grp;      // this group's first stage (index grp): raw slot grp, A slot grp (RS, AW >= 2)
-      uint32_t ph = 0, aph = 0;
-      for (int i = grp; i < nraw; i += 2) {
-        if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
-        const uint32_t slot = sbase + p.off_raw + s * kRawSlotBytes;
-        const int nq = min(kSub, nmma - i * kSub);
-        const uint32_t a_slot = tmem_base + lane_base + p.col_a + static_cast<uint32_t>(w * kSub * kAStageCols);
-        bool ok = true;
-#pragma unroll
-        for (int q = 0; q < kSub; ++q) {
-          if (q >= nq) break;
-          // MMA stage q: 16-byte code chunks 2q, 2q + 1 of the row (128-byte
-          // swizzle) and the scales of the same K range.
-          uint32_t o[32];
-          dequant_mma_stage(slot, row, q, wt, o);
-          // The slot's previous MMAs must be done before the first store
-          // (the first conversion overlaps that wait).
-          if (q == 0 && !warp_wait(ab_empty(w), aph ^ 1, abort_flag, p.status)) {
-            ok = false;
-            break;
+          w += 2;
+          if (w >= AW) {
+            w -= AW;
+            aph ^= 1;
           }
-          tmem_st_x32(a_slot + q * kAStageCols, o);
-        }
-        if (!ok) break;
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_a(ab_full(w));
-          mbar_arrive_a(raw_empty(s));
-        }
-        s += 2;
-        if (s >= RS) {
-          s -= RS;
-          ph ^= 1;
-        }
-        w += 2;
-        if (w >= AW) {
-          w -= AW;
-          aph ^= 1;
         }
       }
-    }
+    };
+    if (lut != 0u)
+      dequant_loops(std::true_type{});
+    else
+      dequant_loops(std::false_type{});
     if (do_lora && !p.pair) {
       // The LoRA operand's t tiles, by all 256 dequant threads once their
       // stream is done: from the rows the LoRA warp staged (early), or from
@@ -2245,8 +2290,11 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   ab_cap -= ab_cap % kSub;
   if (ab_cap < kSub) return QERL_ERR_UNSUPPORTED_SHAPE;
   struct Plan {
-    uint32_t raw, b, lora, tstage, sm, bars, total;
+    uint32_t raw, b, lora, tstage, sm, bars, lut, total;
   };
+  bool any_nf4 = false;
+  for (int i = 0; i < nlin; ++i) any_nf4 = any_nf4 || a.lin[i].nf4;
+  const uint32_t lut_bytes = any_nf4 ? 1024u : 0u;  // 256 fp16 pairs
   // Up to 64 tokens a weight stage's activation slabs ride in its raw-ring
   // slot; above, a separate activation ring is filled by one bulk copy per
   // weight stage.
@@ -2266,7 +2314,8 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     // + 1024-byte alignment slack; at least 116 KB so that two CTAs never share
     // an SM (each allocates all of tensor memory, and partners in a cluster
     // wait for one another).
-    P.total = std::max(P.bars + kBarBytes + 1024u, 118784u);
+    P.lut = P.bars + kBarBytes;
+    P.total = std::max(P.lut + lut_bytes + 1024u, 118784u);
     return P;
   };
   const int ab_stages = ab_cap;
@@ -2470,6 +2519,13 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     L.y_f32 = a.lin[i].y_f32 ? 1 : 0;
     L.tile_begin = tile_begin[i];
     L.lora_scale = ranks[i] > 0 ? a.lin[i].alpha / static_cast<float>(ranks[i]) : 0.0f;
+    L.nf4 = a.lin[i].nf4 ? 1 : 0;
+  }
+  if (any_nf4) {
+    const Nf4Tables& nt = nf4_tables();
+    for (int j = 0; j < 16; ++j)
+      mp.nf4_half[j] = __half_as_ushort(__float2half_rn(static_cast<float>(nt.level[j])));
+    mp.off_lut = P.lut;
   }
   mp.status = status;
   mp.M = M;

@@ -70,7 +70,7 @@ extern "C" qerl_status qerl_lora_linear_noalloc(const void* x, int64_t m, int64_
   // that the workspace entry point rejects is rejected here with the same
   // code, before anything is enqueued.
   if (n < 0 || r < 0) return QERL_ERR_INVALID_ARGUMENT;
-  const qerl_linear_desc d{wpacked, tensor_scale, n, A, B, r, alpha, y, y_dtype};
+  const qerl_linear_desc d{wpacked, tensor_scale, n, A, B, r, alpha, y, y_dtype, QERL_W_NVFP4};
   qerl::LinearArgs a{};
   bool empty = false;
   qerl_status st = qerl::prepare_linear_group(x, m, k, ldx, z, &d, 1, &a, &empty);

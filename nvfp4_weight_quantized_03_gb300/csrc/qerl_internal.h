@@ -20,7 +20,14 @@ qerl_status launch_amax(const void* W, bool bf16, int64_t n, int64_t k, int64_t 
                         cudaStream_t s);
 qerl_status launch_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w,
                           const unsigned* amax_bits, const float* s_in, float* s_out, uint8_t* codes,
-                          uint8_t* scales, int* status, cudaStream_t s);
+                          uint8_t* scales, int* status, cudaStream_t s, bool nf4 = false);
+// NF4 (quantize.cu): the 16 levels (fp64, ascending, code c = level c) and
+// the fp32 midpoints of adjacent levels.
+struct Nf4Tables {
+  double level[16];
+  float mid[15];
+};
+const Nf4Tables& nf4_tables();
 qerl_status launch_amax_to_float(const unsigned* amax_bits, float* amax, cudaStream_t s);
 qerl_status launch_tensor_scale(const float* amax, float* S, cudaStream_t s);
 
@@ -55,6 +62,7 @@ struct LinearDesc {
   float alpha;
   void* y;
   bool y_f32;
+  bool nf4;  // NF4 element codes (the level table) instead of E2M1
 };
 struct LinearArgs {  // up to 4 linears sharing x, z and k
   const void* x;

@@ -13,6 +13,8 @@
 //      documented order, so codes and scales are bit-reproducible.
 #include <cuda_bf16.h>
 
+#include <cmath>
+
 #include "qerl_internal.h"
 #include "qerl_ptx.cuh"
 
@@ -62,12 +64,20 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint8_t* __restric
 // One thread per 16-element block; threads of a warp cover consecutive blocks
 // of a row, so loads (64 B or 32 B per thread) and the 8-byte code stores are
 // contiguous across the warp.
+// NF4 mode (nf4.on): the level range is 1 instead of 6 -- S = amax / 448,
+// block scale E4M3(amax_b / S) -- and an element's code is the number of
+// level midpoints (fp32, ascending) at or below w / (S dec(s)).
+struct Nf4Mids {
+  float mid[15];
+  int on;
+};
+
 __global__ void __launch_bounds__(kThreads) encode_kernel(const uint8_t* __restrict__ W, int64_t n, int64_t k,
                                                           int64_t ld_bytes, bool bf16,
                                                           const unsigned* __restrict__ amax_bits,
                                                           const float* __restrict__ s_in, float* __restrict__ s_out,
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                          int* __restrict__ status) {
+                                                          int* __restrict__ status, const Nf4Mids nf4) {
   float S;
   if (s_in != nullptr) {
     S = *s_in;
@@ -84,7 +94,7 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(const uint8_t* __restr
       }
       return;
     }
-    S = __fdiv_rn(__uint_as_float(ab), 2688.0f);  // amax / (6 * 448)
+    S = __fdiv_rn(__uint_as_float(ab), nf4.on ? 448.0f : 2688.0f);  // amax / (level range * 448)
     if (S == 0.0f) S = 1.0f;
     if (blockIdx.x == 0 && threadIdx.x == 0 && s_out != nullptr) *s_out = S;
   }
@@ -121,12 +131,24 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(const uint8_t* __restr
         record_error(status, 6);
         continue;
       }
-      const float rb = __fdiv_rn(__fdiv_rn(__uint_as_float(mb), 6.0f), S);
+      const float rb = nf4.on ? __fdiv_rn(__uint_as_float(mb), S) : __fdiv_rn(__fdiv_rn(__uint_as_float(mb), 6.0f), S);
       const uint32_t sb = f32_to_e4m3_satfinite(rb);
       const float dec = __half2float(__low2half(e4m3x2_to_half2(sb)));
       const float sc = __fmul_rn(S, dec);
       uint32_t packed[2] = {0u, 0u};
-      if (sc != 0.0f) {
+      if (nf4.on) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          uint32_t c = 7u;  // zero
+          if (sc != 0.0f) {
+            const float q = __fdiv_rn(w[i], sc);
+            c = 0u;
+#pragma unroll
+            for (int j = 0; j < 15; ++j) c += nf4.mid[j] <= q ? 1u : 0u;
+          }
+          packed[i >> 3] |= c << (4 * (i & 7));
+        }
+      } else if (sc != 0.0f) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           uint32_t byte = f32x2_to_e2m1x2_satfinite(__fdiv_rn(w[2 * i], sc), __fdiv_rn(w[2 * i + 1], sc));
@@ -435,12 +457,52 @@ qerl_status launch_amax(const void* W, bool bf16, int64_t n, int64_t k, int64_t 
 
 qerl_status launch_encode(const void* W, bool bf16, int64_t n, int64_t k, int64_t ld_w,
                           const unsigned* amax_bits, const float* s_in, float* s_out, uint8_t* codes,
-                          uint8_t* scales, int* status, cudaStream_t s) {
+                          uint8_t* scales, int* status, cudaStream_t s, bool nf4) {
   const int64_t esz = bf16 ? 2 : 4;
+  Nf4Mids mids{};
+  if (nf4) {
+    const Nf4Tables& t = nf4_tables();
+    for (int i = 0; i < 15; ++i) mids.mid[i] = t.mid[i];
+    mids.on = 1;
+  }
   encode_kernel<<<grid_for_rows(n > 0 ? n : 1), kThreads, 0, s>>>(static_cast<const uint8_t*>(W), n, k,
                                                                    ld_w * esz, bf16, amax_bits, s_in, s_out,
-                                                                   codes, scales, status);
+                                                                   codes, scales, status, mids);
   return cuda_status(cudaGetLastError());
+}
+
+// The NF4 levels (QLoRA's construction: normalised standard-normal quantiles
+// at evenly spaced probabilities with an exact zero; see qerl.h), computed
+// once in fp64 by Newton's method on Phi(x) = erfc(-x / sqrt 2) / 2, then the
+// fp32 midpoints the encoder compares against and the fp16 levels the linear
+// looks up.
+const Nf4Tables& nf4_tables() {
+  static Nf4Tables t = [] {
+    auto ppf = [](double prob) {
+      double x = 0.0;
+      for (int it = 0; it < 100; ++it) {
+        const double f = 0.5 * std::erfc(-x / std::sqrt(2.0)) - prob;
+        const double d = std::exp(-0.5 * x * x) / std::sqrt(2.0 * 3.14159265358979323846);
+        const double nx = x - f / d;
+        if (nx == x) break;
+        x = nx;
+      }
+      return x;
+    };
+    Nf4Tables r{};
+    const double p = ((1.0 - 1.0 / 32.0) + (1.0 - 1.0 / 30.0)) / 2.0;
+    const double top = ppf(p);
+    double lv[16];
+    for (int i = 1; i <= 7; ++i) lv[7 - i] = -ppf(0.5 + (i / 7.0) * (p - 0.5)) / top;
+    lv[7] = 0.0;
+    for (int i = 1; i <= 8; ++i) lv[7 + i] = ppf(0.5 + (i / 8.0) * (p - 0.5)) / top;
+    lv[0] = -1.0;
+    lv[15] = 1.0;
+    for (int i = 0; i < 15; ++i) r.mid[i] = static_cast<float>((lv[i] + lv[i + 1]) / 2.0);
+    for (int i = 0; i < 16; ++i) r.level[i] = lv[i];
+    return r;
+  }();
+  return t;
 }
 
 qerl_status launch_tensor_scale(const float* amax, float* S, cudaStream_t s) {

@@ -138,6 +138,7 @@ def test_group_validation(L):
     assert E[_group(L, [])] == "QERL_ERR_INVALID_ARGUMENT"
     assert E[_group(L, [ok] * 5)] == "QERL_ERR_INVALID_ARGUMENT"
     assert E[_group(L, [ok, _desc(y_dtype=5)])] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[_group(L, [ok, _desc(w_format=2)])] == "QERL_ERR_INVALID_ARGUMENT"
     assert E[_group(L, [ok, _desc(A=0x6000)])] == "QERL_ERR_INVALID_ARGUMENT"
     assert E[_group(L, [ok, _desc(A=0x6000, B=0x7000, r=12)])] == "QERL_ERR_UNSUPPORTED_SHAPE"
     assert E[_group(L, [ok, _desc(wpacked=0x2008)])] == "QERL_ERR_MISALIGNED"
@@ -279,6 +280,19 @@ def test_backward_validation(L):
     assert E[pt(n=65536 + 64)] == "QERL_ERR_UNSUPPORTED_SHAPE"
     assert E[pt(out=None)] == "QERL_ERR_INVALID_ARGUMENT"
     assert E[pt(codes=0x1008)] == "QERL_ERR_MISALIGNED"
+
+
+def test_nf4_quantize_validation(L):
+    E = q.STATUS_NAMES
+    qz = lambda **kw: L.qerl_nf4_quantize(
+        kw.get("W", 0x1000), kw.get("dt", q.QERL_F32), kw.get("n", 4), kw.get("k", 64), kw.get("ld", 64),
+        kw.get("codes", 0x2000), kw.get("scales", 0x3000), kw.get("ts", 0x4000), kw.get("ws", 0x10000),
+        kw.get("wsb", 256), None)
+    assert E[qz(k=48, ld=48)] == "QERL_ERR_UNSUPPORTED_SHAPE"
+    assert E[qz(dt=5)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[qz(ts=None)] == "QERL_ERR_INVALID_ARGUMENT"
+    assert E[qz(codes=0x2008)] == "QERL_ERR_MISALIGNED"
+    assert E[qz(wsb=255)] == "QERL_ERR_WORKSPACE"
 
 
 def test_product_and_oracle_are_independent():
