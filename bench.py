@@ -887,7 +887,7 @@ def bench_32b_stream(q, hbm_peak):
             qt_ms += e0.elapsed_time(e1)
             n_weights += lin.n * lin.k
             ql = QLinear.__new__(QLinear)
-            ql.lin, ql.S, ql.wp = lin, S, q.pack(codes, scales)
+            ql.lin, ql.S, ql.wp, ql.w_format = lin, S, q.pack(codes, scales), q.QERL_W_NVFP4
             ql.A = wl.normal_bf16_device((RANK_R, lin.k), 1.0 / math.sqrt(lin.k), 32, li, j, 2)
             ql.B = wl.normal_bf16_device((lin.n, RANK_R), 0.01, 32, li, j, 3)
             layer.append(ql)
