@@ -1139,7 +1139,7 @@ def _oracle_slice_worker(idx, nproc, ms, barrier, out_q):
     out_q.put((t0, time.monotonic(), wbytes))
 
 
-def cpu_baseline_oracle_all_cores(ms=(1, 8)):
+def cpu_baseline_oracle_all_cores(ms=DECODE_MS):
     """The same oracle on every host core: one spawned process per core, each owning an
     interleaved slice of every linear's output rows; wall time from the common start to the
     last finish."""

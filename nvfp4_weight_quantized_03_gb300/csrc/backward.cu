@@ -31,7 +31,7 @@ namespace qerl {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSkM = 16;  // tokens per shared-memory chunk
+constexpr int kSkM = 32;  // tokens per shared-memory chunk
 
 // out[c][r] = in[r][c] for a bf16 rows x cols matrix (row stride ld_in); 32x32 tiles.
 __global__ void __launch_bounds__(kThreads) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in, int64_t ld_in,
@@ -55,59 +55,80 @@ __global__ void __launch_bounds__(kThreads) transpose_bf16_kernel(const __nv_bfl
 //   partial[split][p][j] = sum_{m in range} X[m][p] * T[m][j],
 // T[m][j] = sum over `parts` arrays (part_stride apart) of [m][r] fp32.
 // A thread owns 4 consecutive p and 8 consecutive j; the block's p tile is
-// 4 * (256 / jg) wide, jg = the power of two >= ceil(r / 8).
+// 4 * (256 / jg) wide, jg = the power of two >= ceil(r / 8).  kSkM-token
+// chunks go through shared memory (X as fp32, T summed over its parts); the
+// next chunk's loads are issued into registers before the current chunk's
+// FMAs, so their latency overlaps the arithmetic.
+template <int JG>
 __global__ void __launch_bounds__(kThreads) skinny_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int M,
                                                           int P, const float* __restrict__ T, int parts,
-                                                          int64_t part_stride, int r, int jg, int m_per_split,
+                                                          int64_t part_stride, int r, int m_per_split,
                                                           float* __restrict__ partial) {
   extern __shared__ __align__(16) float sk_smem[];
-  const int ptile = 4 * (kThreads / jg);
+  constexpr int ptile = 4 * (kThreads / JG);
+  constexpr int tw = 8 * JG;
+  constexpr int nxv = kSkM * ptile / 8 / kThreads;  // X loads (8 bf16 each) per thread per chunk
+  constexpr int ntv = kSkM * tw / kThreads;          // T values per thread per chunk
+  static_assert(nxv >= 1 && ntv >= 1, "chunk covers every thread");
+  constexpr int kSkMaxXv = nxv, kSkMaxTv = ntv;
   float* Xs = sk_smem;                 // [kSkM][ptile]
-  float* Ts = sk_smem + kSkM * ptile;  // [kSkM][8 * jg]
-  const int tw = 8 * jg;
+  float* Ts = sk_smem + kSkM * ptile;  // [kSkM][tw]
   const int p0 = blockIdx.x * ptile;
   const int m_begin = blockIdx.y * m_per_split, m_end = min(M, m_begin + m_per_split);
-  const int tj = threadIdx.x % jg, tp = threadIdx.x / jg;
+  const int tj = threadIdx.x % JG, tp = threadIdx.x / JG;
   float acc[4][8];
 #pragma unroll
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
-  for (int m0 = m_begin; m0 < m_end; m0 += kSkM) {
-    // X chunk: kSkM rows x ptile columns, 8 bf16 per load.
-    for (int idx = threadIdx.x; idx < kSkM * ptile / 8; idx += kThreads) {
+  uint4 xv[kSkMaxXv];
+  float tv[kSkMaxTv];
+  auto load = [&](int m0) {
+#pragma unroll
+    for (int u = 0; u < kSkMaxXv; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
       const int row = idx / (ptile / 8), c8 = (idx % (ptile / 8)) * 8;
       const int m = m0 + row, p = p0 + c8;
-      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (m < m_end && p < P) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m) * ldx + p));
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[2 * i] = __uint_as_float(u[i] << 16);
-          v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-        }
-      }
-      float4* d = reinterpret_cast<float4*>(Xs + row * ptile + c8);
-      d[0] = make_float4(v[0], v[1], v[2], v[3]);
-      d[1] = make_float4(v[4], v[5], v[6], v[7]);
+      xv[u] = (m < m_end && p < P) ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m) * ldx + p))
+                                   : make_uint4(0u, 0u, 0u, 0u);
     }
-    // T chunk: kSkM rows x tw ranks (zero past r and past the range).
-    for (int idx = threadIdx.x; idx < kSkM * tw; idx += kThreads) {
+#pragma unroll
+    for (int u = 0; u < kSkMaxTv; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
       const int row = idx / tw, j = idx % tw;
       const int m = m0 + row;
       float v = 0.0f;
       if (m < m_end && j < r)
         for (int g = 0; g < parts; ++g) v += __ldg(T + g * part_stride + static_cast<int64_t>(m) * r + j);
-      Ts[row * tw + j] = v;
+      tv[u] = v;
     }
+  };
+  auto store = [&]() {
+#pragma unroll
+    for (int u = 0; u < kSkMaxXv; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
+      const int row = idx / (ptile / 8), c8 = (idx % (ptile / 8)) * 8;
+      const uint32_t w[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+      float4* d = reinterpret_cast<float4*>(Xs + row * ptile + c8);
+      d[0] = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u),
+                         __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
+      d[1] = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u),
+                         __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
+    }
+#pragma unroll
+    for (int u = 0; u < kSkMaxTv; ++u) Ts[threadIdx.x + u * kThreads] = tv[u];
+  };
+  if (m_begin < m_end) load(m_begin);
+  for (int m0 = m_begin; m0 < m_end; m0 += kSkM) {
+    store();
     __syncthreads();
+    if (m0 + kSkM < m_end) load(m0 + kSkM);  // in flight during the FMAs below
 #pragma unroll 4
     for (int mm = 0; mm < kSkM; ++mm) {
-      const float4 xv = *reinterpret_cast<const float4*>(Xs + mm * ptile + 4 * tp);
+      const float4 xq = *reinterpret_cast<const float4*>(Xs + mm * ptile + 4 * tp);
       const float4 t0 = *reinterpret_cast<const float4*>(Ts + mm * tw + 8 * tj);
       const float4 t1 = *reinterpret_cast<const float4*>(Ts + mm * tw + 8 * tj + 4);
-      const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+      const float xa[4] = {xq.x, xq.y, xq.z, xq.w};
       const float ta[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
 #pragma unroll
       for (int a = 0; a < 4; ++a)
@@ -208,12 +229,24 @@ qerl_status launch_skinny(const void* X, int64_t ldx, int64_t M, int64_t P, cons
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    const int lim = 160 * 1024;  // the r <= 8 tile: 32 x (1024 + 8) floats
+    err = cudaFuncSetAttribute(skinny_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   });
   if (err != cudaSuccess) return QERL_ERR_CUDA;
-  skinny_kernel<<<dim3(static_cast<unsigned>(sp.ptiles), static_cast<unsigned>(sp.splits)), kThreads, sp.smem, s>>>(
-      static_cast<const __nv_bfloat16*>(X), ldx, static_cast<int>(M), static_cast<int>(P), T.t, T.parts,
-      T.part_stride, r, sp.jg, sp.m_per_split, partial);
+  const dim3 grid(static_cast<unsigned>(sp.ptiles), static_cast<unsigned>(sp.splits));
+  const auto* xb = static_cast<const __nv_bfloat16*>(X);
+  const int Mi = static_cast<int>(M), Pi = static_cast<int>(P);
+  switch (sp.jg) {
+    case 1: skinny_kernel<1><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
+    case 2: skinny_kernel<2><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
+    case 4: skinny_kernel<4><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
+    case 8: skinny_kernel<8><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
+    default: skinny_kernel<16><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
+  }
   if (cudaGetLastError() != cudaSuccess) return QERL_ERR_CUDA;
   const int64_t total = P * r;
   const int blocks = static_cast<int>(std::min<int64_t>((total + kThreads - 1) / kThreads, 4 * sms()));

@@ -2245,12 +2245,15 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     }
     return sp_best;
   };
-  // Decode tiles above 64 tokens run in pair mode -- one CTA per two adjacent
-  // 128-row weight tiles of a linear, sharing the activation slabs -- when
-  // each CTA then streams at least 6 weight stages: its mainloop is about
-  // twice as fast per tile, its fixed costs (two tiles' epilogue) higher.
-  const int split_pair = n_tok > 64 && n_tok <= 128 ? best_split(all_pairs) : 1;
-  const bool pair = n_tok > 64 && n_tok <= 128 && (raw_total + split_pair - 1) / split_pair >= 6;
+  // Tiles above 32 tokens run in pair mode -- one CTA per two adjacent 128-row
+  // weight tiles of a linear, sharing the activation slabs, with the
+  // activation ring separate from the weights -- when each CTA then streams at
+  // least 6 weight stages: half as many CTAs (one wave instead of two for the
+  // 7B gate + up launch) and half the activation bytes per weight byte; its
+  // fixed costs (two tiles' epilogue) are higher.  (Measured at 33-64 tokens:
+  // 7% less time per layer than single tiles with four issuers.)
+  const int split_pair = n_tok > 32 && n_tok <= 128 ? best_split(all_pairs) : 1;
+  const bool pair = n_tok > 32 && n_tok <= 128 && (raw_total + split_pair - 1) / split_pair >= 6;
   int tile_begin[kMaxLinears + 1] = {0, 0, 0, 0, 0};  // in grid-y units: tiles, or pairs of tiles
   for (int i = 0; i < nlin; ++i) tile_begin[i + 1] = tile_begin[i] + (pair ? (tiles[i] + 1) / 2 : tiles[i]);
   const bool lora = r > 0;
@@ -2281,13 +2284,14 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // count, so small tiles take more issuers (each with its own accumulator,
   // which tensor memory must hold next to the A ring).
   // Pair mode: one issuer per tile.
-  const int issuers = n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2);
+  const int issuers = pair ? 2 : (n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2));
   const uint32_t col_a = static_cast<uint32_t>(align_up(issuers * n_tok, 32));
   if (col_a > static_cast<uint32_t>(kTmemCols)) return QERL_ERR_UNSUPPORTED_SHAPE;
   int ab_cap = std::min(kMaxAB, static_cast<int>((kTmemCols - col_a) / kAStageCols));
   // The ring is handed over a weight stage (kSub consecutive MMA stages) at
   // a time: a multiple of kSub.
   ab_cap -= ab_cap % kSub;
+  if (pair) ab_cap = std::min(ab_cap, 2 * kSub);  // one slot per (tile, MMA stage)
   if (ab_cap < kSub) return QERL_ERR_UNSUPPORTED_SHAPE;
   struct Plan {
     uint32_t raw, b, lora, tstage, sm, bars, lut, total;
@@ -2298,7 +2302,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // Up to 64 tokens a weight stage's activation slabs ride in its raw-ring
   // slot; above, a separate activation ring is filled by one bulk copy per
   // weight stage.
-  const int coupled = n_tok <= 64 ? 1 : 0;
+  const int coupled = (n_tok <= 64 && !pair) ? 1 : 0;
   const uint32_t raw_b = coupled ? static_cast<uint32_t>(kSub) * b_stage : 0u;
   auto plan_for = [&](int rs, int bs) {
     Plan P;
