@@ -299,11 +299,13 @@ def group_algorithmic_bytes(lins, m, r=RANK_R):
 
 # Dominant launch of the decode step: the grouped gate + up launch (two
 # 18944 x 3584 linears sharing x; the largest of the step's four launches) at
-# M = 8.  DRAM traffic of one such launch (prep_kernel + mma_kernel), from the
-# ncu capture summarized in profiles/mma_kernel_decode_gateup_m8.md; None
-# while no capture of the current kernels exists.
+# M = 8.  DRAM traffic of one such launch (prep_kernel + mma_kernel):
+# dram__bytes_read.sum + dram__bytes_write.sum from a 1-pass ncu capture of
+# `bench.py --case 8,18944+18944,3584,32` (taken on the build with the NF4
+# table path and the tensor-core LoRA down-projection; the 8-token decode path
+# is unchanged since).
 DOMINANT = ("gate_up", 8)
-DOMINANT_TRAFFIC_BYTES = 79609600  # prep 565,248 + mma 79,023,872 read + 20,480 written (ncu, 1 pass)
+DOMINANT_TRAFFIC_BYTES = 79695360  # prep 599,296 + mma 79,077,632 read + 18,432 written (ncu, 1 pass)
 
 
 def dominant_call(q, layers, acts, hbm_peak, reps=64):

@@ -166,9 +166,11 @@ QERL_API qerl_status qerl_nvfp4_pack_transposed(const uint8_t* codes, const uint
                                                 uint8_t* packed_t, void* stream);
 
 /* ========================================================================
- * NF4, the QLoRA format the digest sets against NVFP4 (its levels sit at
+ * NF4, the QLoRA format the digest sets against NVFP4 ("QLoRA's 4-bit
+ * Quantization Addresses Memory but Degrades Speed", and "NVFP4
+ * Quantization", comparison to other 4-bit formats: its levels sit at
  * quantiles of the Gaussian and are recovered through a lookup table, the
- * "unpacking" cost the digest ascribes to QLoRA).  Levels (the QLoRA
+ * unpacking cost the digest ascribes to QLoRA).  Levels (the QLoRA
  * construction; the digest gives none): standard-normal quantiles at evenly
  * spaced probabilities with an exact zero -- Phi^-1(1/2 + (i/8)(p - 1/2)),
  * i = 1..8, their 7-point negative counterpart and 0, p = (1 - 1/32 + 1 -

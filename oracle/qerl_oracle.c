@@ -310,8 +310,9 @@ void orc_mxfp4_dequant(const uint8_t* codes, const uint8_t* scales, int64_t n, i
 
 /* ------------------------------------------------------------------------ */
 /* NF4, the QLoRA format the digest sets against NVFP4 ([QeRL] "NVFP4      */
-/* Quantization", other 4-bit formats, and the QLoRA discussion: levels at   */
-/* quantiles of the Gaussian, recovered through a lookup table).  The digest */
+/* Quantization", comparison to other 4-bit formats; "QLoRA's 4-bit          */
+/* Quantization Addresses Memory but Degrades Speed": levels at quantiles of */
+/* the Gaussian, recovered through a lookup table).  The digest             */
 /* gives no construction; reading (the QLoRA one): 16 levels, ascending, are */
 /* standard-normal quantiles at evenly spaced probabilities with an exact    */
 /* zero -- 8 positive levels Phi^-1(1/2 + (i/8)(p - 1/2)), i = 1..8, 7       */

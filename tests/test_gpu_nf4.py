@@ -1,6 +1,7 @@
 """NF4 through the kernels, against the fp64 oracle.
 
-QeRL digest, "NVFP4 Quantization" (other 4-bit formats) and the QLoRA discussion: NF4's levels sit
+QeRL digest, "NVFP4 Quantization" (comparison to other 4-bit formats) and "QLoRA's 4-bit
+Quantization Addresses Memory but Degrades Speed": NF4's levels sit
 at Gaussian quantiles and are recovered through a lookup table.
 - qerl_nf4_quantize: codes, E4M3 scales and tensor scale bit-exact against orc.nf4_quantize (both
   decide each code in fp32 against fp32 level midpoints; each side computes its levels itself).

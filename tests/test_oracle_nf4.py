@@ -1,6 +1,7 @@
 """Pins for the oracle's NF4 format (the QLoRA 4-bit format the digest contrasts with NVFP4).
 
-QeRL digest, "NVFP4 Quantization" (other 4-bit formats) and the QLoRA discussion: NF4 places its
+QeRL digest, "NVFP4 Quantization" (comparison to other 4-bit formats) and "QLoRA's 4-bit
+Quantization Addresses Memory but Degrades Speed": NF4 places its
 levels at quantiles of the Gaussian and recovers them through a lookup table.  The construction
 (evenly spaced probabilities, 8 positive / 7 negative quantiles and an exact zero, normalised to
 [-1, 1]) is a reading; it is pinned to scipy's normal quantile function, which the oracle does not
