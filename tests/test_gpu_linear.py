@@ -93,6 +93,14 @@ SMALL = [
     (65, 128, 512, 8, 0.0),       # a single tile in pair mode
     (48, 384, 3584, 128, 1e-2),   # rank 128 at 33..64 tokens: the LoRA operand built late, in the idle ring
     (128, 512, 18944, 128, 5e-3), # rank 128 at 128 tokens, long K (pair mode, summed LoRA groups)
+    # pair mode at 33..64 tokens (one wave of pairs, separate activation ring)
+    (40, 512, 2048, 32, 1e-2),
+    (64, 768, 3584, 16, 5e-3),
+    # pair mode over several 128-token tiles (> 128 tokens)
+    (257, 512, 2048, 32, 1e-2),   # 3 token tiles, ragged last rows
+    (384, 256, 1536, 16, 5e-3),   # 6 weight stages (the pair-mode minimum)
+    (512, 1024, 2048, 0, 1e-2),   # 4 token tiles, no LoRA
+    (300, 256, 2048, 128, 1e-2),  # rank 128
 ]
 
 
@@ -293,3 +301,20 @@ def test_no_writes_past_the_buffers(q, orc, m, n, k, r):
                           *orc.quantize(W), z=wl.noise_vector(k, 1e-2, 95), A_bits=wl.lora_A_bits(r, k, 93, 2),
                           B_bits=wl.lora_B_bits(n, r, 94, 3), alpha=2.0 * r)
     assert_linear_close(y if rows is None else y[torch.from_numpy(rows).cuda()], ref, orc, what="guarded")
+
+
+def test_linear_group_pair_mode_several_token_tiles(q, orc):
+    """A grouped launch at 260 tokens (3 token tiles, pair mode) of two members with different
+    tile counts and ranks."""
+    m, k = 260, 2048
+    cases = [Case(q, orc, m, n, k, r, 1e-2, seed=90 + i) for i, (n, r) in enumerate([(512, 32), (768, 16)])]
+    x = cases[0].x
+    for c in cases:
+        c.x, c.x_bits, c.z, c.zd = x, cases[0].x_bits, cases[0].z, cases[0].zd
+    ys = [torch.full((m, c.n), float("nan"), dtype=torch.bfloat16, device="cuda") for c in cases]
+    lin = [(c.wp, c.S, c.A, c.B, c.alpha, y) for c, y in zip(cases, ys)]
+    ws = q.workspace(q.qerl_lora_linear_group_workspace_size(m, k, lin))
+    q.check(q.qerl_lora_linear_group(x, cases[0].zd, lin, ws))
+    assert q.qerl_read_status(ws) == 0
+    for c, y in zip(cases, ys):
+        assert_linear_close(y, c.oracle(orc), orc, what=f"pair group m{m} n{c.n}")
