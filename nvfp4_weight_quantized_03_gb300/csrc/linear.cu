@@ -824,6 +824,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const uint32_t acc_full = bars + 8u * (kB2 + 2);
   const uint32_t tmem_holder = bars + 8u * (kB2 + 3);
   const uint32_t t_full = bars + 8u * (kB2 + 4);
+  // Coupled: the activation slabs of the first ring's stages (later stages'
+  // ride in their weight slot's barrier).
+  const uint32_t x_early = bars + 8u * (kB2 + 5);
   // The activation ring has its own depth and barriers.
   auto b_full = [&](int s) { return bars + 8u * (kB2 + 8 + s); };
   auto b_empty = [&](int s) { return bars + 8u * (kB2 + 8 + kMaxB + s); };
@@ -890,6 +893,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     mbar_init_a(acc_full, n_iss);
 #endif
     mbar_init_a(t_full, 1);
+    mbar_init_a(x_early, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -929,26 +933,35 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     };
     // The first ring of weight blocks (and L2 prefetches further
     // ahead) is requested at once: the weights were written before the
-    // preceding kernel of this call started.  Coupled: the stages' activation
-    // slabs, and the arrivals that let them complete, follow once that kernel
-    // has finished.
+    // preceding kernel of this call started, and their barriers complete on
+    // the weight bytes alone, so the dequant of those stages runs while that
+    // kernel is still at work.  Coupled: the stages' activation slabs follow
+    // on their own barrier once it has finished.
     const int early = min(RS, nraw);
     if (lane == 0) {
       for (int i = 0; i < min(kPrefetch, nraw); ++i)
         for (int t = 0; t < ntl; ++t)
           bulk_prefetch_l2(wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes);
       for (int i = 0; i < early; ++i) {
-        if (coupled)
-          mbar_expect_tx_a(raw_full(i), kRawSlotBytes);
-        else
-          mbar_arrive_expect_tx_a(raw_full(i), ntl * kRawSlotBytes);
+        mbar_arrive_expect_tx_a(raw_full(i), ntl * kRawSlotBytes);
         for (int t = 0; t < ntl; ++t)
           bulk_load(sbase + p.off_raw + i * rslot + t * kRawSlotBytes,
                     wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes,
                     raw_full(i));
       }
     }
-    if (coupled) griddep_wait();
+    if (coupled) {
+      griddep_wait();
+      if (lane == 0) {
+        uint32_t xb = 0;
+        for (int i = 0; i < early; ++i) xb += xbytes_of(rb + i);
+        mbar_arrive_expect_tx_a(x_early, xb);
+        for (int i = 0; i < early; ++i)
+          bulk_load(sbase + p.off_b + i * p.raw_b_bytes,
+                    reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rb + i) * p.raw_b_bytes,
+                    xbytes_of(rb + i), x_early);
+      }
+    }
     if (lane == 0) {
       uint32_t ph = 0;
       for (int i = 0, s = 0; i < nraw; ++i) {
@@ -957,20 +970,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             bulk_prefetch_l2(wtile + t * tile_stride + static_cast<int64_t>(rb + i + kPrefetch) * kRawSlotBytes,
                              kRawSlotBytes);
         const int rst = rb + i;
-        const uint32_t xbytes = xbytes_of(rst);
-        if (i < early) {
-          if (coupled) mbar_arrive_expect_tx_a(raw_full(s), xbytes);
-        } else {
+        if (i >= early) {
+          const uint32_t xbytes = xbytes_of(rst);
           if (!mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status)) break;
           mbar_arrive_expect_tx_a(raw_full(s), ntl * kRawSlotBytes + xbytes);
           for (int t = 0; t < ntl; ++t)
             bulk_load(sbase + p.off_raw + s * rslot + t * kRawSlotBytes,
                       wtile + t * tile_stride + static_cast<int64_t>(rst) * kRawSlotBytes, kRawSlotBytes, raw_full(s));
+          if (coupled)
+            bulk_load(sbase + p.off_b + s * p.raw_b_bytes,
+                      reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rst) * p.raw_b_bytes, xbytes,
+                      raw_full(s));
         }
-        if (coupled)
-          bulk_load(sbase + p.off_b + s * p.raw_b_bytes,
-                    reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rst) * p.raw_b_bytes, xbytes,
-                    raw_full(s));
         if (++s == RS) {
           s = 0;
           ph ^= 1;
@@ -1089,7 +1100,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         uint32_t wph = 0;
         int js = 0, jsb = 0;  // separate activation ring: slab 0 is in slot 0, phase 0
         uint32_t jph = 0;
-        for (int wi = 0; wi < nraw; ++wi) {
+        // Coupled: the first ring's activation slabs have their own barrier
+        // (the first MMA always reads one of them).
+        const bool xe_ok = !p.coupled || warp_wait(x_early, 0, abort_flag, p.status);
+        for (int wi = 0; xe_ok && wi < nraw; ++wi) {
           if (!warp_wait(ab_full(w), wph, abort_flag, p.status)) break;
           const int nq = min(kSub, nmma - wi * kSub);
           const int u1 = min(u0 + per, 4 * nq);  // this issuer's MMAs in this weight stage: [u0, u1)
@@ -2289,7 +2303,9 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   const int issuers = pair ? 2 : (n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2));
   const uint32_t col_a = static_cast<uint32_t>(align_up(issuers * n_tok, 32));
   if (col_a > static_cast<uint32_t>(kTmemCols)) return QERL_ERR_UNSUPPORTED_SHAPE;
-  int ab_cap = std::min(kMaxAB, static_cast<int>((kTmemCols - col_a) / kAStageCols));
+  // (Up to four weight stages; the barrier pairs are per weight stage, or
+  // per (tile, MMA stage) in pair mode.)
+  int ab_cap = std::min(pair ? kMaxAB : 4 * kSub, static_cast<int>((kTmemCols - col_a) / kAStageCols));
   // The ring is handed over a weight stage (kSub consecutive MMA stages) at
   // a time: a multiple of kSub.
   ab_cap -= ab_cap % kSub;
