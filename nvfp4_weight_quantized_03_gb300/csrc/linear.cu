@@ -1436,15 +1436,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
               stsf(part + 4u * (tile_out + static_cast<uint32_t>((c + e) * kTileN + nl)), ok ? w[e] * sc[e] : 0.0f);
         } else if (p.stage_out) {
           // staged [tile][token][128 rows], stored below as 16-byte vectors
+          const uint32_t el0 = tile_out + static_cast<uint32_t>(c * kTileN + nl);
+          if (L.y_f32) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            if (c + e >= p.n_tok) break;
-            const uint32_t el = tile_out + static_cast<uint32_t>((c + e) * kTileN + nl);
-            const float val = ok ? w[e] * sc[e] : 0.0f;
-            if (L.y_f32)
-              stsf(sbase + 4u * el, val);
-            else
-              sts16(sbase + 2u * el, __bfloat16_as_ushort(__float2bfloat16_rn(val)));
+            for (int e = 0; e < 32; ++e)
+              if (c + e < p.n_tok) stsf(sbase + 4u * (el0 + e * kTileN), ok ? w[e] * sc[e] : 0.0f);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c + e < p.n_tok)
+                sts16(sbase + 2u * (el0 + e * kTileN), __bfloat16_as_ushort(__float2bfloat16_rn(ok ? w[e] * sc[e] : 0.0f)));
           }
         } else if (n < L.N) {
 #pragma unroll
@@ -1487,9 +1488,30 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int e = 0; e < 32; ++e) emit(c, e, ok ? w[e] * sc[e] : 0.0f);
       }
     } else {
+    // (This runs once per CTA, its instructions fetched cold: kept compact --
+    // a rolled loop over groups of four accumulators, one store loop per
+    // output kind.)
+    auto emit8 = [&](int c, const float (&val)[8]) {
+      const uint32_t el0 = tile_out + static_cast<uint32_t>(c * kTileN + nl);
+      if (p.split > 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) stsf(part + 4u * (el0 + e * kTileN), val[e]);
+      } else if (!p.stage_out) {
+        for (int e = 0; e < 8; ++e)
+          if (m0 + c + e < p.M && n < L.N) store_out(L, m0 + c + e, n, val[e]);
+      } else if (L.y_f32) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) stsf(sbase + 4u * (el0 + e * kTileN), val[e]);  // staged: [tile][token][128 rows]
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          sts16(sbase + 2u * (el0 + e * kTileN), __bfloat16_as_ushort(__float2bfloat16_rn(val[e])));
+      }
+    };
     for (int c = c0; !p.pair && c < c0 + cols; c += 8) {
       float v[8];
       // Four accumulators' columns per wait (issuer 0's holds the LoRA term).
+#pragma unroll 1
       for (int a0 = 0; a0 < nacc; a0 += 4) {
         float w[4][8];
 #pragma unroll
@@ -1508,8 +1530,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
       const float4 s0 = lds128f(smv + 4u * c), s1 = lds128f(smv + 4u * (c + 4));
       const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      float o8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) emit(c, e, ok ? v[e] * sc[e] : 0.0f);
+      for (int e = 0; e < 8; ++e) o8[e] = ok ? v[e] * sc[e] : 0.0f;
+      emit8(c, o8);
     }
     }
     if (p.split == 1 && p.stage_out) {
@@ -1576,64 +1600,50 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // store when the row pitch and base allow it.
       const bool vec4 = (reinterpret_cast<uintptr_t>(L.y) & 15u) == 0 && L.N % 4 == 0;
       const int per_tile = max(0, me - mb) * (kTileN / 4);
-      // Every partner's partial tile, mapped once.  Each thread sums two
-      // 4-column groups at a time and issues all their remote loads (up to
-      // 2 x 8) before the first add, so the distributed-shared-memory latency
-      // is paid once per group pair, not once per partner.
+      // Every partner's partial tile, mapped once.  Each thread sums one
+      // 4-column group per step and issues all its partners' remote loads (up
+      // to 8) before the first add, so the distributed-shared-memory latency
+      // is paid once per group, not once per partner.  (One group per step,
+      // not two: this code runs once per CTA and its instructions are fetched
+      // cold, so it is kept small.)
       uint32_t rpart[kMaxSplit];
 #pragma unroll
       for (int qq = 0; qq < kMaxSplit; ++qq) rpart[qq] = qq < p.split ? mapa_shared(part, qq) : 0u;
-      for (int it0 = dt; it0 < ntl_e * per_tile; it0 += 512) {
-        float4 v[2][kMaxSplit];
-        uint32_t off[2];
-        bool have[2];
+      for (int it = dt; it < ntl_e * per_tile; it += 256) {
+        const int t = it / per_tile, rem = it - t * per_tile;
+        const int ml = mb + rem / (kTileN / 4);
+        const int nl4 = 4 * (rem % (kTileN / 4)) + t * kTileN;  // column within this CTA's tiles
+        const uint32_t off = 4u * static_cast<uint32_t>(t * p.n_tok * kTileN + ml * kTileN + 4 * (rem % (kTileN / 4)));
+        float4 v[kMaxSplit];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int it = it0 + u * 256;
-          have[u] = it < ntl_e * per_tile;
-          const int t = have[u] ? it / per_tile : 0, rem = have[u] ? it - t * per_tile : 0;
-          const int ml = mb + rem / (kTileN / 4);
-          off[u] = 4u * static_cast<uint32_t>(t * p.n_tok * kTileN + ml * kTileN + 4 * (rem % (kTileN / 4)));
-        }
+        for (int qq = 0; qq < kMaxSplit; ++qq)
+          if (qq < p.split) v[qq] = ld_shared_cluster_f32x4(rpart[qq] + off);
+        float4 acc = v[0];
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-          for (int qq = 0; qq < kMaxSplit; ++qq)
-            if (have[u] && qq < p.split) v[u][qq] = ld_shared_cluster_f32x4(rpart[qq] + off[u]);
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (!have[u]) continue;
-          const int it = it0 + u * 256;
-          const int t = it / per_tile, rem = it - t * per_tile;
-          const int ml = mb + rem / (kTileN / 4);
-          const int nl4 = 4 * (rem % (kTileN / 4)) + t * kTileN;  // column within this CTA's tiles
-          float4 acc = v[u][0];
-#pragma unroll
-          for (int qq = 1; qq < kMaxSplit; ++qq)
-            if (qq < p.split) {
-              acc.x += v[u][qq].x;
-              acc.y += v[u][qq].y;
-              acc.z += v[u][qq].z;
-              acc.w += v[u][qq].w;
-            }
-          const float out[4] = {acc.x, acc.y, acc.z, acc.w};
-          const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0 + nl4;
-          if (vec4 && n0 + nl4 + 3 < L.N) {
-            if (L.y_f32) {
-              *reinterpret_cast<float4*>(reinterpret_cast<float*>(L.y) + gi) = acc;
-            } else {
-              uint2 pk;
-              pk.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
-                     (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
-              pk.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
-                     (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
-              *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(L.y) + gi) = pk;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (n0 + nl4 + e < L.N) store_out(L, m0 + ml, n0 + nl4 + e, out[e]);
+        for (int qq = 1; qq < kMaxSplit; ++qq)
+          if (qq < p.split) {
+            acc.x += v[qq].x;
+            acc.y += v[qq].y;
+            acc.z += v[qq].z;
+            acc.w += v[qq].w;
           }
+        const int64_t gi = static_cast<int64_t>(m0 + ml) * L.N + n0 + nl4;
+        if (vec4 && n0 + nl4 + 3 < L.N) {
+          if (L.y_f32) {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(L.y) + gi) = acc;
+          } else {
+            uint2 pk;
+            pk.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
+            pk.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(L.y) + gi) = pk;
+          }
+        } else {
+          const float out[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (n0 + nl4 + e < L.N) store_out(L, m0 + ml, n0 + nl4 + e, out[e]);
         }
       }
     }
