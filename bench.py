@@ -301,11 +301,10 @@ def group_algorithmic_bytes(lins, m, r=RANK_R):
 # 18944 x 3584 linears sharing x; the largest of the step's four launches) at
 # M = 8.  DRAM traffic of one such launch (prep_kernel + mma_kernel):
 # dram__bytes_read.sum + dram__bytes_write.sum from a 1-pass ncu capture of
-# `bench.py --case 8,18944+18944,3584,32` (taken on the build with the NF4
-# table path and the tensor-core LoRA down-projection; the 8-token decode path
-# is unchanged since).
+# `bench.py --case 8,18944+18944,3584,32` (taken on the build with the compact
+# epilogue and the early weight stages that complete without the activations).
 DOMINANT = ("gate_up", 8)
-DOMINANT_TRAFFIC_BYTES = 79695360  # prep 599,296 + mma 79,077,632 read + 18,432 written (ncu, 1 pass)
+DOMINANT_TRAFFIC_BYTES = 79666944  # prep 599,552 + mma 79,044,608 read + 22,784 written (ncu, 1 pass)
 
 
 def dominant_call(q, layers, acts, hbm_peak, reps=64):
@@ -346,7 +345,7 @@ def dominant_call(q, layers, acts, hbm_peak, reps=64):
     names = " + ".join(f"{l.name} {l.n}x{l.k}" for l in lins)
     return {
         "bound": "hbm",
-        "kernel": f"qerl_lora_linear_group launch (prep_kernel + mma_kernel<1>), Qwen2.5-7B {names}, "
+        "kernel": f"qerl_lora_linear_group launch (prep_kernel + mma_kernel), Qwen2.5-7B {names}, "
                   f"M={m}, r={RANK_R}",
         "achieved": round(achieved, 1),
         "peak": hbm_peak,
