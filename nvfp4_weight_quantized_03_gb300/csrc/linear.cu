@@ -437,18 +437,44 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   for (int i = 0; i < kRowsPerThread; ++i) part[(kRowsPerThread * rq + i) * kLoraTileR + lr] = acc[i];
   cluster_sync_all();
   const uint32_t part_s = smem_u32(part);
+  // Every partner's value is loaded before the first add (the remote-load
+  // latency is paid once, not once per partner), then added in rank order.
+  // A thread sums at most two entries (512 per tile, >= 256 threads).
+  constexpr int kPerThread = (kLoraTileM * kLoraTileR + kPrepThreads - 1) / kPrepThreads;
+  float vsum[kPerThread];
+  int vidx[kPerThread];
+  int nsum = 0;
   for (int idx = ks * kPrepThreads + tid; idx < kLoraTileM * kLoraTileR; idx += p.cluster * kPrepThreads) {
+    float vq[kPrepMaxCluster];
+#pragma unroll
+    for (int q = 0; q < kPrepMaxCluster; ++q)
+      vq[q] = q < p.cluster ? ld_shared_cluster_f32(mapa_shared(part_s + 4u * idx, q)) : 0.0f;
     float v = 0.0f;
-    for (int q = 0; q < p.cluster; ++q) v += ld_shared_cluster_f32(mapa_shared(part_s + 4u * idx, q));
-    const int row = row0 + idx / kLoraTileR, rank = rank0 + idx % kLoraTileR;
+#pragma unroll
+    for (int q = 0; q < kPrepMaxCluster; ++q)
+      if (q < p.cluster) v += vq[q];
+    vsum[nsum] = v;
+    vidx[nsum] = idx;
+    ++nsum;
+  }
+  // Done with the partners' shared memory: they may leave once all have
+  // arrived, and the writes below overlap that wait -- unless the group sum
+  // follows, whose counter must see every partner's writes first (release).
+  const bool group_sum = p.sum_groups && p.groups > 1;
+  if (!group_sum) cluster_arrive();
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) {
+    if (u >= nsum) break;
+    const int row = row0 + vidx[u] / kLoraTileR, rank = rank0 + vidx[u] % kLoraTileR;
     if (row < p.M && rank < rr_) {
       if (p.sum_groups && p.groups == 1)
-        p.tf[li][static_cast<int64_t>(row) * rr_ + rank] = v;  // one group: already the sum
+        p.tf[li][static_cast<int64_t>(row) * rr_ + rank] = vsum[u];  // one group: already the sum
       else
-        tout[(static_cast<int64_t>(g) * p.M + row) * rr_ + rank] = v;
+        tout[(static_cast<int64_t>(g) * p.M + row) * rr_ + rank] = vsum[u];
     }
   }
-  cluster_sync_all();  // partners are done reading this CTA's partial tile; the group's writes are ordered
+  if (group_sum) cluster_arrive();
+  cluster_wait();  // partners are done reading this CTA's partial tile
   if (!p.sum_groups || p.groups == 1) return;
   // The last cluster to finish this LoRA tile (one per K group) adds the
   // groups' partial sums in group order -- deterministic -- into tf, so the
@@ -1647,7 +1673,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
       }
     }
-    cluster_sync_all();  // partners are done reading this CTA's partial tile
+    // Partners are done reading this CTA's partial tile.  (Relaxed: this
+    // CTA's own remote loads have all been consumed, and its output stores
+    // need not be ordered for the partners.)
+    cluster_arrive_relaxed();
+    cluster_wait();
   }
   if (warp == kIssuerWarp0) tmem_dealloc(tmem_base, kTmemCols);
 }
