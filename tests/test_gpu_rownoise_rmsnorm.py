@@ -152,3 +152,27 @@ def test_rmsnorm_fused_linear(q, orc, m):
     for y, oc, osc, oS, A_bits, B_bits, alpha in ys:
         ref = orc.lora_linear(xt_bits, oc, osc, oS, z=None, A_bits=A_bits, B_bits=B_bits, alpha=alpha)
         assert_linear_close(y, ref, orc, what=f"rmsnorm fused m{m} n{oc.shape[0]}")
+
+
+@pytest.mark.parametrize("m", [1, 13, 16])
+def test_grouped_lora_ranks_per_row_noise(q, orc, m):
+    """Four linears of one input with ranks 32, 8, 24 and 16 at up to 16 tokens (four LoRA tiles of
+    the prep kernel per K slice, one per linear, each with its own rank padding), with per-row
+    noise and a ragged row count: every output against the oracle."""
+    k = 1536
+    shapes = [(384, 32), (256, 8), (128, 24), (512, 16)]
+    x_bits = wl.activations_bits(m, k, 92, 1)
+    z = _row_noise(m, k, 1e-2, 93)
+    x, zd = dev_bf16(x_bits), torch.from_numpy(z).cuda()
+    descs, refs = [], []
+    for i, (n, r) in enumerate(shapes):
+        wp, S, oc, osc, oS = _weights(q, orc, n, k, seed=94 + i)
+        A_bits, B_bits = wl.lora_A_bits(r, k, 100 + i, 2), wl.lora_B_bits(n, r, 110 + i, 3)
+        y = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+        descs.append((wp, S, dev_bf16(A_bits), dev_bf16(B_bits), 2.0 * r, y))
+        refs.append(orc.lora_linear(x_bits, oc, osc, oS, z=z, A_bits=A_bits, B_bits=B_bits, alpha=2.0 * r))
+    ws = q.workspace(q.qerl_lora_linear_group_workspace_size(m, k, descs))
+    q.check(q.qerl_lora_linear_group_rowz(x, zd, descs, ws))
+    assert q.qerl_read_status(ws) == 0
+    for (n, r), d, ref in zip(shapes, descs, refs):
+        assert_linear_close(d[5], ref, orc, what=f"grouped ranks m{m} n{n} r{r}")
