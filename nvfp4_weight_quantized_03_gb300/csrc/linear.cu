@@ -2338,9 +2338,13 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // The dequantized weights go to tensor memory as the MMA's A operand.
   // Each MMA occupies its issuing thread for ~150 cycles whatever the token
   // count, so small tiles take more issuers (each with its own accumulator,
-  // which tensor memory must hold next to the A ring).
-  // Pair mode: one issuer per tile.
-  const int issuers = pair ? 2 : (n_tok <= 32 ? 8 : (n_tok <= 64 ? 4 : 2));
+  // which tensor memory must hold next to the A ring, and which the epilogue
+  // reads and adds).  Four issuers up to 64 tokens: 600 issue cycles per
+  // weight stage against a ~1250-cycle stage period, one tensor-memory read
+  // round in the epilogue and a third weight stage of A at 32 tokens
+  // (measured 1.2% faster than eight at <= 32 tokens, and two issuers 5%
+  // slower).  Pair mode: one issuer per tile.
+  const int issuers = pair ? 2 : (n_tok <= 64 ? 4 : 2);
   const uint32_t col_a = static_cast<uint32_t>(align_up(issuers * n_tok, 32));
   if (col_a > static_cast<uint32_t>(kTmemCols)) return QERL_ERR_UNSUPPORTED_SHAPE;
   // (Up to four weight stages; the barrier pairs are per weight stage, or
