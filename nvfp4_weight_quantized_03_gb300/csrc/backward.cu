@@ -161,8 +161,18 @@ __global__ void __launch_bounds__(kThreads) skinny_reduce_kernel(const float* __
     // transposed: idx walks [j][p] (p fastest, coalesced stores); else [p][j]
     const int64_t p = transposed ? idx % P : idx / r;
     const int64_t j = transposed ? idx / P : idx % r;
+    // Eight partials' loads in flight before their adds (in split order).
+    const float* src = partial + p * r + j;
     float v = 0.0f;
-    for (int sp = 0; sp < splits; ++sp) v += partial[sp * total + p * r + j];
+    int sp = 0;
+    for (; sp + 8 <= splits; sp += 8) {
+      float w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) w[u] = __ldg(src + (sp + u) * total);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v += w[u];
+    }
+    for (; sp < splits; ++sp) v += __ldg(src + sp * total);
     out[idx] = scale * v;
   }
 }
@@ -185,9 +195,10 @@ SkinnyPlan skinny_plan(int64_t M, int64_t P, int r) {
   while (8 * s.jg < r) s.jg *= 2;
   s.ptile = 4 * (kThreads / s.jg);
   s.ptiles = static_cast<int>((P + s.ptile - 1) / s.ptile);
-  // Enough blocks for two waves, at least 64 tokens per split.
+  // Two blocks per SM at most (one wave; a few blocks over that would form a
+  // second wave of their own), at least 64 tokens per split.
   const int64_t max_splits = std::max<int64_t>(1, (M + 63) / 64);
-  int64_t splits = std::max<int64_t>(1, (2 * sms() + s.ptiles - 1) / s.ptiles);
+  int64_t splits = std::max<int64_t>(1, (2 * sms()) / s.ptiles);
   splits = std::min(splits, max_splits);
   const int64_t mps = ((M + splits - 1) / splits + kSkM - 1) / kSkM * kSkM;
   s.m_per_split = static_cast<int>(std::max<int64_t>(mps, kSkM));
