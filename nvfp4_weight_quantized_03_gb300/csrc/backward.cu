@@ -15,10 +15,10 @@
 // tensor-core kernel, its pipelines and its epilogue are the forward's; only
 // the weight layout's scale addressing differs.
 // dA and dB are rank-r products summed over the m tokens: t = x~ A^T comes
-// from the prep kernel's LoRA tiles, and `skinny_kernel` forms
-// out[p][j] = sum_m X[m][p] T[m][j] (X = dy or x~, T = t or u) on CUDA cores,
-// split over m into fixed partial sums that `skinny_reduce_kernel` adds in
-// order (deterministic).
+// from the LoRA down-projection kernels, and `skinny_tc_kernel` forms
+// out[p][j] = sum_m X[m][p] T[m][j] (X = dy or x~, T = t or u) on the tensor
+// cores, split over m into fixed partial sums that `skinny_reduce_kernel`
+// adds in order (deterministic).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -31,7 +31,6 @@ namespace qerl {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSkM = 32;  // tokens per shared-memory chunk
 
 // out[c][r] = in[r][c] for a bf16 rows x cols matrix (row stride ld_in); 32x32 tiles.
 __global__ void __launch_bounds__(kThreads) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in, int64_t ld_in,
@@ -51,103 +50,176 @@ __global__ void __launch_bounds__(kThreads) transpose_bf16_kernel(const __nv_bfl
   }
 }
 
-// Partial sums over the token range of split blockIdx.y:
-//   partial[split][p][j] = sum_{m in range} X[m][p] * T[m][j],
-// T[m][j] = sum over `parts` arrays (part_stride apart) of [m][r] fp32.
-// A thread owns 4 consecutive p and 8 consecutive j; the block's p tile is
-// 4 * (256 / jg) wide, jg = the power of two >= ceil(r / 8).  kSkM-token
-// chunks go through shared memory (X as fp32, T summed over its parts); the
-// next chunk's loads are issued into registers before the current chunk's
-// FMAs, so their latency overlaps the arithmetic.
-template <int JG>
-__global__ void __launch_bounds__(kThreads) skinny_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int M,
-                                                          int P, const float* __restrict__ T, int parts,
-                                                          int64_t part_stride, int r, int m_per_split,
-                                                          float* __restrict__ partial) {
-  extern __shared__ __align__(16) float sk_smem[];
-  constexpr int ptile = 4 * (kThreads / JG);
-  constexpr int tw = 8 * JG;
-  constexpr int nxv = kSkM * ptile / 8 / kThreads;  // X loads (8 bf16 each) per thread per chunk
-  constexpr int ntv = kSkM * tw / kThreads;          // T values per thread per chunk
-  static_assert(nxv >= 1 && ntv >= 1, "chunk covers every thread");
-  constexpr int kSkMaxXv = nxv, kSkMaxTv = ntv;
-  float* Xs = sk_smem;                 // [kSkM][ptile]
-  float* Ts = sk_smem + kSkM * ptile;  // [kSkM][tw]
-  const int p0 = blockIdx.x * ptile;
+// ---------------------------------------------------------------------------
+// Partial sums over the token range of split blockIdx.y, on the tensor cores:
+//   partial[split][p][j] = sum_{m in range} X[m][p] * T[m][j]
+// (T[m][j] = sum over `parts` arrays, part_stride apart, of [m][r] fp32), as
+//   D[p][j] += sum_m A[p][m] B[j][m],  A = X^T (128 p rows per CTA), B = T^T.
+// Each 64-token chunk of X (bf16) is transposed through registers into the
+// K-major 128-byte-swizzled layout of A (128 rows x 64 tokens), and T (fp32)
+// into three bf16 terms t1 = bf16(T), t2 = bf16(T - t1), t3 = bf16(T - t1 -
+// t2) (together T to ~24 significant bits), each laid out likewise as a B
+// tile (rn = round16(r) rows x 64 tokens).  Per chunk 4 K-steps x 3 MMAs
+// (M = 128, N = rn, K = 16, bf16 products exact, fp32 accumulation in tensor
+// memory); two chunk buffers, each released by the MMAs' commit.
+constexpr int kTcThreads = 256;
+constexpr int kTcM = 64;   // tokens per chunk (the MMAs' K)
+constexpr int kTcP = 128;  // p rows per CTA (the MMAs' M)
+__host__ __device__ inline int tc_rn(int r) { return (r + 15) / 16 * 16; }
+__host__ __device__ inline int tc_tmem_cols(int r) {
+  int c = 32;
+  while (c < tc_rn(r)) c *= 2;
+  return c;
+}
+__host__ __device__ inline uint32_t tc_buf_bytes(int r) { return 16384u + 3u * static_cast<uint32_t>(tc_rn(r)) * 128u; }
+__host__ __device__ inline size_t tc_smem_bytes(int r) { return 1024 + 2 * static_cast<size_t>(tc_buf_bytes(r)) + 64; }
+
+// Byte offset of the 32-bit word holding elements (kl, kl + 1) of row R in a
+// K-major 128-byte-swizzled tile (64 elements per 128-byte row, kl even).
+__device__ __forceinline__ uint32_t sw128_word(int R, int kl) {
+  return static_cast<uint32_t>((R >> 3) * 1024 + (R & 7) * 128 + ((((kl >> 3) ^ (R & 7)) << 4)) + (kl & 7) * 2);
+}
+__device__ __forceinline__ uint32_t bf16_bits(float v) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) skinny_tc_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx,
+                                                                 int M, int P, const float* __restrict__ T,
+                                                                 int parts, int64_t part_stride, int r,
+                                                                 int m_per_split, float* __restrict__ partial,
+                                                                 int* status) {
+  extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
+  const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(tc_smem_raw));
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = tc_smem_raw + (sbase - raw);
+  const int rn = tc_rn(r);
+  const uint32_t bufb = tc_buf_bytes(r);
+  const uint32_t bars = sbase + 2 * bufb;
+  auto mma_done = [&](int b) { return bars + 8u * b; };
+  const uint32_t acc_done = bars + 16u;
+  const uint32_t holder = bars + 24u;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + 2 * bufb + 28);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int p0 = blockIdx.x * kTcP;
   const int m_begin = blockIdx.y * m_per_split, m_end = min(M, m_begin + m_per_split);
-  const int tj = threadIdx.x % JG, tp = threadIdx.x / JG;
-  float acc[4][8];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
-  uint4 xv[kSkMaxXv];
-  float tv[kSkMaxTv];
-  auto load = [&](int m0) {
-#pragma unroll
-    for (int u = 0; u < kSkMaxXv; ++u) {
-      const int idx = threadIdx.x + u * kThreads;
-      const int row = idx / (ptile / 8), c8 = (idx % (ptile / 8)) * 8;
-      const int m = m0 + row, p = p0 + c8;
-      xv[u] = (m < m_end && p < P) ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m) * ldx + p))
-                                   : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kSkMaxTv; ++u) {
-      const int idx = threadIdx.x + u * kThreads;
-      const int row = idx / tw, j = idx % tw;
-      const int m = m0 + row;
-      float v = 0.0f;
-      if (m < m_end && j < r)
-        for (int g = 0; g < parts; ++g) v += __ldg(T + g * part_stride + static_cast<int64_t>(m) * r + j);
-      tv[u] = v;
-    }
-  };
-  auto store = [&]() {
-#pragma unroll
-    for (int u = 0; u < kSkMaxXv; ++u) {
-      const int idx = threadIdx.x + u * kThreads;
-      const int row = idx / (ptile / 8), c8 = (idx % (ptile / 8)) * 8;
-      const uint32_t w[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-      float4* d = reinterpret_cast<float4*>(Xs + row * ptile + c8);
-      d[0] = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u),
-                         __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
-      d[1] = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u),
-                         __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
-    }
-#pragma unroll
-    for (int u = 0; u < kSkMaxTv; ++u) Ts[threadIdx.x + u * kThreads] = tv[u];
-  };
-  if (m_begin < m_end) load(m_begin);
-  for (int m0 = m_begin; m0 < m_end; m0 += kSkM) {
-    store();
-    __syncthreads();
-    if (m0 + kSkM < m_end) load(m0 + kSkM);  // in flight during the FMAs below
-#pragma unroll 4
-    for (int mm = 0; mm < kSkM; ++mm) {
-      const float4 xq = *reinterpret_cast<const float4*>(Xs + mm * ptile + 4 * tp);
-      const float4 t0 = *reinterpret_cast<const float4*>(Ts + mm * tw + 8 * tj);
-      const float4 t1 = *reinterpret_cast<const float4*>(Ts + mm * tw + 8 * tj + 4);
-      const float xa[4] = {xq.x, xq.y, xq.z, xq.w};
-      const float ta[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xa[a], ta[b], acc[a][b]);
-    }
-    __syncthreads();
+  const uint32_t ncols = static_cast<uint32_t>(tc_tmem_cols(r));
+  if (tid == 0) {
+    mbar_init_a(mma_done(0), 1);
+    mbar_init_a(mma_done(1), 1);
+    mbar_init_a(acc_done, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
   }
-  float* out = partial + static_cast<int64_t>(blockIdx.y) * P * r;
+  if (warp == 0) {
+    tmem_alloc(holder, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + 2 * bufb + 24);
+  const uint32_t idesc = idesc_bf16_f32(kTcP, static_cast<uint32_t>(rn));
+  const int nchunks = m_end > m_begin ? (m_end - m_begin + kTcM - 1) / kTcM : 0;
+  bool ok = true;
+  for (int c = 0; c < nchunks; ++c) {
+    const int b = c & 1;
+    const uint32_t abuf = sbase + static_cast<uint32_t>(b) * bufb, bbuf = abuf + 16384u;
+    // The buffer's previous MMAs (chunk c - 2) are done reading it.
+    if (c >= 2 && !mbar_wait_a(mma_done(b), static_cast<uint32_t>(((c - 2) >> 1) & 1), abort_flag, status)) {
+      ok = false;
+      break;
+    }
+    const int m0 = m_begin + c * kTcM;
+    {
+      // X: a thread takes token rows (ml, ml + 1) and 16 consecutive p.
+      const int ml = 2 * (tid >> 3), pl = (tid & 7) * 16;
+      const int m = m0 + ml, p = p0 + pl;
+      uint4 x0[2], x1[2];
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int p = p0 + 4 * tp + a;
-    if (p >= P) continue;
+      for (int h = 0; h < 2; ++h) {
+        x0[h] = (m < m_end && p < P) ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m) * ldx + p + 8 * h))
+                                     : make_uint4(0u, 0u, 0u, 0u);
+        x1[h] = (m + 1 < m_end && p < P)
+                    ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m + 1) * ldx + p + 8 * h))
+                    : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int j = 8 * tj + b;
-      if (j < r) out[static_cast<int64_t>(p) * r + j] = acc[a][b];
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t a[4] = {x0[h].x, x0[h].y, x0[h].z, x0[h].w};
+        const uint32_t c4[4] = {x1[h].x, x1[h].y, x1[h].z, x1[h].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int R = pl + 8 * h + 2 * k;  // rows R (low halves) and R + 1 (high halves)
+          sts32(abuf + sw128_word(R, ml), __byte_perm(a[k], c4[k], 0x5410));
+          sts32(abuf + sw128_word(R + 1, ml), __byte_perm(a[k], c4[k], 0x7632));
+        }
+      }
+    }
+    // T: items (token pair, j), j fastest (coalesced loads); rows j >= r are zero.
+    for (int it = tid; it < (kTcM / 2) * rn; it += kTcThreads) {
+      const int ml = 2 * (it / rn), j = it % rn;
+      const int m = m0 + ml;
+      float t0 = 0.0f, t1 = 0.0f;
+      if (j < r) {
+        for (int g = 0; g < parts; ++g) {
+          if (m < m_end) t0 += __ldg(T + g * part_stride + static_cast<int64_t>(m) * r + j);
+          if (m + 1 < m_end) t1 += __ldg(T + g * part_stride + static_cast<int64_t>(m + 1) * r + j);
+        }
+      }
+      const uint32_t off = sw128_word(j, ml);
+      float u0 = t0, u1 = t1;
+#pragma unroll
+      for (int k3 = 0; k3 < 3; ++k3) {
+        const uint32_t h0 = bf16_bits(u0), h1 = bf16_bits(u1);
+        sts32(bbuf + static_cast<uint32_t>(k3 * rn * 128) + off, h0 | (h1 << 16));
+        u0 -= __uint_as_float(h0 << 16);  // exact: the remainder of a rounding
+        u1 -= __uint_as_float(h1 << 16);
+      }
+    }
+    fence_proxy_async_smem();  // the tiles are read by the MMAs (async proxy)
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < kTcM / 16; ++ks) {
+        const uint64_t ad = sw128_kmajor_desc(abuf + 32u * ks);
+#pragma unroll
+        for (int k3 = 0; k3 < 3; ++k3)
+          tc_mma_f16(tmem, ad, sw128_kmajor_desc(bbuf + static_cast<uint32_t>(k3 * rn * 128) + 32u * ks), idesc,
+                     (c > 0 || ks > 0 || k3 > 0) ? 1u : 0u);
+      }
+      tc_commit(mma_done(b));
     }
   }
+  if (tid == 0) tc_commit(acc_done);  // once every MMA issued above is done (at once without any)
+  ok = mbar_wait_a(acc_done, 0, abort_flag, status) && ok;
+  tc_fence_after();
+  // Warp w reads lanes 32 (w % 4) .. + 31 (its TMEM quadrant), columns of half w / 4.
+  {
+    const int q = warp & 3, half = warp >> 2;
+    const int p = p0 + 32 * q + lane;
+    float* out = partial + static_cast<int64_t>(blockIdx.y) * P * r + static_cast<int64_t>(p) * r;
+    const int cb = half * (rn / 2), ce = cb + rn / 2;
+    for (int c8 = cb; c8 < ce; c8 += 8) {
+      float v[8];
+      tmem_ld_x8(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c8), v);
+      tmem_ld_wait();
+      if (p < P) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (c8 + e < r) out[c8 + e] = (ok && nchunks > 0) ? v[e] : 0.0f;
+      }
+    }
+  }
+  if (*abort_flag) {
+    // Let the MMAs already issued finish before shared and tensor memory go.
+    const long long t0 = clock64();
+    while (clock64() - t0 < 200000ll) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 
 // out = scale * sum over the splits, in split order: [P][r] (transposed = 0)
@@ -184,28 +256,23 @@ int sms() {
   return n;
 }
 
-struct SkinnyPlan {
-  int jg, ptile, ptiles, splits, m_per_split;
+// The tensor-core reduction's grid: 128 p rows per block, the tokens split
+// so that the blocks fit one wave at two per SM, 64-token chunks.
+struct TcPlan {
+  int ptiles, splits, m_per_split;
   size_t smem;
 };
-
-SkinnyPlan skinny_plan(int64_t M, int64_t P, int r) {
-  SkinnyPlan s;
-  s.jg = 1;
-  while (8 * s.jg < r) s.jg *= 2;
-  s.ptile = 4 * (kThreads / s.jg);
-  s.ptiles = static_cast<int>((P + s.ptile - 1) / s.ptile);
-  // Two blocks per SM at most (one wave; a few blocks over that would form a
-  // second wave of their own), at least 64 tokens per split.
-  const int64_t max_splits = std::max<int64_t>(1, (M + 63) / 64);
-  int64_t splits = std::max<int64_t>(1, (2 * sms()) / s.ptiles);
+TcPlan skinny_tc_plan(int64_t M, int64_t P, int r) {
+  TcPlan t;
+  t.ptiles = static_cast<int>((P + kTcP - 1) / kTcP);
+  const int64_t max_splits = std::max<int64_t>(1, (M + kTcM - 1) / kTcM);
+  int64_t splits = std::max<int64_t>(1, (2 * sms()) / t.ptiles);
   splits = std::min(splits, max_splits);
-  const int64_t mps = ((M + splits - 1) / splits + kSkM - 1) / kSkM * kSkM;
-  s.m_per_split = static_cast<int>(std::max<int64_t>(mps, kSkM));
-  s.splits = static_cast<int>((M + s.m_per_split - 1) / s.m_per_split);
-  if (s.splits < 1) s.splits = 1;
-  s.smem = static_cast<size_t>(kSkM) * (s.ptile + 8 * s.jg) * sizeof(float);
-  return s;
+  const int64_t mps = ((M + splits - 1) / splits + kTcM - 1) / kTcM * kTcM;
+  t.m_per_split = static_cast<int>(std::max<int64_t>(mps, kTcM));
+  t.splits = std::max(1, static_cast<int>((M + t.m_per_split - 1) / t.m_per_split));
+  t.smem = tc_smem_bytes(r);
+  return t;
 }
 
 struct BwdLayout {
@@ -226,7 +293,7 @@ BwdLayout bwd_layout(int64_t m, int64_t n, int64_t k, int r) {
   L.partial = off;  // skinny partial sums, reused by dB then dA
   size_t part = 0;
   if (r > 0) {
-    const SkinnyPlan pb = skinny_plan(m, n, r), pa = skinny_plan(m, k, r);
+    const TcPlan pb = skinny_tc_plan(m, n, r), pa = skinny_tc_plan(m, k, r);
     part = std::max(static_cast<size_t>(pb.splits) * n * r, static_cast<size_t>(pa.splits) * k * r) * 4;
   }
   off = align_up(off + part, 256);
@@ -235,33 +302,22 @@ BwdLayout bwd_layout(int64_t m, int64_t n, int64_t k, int r) {
 }
 
 qerl_status launch_skinny(const void* X, int64_t ldx, int64_t M, int64_t P, const LoraDown& T, int r, float scale,
-                          bool transposed, float* partial, float* out, cudaStream_t s) {
-  const SkinnyPlan sp = skinny_plan(M, P, r);
+                          bool transposed, float* partial, float* out, int* status, cudaStream_t s) {
+  const TcPlan tp = skinny_tc_plan(M, P, r);
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    const int lim = 160 * 1024;  // the r <= 8 tile: 32 x (1024 + 8) floats
-    err = cudaFuncSetAttribute(skinny_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    err = cudaFuncSetAttribute(skinny_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tc_smem_bytes(128)));
   });
   if (err != cudaSuccess) return QERL_ERR_CUDA;
-  const dim3 grid(static_cast<unsigned>(sp.ptiles), static_cast<unsigned>(sp.splits));
-  const auto* xb = static_cast<const __nv_bfloat16*>(X);
-  const int Mi = static_cast<int>(M), Pi = static_cast<int>(P);
-  switch (sp.jg) {
-    case 1: skinny_kernel<1><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
-    case 2: skinny_kernel<2><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
-    case 4: skinny_kernel<4><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
-    case 8: skinny_kernel<8><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
-    default: skinny_kernel<16><<<grid, kThreads, sp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, sp.m_per_split, partial); break;
-  }
+  skinny_tc_kernel<<<dim3(static_cast<unsigned>(tp.ptiles), static_cast<unsigned>(tp.splits)), kTcThreads, tp.smem,
+                     s>>>(static_cast<const __nv_bfloat16*>(X), ldx, static_cast<int>(M), static_cast<int>(P), T.t,
+                          T.parts, T.part_stride, r, tp.m_per_split, partial, status);
   if (cudaGetLastError() != cudaSuccess) return QERL_ERR_CUDA;
   const int64_t total = P * r;
   const int blocks = static_cast<int>(std::min<int64_t>((total + kThreads - 1) / kThreads, 4 * sms()));
-  skinny_reduce_kernel<<<std::max(blocks, 1), kThreads, 0, s>>>(partial, sp.splits, static_cast<int>(P), r, scale,
+  skinny_reduce_kernel<<<std::max(blocks, 1), kThreads, 0, s>>>(partial, tp.splits, static_cast<int>(P), r, scale,
                                                                 transposed ? 1 : 0, out);
   return cuda_status(cudaGetLastError());
 }
@@ -315,12 +371,16 @@ qerl_status launch_lora_linear_backward(const BackwardArgs& b, cudaStream_t s) {
     if ((st = launch_lora_down(b.xt, m, k, b.ldxt, b.A, r, ws + L.down, &t, reinterpret_cast<int*>(ws), s)) !=
         QERL_OK)
       return st;
-    if ((st = launch_skinny(b.dy, b.lddy, m, n, t, r, scale, false, partial, b.dB, s)) != QERL_OK) return st;
+    if ((st = launch_skinny(b.dy, b.lddy, m, n, t, r, scale, false, partial, b.dB, reinterpret_cast<int*>(ws), s)) !=
+        QERL_OK)
+      return st;
   }
   if (b.dA != nullptr) {
     // dA = s u^T x~ with u = dy B, the down-projection of the dx~ launch.
     const LoraDown u = linear_lora_down(a, 0);
-    if ((st = launch_skinny(b.xt, b.ldxt, m, k, u, r, scale, true, partial, b.dA, s)) != QERL_OK) return st;
+    if ((st = launch_skinny(b.xt, b.ldxt, m, k, u, r, scale, true, partial, b.dA, reinterpret_cast<int*>(ws), s)) !=
+        QERL_OK)
+      return st;
   }
   return QERL_OK;
 }
