@@ -59,20 +59,30 @@ __global__ void __launch_bounds__(kThreads) transpose_bf16_kernel(const __nv_bfl
 // K-major 128-byte-swizzled layout of A (128 rows x 64 tokens), and T (fp32)
 // into three bf16 terms t1 = bf16(T), t2 = bf16(T - t1), t3 = bf16(T - t1 -
 // t2) (together T to ~24 significant bits), each laid out likewise as a B
-// tile (rn = round16(r) rows x 64 tokens).  Per chunk 4 K-steps x 3 MMAs
-// (M = 128, N = rn, K = 16, bf16 products exact, fp32 accumulation in tensor
-// memory); two chunk buffers, each released by the MMAs' commit.
+// tile (rn = round16(r) rows x 64 tokens).  Per chunk 4 K-steps of MMAs
+// (M = 128, K = 16, bf16 products exact, fp32 accumulation in tensor
+// memory); two A/B buffers, each released by the MMAs' commit.
 constexpr int kTcThreads = 256;
 constexpr int kTcM = 64;   // tokens per chunk (the MMAs' K)
 constexpr int kTcP = 128;  // p rows per CTA (the MMAs' M)
 __host__ __device__ inline int tc_rn(int r) { return (r + 15) / 16 * 16; }
+// Up to r = 64 the three terms' B tiles form one B operand of 3 rn rows (one
+// MMA per K-step; the accumulator's three column blocks are added at the
+// end); above, one MMA per term into the same accumulator.
+__host__ __device__ inline bool tc_fused(int r) { return 3 * tc_rn(r) <= 256; }
 __host__ __device__ inline int tc_tmem_cols(int r) {
+  const int need = tc_fused(r) ? 3 * tc_rn(r) : tc_rn(r);
   int c = 32;
-  while (c < tc_rn(r)) c *= 2;
+  while (c < need) c *= 2;
   return c;
 }
 __host__ __device__ inline uint32_t tc_buf_bytes(int r) { return 16384u + 3u * static_cast<uint32_t>(tc_rn(r)) * 128u; }
-__host__ __device__ inline size_t tc_smem_bytes(int r) { return 1024 + 2 * static_cast<size_t>(tc_buf_bytes(r)) + 64; }
+// Staging of one chunk as it arrives (cp.async): X [64][128] bf16, T [64][rn] fp32.
+constexpr int kTcStages = 2;
+__host__ __device__ inline uint32_t tc_stage_bytes(int r) { return 16384u + 64u * static_cast<uint32_t>(tc_rn(r)) * 4u; }
+__host__ __device__ inline size_t tc_smem_bytes(int r) {
+  return 1024 + 2 * static_cast<size_t>(tc_buf_bytes(r)) + kTcStages * static_cast<size_t>(tc_stage_bytes(r)) + 64;
+}
 
 // Byte offset of the 32-bit word holding elements (kl, kl + 1) of row R in a
 // K-major 128-byte-swizzled tile (64 elements per 128-byte row, kl even).
@@ -83,6 +93,8 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
 }
 
+// RMAX: the rank class (32, 64 or 128).
+template <int RMAX>
 __global__ void __launch_bounds__(kTcThreads, 1) skinny_tc_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx,
                                                                  int M, int P, const float* __restrict__ T,
                                                                  int parts, int64_t part_stride, int r,
@@ -94,11 +106,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) skinny_tc_kernel(const __nv_bfl
   uint8_t* sgen = tc_smem_raw + (sbase - raw);
   const int rn = tc_rn(r);
   const uint32_t bufb = tc_buf_bytes(r);
-  const uint32_t bars = sbase + 2 * bufb;
+  const uint32_t bars = sbase + 2 * bufb + kTcStages * tc_stage_bytes(r);
   auto mma_done = [&](int b) { return bars + 8u * b; };
   const uint32_t acc_done = bars + 16u;
   const uint32_t holder = bars + 24u;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + 2 * bufb + 28);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + (bars - sbase) + 28);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int p0 = blockIdx.x * kTcP;
   const int m_begin = blockIdx.y * m_per_split, m_end = min(M, m_begin + m_per_split);
@@ -117,80 +129,109 @@ __global__ void __launch_bounds__(kTcThreads, 1) skinny_tc_kernel(const __nv_bfl
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + 2 * bufb + 24);
-  const uint32_t idesc = idesc_bf16_f32(kTcP, static_cast<uint32_t>(rn));
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + (bars - sbase) + 24);
+  const bool fused = tc_fused(r);
+  const uint32_t idesc = idesc_bf16_f32(kTcP, static_cast<uint32_t>(fused ? 3 * rn : rn));
   const int nchunks = m_end > m_begin ? (m_end - m_begin + kTcM - 1) / kTcM : 0;
+  // Chunks arrive by cp.async into a kTcStages-deep staging ring (X rows as
+  // they are, T part 0; rows past the split and p past P zero-filled), so
+  // that the loads of the next chunks are in flight while the current one
+  // is transposed into its A/B buffer and multiplied.  Other T parts (small
+  // token counts) are added from global memory during the transpose.
+  const uint32_t stage0 = sbase + 2 * bufb;
+  const uint32_t sstride = tc_stage_bytes(r);
+  auto issue_chunk = [&](int c) {
+    if (c < nchunks) {
+      const uint32_t st = stage0 + static_cast<uint32_t>(c % kTcStages) * sstride;
+      const int m0 = m_begin + c * kTcM;
+      for (int v = tid; v < kTcM * (kTcP / 8); v += kTcThreads) {  // X: 64 rows x 16 pieces of 16 B
+        const int ml = v >> 4, pc = (v & 15) * 8;
+        const bool in = m0 + ml < m_end && p0 + pc < P;
+        cp_async_16(st + static_cast<uint32_t>(v) * 16u,
+                    in ? static_cast<const void*>(X + static_cast<int64_t>(m0 + ml) * ldx + p0 + pc) : X, in ? 16u : 0u);
+      }
+      const int tq = rn / 4;  // T: 64 rows x rn / 4 pieces of 16 B (r % 8 == 0: a piece is all in or all out)
+      for (int v = tid; v < kTcM * tq; v += kTcThreads) {
+        const int ml = v / tq, jc = (v % tq) * 4;
+        const bool in = m0 + ml < m_end && jc < r;
+        cp_async_16(st + 16384u + static_cast<uint32_t>(v) * 16u,
+                    in ? static_cast<const void*>(T + static_cast<int64_t>(m0 + ml) * r + jc) : T, in ? 16u : 0u);
+      }
+    }
+    cp_async_commit();  // one group per chunk slot (empty past the end)
+  };
+  const int ml_x = 2 * (tid >> 3), pl = (tid & 7) * 16;
+  const int titems = (kTcM / 2) * rn;
   bool ok = true;
+  for (int c = 0; c < kTcStages; ++c) issue_chunk(c);
   for (int c = 0; c < nchunks; ++c) {
     const int b = c & 1;
     const uint32_t abuf = sbase + static_cast<uint32_t>(b) * bufb, bbuf = abuf + 16384u;
+    const uint32_t st = stage0 + static_cast<uint32_t>(c % kTcStages) * sstride;
+    cp_async_wait_group<kTcStages - 1>();  // this thread's copies of chunk c have landed
     // The buffer's previous MMAs (chunk c - 2) are done reading it.
     if (c >= 2 && !mbar_wait_a(mma_done(b), static_cast<uint32_t>(((c - 2) >> 1) & 1), abort_flag, status)) {
       ok = false;
       break;
     }
-    const int m0 = m_begin + c * kTcM;
+    __syncthreads();  // every thread's copies of chunk c are visible
     {
-      // X: a thread takes token rows (ml, ml + 1) and 16 consecutive p.
-      const int ml = 2 * (tid >> 3), pl = (tid & 7) * 16;
-      const int m = m0 + ml, p = p0 + pl;
-      uint4 x0[2], x1[2];
+      // X: token rows (ml_x, ml_x + 1) x 16 consecutive p -> 16 words of A.
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        x0[h] = (m < m_end && p < P) ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m) * ldx + p + 8 * h))
-                                     : make_uint4(0u, 0u, 0u, 0u);
-        x1[h] = (m + 1 < m_end && p < P)
-                    ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m + 1) * ldx + p + 8 * h))
-                    : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t a[4] = {x0[h].x, x0[h].y, x0[h].z, x0[h].w};
-        const uint32_t c4[4] = {x1[h].x, x1[h].y, x1[h].z, x1[h].w};
+        const uint4 a4 = lds128(st + static_cast<uint32_t>(ml_x * 256 + (pl + 8 * h) * 2));
+        const uint4 c4v = lds128(st + static_cast<uint32_t>((ml_x + 1) * 256 + (pl + 8 * h) * 2));
+        const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
+        const uint32_t c4[4] = {c4v.x, c4v.y, c4v.z, c4v.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int R = pl + 8 * h + 2 * k;  // rows R (low halves) and R + 1 (high halves)
-          sts32(abuf + sw128_word(R, ml), __byte_perm(a[k], c4[k], 0x5410));
-          sts32(abuf + sw128_word(R + 1, ml), __byte_perm(a[k], c4[k], 0x7632));
+          sts32(abuf + sw128_word(R, ml_x), __byte_perm(a[k], c4[k], 0x5410));
+          sts32(abuf + sw128_word(R + 1, ml_x), __byte_perm(a[k], c4[k], 0x7632));
         }
       }
-    }
-    // T: items (token pair, j), j fastest (coalesced loads); rows j >= r are zero.
-    for (int it = tid; it < (kTcM / 2) * rn; it += kTcThreads) {
-      const int ml = 2 * (it / rn), j = it % rn;
-      const int m = m0 + ml;
-      float t0 = 0.0f, t1 = 0.0f;
-      if (j < r) {
-        for (int g = 0; g < parts; ++g) {
-          if (m < m_end) t0 += __ldg(T + g * part_stride + static_cast<int64_t>(m) * r + j);
-          if (m + 1 < m_end) t1 += __ldg(T + g * part_stride + static_cast<int64_t>(m + 1) * r + j);
-        }
-      }
-      const uint32_t off = sw128_word(j, ml);
-      float u0 = t0, u1 = t1;
+      // T: items (token pair, j) -> three bf16 terms, B tiles 1..3.
+      const int m0 = m_begin + c * kTcM;
+      for (int it = tid; it < titems; it += kTcThreads) {
+        const int ml = 2 * (it / rn), j = it % rn;
+        float u0 = ldsf(st + 16384u + static_cast<uint32_t>((ml * rn + j) * 4));
+        float u1 = ldsf(st + 16384u + static_cast<uint32_t>(((ml + 1) * rn + j) * 4));
+        if (parts > 1 && j < r)
+          for (int g = 1; g < parts; ++g) {
+            if (m0 + ml < m_end) u0 += __ldg(T + g * part_stride + static_cast<int64_t>(m0 + ml) * r + j);
+            if (m0 + ml + 1 < m_end) u1 += __ldg(T + g * part_stride + static_cast<int64_t>(m0 + ml + 1) * r + j);
+          }
+        const uint32_t off = sw128_word(j, ml);
 #pragma unroll
-      for (int k3 = 0; k3 < 3; ++k3) {
-        const uint32_t h0 = bf16_bits(u0), h1 = bf16_bits(u1);
-        sts32(bbuf + static_cast<uint32_t>(k3 * rn * 128) + off, h0 | (h1 << 16));
-        u0 -= __uint_as_float(h0 << 16);  // exact: the remainder of a rounding
-        u1 -= __uint_as_float(h1 << 16);
+        for (int k3 = 0; k3 < 3; ++k3) {
+          const uint32_t h0 = bf16_bits(u0), h1 = bf16_bits(u1);
+          sts32(bbuf + static_cast<uint32_t>(k3 * rn * 128) + off, h0 | (h1 << 16));
+          u0 -= __uint_as_float(h0 << 16);  // exact: the remainder of a rounding
+          u1 -= __uint_as_float(h1 << 16);
+        }
       }
     }
     fence_proxy_async_smem();  // the tiles are read by the MMAs (async proxy)
-    __syncthreads();
+    __syncthreads();           // A/B ready; the staging slot of chunk c is free
+    issue_chunk(c + kTcStages);
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < kTcM / 16; ++ks) {
         const uint64_t ad = sw128_kmajor_desc(abuf + 32u * ks);
+        if (fused) {
+          tc_mma_f16(tmem, ad, sw128_kmajor_desc(bbuf + 32u * ks), idesc, (c > 0 || ks > 0) ? 1u : 0u);
+        } else {
 #pragma unroll
-        for (int k3 = 0; k3 < 3; ++k3)
-          tc_mma_f16(tmem, ad, sw128_kmajor_desc(bbuf + static_cast<uint32_t>(k3 * rn * 128) + 32u * ks), idesc,
-                     (c > 0 || ks > 0 || k3 > 0) ? 1u : 0u);
+          for (int k3 = 0; k3 < 3; ++k3)
+            tc_mma_f16(tmem, ad, sw128_kmajor_desc(bbuf + static_cast<uint32_t>(k3 * rn * 128) + 32u * ks), idesc,
+                       (c > 0 || ks > 0 || k3 > 0) ? 1u : 0u);
+        }
       }
       tc_commit(mma_done(b));
     }
   }
+  cp_async_wait_group<0>();  // no copy outlives the block
   if (tid == 0) tc_commit(acc_done);  // once every MMA issued above is done (at once without any)
   ok = mbar_wait_a(acc_done, 0, abort_flag, status) && ok;
   tc_fence_after();
@@ -200,9 +241,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) skinny_tc_kernel(const __nv_bfl
     const int p = p0 + 32 * q + lane;
     float* out = partial + static_cast<int64_t>(blockIdx.y) * P * r + static_cast<int64_t>(p) * r;
     const int cb = half * (rn / 2), ce = cb + rn / 2;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
     for (int c8 = cb; c8 < ce; c8 += 8) {
       float v[8];
-      tmem_ld_x8(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c8), v);
+      tmem_ld_x8(lane_addr + static_cast<uint32_t>(c8), v);
+      if (fused) {  // the three terms' column blocks, added in term order
+        float v2[8], v3[8];
+        tmem_ld_x8(lane_addr + static_cast<uint32_t>(rn + c8), v2);
+        tmem_ld_x8(lane_addr + static_cast<uint32_t>(2 * rn + c8), v3);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = (v[e] + v2[e]) + v3[e];
+      }
       tmem_ld_wait();
       if (p < P) {
 #pragma unroll
@@ -307,13 +357,21 @@ qerl_status launch_skinny(const void* X, int64_t ldx, int64_t M, int64_t P, cons
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(skinny_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tc_smem_bytes(128)));
+    const int lim = static_cast<int>(tc_smem_bytes(128));
+    err = cudaFuncSetAttribute(skinny_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(skinny_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   });
   if (err != cudaSuccess) return QERL_ERR_CUDA;
-  skinny_tc_kernel<<<dim3(static_cast<unsigned>(tp.ptiles), static_cast<unsigned>(tp.splits)), kTcThreads, tp.smem,
-                     s>>>(static_cast<const __nv_bfloat16*>(X), ldx, static_cast<int>(M), static_cast<int>(P), T.t,
-                          T.parts, T.part_stride, r, tp.m_per_split, partial, status);
+  const dim3 grid(static_cast<unsigned>(tp.ptiles), static_cast<unsigned>(tp.splits));
+  const auto* xb = static_cast<const __nv_bfloat16*>(X);
+  const int Mi = static_cast<int>(M), Pi = static_cast<int>(P);
+  if (r <= 32)
+    skinny_tc_kernel<32><<<grid, kTcThreads, tp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, tp.m_per_split, partial, status);
+  else if (r <= 64)
+    skinny_tc_kernel<64><<<grid, kTcThreads, tp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, tp.m_per_split, partial, status);
+  else
+    skinny_tc_kernel<128><<<grid, kTcThreads, tp.smem, s>>>(xb, ldx, Mi, Pi, T.t, T.parts, T.part_stride, r, tp.m_per_split, partial, status);
   if (cudaGetLastError() != cudaSuccess) return QERL_ERR_CUDA;
   const int64_t total = P * r;
   const int blocks = static_cast<int>(std::min<int64_t>((total + kThreads - 1) / kThreads, 4 * sms()));
