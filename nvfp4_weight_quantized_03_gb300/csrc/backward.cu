@@ -84,11 +84,6 @@ __host__ __device__ inline size_t tc_smem_bytes(int r) {
   return 1024 + 2 * static_cast<size_t>(tc_buf_bytes(r)) + kTcStages * static_cast<size_t>(tc_stage_bytes(r)) + 64;
 }
 
-// Byte offset of the 32-bit word holding elements (kl, kl + 1) of row R in a
-// K-major 128-byte-swizzled tile (64 elements per 128-byte row, kl even).
-__device__ __forceinline__ uint32_t sw128_word(int R, int kl) {
-  return static_cast<uint32_t>((R >> 3) * 1024 + (R & 7) * 128 + ((((kl >> 3) ^ (R & 7)) << 4)) + (kl & 7) * 2);
-}
 __device__ __forceinline__ uint32_t bf16_bits(float v) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
 }
@@ -160,8 +155,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) skinny_tc_kernel(const __nv_bfl
     }
     cp_async_commit();  // one group per chunk slot (empty past the end)
   };
-  const int ml_x = 2 * (tid >> 3), pl = (tid & 7) * 16;
-  const int titems = (kTcM / 2) * rn;
   bool ok = true;
   for (int c = 0; c < kTcStages; ++c) issue_chunk(c);
   for (int c = 0; c < nchunks; ++c) {
@@ -176,38 +169,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) skinny_tc_kernel(const __nv_bfl
     }
     __syncthreads();  // every thread's copies of chunk c are visible
     {
-      // X: token rows (ml_x, ml_x + 1) x 16 consecutive p -> 16 words of A.
+      // X: work item (token octet mo, p pair pp): eight 32-bit words (tokens
+      // 8 mo .. 8 mo + 7, p pair) give A rows 2 pp and 2 pp + 1 one 16-byte
+      // piece each (tokens of a row are contiguous in the K-major layout).
+      // Lanes take consecutive p pairs: conflict-free reads, and the
+      // swizzle spreads the 16-byte stores.
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 a4 = lds128(st + static_cast<uint32_t>(ml_x * 256 + (pl + 8 * h) * 2));
-        const uint4 c4v = lds128(st + static_cast<uint32_t>((ml_x + 1) * 256 + (pl + 8 * h) * 2));
-        const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
-        const uint32_t c4[4] = {c4v.x, c4v.y, c4v.z, c4v.w};
+      for (int u = 0; u < (kTcM / 8) * (kTcP / 2) / kTcThreads; ++u) {
+        const int item = tid + u * kTcThreads;
+        const int pp = item & (kTcP / 2 - 1), mo = item / (kTcP / 2);
+        uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int R = pl + 8 * h + 2 * k;  // rows R (low halves) and R + 1 (high halves)
-          sts32(abuf + sw128_word(R, ml_x), __byte_perm(a[k], c4[k], 0x5410));
-          sts32(abuf + sw128_word(R + 1, ml_x), __byte_perm(a[k], c4[k], 0x7632));
-        }
+        for (int e = 0; e < 8; ++e) w[e] = lds32(st + static_cast<uint32_t>((8 * mo + e) * (kTcP * 2) + 4 * pp));
+        uint4 lo, hi;
+        lo.x = __byte_perm(w[0], w[1], 0x5410);
+        lo.y = __byte_perm(w[2], w[3], 0x5410);
+        lo.z = __byte_perm(w[4], w[5], 0x5410);
+        lo.w = __byte_perm(w[6], w[7], 0x5410);
+        hi.x = __byte_perm(w[0], w[1], 0x7632);
+        hi.y = __byte_perm(w[2], w[3], 0x7632);
+        hi.z = __byte_perm(w[4], w[5], 0x7632);
+        hi.w = __byte_perm(w[6], w[7], 0x7632);
+        const int R = 2 * pp;
+        sts128(abuf + static_cast<uint32_t>((R >> 3) * 1024 + (R & 7) * 128 + ((mo ^ (R & 7)) << 4)), lo);
+        sts128(abuf + static_cast<uint32_t>(((R + 1) >> 3) * 1024 + ((R + 1) & 7) * 128 + ((mo ^ ((R + 1) & 7)) << 4)),
+               hi);
       }
-      // T: items (token pair, j) -> three bf16 terms, B tiles 1..3.
+      // T: work item (token octet mo, j): eight values -> three bf16 terms,
+      // one 16-byte piece of row j in each of the B tiles.
       const int m0 = m_begin + c * kTcM;
-      for (int it = tid; it < titems; it += kTcThreads) {
-        const int ml = 2 * (it / rn), j = it % rn;
-        float u0 = ldsf(st + 16384u + static_cast<uint32_t>((ml * rn + j) * 4));
-        float u1 = ldsf(st + 16384u + static_cast<uint32_t>(((ml + 1) * rn + j) * 4));
+      for (int item = tid; item < (kTcM / 8) * rn; item += kTcThreads) {
+        const int j = item % rn, mo = item / rn;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = ldsf(st + 16384u + static_cast<uint32_t>(((8 * mo + e) * rn + j) * 4));
         if (parts > 1 && j < r)
-          for (int g = 1; g < parts; ++g) {
-            if (m0 + ml < m_end) u0 += __ldg(T + g * part_stride + static_cast<int64_t>(m0 + ml) * r + j);
-            if (m0 + ml + 1 < m_end) u1 += __ldg(T + g * part_stride + static_cast<int64_t>(m0 + ml + 1) * r + j);
-          }
-        const uint32_t off = sw128_word(j, ml);
+          for (int g = 1; g < parts; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (m0 + 8 * mo + e < m_end) v[e] += __ldg(T + g * part_stride + static_cast<int64_t>(m0 + 8 * mo + e) * r + j);
+        const uint32_t off = static_cast<uint32_t>((j >> 3) * 1024 + (j & 7) * 128 + ((mo ^ (j & 7)) << 4));
 #pragma unroll
         for (int k3 = 0; k3 < 3; ++k3) {
-          const uint32_t h0 = bf16_bits(u0), h1 = bf16_bits(u1);
-          sts32(bbuf + static_cast<uint32_t>(k3 * rn * 128) + off, h0 | (h1 << 16));
-          u0 -= __uint_as_float(h0 << 16);  // exact: the remainder of a rounding
-          u1 -= __uint_as_float(h1 << 16);
+          uint32_t hb[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            hb[e] = bf16_bits(v[e]);
+            v[e] -= __uint_as_float(hb[e] << 16);  // exact: the remainder of a rounding
+          }
+          sts128(bbuf + static_cast<uint32_t>(k3 * rn * 128) + off,
+                 make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16), hb[6] | (hb[7] << 16)));
         }
       }
     }

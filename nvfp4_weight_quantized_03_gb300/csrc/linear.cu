@@ -776,12 +776,6 @@ __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, const Linear
 // weight's transpose for the input gradient, K being the original output
 // dimension): a scale per element along K, shared by the 16 rows of a row
 // group, at kCodesRawBytes + (row / 16) * 256 + k.
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
-
 // Element pairs of 8 codes (a 32-bit word): E2M1 by conversion, or (kLut)
 // NF4 by the byte-indexed table of fp16 pairs at `lut`.
 template <bool kLut>
