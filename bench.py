@@ -301,10 +301,11 @@ def group_algorithmic_bytes(lins, m, r=RANK_R):
 # 18944 x 3584 linears sharing x; the largest of the step's four launches) at
 # M = 8.  DRAM traffic of one such launch (prep_kernel + mma_kernel):
 # dram__bytes_read.sum + dram__bytes_write.sum from a 1-pass ncu capture of
-# `bench.py --case 8,18944+18944,3584,32` (taken on the build with the compact
-# epilogue and the early weight stages that complete without the activations).
+# `bench.py --case 8,18944+18944,3584,32` (taken on the build with four MMA
+# issuers up to 64 tokens, the compact epilogue and the early weight stages
+# that complete without the activations).
 DOMINANT = ("gate_up", 8)
-DOMINANT_TRAFFIC_BYTES = 79666944  # prep 599,552 + mma 79,044,608 read + 22,784 written (ncu, 1 pass)
+DOMINANT_TRAFFIC_BYTES = 79692288  # prep 616,448 + mma 79,044,608 read + 31,232 written (ncu, 1 pass)
 
 
 def dominant_call(q, layers, acts, hbm_peak, reps=64):
