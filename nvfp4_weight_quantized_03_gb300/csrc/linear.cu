@@ -149,7 +149,9 @@ __host__ inline int lora_tile_count(int64_t m, const int* ranks, int nlin) {
 // groups; smaller tiles stage every group's partial sums and add them, so
 // their group count is bounded by that staging buffer (256 / n_tok groups).
 __host__ inline bool lora_sum_in_prep(int64_t m) { return m > 64; }
-__host__ inline LoraSplit lora_split(int64_t m, int64_t k, const int* ranks, int nlin) {
+// `chunks`: the 64-wide chunks a prep CTA takes up to 64 tokens (2 by
+// default; the workspace is sized for that, the largest group count).
+__host__ inline LoraSplit lora_split(int64_t m, int64_t k, const int* ranks, int nlin, int chunks = 2) {
   const int kc_total = static_cast<int>(k / kLoraKc);
   LoraSplit L;
   L.cluster = std::max(1, std::min(kPrepMaxCluster, kc_total));
@@ -157,6 +159,7 @@ __host__ inline LoraSplit lora_split(int64_t m, int64_t k, const int* ranks, int
   if (lora_sum_in_prep(m)) {
     if (lora_tile_count(m, ranks, nlin) > kMaxLoraCounters) g = 1;
   } else {
+    g = (kc_total + chunks * L.cluster - 1) / (chunks * L.cluster);
     const int64_t n_tok = std::min<int64_t>(256, (m + 15) / 16 * 16);
     g = std::min<int>(g, static_cast<int>(std::max<int64_t>(1, 256 / std::max<int64_t>(n_tok, 1))));
   }
@@ -2150,6 +2153,21 @@ void lora_prep_params(PrepParams& pp, int64_t m, int64_t k, int r, const void* A
 
 }  // namespace
 
+// The LoRA split of a launch.  Up to 64 tokens the prep grid's LoRA tiles
+// hold SMs the MMA kernel needs until they finish: when the launch streams
+// many weight stages per SM (a long mainloop, e.g. gate + up or down), a prep
+// CTA takes three chunks (four from 32 tokens) instead of two -- fewer CTAs,
+// later t, which the long mainloop hides.  (Measured on the 7B launches: gate
+// + up at 64 tokens 50.9 -> 44.9 us, at 32 tokens 42.0 -> 40.7 us; q, k, v
+// and o keep two.)
+LoraSplit launch_lora_split(const LinearArgs& a, const int* ranks) {
+  int64_t stage_tiles = 0;
+  for (int i = 0; i < a.nlin; ++i)
+    stage_tiles += ((a.lin[i].n + kTileN - 1) / kTileN) * ((a.k + kRawK - 1) / kRawK);
+  const int chunks = stage_tiles < 8 * static_cast<int64_t>(sm_count()) ? 2 : (a.m >= 32 ? 4 : 3);
+  return lora_split(a.m, a.k, ranks, a.nlin, chunks);
+}
+
 LoraDown linear_lora_down(const LinearArgs& a, int i) {
   int ranks[kMaxLinears] = {0, 0, 0, 0};
   for (int j = 0; j < a.nlin; ++j)
@@ -2162,7 +2180,7 @@ LoraDown linear_lora_down(const LinearArgs& a, int i) {
     d.parts = 1;
   } else {
     d.t = reinterpret_cast<const float*>(ws + WL.t[i]);
-    d.parts = lora_split(a.m, a.k, ranks, a.nlin).groups;
+    d.parts = launch_lora_split(a, ranks).groups;
   }
   d.part_stride = a.m * ranks[i];
   return d;
@@ -2289,7 +2307,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // splits).
   int prep_busy = 0;
   if (M <= 64 && r > 0) {
-    const LoraSplit ls0 = lora_split(M, K, ranks, nlin);
+    const LoraSplit ls0 = launch_lora_split(a, ranks);
     int ltiles = 0;
     for (int i = 0; i < nlin; ++i)
       if (ranks[i] > 0) ltiles += ((M + kLoraTileM - 1) / kLoraTileM) * ((ranks[i] + kLoraTileR - 1) / kLoraTileR);
@@ -2355,7 +2373,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // The LoRA operand is built early (its own region) up to 128 tokens: from
   // partial sums staged in shared memory, or in pair mode straight from
   // global memory by the idle issuer warps.
-  const int t_groups = lora_sum_in_prep(M) ? 1 : lora_split(M, K, ranks, nlin).groups;  // partial sums the MMA kernel adds
+  const int t_groups = lora_sum_in_prep(M) ? 1 : launch_lora_split(a, ranks).groups;  // partial sums the MMA kernel adds
   const uint32_t tstage_bytes = (r > 0 && !pair) ? static_cast<uint32_t>(t_groups * n_tok * r * 4) : 0u;
   int lora_early = (r > 0 && n_tok <= 128) ? 1 : 0;
   const uint32_t part_bytes = split > 1 ? static_cast<uint32_t>(tpc * n_tok) * kTileN * 4u : 0u;
@@ -2501,7 +2519,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   pp.ldx = a.ldx;
   pp.M = M;
   pp.K = K;
-  const LoraSplit ls = lora_split(M, K, ranks, nlin);
+  const LoraSplit ls = launch_lora_split(a, ranks);
   pp.cluster = lora ? ls.cluster : 1;
   pp.groups = lora ? ls.groups : 0;
   pp.tiled_rows = xs_rowmajor ? 0 : n_tok;
