@@ -1477,43 +1477,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
       }
     }
-    // One accumulator (one issuer, e.g. 256-token tiles): 32 token columns
-    // per TMEM load and wait.  Several: 8 columns of up to four of them per
+    // Up to two accumulators (65-128 tokens): 32 token columns of each per
+    // TMEM wait.  More (up to 64 tokens): 8 columns of up to four of them per
     // wait.  The row scales arrive as vectors (one shared-memory load per
-    // four values, not one per value).
-    auto emit = [&](int c, int e, float val) {
-      const uint32_t el = tile_out + static_cast<uint32_t>((c + e) * kTileN + nl);
-      if (p.split > 1)
-        stsf(part + 4u * el, val);
-      else if (!p.stage_out) {
-        if (m0 + c + e < p.M && n < L.N) store_out(L, m0 + c + e, n, val);
-      } else if (L.y_f32) {
-        stsf(sbase + 4u * el, val);  // staged: [tile][token][128 rows]
-      } else {
-        sts16(sbase + 2u * el, __bfloat16_as_ushort(__float2bfloat16_rn(val)));
-      }
-    };
-    if (!p.pair && nacc == 1 && cols % 32 == 0) {
-      for (int c = c0; c < c0 + cols; c += 32) {
-        float w[32];
-        tmem_ld_x32(tmem_base + acc0 + lane_off + c, w);
-        float sc[32];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 s4 = lds128f(smv + 4u * (c + e));
-          sc[e] = s4.x;
-          sc[e + 1] = s4.y;
-          sc[e + 2] = s4.z;
-          sc[e + 3] = s4.w;
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) emit(c, e, ok ? w[e] * sc[e] : 0.0f);
-      }
-    } else {
-    // (This runs once per CTA, its instructions fetched cold: kept compact --
-    // a rolled loop over groups of four accumulators, one store loop per
-    // output kind.)
+    // four values, not one per value).  (This runs once per CTA, its
+    // instructions fetched cold: kept compact -- rolled loops, one store loop
+    // per output kind.)
     auto emit8 = [&](int c, const float (&val)[8]) {
       const uint32_t el0 = tile_out + static_cast<uint32_t>(c * kTileN + nl);
       if (p.split > 1) {
@@ -1531,6 +1500,26 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           sts16(sbase + 2u * (el0 + e * kTileN), __bfloat16_as_ushort(__float2bfloat16_rn(val[e])));
       }
     };
+    if (!p.pair && nacc <= 2 && cols % 32 == 0) {
+      for (int c = c0; c < c0 + cols; c += 32) {
+        float w[32], w2[32];
+        tmem_ld_x32(tmem_base + acc0 + lane_off + c, w);
+        if (nacc == 2) tmem_ld_x32(tmem_base + acc0 + static_cast<uint32_t>(p.n_tok) + lane_off + c, w2);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e8 = 0; e8 < 32; e8 += 8) {
+          const float4 s0 = lds128f(smv + 4u * (c + e8)), s1 = lds128f(smv + 4u * (c + e8 + 4));
+          const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+          float o8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float a = nacc == 2 ? w[e8 + e] + w2[e8 + e] : w[e8 + e];
+            o8[e] = ok ? a * sc[e] : 0.0f;
+          }
+          emit8(c + e8, o8);
+        }
+      }
+    } else {
     for (int c = c0; !p.pair && c < c0 + cols; c += 8) {
       float v[8];
       // Four accumulators' columns per wait (issuer 0's holds the LoRA term).
