@@ -30,19 +30,21 @@
 //   Nineteen warps; the light roles take the low (older) warp numbers so the
 //   scheduler does not starve them behind the ALU-bound dequant warps:
 //     warp 0       weight producer: L2 prefetch a few stages ahead, bulk copy
-//                  of each block (and, for <= 64 tokens, the x~ slabs of the
-//                  same K range on the same barrier; the first ring of blocks
-//                  is requested before waiting for the preceding kernel).
-//     warp 1       activation producer (more than 64 tokens): x~ per stage,
-//                  bulk-copied slabs up to 128 tokens, 2-D TMA tiles beyond.
+//                  of each block (the first ring of blocks is requested
+//                  before waiting for the preceding kernel).
+//     warp 1       activation producer: x~ per stage, bulk-copied slabs up to
+//                  128 tokens, 2-D TMA tiles beyond.  Up to 64 tokens a weight
+//                  stage's slabs share its tensor-memory A slot's index and
+//                  empty barrier (one commit per issuer frees both).
 //     warp 2       LoRA operands: sums the down-projection groups, scales each
 //                  token row and splits t into bf16 hi + lo.
-//     warps 3..10  MMA issuers (1, 2, 4 or 8 of them; lane 0 issues):
+//     warps 3..10  MMA issuers (2, 4 or 8 of them; lane 0 issues):
 //                  tcgen05.mma kind::f16, K=16, each into its own fp32 TMEM
 //                  accumulator, so that the ~150-cycle issue cost of an MMA
-//                  overlaps across threads; the epilogue adds them.  Issuer 0
-//                  also adds the LoRA up-projection B . (t_hi + t_lo)^T into
-//                  its accumulator.
+//                  overlaps across threads; the epilogue adds them.  Up to 64
+//                  tokens they form two groups on alternate weight stages.
+//                  Issuer 0 also adds the LoRA up-projection
+//                  B . (t_hi + t_lo)^T into its accumulator.
 //     warps 11..18 dequant: E2M1 pairs -> fp16 pairs, times the block scale
 //                  (exact products).  Decode writes them to tensor memory as
 //                  the MMA's A operand (tcgen05.st), a weight stage per
@@ -72,6 +74,7 @@ namespace {
 
 constexpr int kMaxLinears = 4;  // linears sharing one launch (x, z and K)
 constexpr int kPrepThreads = 256;
+constexpr uint32_t kSmemPerSm = 233472;  // 228 KB per SM, 1 KB of it reserved per resident CTA
 constexpr int kLoraTileM = 16;   // token rows per LoRA tile
 constexpr int kLoraTileR = 32;   // ranks per LoRA tile
 constexpr int kLoraKc = 64;      // K per shared-memory chunk
@@ -256,15 +259,16 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
       }
       if (p.xs == nullptr) return;  // the normalisation step alone
     } else {
-    // Four vectors per thread per round: their loads are all in flight
+    // kRowVec vectors per thread per round: their loads are all in flight
     // before the first is used.
     const float4* z4 = reinterpret_cast<const float4*>(p.z != nullptr ? p.z + m * p.ldz : nullptr);
     uint4* xo = p.xt_out != nullptr ? reinterpret_cast<uint4*>(p.xt_out + static_cast<int64_t>(m) * p.ldo) : nullptr;
-    for (int v0 = tid; v0 < nv; v0 += 4 * kPrepThreads) {
-      uint4 raw[4];
-      float4 za[4], zb[4];
+    constexpr int kRowVec = 4;
+    for (int v0 = tid; v0 < nv; v0 += kRowVec * kPrepThreads) {
+      uint4 raw[kRowVec];
+      float4 za[kRowVec], zb[kRowVec];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kRowVec; ++u) {
         const int v = v0 + u * kPrepThreads;
         if (v < nv) {
           raw[u] = __ldg(xrow + v);
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kRowVec; ++u) {
         const int v = v0 + u * kPrepThreads;
         if (v >= nv) break;
         __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&raw[u]);
@@ -442,23 +446,26 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   const uint32_t part_s = smem_u32(part);
   // Every partner's value is loaded before the first add (the remote-load
   // latency is paid once, not once per partner), then added in rank order.
-  // A thread sums at most two entries (512 per tile, >= 256 threads).
+  // A thread sums at most two entries (512 per tile, 256 threads).
   constexpr int kPerThread = (kLoraTileM * kLoraTileR + kPrepThreads - 1) / kPrepThreads;
+  // Entry u of this thread: idx0 + u * stride (fixed trip count, so the
+  // sums stay in registers).
+  const int idx0 = ks * kPrepThreads + tid, stride = p.cluster * kPrepThreads;
   float vsum[kPerThread];
-  int vidx[kPerThread];
-  int nsum = 0;
-  for (int idx = ks * kPrepThreads + tid; idx < kLoraTileM * kLoraTileR; idx += p.cluster * kPrepThreads) {
-    float vq[kPrepMaxCluster];
 #pragma unroll
-    for (int q = 0; q < kPrepMaxCluster; ++q)
-      vq[q] = q < p.cluster ? ld_shared_cluster_f32(mapa_shared(part_s + 4u * idx, q)) : 0.0f;
+  for (int u = 0; u < kPerThread; ++u) {
+    const int idx = idx0 + u * stride;
     float v = 0.0f;
+    if (idx < kLoraTileM * kLoraTileR) {
+      float vq[kPrepMaxCluster];
 #pragma unroll
-    for (int q = 0; q < kPrepMaxCluster; ++q)
-      if (q < p.cluster) v += vq[q];
-    vsum[nsum] = v;
-    vidx[nsum] = idx;
-    ++nsum;
+      for (int q = 0; q < kPrepMaxCluster; ++q)
+        vq[q] = q < p.cluster ? ld_shared_cluster_f32(mapa_shared(part_s + 4u * idx, q)) : 0.0f;
+#pragma unroll
+      for (int q = 0; q < kPrepMaxCluster; ++q)
+        if (q < p.cluster) v += vq[q];
+    }
+    vsum[u] = v;
   }
   // Done with the partners' shared memory: they may leave once all have
   // arrived, and the writes below overlap that wait -- unless the group sum
@@ -467,8 +474,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
   if (!group_sum) cluster_arrive();
 #pragma unroll
   for (int u = 0; u < kPerThread; ++u) {
-    if (u >= nsum) break;
-    const int row = row0 + vidx[u] / kLoraTileR, rank = rank0 + vidx[u] % kLoraTileR;
+    const int idx = idx0 + u * stride;
+    if (idx >= kLoraTileM * kLoraTileR) break;
+    const int row = row0 + idx / kLoraTileR, rank = rank0 + idx % kLoraTileR;
     if (row < p.M && rank < rr_) {
       if (p.sum_groups && p.groups == 1)
         p.tf[li][static_cast<int64_t>(row) * rr_ + rank] = vsum[u];  // one group: already the sum
@@ -514,11 +522,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
 // dequant warps last: otherwise the MMA issuers starve behind them.  Each
 // group of four consecutive dequant warps covers the four tensor-memory lane
 // quadrants (warp % 4).
-constexpr int kMmaThreads = 608;  // 19 warps
+constexpr int kMmaThreads = 608;  // 19 warps (15 when coupled: four issuer warps)
 constexpr int kWeightWarp = 0, kActWarp = 1, kLoraWarp = 2;
 constexpr int kIssuerWarp0 = 3, kMaxIssuers = 8;
 constexpr int kDeqWarp0 = kIssuerWarp0 + kMaxIssuers;  // dequant + epilogue: warps 11..18
 static_assert(kDeqWarp0 + 8 == kMmaThreads / 32, "warp roles");
+// Coupled launches (up to 64 tokens) run 15 warps: issuers 3..6, dequant
+// 7..14.  With 96 registers a thread, four warps per SM sub-partition leave
+// room for two warps of a 256-thread, 64-register prep CTA beside them (a
+// sub-partition holds 16384 registers), so the prep grid does not keep MMA
+// CTAs off its SMs.
+constexpr int kCoupledWarps = 15;
 constexpr int kTileN = 128;       // output features per CTA (MMA M)
 constexpr int kStageK = 64;       // K per MMA stage (4 x K=16 instructions)
 constexpr int kRawK = 256;        // K per weight-load stage: 128 contiguous bytes of codes per row
@@ -566,14 +580,15 @@ struct MmaParams {
   int raw_stages;  // weight-stage ring depth
   int ab_stages;   // tensor-memory A ring depth, in MMA stages
   int b_stages;    // !coupled: activation ring depth in 64-wide slabs (one barrier pair each; a multiple of kSub)
-  int coupled;     // a weight stage's activation slabs travel with its codes (same barrier, raw ring)
+  int coupled;     // a weight stage's activation slabs sit in the slot of its A stage (same index and empty barrier)
   int issuers;     // MMA-issuing threads, each with its own accumulator
   int t_groups;    // t holds this many partial sums [t_groups][M][r], added in order
   uint32_t off_raw, off_b, off_lora, off_tstage, off_sm, off_bars;
-  uint32_t raw_b_bytes;  // coupled: activation bytes per weight stage (kSub slabs)
+  uint32_t raw_b_bytes;  // coupled: activation slot bytes per weight stage (kSub slabs)
   uint32_t col_a;  // TMEM column of the A stages (accumulators: issuer i at i * n_tok)
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
   int wave;        // CTAs per wave (one per SM) when split == 1, else 0
+  int n_warps;     // 19, or kCoupledWarps (dequant warps: the last eight)
   int stage_out;   // the widest output tile (fp32) fits in the idle ring: staged stores
   // More than 64 tokens: a CTA takes a pair of adjacent 128-row tiles
   // of one linear (grid y counts pairs), so every activation slab it receives
@@ -768,8 +783,8 @@ __device__ __forceinline__ void issue_lora_mmas(const MmaParams& p, const Linear
 }
 
 // The dequantized weight operand goes to tensor memory (tcgen05.st), each MMA
-// reads it from there, and `issuers` threads issue MMAs for interleaved
-// stages into their own accumulators (an MMA occupies its issuing thread for
+// reads it from there, and `issuers` threads issue MMAs for disjoint K steps
+// into their own accumulators (an MMA occupies its issuing thread for
 // far longer than the tensor pipe needs for a 128 x n_tok x 16 product, so
 // one issuer cannot keep the pipe busy at decode token counts).
 // One MMA stage (64 K) of weight row `row` of a staged packed block at
@@ -847,15 +862,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const uint32_t acc_full = bars + 8u * (kB2 + 2);
   const uint32_t tmem_holder = bars + 8u * (kB2 + 3);
   const uint32_t t_full = bars + 8u * (kB2 + 4);
-  // Coupled: the activation slabs of the first ring's stages (later stages'
-  // ride in their weight slot's barrier).
-  const uint32_t x_early = bars + 8u * (kB2 + 5);
   // The activation ring has its own depth and barriers.
   auto b_full = [&](int s) { return bars + 8u * (kB2 + 8 + s); };
   auto b_empty = [&](int s) { return bars + 8u * (kB2 + 8 + kMaxB + s); };
+
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_gen + p.off_bars + 8 * (kB2 + 3) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int deq0 = p.n_warps - 8;  // first dequant warp
   const int split_idx = blockIdx.x;
   // This CTA's linear: the one whose tile range holds blockIdx.y.
   int gi = 0;
@@ -881,10 +895,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
       mbar_init_a(raw_full(s), 1);  // producer expect_tx
-      // The four dequant warps of the stage's group (+ each issuer's
-      // commit when the activation slabs ride in the slot); pair mode: the
-      // groups of both tiles; else all eight.
-      mbar_init_a(raw_empty(s), p.pair ? 4 * ntl : 4 + (p.coupled ? NI : 0));
+      // The four dequant warps of the stage's group; pair mode: the groups
+      // of both tiles.
+      mbar_init_a(raw_empty(s), p.pair ? 4 * ntl : 4);
     }
     if (p.pair) {
       // One barrier pair per (tile, MMA stage) slot of tensor memory: the
@@ -894,12 +907,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         mbar_init_a(ab_empty(w), 1);
       }
     } else {
-      // One barrier pair per weight stage of the tensor-memory ring (kSub MMA
-      // stages): the four warps of the dequant group that wrote it arrive
-      // once each, every issuer commits once.
-      for (int w = 0; w < AS / kSub; ++w) {
-        mbar_init_a(ab_full(w), 4);
-        mbar_init_a(ab_empty(w), NI);
+      // A ring of 2 x (tensor-memory A slots) barrier pairs: weight stage i
+      // uses pair i mod 2AW and A slot i mod AW, so every pair serves stages
+      // of one parity -- one dequant group and, coupled, one issuer group --
+      // and each waiter visits its pairs' phases in order.  Full: the four
+      // warps of the dequant group that wrote the stage (+ coupled, the
+      // activation producer's expect_tx for the stage's slabs); empty: every
+      // issuer of the stage once.
+      for (int b = 0; b < 2 * (AS / kSub); ++b) {
+        mbar_init_a(ab_full(b), 4 + (p.coupled ? 1 : 0));
+        mbar_init_a(ab_empty(b), p.coupled ? NI / 2 : NI);
       }
     }
     for (int s = 0; s < BS; ++s) {
@@ -916,7 +933,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     mbar_init_a(acc_full, n_iss);
 #endif
     mbar_init_a(t_full, 1);
-    mbar_init_a(x_early, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -939,32 +955,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // ------------------------------------------------------------ weight producer
     // One bulk copy per weight stage: the packed block (codes in their
     // swizzled image, then the scale pairs) is contiguous in memory.
-    // Coupled: the stage's activation slabs follow in the same queue
-    // position and complete on the same barrier; they come from the
-    // preceding kernel.
-    const bool coupled = p.coupled != 0;
     const uint8_t* wtile = L.wpacked + static_cast<int64_t>(n0 / kTileN) * raw_total * kRawSlotBytes;
     const int64_t tile_stride = static_cast<int64_t>(raw_total) * kRawSlotBytes;  // next tile's blocks (pair mode)
-    const int kslabs = p.K / kStageK;
-    // The copies into the ring are held for a stage's whole dequant + MMA
-    // time, so the ring alone cannot cover HBM latency at full rate: the
+    // The copies into the ring are held for a stage's whole dequant time,
+    // so the ring alone cannot cover HBM latency at full rate: the
     // blocks kPrefetch stages ahead are prefetched into L2 (bounded by L2
     // capacity, not shared memory) and the ring refills from L2.
     constexpr int kPrefetch = kPrefetchStages;
-    auto xbytes_of = [&](int rst) {
-      return coupled ? static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128) : 0u;
-    };
     // The first ring of weight blocks (and L2 prefetches further
     // ahead) is requested at once: the weights were written before the
-    // preceding kernel of this call started, and their barriers complete on
-    // the weight bytes alone, so the dequant of those stages runs while that
-    // kernel is still at work.  Coupled: the stages' activation slabs follow
-    // on their own barrier once it has finished.
+    // preceding kernel of this call started, so the dequant of those stages
+    // runs while that kernel is still at work.
     const int early = min(RS, nraw);
-    if (lane == 0) {
-      for (int i = 0; i < min(kPrefetch, nraw); ++i)
+    // Coupled, the prep grid runs beside this one and its loads (x, z, the
+    // LoRA A) gate the first MMAs: the L2 prefetches beyond the ring wait
+    // until it has finished, so they do not queue ahead of its loads.
+    auto prefetch_first = [&](int from) {
+      for (int i = from; i < min(kPrefetch, nraw); ++i)
         for (int t = 0; t < ntl; ++t)
           bulk_prefetch_l2(wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes);
+    };
+    if (lane == 0) {
+      if (!p.coupled) prefetch_first(0);
       for (int i = 0; i < early; ++i) {
         mbar_arrive_expect_tx_a(raw_full(i), ntl * kRawSlotBytes);
         for (int t = 0; t < ntl; ++t)
@@ -973,17 +985,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     raw_full(i));
       }
     }
-    if (coupled) {
+    if (p.coupled) {
       griddep_wait();
-      if (lane == 0) {
-        uint32_t xb = 0;
-        for (int i = 0; i < early; ++i) xb += xbytes_of(rb + i);
-        mbar_arrive_expect_tx_a(x_early, xb);
-        for (int i = 0; i < early; ++i)
-          bulk_load(sbase + p.off_b + i * p.raw_b_bytes,
-                    reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rb + i) * p.raw_b_bytes,
-                    xbytes_of(rb + i), x_early);
-      }
+      if (lane == 0) prefetch_first(early);  // the ring's blocks are being loaded
     }
     if (lane == 0) {
       uint32_t ph = 0;
@@ -994,16 +998,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                              kRawSlotBytes);
         const int rst = rb + i;
         if (i >= early) {
-          const uint32_t xbytes = xbytes_of(rst);
           if (!mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status)) break;
-          mbar_arrive_expect_tx_a(raw_full(s), ntl * kRawSlotBytes + xbytes);
+          mbar_arrive_expect_tx_a(raw_full(s), ntl * kRawSlotBytes);
           for (int t = 0; t < ntl; ++t)
             bulk_load(sbase + p.off_raw + s * rslot + t * kRawSlotBytes,
                       wtile + t * tile_stride + static_cast<int64_t>(rst) * kRawSlotBytes, kRawSlotBytes, raw_full(s));
-          if (coupled)
-            bulk_load(sbase + p.off_b + s * p.raw_b_bytes,
-                      reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rst) * p.raw_b_bytes, xbytes,
-                      raw_full(s));
         }
         if (++s == RS) {
           s = 0;
@@ -1029,7 +1028,36 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // ------------------------------------------------------------ activation producer
     griddep_wait();  // the staged activations are written by the preceding kernel
     {
-      if (!p.coupled && lane == 0) {
+      if (p.coupled && lane == 0) {
+        // Up to 64 tokens: one bulk copy of a weight stage's kSub slabs (the
+        // tiled layout keeps them contiguous) into the activation slot of its
+        // tensor-memory A slot, completing on the stage's full barrier.  The
+        // stage AW earlier (same slots) must have finished its MMAs: its
+        // empty barrier releases A and the slabs together, so a weight slot
+        // is refilled as soon as it is dequantized, whatever the MMAs still
+        // read.  (That stage's completion also orders the previous phase of
+        // this full barrier before the arrival below.)  For the first AW
+        // stages the wait is on a fresh barrier's parity 1 and passes.
+        const int AW = AS / kSub, BW = 2 * AW;
+        const int kslabs = p.K / kStageK;
+        int w = 0, b = 0, e = AW;  // A slot, barrier pair of stage i; barrier pair of stage i - AW
+        uint32_t eph = 1;          // phase parity of stage i - AW on its pair (use -1 at first)
+        for (int i = 0; i < nraw; ++i) {
+          if (!mbar_wait_a(ab_empty(e), eph, abort_flag, p.status)) break;
+          const int rst = rb + i;
+          const uint32_t xbytes = static_cast<uint32_t>(min(kSub, kslabs - rst * kSub) * p.n_tok * 128);
+          mbar_arrive_expect_tx_a(ab_full(b), xbytes);
+          bulk_load(sbase + p.off_b + w * p.raw_b_bytes,
+                    reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(rst) * p.raw_b_bytes, xbytes,
+                    ab_full(b));
+          if (++w == AW) w = 0;
+          if (++b == BW) b = 0;
+          if (++e == BW) {
+            e = 0;
+            eph ^= 1;
+          }
+        }
+      } else if (!p.coupled && lane == 0) {
         // One bulk copy per 64-wide K slab (tiled layout: the slabs of
         // consecutive MMA stages are contiguous), each slot with its own full
         // and empty barrier, so a slot is refilled as soon as the MMAs that
@@ -1057,7 +1085,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
       }
     }
-  } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kMaxIssuers) {
+  } else if (warp >= kIssuerWarp0 && warp < deq0) {
     // ------------------------------------------------------------ MMA issuers
     const int ii = warp - kIssuerWarp0;
     if (ii < n_iss) {
@@ -1104,43 +1132,42 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       } else {
         // The whole warp runs the loop (waits, addresses and descriptors are
         // warp-uniform); lane 0 issues the MMAs and their commits.  A weight
-        // stage holds kSub x 4 MMAs (u = 4 q + kk: MMA stage q, K step kk);
-        // issuer ii takes the contiguous block of `per` of them starting at
-        // ii * per, into its own accumulator (with <= 4 issuers an MMA stage
-        // therefore has a single issuer).  Every issuer waits for the slot's
-        // full barrier and commits once to its empty barrier (and, coupled,
-        // to the raw slot whose activation slabs it read), so a slot cannot
-        // be refilled before all of them are done and no waiter falls two
-        // phases behind.  Coupled, the activation slabs landed with the
-        // weight stage on its raw barrier, which the dequant warps waited for
-        // before arriving on the slot's full barrier: waiting for that barrier
-        // orders the slabs before these MMAs too.
-        const int AW = AS / kSub;
-        const int per = kSub * 4 / NI;
-        const int u0 = ii * per;
+        // stage holds kSub x 4 MMAs (u = 4 q + kk: MMA stage q, K step kk).
+        // Coupled, the issuers form two groups that take alternate weight
+        // stages (the stages of one barrier pair), so one group's waits,
+        // fences and commits overlap the other's MMAs; otherwise one group
+        // takes every stage.  Within a group, issuer j takes the contiguous
+        // block of `per` MMAs starting at j * per, into its own accumulator.
+        // Every issuer of the group waits for the stage's full barrier and
+        // commits once to its empty barrier, so the slots cannot be refilled
+        // before all of them are done.  Coupled, the stage's activation slabs
+        // sit in the activation slot of its A slot's index and land on the
+        // same full barrier.
+        const int AW = AS / kSub, BW = 2 * AW;
+        const int NG = p.coupled ? 2 : 1;
+        const int gsz = NI / NG;
+        const int g = ii / gsz;
+        const int per = kSub * 4 / gsz;
+        const int u0 = (ii - g * gsz) * per;
         const uint32_t b_slab = static_cast<uint32_t>(p.n_tok * 128);
-        int w = 0, rs = 0;
-        uint32_t wph = 0;
+        int w = g, b = g;  // A slot and barrier pair of stage wi
+        uint32_t bph = 0;
         int js = 0, jsb = 0;  // separate activation ring: slab 0 is in slot 0, phase 0
         uint32_t jph = 0;
-        // Coupled: the first ring's activation slabs have their own barrier
-        // (the first MMA always reads one of them).
-        const bool xe_ok = !p.coupled || warp_wait(x_early, 0, abort_flag, p.status);
-        for (int wi = 0; xe_ok && wi < nraw; ++wi) {
-          if (!warp_wait(ab_full(w), wph, abort_flag, p.status)) break;
+        for (int wi = g; wi < nraw; wi += NG) {
+          if (!warp_wait(ab_full(b), bph, abort_flag, p.status)) break;
           const int nq = min(kSub, nmma - wi * kSub);
           const int u1 = min(u0 + per, 4 * nq);  // this issuer's MMAs in this weight stage: [u0, u1)
           const uint32_t a_st = tmem_base + p.col_a + static_cast<uint32_t>(w * kSub * kAStageCols);
           tc_fence_after();
           if (p.coupled) {
-            const uint32_t b_st = sbase + p.off_b + static_cast<uint32_t>(rs) * p.raw_b_bytes;
+            const uint32_t b_st = sbase + p.off_b + static_cast<uint32_t>(w) * p.raw_b_bytes;
             if (lane == 0) {
               for (int u = u0; u < u1; ++u)
                 tc_mma_f16_ts(d_acc, a_st + (u >> 2) * kAStageCols + (u & 3) * 8,
                               sw128_kmajor_desc(b_st + (u >> 2) * b_slab + (u & 3) * 32), idesc,
-                              (u > u0 || wi > 0) ? 1u : acc);
-              tc_commit(ab_empty(w));
-              tc_commit(raw_empty(rs));
+                              u > u0 ? 1u : acc);
+              tc_commit(ab_empty(b));
             }
             if (u1 > u0) acc = 1;
           } else {
@@ -1175,14 +1202,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
               acc = 1;
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(ab_empty(w));
+            if (lane == 0) tc_commit(ab_empty(b));
           }
           __syncwarp();
-          if (++w == AW) {
-            w = 0;
-            wph ^= 1;
+          w += NG;
+          if (w >= AW) w -= AW;
+          b += NG;
+          if (b >= BW) {
+            b -= BW;
+            bph ^= 1;
           }
-          if (++rs == RS) rs = 0;
         }
       }
       if (lane == 0) {
@@ -1230,16 +1259,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_a(lora_full);
     }
-  } else if (warp >= kDeqWarp0) {
+  } else if (warp >= deq0) {
     // ------------------------------------------------------------ dequant warps
-    const int dw = warp - kDeqWarp0;
+    const int dw = warp - deq0;
     const bool wt = p.wt != 0;
     uint32_t lut = 0u;
     if (L.nf4) {
       // The NF4 table: entry e (a code byte) = the fp16 pair (level[e & 15],
       // level[e >> 4]), low element in the low half as the E2M1 conversion.
       lut = sbase + p.off_lut;
-      const int e = static_cast<int>(threadIdx.x) - 32 * kDeqWarp0;  // 0..255
+      const int e = static_cast<int>(threadIdx.x) - 32 * deq0;  // 0..255
       sts32(lut + 4u * e, static_cast<uint32_t>(p.nf4_half[e & 15]) | (static_cast<uint32_t>(p.nf4_half[e >> 4]) << 16));
       named_barrier_sync(3, 256);
     }
@@ -1299,9 +1328,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const int grp = dw >> 2;
         const int row = 32 * (warp & 3) + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        const int AW = AS / kSub;  // tensor-memory slots, one weight stage each (>= 2)
-        int s = grp, w = grp;      // this group's first stage (index grp): raw slot grp, A slot grp (RS, AW >= 2)
-        uint32_t ph = 0, aph = 0;
+        const int AW = AS / kSub, BW = 2 * AW;  // tensor-memory slots (one weight stage each, >= 2); barrier pairs
+        // Stage i: raw slot i mod RS, A slot i mod AW, barrier pair i mod BW;
+        // before its first store, stage i - AW (same A slot) must have
+        // finished its MMAs: pair (i - AW) mod BW, whose phase parity for
+        // that stage starts at 1 (a fresh barrier: the first AW stages pass).
+        int s = grp, w = grp, b = grp, e = grp + AW;
+        uint32_t ph = 0, eph = 1;
         for (int i = grp; i < nraw; i += 2) {
           if (!warp_wait(raw_full(s), ph, abort_flag, p.status)) break;
           const uint32_t slot = sbase + p.off_raw + s * kRawSlotBytes;
@@ -1319,7 +1352,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             dequant_mma_stage<kLut>(slot, row, q, wt, lut, o);
             // The slot's previous MMAs must be done before the first store
             // (the first conversion overlaps that wait).
-            if (q == 0 && !warp_wait(ab_empty(w), aph ^ 1, abort_flag, p.status)) {
+            if (q == 0 && !warp_wait(ab_empty(e), eph, abort_flag, p.status)) {
               ok = false;
               break;
             }
@@ -1330,7 +1363,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive_a(ab_full(w));
+            mbar_arrive_a(ab_full(b));
             mbar_arrive_a(raw_empty(s));
           }
           s += 2;
@@ -1339,9 +1372,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             ph ^= 1;
           }
           w += 2;
-          if (w >= AW) {
-            w -= AW;
-            aph ^= 1;
+          if (w >= AW) w -= AW;
+          b += 2;
+          if (b >= BW) b -= BW;
+          e += 2;
+          if (e >= BW) {
+            e -= BW;
+            eph ^= 1;
           }
         }
       }
@@ -1354,7 +1391,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // The LoRA operand's t tiles, by all 256 dequant threads once their
       // stream is done: from the rows the LoRA warp staged (early), or from
       // global memory into the idle ring (late).
-      const int dtid = static_cast<int>(threadIdx.x) - 32 * kDeqWarp0;
+      const int dtid = static_cast<int>(threadIdx.x) - 32 * deq0;
       griddep_wait();  // the row exponents come from the preceding kernel
       fill_lora_factors(p, L, smv + 4u * p.n_tok, m0, dtid, 256);
       named_barrier_sync(1, 256);
@@ -1403,9 +1440,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   // ---------------------------------------------------------------- epilogue
   const uint32_t part = sbase;  // [tile][n_tok][128] fp32 scaled partial tiles (split > 1), ring reused
-  const int dt = static_cast<int>(threadIdx.x) - 32 * kDeqWarp0;  // dequant-warp thread index
+  const int dt = static_cast<int>(threadIdx.x) - 32 * deq0;  // dequant-warp thread index
   const int ntl_e = p.pair ? ntl : 1;                              // weight tiles of this CTA
-  if (warp >= kDeqWarp0) {
+  if (warp >= deq0) {
     // Row scales S * 2^-e_m come from the preceding kernel; the dequant above did not need them.
     griddep_wait();
     {
@@ -1420,19 +1457,29 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int nl = q * 32 + lane;
     // Pair mode: warp group eg reads tile eg's accumulator, all token columns;
     // otherwise the two groups split the token columns of the one tile.
-    const int eg = p.pair ? (warp - kDeqWarp0) >> 2 : 0;
+    const int eg = p.pair ? (warp - deq0) >> 2 : 0;
     const bool live = eg < ntl_e;
     const int n = n0 + eg * kTileN + nl;
     const int cols = p.pair ? p.n_tok : p.n_tok / 2;
-    const int c0 = p.pair ? 0 : ((warp - kDeqWarp0) >> 2) * cols;
+    const int c0 = p.pair ? 0 : ((warp - deq0) >> 2) * cols;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acc0 = static_cast<uint32_t>(eg * p.n_tok);       // first accumulator column
     const uint32_t tile_out = static_cast<uint32_t>(eg * p.n_tok * kTileN);  // element offset of its staged tile
-    // Issuer a holds a sum iff its first MMA falls in the first weight
-    // stage's (up to kSub) MMA stages: a prefix of the issuers.  Pair mode:
-    // one accumulator per tile.
-    const int nq0 = min(kSub, nmma);
-    const int nacc = p.pair ? 1 : min(NI, (nq0 * NI + 3) / 4);
+    // Issuer a holds a sum iff it issued an MMA, i.e. iff its block of MMAs
+    // starts inside the first weight stage of its group (only the last stage
+    // can be short).  One group: a prefix of the issuers.  Two groups
+    // (coupled): group g's first stage is stage g.  Pair mode: one
+    // accumulator per tile.
+    uint32_t accs = 1u;
+    if (!p.pair) {
+      const int NG = p.coupled ? 2 : 1, gsz = NI / NG, per = kSub * 4 / gsz;
+      accs = 0u;
+      for (int g = 0; g < NG && g < nraw; ++g) {
+        const int nq = min(kSub, nmma - g * kSub);
+        for (int j = 0; j < gsz && j * per < 4 * nq; ++j) accs |= 1u << (g * gsz + j);
+      }
+    }
+    const int nacc = 32 - __clz(static_cast<int>(accs));  // accumulator slots to scan
     if (p.pair && live) {
       // One accumulator per tile: 32 token columns per TMEM load and wait
       // (columns past n_tok are read -- they lie inside tensor memory -- but
@@ -1500,7 +1547,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           sts16(sbase + 2u * (el0 + e * kTileN), __bfloat16_as_ushort(__float2bfloat16_rn(val[e])));
       }
     };
-    if (!p.pair && nacc <= 2 && cols % 32 == 0) {
+    if (!p.pair && (accs == 1u || accs == 3u) && cols % 32 == 0) {
       for (int c = c0; c < c0 + cols; c += 32) {
         float w[32], w2[32];
         tmem_ld_x32(tmem_base + acc0 + lane_off + c, w);
@@ -1528,15 +1575,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         float w[4][8];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
-          if (a0 + a < nacc)
+          if ((accs >> (a0 + a)) & 1u)
             tmem_ld_x8(tmem_base + acc0 + static_cast<uint32_t>((a0 + a) * p.n_tok) + lane_off + c, w[a]);
         tmem_ld_wait();
+        // (Accumulator 0 always holds a sum.)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          float t = a0 == 0 ? w[0][e] : v[e] + w[0][e];
+          float t = a0 == 0 ? w[0][e] : v[e];
+          if (a0 > 0 && ((accs >> a0) & 1u)) t += w[0][e];
 #pragma unroll
           for (int a = 1; a < 4; ++a)
-            if (a0 + a < nacc) t += w[a][e];
+            if ((accs >> (a0 + a)) & 1u) t += w[a][e];
           v[e] = t;
         }
       }
@@ -1603,7 +1652,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   if (p.split > 1) {
     cluster_sync_all();  // every partner's scaled partial tile is in its shared memory
-    if (warp >= kDeqWarp0) {
+    if (warp >= deq0) {
       const int rank = static_cast<int>(cluster_ctarank());
       const int per = (p.n_tok + p.split - 1) / p.split;
       const int mb = rank * per;
@@ -2111,6 +2160,9 @@ bool kernel_attrs_ok() {
                                       cudaSharedmemCarveoutMaxShared);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      cudaSharedmemCarveoutMaxShared);
   });
   return attr_err == cudaSuccess;
 }
@@ -2286,16 +2338,16 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // waves x weight stages per CTA, with a small per-CTA fixed cost.  A wave is
   // as many clusters as can be resident at once (clusters live inside one
   // GPC, so e.g. 7-CTA clusters leave SMs unused).
-  // Up to 64 tokens the prep grid that precedes the MMA kernel holds SMs
-  // until its LoRA tiles finish (a row task or LoRA CTA each; an MMA CTA
-  // cannot share an SM with one), so MMA CTAs beyond the free SMs start only
-  // then.  When the chosen split does not fit the free SMs but a smaller one
+  // Coupled launches (up to 64 tokens, single tiles) share each SM with a
+  // prep CTA.  Pair-mode launches (33-64 tokens) cannot: the prep grid holds
+  // SMs until its LoRA tiles finish, so MMA CTAs beyond the free SMs start
+  // only then.  When the chosen split does not fit the free SMs but a smaller one
   // does, at most twice the weight stages per CTA, the smaller one is taken:
   // every CTA then dequantizes ahead while prep runs (measured: the 7B o
   // launch at <= 16 tokens, 13.1 -> 12.2 us with 3-way instead of 5-way
   // splits).
   int prep_busy = 0;
-  if (M <= 64 && r > 0) {
+  if (M > 32 && M <= 64 && r > 0) {  // up to 32 tokens the launch is coupled: prep runs beside it
     const LoraSplit ls0 = launch_lora_split(a, ranks);
     int ltiles = 0;
     for (int i = 0; i < nlin; ++i)
@@ -2369,13 +2421,12 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   const uint32_t b_stage = static_cast<uint32_t>(n_tok) * 128u;
   // The dequantized weights go to tensor memory as the MMA's A operand.
   // Each MMA occupies its issuing thread for ~150 cycles whatever the token
-  // count, so small tiles take more issuers (each with its own accumulator,
-  // which tensor memory must hold next to the A ring, and which the epilogue
-  // reads and adds).  Four issuers up to 64 tokens: 600 issue cycles per
-  // weight stage against a ~1250-cycle stage period, one tensor-memory read
-  // round in the epilogue and a third weight stage of A at 32 tokens
-  // (measured 1.2% faster than eight at <= 32 tokens, and two issuers 5%
-  // slower).  Pair mode: one issuer per tile.
+  // count, and each weight stage costs an issuer ~600 more cycles of waits,
+  // fences and commits; so small tiles take more issuers, each with its own
+  // accumulator (which tensor memory must hold next to the A ring, and which
+  // the epilogue reads and adds).  Up to 64 tokens two groups of two issuers
+  // take alternate weight stages (the 15-warp layout has four issuer warps).
+  // Pair mode: one issuer per tile.
   const int issuers = pair ? 2 : (n_tok <= 64 ? 4 : 2);
   const uint32_t col_a = static_cast<uint32_t>(align_up(issuers * n_tok, 32));
   if (col_a > static_cast<uint32_t>(kTmemCols)) return QERL_ERR_UNSUPPORTED_SHAPE;
@@ -2393,16 +2444,16 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   bool any_nf4 = false;
   for (int i = 0; i < nlin; ++i) any_nf4 = any_nf4 || a.lin[i].nf4;
   const uint32_t lut_bytes = any_nf4 ? 1024u : 0u;  // 256 fp16 pairs
-  // Up to 64 tokens a weight stage's activation slabs ride in its raw-ring
-  // slot; above, a separate activation ring is filled by one bulk copy per
-  // weight stage.
+  // Up to 64 tokens a weight stage's activation slabs (one bulk copy) sit in
+  // the activation slot of its tensor-memory A stage and are released with it;
+  // above, a separate activation ring holds one slab per slot.
   const int coupled = (n_tok <= 64 && !pair) ? 1 : 0;
   const uint32_t raw_b = coupled ? static_cast<uint32_t>(kSub) * b_stage : 0u;
   auto plan_for = [&](int rs, int bs) {
     Plan P;
     P.raw = 0;  // packed weight blocks (codes + scale pairs); 18 KB slots keep 1024-byte alignment
     P.b = P.raw + rs * tpc * kRawSlotBytes;
-    uint32_t ring = P.b + (coupled ? rs * raw_b : bs * b_stage);
+    uint32_t ring = P.b + (coupled ? static_cast<uint32_t>(ab_cap / kSub) * raw_b : bs * b_stage);
     if (!lora_early) ring = std::max(ring, lb);  // late LoRA tiles are built inside the ring
     ring = std::max(ring, part_bytes);
     P.lora = static_cast<uint32_t>(align_up(ring, 1024));
@@ -2418,6 +2469,14 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   };
   const int ab_stages = ab_cap;
   int raw_stages = 0, b_stages = 0;
+  // Coupled (up to 64 tokens) a prep CTA runs beside each MMA CTA: the ring
+  // leaves room for its shared memory (dynamic + static) and both CTAs'
+  // reserved kilobyte.
+  size_t prep_smem_est = static_cast<size_t>(K) * 2;
+  if (r > 0) prep_smem_est = std::max(prep_smem_est, static_cast<size_t>(kLoraSmemBytes));
+  const uint32_t smem_cap = (coupled && prep_smem_est + 3072 < kSmemPerSm)
+                                ? std::min<uint32_t>(kSmemLimit, kSmemPerSm - 3072u - static_cast<uint32_t>(prep_smem_est))
+                                : static_cast<uint32_t>(kSmemLimit);
   {
     // A lives in tensor memory: keep its depth.  Mbarrier waits test a phase
     // parity, so every ring slot must always be waited on by the same thread
@@ -2433,7 +2492,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
     // any depth >= 2 works.)
     auto max_rs = [&](int bs) {
       int rs = kMaxRaw;
-      while (rs >= 2 && plan_for(rs, bs).total > static_cast<uint32_t>(kSmemLimit)) --rs;
+      while (rs >= 2 && plan_for(rs, bs).total > smem_cap) --rs;
       return pair ? rs : rs & ~1;
     };
     int best_rs = 0, best_bs = 0;
@@ -2474,7 +2533,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // A weight stage is handed over (and its activations loaded) at once.
   if (ab_stages < 2 * kSub || ab_stages % kSub != 0 || b_stages < kSub || b_stages % kSub != 0 ||
       (!pair && raw_stages % 2 != 0) || (kSub * 4) % issuers != 0 || (!coupled && issuers > kSub) ||
-      (pair && (issuers != 2 || ab_stages != 2 * kSub)))
+      (pair && (issuers != 2 || ab_stages != 2 * kSub)) || (coupled && issuers > kCoupledWarps - 8 - kIssuerWarp0))
     return QERL_ERR_UNSUPPORTED_SHAPE;
   const Plan P = plan_for(raw_stages, b_stages);
 
@@ -2636,6 +2695,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.coupled = coupled;
   mp.raw_b_bytes = raw_b;
   mp.issuers = issuers;
+  mp.n_warps = coupled ? kCoupledWarps : kMmaThreads / 32;
   mp.t_groups = pp.sum_groups ? 1 : pp.groups;  // == t_groups
   mp.col_a = col_a;
   mp.off_raw = P.raw;
@@ -2655,7 +2715,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(split), static_cast<unsigned>(n_tiles), static_cast<unsigned>(m_tiles));
-  cfg.blockDim = dim3(kMmaThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(32 * mp.n_warps), 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attrs[2];
