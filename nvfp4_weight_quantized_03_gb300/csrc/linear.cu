@@ -2205,8 +2205,25 @@ LoraSplit launch_lora_split(const LinearArgs& a, const int* ranks) {
   int64_t stage_tiles = 0;
   for (int i = 0; i < a.nlin; ++i)
     stage_tiles += ((a.lin[i].n + kTileN - 1) / kTileN) * ((a.k + kRawK - 1) / kRawK);
-  const int chunks = stage_tiles < 8 * static_cast<int64_t>(sm_count()) ? 2 : (a.m >= 32 ? 4 : 3);
-  return lora_split(a.m, a.k, ranks, a.nlin, chunks);
+  int chunks = stage_tiles < 8 * static_cast<int64_t>(sm_count()) ? 2 : (a.m >= 32 ? 4 : 3);
+  LoraSplit L = lora_split(a.m, a.k, ranks, a.nlin, chunks);
+  // Up to 32 tokens each SM holds one prep CTA beside its MMA CTA: more
+  // chunks per LoRA CTA until the prep grid (row tasks + LoRA tiles) fits
+  // one CTA per SM.
+  if (a.m <= 32) {
+    int ltiles = 0;
+    for (int i = 0; i < a.nlin; ++i)
+      if (ranks[i] > 0)
+        ltiles += static_cast<int>((a.m + kLoraTileM - 1) / kLoraTileM) * ((ranks[i] + kLoraTileR - 1) / kLoraTileR);
+    const int n_tok = static_cast<int>((a.m + 15) / 16 * 16);
+    const int sms = sm_count();
+    for (;;) {
+      const int rows = (std::max(static_cast<int>(a.m), n_tok) + L.cluster - 1) / L.cluster * L.cluster;
+      if (rows + ltiles * L.groups * L.cluster <= sms || L.groups == 1 || chunks >= 64) break;
+      L = lora_split(a.m, a.k, ranks, a.nlin, ++chunks);
+    }
+  }
+  return L;
 }
 
 LoraDown linear_lora_down(const LinearArgs& a, int i) {
