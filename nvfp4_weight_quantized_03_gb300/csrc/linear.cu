@@ -589,6 +589,10 @@ struct MmaParams {
   int lora_early;  // LoRA operand tiles built at kernel start (dedicated region) or after the mainloop (in the ring)
   int wave;        // CTAs per wave (one per SM) when split == 1, else 0
   int n_warps;     // 19, or kCoupledWarps (dequant warps: the last eight)
+  // 1: the staged x~ and row scales come from a kernel that finished before
+  // the preceding one (the tensor-core LoRA down-projection) started, so they
+  // are read without waiting for that kernel; only t waits for it.
+  int acts_ready;
   int stage_out;   // the widest output tile (fp32) fits in the idle ring: staged stores
   // More than 64 tokens: a CTA takes a pair of adjacent 128-row tiles
   // of one linear (grid y counts pairs), so every activation slab it receives
@@ -1026,7 +1030,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
   } else if (warp == kActWarp) {
     // ------------------------------------------------------------ activation producer
-    griddep_wait();  // the staged activations are written by the preceding kernel
+    if (!p.acts_ready) griddep_wait();  // the staged activations are written by the preceding kernel
     {
       if (p.coupled && lane == 0) {
         // Up to 64 tokens: one bulk copy of a weight stage's kSub slabs (the
@@ -1443,8 +1447,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int dt = static_cast<int>(threadIdx.x) - 32 * deq0;  // dequant-warp thread index
   const int ntl_e = p.pair ? ntl : 1;                              // weight tiles of this CTA
   if (warp >= deq0) {
-    // Row scales S * 2^-e_m come from the preceding kernel; the dequant above did not need them.
-    griddep_wait();
+    // Row scales S * 2^-e_m come from the preceding kernel (or, acts_ready,
+    // the one before it); the dequant above did not need them.
+    if (!p.acts_ready) griddep_wait();
     {
       const float S = *L.tensor_scale;
       for (int i = dt; i < p.n_tok; i += 256)
@@ -2077,7 +2082,11 @@ qerl_status lora_down_tc(const void* x, int64_t ldx, int64_t M, int64_t K, const
   // Split K over a cluster, then over groups of clusters, until the grid
   // covers the SMs once (a CTA streams 20 KB per K chunk into one SM, so few
   // CTAs over a long K are bound by that SM's ingress).
-  const int want = (sm_count() + m_tiles * nz - 1) / (m_tiles * nz);
+  // One token tile (decode, up to 128 tokens): a quarter of the SMs.  The
+  // MMA grid that follows reads t only after its main loop, and the SMs this
+  // grid leaves free take MMA CTAs at once.
+  const int cover = m_tiles == 1 ? std::max(1, sm_count() / 4) : sm_count();
+  const int want = (cover + m_tiles * nz - 1) / (m_tiles * nz);
   int split = std::max(1, std::min(want, std::min(kLdMaxSplit, nk)));
   int groups = (want + split - 1) / split;
   groups = std::max(1, std::min({groups, max_groups, nk / split}));
@@ -2713,6 +2722,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.raw_b_bytes = raw_b;
   mp.issuers = issuers;
   mp.n_warps = coupled ? kCoupledWarps : kMmaThreads / 32;
+  mp.acts_ready = tc_lora ? 1 : 0;  // prep, then the down-projection, then this kernel
   mp.t_groups = pp.sum_groups ? 1 : pp.groups;  // == t_groups
   mp.col_a = col_a;
   mp.off_raw = P.raw;
