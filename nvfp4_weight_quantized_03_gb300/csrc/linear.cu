@@ -593,6 +593,7 @@ struct MmaParams {
   // the preceding one (the tensor-core LoRA down-projection) started, so they
   // are read without waiting for that kernel; only t waits for it.
   int acts_ready;
+  int w_evict_first;  // one token tile: each weight block is read once, so it leaves L2 first
   int stage_out;   // the widest output tile (fp32) fits in the idle ring: staged stores
   // More than 64 tokens: a CTA takes a pair of adjacent 128-row tiles
   // of one linear (grid y counts pairs), so every activation slab it receives
@@ -979,14 +980,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int t = 0; t < ntl; ++t)
           bulk_prefetch_l2(wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes);
     };
+    // One token tile reads each weight block once: after its copy into the
+    // ring it is marked first to leave L2, so the stream does not evict the
+    // activations, the outputs and this kernel's code.
+    const uint64_t wpol = p.w_evict_first ? l2_policy_evict_first() : 0ull;
+    auto load_w = [&](uint32_t dst, const uint8_t* src, uint32_t bar) {
+      if (p.w_evict_first)
+        bulk_load_hint(dst, src, kRawSlotBytes, bar, wpol);
+      else
+        bulk_load(dst, src, kRawSlotBytes, bar);
+    };
     if (lane == 0) {
       if (!p.coupled) prefetch_first(0);
       for (int i = 0; i < early; ++i) {
         mbar_arrive_expect_tx_a(raw_full(i), ntl * kRawSlotBytes);
         for (int t = 0; t < ntl; ++t)
-          bulk_load(sbase + p.off_raw + i * rslot + t * kRawSlotBytes,
-                    wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, kRawSlotBytes,
-                    raw_full(i));
+          load_w(sbase + p.off_raw + i * rslot + t * kRawSlotBytes,
+                 wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, raw_full(i));
       }
     }
     if (p.coupled) {
@@ -1005,8 +1015,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           if (!mbar_wait_a(raw_empty(s), ph ^ 1, abort_flag, p.status)) break;
           mbar_arrive_expect_tx_a(raw_full(s), ntl * kRawSlotBytes);
           for (int t = 0; t < ntl; ++t)
-            bulk_load(sbase + p.off_raw + s * rslot + t * kRawSlotBytes,
-                      wtile + t * tile_stride + static_cast<int64_t>(rst) * kRawSlotBytes, kRawSlotBytes, raw_full(s));
+            load_w(sbase + p.off_raw + s * rslot + t * kRawSlotBytes,
+                   wtile + t * tile_stride + static_cast<int64_t>(rst) * kRawSlotBytes, raw_full(s));
         }
         if (++s == RS) {
           s = 0;
@@ -2723,6 +2733,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   mp.issuers = issuers;
   mp.n_warps = coupled ? kCoupledWarps : kMmaThreads / 32;
   mp.acts_ready = tc_lora ? 1 : 0;  // prep, then the down-projection, then this kernel
+  mp.w_evict_first = m_tiles == 1 ? 1 : 0;
   mp.t_groups = pp.sum_groups ? 1 : pp.groups;  // == t_groups
   mp.col_a = col_a;
   mp.off_raw = P.raw;
