@@ -1071,6 +1071,34 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             eph ^= 1;
           }
         }
+      } else if (p.pair && lane == 0) {
+        // Pair mode: the ring's BS slabs form two halves of G = BS / 2 slabs
+        // (a weight stage's kSub slabs, or half of them), each half one
+        // barrier pair filled at once, so each issuer waits and commits once
+        // per G MMA stages.  One token tile: the tiled layout keeps the slabs
+        // contiguous (one bulk copy); several token tiles: one 2-D TMA tile
+        // per slab from [M][K] (rows past M are zero-filled).
+        const uint32_t slab = static_cast<uint32_t>(p.n_tok) * 128u;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.xs) + static_cast<int64_t>(mma_begin) * slab;
+        const bool rowmajor = p.xs_rowmajor != 0;
+        const int G = BS / 2;
+        int sj = 0;
+        uint32_t sph = 0;
+        for (int g0 = 0; g0 < nmma; g0 += G) {
+          const int nq = min(G, nmma - g0);
+          if (!mbar_wait_a(b_empty(sj), sph ^ 1, abort_flag, p.status)) break;
+          mbar_arrive_expect_tx_a(b_full(sj), static_cast<uint32_t>(nq) * slab);
+          const uint32_t dst = sbase + p.off_b + static_cast<uint32_t>(sj * G) * slab;
+          if (rowmajor) {
+            for (int q = 0; q < nq; ++q)
+              tma_load_2d(dst + static_cast<uint32_t>(q) * slab, &tm_xs, (mma_begin + g0 + q) * kStageK, m0,
+                          b_full(sj));
+          } else {
+            bulk_load(dst, src + static_cast<int64_t>(g0) * slab, static_cast<uint32_t>(nq) * slab, b_full(sj));
+          }
+          sj ^= 1;
+          if (sj == 0) sph ^= 1;
+        }
       } else if (!p.coupled && lane == 0) {
         // One bulk copy per 64-wide K slab (tiled layout: the slabs of
         // consecutive MMA stages are contiguous), each slot with its own full
@@ -1109,39 +1137,42 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (p.pair) {
         // Pair mode: this issuer owns tile ii of the pair (its accumulator,
         // its tensor-memory A slot per MMA stage q: ab_*(ii * kSub + q)) and
-        // reads every activation slab in order; each slab's empty barrier
-        // takes the commits of both issuers.
+        // reads the activation slabs half a ring (G = BS / 2 MMA stages) at a
+        // time: one wait before a half's first MMA stage, one commit after its
+        // last.
         const uint32_t b_slab = static_cast<uint32_t>(p.n_tok * 128);
-        int jsb = 0;
-        uint32_t jph = 0;
-        for (int wi = 0; wi < nraw; ++wi) {
+        const int G = BS / 2;
+        int sj = 0, jj = 0, j = 0;  // slab half, MMA stage within it, MMA stage of the CTA
+        uint32_t sph = 0;
+        bool ok = true;
+        for (int wi = 0; ok && wi < nraw; ++wi) {
           const int nq = min(kSub, nmma - wi * kSub);
-          bool ok = true;
-          for (int q = 0; q < nq; ++q) {
+          for (int q = 0; q < nq; ++q, ++j) {
             const int sl = ii * kSub + q;
-            if (!warp_wait(ab_full(sl), wi & 1, abort_flag, p.status) ||
-                !warp_wait(b_full(jsb), jph, abort_flag, p.status)) {
+            if ((jj == 0 && !warp_wait(b_full(sj), sph, abort_flag, p.status)) ||
+                !warp_wait(ab_full(sl), wi & 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t a_st = tmem_base + p.col_a + static_cast<uint32_t>(sl * kAStageCols);
-            const uint32_t b_addr = sbase + p.off_b + jsb * b_slab;
+            const uint32_t b_addr = sbase + p.off_b + static_cast<uint32_t>(sj * G + jj) * b_slab;
+            const bool last = ++jj == G || j + 1 == nmma;
             if (lane == 0) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 tc_mma_f16_ts(d_acc, a_st + kk * 8, sw128_kmajor_desc(b_addr + kk * 32), idesc,
                               (wi > 0 || q > 0 || kk > 0) ? 1u : 0u);
               tc_commit(ab_empty(sl));
-              tc_commit(b_empty(jsb));
+              if (last) tc_commit(b_empty(sj));
             }
-            if (++jsb == BS) {
-              jsb = 0;
-              jph ^= 1;
+            if (last) {
+              jj = 0;
+              sj ^= 1;
+              if (sj == 0) sph ^= 1;
             }
           }
           __syncwarp();
-          if (!ok) break;
         }
       } else {
         // The whole warp runs the loop (waits, addresses and descriptors are
