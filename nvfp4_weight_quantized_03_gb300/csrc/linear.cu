@@ -83,8 +83,14 @@ constexpr int kLoraStages = 3;   // chunks in flight (cp.async ring)
 // One ring stage: x [16][64] bf16, A [32][64] bf16, z [16][64] fp32 (one
 // row of it when the noise is shared by all rows).
 constexpr int kLoraStageBytes = (kLoraTileM + kLoraTileR) * kLoraKc * 2 + kLoraTileM * kLoraKc * 4;
-constexpr int kLoraSmemBytes = kLoraStages * kLoraStageBytes + (kLoraTileM + kLoraTileR) * kLoraPad * 4;
-constexpr int kPrepMaxCluster = 8;
+constexpr int kLoraTileSmemBytes = kLoraStages * kLoraStageBytes + (kLoraTileM + kLoraTileR) * kLoraPad * 4;
+constexpr int kPrepMaxClusterC = 8;
+// + the receive buffer of the partial-tile push (each CTA of a cluster owns
+// ceil(512 / cluster) entries and receives them from every partner: at most
+// 519 fp32) and its mbarrier.
+constexpr int kLoraRecvBytes = 2080;
+constexpr int kLoraSmemBytes = kLoraTileSmemBytes + kLoraRecvBytes + 16;
+constexpr int kPrepMaxCluster = kPrepMaxClusterC;
 
 struct PrepParams {
   const __nv_bfloat16* x;
@@ -105,6 +111,7 @@ struct PrepParams {
   float* t[kMaxLinears];   // [groups][M][r] partial sums of x~ . A^T over K group g, per linear
   float* tf[kMaxLinears];  // [M][r] their sum (written by the last cluster to finish a LoRA tile)
   unsigned* tile_count;    // per LoRA tile (lora_tiles of them): clusters done; reset by the last one
+  int* status;             // error record (a partial-tile push that never completed)
   int sum_groups;          // 1: sum the groups into tf (the consumer reads one sum); 0: the consumer adds them
   int tile_begin[kMaxLinears + 1];  // LoRA tiles of linear l: [tile_begin[l], tile_begin[l+1])
   __half* xs;   // staged x~ * 2^e_m: [M][K], or tiled (see xs_tile_offset)
@@ -190,7 +197,9 @@ __device__ __forceinline__ float noisy(float xv, float zv) {
 //   LoRA tiles: t[16 rows][32 ranks] = x~ . A^T; the cluster's CTAs each sum
 //   one K slice and the partial tiles are added over distributed shared
 //   memory in a fixed order, so t is written once, deterministically.
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
+// At most 64 registers (four CTAs' worth per SM): two of its warps fit beside
+// four 96-register MMA warps in an SM sub-partition.
+__global__ void __launch_bounds__(kPrepThreads, 4) prep_kernel(PrepParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int tid = threadIdx.x;
   // The MMA kernel may start its prologue (barriers, TMEM, weight loads) now;
@@ -387,6 +396,27 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
       }
     }
   };
+  // Without a group sum, the cluster's partial tiles are pushed to their
+  // owners -- CTA q owns entries [q * E, (q + 1) * E) of the 512, E =
+  // ceil(512 / cluster) -- into a receive buffer [cluster][E], each 4-byte
+  // store counted on the owner's mbarrier; the owner adds the partners in
+  // rank order.  The barriers are initialised before any CTA of the cluster
+  // pushes (one cluster barrier here, none at the end).
+  constexpr int kTileEntries = kLoraTileM * kLoraTileR;
+  const bool group_sum = p.sum_groups && p.groups > 1;
+  const bool push = !group_sum && p.cluster > 1;
+  const int E = (kTileEntries + p.cluster - 1) / p.cluster;
+  const int own = max(0, min(E, kTileEntries - ks * E));  // entries this CTA owns
+  const uint32_t recv = smem_u32(sm) + static_cast<uint32_t>(kLoraTileSmemBytes);
+  const uint32_t recv_bar = recv + static_cast<uint32_t>(kLoraRecvBytes);
+  if (push) {
+    if (tid == 0) {
+      mbar_init_a(recv_bar, 1);
+      mbar_arrive_expect_tx_a(recv_bar, static_cast<uint32_t>(p.cluster * own * 4));
+      fence_mbarrier_init();
+    }
+    cluster_sync_all();
+  }
   for (int st = 0; st < kLoraStages; ++st) {
     if (kc_begin + st < kc_end) issue_chunk(kc_begin + st, st);
     cp_async_commit();  // one group per chunk slot, empty past the slice
@@ -436,8 +466,48 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     }
   }
   cp_async_wait_group<0>();
-  // Partial tile [kLoraTileM][kLoraTileR] of this K slice -> shared memory,
-  // then CTA q of the cluster sums entries q, q + cluster, ... over all slices.
+  auto write_t = [&](int idx, float v) {
+    const int row = row0 + idx / kLoraTileR, rank = rank0 + idx % kLoraTileR;
+    if (row < p.M && rank < rr_) {
+      if (p.sum_groups && p.groups == 1)
+        p.tf[li][static_cast<int64_t>(row) * rr_ + rank] = v;  // one group: already the sum
+      else
+        tout[(static_cast<int64_t>(g) * p.M + row) * rr_ + rank] = v;
+    }
+  };
+  if (!group_sum) {
+    if (!push) {  // one CTA: its partial tile is the sum
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i) write_t((kRowsPerThread * rq + i) * kLoraTileR + lr, acc[i]);
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+      const int idx = (kRowsPerThread * rq + i) * kLoraTileR + lr;
+      const int owner = idx / E;
+      const uint32_t slot = static_cast<uint32_t>(ks * E + (idx - owner * E));
+      st_async_f32(mapa_shared(recv + 4u * slot, static_cast<uint32_t>(owner)), acc[i],
+                   mapa_shared(recv_bar, static_cast<uint32_t>(owner)));
+    }
+    if (own == 0) return;
+    // Bounded wait for every partner's entries (parity 0: the first phase).
+    const long long t0 = clock64();
+    while (!mbar_try_wait_a(recv_bar, 0)) {
+      if (clock64() - t0 > QERL_WAIT_LIMIT) {
+        if (tid == 0) record_error(p.status, 5);
+        return;
+      }
+    }
+    if (tid < own) {
+      float v = 0.0f;
+      for (int q = 0; q < p.cluster; ++q) v += ldsf(recv + 4u * static_cast<uint32_t>(q * E + tid));
+      write_t(ks * E + tid, v);
+    }
+    return;
+  }
+  // Group sum: partial tile [kLoraTileM][kLoraTileR] of this K slice -> shared
+  // memory, then CTA q of the cluster sums entries q, q + cluster, ... over
+  // all slices, and the last cluster of the tile adds the groups.
   __syncthreads();
   float* part = reinterpret_cast<float*>(sm);
 #pragma unroll
@@ -467,26 +537,16 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams p) {
     }
     vsum[u] = v;
   }
-  // Done with the partners' shared memory: they may leave once all have
-  // arrived, and the writes below overlap that wait -- unless the group sum
-  // follows, whose counter must see every partner's writes first (release).
-  const bool group_sum = p.sum_groups && p.groups > 1;
-  if (!group_sum) cluster_arrive();
 #pragma unroll
   for (int u = 0; u < kPerThread; ++u) {
     const int idx = idx0 + u * stride;
     if (idx >= kLoraTileM * kLoraTileR) break;
-    const int row = row0 + idx / kLoraTileR, rank = rank0 + idx % kLoraTileR;
-    if (row < p.M && rank < rr_) {
-      if (p.sum_groups && p.groups == 1)
-        p.tf[li][static_cast<int64_t>(row) * rr_ + rank] = vsum[u];  // one group: already the sum
-      else
-        tout[(static_cast<int64_t>(g) * p.M + row) * rr_ + rank] = vsum[u];
-    }
+    write_t(idx, vsum[u]);
   }
-  if (group_sum) cluster_arrive();
+  // The group's writes are done before the arrival (release): the counter
+  // below sees them.
+  cluster_arrive();
   cluster_wait();  // partners are done reading this CTA's partial tile
-  if (!p.sum_groups || p.groups == 1) return;
   // The last cluster to finish this LoRA tile (one per K group) adds the
   // groups' partial sums in group order -- deterministic -- into tf, so the
   // MMA kernel reads one sum per element.  It resets the counter for the next
@@ -2316,6 +2376,7 @@ qerl_status launch_lora_down(const void* x, int64_t m, int64_t k, int64_t ldx, c
   pp.ldx = ldx;
   lora_prep_params(pp, m, k, r, A, ws, WL);
   pp.row_groups = 0;
+  pp.status = status;
   out->t = pp.sum_groups ? pp.tf[0] : pp.t[0];
   out->parts = pp.sum_groups ? 1 : pp.groups;
   out->part_stride = m * r;
@@ -2651,6 +2712,7 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   }
   pp.lora_tiles = pp.tile_begin[kMaxLinears];
   pp.tile_count = reinterpret_cast<unsigned*>(ws + WL.count);
+  pp.status = status;
   pp.sum_groups = lora_sum_in_prep(M) ? 1 : 0;
   size_t prep_smem = static_cast<size_t>(K) * 2;  // row tasks stage the row
   if (lora) prep_smem = std::max(prep_smem, static_cast<size_t>(kLoraSmemBytes));
