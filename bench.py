@@ -305,7 +305,7 @@ def group_algorithmic_bytes(lins, m, r=RANK_R):
 # issuers up to 64 tokens, the compact epilogue and the early weight stages
 # that complete without the activations).
 DOMINANT = ("gate_up", 8)
-DOMINANT_TRAFFIC_BYTES = 79706112  # prep 598,784 + mma 79,053,568 read + 53,760 written (ncu, 1 pass)
+DOMINANT_TRAFFIC_BYTES = 79654912  # prep 596,480 + mma 79,043,584 read + 14,848 written (ncu, 1 pass)
 
 
 def dominant_call(q, layers, acts, hbm_peak, reps=64):
