@@ -2516,12 +2516,13 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   // Tiles above 32 tokens run in pair mode -- one CTA per two adjacent 128-row
   // weight tiles of a linear, sharing the activation slabs, with the
   // activation ring separate from the weights -- when each CTA then streams at
-  // least 6 weight stages: half as many CTAs (one wave instead of two for the
+  // least 12 weight stages: half as many CTAs (one wave instead of two for the
   // 7B gate + up launch) and half the activation bytes per weight byte; its
-  // fixed costs (two tiles' epilogue) are higher.  (Measured at 33-64 tokens:
-  // 7% less time per layer than single tiles with four issuers.)
+  // fixed costs (two tiles' epilogue) are higher, and it cannot share SMs with
+  // the prep grid.  (Measured: 6 stages made the 7B down launch 2-6 us slower
+  // at 48-128 tokens, as 9-10-stage pair CTAs; gate + up keeps 14.)
   const int split_pair = n_tok > 32 && n_tok <= 128 ? best_split(all_pairs) : 1;
-  const bool pair = n_tok > 32 && n_tok <= 128 && (raw_total + split_pair - 1) / split_pair >= 6;
+  const bool pair = n_tok > 32 && n_tok <= 128 && (raw_total + split_pair - 1) / split_pair >= 12;
   int tile_begin[kMaxLinears + 1] = {0, 0, 0, 0, 0};  // in grid-y units: tiles, or pairs of tiles
   for (int i = 0; i < nlin; ++i) tile_begin[i + 1] = tile_begin[i] + (pair ? (tiles[i] + 1) / 2 : tiles[i]);
   const bool lora = r > 0;
