@@ -909,9 +909,15 @@ __device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q,
   }
 }
 
+// kCoupledT: the coupled layout (up to 64 tokens, single tiles, 15 warps) or
+// the general one (pair mode and the rest); each instantiation carries only
+// its own paths, so the code a CTA runs once is more compact.
+template <int kCoupledT>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ BtMaps tm_bls,
                const MmaParams p) {
+  constexpr bool kCpl = kCoupledT != 0;
+  const bool pairm = !kCpl && p.pair != 0;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -941,10 +947,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   while (gi + 1 < p.nlin && static_cast<int>(blockIdx.y) >= p.lin[gi + 1].tile_begin) ++gi;
   const LinearSlot& L = p.lin[gi];
   const CUtensorMap* tm_bl = &tm_bls.m[gi];
-  const int n0 = (static_cast<int>(blockIdx.y) - L.tile_begin) * kTileN * (p.pair ? 2 : 1);
+  const int n0 = (static_cast<int>(blockIdx.y) - L.tile_begin) * kTileN * (pairm ? 2 : 1);
   // Weight tiles this CTA streams: 1, or 2 in pair mode (1 for an odd last tile).
-  const int ntl = p.pair ? min(2, (L.N - n0 + kTileN - 1) / kTileN) : 1;
-  const uint32_t rslot = static_cast<uint32_t>(p.pair ? 2 : 1) * kRawSlotBytes;  // raw-ring slot size
+  const int ntl = pairm ? min(2, (L.N - n0 + kTileN - 1) / kTileN) : 1;
+  const uint32_t rslot = static_cast<uint32_t>(pairm ? 2 : 1) * kRawSlotBytes;  // raw-ring slot size
   const int m0 = blockIdx.z * p.n_tok;
   const int raw_total = (p.K + kRawK - 1) / kRawK;
   const int rb = static_cast<int>(static_cast<int64_t>(split_idx) * raw_total / p.split);
@@ -955,16 +961,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int nmma = min(kSub * re, kb_total) - mma_begin;
   const int RS = p.raw_stages, AS = p.ab_stages, NI = p.issuers, BS = p.b_stages;
   const bool do_lora = L.r > 0 && split_idx == 0;  // one CTA of a K-split cluster adds the LoRA term
-  const int n_iss = p.pair ? ntl : NI;              // issuers with work (each commits once to the barriers below)
+  const int n_iss = pairm ? ntl : NI;              // issuers with work (each commits once to the barriers below)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
       mbar_init_a(raw_full(s), 1);  // producer expect_tx
       // The four dequant warps of the stage's group; pair mode: the groups
       // of both tiles.
-      mbar_init_a(raw_empty(s), p.pair ? 4 * ntl : 4);
+      mbar_init_a(raw_empty(s), pairm ? 4 * ntl : 4);
     }
-    if (p.pair) {
+    if (pairm) {
       // One barrier pair per (tile, MMA stage) slot of tensor memory: the
       // tile's four dequant warps arrive, its issuer commits.
       for (int w = 0; w < 2 * kSub; ++w) {
@@ -980,18 +986,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // activation producer's expect_tx for the stage's slabs); empty: every
       // issuer of the stage once.
       for (int b = 0; b < 2 * (AS / kSub); ++b) {
-        mbar_init_a(ab_full(b), 4 + (p.coupled ? 1 : 0));
-        mbar_init_a(ab_empty(b), p.coupled ? NI / 2 : NI);
+        mbar_init_a(ab_full(b), 4 + (kCpl ? 1 : 0));
+        mbar_init_a(ab_empty(b), kCpl ? NI / 2 : NI);
       }
     }
     for (int s = 0; s < BS; ++s) {
         mbar_init_a(b_full(s), 1);                  // producer expect_tx
-        mbar_init_a(b_empty(s), p.pair ? ntl : 1);  // tcgen05.commit of each issuer reading the slab
+        mbar_init_a(b_empty(s), pairm ? ntl : 1);  // tcgen05.commit of each issuer reading the slab
       }
     mbar_init_a(ring_free, n_iss);
     // B^T TMA (expect_tx) + the warps that build the t tiles: the eight
     // dequant warps, or in pair mode the six issuer warps without a tile.
-    mbar_init_a(lora_full, p.pair ? 1 + kPairLoraWarps : 9);
+    mbar_init_a(lora_full, pairm ? 1 + kPairLoraWarps : 9);
 #ifdef QERL_TEST_HOOKS
     mbar_init_a(acc_full, n_iss + (g_test_extra_arrival ? 1 : 0));
 #else
@@ -1051,7 +1057,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         bulk_load(dst, src, kRawSlotBytes, bar);
     };
     if (lane == 0) {
-      if (!p.coupled) prefetch_first(0);
+      if (!kCpl) prefetch_first(0);
       for (int i = 0; i < early; ++i) {
         mbar_arrive_expect_tx_a(raw_full(i), ntl * kRawSlotBytes);
         for (int t = 0; t < ntl; ++t)
@@ -1059,7 +1065,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                  wtile + t * tile_stride + static_cast<int64_t>(rb + i) * kRawSlotBytes, raw_full(i));
       }
     }
-    if (p.coupled) {
+    if (kCpl) {
       griddep_wait();
       if (lane == 0) prefetch_first(early);  // the ring's blocks are being loaded
     }
@@ -1102,7 +1108,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // ------------------------------------------------------------ activation producer
     if (!p.acts_ready) griddep_wait();  // the staged activations are written by the preceding kernel
     {
-      if (p.coupled && lane == 0) {
+      if (kCpl && lane == 0) {
         // Up to 64 tokens: one bulk copy of a weight stage's kSub slabs (the
         // tiled layout keeps them contiguous) into the activation slot of its
         // tensor-memory A slot, completing on the stage's full barrier.  The
@@ -1131,7 +1137,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             eph ^= 1;
           }
         }
-      } else if (p.pair && lane == 0) {
+      } else if (pairm && lane == 0) {
         // Pair mode: the ring's BS slabs form two halves of G = BS / 2 slabs
         // (a weight stage's kSub slabs, or half of them), each half one
         // barrier pair filled at once, so each issuer waits and commits once
@@ -1159,7 +1165,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           sj ^= 1;
           if (sj == 0) sph ^= 1;
         }
-      } else if (!p.coupled && lane == 0) {
+      } else if (!kCpl && lane == 0) {
         // One bulk copy per 64-wide K slab (tiled layout: the slabs of
         // consecutive MMA stages are contiguous), each slot with its own full
         // and empty barrier, so a slot is refilled as soon as the MMAs that
@@ -1194,7 +1200,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(p.n_tok));
       const uint32_t d_acc = tmem_base + static_cast<uint32_t>(ii * p.n_tok);
       uint32_t acc = 0;
-      if (p.pair) {
+      if (pairm) {
         // Pair mode: this issuer owns tile ii of the pair (its accumulator,
         // its tensor-memory A slot per MMA stage q: ab_*(ii * kSub + q)) and
         // reads the activation slabs half a ring (G = BS / 2 MMA stages) at a
@@ -1249,7 +1255,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // sit in the activation slot of its A slot's index and land on the
         // same full barrier.
         const int AW = AS / kSub, BW = 2 * AW;
-        const int NG = p.coupled ? 2 : 1;
+        const int NG = kCpl ? 2 : 1;
         const int gsz = NI / NG;
         const int g = ii / gsz;
         const int per = kSub * 4 / gsz;
@@ -1265,7 +1271,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           const int u1 = min(u0 + per, 4 * nq);  // this issuer's MMAs in this weight stage: [u0, u1)
           const uint32_t a_st = tmem_base + p.col_a + static_cast<uint32_t>(w * kSub * kAStageCols);
           tc_fence_after();
-          if (p.coupled) {
+          if (kCpl) {
             const uint32_t b_st = sbase + p.off_b + static_cast<uint32_t>(w) * p.raw_b_bytes;
             if (lane == 0) {
               for (int u = u0; u < u1; ++u)
@@ -1322,14 +1328,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (lane == 0) {
         // The LoRA up-projection goes last, so a slow producer of t never
         // holds up the weight stream.
-        if ((p.pair || ii == 0) && do_lora && p.lora_early) {
+        if ((pairm || ii == 0) && do_lora && p.lora_early) {
           // Pair mode: each issuer adds its own tile's up-projection (its B^T
           // chunk set; the t tiles are shared).  Otherwise issuer 0 does.
           if (mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
             tc_fence_after();
             const int rc = lora_chunks(L.r);
-            const int nbt = p.pair ? 2 : 1;
-            issue_lora_mmas(p, L, lora_base + static_cast<uint32_t>((p.pair ? ii : 0) * rc * kBtChunkBytes),
+            const int nbt = pairm ? 2 : 1;
+            issue_lora_mmas(p, L, lora_base + static_cast<uint32_t>((pairm ? ii : 0) * rc * kBtChunkBytes),
                             lora_base + static_cast<uint32_t>(nbt * rc * kBtChunkBytes), d_acc);
           }
         }
@@ -1337,17 +1343,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           tc_commit(ring_free);  // the ring is idle once every mainloop MMA is done
           // Pair mode: each issuer adds its own tile's up-projection (its B^T
           // chunk set; the t tiles are shared).  Otherwise issuer 0 does.
-          if ((p.pair || ii == 0) && mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
+          if ((pairm || ii == 0) && mbar_wait_a(lora_full, 0, abort_flag, p.status)) {
             tc_fence_after();
             const int rc = lora_chunks(L.r);
-            const int nbt = p.pair ? 2 : 1;
-            issue_lora_mmas(p, L, lora_base + static_cast<uint32_t>((p.pair ? ii : 0) * rc * kBtChunkBytes),
+            const int nbt = pairm ? 2 : 1;
+            issue_lora_mmas(p, L, lora_base + static_cast<uint32_t>((pairm ? ii : 0) * rc * kBtChunkBytes),
                             lora_base + static_cast<uint32_t>(nbt * rc * kBtChunkBytes), d_acc);
           }
         }
         tc_commit(acc_full);  // always, so the epilogue's wait completes even after an abort
       }
-    } else if (p.pair && do_lora && ii >= 2) {
+    } else if (pairm && do_lora && ii >= 2) {
       // Pair mode: the issuer warps without a tile build the LoRA operand's
       // t tiles (shared by both tiles) from the partial sums in global
       // memory while the weights stream, into the dedicated LoRA region.
@@ -1381,7 +1387,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // path carries no per-word branch.
     auto dequant_loops = [&](auto lut_on) {
       constexpr bool kLut = decltype(lut_on)::value;
-      if (p.pair) {
+      if (pairm) {
         // Pair mode: group g = dw / 4 dequantizes tile g of the pair (a thread
         // is one weight row of it), every weight stage, and hands each MMA
         // stage's 32 TMEM columns over as soon as they are stored, so the next
@@ -1492,7 +1498,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       dequant_loops(std::true_type{});
     else
       dequant_loops(std::false_type{});
-    if (do_lora && !p.pair) {
+    if (do_lora && !pairm) {
       // The LoRA operand's t tiles, by all 256 dequant threads once their
       // stream is done: from the rows the LoRA warp staged (early), or from
       // global memory into the idle ring (late).
@@ -1505,7 +1511,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           build_t_tiles_staged(p, L, lora_base, sbase + p.off_tstage, smv + 4u * p.n_tok, min(p.n_tok, p.M - m0),
                                dtid, 256);
       } else if (warp_wait(ring_free, 0, abort_flag, p.status)) {
-        build_t_tiles(p, L, lora_base, smv + 4u * p.n_tok, m0, dtid, 256, p.pair ? 2 : 1);
+        build_t_tiles(p, L, lora_base, smv + 4u * p.n_tok, m0, dtid, 256, pairm ? 2 : 1);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -1514,7 +1520,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp == kLoraWarp) {
     // ------------------------------------------------------------ LoRA operands
     if (do_lora) {
-      if (p.lora_early && p.pair) {
+      if (p.lora_early && pairm) {
         // Both tiles' B^T chunk sets (a missing second tile: zeros); the
         // idle issuer warps build the t tiles.
         if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full, 2);
@@ -1536,7 +1542,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       } else if (warp_wait(ring_free, 0, abort_flag, p.status)) {
         // Pair mode: both tiles' B^T chunk sets (the second one's rows past N
         // read as zeros); otherwise this tile's.
-        if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full, p.pair ? ntl : 1);
+        if (lane == 0) load_bt_tiles(L, tm_bl, lora_base, n0, lora_full, pairm ? ntl : 1);
       } else if (lane == 0) {
         mbar_arrive_expect_tx_a(lora_full, 0);  // after an abort: keep the barrier count consistent
       }
@@ -1546,7 +1552,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // ---------------------------------------------------------------- epilogue
   const uint32_t part = sbase;  // [tile][n_tok][128] fp32 scaled partial tiles (split > 1), ring reused
   const int dt = static_cast<int>(threadIdx.x) - 32 * deq0;  // dequant-warp thread index
-  const int ntl_e = p.pair ? ntl : 1;                              // weight tiles of this CTA
+  const int ntl_e = pairm ? ntl : 1;                              // weight tiles of this CTA
   if (warp >= deq0) {
     // Row scales S * 2^-e_m come from the preceding kernel (or, acts_ready,
     // the one before it); the dequant above did not need them.
@@ -1563,11 +1569,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int nl = q * 32 + lane;
     // Pair mode: warp group eg reads tile eg's accumulator, all token columns;
     // otherwise the two groups split the token columns of the one tile.
-    const int eg = p.pair ? (warp - deq0) >> 2 : 0;
+    const int eg = pairm ? (warp - deq0) >> 2 : 0;
     const bool live = eg < ntl_e;
     const int n = n0 + eg * kTileN + nl;
-    const int cols = p.pair ? p.n_tok : p.n_tok / 2;
-    const int c0 = p.pair ? 0 : ((warp - deq0) >> 2) * cols;
+    const int cols = pairm ? p.n_tok : p.n_tok / 2;
+    const int c0 = pairm ? 0 : ((warp - deq0) >> 2) * cols;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acc0 = static_cast<uint32_t>(eg * p.n_tok);       // first accumulator column
     const uint32_t tile_out = static_cast<uint32_t>(eg * p.n_tok * kTileN);  // element offset of its staged tile
@@ -1577,8 +1583,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // (coupled): group g's first stage is stage g.  Pair mode: one
     // accumulator per tile.
     uint32_t accs = 1u;
-    if (!p.pair) {
-      const int NG = p.coupled ? 2 : 1, gsz = NI / NG, per = kSub * 4 / gsz;
+    if (!pairm) {
+      const int NG = kCpl ? 2 : 1, gsz = NI / NG, per = kSub * 4 / gsz;
       accs = 0u;
       for (int g = 0; g < NG && g < nraw; ++g) {
         const int nq = min(kSub, nmma - g * kSub);
@@ -1586,7 +1592,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
     const int nacc = 32 - __clz(static_cast<int>(accs));  // accumulator slots to scan
-    if (p.pair && live) {
+    if (pairm && live) {
       // One accumulator per tile: 32 token columns per TMEM load and wait
       // (columns past n_tok are read -- they lie inside tensor memory -- but
       // not stored).  The row scales come in as vectors; an unsplit tile is
@@ -1653,7 +1659,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           sts16(sbase + 2u * (el0 + e * kTileN), __bfloat16_as_ushort(__float2bfloat16_rn(val[e])));
       }
     };
-    if (!p.pair && (accs == 1u || accs == 3u) && cols % 32 == 0) {
+    if (!pairm && (accs == 1u || accs == 3u) && cols % 32 == 0) {
       for (int c = c0; c < c0 + cols; c += 32) {
         float w[32], w2[32];
         tmem_ld_x32(tmem_base + acc0 + lane_off + c, w);
@@ -1673,7 +1679,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
       }
     } else {
-    for (int c = c0; !p.pair && c < c0 + cols; c += 8) {
+    for (int c = c0; !pairm && c < c0 + cols; c += 8) {
       float v[8];
       // Four accumulators' columns per wait (issuer 0's holds the LoRA term).
 #pragma unroll 1
@@ -2134,7 +2140,7 @@ int resident_clusters(int sp) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<0>, &cfg) != cudaSuccess) {
       cudaGetLastError();  // the query failed: fall back to whole SMs
       n = sm_count() / sp;
     }
@@ -2269,9 +2275,14 @@ bool kernel_attrs_ok() {
       attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                       cudaSharedmemCarveoutMaxShared);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+      attr_err = cudaFuncSetAttribute(mma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+      attr_err = cudaFuncSetAttribute(mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(mma_kernel<0>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      cudaSharedmemCarveoutMaxShared);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(mma_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                       cudaSharedmemCarveoutMaxShared);
   });
   return attr_err == cudaSuccess;
@@ -2859,7 +2870,8 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  const cudaError_t le = cudaLaunchKernelEx(&cfg, mma_kernel, tm_xs, tm_bls, mp);
+  const cudaError_t le = coupled ? cudaLaunchKernelEx(&cfg, mma_kernel<1>, tm_xs, tm_bls, mp)
+                                  : cudaLaunchKernelEx(&cfg, mma_kernel<0>, tm_xs, tm_bls, mp);
   if (le != cudaSuccess) return QERL_ERR_CUDA;
   return QERL_OK;
 }
