@@ -871,15 +871,15 @@ __device__ __forceinline__ void codes8_to_f16x2x4(uint32_t w, uint32_t lut, uint
   }
 }
 
-template <bool kLut>
-__device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q, bool wt, uint32_t lut,
+template <bool kLut, bool kWt>
+__device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q, uint32_t lut,
                                                   uint32_t (&o)[32]) {
   const uint32_t crow = slot + row * 128;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const uint4 cw = lds128(crow + (((2 * q + h) ^ (row & 7)) << 4));
     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-    if (!wt) {
+    if constexpr (!kWt) {
       const __half2 s01 = e4m3x2_to_half2(lds16(slot + kCodesRawBytes + row * 2 + (2 * q + h) * 256));
       const __half2 sa2 = __low2half2(s01), sb2 = __high2half2(s01);
       const uint32_t sa = *reinterpret_cast<const uint32_t*>(&sa2);
@@ -910,13 +910,15 @@ __device__ __forceinline__ void dequant_mma_stage(uint32_t slot, int row, int q,
 }
 
 // kCoupledT: the coupled layout (up to 64 tokens, single tiles, 15 warps) or
-// the general one (pair mode and the rest); each instantiation carries only
-// its own paths, so the code a CTA runs once is more compact.
-template <int kCoupledT>
+// the general one (pair mode and the rest); kWtT: the transposed weight
+// layout (the input gradient).  Each instantiation carries only its own
+// paths, so the code a CTA runs once is more compact.
+template <int kCoupledT, int kWtT>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ BtMaps tm_bls,
                const MmaParams p) {
   constexpr bool kCpl = kCoupledT != 0;
+  constexpr bool kWt = kWtT != 0;
   const bool pairm = !kCpl && p.pair != 0;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -1373,7 +1375,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp >= deq0) {
     // ------------------------------------------------------------ dequant warps
     const int dw = warp - deq0;
-    const bool wt = p.wt != 0;
     uint32_t lut = 0u;
     if (L.nf4) {
       // The NF4 table: entry e (a code byte) = the fp16 pair (level[e & 15],
@@ -1407,7 +1408,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             for (int q = 0; q < kSub; ++q) {
               if (q >= nq) break;
               uint32_t o[32];
-              dequant_mma_stage<kLut>(slot, row, q, wt, lut, o);
+              dequant_mma_stage<kLut, kWt>(slot, row, q, lut, o);
               const int sl = g * kSub + q;
               if (!warp_wait(ab_empty(sl), (i & 1) ^ 1, abort_flag, p.status)) {
                 ok = false;
@@ -1460,7 +1461,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             // MMA stage q: 16-byte code chunks 2q, 2q + 1 of the row (128-byte
             // swizzle) and the scales of the same K range.
             uint32_t o[32];
-            dequant_mma_stage<kLut>(slot, row, q, wt, lut, o);
+            dequant_mma_stage<kLut, kWt>(slot, row, q, lut, o);
             // The slot's previous MMAs must be done before the first store
             // (the first conversion overlaps that wait).
             if (q == 0 && !warp_wait(ab_empty(e), eph, abort_flag, p.status)) {
@@ -2140,7 +2141,7 @@ int resident_clusters(int sp) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<0>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<0, 0>, &cfg) != cudaSuccess) {
       cudaGetLastError();  // the query failed: fall back to whole SMs
       n = sm_count() / sp;
     }
@@ -2264,6 +2265,15 @@ constexpr int kPrepSmemLimit = kSmemLimit - 1024;  // leaves room for the kernel
 
 // Kernel attributes are set once per process (not per call), so calls can be
 // captured into CUDA graphs.
+// One attribute on every instantiation of the MMA kernel.
+cudaError_t mma_kernel_attrs(cudaFuncAttribute attr, int value) {
+  cudaError_t e = cudaFuncSetAttribute(mma_kernel<0, 0>, attr, value);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mma_kernel<0, 1>, attr, value);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mma_kernel<1, 0>, attr, value);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mma_kernel<1, 1>, attr, value);
+  return e;
+}
+
 bool kernel_attrs_ok() {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -2275,15 +2285,9 @@ bool kernel_attrs_ok() {
       attr_err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                       cudaSharedmemCarveoutMaxShared);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+      attr_err = mma_kernel_attrs(cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel<0>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                      cudaSharedmemCarveoutMaxShared);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(mma_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                      cudaSharedmemCarveoutMaxShared);
+      attr_err = mma_kernel_attrs(cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   });
   return attr_err == cudaSuccess;
 }
@@ -2870,8 +2874,11 @@ qerl_status launch_lora_linear(const LinearArgs& a, cudaStream_t s) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  const cudaError_t le = coupled ? cudaLaunchKernelEx(&cfg, mma_kernel<1>, tm_xs, tm_bls, mp)
-                                  : cudaLaunchKernelEx(&cfg, mma_kernel<0>, tm_xs, tm_bls, mp);
+  const cudaError_t le =
+      coupled ? (a.wt ? cudaLaunchKernelEx(&cfg, mma_kernel<1, 1>, tm_xs, tm_bls, mp)
+                      : cudaLaunchKernelEx(&cfg, mma_kernel<1, 0>, tm_xs, tm_bls, mp))
+              : (a.wt ? cudaLaunchKernelEx(&cfg, mma_kernel<0, 1>, tm_xs, tm_bls, mp)
+                      : cudaLaunchKernelEx(&cfg, mma_kernel<0, 0>, tm_xs, tm_bls, mp));
   if (le != cudaSuccess) return QERL_ERR_CUDA;
   return QERL_OK;
 }
