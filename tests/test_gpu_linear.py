@@ -86,21 +86,24 @@ SMALL = [
     (600, 256, 256, 128, 1e-2),
     (8, 512, 3584, 32, 1e-2),  # 7B k/v shape at decode (K split across a cluster)
     (32, 1024, 4096, 16, 0.0),
-    # pair mode (65..128 tokens: two 128-row tiles per CTA sharing the activation slabs)
-    (100, 384, 2048, 128, 1e-2),  # 3 tiles: the second CTA has one; rank 128 (late LoRA operand)
-    (72, 1000, 1024, 32, 1e-2),   # ragged N inside the last pair
-    (128, 256, 6144, 32, 1e-2),   # one pair, K split across a cluster
-    (65, 128, 512, 8, 0.0),       # a single tile in pair mode
+    # 65..128 tokens, single tiles (pair mode needs >= 12 weight stages per CTA)
+    (100, 384, 2048, 128, 1e-2),  # rank 128 (late LoRA operand)
+    (72, 1000, 1024, 32, 1e-2),   # ragged N
+    (128, 256, 6144, 32, 1e-2),   # K split across a cluster
+    (65, 128, 512, 8, 0.0),       # one tile
     (48, 384, 3584, 128, 1e-2),   # rank 128 at 33..64 tokens: the LoRA operand built late, in the idle ring
-    (128, 512, 18944, 128, 5e-3), # rank 128 at 128 tokens, long K (pair mode, summed LoRA groups)
-    # pair mode at 33..64 tokens (one wave of pairs, separate activation ring)
+    (128, 512, 18944, 128, 5e-3), # rank 128 at 128 tokens, long K (summed LoRA groups)
+    # 33..64 tokens
     (40, 512, 2048, 32, 1e-2),
     (64, 768, 3584, 16, 5e-3),
-    # pair mode over several 128-token tiles (> 128 tokens)
+    # several 128-token tiles (> 128 tokens)
     (257, 512, 2048, 32, 1e-2),   # 3 token tiles, ragged last rows
-    (384, 256, 1536, 16, 5e-3),   # 6 weight stages (the pair-mode minimum)
+    (384, 256, 1536, 16, 5e-3),
     (512, 1024, 2048, 0, 1e-2),   # 4 token tiles, no LoRA
     (300, 256, 2048, 128, 1e-2),  # rank 128
+    # pair mode (two 128-row tiles per CTA sharing the activation slabs; >= 12 weight stages)
+    (257, 512, 3072, 32, 1e-2),   # 12 stages, 3 token tiles, ragged last rows
+    (130, 384, 4096, 16, 5e-3),   # 16 stages, 2 token tiles; the second pair has one tile
 ]
 
 
@@ -304,9 +307,9 @@ def test_no_writes_past_the_buffers(q, orc, m, n, k, r):
 
 
 def test_linear_group_pair_mode_several_token_tiles(q, orc):
-    """A grouped launch at 260 tokens (3 token tiles, pair mode) of two members with different
-    tile counts and ranks."""
-    m, k = 260, 2048
+    """A grouped launch at 260 tokens (3 token tiles, pair mode: 12 weight stages) of two members
+    with different tile counts and ranks."""
+    m, k = 260, 3072
     cases = [Case(q, orc, m, n, k, r, 1e-2, seed=90 + i) for i, (n, r) in enumerate([(512, 32), (768, 16)])]
     x = cases[0].x
     for c in cases:
