@@ -84,13 +84,17 @@ constexpr int kLoraStages = 3;   // chunks in flight (cp.async ring)
 // row of it when the noise is shared by all rows).
 constexpr int kLoraStageBytes = (kLoraTileM + kLoraTileR) * kLoraKc * 2 + kLoraTileM * kLoraKc * 4;
 constexpr int kLoraTileSmemBytes = kLoraStages * kLoraStageBytes + (kLoraTileM + kLoraTileR) * kLoraPad * 4;
-constexpr int kPrepMaxClusterC = 8;
+constexpr int kPrepMaxCluster = 8;
 // + the receive buffer of the partial-tile push (each CTA of a cluster owns
 // ceil(512 / cluster) entries and receives them from every partner: at most
 // 519 fp32) and its mbarrier.
 constexpr int kLoraRecvBytes = 2080;
+constexpr bool lora_recv_fits(int c) {
+  return c > kPrepMaxCluster ||
+         (4 * c * ((kLoraTileM * kLoraTileR + c - 1) / c) <= kLoraRecvBytes && lora_recv_fits(c + 1));
+}
+static_assert(lora_recv_fits(1), "LoRA receive buffer");
 constexpr int kLoraSmemBytes = kLoraTileSmemBytes + kLoraRecvBytes + 16;
-constexpr int kPrepMaxCluster = kPrepMaxClusterC;
 
 struct PrepParams {
   const __nv_bfloat16* x;
