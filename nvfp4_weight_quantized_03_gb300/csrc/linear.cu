@@ -2323,13 +2323,15 @@ void lora_prep_params(PrepParams& pp, int64_t m, int64_t k, int r, const void* A
 
 }  // namespace
 
-// The LoRA split of a launch.  Up to 64 tokens the prep grid's LoRA tiles
-// hold SMs the MMA kernel needs until they finish: when the launch streams
-// many weight stages per SM (a long mainloop, e.g. gate + up or down), a prep
-// CTA takes three chunks (four from 32 tokens) instead of two -- fewer CTAs,
-// later t, which the long mainloop hides.  (Measured on the 7B launches: gate
-// + up at 64 tokens 50.9 -> 44.9 us, at 32 tokens 42.0 -> 40.7 us; q, k, v
-// and o keep two.)
+// The LoRA split of a launch.  When the launch streams many weight stages
+// per SM (a long main loop, e.g. gate + up or down), a prep CTA takes three
+// chunks (four from 32 tokens) instead of two: fewer CTAs and fewer K groups
+// (whose partial sums the MMA kernel stages in shared memory), later t, which
+// the long main loop hides.  (Measured on the 7B launches: gate + up at 64
+// tokens 50.9 -> 44.9 us, at 32 tokens 42.0 -> 40.7 us; with the prep grid
+// sharing SMs, two chunks everywhere was 2% slower -- down then needs 16
+// groups, whose staging shortens the MMA kernel's ring.  q, k, v and o keep
+// two.)
 LoraSplit launch_lora_split(const LinearArgs& a, const int* ranks) {
   int64_t stage_tiles = 0;
   for (int i = 0; i < a.nlin; ++i)
